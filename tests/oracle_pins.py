@@ -1,0 +1,468 @@
+"""Checks that pin the oracle to facts fixed outside itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` (the real one, or a copy with a planted
+mistake) and raises AssertionError when the oracle disagrees with the fact it pins.  The
+facts come from the pages (worked example, printed depths, the losslessness theorem and
+its corollaries), from the Philox publication (known-answer vectors), or from textbook
+routines (numpy argmax, scipy logsumexp, a chi-squared test).
+
+Sources (page title -- section):
+  [SD] "7.6 Speculative Decoding: Draft Models, Medusa, EAGLE & Lookahead"
+  [MS] "Medusa, EAGLE and self-speculation"
+  [HB] "Speculative Decoding: Draft Models, EAGLE, and How to Actually Use It"
+"""
+from __future__ import annotations
+
+import itertools
+import os
+
+import numpy as np
+from scipy import special, stats
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _softmax(l, T):
+    l = np.asarray(l, np.float64) / T
+    m = np.max(l)
+    e = np.exp(l - m)
+    return e / e.sum()
+
+
+# --------------------------------------------------------------------------------------
+# Philox4x32-10 known-answer vectors (SC'11 reference implementation)
+# --------------------------------------------------------------------------------------
+def pin_philox_kat(orc):
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) as f:
+        lines = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    assert lines
+    for ln in lines:
+        v = [int(x, 16) for x in ln]
+        out = orc.philox4x32_10(v[0:4], v[4:6])
+        assert list(out) == v[6:10], (ln, [hex(x) for x in out])
+
+
+def pin_uniform_definition(orc):
+    """u = (word0 >> 8) * 2^-24 of Philox at counter (4i + purpose, b, off lo, off hi)."""
+    rng = np.random.RandomState(7)
+    for _ in range(200):
+        seed = int(rng.randint(0, 2**62)) * 3 + 1
+        off = int(rng.randint(0, 2**62))
+        b, i, pur = int(rng.randint(0, 2**20)), int(rng.randint(0, 2**10)), int(rng.randint(0, 2))
+        w = orc.philox4x32_10([(i << 2) | pur, b, off & 0xFFFFFFFF, off >> 32],
+                              [seed & 0xFFFFFFFF, seed >> 32])
+        u = orc.uniform(seed, off, b, i, pur)
+        assert u == (int(w[0]) >> 8) * 2.0**-24
+        assert 0.0 <= u <= 1.0 - 2.0**-24
+
+
+# --------------------------------------------------------------------------------------
+# P1: brute-force losslessness [SD "The proof that this is exact"; HB "The Algorithm"]
+# --------------------------------------------------------------------------------------
+def _tiny_model(prefix, V, salt, scale, mask_frac=0.0):
+    """Deterministic prefix-dependent logits of a toy language model."""
+    h = salt
+    for t in prefix:
+        h = (h * 1000003 + 7919 * (t + 1)) % (2**32)
+    rs = np.random.RandomState(h)
+    l = rs.normal(0.0, scale, V)
+    if mask_frac > 0:
+        masked = rs.rand(V) < mask_frac
+        if masked.all():
+            masked[rs.randint(V)] = False
+        l[masked] = -np.inf
+    return l
+
+
+def speculative_law(orc, V, gamma, L, T, salt_p=11, salt_q=23, mask_p=0.0):
+    """Law of the first L emitted tokens when rounds of the oracle's enumeration mode are
+    composed, drafts drawn from the toy draft model; prefixes are merged so the work stays
+    polynomial."""
+    law = {}
+    frontier = {(): 1.0}
+    while frontier:
+        nxt = {}
+        for y, w in frontier.items():
+            if len(y) >= L:
+                law[y[:L]] = law.get(y[:L], 0.0) + w
+                continue
+            for x in itertools.product(range(V), repeat=gamma):
+                qx = 1.0
+                for i in range(gamma):
+                    qx *= _softmax(_tiny_model(y + x[:i], V, salt_q, 1.5), T)[x[i]]
+                if qx == 0.0:
+                    continue
+                t_rows = [_tiny_model(y + x[:i], V, salt_p, 1.5, mask_p) for i in range(gamma + 1)]
+                d_rows = [_tiny_model(y + x[:i], V, salt_q, 1.5) for i in range(gamma)]
+                P = orc.exact_probs(np.array(t_rows), np.array(d_rows).reshape(gamma, V),
+                                    np.array(x, np.int32), T)
+                for k in range(gamma + 1):
+                    for j in range(V):
+                        if P[k, j] > 0.0:
+                            z = y + tuple(x[:k]) + (j,)
+                            nxt[z] = nxt.get(z, 0.0) + w * qx * P[k, j]
+        frontier = nxt
+    return law
+
+
+def target_law(V, L, T, salt_p=11, mask_p=0.0):
+    law = {}
+    for s in itertools.product(range(V), repeat=L):
+        pr = 1.0
+        for l in range(L):
+            pr *= _softmax(_tiny_model(s[:l], V, salt_p, 1.5, mask_p), T)[s[l]]
+        law[s] = pr
+    return law
+
+
+def pin_bruteforce_lossless(orc, cases=((3, 2, 3, 0.8, 0.0), (2, 3, 4, 1.3, 0.0),
+                                        (4, 1, 2, 1.0, 0.3), (5, 2, 2, 0.7, 0.25))):
+    for V, gamma, L, T, mask in cases:
+        got = speculative_law(orc, V, gamma, L, T, mask_p=mask)
+        want = target_law(V, L, T, mask_p=mask)
+        keys = set(got) | set(want)
+        err = max(abs(got.get(k, 0.0) - want.get(k, 0.0)) for k in keys)
+        assert err < 1e-12, (V, gamma, L, T, mask, err)
+        assert abs(sum(got.values()) - 1.0) < 1e-12
+
+
+# --------------------------------------------------------------------------------------
+# P2: chi-squared test of the Philox-driven sampler against p [SD "The rule"]
+# --------------------------------------------------------------------------------------
+def _chi2_rows(V, gamma):
+    rs = np.random.RandomState(4242)
+    # rows for absolute positions 0..gamma+1 (target) and 0..gamma (draft); the toy model
+    # is position-dependent but prefix-independent, so the law of (y0, y1) is p0 x p1
+    t = rs.normal(0, 1.3, (gamma + 2, V))
+    d = t[: gamma + 1] + rs.normal(0, 1.0, (gamma + 1, V))
+    return t.astype(np.float32), d.astype(np.float32)
+
+
+def pin_chi2_sampler(orc, trials=1_000_000, V=5, gamma=2, T=0.9, seed=0xC0FFEE, alpha=1e-3):
+    t, d = _chi2_rows(V, gamma)
+    p = [_softmax(t[l], T) for l in range(gamma + 2)]
+    q = [_softmax(d[l], T) for l in range(gamma + 1)]
+    rng = np.random.RandomState(99)
+
+    def drafts(start):
+        cols = []
+        for i in range(gamma):
+            cdf = np.cumsum(q[start + i])
+            cols.append(np.minimum(np.searchsorted(cdf, rng.rand(trials), side="right"), V - 1))
+        return np.stack(cols, 1).astype(np.int32)
+
+    def rows(a, start, n):
+        return np.broadcast_to(a[start:start + n][None], (trials, n, V))
+
+    x1 = drafts(0)
+    acc1, out1, _ = orc.verify_sample(rows(t, 0, gamma + 1), rows(d, 0, gamma), x1, T, seed, 0)
+    y0 = out1[:, 0]
+    # second token: from this round when it emitted >= 2 tokens, else from a second round
+    # that starts at position 1 with fresh uniforms (offset 1)
+    x2 = drafts(1)
+    acc2, out2, _ = orc.verify_sample(rows(t, 1, gamma + 1), rows(d, 1, gamma), x2, T, seed, 1)
+    y1 = np.where(acc1 >= 1, out1[:, 1], out2[:, 0])
+    assert (acc1 >= 0).all() and (acc1 <= gamma).all()
+    obs0 = np.bincount(y0, minlength=V)
+    _, pv0 = stats.chisquare(obs0, p[0] * trials)
+    obs01 = np.bincount(y0 * V + y1, minlength=V * V)
+    _, pv01 = stats.chisquare(obs01, np.outer(p[0], p[1]).ravel() * trials)
+    assert pv0 > alpha, ("first token", pv0, obs0 / trials, p[0])
+    assert pv01 > alpha, ("first two tokens", pv01)
+
+
+# --------------------------------------------------------------------------------------
+# P3: q == p accepts every draft (u < 1 = p/q) [SD "The rule"]
+# --------------------------------------------------------------------------------------
+def pin_identical_rows_accept_all(orc):
+    rs = np.random.RandomState(3)
+    for gamma, V, T in ((1, 7, 1.0), (4, 50, 0.7), (8, 33, 1.3)):
+        B = 500
+        t = rs.normal(0, 2.0, (B, gamma + 1, V)).astype(np.float32)
+        d = t[:, :gamma, :].copy()
+        x = np.stack([[rs.choice(V, p=_softmax(d[b, i], T)) for i in range(gamma)]
+                      for b in range(B)]).astype(np.int32)
+        acc, out, _ = orc.verify_sample(t, d, x, T, 1234, 0)
+        assert (acc == gamma).all(), np.bincount(acc)
+        assert (out[:, :gamma] == x).all()
+
+
+# --------------------------------------------------------------------------------------
+# P4: point masses reduce sampling to greedy [SD "Extending to a chain": temperature 0]
+# --------------------------------------------------------------------------------------
+def pin_one_hot_equals_greedy(orc):
+    rs = np.random.RandomState(5)
+    B, gamma, V = 400, 5, 40
+    a = rs.randint(0, V, (B, gamma + 1))
+    x = np.where(rs.rand(B, gamma) < 0.7, a[:, :gamma], rs.randint(0, V, (B, gamma)))
+    t = np.full((B, gamma + 1, V), -np.inf, np.float32)
+    d = np.full((B, gamma, V), -np.inf, np.float32)
+    for b in range(B):
+        for i in range(gamma + 1):
+            t[b, i, a[b, i]] = rs.normal()
+        for i in range(gamma):
+            d[b, i, x[b, i]] = rs.normal()
+    acc_s, out_s, _ = orc.verify_sample(t, d, x.astype(np.int32), 1.0, 77, 0)
+    acc_g, out_g = orc.verify_greedy(t, x.astype(np.int32))
+    assert (acc_s == acc_g).all() and (out_s == out_g).all()
+
+
+def pin_one_hot_draft_accept_prob(orc):
+    """q one-hot on x*: P(accept) = p(x*) exactly, residual = p off x*, renormalised."""
+    rs = np.random.RandomState(6)
+    for V in (2, 5, 17):
+        t = rs.normal(0, 1.5, (2, V))
+        xs = int(rs.randint(V))
+        d = np.full((1, V), -np.inf)
+        d[0, xs] = 0.0
+        P = orc.exact_probs(t, d, np.array([xs], np.int32), 1.0)
+        p0 = _softmax(t[0], 1.0)
+        assert abs(P[1].sum() - p0[xs]) < 1e-15
+        res = p0.copy()
+        res[xs] = 0.0
+        res /= res.sum()
+        assert np.max(np.abs(P[0] - (1 - p0[xs]) * res)) < 1e-15
+
+
+# --------------------------------------------------------------------------------------
+# P5: structural invariants of a sampling round [SD "Extending to a chain"]
+# --------------------------------------------------------------------------------------
+def pin_round_invariants(orc):
+    rs = np.random.RandomState(8)
+    for gamma, V in ((1, 3), (3, 11), (6, 64)):
+        B = 300
+        t = rs.normal(0, 2, (B, gamma + 1, V)).astype(np.float32)
+        d = (t[:, :gamma] + rs.normal(0, 1.0, (B, gamma, V))).astype(np.float32)
+        x = rs.randint(0, V, (B, gamma)).astype(np.int32)
+        acc, out, _ = orc.verify_sample(t, d, x, 1.0, 5, 3)
+        assert ((acc >= 0) & (acc <= gamma)).all()
+        for b in range(B):
+            k = acc[b]
+            assert (out[b, :k] == x[b, :k]).all()
+            assert 0 <= out[b, k] < V
+            assert (out[b, k + 1:] == -1).all()
+
+
+# --------------------------------------------------------------------------------------
+# P6: the worked p/q example [HB "The Algorithm"]
+# --------------------------------------------------------------------------------------
+def pin_worked_example(orc):
+    with open(os.path.join(GOLDEN, "worked_example_accept.txt")) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
+    # two-token vocabulary per position: index 0 is the drafted token, index 1 "the rest"
+    qs = [float(r[2]) for r in rows]
+    ps = [float(r[3]) for r in rows]
+    printed = [float(r[4]) for r in rows]
+    gamma = len(rows)
+    t = np.log(np.array([[p, 1 - p] for p in ps] + [[0.5, 0.5]]))
+    d = np.log(np.array([[q, 1 - q] for q in qs]))
+    P = orc.exact_probs(t, d, np.zeros(gamma, np.int32), 1.0)
+    reach = [P[k:].sum() for k in range(gamma + 1)]
+    for i in range(gamma):
+        cond = reach[i + 1] / reach[i]
+        assert abs(cond - min(1.0, ps[i] / qs[i])) < 1e-12
+        assert round(cond, 2) == printed[i], (i, cond, printed[i])
+    # "accepted [A, B], rejected C": the correction after rejecting C never re-emits C,
+    # because the residual (p - q)+ is zero where the draft over-covered
+    assert P[2, 0] == 0.0 and P[2, 1] > 0.0
+
+
+# --------------------------------------------------------------------------------------
+# P7: alpha = sum min(p, q) = 1 - TV(p, q) [SD Exercise 2c] and E[tokens] per round
+#     (1 - alpha^(gamma+1)) / (1 - alpha) = 3.36 at alpha 0.8, k = 4 [HB "The Algorithm"]
+# --------------------------------------------------------------------------------------
+def pin_acceptance_rate(orc):
+    rs = np.random.RandomState(9)
+    for V in (2, 4, 9):
+        t = rs.normal(0, 1.2, (2, V))
+        d = rs.normal(0, 1.2, (1, V))
+        p, q = _softmax(t[0], 1.0), _softmax(d[0], 1.0)
+        acc = sum(q[x] * orc.exact_probs(t, d, np.array([x], np.int32), 1.0)[1].sum()
+                  for x in range(V))
+        assert abs(acc - np.minimum(p, q).sum()) < 1e-14
+        assert abs(acc - (1.0 - 0.5 * np.abs(p - q).sum())) < 1e-14
+    gamma, alpha = 4, 0.8
+    p, q = np.array([0.9, 0.1]), np.array([0.7, 0.3])  # sum min(p, q) = 0.8
+    t = np.log(np.tile(p, (gamma + 1, 1)))
+    d = np.log(np.tile(q, (gamma, 1)))
+    E = 0.0
+    for x in itertools.product(range(2), repeat=gamma):
+        w = np.prod([q[xi] for xi in x])
+        P = orc.exact_probs(t, d, np.array(x, np.int32), 1.0)
+        E += w * sum((k + 1) * P[k].sum() for k in range(gamma + 1))
+    assert abs(E - (1 - alpha ** (gamma + 1)) / (1 - alpha)) < 1e-12
+    assert round(E, 2) == 3.36
+
+
+# --------------------------------------------------------------------------------------
+# P8: greedy = longest prefix matching a textbook argmax [SD "Extending to a chain";
+#     MS speculative_greedy]
+# --------------------------------------------------------------------------------------
+def _bf16_bits_from_float(a):
+    """Round-to-nearest-even fp32 -> bf16 bit patterns (test-side helper)."""
+    u = np.asarray(a, np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    return r
+
+
+def pin_greedy_textbook(orc):
+    rs = np.random.RandomState(10)
+    for gamma, V, dt in ((1, 5, "f32"), (4, 37, "bf16"), (6, 300, "f32"), (3, 1, "f32")):
+        B = 300
+        # small integers -> many exact ties, so the lowest-index rule is exercised
+        vals = rs.randint(-3, 4, (B, gamma + 1, V)).astype(np.float32)
+        a = np.argmax(vals, axis=-1)  # numpy: first occurrence of the maximum
+        x = np.where(rs.rand(B, gamma) < 0.75, a[:, :gamma], rs.randint(0, V, (B, gamma)))
+        x = x.astype(np.int32)
+        nan_rows = rs.rand(B) < 0.05
+        vals[nan_rows, rs.randint(0, gamma + 1), rs.randint(0, V)] = np.nan
+        bad_tok = (rs.rand(B) < 0.03) & (gamma > 0)
+        x[bad_tok, 0] = V + 3
+        logits = _bf16_bits_from_float(vals) if dt == "bf16" else vals
+        acc, out = orc.verify_greedy(logits, x)
+        for b in range(B):
+            if nan_rows[b] or bad_tok[b]:
+                assert acc[b] == -1 and (out[b] == -1).all()
+                continue
+            n = 0
+            while n < gamma and x[b, n] == a[b, n]:
+                n += 1
+            assert acc[b] == n
+            assert list(out[b, :n]) == list(x[b, :n]) and out[b, n] == a[b, n]
+            assert (out[b, n + 1:] == -1).all()
+
+
+# --------------------------------------------------------------------------------------
+# P9: trees -- the printed depths [SD "Tree Attention"], a chain tree equals greedy, and
+#     brute force over root paths [SD Exercise 5]
+# --------------------------------------------------------------------------------------
+def pin_tree_printed_depths(orc):
+    with open(os.path.join(GOLDEN, "tree_depths.txt")) as f:
+        kv = {ln.split()[0]: [int(v) for v in ln.split()[1:]] for ln in f
+              if ln.strip() and not ln.startswith("#")}
+    parents, depths = kv["parents"], kv["depths"]
+    N, V = len(parents), 8
+    # one sequence per node v: only the path root -> v matches, so accepted_len = depth(v)
+    B = N
+    t = np.zeros((B, N, V), np.float32)
+    tokens = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for u in range(N):
+            t[b, u, (u + 1) % V] = 5.0  # argmax of node u is (u + 1) % V
+        on_path = set()
+        w = b
+        while w != -1:
+            on_path.add(w)
+            w = parents[w]
+        for u in range(1, N):
+            want = (parents[u] + 1) % V
+            tokens[b, u] = want if u in on_path else (want + 1) % V
+    acc, out, path, _ = orc.verify_tree_greedy(t, parents, tokens, max(depths))
+    assert list(acc) == depths
+    for b in range(B):
+        assert path[b, depths[b]] == b
+
+
+def pin_chain_tree_equals_greedy(orc):
+    rs = np.random.RandomState(12)
+    for gamma, V in ((1, 4), (5, 23), (7, 100)):
+        B = 200
+        vals = rs.randint(-2, 3, (B, gamma + 1, V)).astype(np.float32)
+        a = np.argmax(vals, axis=-1)
+        x = np.where(rs.rand(B, gamma) < 0.8, a[:, :gamma], rs.randint(0, V, (B, gamma)))
+        x = x.astype(np.int32)
+        parent = [-1] + list(range(gamma))
+        tokens = np.concatenate([np.zeros((B, 1), np.int32), x], 1)
+        acc_t, out_t, path_t, _ = orc.verify_tree_greedy(vals, parent, tokens, gamma)
+        acc_g, out_g = orc.verify_greedy(vals, x)
+        assert (acc_t == acc_g).all() and (out_t == out_g).all()
+        for b in range(B):
+            assert list(path_t[b, :acc_t[b] + 1]) == list(range(acc_t[b] + 1))
+
+
+def random_tree(rs, N):
+    parent = [-1] + [int(rs.randint(0, v)) for v in range(1, N)]
+    return parent
+
+
+def pin_tree_bruteforce(orc):
+    rs = np.random.RandomState(13)
+    for N, V, dup in ((1, 3, False), (2, 2, False), (9, 3, True), (30, 5, True), (64, 50, False)):
+        B = 150
+        parent = random_tree(rs, N)
+        depth = [0] * N
+        for v in range(1, N):
+            depth[v] = depth[parent[v]] + 1
+        D = max(depth)
+        vals = rs.randint(-2, 3, (B, N, V)).astype(np.float32)
+        a = np.argmax(vals, axis=-1)
+        tokens = rs.randint(0, V, (B, N)).astype(np.int32)
+        for b in range(B):
+            for v in range(1, N):
+                if rs.rand() < 0.6:
+                    tokens[b, v] = a[b, parent[v]]
+        acc, out, path, flags = orc.verify_tree_greedy(vals, parent, tokens, D)
+        for b in range(B):
+            ok = []
+            for v in range(N):  # a node is accepted iff every edge on its root path matches
+                w, good = v, True
+                while w != 0:
+                    good &= tokens[b, w] == a[b, parent[w]]
+                    w = parent[w]
+                ok.append(good)
+            cands = [v for v in range(N) if ok[v]]
+            best = min(cands, key=lambda v: (-depth[v], v))
+            chain = []
+            w = best
+            while w != -1:
+                chain.append(w)
+                w = parent[w]
+            chain = chain[::-1]
+            assert acc[b] == depth[best]
+            assert list(path[b, :len(chain)]) == chain and (path[b, len(chain):] == -1).all()
+            assert list(out[b, :depth[best]]) == [tokens[b, w] for w in chain[1:]]
+            assert out[b, depth[best]] == a[b, best]
+            # Exercise 5's greedy walk takes the first matching child at each node
+            node, walk = 0, [0]
+            while True:
+                nxt = [c for c in range(N) if parent[c] == node and tokens[b, c] == a[b, node]]
+                if not nxt:
+                    break
+                node = nxt[0]
+                walk.append(node)
+            assert bool(flags[b] & 1) == (walk != chain)
+    # a malformed or too-deep tree invalidates every sequence
+    vals = np.zeros((2, 3, 4), np.float32)
+    toks = np.zeros((2, 3), np.int32)
+    for par, D in (([-1, 0, 2], 2), ([0, 0, 1], 2), ([-1, 0, 1], 1)):
+        acc, out, path, _ = orc.verify_tree_greedy(vals, par, toks, D)
+        assert (acc == -1).all() and (out == -1).all() and (path == -1).all()
+
+
+# --------------------------------------------------------------------------------------
+# P10: row max / log-sum-exp against scipy's logsumexp [SD apply_temperature]
+# --------------------------------------------------------------------------------------
+def pin_row_stats(orc):
+    rs = np.random.RandomState(14)
+    for V, T in ((1, 1.0), (7, 0.7), (1000, 1.3), (4099, 0.5)):
+        l = rs.normal(0, 3, (3, 4, V)).astype(np.float32)
+        l[0, 1, : V // 2] = -np.inf
+        m, lse, valid = orc.row_stats(l, T)
+        ref = special.logsumexp(l.astype(np.float64) / T, axis=-1)
+        assert valid.all()
+        assert np.max(np.abs(lse - ref) / np.maximum(np.abs(ref), 1)) < 1e-13
+        assert np.array_equal(m, np.max(l.astype(np.float64), -1) / T)
+    l = np.zeros((1, 3, 4), np.float32)
+    l[0, 0, 1] = np.nan
+    l[0, 1, :] = -np.inf
+    l[0, 2, 2] = np.inf
+    _, _, valid = orc.row_stats(l, 1.0)
+    assert not valid.any()
+
+
+ALL_PINS = [
+    pin_philox_kat, pin_uniform_definition, pin_bruteforce_lossless, pin_chi2_sampler,
+    pin_identical_rows_accept_all, pin_one_hot_equals_greedy, pin_one_hot_draft_accept_prob,
+    pin_round_invariants, pin_worked_example, pin_acceptance_rate, pin_greedy_textbook,
+    pin_tree_printed_depths, pin_chain_tree_equals_greedy, pin_tree_bruteforce, pin_row_stats,
+]
