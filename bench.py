@@ -1,0 +1,495 @@
+#!/usr/bin/env python
+"""Throughput of the speculative-decoding verification step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one verify call over one batch of the workload (default: sampling verify,
+B=256, V=128256, gamma=8, bf16 logits, T=0.7 -- every kernel of the sampling path).  The
+greedy (B=512, V=152064, gamma=6) and tree (B=64, N=64, V=128256) workloads are measured
+the same way and reported under "modes".  Inputs are synthetic and resident in HBM; each
+step reads more than L2 holds, so no flush is needed between steps.
+
+Under torchrun (N > 1) each rank verifies its own batch (sequences are independent: weak
+scaling, no collective on the data path); the time is the max over ranks.
+
+--impl reference times the oracle (plain fp64 C, tests' reference) on the host cores over
+a bounded sample of the same workload, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "sample_b256"
+SECONDARY = ["greedy_b512", "tree_b64"]
+METRIC = "verified seqs/s"
+UNIT = "seqs/s"
+FALLBACK_HBM_GBS = 6800.0
+DOMINANT_KERNEL = {"sample": "stats_partial_kernel", "greedy": "argmax_partial_kernel",
+                   "tree": "argmax_partial_kernel"}
+STAGES = {"sample": ["row_stats", "decide", "residual_mass", "inverse_cdf"],
+          "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"]}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-modes", action="store_true", help="skip the greedy / tree workloads")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=30)
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------------------
+# process group
+# ----------------------------------------------------------------------------------------
+def dist_setup(backend="nccl"):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{self.gpu}.csv")
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1].split()[0]))
+                mx = float(parts[2].split()[0])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------------------
+# measured peaks and committed ncu traffic
+# ----------------------------------------------------------------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    csrc = os.path.join(ROOT, "speculative_decoding_verify_spec_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from profiles/traffic.txt, if the
+    capture was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    digest = source_digest()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and \
+                parts[1] == workload and parts[2] == digest:
+            return float(parts[3])
+    return None
+
+
+# ----------------------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------------------
+def kernel_bytes(name: str) -> int:
+    """Algorithmic bytes of the dominant kernel per launch: every logit it streams, once."""
+    from speculative_decoding_verify_spec_gb300 import workloads as W
+    cfg = W.WORKLOADS[name]
+    s = 2 if cfg["dtype"] == "bf16" else 4
+    return W.rows(name) * cfg["V"] * s
+
+
+def make_call(name, inputs, dev):
+    """A closure that runs one verify call of the workload into preallocated outputs."""
+    import torch
+    import speculative_decoding_verify_spec_gb300 as sv
+    from speculative_decoding_verify_spec_gb300 import binding
+    from speculative_decoding_verify_spec_gb300 import workloads as W
+
+    cfg = W.WORKLOADS[name]
+    mode = cfg["mode"]
+    B, V = cfg["B"], cfg["V"]
+    dt = binding.BF16 if cfg["dtype"] == "bf16" else binding.FP32
+    if mode == "sample":
+        g = cfg["gamma"]
+        ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_SAMPLE, B, g, V, dt),
+                         dtype=torch.uint8, device=dev)
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        out = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+        step_counter = [0]
+
+        def call(target=inputs.target, draft=inputs.draft, tokens=inputs.draft_tokens):
+            step_counter[0] += 1
+            return sv.spec_verify_sample(target, draft, tokens, inputs.temperature, inputs.seed,
+                                         step_counter[0], workspace=ws, accepted_len=acc,
+                                         out_tokens=out)
+        return call, (acc, out)
+    if mode == "greedy":
+        g = cfg["gamma"]
+        ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_GREEDY, B, g, V, dt),
+                         dtype=torch.uint8, device=dev)
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        out = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+
+        def call(target=inputs.target, tokens=inputs.draft_tokens):
+            return sv.spec_verify_greedy(target, tokens, workspace=ws, accepted_len=acc, out_tokens=out)
+        return call, (acc, out)
+    N = cfg["N"]
+    ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_TREE, B, N, V, dt),
+                     dtype=torch.uint8, device=dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    out = torch.empty((B, inputs.max_depth + 1), dtype=torch.int32, device=dev)
+    path = torch.empty((B, inputs.max_depth + 1), dtype=torch.int32, device=dev)
+
+    def call(target=inputs.target, tokens=inputs.node_tokens):
+        return sv.spec_verify_tree_greedy(target, inputs.parent, tokens, inputs.max_depth,
+                                          workspace=ws, accepted_len=acc, out_tokens=out,
+                                          out_path=path)
+    return call, (acc, out, path)
+
+
+def measure(name, steps, warmup, rank, world, dev, peak, peak_kind):
+    import torch
+    from speculative_decoding_verify_spec_gb300 import binding
+    from speculative_decoding_verify_spec_gb300 import workloads as W
+
+    cfg = W.WORKLOADS[name]
+    mode = cfg["mode"]
+    inputs = W.make(name, device=dev, input_seed=cfg["input_seed"] + 7919 * rank)
+    call, outs = make_call(name, inputs, dev)
+    nst = len(STAGES[mode])
+    if mode == "sample" and cfg["gamma"] == 0:
+        nst = 4
+    for _ in range(max(3, warmup)):
+        call()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(steps)]
+    for row in ev:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for k in range(steps):
+        binding.set_stage_events(ev[k])
+        call()
+    end.record()
+    binding.set_stage_events(None)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(end)
+    ms_max = max_over_ranks(ms, world, dev)
+    stage_ms = [sum(ev[k][s].elapsed_time(ev[k][s + 1]) for k in range(steps)) / steps
+                for s in range(nst)]
+    ms_step = ms_max / steps
+    B = cfg["B"]
+    value = world * B / (ms_step / 1e3)
+    logical = W.logical_bytes(name)
+    kb = kernel_bytes(name)
+    dom_ms = stage_ms[0]
+    achieved = kb / (dom_ms / 1e3) / 1e9
+    kernel = DOMINANT_KERNEL[mode]
+    acc = outs[0].float()
+    res = {
+        "workload": W.DESCRIPTIONS[name], "value": value, "unit": UNIT, "ms_per_step": ms_step,
+        "steps": steps, "rows_per_s": world * W.rows(name) / (ms_step / 1e3),
+        "hbm_gbs_step": logical / (ms_step / 1e3) / 1e9,
+        "frac_of_8tbs_step": logical / (ms_step / 1e3) / 8e12,
+        "stages_ms": dict(zip(STAGES[mode], stage_ms)),
+        "mean_accepted_len": float(acc[acc >= 0].mean().item()) if (acc >= 0).any() else None,
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "bytes_per_launch": kb,
+                     "traffic": committed_traffic(kernel, name)},
+        "gpu_launches": steps * (nst if mode != "sample" or cfg["gamma"] > 0 else 3),
+    }
+    return res, inputs, call
+
+
+def measure_e2e(name, inputs, steps, dev):
+    """The same metric through the public call with host buffers: every step copies its
+    inputs from pinned host memory and reads the results back."""
+    import torch
+    from speculative_decoding_verify_spec_gb300 import workloads as W
+
+    cfg = W.WORKLOADS[name]
+    mode = cfg["mode"]
+    host_in = {}
+    dev_in = {}
+    keys = ["target", "draft", "draft_tokens"] if mode == "sample" else (
+        ["target", "draft_tokens"] if mode == "greedy" else ["target", "node_tokens"])
+    for k in keys:
+        t = getattr(inputs, k)
+        host_in[k] = t.cpu().pin_memory()
+        dev_in[k] = torch.empty_like(t)
+    call, outs = make_call(name, inputs, dev)
+    host_out = [o.cpu().pin_memory() for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def step():
+        for k in keys:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        if mode == "sample":
+            call(dev_in["target"], dev_in["draft"], dev_in["draft_tokens"])
+        elif mode == "greedy":
+            call(dev_in["target"], dev_in["draft_tokens"])
+        else:
+            call(dev_in["target"], dev_in["node_tokens"])
+        for h, o in zip(host_out, outs):
+            h.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return {"value": cfg["B"] / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def oracle_run(name, inputs, threads):
+    """The oracle over a batch, one thread per range of sequences."""
+    import numpy as np
+    import oracle
+    from speculative_decoding_verify_spec_gb300 import workloads as W
+
+    cfg = W.WORKLOADS[name]
+    mode = cfg["mode"]
+    orc = oracle.default()
+    t = oracle.as_oracle_logits(inputs.target)
+    B = t.shape[0]
+    step = max(1, (B + threads - 1) // threads)
+    ranges = [(s, min(B, s + step)) for s in range(0, B, step)]
+    if mode == "sample":
+        d = oracle.as_oracle_logits(inputs.draft)
+        x = inputs.draft_tokens.cpu().numpy()
+        fn = lambda r: orc.verify_sample(t[r[0]:r[1]], d[r[0]:r[1]], x[r[0]:r[1]],
+                                         inputs.temperature, inputs.seed, 0, b0=r[0])
+    elif mode == "greedy":
+        x = inputs.draft_tokens.cpu().numpy()
+        fn = lambda r: orc.verify_greedy(t[r[0]:r[1]], x[r[0]:r[1]])
+    else:
+        par = inputs.parent.cpu().numpy()
+        x = inputs.node_tokens.cpu().numpy()
+        fn = lambda r: orc.verify_tree_greedy(t[r[0]:r[1]], par, x[r[0]:r[1]], inputs.max_depth)
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(fn, ranges))
+    return B, len(ranges)
+
+
+def cpu_baseline(name, inputs):
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    B, used = oracle_run(name, inputs, cores)
+    dt = time.perf_counter() - t0
+    return {"value": B / dt, "unit": UNIT, "cores": min(cores, used), "kind": "oracle",
+            "sample": f"the full batch of {B} sequences of the same workload, once "
+                      f"({dt:.2f} s wall on {min(cores, used)} threads)"}
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_setup("nccl" if args.gpus > 1 else "gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    from speculative_decoding_verify_spec_gb300 import workloads as W
+
+    peak, peak_kind = hbm_peak()
+    clocks = ClockSampler(local)
+    clocks.start()
+    main, inputs, _ = measure(args.workload, args.steps, args.warmup, rank, world, dev, peak, peak_kind)
+    clk = clocks.stop()
+    modes = {}
+    if not args.no_modes:
+        for name in SECONDARY:
+            if name == args.workload:
+                continue
+            r, inp, _ = measure(name, args.steps, args.warmup, rank, world, dev, peak, peak_kind)
+            modes[name] = r
+            del inp
+            torch.cuda.empty_cache()
+    e2e = measure_e2e(args.workload, inputs, max(3, args.e2e_steps), dev)
+    e2e_val = max_over_ranks(e2e["ms_per_step"], world, dev)
+    e2e["value"] = world * W.WORKLOADS[args.workload]["B"] / (e2e_val / 1e3)
+    e2e["ms_per_step"] = e2e_val
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload, inputs)
+    if rank == 0:
+        cfg = W.WORKLOADS[args.workload]
+        line = {
+            "metric": METRIC, "value": main["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded generators, resident in HBM)",
+            "config": {"workload": W.DESCRIPTIONS[args.workload], "B": cfg["B"],
+                       "gamma": cfg.get("gamma"), "V": cfg["V"], "logits": cfg["dtype"],
+                       "temperature": cfg.get("temperature"),
+                       "l2": f"inputs larger than L2 ({W.logical_bytes(args.workload) / 1e9:.2f} GB "
+                             "read per step), no flush",
+                       "parallelism": f"replicas x{world} (independent batches per GPU)"},
+            "rows_per_s": main["rows_per_s"], "hbm_gbs": main["hbm_gbs_step"],
+            "frac_of_8tbs": main["frac_of_8tbs_step"],
+            "mean_accepted_len": main["mean_accepted_len"], "stages_ms": main["stages_ms"],
+            "roofline": main["roofline"], "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": main["gpu_launches"], "clocks": clk, "modes": modes,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ----------------------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    from speculative_decoding_verify_spec_gb300 import workloads as W
+    import __graft_entry__
+
+    __graft_entry__._build_oracle()
+    name = args.workload
+    cfg = W.WORKLOADS[name]
+    cores = os.cpu_count() or 1
+    per_step = min(cfg["B"], cores)
+    inputs = W.make(name, device="cpu", B=per_step)
+    for _ in range(max(1, min(args.warmup, 3))):
+        oracle_run(name, inputs, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_run(name, inputs, cores)
+    dt = time.perf_counter() - t0
+    value = args.steps * per_step / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generators)",
+        "config": {"workload": W.DESCRIPTIONS[name], "B": cfg["B"], "gamma": cfg.get("gamma"),
+                   "V": cfg["V"], "logits": cfg["dtype"]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, per_step), "kind": "oracle",
+                         "sample": f"{per_step} sequences of the workload per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

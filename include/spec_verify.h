@@ -1,0 +1,188 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify, the speculative-decoding verification step on
+ * one GPU (hand-written sm_103a CUDA kernels).
+ *
+ * Sources (page title -- section):
+ *   [SD] "7.6 Speculative Decoding: Draft Models, Medusa, EAGLE & Lookahead": "The rule"
+ *        (accept x with probability min(1, p(x)/q(x)), else resample from the normalised
+ *        residual (p - q)+), "Extending to a chain of gamma draft tokens" (left to right,
+ *        stop at the first rejection, bonus token from row gamma when all are accepted;
+ *        temperature 0 = longest matching prefix), "A From-Scratch Implementation"
+ *        (apply_temperature on BOTH models; row i of the target predicts the token after
+ *        draft i), "Tree Attention" and Exercise 5 (verify_tree_greedy on a parent-indexed
+ *        tree whose row i predicts the token after node i).
+ *   [MS] "Medusa, EAGLE and self-speculation": speculative_greedy (the correction token is
+ *        the argmax at the first mismatching row).
+ *   [HB] "Speculative Decoding: Draft Models, EAGLE, and How to Actually Use It": "The
+ *        Algorithm" (steps 1-4).
+ *
+ * Conventions shared by every entry point
+ *   - Every array argument is a DEVICE pointer; the caller owns all memory.  The library
+ *     allocates nothing and keeps no state between calls (apart from the optional,
+ *     thread-local timing events of spec_verify_set_stage_events).
+ *   - Logits are [B][rows][V] with a contiguous last axis.  Strides are in ELEMENTS and may
+ *     be 0 (broadcast).  Rows are read with 16-byte vector loads when the base pointer and
+ *     both strides (times the element size) are multiples of 16 bytes, else element-wise.
+ *   - Integer arrays (tokens, lengths, parents, paths) are int32, contiguous, row-major.
+ *   - A call validates its arguments on the host and returns an error code BEFORE any
+ *     work is enqueued; otherwise it enqueues its kernels on `stream` (a cudaStream_t;
+ *     NULL = the legacy default stream) and returns without synchronising.  A launch
+ *     failure returns SV_ERR_CUDA.
+ *   - Bad data inside one sequence (a NaN, or for sampling a +inf or an all -inf row; a
+ *     token outside [0, V)) is reported per sequence: accepted_len[b] = -1 and every output
+ *     token of that sequence = -1.  Other sequences are unaffected.
+ *   - `workspace` is caller-provided device scratch of at least
+ *     spec_verify_workspace_size(...) bytes, 16-byte aligned.  Its contents need no
+ *     initialisation and are meaningless after the call.  Calls that run concurrently
+ *     need distinct workspaces.
+ *   - A round emits accepted_len[b] + 1 tokens (always >= 1) [SD "Extending to a chain"].
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1, /* a size, stride, pointer or temperature is out of range */
+    SV_ERR_UNSUPPORTED = 2, /* dtype or mode not supported */
+    SV_ERR_CUDA = 3,        /* a CUDA launch failed; see cudaGetLastError semantics */
+    SV_ERR_TIMEOUT = 4,     /* reserved: a bounded device wait gave up */
+    SV_ERR_WORKSPACE = 5    /* workspace NULL, too small or not 16-byte aligned */
+} sv_status;
+
+typedef enum { SV_FP32 = 0, SV_BF16 = 1 } sv_dtype;
+
+typedef enum {
+    SV_MODE_SAMPLE = 0,    /* spec_verify_sample:      rows = gamma */
+    SV_MODE_GREEDY = 1,    /* spec_verify_greedy:      rows = gamma */
+    SV_MODE_TREE = 2,      /* spec_verify_tree_greedy: rows = N     */
+    SV_MODE_ROW_STATS = 3  /* spec_verify_row_stats:   rows = rows_per_seq */
+} sv_mode;
+
+/* Limits checked on the host (SV_ERR_INVALID_ARG beyond them). */
+#define SV_MAX_GAMMA 1024
+#define SV_MAX_TREE_NODES 1024
+#define SV_MAX_VOCAB (1 << 30)
+
+/* Bytes of device workspace the given call needs (0 when B == 0).  Pure host function. */
+size_t spec_verify_workspace_size(sv_mode mode, int B, int rows, int V, sv_dtype dtype);
+
+/*
+ * Sampling verification [SD "The rule", "Extending to a chain"; HB "The Algorithm"].
+ *
+ *   target_logits  [B][gamma+1][V]  row i predicts the token after draft i; row gamma is the
+ *                                   bonus row.  Strides t_batch_stride, t_row_stride.
+ *   draft_logits   [B][gamma][V]    the drafter's logits at the drafted positions (may be
+ *                                   NULL when gamma == 0).  Strides d_batch_stride, d_row_stride.
+ *   dtype          both logits arrays have this element type (fp32 or bf16).
+ *   draft_tokens   [B][gamma]       x_0 .. x_{gamma-1}, drawn by the drafter from q.
+ *   temperature    > 0 and finite; p = softmax(target / T), q = softmax(draft / T) (the
+ *                  temperature applies to BOTH models).
+ *   seed, offset   key the Philox4x32-10 uniforms: u(b, i, purpose) is word 0 of Philox
+ *                  at counter (4 i + purpose, b, offset lo32, offset hi32) with key
+ *                  (seed lo32, seed hi32), mapped to (w >> 8) * 2^-24.  purpose 0: the
+ *                  accept test of draft i; purpose 1: the final draw on row i.  Callers vary
+ *                  seed or offset between rounds.
+ * Per sequence b: draft i is accepted iff u(b,i,0) * q_i(x_i) < p_i(x_i) (the strict test
+ * u < min(1, p/q) with the division cleared).  The first rejection at k ends the round and
+ * the token at k is drawn from (p_k - q_k)+ (if that residual is exactly 0, from p_k);
+ * if all gamma are accepted, k = gamma and the bonus token is drawn from p_gamma.  A draw
+ * is the inverse CDF in vocabulary order: the first j with r_0 + ... + r_j > u(b,k,1) * R.
+ * Outputs:
+ *   accepted_len   [B]           k, or -1 for bad data.
+ *   out_tokens     [B][gamma+1]  x_0 .. x_{k-1}, the drawn token at k, then -1.
+ */
+sv_status spec_verify_sample(const void *target_logits, int64_t t_batch_stride,
+                             int64_t t_row_stride, const void *draft_logits,
+                             int64_t d_batch_stride, int64_t d_row_stride, sv_dtype dtype, int B,
+                             int gamma, int V, const int32_t *draft_tokens, float temperature,
+                             uint64_t seed, uint64_t offset, int32_t *accepted_len,
+                             int32_t *out_tokens, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
+ * Greedy verification [SD "Extending to a chain" (temperature 0); MS speculative_greedy].
+ *
+ *   target_logits  [B][gamma+1][V], draft_tokens [B][gamma].
+ * a_i = argmax of row i (ties to the lowest index, values compared exactly after widening
+ * to fp32).  n = the longest prefix with draft_tokens[b][i] == a_i.  Outputs:
+ *   accepted_len [B] = n (or -1: a NaN in any row, or a draft token outside [0, V));
+ *   out_tokens [B][gamma+1] = x_0 .. x_{n-1}, a_n, then -1.
+ */
+sv_status spec_verify_greedy(const void *target_logits, int64_t t_batch_stride,
+                             int64_t t_row_stride, sv_dtype dtype, int B, int gamma, int V,
+                             const int32_t *draft_tokens, int32_t *accepted_len,
+                             int32_t *out_tokens, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
+ * Greedy token-tree verification [SD "Tree Attention", Exercise 5].
+ *
+ *   target_logits  [B][N][V]  row v predicts the token that follows node v.
+ *   parent         [N]        parent[0] = -1, 0 <= parent[v] < v (parents before children);
+ *                             one tree shared by the whole batch.
+ *   node_tokens    [B][N]     the drafted token at node v ([b][0], the committed root, is
+ *                             ignored).
+ *   max_depth      >= the tree's depth; the width of the outputs is max_depth + 1.
+ * Node v != 0 is accepted when node_tokens[b][v] == argmax(row parent[v]) and its parent is
+ * accepted (the root always is).  v* = the deepest accepted node, the lowest index among
+ * equally deep ones.  Outputs (each row max_depth+1 wide, -1 padded):
+ *   accepted_len [B] = depth(v*);  out_tokens[b] = tokens on the path root -> v* without
+ *   the root, then argmax(row v*) (the bonus);  out_path[b] = node ids root .. v* (out_path
+ *   may be NULL).  A malformed tree, or one deeper than max_depth, makes every sequence -1;
+ *   a NaN in any row of b, or a token of b outside [0, V), makes sequence b -1.
+ */
+sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_stride,
+                                  int64_t t_row_stride, sv_dtype dtype, int B, int N, int V,
+                                  const int32_t *parent, const int32_t *node_tokens,
+                                  int max_depth, int32_t *accepted_len, int32_t *out_tokens,
+                                  int32_t *out_path, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/*
+ * Test hook: the per-row statistics of the sampling path [SD apply_temperature].
+ *   logits [B][rows_per_seq][V].  m_out[b*rows_per_seq + r] = max_j l_j / T,
+ *   lse_out[...] = m + ln sum_j exp(l_j / T - m); both NaN for a row with a NaN, a +inf or
+ *   no finite entry.  Computed by the same kernels as spec_verify_sample.
+ */
+sv_status spec_verify_row_stats(const void *logits, int64_t batch_stride, int64_t row_stride,
+                                sv_dtype dtype, int B, int rows_per_seq, int V,
+                                float temperature, float *m_out, float *lse_out,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Test hook: the uniforms the sampler draws.  out[b * positions + i] = u(b, i, purpose) as
+ * defined under spec_verify_sample, for b < B, i < positions, purpose in {0, 1}.
+ */
+sv_status spec_verify_uniforms(uint64_t seed, uint64_t offset, int B, int positions,
+                               int purpose, float *out, void *stream);
+
+/*
+ * Optional timing instrumentation for the CALLING THREAD (the only state the library
+ * keeps, and it is thread-local).  With events != NULL, each later call of
+ * spec_verify_sample / _greedy / _tree_greedy on this thread records events[0] on its
+ * stream before its first kernel and events[s] after its s-th kernel (s = 1 .. n_events-1;
+ * sampling has 4 kernels: row statistics, decide, residual masses, inverse-CDF draw; greedy
+ * and tree have 2: argmax partials, finalize).  The events are cudaEvent_t handles created
+ * and owned by the caller; recording them adds no synchronisation.  Pass NULL (or 0) to
+ * turn it off.  Returns SV_ERR_INVALID_ARG for n_events < 0 or > 8.
+ */
+sv_status spec_verify_set_stage_events(void *const *events, int n_events);
+
+/* A static, human-readable name for a status code. */
+const char *spec_verify_status_string(sv_status status);
+
+/* ABI version of this header (major * 100 + minor). */
+int spec_verify_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,241 @@
+"""Thin Python binding of libspecverify (ctypes).
+
+Argument marshalling only: each function checks tensor placement, dtype and shape, takes
+element strides and the current CUDA stream from PyTorch, allocates the outputs and the
+workspace with PyTorch's caching allocator, and calls the C entry point of the same name.
+Every step of the verification runs in the library's CUDA kernels; there is no CPU path.
+If the shared library is missing the first call raises, telling how to build it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import _build
+
+SV_OK = 0
+MODE_SAMPLE, MODE_GREEDY, MODE_TREE, MODE_ROW_STATS = 0, 1, 2, 3
+FP32, BF16 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libspecverify.so (built in-tree by __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise SpecVerifyError(
+                f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(path)
+        P, i64, i32, u64, f32, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64,
+                                     ctypes.c_float, ctypes.c_size_t)
+        lib.spec_verify_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        lib.spec_verify_workspace_size.restype = sz
+        lib.spec_verify_sample.argtypes = [P, i64, i64, P, i64, i64, i32, i32, i32, i32, P, f32, u64,
+                                           u64, P, P, P, sz, P]
+        lib.spec_verify_sample.restype = i32
+        lib.spec_verify_greedy.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, P, P, sz, P]
+        lib.spec_verify_greedy.restype = i32
+        lib.spec_verify_tree_greedy.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, i32, P, P, P,
+                                                P, sz, P]
+        lib.spec_verify_tree_greedy.restype = i32
+        lib.spec_verify_row_stats.argtypes = [P, i64, i64, i32, i32, i32, i32, f32, P, P, P, sz, P]
+        lib.spec_verify_row_stats.restype = i32
+        lib.spec_verify_uniforms.argtypes = [u64, u64, i32, i32, i32, P, P]
+        lib.spec_verify_uniforms.restype = i32
+        lib.spec_verify_set_stage_events.argtypes = [P, i32]
+        lib.spec_verify_set_stage_events.restype = i32
+        lib.spec_verify_status_string.argtypes = [i32]
+        lib.spec_verify_status_string.restype = ctypes.c_char_p
+        lib.spec_verify_version.argtypes = []
+        lib.spec_verify_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _check(status: int, what: str):
+    if status != SV_OK:
+        msg = load_library().spec_verify_status_string(status).decode()
+        raise SpecVerifyError(f"{what} failed with status {status}: {msg}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _logits3(t: torch.Tensor, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the verifier has no CPU path)")
+    if t.dim() != 3 or (t.shape[2] > 1 and t.stride(2) != 1):
+        raise ValueError(f"{name} must be [B, rows, V] with a contiguous last axis")
+    return t.stride(0), t.stride(1)
+
+
+def _ints(t: torch.Tensor, name: str, shape) -> torch.Tensor:
+    if not t.is_cuda or t.dtype != torch.int32:
+        raise ValueError(f"{name} must be an int32 CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.contiguous()
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def spec_verify_workspace_size(mode: int, B: int, rows: int, V: int, dtype: int) -> int:
+    return int(load_library().spec_verify_workspace_size(mode, B, rows, V, dtype))
+
+
+def _workspace(mode, B, rows, V, dtype, device, workspace):
+    n = spec_verify_workspace_size(mode, B, rows, V, dtype)
+    if workspace is None:
+        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=device)
+    elif workspace.numel() * workspace.element_size() < n:
+        raise ValueError(f"workspace too small: need {n} bytes")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def spec_verify_sample(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor,
+                       temperature: float, seed: int, offset: int = 0, *, workspace=None,
+                       accepted_len=None, out_tokens=None):
+    """Sampling verification; returns (accepted_len [B] int32, out_tokens [B, gamma+1] int32)."""
+    lib = load_library()
+    tsb, tsr = _logits3(target, "target")
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    dt = _dtype_code(target)
+    if gamma > 0:
+        dsb, dsr = _logits3(draft, "draft")
+        if draft.dtype != target.dtype or tuple(draft.shape) != (B, gamma, V):
+            raise ValueError("draft must be [B, gamma, V] with the target's dtype")
+        dptr = draft.data_ptr()
+        x = _ints(draft_tokens, "draft_tokens", (B, gamma))
+        xptr = x.data_ptr()
+    else:
+        dsb = dsr = 0
+        dptr = xptr = None
+    dev = target.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    ws, wsb = _workspace(MODE_SAMPLE, B, gamma, V, dt, dev, workspace)
+    st = lib.spec_verify_sample(target.data_ptr(), tsb, tsr, dptr, dsb, dsr, dt, B, gamma, V, xptr,
+                                float(temperature), int(seed) & (2**64 - 1),
+                                int(offset) & (2**64 - 1), accepted_len.data_ptr(),
+                                out_tokens.data_ptr(), ws.data_ptr(), wsb, _stream(dev))
+    _check(st, "spec_verify_sample")
+    return accepted_len, out_tokens
+
+
+def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, *, workspace=None,
+                       accepted_len=None, out_tokens=None):
+    """Greedy verification; returns (accepted_len [B], out_tokens [B, gamma+1])."""
+    lib = load_library()
+    tsb, tsr = _logits3(target, "target")
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    dt = _dtype_code(target)
+    x = _ints(draft_tokens, "draft_tokens", (B, gamma)) if gamma > 0 else None
+    dev = target.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    ws, wsb = _workspace(MODE_GREEDY, B, gamma, V, dt, dev, workspace)
+    st = lib.spec_verify_greedy(target.data_ptr(), tsb, tsr, dt, B, gamma, V,
+                                x.data_ptr() if x is not None else None, accepted_len.data_ptr(),
+                                out_tokens.data_ptr(), ws.data_ptr(), wsb, _stream(dev))
+    _check(st, "spec_verify_greedy")
+    return accepted_len, out_tokens
+
+
+def spec_verify_tree_greedy(target: torch.Tensor, parent: torch.Tensor, node_tokens: torch.Tensor,
+                            max_depth: int, *, with_path: bool = True, workspace=None,
+                            accepted_len=None, out_tokens=None, out_path=None):
+    """Greedy token-tree verification; returns (accepted_len [B], out_tokens [B, D+1],
+    out_path [B, D+1] or None)."""
+    lib = load_library()
+    tsb, tsr = _logits3(target, "target")
+    B, N, V = target.shape
+    dt = _dtype_code(target)
+    par = _ints(parent, "parent", (N,))
+    tok = _ints(node_tokens, "node_tokens", (B, N))
+    dev = target.device
+    W = int(max_depth) + 1
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, W), dtype=torch.int32, device=dev)
+    if with_path and out_path is None:
+        out_path = torch.empty((B, W), dtype=torch.int32, device=dev)
+    ws, wsb = _workspace(MODE_TREE, B, N, V, dt, dev, workspace)
+    st = lib.spec_verify_tree_greedy(target.data_ptr(), tsb, tsr, dt, B, N, V, par.data_ptr(),
+                                     tok.data_ptr(), int(max_depth), accepted_len.data_ptr(),
+                                     out_tokens.data_ptr(),
+                                     out_path.data_ptr() if out_path is not None else None,
+                                     ws.data_ptr(), wsb, _stream(dev))
+    _check(st, "spec_verify_tree_greedy")
+    return accepted_len, out_tokens, out_path
+
+
+def spec_verify_row_stats(logits: torch.Tensor, temperature: float = 1.0, *, workspace=None):
+    """Test hook: (m, lse) per row of [B, rows, V] logits, fp32 [B, rows] each."""
+    lib = load_library()
+    sb, sr = _logits3(logits, "logits")
+    B, R, V = logits.shape
+    dt = _dtype_code(logits)
+    dev = logits.device
+    m = torch.empty((B, R), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, R), dtype=torch.float32, device=dev)
+    ws, wsb = _workspace(MODE_ROW_STATS, B, R, V, dt, dev, workspace)
+    st = lib.spec_verify_row_stats(logits.data_ptr(), sb, sr, dt, B, R, V, float(temperature),
+                                   m.data_ptr(), lse.data_ptr(), ws.data_ptr(), wsb, _stream(dev))
+    _check(st, "spec_verify_row_stats")
+    return m, lse
+
+
+def spec_verify_uniforms(seed: int, offset: int, B: int, positions: int, purpose: int,
+                         device="cuda") -> torch.Tensor:
+    """Test hook: the sampler's uniforms u(b, i, purpose) as a [B, positions] fp32 tensor."""
+    lib = load_library()
+    out = torch.empty((B, positions), dtype=torch.float32, device=device)
+    st = lib.spec_verify_uniforms(int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), B, positions,
+                                  purpose, out.data_ptr(), _stream(out.device))
+    _check(st, "spec_verify_uniforms")
+    return out
+
+
+def set_stage_events(events) -> None:
+    """Record the given torch.cuda.Event objects around the kernels of later calls made by
+    this thread (see spec_verify_set_stage_events); None turns it off."""
+    lib = load_library()
+    if not events:
+        _check(lib.spec_verify_set_stage_events(None, 0), "spec_verify_set_stage_events")
+        return
+    for e in events:
+        if e.cuda_event == 0:
+            e.record()  # torch creates the underlying event lazily
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(lib.spec_verify_set_stage_events(arr, len(events)), "spec_verify_set_stage_events")

@@ -1,0 +1,276 @@
+// sv_api.cu -- the C ABI of libspecverify: argument checks, workspace layout and the
+// launch sequence of each entry point.  Every check happens before the first launch, so
+// an error return means nothing was enqueued.
+#include <cmath>
+#include <cstdint>
+
+#include "spec_verify.h"
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace {
+
+using sv::Logits;
+
+constexpr int64_t kMaxGrid = 0x7FFFFFFF;
+
+bool dtype_ok(sv_dtype d) { return d == SV_FP32 || d == SV_BF16; }
+int elem_bytes(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
+int chunk_elems(sv_dtype d) { return d == SV_BF16 ? sv::chunk_elems<sv::BF16>() : sv::chunk_elems<sv::F32>(); }
+int nchunk_of(int V, sv_dtype d) { return int((int64_t(V) + chunk_elems(d) - 1) / chunk_elems(d)); }
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// 16-byte vector loads are legal when the base and both strides keep every row aligned.
+bool vec_ok(const void *p, int64_t sb, int64_t sr, sv_dtype d) {
+    const int64_t e = elem_bytes(d);
+    return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((sb * e) % 16 == 0) && ((sr * e) % 16 == 0);
+}
+
+struct Layout {
+    size_t partial = 0, rowstat = 0, plan = 0, csum = 0, total = 0;
+};
+
+// Workspace regions (each 256-byte aligned):
+//   partial  per (row, chunk): float2 (M, S) for sampling / row stats, int2 (value, index) for
+//            greedy / tree;
+//   rowstat  per row: float2 (M, S)                     (sampling only)
+//   plan     per sequence: int2 (stop row k, mode)      (sampling only)
+//   csum     per (sequence, chunk): residual mass       (sampling only)
+Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
+    Layout L;
+    if (B <= 0 || V <= 0 || rows < 0 || !dtype_ok(dtype)) return L;
+    const size_t nchunk = size_t(nchunk_of(V, dtype));
+    size_t R = 0;
+    switch (mode) {
+    case SV_MODE_SAMPLE: R = size_t(2) * rows + 1; break;
+    case SV_MODE_GREEDY: R = size_t(rows) + 1; break;
+    case SV_MODE_TREE:
+    case SV_MODE_ROW_STATS: R = size_t(rows); break;
+    default: return L;
+    }
+    L.partial = 0;
+    size_t off = up256(size_t(B) * R * nchunk * 8);
+    if (mode == SV_MODE_SAMPLE) {
+        L.rowstat = off;
+        off += up256(size_t(B) * R * 8);
+        L.plan = off;
+        off += up256(size_t(B) * 8);
+        L.csum = off;
+        off += up256(size_t(B) * nchunk * 4);
+    }
+    L.total = off;
+    return L;
+}
+
+sv_status check_workspace(const Layout &L, void *ws, size_t bytes) {
+    if (L.total == 0) return SV_OK;
+    if (ws == nullptr || bytes < L.total || reinterpret_cast<uintptr_t>(ws) % 16 != 0)
+        return SV_ERR_WORKSPACE;
+    return SV_OK;
+}
+
+char *at(void *ws, size_t off) { return static_cast<char *>(ws) + off; }
+
+sv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
+
+bool grid_fits(int B, int64_t R, int nchunk) { return int64_t(B) * R * nchunk <= kMaxGrid; }
+
+// Optional per-thread timing events (spec_verify_set_stage_events).
+constexpr int kMaxStageEvents = 8;
+thread_local cudaEvent_t t_events[kMaxStageEvents];
+thread_local int t_nevents = 0;
+
+// Records event `s` of the calling thread's list, if there is one; stage 0 is "before the
+// first kernel".
+cudaError_t mark(int s, cudaStream_t stream) {
+    if (s < t_nevents && t_events[s] != nullptr) return cudaEventRecord(t_events[s], stream);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_version(void) { return 100; }
+
+const char *spec_verify_status_string(sv_status s) {
+    switch (s) {
+    case SV_OK: return "ok";
+    case SV_ERR_INVALID_ARG: return "invalid argument";
+    case SV_ERR_UNSUPPORTED: return "unsupported dtype or mode";
+    case SV_ERR_CUDA: return "CUDA launch failed";
+    case SV_ERR_TIMEOUT: return "a bounded device wait gave up";
+    case SV_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    }
+    return "unknown status";
+}
+
+size_t spec_verify_workspace_size(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
+    return layout(mode, B, rows, V, dtype).total;
+}
+
+sv_status spec_verify_sample(const void *target_logits, int64_t t_batch_stride,
+                             int64_t t_row_stride, const void *draft_logits,
+                             int64_t d_batch_stride, int64_t d_row_stride, sv_dtype dtype, int B,
+                             int gamma, int V, const int32_t *draft_tokens, float temperature,
+                             uint64_t seed, uint64_t offset, int32_t *accepted_len,
+                             int32_t *out_tokens, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+    if (!dtype_ok(dtype)) return SV_ERR_UNSUPPORTED;
+    if (B < 0 || gamma < 0 || gamma > SV_MAX_GAMMA || V < 1 || V > SV_MAX_VOCAB)
+        return SV_ERR_INVALID_ARG;
+    if (t_batch_stride < 0 || t_row_stride < 0 || d_batch_stride < 0 || d_row_stride < 0)
+        return SV_ERR_INVALID_ARG;
+    if (!(temperature > 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !accepted_len || !out_tokens) return SV_ERR_INVALID_ARG;
+    if (gamma > 0 && (!draft_logits || !draft_tokens)) return SV_ERR_INVALID_ARG;
+    const int nchunk = nchunk_of(V, dtype);
+    const int R = 2 * gamma + 1;
+    if (!grid_fits(B, R, nchunk)) return SV_ERR_INVALID_ARG;
+    const Layout L = layout(SV_MODE_SAMPLE, B, gamma, V, dtype);
+    if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
+
+    const bool vec = vec_ok(target_logits, t_batch_stride, t_row_stride, dtype) &&
+                     (gamma == 0 || vec_ok(draft_logits, d_batch_stride, d_row_stride, dtype));
+    const Logits t{target_logits, t_batch_stride, t_row_stride};
+    const Logits d{gamma > 0 ? draft_logits : target_logits, d_batch_stride, d_row_stride};
+    const float c = float(1.4426950408889634 / double(temperature));  // log2(e) / T
+    const int dt = dtype == SV_BF16 ? 1 : 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *partial = at(workspace, L.partial), *rowstat = at(workspace, L.rowstat);
+    void *plan = at(workspace, L.plan);
+    float *csum = reinterpret_cast<float *>(at(workspace, L.csum));
+
+    cudaError_t e = mark(0, s);
+    if (e == cudaSuccess)
+        e = sv::launch_stats_partial(dt, vec, t, gamma + 1, d, R, B, V, nchunk, c, partial, s);
+    if (e == cudaSuccess) e = mark(1, s);
+    if (e == cudaSuccess)
+        e = sv::launch_decide(dt, t, d, B, gamma, V, nchunk, c, draft_tokens, seed, offset, partial,
+                              rowstat, plan, accepted_len, out_tokens, s);
+    if (e == cudaSuccess) e = mark(2, s);
+    if (e == cudaSuccess && gamma > 0)
+        e = sv::launch_residual_chunks(dt, vec, t, d, B, gamma, V, nchunk, c, rowstat, plan, csum, s);
+    if (e == cudaSuccess) e = mark(3, s);
+    if (e == cudaSuccess)
+        e = sv::launch_locate(dt, vec, t, d, B, gamma, V, nchunk, c, seed, offset, partial, rowstat,
+                              plan, csum, out_tokens, s);
+    if (e == cudaSuccess) e = mark(4, s);
+    return cuda_status(e);
+}
+
+sv_status spec_verify_greedy(const void *target_logits, int64_t t_batch_stride,
+                             int64_t t_row_stride, sv_dtype dtype, int B, int gamma, int V,
+                             const int32_t *draft_tokens, int32_t *accepted_len,
+                             int32_t *out_tokens, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+    if (!dtype_ok(dtype)) return SV_ERR_UNSUPPORTED;
+    if (B < 0 || gamma < 0 || gamma > SV_MAX_GAMMA || V < 1 || V > SV_MAX_VOCAB)
+        return SV_ERR_INVALID_ARG;
+    if (t_batch_stride < 0 || t_row_stride < 0) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !accepted_len || !out_tokens || (gamma > 0 && !draft_tokens))
+        return SV_ERR_INVALID_ARG;
+    const int nchunk = nchunk_of(V, dtype);
+    if (!grid_fits(B, gamma + 1, nchunk)) return SV_ERR_INVALID_ARG;
+    const Layout L = layout(SV_MODE_GREEDY, B, gamma, V, dtype);
+    if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
+    const bool vec = vec_ok(target_logits, t_batch_stride, t_row_stride, dtype);
+    const Logits t{target_logits, t_batch_stride, t_row_stride};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *partial = at(workspace, L.partial);
+    cudaError_t e = mark(0, s);
+    if (e == cudaSuccess)
+        e = sv::launch_argmax_partial(dtype == SV_BF16, vec, t, gamma + 1, B, V, nchunk, partial, s);
+    if (e == cudaSuccess) e = mark(1, s);
+    if (e == cudaSuccess)
+        e = sv::launch_greedy_finalize(B, gamma, V, nchunk, partial, draft_tokens, accepted_len,
+                                       out_tokens, s);
+    if (e == cudaSuccess) e = mark(2, s);
+    return cuda_status(e);
+}
+
+sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_stride,
+                                  int64_t t_row_stride, sv_dtype dtype, int B, int N, int V,
+                                  const int32_t *parent, const int32_t *node_tokens,
+                                  int max_depth, int32_t *accepted_len, int32_t *out_tokens,
+                                  int32_t *out_path, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+    if (!dtype_ok(dtype)) return SV_ERR_UNSUPPORTED;
+    if (B < 0 || N < 1 || N > SV_MAX_TREE_NODES || V < 1 || V > SV_MAX_VOCAB)
+        return SV_ERR_INVALID_ARG;
+    if (max_depth < 0 || max_depth >= N || t_batch_stride < 0 || t_row_stride < 0)
+        return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !parent || !node_tokens || !accepted_len || !out_tokens)
+        return SV_ERR_INVALID_ARG;
+    const int nchunk = nchunk_of(V, dtype);
+    if (!grid_fits(B, N, nchunk)) return SV_ERR_INVALID_ARG;
+    const Layout L = layout(SV_MODE_TREE, B, N, V, dtype);
+    if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
+    const bool vec = vec_ok(target_logits, t_batch_stride, t_row_stride, dtype);
+    const Logits t{target_logits, t_batch_stride, t_row_stride};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *partial = at(workspace, L.partial);
+    cudaError_t e = mark(0, s);
+    if (e == cudaSuccess)
+        e = sv::launch_argmax_partial(dtype == SV_BF16, vec, t, N, B, V, nchunk, partial, s);
+    if (e == cudaSuccess) e = mark(1, s);
+    if (e == cudaSuccess)
+        e = sv::launch_tree_finalize(B, N, V, nchunk, partial, parent, node_tokens, max_depth,
+                                     accepted_len, out_tokens, out_path, s);
+    if (e == cudaSuccess) e = mark(2, s);
+    return cuda_status(e);
+}
+
+sv_status spec_verify_row_stats(const void *logits, int64_t batch_stride, int64_t row_stride,
+                                sv_dtype dtype, int B, int rows_per_seq, int V,
+                                float temperature, float *m_out, float *lse_out,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+    if (!dtype_ok(dtype)) return SV_ERR_UNSUPPORTED;
+    if (B < 0 || rows_per_seq < 1 || V < 1 || V > SV_MAX_VOCAB || batch_stride < 0 || row_stride < 0)
+        return SV_ERR_INVALID_ARG;
+    if (!(temperature > 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!logits || !m_out || !lse_out) return SV_ERR_INVALID_ARG;
+    const int nchunk = nchunk_of(V, dtype);
+    if (!grid_fits(B, rows_per_seq, nchunk) || int64_t(B) * rows_per_seq > kMaxGrid)
+        return SV_ERR_INVALID_ARG;
+    const Layout L = layout(SV_MODE_ROW_STATS, B, rows_per_seq, V, dtype);
+    if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
+    const bool vec = vec_ok(logits, batch_stride, row_stride, dtype);
+    const Logits a{logits, batch_stride, row_stride};
+    const float c = float(1.4426950408889634 / double(temperature));
+    const float inv_t = float(1.0 / double(temperature));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *partial = at(workspace, L.partial);
+    cudaError_t e = sv::launch_stats_partial(dtype == SV_BF16, vec, a, rows_per_seq, a, rows_per_seq, B,
+                                             V, nchunk, c, partial, s);
+    if (e == cudaSuccess)
+        e = sv::launch_rowstats_finalize(B * rows_per_seq, nchunk, c, inv_t, partial, m_out, lse_out, s);
+    return cuda_status(e);
+}
+
+sv_status spec_verify_set_stage_events(void *const *events, int n_events) {
+    if (n_events < 0 || n_events > kMaxStageEvents) return SV_ERR_INVALID_ARG;
+    if (events == nullptr || n_events == 0) {
+        t_nevents = 0;
+        return SV_OK;
+    }
+    for (int i = 0; i < n_events; ++i) t_events[i] = static_cast<cudaEvent_t>(events[i]);
+    t_nevents = n_events;
+    return SV_OK;
+}
+
+sv_status spec_verify_uniforms(uint64_t seed, uint64_t offset, int B, int positions, int purpose,
+                               float *out, void *stream) {
+    if (B < 0 || positions < 0 || purpose < 0 || purpose > 1) return SV_ERR_INVALID_ARG;
+    if (int64_t(B) * positions > kMaxGrid) return SV_ERR_INVALID_ARG;
+    if (B == 0 || positions == 0) return SV_OK;
+    if (!out) return SV_ERR_INVALID_ARG;
+    return cuda_status(sv::launch_uniforms(seed, offset, B, positions, purpose, out,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

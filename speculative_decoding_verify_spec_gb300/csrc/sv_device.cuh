@@ -1,0 +1,290 @@
+// sv_device.cuh -- device-side building blocks of libspecverify (sm_103a).
+//
+// Layout of one unit of work ("chunk"): a CTA of kThreads threads covers kChunkVecs
+// 16-byte vectors of one logits row, i.e. 32 KB (16384 bf16 or 8192 fp32 logits).  In the
+// streaming kernels thread t holds vectors t, t + kThreads, ... (coalesced across the
+// warp); in the in-order scan of the sampler thread t holds vectors 8t .. 8t + 7 (a
+// contiguous run, so a per-thread prefix followed by a block scan is in index order).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sv {
+
+constexpr int kThreads = 256;                          // threads per streaming CTA
+constexpr int kVecPerThread = 8;                       // 16-byte vectors per thread
+constexpr int kChunkVecs = kThreads * kVecPerThread;   // vectors per chunk (32 KB)
+constexpr int kWarps = kThreads / 32;
+constexpr int kNoIndex = 0x7FFFFFFF;                   // "no element" in argmax partials
+
+// Element types.  EPV = elements per 16-byte vector; kNegInfWord = a 32-bit word whose
+// elements are all -inf (the fill value of padding lanes).
+struct F32 {
+    static constexpr int EPV = 4;
+    static constexpr int kBytes = 4;
+    static constexpr uint32_t kNegInfWord = 0xFF800000u;
+};
+struct BF16 {
+    static constexpr int EPV = 8;
+    static constexpr int kBytes = 2;
+    static constexpr uint32_t kNegInfWord = 0xFF80FF80u;
+};
+
+template <class D>
+__host__ __device__ constexpr int chunk_elems() { return kChunkVecs * D::EPV; }
+
+// Number of real elements in the chunk that starts at element c0 of a row of V.
+template <class D>
+__device__ __forceinline__ int chunk_len(int V, int64_t c0) {
+    const int64_t rest = int64_t(V) - c0;
+    return rest < chunk_elems<D>() ? int(rest) : chunk_elems<D>();
+}
+
+// ------------------------------------------------------------------------------------
+// Scalar helpers
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ float ex2(float x) {  // MUFU.EX2 (PTX ex2.approx.ftz.f32)
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float max_nan(float a, float b) {  // NaN-propagating max
+    float y;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+    return y;
+}
+
+__device__ __forceinline__ bool is_finite(float x) { return fabsf(x) < __int_as_float(0x7f800000); }
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Element j of a row (any alignment), widened to fp32.
+template <class D>
+__device__ __forceinline__ float load_elem(const char *row, int64_t j);
+template <>
+__device__ __forceinline__ float load_elem<F32>(const char *row, int64_t j) {
+    return __ldg(reinterpret_cast<const float *>(row) + j);
+}
+template <>
+__device__ __forceinline__ float load_elem<BF16>(const char *row, int64_t j) {
+    return __uint_as_float(uint32_t(__ldg(reinterpret_cast<const unsigned short *>(row) + j)) << 16);
+}
+
+// Element e (0 <= e < EPV) of a packed vector, widened to fp32.
+template <class D>
+__device__ __forceinline__ float vec_elem(const uint4 &v, int e);
+template <>
+__device__ __forceinline__ float vec_elem<F32>(const uint4 &v, int e) {
+    const uint32_t w = e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+    return __uint_as_float(w);
+}
+template <>
+__device__ __forceinline__ float vec_elem<BF16>(const uint4 &v, int e) {
+    const uint32_t w = (e >> 1) == 0 ? v.x : (e >> 1) == 1 ? v.y : (e >> 1) == 2 ? v.z : v.w;
+    return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+}
+
+// ------------------------------------------------------------------------------------
+// Loading one 16-byte vector of a chunk.  `e0` is the element offset of the vector inside
+// the chunk, `len` the number of real elements in the chunk.  A whole in-range vector of
+// an aligned row is one 128-bit read-only load; anything else is read element by element
+// and the missing elements are filled with -inf.
+// ------------------------------------------------------------------------------------
+template <class D, bool VEC>
+__device__ __forceinline__ uint4 load_vec(const char *row, int64_t c0, int e0, int len) {
+    if (VEC && e0 + D::EPV <= len)
+        return __ldg(reinterpret_cast<const uint4 *>(row + (c0 + e0) * D::kBytes));
+    uint32_t w[4] = {D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord};
+    if constexpr (D::EPV == 4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (e0 + e < len) w[e] = __float_as_uint(load_elem<F32>(row, c0 + e0 + e));
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (e0 + e < len) {
+                const uint32_t h = __float_as_uint(load_elem<BF16>(row, c0 + e0 + e)) >> 16;
+                w[e >> 1] = (e & 1) ? ((w[e >> 1] & 0x0000FFFFu) | (h << 16))
+                                    : ((w[e >> 1] & 0xFFFF0000u) | h);
+            }
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// NaN-propagating max over a packed vector.
+template <class D>
+__device__ __forceinline__ uint32_t vec_max_word(const uint4 &v);
+template <>
+__device__ __forceinline__ uint32_t vec_max_word<BF16>(const uint4 &v) {
+    // max.NaN.bf16x2 on pairs: 3 ops for 8 elements
+    __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&v.x);
+    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&v.y);
+    __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162 *>(&v.z);
+    __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162 *>(&v.w);
+    __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+    return *reinterpret_cast<uint32_t *>(&m);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t x, uint32_t y) {
+    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&x);
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&y);
+    __nv_bfloat162 m = __hmax2_nan(a, b);
+    return *reinterpret_cast<uint32_t *>(&m);
+}
+
+// Max (NaN-propagating) over a thread's kVecPerThread vectors, as fp32.
+template <class D>
+__device__ __forceinline__ float thread_max(const uint4 (&v)[kVecPerThread]) {
+    if constexpr (D::EPV == 8) {
+        uint32_t m = vec_max_word<BF16>(v[0]);
+#pragma unroll
+        for (int u = 1; u < kVecPerThread; ++u) m = bf16x2_max_nan(m, vec_max_word<BF16>(v[u]));
+        return max_nan(bf16_lo(m), bf16_hi(m));
+    } else {
+        float m = __uint_as_float(v[0].x);
+#pragma unroll
+        for (int u = 0; u < kVecPerThread; ++u) {
+            m = max_nan(m, __uint_as_float(v[u].x));
+            m = max_nan(m, __uint_as_float(v[u].y));
+            m = max_nan(m, __uint_as_float(v[u].z));
+            m = max_nan(m, __uint_as_float(v[u].w));
+        }
+        return m;
+    }
+}
+
+// sum_j 2^(x_j * c - mc) over a thread's vectors (one FFMA2 per pair, one MUFU.EX2 per
+// element, one FADD2 per pair).
+template <class D>
+__device__ __forceinline__ float thread_sumexp(const uint4 (&v)[kVecPerThread], float c, float mc) {
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    const float2 cc = make_float2(c, c), nm = make_float2(-mc, -mc);
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; q += 2) {
+            float2 a, b;
+            if constexpr (D::EPV == 8) {
+                a = make_float2(bf16_lo(w[q]), bf16_hi(w[q]));
+                b = make_float2(bf16_lo(w[q + 1]), bf16_hi(w[q + 1]));
+            } else {
+                a = make_float2(__uint_as_float(w[q]), __uint_as_float(w[q + 1]));
+                b = make_float2(0.f, 0.f);
+            }
+            float2 ya = __ffma2_rn(a, cc, nm);
+            acc0 = __fadd2_rn(acc0, make_float2(ex2(ya.x), ex2(ya.y)));
+            if constexpr (D::EPV == 8) {
+                float2 yb = __ffma2_rn(b, cc, nm);
+                acc1 = __fadd2_rn(acc1, make_float2(ex2(yb.x), ex2(yb.y)));
+            }
+        }
+    }
+    return (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+
+// ------------------------------------------------------------------------------------
+// Softmax statistics in base 2.  A partial (M, S) of a set of logits means
+// S = sum 2^((l - M) c) with M the largest logit; M = NaN or +inf marks bad data,
+// M = -inf an all -inf set (S = 0).
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ float2 merge_stats(float2 a, float2 b, float c) {
+    const float M = max_nan(a.x, b.x);
+    if (!is_finite(M)) return make_float2(M, 0.f);
+    const float S = a.y * ex2((a.x - M) * c) + b.y * ex2((b.x - M) * c);
+    return make_float2(M, S);
+}
+
+// Argmax partial (value, index): larger value wins, equal values go to the lower index;
+// a NaN value marks bad data and absorbs everything.
+__device__ __forceinline__ int2 merge_argmax(int2 a, int2 b) {
+    const float va = __int_as_float(a.x), vb = __int_as_float(b.x);
+    if (va != va) return a;
+    if (vb != vb) return b;
+    if (vb > va || (vb == va && b.y < a.y)) return b;
+    return a;
+}
+
+template <class T, class Op>
+__device__ __forceinline__ T warp_reduce(T v, Op op) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        T w;
+        if constexpr (sizeof(T) == 8) {
+            long long bits = *reinterpret_cast<long long *>(&v);
+            bits = __shfl_xor_sync(0xFFFFFFFFu, bits, o);
+            w = *reinterpret_cast<T *>(&bits);
+        } else {
+            w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        }
+        v = op(v, w);
+    }
+    return v;
+}
+
+// Block-wide reduction; every thread returns the result.  `scratch` holds kWarps values.
+template <class T, class Op>
+__device__ __forceinline__ T block_reduce(T v, Op op, T *scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_reduce(v, op);
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    T r = scratch[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) r = op(r, scratch[w]);
+    return r;
+}
+
+// Inclusive scan of one float per thread across the block (index order = thread order);
+// returns the inclusive prefix; *total receives the block total.  scratch: kWarps floats.
+__device__ __forceinline__ float block_inclusive_scan(float v, float *scratch, float *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float w = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= o) v += w;
+    }
+    __syncthreads();
+    if (lane == 31) scratch[warp] = v;
+    __syncthreads();
+    float before = 0.f, all = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) before += scratch[w];
+        all += scratch[w];
+    }
+    *total = all;
+    return before + v;
+}
+
+// ------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon et al., SC'11): ten rounds; round r uses the key plus r times the
+// Weyl increments (0x9E3779B9, 0xBB67AE85); multipliers 0xD2511F53 and 0xCD9E8D57.
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 ctr, uint2 key) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t a_hi = __umulhi(0xD2511F53u, ctr.x), a_lo = 0xD2511F53u * ctr.x;
+        const uint32_t b_hi = __umulhi(0xCD9E8D57u, ctr.z), b_lo = 0xCD9E8D57u * ctr.z;
+        ctr = make_uint4(b_hi ^ ctr.y ^ key.x, b_lo, a_hi ^ ctr.w ^ key.y, a_lo);
+        key.x += 0x9E3779B9u;
+        key.y += 0xBB67AE85u;
+    }
+    return ctr;
+}
+
+// The verifier's uniform at (sequence b, position i, purpose): word 0 of Philox at counter
+// (4 i + purpose, b, offset lo, offset hi), key (seed lo, seed hi); (w >> 8) * 2^-24.
+__device__ __forceinline__ float uniform01(uint64_t seed, uint64_t offset, uint32_t b, uint32_t i,
+                                           uint32_t purpose) {
+    const uint4 ctr = make_uint4((i << 2) | (purpose & 3u), b, uint32_t(offset), uint32_t(offset >> 32));
+    const uint2 key = make_uint2(uint32_t(seed), uint32_t(seed >> 32));
+    return float(philox4x32_10(ctr, key).x >> 8) * 0x1p-24f;
+}
+
+}  // namespace sv

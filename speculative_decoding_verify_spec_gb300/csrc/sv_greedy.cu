@@ -1,0 +1,225 @@
+// sv_greedy.cu -- greedy and greedy token-tree verification.
+//
+// Method: temperature 0 turns p and q into point masses, so the accept rule becomes
+// "accept while the draft equals the target argmax" and the token at the first mismatch
+// (or after the last draft) is that row's argmax ("7.6 Speculative Decoding: Draft Models,
+// Medusa, EAGLE & Lookahead": "Extending to a chain of gamma draft tokens"; "Medusa, EAGLE
+// and self-speculation": speculative_greedy).  For a token tree, a node is kept when its
+// token is the argmax of its parent's row and its parent is kept; the deepest kept node
+// ends the path and its own row's argmax is the bonus (same page, "Tree Attention" and
+// Exercise 5, verify_tree_greedy).
+//
+// GPU decomposition:
+//   argmax_partial   every (row, 32 KB chunk): NaN-propagating max and its lowest index.
+//   greedy_finalize  one warp per sequence: merge chunks, longest matching prefix.
+//   tree_finalize    one CTA per sequence: merge chunks for all N nodes, validate the
+//                    tree, accepted flags by walking each node's root path, deepest node
+//                    (lowest index on ties), write the path.
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+__device__ __forceinline__ const char *row_ptr(const Logits &L, int bytes, int64_t b, int64_t r) {
+    return static_cast<const char *>(L.ptr) + (b * L.batch_stride + r * L.row_stride) * bytes;
+}
+
+template <class D, bool VEC>
+__global__ void __launch_bounds__(kThreads, 4)
+    argmax_partial_kernel(Logits t, int R, int V, int nchunk, int2 *__restrict__ partial) {
+    __shared__ int2 red[kWarps];
+    const int64_t item = blockIdx.x;
+    const int64_t row = item / nchunk;
+    const int chunk = int(item - row * nchunk);
+    const int64_t seq = row / R;
+    const int local = int(row - seq * R);
+    const char *rp = row_ptr(t, D::kBytes, seq, local);
+    const int64_t c0 = int64_t(chunk) * chunk_elems<D>();
+    const int len = chunk_len<D>(V, c0);
+
+    uint4 v[kVecPerThread];
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u) {
+        const int e0 = (threadIdx.x + u * kThreads) * D::EPV;
+        v[u] = e0 < len ? load_vec<D, VEC>(rp, c0, e0, len)
+                        : make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
+    }
+    const float m = thread_max<D>(v);
+    int idx = kNoIndex;
+    if (m == m) {  // first element equal to the max, in index order (ties to the lowest index)
+#pragma unroll
+        for (int u = 0; u < kVecPerThread; ++u) {
+            const int e0 = (threadIdx.x + u * kThreads) * D::EPV;
+#pragma unroll
+            for (int e = 0; e < D::EPV; ++e)
+                if (idx == kNoIndex && e0 + e < len && vec_elem<D>(v[u], e) == m) idx = int(c0) + e0 + e;
+        }
+    }
+    const int2 r = block_reduce(make_int2(__float_as_int(m), idx),
+                                [](int2 a, int2 b) { return merge_argmax(a, b); }, red);
+    if (threadIdx.x == 0) partial[item] = r;
+}
+
+// Merge the chunk partials of one row, in chunk order; returns (value bits, index).
+__device__ __forceinline__ int2 row_argmax(const int2 *__restrict__ p, int nchunk) {
+    int2 best = p[0];
+    for (int ch = 1; ch < nchunk; ++ch) best = merge_argmax(best, p[ch]);
+    return best;
+}
+
+__global__ void __launch_bounds__(128)
+    greedy_finalize_kernel(int B, int gamma, int V, int nchunk, const int2 *__restrict__ partial,
+                           const int32_t *__restrict__ x, int32_t *__restrict__ accepted_len,
+                           int32_t *__restrict__ out_tokens) {
+    extern __shared__ int s_arg[];  // (gamma + 1) argmaxes per warp
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t seq = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (seq >= B) return;
+    const int R = gamma + 1;
+    int *a = s_arg + warp * R;
+    bool ok = true;
+    for (int i = lane; i < R; i += 32) {
+        const int2 best = row_argmax(partial + (seq * R + i) * nchunk, nchunk);
+        const float v = __int_as_float(best.x);
+        ok &= v == v;
+        a[i] = best.y;
+    }
+    for (int i = lane; i < gamma; i += 32) {
+        const int32_t xi = x[seq * gamma + i];
+        ok &= xi >= 0 && xi < V;
+    }
+    ok = __all_sync(0xFFFFFFFFu, ok);
+    int32_t *out = out_tokens + seq * R;
+    if (!ok) {
+        for (int i = lane; i < R; i += 32) out[i] = -1;
+        if (lane == 0) accepted_len[seq] = -1;
+        return;
+    }
+    __syncwarp();
+    int n = gamma;
+    for (int i0 = 0; i0 < gamma; i0 += 32) {
+        const int i = i0 + lane;
+        const bool miss = i < gamma && x[seq * gamma + i] != a[i];
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, miss);
+        if (m) {
+            n = i0 + __ffs(m) - 1;
+            break;
+        }
+    }
+    for (int i = lane; i < R; i += 32) out[i] = i < n ? x[seq * gamma + i] : (i == n ? a[n] : -1);
+    if (lane == 0) accepted_len[seq] = n;
+}
+
+constexpr int kTreeThreads = 256;
+constexpr int kKeyShift = 11;  // node index < 2^11 (SV_MAX_TREE_NODES = 1024)
+
+__global__ void __launch_bounds__(kTreeThreads)
+    tree_finalize_kernel(int B, int N, int V, int nchunk, const int2 *__restrict__ partial,
+                         const int32_t *__restrict__ parent, const int32_t *__restrict__ node_tokens,
+                         int max_depth, int32_t *__restrict__ accepted_len,
+                         int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_path) {
+    extern __shared__ int s_tree[];  // a[N], par[N], tok[N]
+    __shared__ int red[kWarps];
+    int *a = s_tree, *par = s_tree + N, *tok = s_tree + 2 * N;
+    const int64_t seq = blockIdx.x;
+    const int W = max_depth + 1;
+    int tree_ok = 1, seq_ok = 1;
+    for (int v = threadIdx.x; v < N; v += kTreeThreads) {
+        const int p = parent[v];
+        par[v] = p;
+        tree_ok &= v == 0 ? p == -1 : (p >= 0 && p < v);
+        const int2 best = row_argmax(partial + (seq * N + v) * nchunk, nchunk);
+        const float val = __int_as_float(best.x);
+        seq_ok &= val == val;
+        a[v] = best.y;
+        const int tk = node_tokens[seq * N + v];
+        tok[v] = tk;
+        if (v > 0) seq_ok &= tk >= 0 && tk < V;
+    }
+    tree_ok = __syncthreads_and(tree_ok);
+    seq_ok = __syncthreads_and(seq_ok);
+
+    int best_key = -1, max_d = 0;
+    if (tree_ok) {  // parents precede children, so every walk ends at the root
+        for (int v = threadIdx.x; v < N; v += kTreeThreads) {
+            int d = 0, w = v;
+            bool kept = true;
+            while (w != 0) {
+                const int p = par[w];
+                kept = kept && tok[w] == a[p];
+                w = p;
+                ++d;
+            }
+            max_d = max(max_d, d);
+            if (kept) best_key = max(best_key, (d << kKeyShift) | ((1 << kKeyShift) - 1 - v));
+        }
+    }
+    max_d = block_reduce(max_d, [](int x, int y) { return max(x, y); }, red);
+    best_key = block_reduce(best_key, [](int x, int y) { return max(x, y); }, red);
+    if (threadIdx.x != 0) return;
+
+    int32_t *out = out_tokens + seq * W;
+    int32_t *path = out_path ? out_path + seq * W : nullptr;
+    if (!tree_ok || !seq_ok || max_d > max_depth) {
+        for (int s = 0; s < W; ++s) {
+            out[s] = -1;
+            if (path) path[s] = -1;
+        }
+        accepted_len[seq] = -1;
+        return;
+    }
+    const int d = best_key >> kKeyShift;
+    const int vstar = (1 << kKeyShift) - 1 - (best_key & ((1 << kKeyShift) - 1));
+    for (int s = d + 1; s < W; ++s) {
+        out[s] = -1;
+        if (path) path[s] = -1;
+    }
+    out[d] = a[vstar];  // the bonus: argmax of the deepest kept node's row
+    for (int s = d, w = vstar; s >= 0; --s) {
+        if (path) path[s] = w;
+        if (s >= 1) out[s - 1] = tok[w];
+        w = par[w];
+    }
+    accepted_len[seq] = d;
+}
+
+}  // namespace
+
+cudaError_t launch_argmax_partial(int dtype, bool vec, Logits t, int R, int B, int V, int nchunk,
+                                  void *partial, cudaStream_t s) {
+    const unsigned grid = unsigned(int64_t(B) * R * nchunk);
+    int2 *p = static_cast<int2 *>(partial);
+    if (dtype == 1) {
+        if (vec) argmax_partial_kernel<BF16, true><<<grid, kThreads, 0, s>>>(t, R, V, nchunk, p);
+        else argmax_partial_kernel<BF16, false><<<grid, kThreads, 0, s>>>(t, R, V, nchunk, p);
+    } else {
+        if (vec) argmax_partial_kernel<F32, true><<<grid, kThreads, 0, s>>>(t, R, V, nchunk, p);
+        else argmax_partial_kernel<F32, false><<<grid, kThreads, 0, s>>>(t, R, V, nchunk, p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_greedy_finalize(int B, int gamma, int V, int nchunk, const void *partial,
+                                   const int32_t *x, int32_t *accepted_len, int32_t *out_tokens,
+                                   cudaStream_t s) {
+    const unsigned grid = unsigned((int64_t(B) * 32 + 127) / 128);
+    const size_t smem = size_t(4) * (gamma + 1) * sizeof(int);
+    greedy_finalize_kernel<<<grid, 128, smem, s>>>(B, gamma, V, nchunk,
+                                                   static_cast<const int2 *>(partial), x,
+                                                   accepted_len, out_tokens);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tree_finalize(int B, int N, int V, int nchunk, const void *partial,
+                                 const int32_t *parent, const int32_t *node_tokens, int max_depth,
+                                 int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
+                                 cudaStream_t s) {
+    const size_t smem = size_t(3) * N * sizeof(int);
+    tree_finalize_kernel<<<unsigned(B), kTreeThreads, smem, s>>>(
+        B, N, V, nchunk, static_cast<const int2 *>(partial), parent, node_tokens, max_depth,
+        accepted_len, out_tokens, out_path);
+    return cudaGetLastError();
+}
+
+}  // namespace sv

@@ -1,0 +1,95 @@
+"""Helpers shared by the GPU parity tests: run the oracle (in threads over sequence ranges)
+on the same inputs the CUDA path sees, and compare."""
+from __future__ import annotations
+
+import json
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import torch
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    return oracle.as_oracle_logits(t)
+
+
+def _ranges(B, parts):
+    step = max(1, (B + parts - 1) // parts)
+    return [(s, min(B, s + step)) for s in range(0, B, step)]
+
+
+def oracle_sample(target, draft, tokens, T, seed, offset=0, threads=None):
+    """The oracle over the whole batch, split over threads (each range keeps its global
+    sequence index b0, which keys the uniforms)."""
+    t, d = host(target), host(draft)
+    x = tokens.cpu().numpy().astype(np.int32).reshape(t.shape[0], -1)
+    B = t.shape[0]
+    threads = threads or min(16, os.cpu_count() or 1)
+    orc = oracle.default()
+
+    def run(rg):
+        s, e = rg
+        return orc.verify_sample(t[s:e], d[s:e], x[s:e], T, seed, offset, b0=s)
+
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(run, _ranges(B, threads)))
+    return tuple(np.concatenate([p[i] for p in parts]) for i in range(3))
+
+
+def oracle_greedy(target, tokens, threads=None):
+    t = host(target)
+    B = t.shape[0]
+    x = tokens.cpu().numpy().astype(np.int32).reshape(B, -1)
+    threads = threads or min(16, os.cpu_count() or 1)
+    orc = oracle.default()
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(lambda rg: orc.verify_greedy(t[rg[0]:rg[1]], x[rg[0]:rg[1]]),
+                            _ranges(B, threads)))
+    return tuple(np.concatenate([p[i] for p in parts]) for i in range(2))
+
+
+def oracle_tree(target, parent, tokens, max_depth, threads=None):
+    t = host(target)
+    B = t.shape[0]
+    par = np.asarray(parent.cpu().numpy() if torch.is_tensor(parent) else parent, np.int32)
+    x = tokens.cpu().numpy().astype(np.int32)
+    threads = threads or min(16, os.cpu_count() or 1)
+    orc = oracle.default()
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(lambda rg: orc.verify_tree_greedy(t[rg[0]:rg[1]], par, x[rg[0]:rg[1]],
+                                                              max_depth), _ranges(B, threads)))
+    return tuple(np.concatenate([p[i] for p in parts]) for i in range(4))
+
+
+def compare_sample(acc, out, o_acc, o_out, o_flags, label="", record=None):
+    """Tokens and lengths must agree wherever the oracle raised no flag; returns
+    (n, mismatches, flagged)."""
+    acc = acc.cpu().numpy()
+    out = out.cpu().numpy()
+    same = (acc == o_acc) & (out == o_out).all(1)
+    flagged = o_flags != 0
+    bad = ~same & ~flagged
+    if bad.any():
+        i = int(np.nonzero(bad)[0][0])
+        raise AssertionError(f"{label}: unflagged mismatch at sequence {i}: gpu acc={acc[i]} "
+                             f"out={out[i].tolist()} oracle acc={o_acc[i]} out={o_out[i].tolist()}")
+    n, mism, flg = len(acc), int((~same).sum()), int(flagged.sum())
+    if record is not None:
+        record_rates(label, n, mism, flg, o_flags)
+    return n, mism, flg
+
+
+def record_rates(label, n, mismatches, flagged, flags):
+    """Append the flag / mismatch counts of a parity case to gpurun_out/parity_rates.jsonl."""
+    out_dir = os.path.join(ROOT, "gpurun_out")
+    os.makedirs(out_dir, exist_ok=True)
+    rec = {"case": label, "sequences": n, "mismatches": mismatches, "flagged": flagged,
+           "flag_accept": int(((flags & 1) != 0).sum()), "flag_cdf": int(((flags & 2) != 0).sum()),
+           "flag_residual_small": int(((flags & 4) != 0).sum())}
+    with open(os.path.join(out_dir, "parity_rates.jsonl"), "a") as f:
+        f.write(json.dumps(rec) + "\n")

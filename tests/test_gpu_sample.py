@@ -1,0 +1,220 @@
+"""GPU parity of the sampling path against the oracle, through the C ABI.
+
+Bar: accepted_len and every token equal the oracle's, except on sequences the oracle flags
+(a uniform within 1e-5 of an accept threshold or a CDF boundary, or a near-zero residual);
+per-row max and log-sum-exp within 1e-4 relative (denominator max(|x|, 1)); the uniforms
+bit-identical.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verify_spec_gb300 as sv
+from speculative_decoding_verify_spec_gb300 import workloads as W
+
+from parity_util import compare_sample, host, oracle_sample
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _run(s, label, offset=0):
+    acc, out = sv.spec_verify_sample(s.target, s.draft, s.draft_tokens, s.temperature, s.seed, offset)
+    o = oracle_sample(s.target, s.draft, s.draft_tokens, s.temperature, s.seed, offset)
+    return compare_sample(acc, out, *o, label=label, record=True)
+
+
+def test_uniforms_bit_identical():
+    for seed, off in ((0, 0), (0x5EED + 3, 7), (2**64 - 1, 2**40 + 5)):
+        for purpose in (0, 1):
+            u = sv.spec_verify_uniforms(seed, off, 37, 9, purpose, DEV).cpu().numpy()
+            ref = np.array([[oracle.uniform(seed, off, b, i, purpose) for i in range(9)]
+                            for b in range(37)], np.float64)
+            assert np.array_equal(u.astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("V,dtype,T", [(1, "bf16", 1.0), (7, "fp32", 0.7), (1000, "fp32", 1.0),
+                                       (16384, "bf16", 1.3), (16385, "bf16", 1.0),
+                                       (33001, "bf16", 0.7), (40000, "fp32", 1.0),
+                                       (128256, "bf16", 0.7)])
+def test_row_stats_match(V, dtype, T):
+    g = torch.Generator(device=DEV).manual_seed(V)
+    x = torch.randn((3, 5, V), generator=g, device=DEV) * 3
+    x[0, 1, : V // 2] = float("-inf")
+    x[2, 3, V - 1] += 12.0
+    x = x.to(torch.bfloat16 if dtype == "bf16" else torch.float32)
+    m, lse = sv.spec_verify_row_stats(x, T)
+    om, olse, ovalid = oracle.row_stats(host(x), T)
+    assert ovalid.all()
+    m, lse = m.cpu().double().numpy(), lse.cpu().double().numpy()
+    assert np.max(np.abs(m - om) / np.maximum(np.abs(om), 1)) < 1e-4
+    assert np.max(np.abs(lse - olse) / np.maximum(np.abs(olse), 1)) < 1e-4
+
+
+def test_row_stats_bad_rows_are_nan():
+    x = torch.zeros((1, 4, 20000), device=DEV, dtype=torch.bfloat16)
+    x[0, 0, 17000] = float("nan")
+    x[0, 1, :] = float("-inf")
+    x[0, 2, 3] = float("inf")
+    m, lse = sv.spec_verify_row_stats(x, 1.0)
+    assert torch.isnan(m[0, :3]).all() and torch.isnan(lse[0, :3]).all()
+    assert abs(lse[0, 3].item() - np.log(20000)) < 1e-4
+
+
+SMALL = [
+    # (B, gamma, V, dtype, recipe, T)
+    (64, 4, 1000, "fp32", "normal", 1.0),
+    (48, 1, 7, "fp32", "normal", 0.7),
+    (32, 8, 33001, "bf16", "peaked", 0.7),
+    (32, 5, 32000, "bf16", "zipf", 1.0),
+    (16, 3, 40000, "fp32", "normal", 1.3),
+    (24, 2, 16385, "bf16", "normal", 1.0),
+    (8, 0, 5000, "bf16", "normal", 1.0),
+    (40, 6, 1, "bf16", "normal", 1.0),
+    (20, 12, 2048, "bf16", "peaked", 0.7),
+    (5, 40, 300, "fp32", "normal", 1.0),
+]
+
+
+@pytest.mark.parametrize("B,gamma,V,dtype,recipe,T", SMALL)
+def test_small_cases(B, gamma, V, dtype, recipe, T):
+    s = W.make_sample(B, gamma, V, dtype=dtype, recipe=recipe, temperature=T, seed=B * 31 + V,
+                      verify_seed=V * 7 + gamma, device=DEV, target_std=3.0, noise_std=1.0,
+                      draft_scale=0.8 if recipe == "peaked" else 1.0)
+    _run(s, f"small B={B} g={gamma} V={V} {dtype} {recipe} T={T}")
+
+
+def test_offsets_change_the_draw():
+    s = W.make_sample(64, 4, 3000, dtype="bf16", seed=5, verify_seed=9, device=DEV)
+    _run(s, "offset 0", 0)
+    _run(s, "offset 12345", 12345)
+
+
+def test_unaligned_rows_use_the_elementwise_path():
+    # slicing off the first element misaligns every row: the element-wise path must agree
+    base = W.make_sample(16, 3, 20001, dtype="bf16", seed=77, verify_seed=1, device=DEV)
+    t = torch.empty((16, 4, 20002), dtype=torch.bfloat16, device=DEV)
+    d = torch.empty((16, 3, 20002), dtype=torch.bfloat16, device=DEV)
+    t[..., 1:] = base.target
+    d[..., 1:] = base.draft
+    ts, ds = t[..., 1:], d[..., 1:]
+    assert ts.data_ptr() % 16 != 0
+    acc, out = sv.spec_verify_sample(ts, ds, base.draft_tokens, base.temperature, base.seed)
+    acc2, out2 = sv.spec_verify_sample(base.target, base.draft, base.draft_tokens, base.temperature,
+                                       base.seed)
+    o = oracle_sample(base.target, base.draft, base.draft_tokens, base.temperature, base.seed)
+    compare_sample(acc, out, *o, label="unaligned", record=True)
+    compare_sample(acc2, out2, *o, label="aligned", record=True)
+
+
+def test_strided_and_broadcast_inputs():
+    # target rows taken from a longer [B, L, V] buffer (positions T-1 .. T+gamma-1), and a
+    # draft broadcast over the batch with stride 0
+    B, gamma, V, L = 12, 4, 8192, 9
+    g = torch.Generator(device=DEV).manual_seed(3)
+    full = (torch.randn((B, L, V), generator=g, device=DEV) * 2).to(torch.bfloat16)
+    target = full[:, 3:3 + gamma + 1, :]
+    draft1 = (full[:1, 3:3 + gamma, :].float() + torch.randn((1, gamma, V), generator=g, device=DEV))
+    draft = draft1.to(torch.bfloat16).expand(B, gamma, V)
+    x = torch.randint(0, V, (B, gamma), generator=g, device=DEV, dtype=torch.int32)
+    acc, out = sv.spec_verify_sample(target, draft, x, 1.0, 42)
+    o = oracle.verify_sample(host(target.contiguous()), host(draft.contiguous()), x.cpu().numpy(), 1.0, 42)
+    compare_sample(acc, out, *o, label="strided", record=True)
+
+
+def test_identical_rows_accept_everything():
+    s = W.make_sample(32, 6, 10000, dtype="bf16", seed=8, device=DEV)
+    draft = s.target[:, :6, :].contiguous()
+    acc, out = sv.spec_verify_sample(s.target, draft, s.draft_tokens, 1.0, 3)
+    assert (acc == 6).all()
+    assert torch.equal(out[:, :6], s.draft_tokens)
+
+
+def test_point_masses_reduce_to_greedy():
+    B, gamma, V = 64, 5, 3000
+    g = torch.Generator(device=DEV).manual_seed(11)
+    a = torch.randint(0, V, (B, gamma + 1), generator=g, device=DEV)
+    keep = torch.rand((B, gamma), generator=g, device=DEV) < 0.7
+    x = torch.where(keep, a[:, :gamma], torch.randint(0, V, (B, gamma), generator=g, device=DEV))
+    t = torch.full((B, gamma + 1, V), float("-inf"), device=DEV)
+    d = torch.full((B, gamma, V), float("-inf"), device=DEV)
+    t.scatter_(2, a.unsqueeze(-1), 0.5)
+    d.scatter_(2, x.unsqueeze(-1), -0.25)
+    x = x.to(torch.int32)
+    acc_s, out_s = sv.spec_verify_sample(t.bfloat16(), d.bfloat16(), x, 1.0, 5)
+    acc_g, out_g = sv.spec_verify_greedy(t.bfloat16(), x)
+    assert torch.equal(acc_s, acc_g) and torch.equal(out_s, out_g)
+
+
+def test_bad_sequences_are_reported_per_sequence():
+    s = W.make_sample(8, 3, 5000, dtype="bf16", seed=12, device=DEV)
+    t, d, x = s.target.clone(), s.draft.clone(), s.draft_tokens.clone()
+    t[1, 2, 77] = float("nan")          # NaN in a target row
+    d[2, 0, 5] = float("inf")           # +inf in a draft row
+    t[3, 3, :] = float("-inf")          # bonus row with no finite logit
+    x[4, 1] = 5000                      # draft token out of range
+    x[5, 0] = -1
+    acc, out = sv.spec_verify_sample(t, d, x, s.temperature, s.seed)
+    o_acc, o_out, o_flags = oracle.verify_sample(host(t), host(d), x.cpu().numpy(), s.temperature, s.seed)
+    assert (o_acc[1:6] == -1).all()
+    acc, out = acc.cpu().numpy(), out.cpu().numpy()
+    assert (acc[1:6] == -1).all() and (out[1:6] == -1).all()
+    good = [0, 6, 7]
+    ok = (acc[good] == o_acc[good]) & (out[good] == o_out[good]).all(1)
+    assert (ok | (o_flags[good] != 0)).all()
+
+
+def test_masked_vocabulary():
+    # top-k style masking: most logits -inf in both models; the residual lives on few tokens
+    s = W.make_sample(32, 4, 12000, dtype="bf16", seed=21, verify_seed=4, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(21)
+    mask = torch.rand(s.target.shape, generator=g, device=DEV) < 0.995
+    t = s.target.masked_fill(mask, float("-inf"))
+    d = s.draft.masked_fill(mask[:, :4], float("-inf"))
+    dl = d.float()
+    x = torch.argmax(dl + -torch.log(-torch.log(torch.rand(dl.shape, generator=g, device=DEV)
+                                                      .clamp(1e-20, 1 - 1e-7))), -1).to(torch.int32)
+    acc, out = sv.spec_verify_sample(t, d, x, 1.0, 99)
+    o = oracle.verify_sample(host(t), host(d), x.cpu().numpy(), 1.0, 99)
+    compare_sample(acc, out, *o, label="masked", record=True)
+
+
+def test_residual_fallback_when_rows_coincide_off_the_draft():
+    # the drafted token is masked in both rows and the rows are otherwise identical: the
+    # draft is rejected (p = q = 0 there) and the residual is exactly zero, so the draw
+    # falls back to p
+    B, V = 16, 4096
+    g = torch.Generator(device=DEV).manual_seed(5)
+    t = (torch.randn((B, 2, V), generator=g, device=DEV) * 2).to(torch.bfloat16)
+    x = torch.randint(0, V, (B, 1), generator=g, device=DEV, dtype=torch.int32)
+    t.scatter_(2, x.long().unsqueeze(-1).expand(B, 2, 1), float("-inf"))
+    d = t[:, :1, :].contiguous()
+    acc, out = sv.spec_verify_sample(t, d, x, 1.0, 17)
+    o_acc, o_out, o_flags = oracle.verify_sample(host(t), host(d), x.cpu().numpy(), 1.0, 17)
+    assert (o_acc == 0).all() and ((o_flags & 8) != 0).all()
+    exact = (o_flags & 2) == 0   # the fallback draw itself may sit on a CDF boundary
+    assert np.array_equal(acc.cpu().numpy(), o_acc)
+    assert np.array_equal(out.cpu().numpy()[exact], o_out[exact])
+
+
+@pytest.mark.parametrize("name", ["sample_b1", "sample_b64", "sample_b256"])
+def test_full_size_workloads(name):
+    s = W.make(name, device=DEV)
+    _run(s, f"full {name}")
+    del s
+    torch.cuda.empty_cache()
+
+
+def test_many_rounds_b1():
+    # the B=1 workload over many seeds: flag and mismatch counts accumulate in the record
+    s = W.make("sample_b1", device=DEV)
+    n = mism = flg = 0
+    for seed in range(400):
+        acc, out = sv.spec_verify_sample(s.target, s.draft, s.draft_tokens, s.temperature, seed)
+        o = oracle.verify_sample(host(s.target), host(s.draft), s.draft_tokens.cpu().numpy(),
+                                 s.temperature, seed)
+        a, b, c = compare_sample(acc, out, *o, label="b1 seeds")
+        n, mism, flg = n + a, mism + b, flg + c
+    from parity_util import record_rates
+    record_rates("sample_b1 x400 seeds", n, mism, flg, np.zeros(0, np.int32))
