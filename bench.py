@@ -51,6 +51,8 @@ def parse_args():
     p.add_argument("--no-modes", action="store_true", help="skip the greedy / tree workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=30)
+    p.add_argument("--batch", type=int, default=None,
+                   help="override the workload's batch size (small profiling cases)")
     return p.parse_args()
 
 
@@ -184,22 +186,23 @@ def committed_traffic(kernel: str, workload: str):
 # ----------------------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------------------
-def kernel_bytes(name: str) -> int:
+def kernel_bytes(name: str, **ov) -> int:
     """Algorithmic bytes of the dominant kernel per launch: every logit it streams, once."""
     from speculative_decoding_verify_spec_gb300 import workloads as W
     cfg = W.WORKLOADS[name]
     s = 2 if cfg["dtype"] == "bf16" else 4
-    return W.rows(name) * cfg["V"] * s
+    return W.rows(name, **ov) * cfg["V"] * s
 
 
-def make_call(name, inputs, dev):
+def make_call(name, inputs, dev, **ov):
     """A closure that runs one verify call of the workload into preallocated outputs."""
     import torch
     import speculative_decoding_verify_spec_gb300 as sv
     from speculative_decoding_verify_spec_gb300 import binding
     from speculative_decoding_verify_spec_gb300 import workloads as W
 
-    cfg = W.WORKLOADS[name]
+    cfg = dict(W.WORKLOADS[name])
+    cfg.update(ov)
     mode = cfg["mode"]
     B, V = cfg["B"], cfg["V"]
     dt = binding.BF16 if cfg["dtype"] == "bf16" else binding.FP32
@@ -241,15 +244,17 @@ def make_call(name, inputs, dev):
     return call, (acc, out, path)
 
 
-def measure(name, steps, warmup, rank, world, dev, peak, peak_kind):
+def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
     import torch
     from speculative_decoding_verify_spec_gb300 import binding
     from speculative_decoding_verify_spec_gb300 import workloads as W
 
-    cfg = W.WORKLOADS[name]
+    cfg = dict(W.WORKLOADS[name])
+    ov = {} if batch is None else {"B": batch}
+    cfg.update(ov)
     mode = cfg["mode"]
-    inputs = W.make(name, device=dev, input_seed=cfg["input_seed"] + 7919 * rank)
-    call, outs = make_call(name, inputs, dev)
+    inputs = W.make(name, device=dev, input_seed=cfg["input_seed"] + 7919 * rank, **ov)
+    call, outs = make_call(name, inputs, dev, **ov)
     nst = len(STAGES[mode])
     if mode == "sample" and cfg["gamma"] == 0:
         nst = 4
@@ -279,15 +284,15 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind):
     ms_step = ms_max / steps
     B = cfg["B"]
     value = world * B / (ms_step / 1e3)
-    logical = W.logical_bytes(name)
-    kb = kernel_bytes(name)
+    logical = W.logical_bytes(name, **ov)
+    kb = kernel_bytes(name, **ov)
     dom_ms = stage_ms[0]
     achieved = kb / (dom_ms / 1e3) / 1e9
     kernel = DOMINANT_KERNEL[mode]
     acc = outs[0].float()
     res = {
         "workload": W.DESCRIPTIONS[name], "value": value, "unit": UNIT, "ms_per_step": ms_step,
-        "steps": steps, "rows_per_s": world * W.rows(name) / (ms_step / 1e3),
+        "steps": steps, "rows_per_s": world * W.rows(name, **ov) / (ms_step / 1e3),
         "hbm_gbs_step": logical / (ms_step / 1e3) / 1e9,
         "frac_of_8tbs_step": logical / (ms_step / 1e3) / 8e12,
         "stages_ms": dict(zip(STAGES[mode], stage_ms)),
@@ -301,13 +306,14 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind):
     return res, inputs, call
 
 
-def measure_e2e(name, inputs, steps, dev):
+def measure_e2e(name, inputs, steps, dev, **ov):
     """The same metric through the public call with host buffers: every step copies its
     inputs from pinned host memory and reads the results back."""
     import torch
     from speculative_decoding_verify_spec_gb300 import workloads as W
 
-    cfg = W.WORKLOADS[name]
+    cfg = dict(W.WORKLOADS[name])
+    cfg.update(ov)
     mode = cfg["mode"]
     host_in = {}
     dev_in = {}
@@ -317,7 +323,7 @@ def measure_e2e(name, inputs, steps, dev):
         t = getattr(inputs, k)
         host_in[k] = t.cpu().pin_memory()
         dev_in[k] = torch.empty_like(t)
-    call, outs = make_call(name, inputs, dev)
+    call, outs = make_call(name, inputs, dev, **ov)
     host_out = [o.cpu().pin_memory() for o in outs]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out)
@@ -402,26 +408,30 @@ def run_ours(args):
     peak, peak_kind = hbm_peak()
     clocks = ClockSampler(local)
     clocks.start()
-    main, inputs, _ = measure(args.workload, args.steps, args.warmup, rank, world, dev, peak, peak_kind)
+    ov = {} if args.batch is None else {"B": args.batch}
+    main, inputs, _ = measure(args.workload, args.steps, args.warmup, rank, world, dev, peak,
+                              peak_kind, args.batch)
     clk = clocks.stop()
     modes = {}
     if not args.no_modes:
         for name in SECONDARY:
             if name == args.workload:
                 continue
-            r, inp, _ = measure(name, args.steps, args.warmup, rank, world, dev, peak, peak_kind)
+            r, inp, _ = measure(name, args.steps, args.warmup, rank, world, dev, peak, peak_kind,
+                                args.batch)
             modes[name] = r
             del inp
             torch.cuda.empty_cache()
-    e2e = measure_e2e(args.workload, inputs, max(3, args.e2e_steps), dev)
+    e2e = measure_e2e(args.workload, inputs, max(3, args.e2e_steps), dev, **ov)
     e2e_val = max_over_ranks(e2e["ms_per_step"], world, dev)
-    e2e["value"] = world * W.WORKLOADS[args.workload]["B"] / (e2e_val / 1e3)
+    e2e["value"] = world * ov.get("B", W.WORKLOADS[args.workload]["B"]) / (e2e_val / 1e3)
     e2e["ms_per_step"] = e2e_val
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload, inputs)
     if rank == 0:
-        cfg = W.WORKLOADS[args.workload]
+        cfg = dict(W.WORKLOADS[args.workload])
+        cfg.update(ov)
         line = {
             "metric": METRIC, "value": main["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
@@ -430,7 +440,7 @@ def run_ours(args):
             "config": {"workload": W.DESCRIPTIONS[args.workload], "B": cfg["B"],
                        "gamma": cfg.get("gamma"), "V": cfg["V"], "logits": cfg["dtype"],
                        "temperature": cfg.get("temperature"),
-                       "l2": f"inputs larger than L2 ({W.logical_bytes(args.workload) / 1e9:.2f} GB "
+                       "l2": f"inputs larger than L2 ({W.logical_bytes(args.workload, **ov) / 1e9:.2f} GB "
                              "read per step), no flush",
                        "parallelism": f"replicas x{world} (independent batches per GPU)"},
             "rows_per_s": main["rows_per_s"], "hbm_gbs": main["hbm_gbs_step"],

@@ -55,7 +55,7 @@ def _bind(lib):
     lib.oracle_row_stats.argtypes = [P, i64, i64, i32, i32, i32, i32, dbl, P, P, P]
     lib.oracle_row_stats.restype = i32
     lib.oracle_verify_sample.argtypes = [P, i64, i64, P, i64, i64, i32, i32, i32, i32, i32,
-                                         P, dbl, u64, u64, P, P, P]
+                                         P, dbl, u64, u64, P, P, P, P]
     lib.oracle_verify_sample.restype = i32
     lib.oracle_exact_probs.argtypes = [P, P, i32, i32, P, dbl, P]
     lib.oracle_exact_probs.restype = i32
@@ -145,8 +145,12 @@ class Oracle:
         assert rc == 0
         return m.reshape(B, R), lse.reshape(B, R), valid.reshape(B, R).astype(bool)
 
-    def verify_sample(self, target, draft, draft_tokens, temperature, seed, offset=0, b0=0):
-        """Sampling verification; returns (accepted_len[B], out_tokens[B, gamma+1], flags[B])."""
+    def verify_sample(self, target, draft, draft_tokens, temperature, seed, offset=0, b0=0,
+                      diagnostics=False):
+        """Sampling verification; returns (accepted_len[B], out_tokens[B, gamma+1], flags[B])
+        and, with diagnostics=True, a [B, 4] array per sequence: final-draw kind (0 bonus,
+        1 residual, 2 residual fell back to p, -1 invalid), its mass R, the distance of u'R
+        to the nearer CDF boundary over R, and the smallest |u - p/q| of the accept tests."""
         t, code, tsb, tsr = _logits(target)
         B, G1, V = t.shape
         gamma = G1 - 1
@@ -161,11 +165,13 @@ class Oracle:
         acc = np.zeros(B, np.int32)
         out = np.zeros((B, G1), np.int32)
         flags = np.zeros(B, np.int32)
+        diag = np.zeros((B, 4), np.float64) if diagnostics else None
         rc = self.lib.oracle_verify_sample(_ptr(t), tsb, tsr, dptr, dsb, dsr, code, B, int(b0),
                                            gamma, V, _ptr(x), float(temperature), int(seed),
-                                           int(offset), _ptr(acc), _ptr(out), _ptr(flags))
+                                           int(offset), _ptr(acc), _ptr(out), _ptr(flags),
+                                           _ptr(diag) if diagnostics else None)
         assert rc == 0
-        return acc, out, flags
+        return (acc, out, flags, diag) if diagnostics else (acc, out, flags)
 
     def exact_probs(self, t_logits, d_logits, draft_tokens, temperature) -> np.ndarray:
         """Enumeration mode: P(accepted_len = k, final token = j) as a [gamma+1, V] array."""
@@ -224,8 +230,10 @@ def row_stats(logits, temperature=1.0):
     return _load().row_stats(logits, temperature)
 
 
-def verify_sample(target, draft, draft_tokens, temperature, seed, offset=0, b0=0):
-    return _load().verify_sample(target, draft, draft_tokens, temperature, seed, offset, b0)
+def verify_sample(target, draft, draft_tokens, temperature, seed, offset=0, b0=0,
+                  diagnostics=False):
+    return _load().verify_sample(target, draft, draft_tokens, temperature, seed, offset, b0,
+                                 diagnostics)
 
 
 def exact_probs(t_logits, d_logits, draft_tokens, temperature):

@@ -222,8 +222,8 @@ static double final_weights(const double *p, const double *q, int V, int residua
 }
 
 /* Inverse CDF in index order: the first j with C_j = r_0 + ... + r_j > u * R.
- * Also reports whether u * R lies within CDF_WINDOW * R of C_{j-1} or of C_j.          */
-static int inverse_cdf(const double *r, int V, double R, double u, int *near_boundary)
+ * Also reports the distance from u * R to the nearer of C_{j-1} and C_j, divided by R.  */
+static int inverse_cdf(const double *r, int V, double R, double u, double *margin)
 {
     double target = u * R;
     double C = 0.0;
@@ -234,11 +234,11 @@ static int inverse_cdf(const double *r, int V, double R, double u, int *near_bou
         if (r[j] > 0.0)
             last_positive = j;
         if (C > target) {
-            *near_boundary = (fabs(target - prev) < CDF_WINDOW * R) || (fabs(C - target) < CDF_WINDOW * R);
+            *margin = fmin(fabs(target - prev), fabs(C - target)) / R;
             return j;
         }
     }
-    *near_boundary = 1;
+    *margin = 0.0;
     return last_positive;
 }
 
@@ -253,7 +253,7 @@ int oracle_verify_sample(const void *target, int64_t t_batch_stride, int64_t t_r
                          const void *draft, int64_t d_batch_stride, int64_t d_row_stride,
                          int dtype, int B, int b0, int gamma, int V, const int32_t *draft_tokens,
                          double T, uint64_t seed, uint64_t offset, int32_t *accepted_len,
-                         int32_t *out_tokens, int32_t *flags)
+                         int32_t *out_tokens, int32_t *flags, double *diag)
 {
     size_t rowsz = sizeof(double) * (size_t)V;
     double *l = (double *)malloc(rowsz);
@@ -273,6 +273,12 @@ int oracle_verify_sample(const void *target, int64_t t_batch_stride, int64_t t_r
             out[i] = -1;
         accepted_len[b] = -1;
         flags[b] = 0;
+        if (diag) {
+            diag[4 * b + 0] = -1.0; /* final draw: 0 bonus, 1 residual, 2 residual fell back to p */
+            diag[4 * b + 1] = 0.0;  /* mass R of the final draw's weights */
+            diag[4 * b + 2] = 0.0;  /* distance of u'R to the nearer CDF boundary, over R */
+            diag[4 * b + 3] = INFINITY; /* smallest |u - p/q| over the accept tests performed */
+        }
 
         /* every row is turned into a distribution first: p_i = softmax(t_i / T),
          * q_i = softmax(d_i / T) -- the temperature applies to BOTH models */
@@ -300,6 +306,8 @@ int oracle_verify_sample(const void *target, int64_t t_batch_stride, int64_t t_r
             double u = oracle_uniform(seed, offset, (uint32_t)(b0 + b), (uint32_t)i, 0u);
             if (qx > 0.0 && fabs(u - px / qx) < ACCEPT_WINDOW)
                 flags[b] |= FLAG_ACCEPT_NEAR_THRESHOLD;
+            if (diag && qx > 0.0 && fabs(u - px / qx) < diag[4 * b + 3])
+                diag[4 * b + 3] = fabs(u - px / qx);
             if (u * qx < px) {
                 out[i] = x; /* accepted */
             } else {
@@ -310,7 +318,8 @@ int oracle_verify_sample(const void *target, int64_t t_batch_stride, int64_t t_r
         }
 
         /* the final token: residual after a rejection, the bonus from p after a full accept */
-        int fell_back = 0, near = 0;
+        int fell_back = 0;
+        double margin = 0.0;
         double R = final_weights(p + (size_t)k * V, residual ? q + (size_t)k * V : NULL, V,
                                  residual, r, &fell_back);
         if (residual) {
@@ -325,10 +334,15 @@ int oracle_verify_sample(const void *target, int64_t t_batch_stride, int64_t t_r
         if (fell_back)
             flags[b] |= FLAG_RESIDUAL_FALLBACK;
         double u2 = oracle_uniform(seed, offset, (uint32_t)(b0 + b), (uint32_t)k, 1u);
-        out[k] = inverse_cdf(r, V, R, u2, &near);
-        if (near)
+        out[k] = inverse_cdf(r, V, R, u2, &margin);
+        if (margin < CDF_WINDOW)
             flags[b] |= FLAG_CDF_NEAR_BOUNDARY;
         accepted_len[b] = k;
+        if (diag) {
+            diag[4 * b + 0] = fell_back ? 2.0 : (residual ? 1.0 : 0.0);
+            diag[4 * b + 1] = R;
+            diag[4 * b + 2] = margin;
+        }
     }
     free(l);
     free(p);

@@ -157,12 +157,14 @@ __device__ __forceinline__ float thread_max(const uint4 (&v)[kVecPerThread]) {
     }
 }
 
-// sum_j 2^(x_j * c - mc) over a thread's vectors (one FFMA2 per pair, one MUFU.EX2 per
-// element, one FADD2 per pair).
+// sum_j 2^((x_j - m) c) over a thread's vectors.  x_j - m is exact for bf16 inputs (and
+// within half an ulp for fp32), so each exponent carries a single rounding proportional to
+// its own size -- the elements near the maximum, which carry the mass, are the most
+// accurate.  Per pair of elements: one FADD2, one FMUL2, two MUFU.EX2, one FADD2.
 template <class D>
-__device__ __forceinline__ float thread_sumexp(const uint4 (&v)[kVecPerThread], float c, float mc) {
+__device__ __forceinline__ float thread_sumexp(const uint4 (&v)[kVecPerThread], float c, float m) {
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-    const float2 cc = make_float2(c, c), nm = make_float2(-mc, -mc);
+    const float2 cc = make_float2(c, c), nm = make_float2(-m, -m);
 #pragma unroll
     for (int u = 0; u < kVecPerThread; ++u) {
         const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
@@ -176,10 +178,10 @@ __device__ __forceinline__ float thread_sumexp(const uint4 (&v)[kVecPerThread], 
                 a = make_float2(__uint_as_float(w[q]), __uint_as_float(w[q + 1]));
                 b = make_float2(0.f, 0.f);
             }
-            float2 ya = __ffma2_rn(a, cc, nm);
+            const float2 ya = __fmul2_rn(__fadd2_rn(a, nm), cc);
             acc0 = __fadd2_rn(acc0, make_float2(ex2(ya.x), ex2(ya.y)));
             if constexpr (D::EPV == 8) {
-                float2 yb = __ffma2_rn(b, cc, nm);
+                const float2 yb = __fmul2_rn(__fadd2_rn(b, nm), cc);
                 acc1 = __fadd2_rn(acc1, make_float2(ex2(yb.x), ex2(yb.y)));
             }
         }

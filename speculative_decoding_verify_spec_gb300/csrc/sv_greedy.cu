@@ -28,7 +28,8 @@ __device__ __forceinline__ const char *row_ptr(const Logits &L, int bytes, int64
 template <class D, bool VEC>
 __global__ void __launch_bounds__(kThreads, 4)
     argmax_partial_kernel(Logits t, int R, int V, int nchunk, int2 *__restrict__ partial) {
-    __shared__ int2 red[kWarps];
+    __shared__ float fred[kWarps];
+    __shared__ int ired[kWarps];
     const int64_t item = blockIdx.x;
     const int64_t row = item / nchunk;
     const int chunk = int(item - row * nchunk);
@@ -45,20 +46,22 @@ __global__ void __launch_bounds__(kThreads, 4)
         v[u] = e0 < len ? load_vec<D, VEC>(rp, c0, e0, len)
                         : make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
     }
+    // the chunk's maximum first (NaN-propagating); only the threads that hold it then look
+    // for its first position, so the index search costs one warp, not the whole CTA
     const float m = thread_max<D>(v);
+    const float bm = block_reduce(m, [](float a, float b) { return max_nan(a, b); }, fred);
     int idx = kNoIndex;
-    if (m == m) {  // first element equal to the max, in index order (ties to the lowest index)
+    if (bm == bm && m == bm) {
 #pragma unroll
         for (int u = 0; u < kVecPerThread; ++u) {
             const int e0 = (threadIdx.x + u * kThreads) * D::EPV;
 #pragma unroll
             for (int e = 0; e < D::EPV; ++e)
-                if (idx == kNoIndex && e0 + e < len && vec_elem<D>(v[u], e) == m) idx = int(c0) + e0 + e;
+                if (idx == kNoIndex && e0 + e < len && vec_elem<D>(v[u], e) == bm) idx = int(c0) + e0 + e;
         }
     }
-    const int2 r = block_reduce(make_int2(__float_as_int(m), idx),
-                                [](int2 a, int2 b) { return merge_argmax(a, b); }, red);
-    if (threadIdx.x == 0) partial[item] = r;
+    idx = block_reduce(idx, [](int a, int b) { return min(a, b); }, ired);
+    if (threadIdx.x == 0) partial[item] = make_int2(__float_as_int(bm), idx);
 }
 
 // Merge the chunk partials of one row, in chunk order; returns (value bits, index).

@@ -32,13 +32,21 @@ __device__ __forceinline__ uint4 neg_inf_vec() {
     return make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
 }
 
-// (p_j - q_j)+ with p_j = 2^(t_j c - M_t c) / S_t and q_j likewise.  Both the chunk-mass
-// kernel and the in-chunk scan call this one function, so the two agree bit for bit.
-__device__ __forceinline__ float residual_weight(float tj, float dj, float c, float nmt, float inv_st,
-                                                 float nmd, float inv_sd) {
-    const float p = ex2(fmaf(tj, c, nmt)) * inv_st;
-    const float q = ex2(fmaf(dj, c, nmd)) * inv_sd;
-    return fmaxf(p - q, 0.f);
+// Unnormalised target weight 2^((t - M) c) = exp((t - M) / T) with a single rounding of
+// the (exact) difference times c.
+__device__ __forceinline__ float weight(float x, float M, float c) {
+    return ex2(__fmul_rn(__fsub_rn(x, M), c));
+}
+
+// (p_j - q_j)+ with p_j = 2^((t_j - M_t) c) / S_t and q_j likewise.  Both the chunk-mass
+// kernel and the in-chunk scan call this one function, so the two agree bit for bit.  The
+// products and the difference are explicitly rounded (no FMA contraction), so rows that
+// are identical give exactly p_j - q_j = 0, as in exact arithmetic.
+__device__ __forceinline__ float residual_weight(float tj, float dj, float c, float mt, float inv_st,
+                                                 float md, float inv_sd) {
+    const float p = __fmul_rn(weight(tj, mt, c), inv_st);
+    const float q = __fmul_rn(weight(dj, md, c), inv_sd);
+    return fmaxf(__fsub_rn(p, q), 0.f);
 }
 
 // ------------------------------------------------------------------------------------
@@ -64,7 +72,7 @@ __global__ void __launch_bounds__(kThreads, 4)
         v[u] = e0 < len ? load_vec<D, VEC>(rp, c0, e0, len) : neg_inf_vec<D>();
     }
     const float m = thread_max<D>(v);
-    const float S = is_finite(m) ? thread_sumexp<D>(v, c, m * c) : 0.f;
+    const float S = is_finite(m) ? thread_sumexp<D>(v, c, m) : 0.f;
     const float2 r = block_reduce(
         make_float2(m, S), [c](float2 x, float2 y) { return merge_stats(x, y, c); }, red);
     if (threadIdx.x == 0) partial[item] = r;
@@ -117,8 +125,8 @@ __global__ void __launch_bounds__(128)
             const float2 sd = rowstat[seq * R + gamma + 1 + i];
             const float tx = load_elem<D>(row_ptr(t, D::kBytes, seq, i), xi);
             const float dx = load_elem<D>(row_ptr(d, D::kBytes, seq, i), xi);
-            const float p = ex2((tx - st.x) * c) / st.y;
-            const float q = ex2((dx - sd.x) * c) / sd.y;
+            const float p = weight(tx, st.x, c) / st.y;
+            const float q = weight(dx, sd.x, c) / sd.y;
             const float u = uniform01(seed, offset, uint32_t(seq), uint32_t(i), 0u);
             reject = !(u * q < p);
         }
@@ -152,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (pl.y != 1) return;  // uniform over the block
     const int k = pl.x, R = 2 * gamma + 1;
     const float2 st = rowstat[seq * R + k], sd = rowstat[seq * R + gamma + 1 + k];
-    const float nmt = -(st.x * c), inv_st = 1.f / st.y, nmd = -(sd.x * c), inv_sd = 1.f / sd.y;
+    const float inv_st = 1.f / st.y, inv_sd = 1.f / sd.y;
     const char *tp = row_ptr(t, D::kBytes, seq, k);
     const char *dp = row_ptr(d, D::kBytes, seq, k);
     const int64_t c0 = int64_t(chunk) * chunk_elems<D>();
@@ -170,8 +178,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int u = 0; u < kVecPerThread; ++u)
 #pragma unroll
         for (int e = 0; e < D::EPV; ++e)
-            acc += residual_weight(vec_elem<D>(tv[u], e), vec_elem<D>(dv[u], e), c, nmt, inv_st, nmd,
-                                   inv_sd);
+            acc += residual_weight(vec_elem<D>(tv[u], e), vec_elem<D>(dv[u], e), c, st.x, inv_st,
+                                   sd.x, inv_sd);
     const float s = block_reduce(acc, [](float a, float b) { return a + b; }, red);
     if (threadIdx.x == 0) csum[item] = s;
 }
@@ -193,14 +201,14 @@ __global__ void __launch_bounds__(kThreads)
     int mode = pl.y;  // 1: residual after a rejection, 0: bonus draw from p
     const float2 st = rowstat[seq * R + k];
     const float2 sd = mode ? rowstat[seq * R + gamma + 1 + k] : make_float2(0.f, 1.f);
-    const float nmt = -(st.x * c), inv_st = 1.f / st.y, nmd = -(sd.x * c), inv_sd = 1.f / sd.y;
+    const float inv_st = 1.f / st.y, inv_sd = 1.f / sd.y;
     const float2 *prow = partial + (seq * R + k) * nchunk;
     const float *crow = csum + seq * nchunk;
-    auto weight = [&](int ch) -> float {
+    auto chunk_mass = [&](int ch) -> float {
         if (ch >= nchunk) return 0.f;
         if (mode) return crow[ch];
         const float2 p = prow[ch];
-        return p.y * ex2((p.x - st.x) * c);  // mass of chunk ch under 2^((l - M) c)
+        return p.y * weight(p.x, st.x, c);  // mass of chunk ch under 2^((l - M) c)
     };
 
     // total mass R (as the deterministic tile-by-tile scan computes it)
@@ -209,7 +217,7 @@ __global__ void __launch_bounds__(kThreads)
         total = 0.f;
         for (int base = 0; base < nchunk; base += kThreads) {
             float tt;
-            block_inclusive_scan(weight(base + threadIdx.x), fsc, &tt);
+            block_inclusive_scan(chunk_mass(base + threadIdx.x), fsc, &tt);
             total += tt;
         }
         if (mode == 1 && !(total > 0.f)) mode = 0;  // exact-zero residual: draw from p
@@ -225,7 +233,7 @@ __global__ void __launch_bounds__(kThreads)
     float last_pos_base = 0.f;
     for (int base = 0; base < nchunk && cstar < 0; base += kThreads) {
         const int ch = base + threadIdx.x;
-        const float w = weight(ch);
+        const float w = chunk_mass(ch);
         float tt;
         const float incl = block_inclusive_scan(w, fsc, &tt);
         const bool hit = ch < nchunk && carry + incl > thr;
@@ -271,8 +279,8 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int e = 0; e < D::EPV; ++e) {
             const float tj = vec_elem<D>(tv, e);
-            const float w = mode ? residual_weight(tj, vec_elem<D>(dv, e), c, nmt, inv_st, nmd, inv_sd)
-                                 : ex2(fmaf(tj, c, nmt));
+            const float w = mode ? residual_weight(tj, vec_elem<D>(dv, e), c, st.x, inv_st, sd.x, inv_sd)
+                                 : weight(tj, st.x, c);
             r[u * D::EPV + e] = w;
             tsum += w;
         }

@@ -23,22 +23,26 @@ def _ranges(B, parts):
     return [(s, min(B, s + step)) for s in range(0, B, step)]
 
 
-def oracle_sample(target, draft, tokens, T, seed, offset=0, threads=None):
+def oracle_sample(target, draft, tokens, T, seed, offset=0, threads=None, diagnostics=False):
     """The oracle over the whole batch, split over threads (each range keeps its global
-    sequence index b0, which keys the uniforms)."""
-    t, d = host(target), host(draft)
-    x = tokens.cpu().numpy().astype(np.int32).reshape(t.shape[0], -1)
+    sequence index b0, which keys the uniforms).  Inputs may be CUDA tensors or the host
+    arrays returned by host() (to convert once for many calls)."""
+    t = target if isinstance(target, np.ndarray) else host(target)
+    d = draft if isinstance(draft, np.ndarray) else host(draft)
+    x = tokens if isinstance(tokens, np.ndarray) else tokens.cpu().numpy()
+    x = x.astype(np.int32).reshape(t.shape[0], -1)
     B = t.shape[0]
     threads = threads or min(16, os.cpu_count() or 1)
     orc = oracle.default()
 
     def run(rg):
         s, e = rg
-        return orc.verify_sample(t[s:e], d[s:e], x[s:e], T, seed, offset, b0=s)
+        return orc.verify_sample(t[s:e], d[s:e], x[s:e], T, seed, offset, b0=s,
+                                 diagnostics=diagnostics)
 
     with ThreadPoolExecutor(threads) as ex:
         parts = list(ex.map(run, _ranges(B, threads)))
-    return tuple(np.concatenate([p[i] for p in parts]) for i in range(3))
+    return tuple(np.concatenate([p[i] for p in parts]) for i in range(4 if diagnostics else 3))
 
 
 def oracle_greedy(target, tokens, threads=None):
@@ -66,9 +70,9 @@ def oracle_tree(target, parent, tokens, max_depth, threads=None):
     return tuple(np.concatenate([p[i] for p in parts]) for i in range(4))
 
 
-def compare_sample(acc, out, o_acc, o_out, o_flags, label="", record=None):
+def compare_sample(acc, out, o_acc, o_out, o_flags, o_diag=None, label="", record=None):
     """Tokens and lengths must agree wherever the oracle raised no flag; returns
-    (n, mismatches, flagged)."""
+    (n, mismatches, flagged, diagnostics of the mismatched sequences)."""
     acc = acc.cpu().numpy()
     out = out.cpu().numpy()
     same = (acc == o_acc) & (out == o_out).all(1)
@@ -76,20 +80,27 @@ def compare_sample(acc, out, o_acc, o_out, o_flags, label="", record=None):
     bad = ~same & ~flagged
     if bad.any():
         i = int(np.nonzero(bad)[0][0])
+        extra = "" if o_diag is None else f" diag={o_diag[i].tolist()}"
         raise AssertionError(f"{label}: unflagged mismatch at sequence {i}: gpu acc={acc[i]} "
-                             f"out={out[i].tolist()} oracle acc={o_acc[i]} out={o_out[i].tolist()}")
+                             f"out={out[i].tolist()} oracle acc={o_acc[i]} out={o_out[i].tolist()}"
+                             + extra)
     n, mism, flg = len(acc), int((~same).sum()), int(flagged.sum())
+    mdiag = [] if o_diag is None else [
+        {"mode": int(o_diag[i, 0]), "R": float(o_diag[i, 1]), "cdf_margin": float(o_diag[i, 2]),
+         "accept_margin": float(o_diag[i, 3]), "acc_equal": bool(acc[i] == o_acc[i])}
+        for i in np.nonzero(~same)[0]]
     if record is not None:
-        record_rates(label, n, mism, flg, o_flags)
-    return n, mism, flg
+        record_rates(label, n, mism, flg, o_flags, mdiag)
+    return n, mism, flg, mdiag
 
 
-def record_rates(label, n, mismatches, flagged, flags):
+def record_rates(label, n, mismatches, flagged, flags, mismatch_diag=()):
     """Append the flag / mismatch counts of a parity case to gpurun_out/parity_rates.jsonl."""
     out_dir = os.path.join(ROOT, "gpurun_out")
     os.makedirs(out_dir, exist_ok=True)
     rec = {"case": label, "sequences": n, "mismatches": mismatches, "flagged": flagged,
            "flag_accept": int(((flags & 1) != 0).sum()), "flag_cdf": int(((flags & 2) != 0).sum()),
-           "flag_residual_small": int(((flags & 4) != 0).sum())}
+           "flag_residual_small": int(((flags & 4) != 0).sum()),
+           "mismatch_diagnostics": list(mismatch_diag)[:50]}
     with open(os.path.join(out_dir, "parity_rates.jsonl"), "a") as f:
         f.write(json.dumps(rec) + "\n")

@@ -21,7 +21,8 @@ DEV = "cuda:0"
 
 def _run(s, label, offset=0):
     acc, out = sv.spec_verify_sample(s.target, s.draft, s.draft_tokens, s.temperature, s.seed, offset)
-    o = oracle_sample(s.target, s.draft, s.draft_tokens, s.temperature, s.seed, offset)
+    o = oracle_sample(s.target, s.draft, s.draft_tokens, s.temperature, s.seed, offset,
+                      diagnostics=True)
     return compare_sample(acc, out, *o, label=label, record=True)
 
 
@@ -210,11 +211,42 @@ def test_many_rounds_b1():
     # the B=1 workload over many seeds: flag and mismatch counts accumulate in the record
     s = W.make("sample_b1", device=DEV)
     n = mism = flg = 0
+    flags = []
     for seed in range(400):
         acc, out = sv.spec_verify_sample(s.target, s.draft, s.draft_tokens, s.temperature, seed)
         o = oracle.verify_sample(host(s.target), host(s.draft), s.draft_tokens.cpu().numpy(),
                                  s.temperature, seed)
-        a, b, c = compare_sample(acc, out, *o, label="b1 seeds")
+        a, b, c, _ = compare_sample(acc, out, *o, label="b1 seeds")
         n, mism, flg = n + a, mism + b, flg + c
+        flags.append(o[2])
     from parity_util import record_rates
-    record_rates("sample_b1 x400 seeds", n, mism, flg, np.zeros(0, np.int32))
+    record_rates("sample_b1 x400 seeds", n, mism, flg, np.concatenate(flags))
+
+
+def test_disagreements_stay_within_the_fp32_error_bound():
+    """Over >= 30k sequences of the B=64 and B=256 workloads (fresh uniforms per round via
+    the offset): every disagreement with the oracle is flagged, and sits within 1e-6 (in
+    units of the draw's mass R) of a CDF boundary or within 1e-6 of an accept threshold --
+    the fp32 kernels' error bound.  Disagreement and flag counts are recorded."""
+    from parity_util import record_rates
+    total = mism = flg = 0
+    for name, rounds in (("sample_b64", 480), ("sample_b256", 24)):
+        s = W.make(name, device=DEV)
+        t, d, x = host(s.target), host(s.draft), s.draft_tokens.cpu().numpy()
+        n_case = m_case = f_case = 0
+        flags, mdiag = [], []
+        for off in range(1, rounds + 1):
+            acc, out = sv.spec_verify_sample(s.target, s.draft, s.draft_tokens, s.temperature,
+                                             s.seed, off)
+            o = oracle_sample(t, d, x, s.temperature, s.seed, off, diagnostics=True)
+            n, m, f, md = compare_sample(acc, out, *o, label=f"{name} offset {off}")
+            n_case, m_case, f_case = n_case + n, m_case + m, f_case + f
+            flags.append(o[2])
+            mdiag += md
+        record_rates(f"{name} x{rounds} rounds", n_case, m_case, f_case, np.concatenate(flags), mdiag)
+        total, mism, flg = total + n_case, mism + m_case, flg + f_case
+        del s
+        torch.cuda.empty_cache()
+        for md in mdiag:
+            assert md["cdf_margin"] < 1e-6 or md["accept_margin"] < 1e-6, md
+    assert total >= 30000

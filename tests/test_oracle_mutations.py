@@ -30,8 +30,8 @@ MUTATIONS = [
      [pins.pin_bruteforce_lossless]),
     ("stop_row_off_by_one", "int k = gamma, residual = 0;", "int k = gamma - 1, residual = 0;",
      [pins.pin_identical_rows_accept_all, pins.pin_round_invariants]),
-    ("cdf_returns_next", "*near_boundary = (fabs(target - prev) < CDF_WINDOW * R) || (fabs(C - target) < CDF_WINDOW * R);\n            return j;",
-     "*near_boundary = 0;\n            return j + 1 < V ? j + 1 : j;", [chi2_quick]),
+    ("cdf_returns_next", "*margin = fmin(fabs(target - prev), fabs(C - target)) / R;\n            return j;",
+     "*margin = 1.0;\n            return j + 1 < V ? j + 1 : j;", [chi2_quick]),
     ("uniform_half_range", "return (double)(w[0] >> 8) * (1.0 / 16777216.0);",
      "return (double)(w[0] >> 9) * (1.0 / 16777216.0);", [pins.pin_uniform_definition, chi2_quick]),
     ("philox_key_not_bumped", "k0 += W0;", "k0 += 0u;", [pins.pin_philox_kat]),
