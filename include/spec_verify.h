@@ -146,6 +146,32 @@ sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_str
                                   void *stream);
 
 /*
+ * Greedy verification that allocates nothing and takes no workspace.  (The pages have no
+ * counterpart: this is a deployment variant of spec_verify_greedy.)
+ *
+ * For callers that cannot hand the library device memory -- code running inside another
+ * runtime's execution step whose framework owns every buffer, or a serving loop that must
+ * not call cudaMalloc once it is running.  Same arguments, rules and results as
+ * spec_verify_greedy, minus the workspace: the per-chunk partials live in a fixed,
+ * 256-byte-aligned device array of SV_NOALLOC_SCRATCH_BYTES that is part of the library and
+ * stays resident on every GPU that loads it until the process exits.
+ *   - Limit: B * (gamma + 1) * ceil(V / chunk) * 8 <= SV_NOALLOC_SCRATCH_BYTES, with chunk =
+ *     16384 logits for bf16 and 8192 for fp32 (4 MiB covers, e.g., B = 512, gamma = 6,
+ *     V = 152064 bf16 with room to spare).  Larger problems return SV_ERR_WORKSPACE before
+ *     anything is enqueued.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - All calls on a device share the array.  Calls whose kernels overlap on the GPU (for
+ *     example on two streams) race on it; the caller must order them.
+ *   - It calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define SV_NOALLOC_SCRATCH_BYTES (4u << 20)
+sv_status spec_verify_greedy_noalloc(const void *target_logits, int64_t t_batch_stride,
+                                     int64_t t_row_stride, sv_dtype dtype, int B, int gamma,
+                                     int V, const int32_t *draft_tokens, int32_t *accepted_len,
+                                     int32_t *out_tokens, void *stream);
+
+/*
  * Test hook: the per-row statistics of the sampling path [SD apply_temperature].
  *   logits [B][rows_per_seq][V].  m_out[b*rows_per_seq + r] = max_j l_j / T,
  *   lse_out[...] = m + ln sum_j exp(l_j / T - m); both NaN for a row with a NaN, a +inf or

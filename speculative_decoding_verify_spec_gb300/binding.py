@@ -59,6 +59,8 @@ def load_library() -> ctypes.CDLL:
         lib.spec_verify_row_stats.restype = i32
         lib.spec_verify_uniforms.argtypes = [u64, u64, i32, i32, i32, P, P]
         lib.spec_verify_uniforms.restype = i32
+        lib.spec_verify_greedy_noalloc.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, P, P]
+        lib.spec_verify_greedy_noalloc.restype = i32
         lib.spec_verify_set_stage_events.argtypes = [P, i32]
         lib.spec_verify_set_stage_events.restype = i32
         lib.spec_verify_status_string.argtypes = [i32]
@@ -239,3 +241,28 @@ def set_stage_events(events) -> None:
             e.record()  # torch creates the underlying event lazily
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(lib.spec_verify_set_stage_events(arr, len(events)), "spec_verify_set_stage_events")
+
+
+def spec_verify_greedy_noalloc(target: torch.Tensor, draft_tokens: torch.Tensor, *,
+                               accepted_len=None, out_tokens=None):
+    """Greedy verification without a workspace: for callers that cannot allocate device
+    memory while they run (the library's fixed device scratch holds the partials).  The
+    outputs are allocated here unless passed in; the C call itself allocates nothing.
+    Calls that overlap on the GPU share that scratch and must not run concurrently."""
+    lib = load_library()
+    tsb, tsr = _logits3(target, "target")
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    dt = _dtype_code(target)
+    x = _ints(draft_tokens, "draft_tokens", (B, gamma)) if gamma > 0 else None
+    dev = target.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    st = lib.spec_verify_greedy_noalloc(target.data_ptr(), tsb, tsr, dt, B, gamma, V,
+                                        x.data_ptr() if x is not None else None,
+                                        accepted_len.data_ptr(), out_tokens.data_ptr(),
+                                        _stream(dev))
+    _check(st, "spec_verify_greedy_noalloc")
+    return accepted_len, out_tokens
