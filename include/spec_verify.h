@@ -152,13 +152,13 @@ sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_str
  * For callers that cannot hand the library device memory -- code running inside another
  * runtime's execution step whose framework owns every buffer, or a serving loop that must
  * not call cudaMalloc once it is running.  Same arguments, rules and results as
- * spec_verify_greedy, minus the workspace: the per-chunk partials live in a fixed,
+ * spec_verify_greedy, minus the workspace: the per-tile partials live in a fixed,
  * 256-byte-aligned device array of SV_NOALLOC_SCRATCH_BYTES that is part of the library and
  * stays resident on every GPU that loads it until the process exits.
- *   - Limit: B * (gamma + 1) * ceil(V / chunk) * 8 <= SV_NOALLOC_SCRATCH_BYTES, with chunk =
- *     16384 logits for bf16 and 8192 for fp32 (4 MiB covers, e.g., B = 512, gamma = 6,
- *     V = 152064 bf16 with room to spare).  Larger problems return SV_ERR_WORKSPACE before
- *     anything is enqueued.
+ *   - Limit: B * (gamma + 1) * ceil(V / tile) * 8 <= SV_NOALLOC_SCRATCH_BYTES, with tile =
+ *     2048 logits for bf16 and 1024 for fp32 (4 MiB covers, e.g., B = 512, gamma = 6,
+ *     V = 152064 bf16: 2.2 MB).  Larger problems return SV_ERR_WORKSPACE before anything is
+ *     enqueued.
  *   - The first call on a device looks up the array's device address (once per device,
  *     with that device current); make that first call before any stream capture.
  *   - All calls on a device share the array.  Calls whose kernels overlap on the GPU (for

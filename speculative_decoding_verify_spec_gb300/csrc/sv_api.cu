@@ -16,8 +16,12 @@ constexpr int64_t kMaxGrid = 0x7FFFFFFF;
 
 bool dtype_ok(sv_dtype d) { return d == SV_FP32 || d == SV_BF16; }
 int elem_bytes(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
-int chunk_elems(sv_dtype d) { return d == SV_BF16 ? sv::chunk_elems<sv::BF16>() : sv::chunk_elems<sv::F32>(); }
-int nchunk_of(int V, sv_dtype d) { return int((int64_t(V) + chunk_elems(d) - 1) / chunk_elems(d)); }
+int tile_elems(sv_dtype d) { return d == SV_BF16 ? sv::tile_elems<sv::BF16>() : sv::tile_elems<sv::F32>(); }
+int res_tile_elems(sv_dtype d) {
+    return d == SV_BF16 ? sv::res_tile_elems<sv::BF16>() : sv::res_tile_elems<sv::F32>();
+}
+int ntile_of(int V, sv_dtype d) { return int((int64_t(V) + tile_elems(d) - 1) / tile_elems(d)); }
+int nrt_of(int V, sv_dtype d) { return int((int64_t(V) + res_tile_elems(d) - 1) / res_tile_elems(d)); }
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // 16-byte vector loads are legal when the base and both strides keep every row aligned.
@@ -31,15 +35,15 @@ struct Layout {
 };
 
 // Workspace regions (each 256-byte aligned):
-//   partial  per (row, chunk): float2 (M, S) for sampling / row stats, int2 (value, index) for
-//            greedy / tree;
-//   rowstat  per row: float2 (M, S)                     (sampling only)
-//   plan     per sequence: int2 (stop row k, mode)      (sampling only)
-//   csum     per (sequence, chunk): residual mass       (sampling only)
+//   partial  per (row, 4 KB tile): float2 (M, S) for sampling / row stats, int2 (value,
+//            index) for greedy / tree;
+//   rowstat  per row: float2 (M, S)                             (sampling only)
+//   plan     per sequence: int2 (stop row k, mode)              (sampling only)
+//   csum     per (sequence, 2 KB residual tile): residual mass  (sampling only)
 Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
     Layout L;
     if (B <= 0 || V <= 0 || rows < 0 || !dtype_ok(dtype)) return L;
-    const size_t nchunk = size_t(nchunk_of(V, dtype));
+    const size_t ntile = size_t(ntile_of(V, dtype));
     size_t R = 0;
     switch (mode) {
     case SV_MODE_SAMPLE: R = size_t(2) * rows + 1; break;
@@ -49,14 +53,14 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
     default: return L;
     }
     L.partial = 0;
-    size_t off = up256(size_t(B) * R * nchunk * 8);
+    size_t off = up256(size_t(B) * R * ntile * 8);
     if (mode == SV_MODE_SAMPLE) {
         L.rowstat = off;
         off += up256(size_t(B) * R * 8);
         L.plan = off;
         off += up256(size_t(B) * 8);
         L.csum = off;
-        off += up256(size_t(B) * nchunk * 4);
+        off += up256(size_t(B) * size_t(nrt_of(V, dtype)) * 4);
     }
     L.total = off;
     return L;
@@ -73,7 +77,8 @@ char *at(void *ws, size_t off) { return static_cast<char *>(ws) + off; }
 
 sv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
 
-bool grid_fits(int B, int64_t R, int nchunk) { return int64_t(B) * R * nchunk <= kMaxGrid; }
+// Tile counts (and every partial index) stay below 2^31.
+bool tiles_fit(int B, int64_t R, int ntile) { return int64_t(B) * R * ntile <= kMaxGrid; }
 
 // Optional per-thread timing events (spec_verify_set_stage_events).
 constexpr int kMaxStageEvents = 8;
@@ -125,9 +130,9 @@ sv_status spec_verify_sample(const void *target_logits, int64_t t_batch_stride,
     if (B == 0) return SV_OK;
     if (!target_logits || !accepted_len || !out_tokens) return SV_ERR_INVALID_ARG;
     if (gamma > 0 && (!draft_logits || !draft_tokens)) return SV_ERR_INVALID_ARG;
-    const int nchunk = nchunk_of(V, dtype);
+    const int ntile = ntile_of(V, dtype), nrt = nrt_of(V, dtype);
     const int R = 2 * gamma + 1;
-    if (!grid_fits(B, R, nchunk)) return SV_ERR_INVALID_ARG;
+    if (!tiles_fit(B, R, ntile)) return SV_ERR_INVALID_ARG;
     const Layout L = layout(SV_MODE_SAMPLE, B, gamma, V, dtype);
     if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
 
@@ -144,18 +149,18 @@ sv_status spec_verify_sample(const void *target_logits, int64_t t_batch_stride,
 
     cudaError_t e = mark(0, s);
     if (e == cudaSuccess)
-        e = sv::launch_stats_partial(dt, vec, t, gamma + 1, d, R, B, V, nchunk, c, partial, s);
+        e = sv::launch_stats_tiles(dt, vec, t, gamma + 1, d, R, B, V, ntile, c, partial, s);
     if (e == cudaSuccess) e = mark(1, s);
     if (e == cudaSuccess)
-        e = sv::launch_decide(dt, t, d, B, gamma, V, nchunk, c, draft_tokens, seed, offset, partial,
+        e = sv::launch_decide(dt, t, d, B, gamma, V, ntile, c, draft_tokens, seed, offset, partial,
                               rowstat, plan, accepted_len, out_tokens, s);
     if (e == cudaSuccess) e = mark(2, s);
     if (e == cudaSuccess && gamma > 0)
-        e = sv::launch_residual_chunks(dt, vec, t, d, B, gamma, V, nchunk, c, rowstat, plan, csum, s);
+        e = sv::launch_residual_tiles(dt, vec, t, d, B, gamma, V, nrt, c, rowstat, plan, csum, s);
     if (e == cudaSuccess) e = mark(3, s);
     if (e == cudaSuccess)
-        e = sv::launch_locate(dt, vec, t, d, B, gamma, V, nchunk, c, seed, offset, partial, rowstat,
-                              plan, csum, out_tokens, s);
+        e = sv::launch_draw(dt, vec, t, d, B, gamma, V, ntile, nrt, c, seed, offset, partial, rowstat,
+                            plan, csum, out_tokens, s);
     if (e == cudaSuccess) e = mark(4, s);
     return cuda_status(e);
 }
@@ -172,8 +177,8 @@ sv_status spec_verify_greedy(const void *target_logits, int64_t t_batch_stride,
     if (B == 0) return SV_OK;
     if (!target_logits || !accepted_len || !out_tokens || (gamma > 0 && !draft_tokens))
         return SV_ERR_INVALID_ARG;
-    const int nchunk = nchunk_of(V, dtype);
-    if (!grid_fits(B, gamma + 1, nchunk)) return SV_ERR_INVALID_ARG;
+    const int ntile = ntile_of(V, dtype);
+    if (!tiles_fit(B, gamma + 1, ntile)) return SV_ERR_INVALID_ARG;
     const Layout L = layout(SV_MODE_GREEDY, B, gamma, V, dtype);
     if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
     const bool vec = vec_ok(target_logits, t_batch_stride, t_row_stride, dtype);
@@ -182,10 +187,10 @@ sv_status spec_verify_greedy(const void *target_logits, int64_t t_batch_stride,
     void *partial = at(workspace, L.partial);
     cudaError_t e = mark(0, s);
     if (e == cudaSuccess)
-        e = sv::launch_argmax_partial(dtype == SV_BF16, vec, t, gamma + 1, B, V, nchunk, partial, s);
+        e = sv::launch_argmax_tiles(dtype == SV_BF16, vec, t, gamma + 1, B, V, ntile, partial, s);
     if (e == cudaSuccess) e = mark(1, s);
     if (e == cudaSuccess)
-        e = sv::launch_greedy_finalize(B, gamma, V, nchunk, partial, draft_tokens, accepted_len,
+        e = sv::launch_greedy_finalize(B, gamma, V, ntile, partial, draft_tokens, accepted_len,
                                        out_tokens, s);
     if (e == cudaSuccess) e = mark(2, s);
     return cuda_status(e);
@@ -205,8 +210,8 @@ sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_str
     if (B == 0) return SV_OK;
     if (!target_logits || !parent || !node_tokens || !accepted_len || !out_tokens)
         return SV_ERR_INVALID_ARG;
-    const int nchunk = nchunk_of(V, dtype);
-    if (!grid_fits(B, N, nchunk)) return SV_ERR_INVALID_ARG;
+    const int ntile = ntile_of(V, dtype);
+    if (!tiles_fit(B, N, ntile)) return SV_ERR_INVALID_ARG;
     const Layout L = layout(SV_MODE_TREE, B, N, V, dtype);
     if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
     const bool vec = vec_ok(target_logits, t_batch_stride, t_row_stride, dtype);
@@ -215,10 +220,10 @@ sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_str
     void *partial = at(workspace, L.partial);
     cudaError_t e = mark(0, s);
     if (e == cudaSuccess)
-        e = sv::launch_argmax_partial(dtype == SV_BF16, vec, t, N, B, V, nchunk, partial, s);
+        e = sv::launch_argmax_tiles(dtype == SV_BF16, vec, t, N, B, V, ntile, partial, s);
     if (e == cudaSuccess) e = mark(1, s);
     if (e == cudaSuccess)
-        e = sv::launch_tree_finalize(B, N, V, nchunk, partial, parent, node_tokens, max_depth,
+        e = sv::launch_tree_finalize(B, N, V, ntile, partial, parent, node_tokens, max_depth,
                                      accepted_len, out_tokens, out_path, s);
     if (e == cudaSuccess) e = mark(2, s);
     return cuda_status(e);
@@ -234,8 +239,8 @@ sv_status spec_verify_row_stats(const void *logits, int64_t batch_stride, int64_
     if (!(temperature > 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
     if (B == 0) return SV_OK;
     if (!logits || !m_out || !lse_out) return SV_ERR_INVALID_ARG;
-    const int nchunk = nchunk_of(V, dtype);
-    if (!grid_fits(B, rows_per_seq, nchunk) || int64_t(B) * rows_per_seq > kMaxGrid)
+    const int ntile = ntile_of(V, dtype);
+    if (!tiles_fit(B, rows_per_seq, ntile) || int64_t(B) * rows_per_seq > kMaxGrid)
         return SV_ERR_INVALID_ARG;
     const Layout L = layout(SV_MODE_ROW_STATS, B, rows_per_seq, V, dtype);
     if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
@@ -245,10 +250,10 @@ sv_status spec_verify_row_stats(const void *logits, int64_t batch_stride, int64_
     const float inv_t = float(1.0 / double(temperature));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void *partial = at(workspace, L.partial);
-    cudaError_t e = sv::launch_stats_partial(dtype == SV_BF16, vec, a, rows_per_seq, a, rows_per_seq, B,
-                                             V, nchunk, c, partial, s);
+    cudaError_t e = sv::launch_stats_tiles(dtype == SV_BF16, vec, a, rows_per_seq, a, rows_per_seq, B, V,
+                                           ntile, c, partial, s);
     if (e == cudaSuccess)
-        e = sv::launch_rowstats_finalize(B * rows_per_seq, nchunk, c, inv_t, partial, m_out, lse_out, s);
+        e = sv::launch_rowstats_finalize(B * rows_per_seq, ntile, c, inv_t, partial, m_out, lse_out, s);
     return cuda_status(e);
 }
 

@@ -1,10 +1,14 @@
 // sv_device.cuh -- device-side building blocks of libspecverify (sm_103a).
 //
-// Layout of one unit of work ("chunk"): a CTA of kThreads threads covers kChunkVecs
-// 16-byte vectors of one logits row, i.e. 32 KB (16384 bf16 or 8192 fp32 logits).  In the
-// streaming kernels thread t holds vectors t, t + kThreads, ... (coalesced across the
-// warp); in the in-order scan of the sampler thread t holds vectors 8t .. 8t + 7 (a
-// contiguous run, so a per-thread prefix followed by a block scan is in index order).
+// Unit of streaming work ("tile"): one warp covers kTileVecs 16-byte vectors per lane of
+// one logits row, i.e. 4 KB (2048 bf16 or 1024 fp32 logits); lane l holds vectors
+// l, l + 32, ... so every load instruction of the warp reads 512 contiguous bytes.  The
+// streaming kernels are persistent: a grid of (SMs x resident CTAs) whose warps step through
+// the tiles of all rows, each warp on its own, and write one partial per tile.
+// A residual tile covers kResVecs vectors per lane of the target row and the same span of
+// the draft row (2 KB of each).  In the in-order scan of the sampler lane l holds a
+// contiguous run of vectors instead, so a per-lane prefix followed by a warp scan is in
+// index order.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -13,10 +17,10 @@
 
 namespace sv {
 
-constexpr int kThreads = 256;                          // threads per streaming CTA
-constexpr int kVecPerThread = 8;                       // 16-byte vectors per thread
-constexpr int kChunkVecs = kThreads * kVecPerThread;   // vectors per chunk (32 KB)
+constexpr int kThreads = 256;                          // threads per CTA
 constexpr int kWarps = kThreads / 32;
+constexpr int kTileVecs = 8;                           // 16-byte vectors per lane per tile
+constexpr int kResVecs = 4;                            // ... per residual tile, of each row
 constexpr int kNoIndex = 0x7FFFFFFF;                   // "no element" in argmax partials
 
 // Element types.  EPV = elements per 16-byte vector; kNegInfWord = a 32-bit word whose
@@ -33,13 +37,14 @@ struct BF16 {
 };
 
 template <class D>
-__host__ __device__ constexpr int chunk_elems() { return kChunkVecs * D::EPV; }
-
-// Number of real elements in the chunk that starts at element c0 of a row of V.
+__host__ __device__ constexpr int tile_elems() { return 32 * kTileVecs * D::EPV; }
 template <class D>
-__device__ __forceinline__ int chunk_len(int V, int64_t c0) {
+__host__ __device__ constexpr int res_tile_elems() { return 32 * kResVecs * D::EPV; }
+
+// Number of real elements in the unit of `unit` elements that starts at element c0.
+__device__ __forceinline__ int unit_len(int V, int64_t c0, int unit) {
     const int64_t rest = int64_t(V) - c0;
-    return rest < chunk_elems<D>() ? int(rest) : chunk_elems<D>();
+    return rest < unit ? int(rest) : unit;
 }
 
 // ------------------------------------------------------------------------------------
@@ -89,8 +94,8 @@ __device__ __forceinline__ float vec_elem<BF16>(const uint4 &v, int e) {
 }
 
 // ------------------------------------------------------------------------------------
-// Loading one 16-byte vector of a chunk.  `e0` is the element offset of the vector inside
-// the chunk, `len` the number of real elements in the chunk.  A whole in-range vector of
+// Loading one 16-byte vector of a unit (tile).  `e0` is the element offset of the vector
+// inside the unit that starts at element c0, `len` the number of real elements in it.  A whole in-range vector of
 // an aligned row is one 128-bit read-only load; anything else is read element by element
 // and the missing elements are filled with -inf.
 // ------------------------------------------------------------------------------------
@@ -136,18 +141,18 @@ __device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t x, uint32_t y) {
     return *reinterpret_cast<uint32_t *>(&m);
 }
 
-// Max (NaN-propagating) over a thread's kVecPerThread vectors, as fp32.
-template <class D>
-__device__ __forceinline__ float thread_max(const uint4 (&v)[kVecPerThread]) {
+// Max (NaN-propagating) over a lane's N vectors, as fp32.
+template <class D, int N>
+__device__ __forceinline__ float thread_max(const uint4 (&v)[N]) {
     if constexpr (D::EPV == 8) {
         uint32_t m = vec_max_word<BF16>(v[0]);
 #pragma unroll
-        for (int u = 1; u < kVecPerThread; ++u) m = bf16x2_max_nan(m, vec_max_word<BF16>(v[u]));
+        for (int u = 1; u < N; ++u) m = bf16x2_max_nan(m, vec_max_word<BF16>(v[u]));
         return max_nan(bf16_lo(m), bf16_hi(m));
     } else {
         float m = __uint_as_float(v[0].x);
 #pragma unroll
-        for (int u = 0; u < kVecPerThread; ++u) {
+        for (int u = 0; u < N; ++u) {
             m = max_nan(m, __uint_as_float(v[u].x));
             m = max_nan(m, __uint_as_float(v[u].y));
             m = max_nan(m, __uint_as_float(v[u].z));
@@ -161,12 +166,12 @@ __device__ __forceinline__ float thread_max(const uint4 (&v)[kVecPerThread]) {
 // within half an ulp for fp32), so each exponent carries a single rounding proportional to
 // its own size -- the elements near the maximum, which carry the mass, are the most
 // accurate.  Per pair of elements: one FADD2, one FMUL2, two MUFU.EX2, one FADD2.
-template <class D>
-__device__ __forceinline__ float thread_sumexp(const uint4 (&v)[kVecPerThread], float c, float m) {
+template <class D, int N>
+__device__ __forceinline__ float thread_sumexp(const uint4 (&v)[N], float c, float m) {
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
     const float2 cc = make_float2(c, c), nm = make_float2(-m, -m);
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
+    for (int u = 0; u < N; ++u) {
         const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int q = 0; q < 4; q += 2) {
@@ -242,26 +247,78 @@ __device__ __forceinline__ T block_reduce(T v, Op op, T *scratch) {
     return r;
 }
 
-// Inclusive scan of one float per thread across the block (index order = thread order);
-// returns the inclusive prefix; *total receives the block total.  scratch: kWarps floats.
-__device__ __forceinline__ float block_inclusive_scan(float v, float *scratch, float *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Inclusive scan of one float per lane across the warp (index order = lane order).
+__device__ __forceinline__ float warp_inclusive_scan(float v, int lane) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const float w = __shfl_up_sync(0xFFFFFFFFu, v, o);
         if (lane >= o) v += w;
     }
-    __syncthreads();
-    if (lane == 31) scratch[warp] = v;
-    __syncthreads();
-    float before = 0.f, all = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        if (w < warp) before += scratch[w];
-        all += scratch[w];
+    return v;
+}
+
+// Compensated (Kahan) running sum, for the draw's prefixes: the threshold is compared with
+// running sums of thousands of terms, where plain fp32 accumulation drifts.
+struct Kahan {
+    float sum = 0.f, comp = 0.f;
+    __device__ __forceinline__ void add(float x) {
+        const float y = __fsub_rn(x, comp);
+        const float t = __fadd_rn(sum, y);
+        comp = __fsub_rn(__fsub_rn(t, sum), y);
+        sum = t;
     }
-    *total = all;
-    return before + v;
+    __device__ __forceinline__ float value() const { return __fsub_rn(sum, comp); }
+};
+
+// A warp's walk over the tiles of a persistent kernel: item it = (seq * R + local) * ntile
+// + tile, stepped by the total number of warps without divisions after the first.
+struct TileWalk {
+    int64_t it, seq;
+    int local, tile;
+    int64_t step_seq;
+    int step_local, step_tile;
+    int R, ntile;
+    __device__ TileWalk(int64_t it0, int64_t nwarps, int R_, int ntile_) : it(it0), R(R_), ntile(ntile_) {
+        const int64_t row = it0 / ntile;
+        tile = int(it0 - row * ntile);
+        seq = row / R;
+        local = int(row - seq * R);
+        const int64_t dq = nwarps / ntile;
+        step_tile = int(nwarps - dq * ntile);
+        step_seq = dq / R;
+        step_local = int(dq - step_seq * R);
+    }
+    __device__ void next(int64_t nwarps) {
+        it += nwarps;
+        tile += step_tile;
+        int carry = 0;
+        if (tile >= ntile) {
+            tile -= ntile;
+            carry = 1;
+        }
+        local += step_local + carry;
+        seq += step_seq;
+        if (local >= R) {
+            local -= R;
+            ++seq;
+        }
+    }
+};
+
+// The persistent streaming grid: SMs x resident CTAs of `kernel`, at most enough CTAs to
+// give every warp one of `items` tiles.
+template <class K>
+inline cudaError_t persistent_grid(K kernel, int64_t items, unsigned *grid) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t need = (items + kWarps - 1) / kWarps;
+    const int64_t full = int64_t(sms) * per_sm;
+    *grid = unsigned(need < full ? (need > 0 ? need : 1) : full);
+    return cudaSuccess;
 }
 
 // ------------------------------------------------------------------------------------

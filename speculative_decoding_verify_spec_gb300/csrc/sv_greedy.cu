@@ -10,9 +10,10 @@
 // Exercise 5, verify_tree_greedy).
 //
 // GPU decomposition:
-//   argmax_partial   every (row, 32 KB chunk): NaN-propagating max and its lowest index.
-//   greedy_finalize  one warp per sequence: merge chunks, longest matching prefix.
-//   tree_finalize    one CTA per sequence: merge chunks for all N nodes, validate the
+//   argmax_tiles     persistent: every 4 KB tile of every row, one warp per tile:
+//                    NaN-propagating max and its lowest index.
+//   greedy_finalize  one warp per sequence: merge tiles, longest matching prefix.
+//   tree_finalize    one CTA per sequence: merge tiles for all N nodes, validate the
 //                    tree, accepted flags by walking each node's root path, deepest node
 //                    (lowest index on ties), write the path.
 #include "sv_device.cuh"
@@ -27,52 +28,76 @@ __device__ __forceinline__ const char *row_ptr(const Logits &L, int bytes, int64
 
 template <class D, bool VEC>
 __global__ void __launch_bounds__(kThreads, 4)
-    argmax_partial_kernel(Logits t, int R, int V, int nchunk, int2 *__restrict__ partial) {
-    __shared__ float fred[kWarps];
-    __shared__ int ired[kWarps];
-    const int64_t item = blockIdx.x;
-    const int64_t row = item / nchunk;
-    const int chunk = int(item - row * nchunk);
-    const int64_t seq = row / R;
-    const int local = int(row - seq * R);
-    const char *rp = row_ptr(t, D::kBytes, seq, local);
-    const int64_t c0 = int64_t(chunk) * chunk_elems<D>();
-    const int len = chunk_len<D>(V, c0);
-
-    uint4 v[kVecPerThread];
+    argmax_tiles_kernel(Logits t, int R, int V, int ntile, int64_t items, int2 *__restrict__ partial) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = int64_t(gridDim.x) * kWarps;
+    for (TileWalk w(int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5), nwarps, R, ntile); w.it < items;
+         w.next(nwarps)) {
+        const char *rp = row_ptr(t, D::kBytes, w.seq, w.local);
+        const int64_t c0 = int64_t(w.tile) * tile_elems<D>();
+        const int len = unit_len(V, c0, tile_elems<D>());
+        uint4 v[kTileVecs];
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-        const int e0 = (threadIdx.x + u * kThreads) * D::EPV;
-        v[u] = e0 < len ? load_vec<D, VEC>(rp, c0, e0, len)
-                        : make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
-    }
-    // the chunk's maximum first (NaN-propagating); only the threads that hold it then look
-    // for its first position, so the index search costs one warp, not the whole CTA
-    const float m = thread_max<D>(v);
-    const float bm = block_reduce(m, [](float a, float b) { return max_nan(a, b); }, fred);
-    int idx = kNoIndex;
-    if (bm == bm && m == bm) {
-#pragma unroll
-        for (int u = 0; u < kVecPerThread; ++u) {
-            const int e0 = (threadIdx.x + u * kThreads) * D::EPV;
-#pragma unroll
-            for (int e = 0; e < D::EPV; ++e)
-                if (idx == kNoIndex && e0 + e < len && vec_elem<D>(v[u], e) == bm) idx = int(c0) + e0 + e;
+        for (int u = 0; u < kTileVecs; ++u) {
+            const int e0 = (lane + 32 * u) * D::EPV;
+            v[u] = e0 < len ? load_vec<D, VEC>(rp, c0, e0, len)
+                            : make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
         }
+        // the tile's maximum first (NaN-propagating), then the lowest index holding it,
+        // branch-free in two steps: the first of this lane's vectors whose maximum is the
+        // tile max, then the first element of that vector equal to it (reverse scans with
+        // selects, so the last match written is the lowest index)
+        const float bm = warp_reduce(thread_max<D>(v), [](float a, float b) { return max_nan(a, b); });
+        int idx = kNoIndex;
+        if (bm == bm) {
+            int uhit = -1;
+#pragma unroll
+            for (int u = kTileVecs - 1; u >= 0; --u) {
+                float vm;
+                if constexpr (D::EPV == 8) {
+                    const uint32_t mw = vec_max_word<BF16>(v[u]);
+                    vm = max_nan(bf16_lo(mw), bf16_hi(mw));
+                } else {
+                    vm = max_nan(max_nan(__uint_as_float(v[u].x), __uint_as_float(v[u].y)),
+                                 max_nan(__uint_as_float(v[u].z), __uint_as_float(v[u].w)));
+                }
+                uhit = vm == bm ? u : uhit;
+            }
+            if (uhit >= 0) {
+                uint4 hv = v[0];
+#pragma unroll
+                for (int u = 1; u < kTileVecs; ++u) hv = uhit == u ? v[u] : hv;
+                const int e0 = (lane + 32 * uhit) * D::EPV;
+#pragma unroll
+                for (int e = D::EPV - 1; e >= 0; --e) {
+                    const bool hit = vec_elem<D>(hv, e) == bm && e0 + e < len;
+                    idx = hit ? int(c0) + e0 + e : idx;
+                }
+            }
+        }
+        idx = warp_reduce(idx, [](int a, int b) { return min(a, b); });
+        if (lane == 0) partial[w.it] = make_int2(__float_as_int(bm), idx);
     }
-    idx = block_reduce(idx, [](int a, int b) { return min(a, b); }, ired);
-    if (threadIdx.x == 0) partial[item] = make_int2(__float_as_int(bm), idx);
 }
 
-// Merge the chunk partials of one row, in chunk order; returns (value bits, index).
-__device__ __forceinline__ int2 row_argmax(const int2 *__restrict__ p, int nchunk) {
-    int2 best = p[0];
-    for (int ch = 1; ch < nchunk; ++ch) best = merge_argmax(best, p[ch]);
+// Merge the tile partials of one row, in tile order; returns (value bits, index).  Loads go
+// out kMergeBatch at a time.
+constexpr int kMergeBatch = 16;
+__device__ int2 row_argmax(const int2 *__restrict__ p, int n) {
+    int2 best = make_int2(__float_as_int(-__int_as_float(0x7f800000)), kNoIndex);
+    for (int q0 = 0; q0 < n; q0 += kMergeBatch) {
+        int2 e[kMergeBatch];
+#pragma unroll
+        for (int q = 0; q < kMergeBatch; ++q) e[q] = q0 + q < n ? p[q0 + q] : make_int2(0, 0);
+#pragma unroll
+        for (int q = 0; q < kMergeBatch; ++q)
+            if (q0 + q < n) best = q0 + q == 0 ? e[q] : merge_argmax(best, e[q]);
+    }
     return best;
 }
 
 __global__ void __launch_bounds__(128)
-    greedy_finalize_kernel(int B, int gamma, int V, int nchunk, const int2 *__restrict__ partial,
+    greedy_finalize_kernel(int B, int gamma, int V, int ntile, const int2 *__restrict__ partial,
                            const int32_t *__restrict__ x, int32_t *__restrict__ accepted_len,
                            int32_t *__restrict__ out_tokens) {
     extern __shared__ int s_arg[];  // (gamma + 1) argmaxes per warp
@@ -83,7 +108,7 @@ __global__ void __launch_bounds__(128)
     int *a = s_arg + warp * R;
     bool ok = true;
     for (int i = lane; i < R; i += 32) {
-        const int2 best = row_argmax(partial + (seq * R + i) * nchunk, nchunk);
+        const int2 best = row_argmax(partial + (seq * R + i) * ntile, ntile);
         const float v = __int_as_float(best.x);
         ok &= v == v;
         a[i] = best.y;
@@ -118,7 +143,7 @@ constexpr int kTreeThreads = 256;
 constexpr int kKeyShift = 11;  // node index < 2^11 (SV_MAX_TREE_NODES = 1024)
 
 __global__ void __launch_bounds__(kTreeThreads)
-    tree_finalize_kernel(int B, int N, int V, int nchunk, const int2 *__restrict__ partial,
+    tree_finalize_kernel(int B, int N, int V, int ntile, const int2 *__restrict__ partial,
                          const int32_t *__restrict__ parent, const int32_t *__restrict__ node_tokens,
                          int max_depth, int32_t *__restrict__ accepted_len,
                          int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_path) {
@@ -132,7 +157,7 @@ __global__ void __launch_bounds__(kTreeThreads)
         const int p = parent[v];
         par[v] = p;
         tree_ok &= v == 0 ? p == -1 : (p >= 0 && p < v);
-        const int2 best = row_argmax(partial + (seq * N + v) * nchunk, nchunk);
+        const int2 best = row_argmax(partial + (seq * N + v) * ntile, ntile);
         const float val = __int_as_float(best.x);
         seq_ok &= val == val;
         a[v] = best.y;
@@ -189,38 +214,36 @@ __global__ void __launch_bounds__(kTreeThreads)
 
 }  // namespace
 
-cudaError_t launch_argmax_partial(int dtype, bool vec, Logits t, int R, int B, int V, int nchunk,
-                                  void *partial, cudaStream_t s) {
-    const unsigned grid = unsigned(int64_t(B) * R * nchunk);
-    int2 *p = static_cast<int2 *>(partial);
-    if (dtype == 1) {
-        if (vec) argmax_partial_kernel<BF16, true><<<grid, kThreads, 0, s>>>(t, R, V, nchunk, p);
-        else argmax_partial_kernel<BF16, false><<<grid, kThreads, 0, s>>>(t, R, V, nchunk, p);
-    } else {
-        if (vec) argmax_partial_kernel<F32, true><<<grid, kThreads, 0, s>>>(t, R, V, nchunk, p);
-        else argmax_partial_kernel<F32, false><<<grid, kThreads, 0, s>>>(t, R, V, nchunk, p);
-    }
+cudaError_t launch_argmax_tiles(int dtype, bool vec, Logits t, int R, int B, int V, int ntile,
+                                void *partial, cudaStream_t s) {
+    const int64_t items = int64_t(B) * R * ntile;
+    auto k = dtype == 1 ? (vec ? argmax_tiles_kernel<BF16, true> : argmax_tiles_kernel<BF16, false>)
+                        : (vec ? argmax_tiles_kernel<F32, true> : argmax_tiles_kernel<F32, false>);
+    unsigned grid = 0;
+    cudaError_t e = persistent_grid(k, items, &grid);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kThreads, 0, s>>>(t, R, V, ntile, items, static_cast<int2 *>(partial));
     return cudaGetLastError();
 }
 
-cudaError_t launch_greedy_finalize(int B, int gamma, int V, int nchunk, const void *partial,
+cudaError_t launch_greedy_finalize(int B, int gamma, int V, int ntile, const void *partial,
                                    const int32_t *x, int32_t *accepted_len, int32_t *out_tokens,
                                    cudaStream_t s) {
     const unsigned grid = unsigned((int64_t(B) * 32 + 127) / 128);
     const size_t smem = size_t(4) * (gamma + 1) * sizeof(int);
-    greedy_finalize_kernel<<<grid, 128, smem, s>>>(B, gamma, V, nchunk,
+    greedy_finalize_kernel<<<grid, 128, smem, s>>>(B, gamma, V, ntile,
                                                    static_cast<const int2 *>(partial), x,
                                                    accepted_len, out_tokens);
     return cudaGetLastError();
 }
 
-cudaError_t launch_tree_finalize(int B, int N, int V, int nchunk, const void *partial,
+cudaError_t launch_tree_finalize(int B, int N, int V, int ntile, const void *partial,
                                  const int32_t *parent, const int32_t *node_tokens, int max_depth,
                                  int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
                                  cudaStream_t s) {
     const size_t smem = size_t(3) * N * sizeof(int);
     tree_finalize_kernel<<<unsigned(B), kTreeThreads, smem, s>>>(
-        B, N, V, nchunk, static_cast<const int2 *>(partial), parent, node_tokens, max_depth,
+        B, N, V, ntile, static_cast<const int2 *>(partial), parent, node_tokens, max_depth,
         accepted_len, out_tokens, out_path);
     return cudaGetLastError();
 }

@@ -16,38 +16,38 @@ struct Logits {
 // Sampling path -----------------------------------------------------------------------
 // Row statistics of B sequences of R = rows_a + rows_b rows: local rows [0, rows_a) come
 // from `a`, [rows_a, R) from `b` (row rows_a + i of b is row i of tensor b).  One partial
-// (M, S) per (row, chunk) is written to partial[(seq * R + row) * nchunk + chunk].
-cudaError_t launch_stats_partial(int dtype, bool vec, Logits a, int rows_a, Logits b, int R, int B,
-                                 int V, int nchunk, float c, void *partial, cudaStream_t s);
-// Merge the chunk partials of every row, run the accept scan, write accepted_len, the
+// (M, S) per (row, 4 KB tile) is written to partial[(seq * R + row) * ntile + tile].
+cudaError_t launch_stats_tiles(int dtype, bool vec, Logits a, int rows_a, Logits b, int R, int B, int V,
+                               int ntile, float c, void *partial, cudaStream_t s);
+// Merge the tile partials of every row, run the accept scan, write accepted_len, the
 // accepted drafts and the -1 padding, and the per-sequence plan (k, mode).
-cudaError_t launch_decide(int dtype, Logits t, Logits d, int B, int gamma, int V, int nchunk,
+cudaError_t launch_decide(int dtype, Logits t, Logits d, int B, int gamma, int V, int ntile,
                           float c, const int32_t *x, uint64_t seed, uint64_t offset,
                           const void *partial, void *rowstat, void *plan, int32_t *accepted_len,
                           int32_t *out_tokens, cudaStream_t s);
-// Residual mass sum_j (p_j - q_j)+ of every chunk of the stop row (sequences that rejected).
-cudaError_t launch_residual_chunks(int dtype, bool vec, Logits t, Logits d, int B, int gamma,
-                                   int V, int nchunk, float c, const void *rowstat,
-                                   const void *plan, float *csum, cudaStream_t s);
+// Residual mass sum_j (p_j - q_j)+ of every residual tile of the stop row (sequences that
+// rejected): csum[seq * nrt + tile].
+cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V,
+                                  int nrt, float c, const void *rowstat, const void *plan, float *csum,
+                                  cudaStream_t s);
 // Inverse-CDF draw of the final token on the stop row of every valid sequence.
-cudaError_t launch_locate(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V,
-                          int nchunk, float c, uint64_t seed, uint64_t offset, const void *partial,
-                          const void *rowstat, const void *plan, const float *csum,
-                          int32_t *out_tokens, cudaStream_t s);
+cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
+                        float c, uint64_t seed, uint64_t offset, const void *partial, const void *rowstat,
+                        const void *plan, const float *csum, int32_t *out_tokens, cudaStream_t s);
 // Test hook: (m, lse) per row from the partials.
-cudaError_t launch_rowstats_finalize(int rows, int nchunk, float c, float inv_t, const void *partial,
+cudaError_t launch_rowstats_finalize(int rows, int ntile, float c, float inv_t, const void *partial,
                                      float *m_out, float *lse_out, cudaStream_t s);
 cudaError_t launch_uniforms(uint64_t seed, uint64_t offset, int B, int positions, int purpose,
                             float *out, cudaStream_t s);
 
 // Greedy / tree path ------------------------------------------------------------------
-// Argmax partial (value, lowest index) per (row, chunk) of [B][R][V].
-cudaError_t launch_argmax_partial(int dtype, bool vec, Logits t, int R, int B, int V, int nchunk,
-                                  void *partial, cudaStream_t s);
-cudaError_t launch_greedy_finalize(int B, int gamma, int V, int nchunk, const void *partial,
+// Argmax partial (value, lowest index) per (row, 4 KB tile) of [B][R][V].
+cudaError_t launch_argmax_tiles(int dtype, bool vec, Logits t, int R, int B, int V, int ntile,
+                                void *partial, cudaStream_t s);
+cudaError_t launch_greedy_finalize(int B, int gamma, int V, int ntile, const void *partial,
                                    const int32_t *x, int32_t *accepted_len, int32_t *out_tokens,
                                    cudaStream_t s);
-cudaError_t launch_tree_finalize(int B, int N, int V, int nchunk, const void *partial,
+cudaError_t launch_tree_finalize(int B, int N, int V, int ntile, const void *partial,
                                  const int32_t *parent, const int32_t *node_tokens, int max_depth,
                                  int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
                                  cudaStream_t s);

@@ -1,6 +1,6 @@
 // sv_noalloc.cu -- greedy verification for callers that cannot allocate device memory.
 //
-// spec_verify_greedy needs a caller-provided workspace for its per-chunk argmax partials.
+// spec_verify_greedy needs a caller-provided workspace for its per-tile argmax partials.
 // Some callers have no way to provide one: code that runs inside another runtime's
 // execution step (a plugin or custom op whose host framework owns every device buffer and
 // forbids allocation while a request is in flight), or a serving loop that must never call
@@ -50,9 +50,9 @@ sv_status scratch_address(void **addr) {
 
 int noalloc_elem_bytes(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
 
-int noalloc_nchunk(int V, sv_dtype d) {
-    const int64_t ce = d == SV_BF16 ? sv::chunk_elems<sv::BF16>() : sv::chunk_elems<sv::F32>();
-    return int((int64_t(V) + ce - 1) / ce);
+int noalloc_ntile(int V, sv_dtype d) {
+    const int64_t te = d == SV_BF16 ? sv::tile_elems<sv::BF16>() : sv::tile_elems<sv::F32>();
+    return int((int64_t(V) + te - 1) / te);
 }
 
 bool noalloc_vec_ok(const void *p, int64_t sb, int64_t sr, sv_dtype d) {
@@ -74,8 +74,8 @@ extern "C" sv_status spec_verify_greedy_noalloc(const void *target_logits, int64
     if (B == 0) return SV_OK;
     if (!target_logits || !accepted_len || !out_tokens || (gamma > 0 && !draft_tokens))
         return SV_ERR_INVALID_ARG;
-    const int nchunk = noalloc_nchunk(V, dtype);
-    const int64_t partials = int64_t(B) * (gamma + 1) * nchunk;
+    const int ntile = noalloc_ntile(V, dtype);
+    const int64_t partials = int64_t(B) * (gamma + 1) * ntile;
     if (partials * int64_t(sizeof(int2)) > int64_t(kNoallocScratchBytes))
         return SV_ERR_WORKSPACE;  // larger than the fixed scratch: use spec_verify_greedy
     void *scratch = nullptr;
@@ -83,10 +83,9 @@ extern "C" sv_status spec_verify_greedy_noalloc(const void *target_logits, int64
     const bool vec = noalloc_vec_ok(target_logits, t_batch_stride, t_row_stride, dtype);
     const sv::Logits t{target_logits, t_batch_stride, t_row_stride};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = sv::launch_argmax_partial(dtype == SV_BF16, vec, t, gamma + 1, B, V, nchunk,
-                                              scratch, s);
+    cudaError_t e = sv::launch_argmax_tiles(dtype == SV_BF16, vec, t, gamma + 1, B, V, ntile, scratch, s);
     if (e == cudaSuccess)
-        e = sv::launch_greedy_finalize(B, gamma, V, nchunk, scratch, draft_tokens, accepted_len,
+        e = sv::launch_greedy_finalize(B, gamma, V, ntile, scratch, draft_tokens, accepted_len,
                                        out_tokens, s);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

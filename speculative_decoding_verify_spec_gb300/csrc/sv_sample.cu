@@ -10,13 +10,16 @@
 //   if all gamma drafts are accepted, draw a bonus token from p_gamma.
 //
 // GPU decomposition (one pass over every logit, then O(1) rows per sequence):
-//   stats_partial   every (row, 32 KB chunk) of the 2 gamma + 1 rows of every sequence:
-//                   NaN-propagating max M and sum 2^((l - M) log2(e) / T), one CTA each.
-//   decide          one warp per sequence: merge the chunk partials into (M, S) per row,
+//   stats_tiles     persistent: every 4 KB tile of the 2 gamma + 1 rows of every sequence
+//                   gives a NaN-propagating max M and sum 2^((l - M) log2(e) / T), one warp
+//                   per tile.
+//   decide          one warp per sequence: merge the tile partials into (M, S) per row,
 //                   gather p_i(x_i), q_i(x_i), draw the Philox uniforms and scan.
-//   residual_chunks (sequences that rejected) the residual mass of every chunk of row k.
-//   locate          one CTA per sequence: prefix over chunk masses, then an in-order block
-//                   scan inside the chosen chunk; first j with C_j > u' R.
+//   residual_tiles  persistent: (sequences that rejected) the residual mass of every 2 KB
+//                   residual tile of row k, one warp per tile.
+//   draw            one warp per sequence: prefix over the unit masses (residual tiles, or
+//                   the tiles of p for a bonus draw), then an in-order scan inside the chosen
+//                   unit held in registers; the first j with C_j > u' R.
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -38,8 +41,8 @@ __device__ __forceinline__ float weight(float x, float M, float c) {
     return ex2(__fmul_rn(__fsub_rn(x, M), c));
 }
 
-// (p_j - q_j)+ with p_j = 2^((t_j - M_t) c) / S_t and q_j likewise.  Both the chunk-mass
-// kernel and the in-chunk scan call this one function, so the two agree bit for bit.  The
+// (p_j - q_j)+ with p_j = 2^((t_j - M_t) c) / S_t and q_j likewise.  Both the tile-mass
+// kernel and the in-unit scan call this one function, so the two agree bit for bit.  The
 // products and the difference are explicitly rounded (no FMA contraction), so rows that
 // are identical give exactly p_j - q_j = 0, as in exact arithmetic.
 __device__ __forceinline__ float residual_weight(float tj, float dj, float c, float mt, float inv_st,
@@ -50,38 +53,54 @@ __device__ __forceinline__ float residual_weight(float tj, float dj, float c, fl
 }
 
 // ------------------------------------------------------------------------------------
+// Row statistics: partial[(seq * R + row) * ntile + tile] = (M, S) of that 4 KB tile, S
+// relative to the tile's own maximum.  Local rows [0, rows_a) come from a, the rest from bt.
 template <class D, bool VEC>
 __global__ void __launch_bounds__(kThreads, 4)
-    stats_partial_kernel(Logits a, int rows_a, Logits bt, int R, int V, int nchunk, float c,
-                         float2 *__restrict__ partial) {
-    __shared__ float2 red[kWarps];
-    const int64_t item = blockIdx.x;
-    const int64_t row = item / nchunk;
-    const int chunk = int(item - row * nchunk);
-    const int64_t seq = row / R;
-    const int local = int(row - seq * R);
-    const char *rp = local < rows_a ? row_ptr(a, D::kBytes, seq, local)
-                                    : row_ptr(bt, D::kBytes, seq, local - rows_a);
-    const int64_t c0 = int64_t(chunk) * chunk_elems<D>();
-    const int len = chunk_len<D>(V, c0);
-
-    uint4 v[kVecPerThread];
+    stats_tiles_kernel(Logits a, int rows_a, Logits bt, int R, int V, int ntile, int64_t items, float c,
+                       float2 *__restrict__ partial) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = int64_t(gridDim.x) * kWarps;
+    for (TileWalk w(int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5), nwarps, R, ntile); w.it < items;
+         w.next(nwarps)) {
+        const char *rp = w.local < rows_a ? row_ptr(a, D::kBytes, w.seq, w.local)
+                                          : row_ptr(bt, D::kBytes, w.seq, w.local - rows_a);
+        const int64_t c0 = int64_t(w.tile) * tile_elems<D>();
+        const int len = unit_len(V, c0, tile_elems<D>());
+        uint4 v[kTileVecs];
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-        const int e0 = (threadIdx.x + u * kThreads) * D::EPV;
-        v[u] = e0 < len ? load_vec<D, VEC>(rp, c0, e0, len) : neg_inf_vec<D>();
+        for (int u = 0; u < kTileVecs; ++u) {
+            const int e0 = (lane + 32 * u) * D::EPV;
+            v[u] = e0 < len ? load_vec<D, VEC>(rp, c0, e0, len) : neg_inf_vec<D>();
+        }
+        // the tile's maximum first (NaN-propagating); every lane then sums relative to it
+        const float M = warp_reduce(thread_max<D>(v), [](float x, float y) { return max_nan(x, y); });
+        float S = 0.f;
+        if (is_finite(M)) S = warp_reduce(thread_sumexp<D>(v, c, M), [](float x, float y) { return x + y; });
+        if (lane == 0) partial[w.it] = make_float2(M, S);
     }
-    const float m = thread_max<D>(v);
-    const float S = is_finite(m) ? thread_sumexp<D>(v, c, m) : 0.f;
-    const float2 r = block_reduce(
-        make_float2(m, S), [c](float2 x, float2 y) { return merge_stats(x, y, c); }, red);
-    if (threadIdx.x == 0) partial[item] = r;
+}
+
+// Merge n tile partials in tile order (one lane); loads go out kMergeBatch at a time so a
+// row costs a few round trips to L2.
+constexpr int kMergeBatch = 16;
+__device__ float2 merge_row(const float2 *__restrict__ p, int n, float c) {
+    float2 s = make_float2(-__int_as_float(0x7f800000), 0.f);
+    for (int q0 = 0; q0 < n; q0 += kMergeBatch) {
+        float2 e[kMergeBatch];
+#pragma unroll
+        for (int q = 0; q < kMergeBatch; ++q) e[q] = q0 + q < n ? p[q0 + q] : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < kMergeBatch; ++q)
+            if (q0 + q < n) s = q0 + q == 0 ? e[q] : merge_stats(s, e[q], c);
+    }
+    return s;
 }
 
 // ------------------------------------------------------------------------------------
 template <class D>
 __global__ void __launch_bounds__(128)
-    decide_kernel(Logits t, Logits d, int B, int gamma, int V, int nchunk, float c,
+    decide_kernel(Logits t, Logits d, int B, int gamma, int V, int ntile, float c,
                   const int32_t *__restrict__ x, uint64_t seed, uint64_t offset,
                   const float2 *__restrict__ partial, float2 *__restrict__ rowstat,
                   int2 *__restrict__ plan, int32_t *__restrict__ accepted_len,
@@ -91,16 +110,25 @@ __global__ void __launch_bounds__(128)
     if (seq >= B) return;
     const int R = 2 * gamma + 1;
 
+    // the accept test's operands for the first 32 drafts do not depend on the statistics:
+    // their loads go out first and overlap the merge
+    int32_t x0 = 0;
+    float tx0 = 0.f, dx0 = 0.f;
+    if (lane < gamma) {
+        x0 = x[seq * gamma + lane];
+        if (x0 >= 0 && x0 < V) {
+            tx0 = load_elem<D>(row_ptr(t, D::kBytes, seq, lane), x0);
+            dx0 = load_elem<D>(row_ptr(d, D::kBytes, seq, lane), x0);
+        }
+    }
     bool ok = true;
     for (int r = lane; r < R; r += 32) {
-        const float2 *p = partial + (seq * R + r) * nchunk;
-        float2 s = p[0];
-        for (int ch = 1; ch < nchunk; ++ch) s = merge_stats(s, p[ch], c);
+        const float2 s = merge_row(partial + (seq * R + r) * ntile, ntile, c);
         rowstat[seq * R + r] = s;
         ok &= is_finite(s.x);
     }
     for (int i = lane; i < gamma; i += 32) {
-        const int32_t xi = x[seq * gamma + i];
+        const int32_t xi = i == lane ? x0 : x[seq * gamma + i];
         ok &= xi >= 0 && xi < V;
     }
     ok = __all_sync(0xFFFFFFFFu, ok);
@@ -120,11 +148,14 @@ __global__ void __launch_bounds__(128)
         const int i = i0 + lane;
         bool reject = false;
         if (i < gamma) {
-            const int32_t xi = x[seq * gamma + i];
             const float2 st = rowstat[seq * R + i];
             const float2 sd = rowstat[seq * R + gamma + 1 + i];
-            const float tx = load_elem<D>(row_ptr(t, D::kBytes, seq, i), xi);
-            const float dx = load_elem<D>(row_ptr(d, D::kBytes, seq, i), xi);
+            float tx = tx0, dx = dx0;
+            if (i0 > 0) {
+                const int32_t xi = x[seq * gamma + i];
+                tx = load_elem<D>(row_ptr(t, D::kBytes, seq, i), xi);
+                dx = load_elem<D>(row_ptr(d, D::kBytes, seq, i), xi);
+            }
             const float p = weight(tx, st.x, c) / st.y;
             const float q = weight(dx, sd.x, c) / sd.y;
             const float u = uniform01(seed, offset, uint32_t(seq), uint32_t(i), 0u);
@@ -147,173 +178,201 @@ __global__ void __launch_bounds__(128)
 }
 
 // ------------------------------------------------------------------------------------
+// Residual masses: csum[seq * nrt + tile] = sum over the residual tile of (p - q)+ at the
+// stop row, for the sequences that rejected (plan mode 1); other entries are not written.
 template <class D, bool VEC>
-__global__ void __launch_bounds__(kThreads, 2)
-    residual_chunks_kernel(Logits t, Logits d, int gamma, int V, int nchunk, float c,
-                           const float2 *__restrict__ rowstat, const int2 *__restrict__ plan,
-                           float *__restrict__ csum) {
-    __shared__ float red[kWarps];
-    const int64_t item = blockIdx.x;
-    const int64_t seq = item / nchunk;
-    const int chunk = int(item - seq * nchunk);
-    const int2 pl = plan[seq];
-    if (pl.y != 1) return;  // uniform over the block
-    const int k = pl.x, R = 2 * gamma + 1;
-    const float2 st = rowstat[seq * R + k], sd = rowstat[seq * R + gamma + 1 + k];
-    const float inv_st = 1.f / st.y, inv_sd = 1.f / sd.y;
-    const char *tp = row_ptr(t, D::kBytes, seq, k);
-    const char *dp = row_ptr(d, D::kBytes, seq, k);
-    const int64_t c0 = int64_t(chunk) * chunk_elems<D>();
-    const int len = chunk_len<D>(V, c0);
-
-    uint4 tv[kVecPerThread], dv[kVecPerThread];
+__global__ void __launch_bounds__(kThreads, 4)
+    residual_tiles_kernel(Logits t, Logits d, int gamma, int V, int nrt, int64_t items, float c,
+                          const float2 *__restrict__ rowstat, const int2 *__restrict__ plan,
+                          float *__restrict__ csum) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = int64_t(gridDim.x) * kWarps;
+    const int R = 2 * gamma + 1;
+    for (TileWalk w(int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5), nwarps, 1, nrt); w.it < items;
+         w.next(nwarps)) {
+        const int2 pl = plan[w.seq];
+        if (pl.y != 1) continue;  // uniform over the warp
+        const int k = pl.x;
+        const float2 st = rowstat[w.seq * R + k], sd = rowstat[w.seq * R + gamma + 1 + k];
+        const char *tp = row_ptr(t, D::kBytes, w.seq, k);
+        const char *dp = row_ptr(d, D::kBytes, w.seq, k);
+        const int64_t c0 = int64_t(w.tile) * res_tile_elems<D>();
+        const int len = unit_len(V, c0, res_tile_elems<D>());
+        uint4 tv[kResVecs], dv[kResVecs];
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-        const int e0 = (threadIdx.x + u * kThreads) * D::EPV;
-        tv[u] = e0 < len ? load_vec<D, VEC>(tp, c0, e0, len) : neg_inf_vec<D>();
-        dv[u] = e0 < len ? load_vec<D, VEC>(dp, c0, e0, len) : neg_inf_vec<D>();
+        for (int u = 0; u < kResVecs; ++u) {
+            const int e0 = (lane + 32 * u) * D::EPV;
+            tv[u] = e0 < len ? load_vec<D, VEC>(tp, c0, e0, len) : neg_inf_vec<D>();
+            dv[u] = e0 < len ? load_vec<D, VEC>(dp, c0, e0, len) : neg_inf_vec<D>();
+        }
+        const float inv_st = 1.f / st.y, inv_sd = 1.f / sd.y;
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < kResVecs; ++u)
+#pragma unroll
+            for (int e = 0; e < D::EPV; ++e)
+                acc += residual_weight(vec_elem<D>(tv[u], e), vec_elem<D>(dv[u], e), c, st.x, inv_st, sd.x,
+                                       inv_sd);
+        const float mass = warp_reduce(acc, [](float x, float y) { return x + y; });
+        if (lane == 0) csum[w.it] = mass;
     }
-    float acc = 0.f;
-#pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u)
-#pragma unroll
-        for (int e = 0; e < D::EPV; ++e)
-            acc += residual_weight(vec_elem<D>(tv[u], e), vec_elem<D>(dv[u], e), c, st.x, inv_st,
-                                   sd.x, inv_sd);
-    const float s = block_reduce(acc, [](float a, float b) { return a + b; }, red);
-    if (threadIdx.x == 0) csum[item] = s;
 }
 
 // ------------------------------------------------------------------------------------
+// The inverse-CDF draw, one warp per sequence.  Units: mode 1 the residual tiles of the
+// stop row (masses from residual_tiles), mode 0 the tiles of p (mass S_u 2^((M_u - M) c)
+// from the row-statistics partials).  A zero residual falls back to p.  Lane l owns the
+// contiguous units [l * per_lane, (l + 1) * per_lane); inside the chosen unit lane l holds
+// a contiguous run of its vectors in registers, summed once and scanned once with the same
+// arithmetic, so both passes see the same bits.
 template <class D, bool VEC>
-__global__ void __launch_bounds__(kThreads)
-    locate_kernel(Logits t, Logits d, int gamma, int V, int nchunk, float c, uint64_t seed,
-                  uint64_t offset, const float2 *__restrict__ partial,
-                  const float2 *__restrict__ rowstat, const int2 *__restrict__ plan,
-                  const float *__restrict__ csum, int32_t *__restrict__ out_tokens) {
-    __shared__ float fsc[kWarps];
-    __shared__ int isc[kWarps];
-    __shared__ float hit_base;
-    const int64_t seq = blockIdx.x;
+__global__ void __launch_bounds__(128)
+    draw_kernel(Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt, float c, uint64_t seed,
+                uint64_t offset, const float2 *__restrict__ partial, const float2 *__restrict__ rowstat,
+                const int2 *__restrict__ plan, const float *__restrict__ csum,
+                int32_t *__restrict__ out_tokens) {
+    const int lane = threadIdx.x & 31;
+    const int64_t seq = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if (seq >= B) return;
     const int2 pl = plan[seq];
     if (pl.y < 0) return;  // invalid sequence: outputs already written by decide
     const int k = pl.x, R = 2 * gamma + 1;
     int mode = pl.y;  // 1: residual after a rejection, 0: bonus draw from p
     const float2 st = rowstat[seq * R + k];
-    const float2 sd = mode ? rowstat[seq * R + gamma + 1 + k] : make_float2(0.f, 1.f);
-    const float inv_st = 1.f / st.y, inv_sd = 1.f / sd.y;
-    const float2 *prow = partial + (seq * R + k) * nchunk;
-    const float *crow = csum + seq * nchunk;
-    auto chunk_mass = [&](int ch) -> float {
-        if (ch >= nchunk) return 0.f;
-        if (mode) return crow[ch];
-        const float2 p = prow[ch];
-        return p.y * weight(p.x, st.x, c);  // mass of chunk ch under 2^((l - M) c)
+    const float2 *prow = partial + (seq * R + k) * ntile;
+    const float *crow = csum + seq * nrt;
+    auto unit_mass = [&](int u) -> float {
+        if (mode) return crow[u];
+        const float2 p = prow[u];
+        return p.y * weight(p.x, st.x, c);  // mass of tile u under 2^((l - M) c)
     };
 
-    // total mass R (as the deterministic tile-by-tile scan computes it)
-    float total = 0.f;
+    float total = 0.f, lane_sum = 0.f;
+    int units = 0, per_lane = 0;
     for (int pass = 0; pass < 2; ++pass) {
-        total = 0.f;
-        for (int base = 0; base < nchunk; base += kThreads) {
-            float tt;
-            block_inclusive_scan(chunk_mass(base + threadIdx.x), fsc, &tt);
-            total += tt;
+        units = mode ? nrt : ntile;
+        per_lane = (units + 31) / 32;
+        lane_sum = 0.f;
+#pragma unroll 4
+        for (int q = 0; q < per_lane; ++q) {
+            const int u = lane * per_lane + q;
+            if (u < units) lane_sum += unit_mass(u);
         }
+        total = __shfl_sync(0xFFFFFFFFu, warp_inclusive_scan(lane_sum, lane), 31);
         if (mode == 1 && !(total > 0.f)) mode = 0;  // exact-zero residual: draw from p
         else break;
     }
     const float thr = uniform01(seed, offset, uint32_t(seq), uint32_t(k), 1u) * total;
+    const float incl = warp_inclusive_scan(lane_sum, lane);
 
-    // the chunk holding the threshold: first ch with C_ch > thr (C inclusive)
-    int cstar = -1;
+    // the unit holding the threshold: the first lane whose range crosses it, then inside it
+    int unit = -1;
+    float base = 0.f;
     bool force_last = false;
-    float carry = 0.f;
-    int last_pos_chunk = -1;
-    float last_pos_base = 0.f;
-    for (int base = 0; base < nchunk && cstar < 0; base += kThreads) {
-        const int ch = base + threadIdx.x;
-        const float w = chunk_mass(ch);
-        float tt;
-        const float incl = block_inclusive_scan(w, fsc, &tt);
-        const bool hit = ch < nchunk && carry + incl > thr;
-        const int first = block_reduce(hit ? ch : kNoIndex, [](int a, int b) { return min(a, b); }, isc);
-        const int lp = block_reduce((ch < nchunk && w > 0.f) ? ch : -1,
-                                    [](int a, int b) { return max(a, b); }, isc);
-        if (first != kNoIndex) {
-            if (ch == first) hit_base = carry + incl - w;
-            __syncthreads();
-            cstar = first;
-            carry = hit_base;
-        } else {
-            if (lp >= 0) {
-                if (ch == lp) hit_base = carry + incl - w;
-                __syncthreads();
-                last_pos_chunk = lp;
-                last_pos_base = hit_base;
+    const unsigned crossing = __ballot_sync(0xFFFFFFFFu, incl > thr);
+    if (crossing) {
+        const int l = __ffs(crossing) - 1;
+        if (lane == l) {
+            float run = incl - lane_sum;
+            int last_in_lane = lane * per_lane;
+            for (int q = 0; q < per_lane; ++q) {
+                const int u = lane * per_lane + q;
+                if (u >= units) break;
+                last_in_lane = u;
+                const float m = unit_mass(u);
+                if (run + m > thr) {
+                    unit = u;
+                    break;
+                }
+                run += m;
             }
-            carry += tt;
+            if (unit < 0) unit = last_in_lane;  // rounding: stay inside this lane's units
+            base = run;
         }
-        __syncthreads();
-    }
-    if (cstar < 0) {  // rounding left the threshold above the last prefix
-        cstar = last_pos_chunk >= 0 ? last_pos_chunk : 0;
-        carry = last_pos_base;
+        unit = __shfl_sync(0xFFFFFFFFu, unit, l);
+        base = __shfl_sync(0xFFFFFFFFu, base, l);
+    } else {  // rounding left the threshold at or above the total: the last unit with mass
+        int lp = -1;
+        for (int q = 0; q < per_lane; ++q) {
+            const int u = lane * per_lane + q;
+            if (u < units && unit_mass(u) > 0.f) lp = u;
+        }
+        lp = warp_reduce(lp, [](int a, int b) { return max(a, b); });
+        unit = lp >= 0 ? lp : 0;
         force_last = true;
     }
 
-    // in-order scan inside chunk cstar: thread t owns elements [t*EPT, (t+1)*EPT)
-    constexpr int EPT = kVecPerThread * D::EPV;
+    // inside the unit: lane l owns the contiguous vectors [l * VPL, (l + 1) * VPL)
+    const int unit_elems = mode ? res_tile_elems<D>() : tile_elems<D>();
+    const int last_unit = (V - 1) / unit_elems;  // units past it hold no element of the row
+    if (unit > last_unit) unit = last_unit;
+    const int VPL = mode ? kResVecs : kTileVecs;
+    const float2 sd = mode ? rowstat[seq * R + gamma + 1 + k] : make_float2(0.f, 1.f);
+    const float inv_st = 1.f / st.y, inv_sd = 1.f / sd.y;
     const char *tp = row_ptr(t, D::kBytes, seq, k);
-    const char *dp = mode ? row_ptr(d, D::kBytes, seq, k) : nullptr;
-    const int64_t c0 = int64_t(cstar) * chunk_elems<D>();
-    const int len = chunk_len<D>(V, c0);
-    float r[EPT];
-    float tsum = 0.f;
+    const char *dp = row_ptr(d, D::kBytes, seq, k);
+    const int64_t u0 = int64_t(unit) * unit_elems;
+    const int len = unit_len(V, u0, unit_elems);
+    uint4 tv[kTileVecs], dv[kResVecs];
 #pragma unroll
-    for (int u = 0; u < kVecPerThread; ++u) {
-        const int e0 = (threadIdx.x * kVecPerThread + u) * D::EPV;
-        const uint4 tv = e0 < len ? load_vec<D, VEC>(tp, c0, e0, len) : neg_inf_vec<D>();
-        uint4 dv = neg_inf_vec<D>();
-        if (mode && e0 < len) dv = load_vec<D, VEC>(dp, c0, e0, len);
+    for (int v = 0; v < kTileVecs; ++v) {
+        const int e0 = (lane * VPL + v) * D::EPV;
+        tv[v] = (v < VPL && e0 < len) ? load_vec<D, VEC>(tp, u0, e0, len) : neg_inf_vec<D>();
+    }
 #pragma unroll
-        for (int e = 0; e < D::EPV; ++e) {
-            const float tj = vec_elem<D>(tv, e);
-            const float w = mode ? residual_weight(tj, vec_elem<D>(dv, e), c, st.x, inv_st, sd.x, inv_sd)
-                                 : weight(tj, st.x, c);
-            r[u * D::EPV + e] = w;
-            tsum += w;
+    for (int v = 0; v < kResVecs; ++v) {
+        const int e0 = (lane * VPL + v) * D::EPV;
+        dv[v] = (mode && e0 < len) ? load_vec<D, VEC>(dp, u0, e0, len) : neg_inf_vec<D>();
+    }
+    auto w_at = [&](const uint4 &t4, const uint4 &d4, int e) -> float {
+        const float tj = vec_elem<D>(t4, e);
+        return mode ? residual_weight(tj, vec_elem<D>(d4, e), c, st.x, inv_st, sd.x, inv_sd)
+                    : weight(tj, st.x, c);
+    };
+    Kahan lsum;
+#pragma unroll
+    for (int v = 0; v < kTileVecs; ++v) {
+        if (v < VPL) {
+#pragma unroll
+            for (int e = 0; e < D::EPV; ++e) lsum.add(w_at(tv[v], dv[v % kResVecs], e));
         }
     }
-    float tt;
-    const float incl = block_inclusive_scan(tsum, fsc, &tt);
-    float P = carry + (incl - tsum);
+    const float tsum = lsum.value();
+    const float lincl = warp_inclusive_scan(tsum, lane);
+    Kahan run;
+    run.add(base);
+    run.add(lincl - tsum);
     int cand = kNoIndex, lastpos = -1;
 #pragma unroll
-    for (int q = 0; q < EPT; ++q) {
-        const int j = threadIdx.x * EPT + q;
-        P += r[q];
-        if (j < len) {
-            if (!force_last && cand == kNoIndex && P > thr) cand = j;
-            if (r[q] > 0.f) lastpos = j;
+    for (int v = 0; v < kTileVecs; ++v) {  // the same registers, the same arithmetic
+        if (v < VPL) {
+            const int e0 = (lane * VPL + v) * D::EPV;
+#pragma unroll
+            for (int e = 0; e < D::EPV; ++e) {
+                const int j = e0 + e;
+                const float w = w_at(tv[v], dv[v % kResVecs], e);
+                run.add(w);
+                if (j < len) {
+                    if (!force_last && cand == kNoIndex && run.value() > thr) cand = j;
+                    if (w > 0.f) lastpos = j;
+                }
+            }
         }
     }
-    cand = block_reduce(cand, [](int a, int b) { return min(a, b); }, isc);
-    lastpos = block_reduce(lastpos, [](int a, int b) { return max(a, b); }, isc);
+    cand = warp_reduce(cand, [](int a, int b) { return min(a, b); });
+    lastpos = warp_reduce(lastpos, [](int a, int b) { return max(a, b); });
     int tok = cand != kNoIndex ? cand : lastpos;
     if (tok < 0) tok = 0;
-    if (threadIdx.x == 0) out_tokens[seq * (gamma + 1) + k] = int32_t(c0 + tok);
+    if (lane == 0) out_tokens[seq * (gamma + 1) + k] = int32_t(u0 + tok);
 }
 
 // ------------------------------------------------------------------------------------
-__global__ void rowstats_finalize_kernel(int rows, int nchunk, float c, float inv_t,
+__global__ void rowstats_finalize_kernel(int rows, int ntile, float c, float inv_t,
                                          const float2 *__restrict__ partial, float *__restrict__ m_out,
                                          float *__restrict__ lse_out) {
     const int64_t r = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (r >= rows) return;
-    const float2 *p = partial + r * nchunk;
-    float2 s = p[0];
-    for (int ch = 1; ch < nchunk; ++ch) s = merge_stats(s, p[ch], c);
+    const float2 s = merge_row(partial + r * ntile, ntile, c);
     if (is_finite(s.x)) {
         const float m = s.x * inv_t;
         m_out[r] = m;
@@ -338,66 +397,64 @@ __global__ void uniforms_kernel(uint64_t seed, uint64_t offset, int B, int posit
 // ------------------------------------------------------------------------------------
 // Launchers
 // ------------------------------------------------------------------------------------
-#define SV_DISPATCH(DTYPE, VEC, KERNEL, GRID, BLOCK, STREAM, ...)                                  \
-    do {                                                                                         \
-        if ((DTYPE) == 1) {                                                                      \
-            if (VEC) KERNEL<BF16, true><<<GRID, BLOCK, 0, STREAM>>>(__VA_ARGS__);                \
-            else KERNEL<BF16, false><<<GRID, BLOCK, 0, STREAM>>>(__VA_ARGS__);                   \
-        } else {                                                                                 \
-            if (VEC) KERNEL<F32, true><<<GRID, BLOCK, 0, STREAM>>>(__VA_ARGS__);                 \
-            else KERNEL<F32, false><<<GRID, BLOCK, 0, STREAM>>>(__VA_ARGS__);                    \
-        }                                                                                        \
-    } while (0)
+template <class KB1, class KB0, class KF1, class KF0>
+inline auto pick(int dtype, bool vec, KB1 b1, KB0 b0, KF1 f1, KF0 f0) {
+    return dtype == 1 ? (vec ? b1 : b0) : (vec ? f1 : f0);
+}
 
-cudaError_t launch_stats_partial(int dtype, bool vec, Logits a, int rows_a, Logits b, int R, int B,
-                                 int V, int nchunk, float c, void *partial, cudaStream_t s) {
-    const unsigned grid = unsigned(int64_t(B) * R * nchunk);
-    SV_DISPATCH(dtype, vec, stats_partial_kernel, grid, kThreads, s, a, rows_a, b, R, V, nchunk, c,
-                static_cast<float2 *>(partial));
+cudaError_t launch_stats_tiles(int dtype, bool vec, Logits a, int rows_a, Logits b, int R, int B, int V,
+                               int ntile, float c, void *partial, cudaStream_t s) {
+    const int64_t items = int64_t(B) * R * ntile;
+    auto k = pick(dtype, vec, stats_tiles_kernel<BF16, true>, stats_tiles_kernel<BF16, false>,
+                  stats_tiles_kernel<F32, true>, stats_tiles_kernel<F32, false>);
+    unsigned grid = 0;
+    cudaError_t e = persistent_grid(k, items, &grid);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kThreads, 0, s>>>(a, rows_a, b, R, V, ntile, items, c, static_cast<float2 *>(partial));
     return cudaGetLastError();
 }
 
-cudaError_t launch_decide(int dtype, Logits t, Logits d, int B, int gamma, int V, int nchunk,
+cudaError_t launch_decide(int dtype, Logits t, Logits d, int B, int gamma, int V, int ntile,
                           float c, const int32_t *x, uint64_t seed, uint64_t offset,
                           const void *partial, void *rowstat, void *plan, int32_t *accepted_len,
                           int32_t *out_tokens, cudaStream_t s) {
     const unsigned grid = unsigned((int64_t(B) * 32 + 127) / 128);
-    if (dtype == 1)
-        decide_kernel<BF16><<<grid, 128, 0, s>>>(t, d, B, gamma, V, nchunk, c, x, seed, offset,
-                                                 static_cast<const float2 *>(partial),
-                                                 static_cast<float2 *>(rowstat), static_cast<int2 *>(plan),
-                                                 accepted_len, out_tokens);
-    else
-        decide_kernel<F32><<<grid, 128, 0, s>>>(t, d, B, gamma, V, nchunk, c, x, seed, offset,
-                                                static_cast<const float2 *>(partial),
-                                                static_cast<float2 *>(rowstat), static_cast<int2 *>(plan),
-                                                accepted_len, out_tokens);
+    auto k = dtype == 1 ? decide_kernel<BF16> : decide_kernel<F32>;
+    k<<<grid, 128, 0, s>>>(t, d, B, gamma, V, ntile, c, x, seed, offset, static_cast<const float2 *>(partial),
+                           static_cast<float2 *>(rowstat), static_cast<int2 *>(plan), accepted_len, out_tokens);
     return cudaGetLastError();
 }
 
-cudaError_t launch_residual_chunks(int dtype, bool vec, Logits t, Logits d, int B, int gamma,
-                                   int V, int nchunk, float c, const void *rowstat,
-                                   const void *plan, float *csum, cudaStream_t s) {
-    const unsigned grid = unsigned(int64_t(B) * nchunk);
-    SV_DISPATCH(dtype, vec, residual_chunks_kernel, grid, kThreads, s, t, d, gamma, V, nchunk, c,
-                static_cast<const float2 *>(rowstat), static_cast<const int2 *>(plan), csum);
+cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V,
+                                  int nrt, float c, const void *rowstat, const void *plan, float *csum,
+                                  cudaStream_t s) {
+    const int64_t items = int64_t(B) * nrt;
+    auto k = pick(dtype, vec, residual_tiles_kernel<BF16, true>, residual_tiles_kernel<BF16, false>,
+                  residual_tiles_kernel<F32, true>, residual_tiles_kernel<F32, false>);
+    unsigned grid = 0;
+    cudaError_t e = persistent_grid(k, items, &grid);
+    if (e != cudaSuccess) return e;
+    k<<<grid, kThreads, 0, s>>>(t, d, gamma, V, nrt, items, c, static_cast<const float2 *>(rowstat),
+                                static_cast<const int2 *>(plan), csum);
     return cudaGetLastError();
 }
 
-cudaError_t launch_locate(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V,
-                          int nchunk, float c, uint64_t seed, uint64_t offset, const void *partial,
-                          const void *rowstat, const void *plan, const float *csum,
-                          int32_t *out_tokens, cudaStream_t s) {
-    SV_DISPATCH(dtype, vec, locate_kernel, unsigned(B), kThreads, s, t, d, gamma, V, nchunk, c, seed,
-                offset, static_cast<const float2 *>(partial), static_cast<const float2 *>(rowstat),
-                static_cast<const int2 *>(plan), csum, out_tokens);
+cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
+                        float c, uint64_t seed, uint64_t offset, const void *partial, const void *rowstat,
+                        const void *plan, const float *csum, int32_t *out_tokens, cudaStream_t s) {
+    const unsigned grid = unsigned((int64_t(B) * 32 + 127) / 128);
+    auto k = pick(dtype, vec, draw_kernel<BF16, true>, draw_kernel<BF16, false>, draw_kernel<F32, true>,
+                  draw_kernel<F32, false>);
+    k<<<grid, 128, 0, s>>>(t, d, B, gamma, V, ntile, nrt, c, seed, offset, static_cast<const float2 *>(partial),
+                           static_cast<const float2 *>(rowstat), static_cast<const int2 *>(plan), csum,
+                           out_tokens);
     return cudaGetLastError();
 }
 
-cudaError_t launch_rowstats_finalize(int rows, int nchunk, float c, float inv_t, const void *partial,
+cudaError_t launch_rowstats_finalize(int rows, int ntile, float c, float inv_t, const void *partial,
                                      float *m_out, float *lse_out, cudaStream_t s) {
     const unsigned grid = unsigned((int64_t(rows) + 255) / 256);
-    rowstats_finalize_kernel<<<grid, 256, 0, s>>>(rows, nchunk, c, inv_t,
+    rowstats_finalize_kernel<<<grid, 256, 0, s>>>(rows, ntile, c, inv_t,
                                                   static_cast<const float2 *>(partial), m_out, lse_out);
     return cudaGetLastError();
 }

@@ -41,8 +41,8 @@ def test_full_size_greedy_fits_and_matches():
 
 
 def test_problem_beyond_the_fixed_scratch_is_rejected_before_launch():
-    # a broadcast view keeps the test small: 4096 sequences x 32 rows x 10 chunks of
-    # partials need 10 MiB, more than the 4 MiB scratch
+    # a broadcast view keeps the test small: 4096 sequences x 32 rows x 75 tiles of
+    # partials need 75 MiB, more than the 4 MiB scratch
     row = torch.zeros((1, 1, 152064), dtype=torch.bfloat16, device=DEV)
     target = row.expand(4096, 32, 152064)
     tokens = torch.zeros((4096, 31), dtype=torch.int32, device=DEV)
