@@ -37,6 +37,7 @@ UNIT = "seqs/s"
 FALLBACK_HBM_GBS = 6800.0
 DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "argmax_tiles_kernel",
                    "tree": "argmax_tiles_kernel"}
+STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
 STAGES = {"sample": ["row_stats", "decide", "residual_mass", "inverse_cdf"],
           "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"]}
 
@@ -261,25 +262,33 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
     for _ in range(max(3, warmup)):
         call()
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(steps)]
-    for row in ev:
-        for e in row:
-            e.record()
-    torch.cuda.synchronize()
+    # the timed steps: nothing but the calls (events between a call's kernels would keep
+    # each kernel from being scheduled while the previous one drains)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     start.record()
     for k in range(steps):
-        binding.set_stage_events(ev[k])
         call()
     end.record()
-    binding.set_stage_events(None)
     torch.cuda.synchronize()
     barrier(world)
     ms = start.elapsed_time(end)
     ms_max = max_over_ranks(ms, world, dev)
-    stage_ms = [sum(ev[k][s].elapsed_time(ev[k][s + 1]) for k in range(steps)) / steps
+    # then the per-kernel breakdown on separate steps, with the library's stage events
+    # recorded on the call's stream around every kernel
+    ksteps = min(steps, STAGE_STEPS)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(ksteps)]
+    for row in ev:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    for k in range(ksteps):
+        binding.set_stage_events(ev[k])
+        call()
+    binding.set_stage_events(None)
+    torch.cuda.synchronize()
+    stage_ms = [sum(ev[k][s].elapsed_time(ev[k][s + 1]) for k in range(ksteps)) / ksteps
                 for s in range(nst)]
     ms_step = ms_max / steps
     B = cfg["B"]

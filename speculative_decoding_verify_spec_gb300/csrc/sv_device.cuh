@@ -15,6 +15,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace sv {
 
 constexpr int kThreads = 256;                          // threads per CTA
@@ -304,6 +306,58 @@ struct TileWalk {
         }
     }
 };
+
+// Programmatic dependent launch.  Every kernel of a call first lets the next kernel of the
+// call be scheduled (its CTAs then wait in griddep_wait on SMs freed by this grid's tail),
+// then, before it reads anything an earlier kernel wrote, waits for the previous grid to
+// complete and flush.  Every CTA waits before it may exit, so a grid is only complete once
+// its predecessor is -- completion is transitive along the call.  For a grid launched
+// without the attribute both instructions are no-ops.
+__device__ __forceinline__ void griddep_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launches `kernel` so that it may start while the previous kernel on the stream drains.
+template <class... Params, class... Args>
+inline cudaError_t launch_after(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem,
+                                cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// One warp merges the n tile partials of a row: lane l takes tiles l, l + 32, ... in order,
+// then the lanes combine in a fixed butterfly.  Every lane returns the row's result.
+__device__ __forceinline__ float2 warp_merge_stats(const float2 *__restrict__ p, int n, float c, int lane) {
+    float2 s = make_float2(-__int_as_float(0x7f800000), 0.f);
+    for (int q0 = lane; q0 < n; q0 += 128) {
+        float2 e[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) e[j] = q0 + 32 * j < n ? p[q0 + 32 * j] : make_float2(-__int_as_float(0x7f800000), 0.f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s = merge_stats(s, e[j], c);
+    }
+    return warp_reduce(s, [c](float2 a, float2 b) { return merge_stats(a, b, c); });
+}
+__device__ __forceinline__ int2 warp_merge_argmax(const int2 *__restrict__ p, int n, int lane) {
+    int2 s = make_int2(__float_as_int(-__int_as_float(0x7f800000)), kNoIndex);
+    for (int q0 = lane; q0 < n; q0 += 128) {
+        int2 e[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            e[j] = q0 + 32 * j < n ? p[q0 + 32 * j] : make_int2(__float_as_int(-__int_as_float(0x7f800000)), kNoIndex);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s = merge_argmax(s, e[j]);
+    }
+    return warp_reduce(s, [](int2 a, int2 b) { return merge_argmax(a, b); });
+}
 
 // The persistent streaming grid: SMs x resident CTAs of `kernel`, at most enough CTAs to
 // give every warp one of `items` tiles.

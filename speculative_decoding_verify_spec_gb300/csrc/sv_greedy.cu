@@ -29,6 +29,7 @@ __device__ __forceinline__ const char *row_ptr(const Logits &L, int bytes, int64
 template <class D, bool VEC>
 __global__ void __launch_bounds__(kThreads, 4)
     argmax_tiles_kernel(Logits t, int R, int V, int ntile, int64_t items, int2 *__restrict__ partial) {
+    griddep_launch_next();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = int64_t(gridDim.x) * kWarps;
     for (TileWalk w(int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5), nwarps, R, ntile); w.it < items;
@@ -80,38 +81,28 @@ __global__ void __launch_bounds__(kThreads, 4)
     }
 }
 
-// Merge the tile partials of one row, in tile order; returns (value bits, index).  Loads go
-// out kMergeBatch at a time.
-constexpr int kMergeBatch = 16;
-__device__ int2 row_argmax(const int2 *__restrict__ p, int n) {
-    int2 best = make_int2(__float_as_int(-__int_as_float(0x7f800000)), kNoIndex);
-    for (int q0 = 0; q0 < n; q0 += kMergeBatch) {
-        int2 e[kMergeBatch];
-#pragma unroll
-        for (int q = 0; q < kMergeBatch; ++q) e[q] = q0 + q < n ? p[q0 + q] : make_int2(0, 0);
-#pragma unroll
-        for (int q = 0; q < kMergeBatch; ++q)
-            if (q0 + q < n) best = q0 + q == 0 ? e[q] : merge_argmax(best, e[q]);
-    }
-    return best;
-}
-
-__global__ void __launch_bounds__(128)
+// Greedy finalize, one CTA per sequence: warp w merges the tile partials of rows w, w + 8,
+// ...; warp 0 then finds the longest matching prefix.
+__global__ void __launch_bounds__(kThreads)
     greedy_finalize_kernel(int B, int gamma, int V, int ntile, const int2 *__restrict__ partial,
                            const int32_t *__restrict__ x, int32_t *__restrict__ accepted_len,
                            int32_t *__restrict__ out_tokens) {
-    extern __shared__ int s_arg[];  // (gamma + 1) argmaxes per warp
+    extern __shared__ int2 s_best[];  // [gamma + 1]
+    griddep_launch_next();
+    griddep_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t seq = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (seq >= B) return;
+    const int64_t seq = blockIdx.x;
     const int R = gamma + 1;
-    int *a = s_arg + warp * R;
+    for (int i = warp; i < R; i += kWarps) {
+        const int2 best = warp_merge_argmax(partial + (seq * R + i) * ntile, ntile, lane);
+        if (lane == 0) s_best[i] = best;
+    }
+    __syncthreads();
+    if (warp != 0) return;
     bool ok = true;
     for (int i = lane; i < R; i += 32) {
-        const int2 best = row_argmax(partial + (seq * R + i) * ntile, ntile);
-        const float v = __int_as_float(best.x);
+        const float v = __int_as_float(s_best[i].x);
         ok &= v == v;
-        a[i] = best.y;
     }
     for (int i = lane; i < gamma; i += 32) {
         const int32_t xi = x[seq * gamma + i];
@@ -124,18 +115,17 @@ __global__ void __launch_bounds__(128)
         if (lane == 0) accepted_len[seq] = -1;
         return;
     }
-    __syncwarp();
     int n = gamma;
     for (int i0 = 0; i0 < gamma; i0 += 32) {
         const int i = i0 + lane;
-        const bool miss = i < gamma && x[seq * gamma + i] != a[i];
+        const bool miss = i < gamma && x[seq * gamma + i] != s_best[i].y;
         const unsigned m = __ballot_sync(0xFFFFFFFFu, miss);
         if (m) {
             n = i0 + __ffs(m) - 1;
             break;
         }
     }
-    for (int i = lane; i < R; i += 32) out[i] = i < n ? x[seq * gamma + i] : (i == n ? a[n] : -1);
+    for (int i = lane; i < R; i += 32) out[i] = i < n ? x[seq * gamma + i] : (i == n ? s_best[n].y : -1);
     if (lane == 0) accepted_len[seq] = n;
 }
 
@@ -149,21 +139,28 @@ __global__ void __launch_bounds__(kTreeThreads)
                          int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_path) {
     extern __shared__ int s_tree[];  // a[N], par[N], tok[N]
     __shared__ int red[kWarps];
+    griddep_launch_next();
     int *a = s_tree, *par = s_tree + N, *tok = s_tree + 2 * N;
     const int64_t seq = blockIdx.x;
     const int W = max_depth + 1;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int tree_ok = 1, seq_ok = 1;
-    for (int v = threadIdx.x; v < N; v += kTreeThreads) {
+    for (int v = threadIdx.x; v < N; v += kTreeThreads) {  // inputs of the call: before the wait
         const int p = parent[v];
         par[v] = p;
         tree_ok &= v == 0 ? p == -1 : (p >= 0 && p < v);
-        const int2 best = row_argmax(partial + (seq * N + v) * ntile, ntile);
-        const float val = __int_as_float(best.x);
-        seq_ok &= val == val;
-        a[v] = best.y;
         const int tk = node_tokens[seq * N + v];
         tok[v] = tk;
         if (v > 0) seq_ok &= tk >= 0 && tk < V;
+    }
+    griddep_wait();
+    for (int v = warp; v < N; v += kTreeThreads / 32) {  // node v's argmax: one warp per row
+        const int2 best = warp_merge_argmax(partial + (seq * N + v) * ntile, ntile, lane);
+        if (lane == 0) {
+            const float val = __int_as_float(best.x);
+            seq_ok &= val == val;
+            a[v] = best.y;
+        }
     }
     tree_ok = __syncthreads_and(tree_ok);
     seq_ok = __syncthreads_and(seq_ok);
@@ -229,12 +226,9 @@ cudaError_t launch_argmax_tiles(int dtype, bool vec, Logits t, int R, int B, int
 cudaError_t launch_greedy_finalize(int B, int gamma, int V, int ntile, const void *partial,
                                    const int32_t *x, int32_t *accepted_len, int32_t *out_tokens,
                                    cudaStream_t s) {
-    const unsigned grid = unsigned((int64_t(B) * 32 + 127) / 128);
-    const size_t smem = size_t(4) * (gamma + 1) * sizeof(int);
-    greedy_finalize_kernel<<<grid, 128, smem, s>>>(B, gamma, V, ntile,
-                                                   static_cast<const int2 *>(partial), x,
-                                                   accepted_len, out_tokens);
-    return cudaGetLastError();
+    const size_t smem = size_t(gamma + 1) * sizeof(int2);
+    return launch_after(greedy_finalize_kernel, unsigned(B), kThreads, smem, s, B, gamma, V, ntile,
+                        static_cast<const int2 *>(partial), x, accepted_len, out_tokens);
 }
 
 cudaError_t launch_tree_finalize(int B, int N, int V, int ntile, const void *partial,
@@ -242,10 +236,9 @@ cudaError_t launch_tree_finalize(int B, int N, int V, int ntile, const void *par
                                  int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
                                  cudaStream_t s) {
     const size_t smem = size_t(3) * N * sizeof(int);
-    tree_finalize_kernel<<<unsigned(B), kTreeThreads, smem, s>>>(
-        B, N, V, ntile, static_cast<const int2 *>(partial), parent, node_tokens, max_depth,
-        accepted_len, out_tokens, out_path);
-    return cudaGetLastError();
+    return launch_after(tree_finalize_kernel, unsigned(B), kTreeThreads, smem, s, B, N, V, ntile,
+                        static_cast<const int2 *>(partial), parent, node_tokens, max_depth, accepted_len,
+                        out_tokens, out_path);
 }
 
 }  // namespace sv

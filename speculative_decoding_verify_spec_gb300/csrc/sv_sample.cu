@@ -59,6 +59,7 @@ template <class D, bool VEC>
 __global__ void __launch_bounds__(kThreads, 4)
     stats_tiles_kernel(Logits a, int rows_a, Logits bt, int R, int V, int ntile, int64_t items, float c,
                        float2 *__restrict__ partial) {
+    griddep_launch_next();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = int64_t(gridDim.x) * kWarps;
     for (TileWalk w(int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5), nwarps, R, ntile); w.it < items;
@@ -81,52 +82,47 @@ __global__ void __launch_bounds__(kThreads, 4)
     }
 }
 
-// Merge n tile partials in tile order (one lane); loads go out kMergeBatch at a time so a
-// row costs a few round trips to L2.
-constexpr int kMergeBatch = 16;
-__device__ float2 merge_row(const float2 *__restrict__ p, int n, float c) {
-    float2 s = make_float2(-__int_as_float(0x7f800000), 0.f);
-    for (int q0 = 0; q0 < n; q0 += kMergeBatch) {
-        float2 e[kMergeBatch];
-#pragma unroll
-        for (int q = 0; q < kMergeBatch; ++q) e[q] = q0 + q < n ? p[q0 + q] : make_float2(0.f, 0.f);
-#pragma unroll
-        for (int q = 0; q < kMergeBatch; ++q)
-            if (q0 + q < n) s = q0 + q == 0 ? e[q] : merge_stats(s, e[q], c);
-    }
-    return s;
-}
-
 // ------------------------------------------------------------------------------------
+// Decide, one CTA per sequence: warp w merges the tile partials of rows w, w + kDecideWarps,
+// ... into (M, S); warp 0 then runs the accept scan.
+constexpr int kDecideWarps = 16;
 template <class D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kDecideWarps * 32)
     decide_kernel(Logits t, Logits d, int B, int gamma, int V, int ntile, float c,
                   const int32_t *__restrict__ x, uint64_t seed, uint64_t offset,
                   const float2 *__restrict__ partial, float2 *__restrict__ rowstat,
                   int2 *__restrict__ plan, int32_t *__restrict__ accepted_len,
                   int32_t *__restrict__ out_tokens) {
-    const int lane = threadIdx.x & 31;
-    const int64_t seq = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (seq >= B) return;
+    extern __shared__ float2 s_stat[];  // [2 gamma + 1]
+    griddep_launch_next();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t seq = blockIdx.x;
     const int R = 2 * gamma + 1;
 
-    // the accept test's operands for the first 32 drafts do not depend on the statistics:
-    // their loads go out first and overlap the merge
+    // the accept test's operands for the first 32 drafts do not depend on the statistics
+    // (nor on an earlier kernel): their loads go out before the wait
     int32_t x0 = 0;
     float tx0 = 0.f, dx0 = 0.f;
-    if (lane < gamma) {
+    if (warp == 0 && lane < gamma) {
         x0 = x[seq * gamma + lane];
         if (x0 >= 0 && x0 < V) {
             tx0 = load_elem<D>(row_ptr(t, D::kBytes, seq, lane), x0);
             dx0 = load_elem<D>(row_ptr(d, D::kBytes, seq, lane), x0);
         }
     }
-    bool ok = true;
-    for (int r = lane; r < R; r += 32) {
-        const float2 s = merge_row(partial + (seq * R + r) * ntile, ntile, c);
-        rowstat[seq * R + r] = s;
-        ok &= is_finite(s.x);
+    griddep_wait();
+    for (int r = warp; r < R; r += kDecideWarps) {
+        const float2 st = warp_merge_stats(partial + (seq * R + r) * ntile, ntile, c, lane);
+        if (lane == 0) {
+            s_stat[r] = st;
+            rowstat[seq * R + r] = st;
+        }
     }
+    __syncthreads();
+    if (warp != 0) return;
+
+    bool ok = true;
+    for (int r = lane; r < R; r += 32) ok &= is_finite(s_stat[r].x);
     for (int i = lane; i < gamma; i += 32) {
         const int32_t xi = i == lane ? x0 : x[seq * gamma + i];
         ok &= xi >= 0 && xi < V;
@@ -141,15 +137,14 @@ __global__ void __launch_bounds__(128)
         }
         return;
     }
-    __syncwarp();  // rowstat written by other lanes of this warp is read below
 
     int k = gamma;
     for (int i0 = 0; i0 < gamma; i0 += 32) {
         const int i = i0 + lane;
         bool reject = false;
         if (i < gamma) {
-            const float2 st = rowstat[seq * R + i];
-            const float2 sd = rowstat[seq * R + gamma + 1 + i];
+            const float2 st = s_stat[i];
+            const float2 sd = s_stat[gamma + 1 + i];
             float tx = tx0, dx = dx0;
             if (i0 > 0) {
                 const int32_t xi = x[seq * gamma + i];
@@ -180,41 +175,52 @@ __global__ void __launch_bounds__(128)
 // ------------------------------------------------------------------------------------
 // Residual masses: csum[seq * nrt + tile] = sum over the residual tile of (p - q)+ at the
 // stop row, for the sequences that rejected (plan mode 1); other entries are not written.
+// Persistent, with blocked work: warp w takes the items [w * per, (w + 1) * per), i.e.
+// runs of consecutive tiles of one or two sequences, so a sequence's plan and statistics
+// are read once per run and the warp's loads walk along the row.
 template <class D, bool VEC>
 __global__ void __launch_bounds__(kThreads, 4)
-    residual_tiles_kernel(Logits t, Logits d, int gamma, int V, int nrt, int64_t items, float c,
+    residual_tiles_kernel(Logits t, Logits d, int gamma, int V, int nrt, int64_t items, int64_t per, float c,
                           const float2 *__restrict__ rowstat, const int2 *__restrict__ plan,
                           float *__restrict__ csum) {
+    griddep_launch_next();
+    griddep_wait();
     const int lane = threadIdx.x & 31;
-    const int64_t nwarps = int64_t(gridDim.x) * kWarps;
     const int R = 2 * gamma + 1;
-    for (TileWalk w(int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5), nwarps, 1, nrt); w.it < items;
-         w.next(nwarps)) {
-        const int2 pl = plan[w.seq];
-        if (pl.y != 1) continue;  // uniform over the warp
-        const int k = pl.x;
-        const float2 st = rowstat[w.seq * R + k], sd = rowstat[w.seq * R + gamma + 1 + k];
-        const char *tp = row_ptr(t, D::kBytes, w.seq, k);
-        const char *dp = row_ptr(d, D::kBytes, w.seq, k);
-        const int64_t c0 = int64_t(w.tile) * res_tile_elems<D>();
-        const int len = unit_len(V, c0, res_tile_elems<D>());
-        uint4 tv[kResVecs], dv[kResVecs];
+    int64_t it = (int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5)) * per;
+    const int64_t end = it + per < items ? it + per : items;
+    while (it < end) {
+        const int64_t seq = it / nrt;
+        const int64_t run_end = (seq + 1) * nrt < end ? (seq + 1) * nrt : end;
+        const int2 pl = plan[seq];
+        if (pl.y == 1) {  // uniform over the warp
+            const int k = pl.x;
+            const float2 st = rowstat[seq * R + k], sd = rowstat[seq * R + gamma + 1 + k];
+            const float inv_st = 1.f / st.y, inv_sd = 1.f / sd.y;
+            const char *tp = row_ptr(t, D::kBytes, seq, k);
+            const char *dp = row_ptr(d, D::kBytes, seq, k);
+            for (; it < run_end; ++it) {
+                const int64_t c0 = (it - seq * nrt) * res_tile_elems<D>();
+                const int len = unit_len(V, c0, res_tile_elems<D>());
+                uint4 tv[kResVecs], dv[kResVecs];
 #pragma unroll
-        for (int u = 0; u < kResVecs; ++u) {
-            const int e0 = (lane + 32 * u) * D::EPV;
-            tv[u] = e0 < len ? load_vec<D, VEC>(tp, c0, e0, len) : neg_inf_vec<D>();
-            dv[u] = e0 < len ? load_vec<D, VEC>(dp, c0, e0, len) : neg_inf_vec<D>();
+                for (int u = 0; u < kResVecs; ++u) {
+                    const int e0 = (lane + 32 * u) * D::EPV;
+                    tv[u] = e0 < len ? load_vec<D, VEC>(tp, c0, e0, len) : neg_inf_vec<D>();
+                    dv[u] = e0 < len ? load_vec<D, VEC>(dp, c0, e0, len) : neg_inf_vec<D>();
+                }
+                float acc = 0.f;
+#pragma unroll
+                for (int u = 0; u < kResVecs; ++u)
+#pragma unroll
+                    for (int e = 0; e < D::EPV; ++e)
+                        acc += residual_weight(vec_elem<D>(tv[u], e), vec_elem<D>(dv[u], e), c, st.x, inv_st,
+                                               sd.x, inv_sd);
+                const float mass = warp_reduce(acc, [](float x, float y) { return x + y; });
+                if (lane == 0) csum[it] = mass;
+            }
         }
-        const float inv_st = 1.f / st.y, inv_sd = 1.f / sd.y;
-        float acc = 0.f;
-#pragma unroll
-        for (int u = 0; u < kResVecs; ++u)
-#pragma unroll
-            for (int e = 0; e < D::EPV; ++e)
-                acc += residual_weight(vec_elem<D>(tv[u], e), vec_elem<D>(dv[u], e), c, st.x, inv_st, sd.x,
-                                       inv_sd);
-        const float mass = warp_reduce(acc, [](float x, float y) { return x + y; });
-        if (lane == 0) csum[w.it] = mass;
+        it = run_end;
     }
 }
 
@@ -231,6 +237,8 @@ __global__ void __launch_bounds__(128)
                 uint64_t offset, const float2 *__restrict__ partial, const float2 *__restrict__ rowstat,
                 const int2 *__restrict__ plan, const float *__restrict__ csum,
                 int32_t *__restrict__ out_tokens) {
+    griddep_launch_next();
+    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t seq = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     if (seq >= B) return;
@@ -370,9 +378,13 @@ __global__ void __launch_bounds__(128)
 __global__ void rowstats_finalize_kernel(int rows, int ntile, float c, float inv_t,
                                          const float2 *__restrict__ partial, float *__restrict__ m_out,
                                          float *__restrict__ lse_out) {
-    const int64_t r = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    griddep_launch_next();
+    griddep_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;  // one warp per row
     if (r >= rows) return;
-    const float2 s = merge_row(partial + r * ntile, ntile, c);
+    const float2 s = warp_merge_stats(partial + r * ntile, ntile, c, lane);
+    if (lane != 0) return;
     if (is_finite(s.x)) {
         const float m = s.x * inv_t;
         m_out[r] = m;
@@ -418,11 +430,11 @@ cudaError_t launch_decide(int dtype, Logits t, Logits d, int B, int gamma, int V
                           float c, const int32_t *x, uint64_t seed, uint64_t offset,
                           const void *partial, void *rowstat, void *plan, int32_t *accepted_len,
                           int32_t *out_tokens, cudaStream_t s) {
-    const unsigned grid = unsigned((int64_t(B) * 32 + 127) / 128);
     auto k = dtype == 1 ? decide_kernel<BF16> : decide_kernel<F32>;
-    k<<<grid, 128, 0, s>>>(t, d, B, gamma, V, ntile, c, x, seed, offset, static_cast<const float2 *>(partial),
-                           static_cast<float2 *>(rowstat), static_cast<int2 *>(plan), accepted_len, out_tokens);
-    return cudaGetLastError();
+    const size_t smem = size_t(2 * gamma + 1) * sizeof(float2);
+    return launch_after(k, unsigned(B), kDecideWarps * 32, smem, s, t, d, B, gamma, V, ntile, c, x, seed, offset,
+                        static_cast<const float2 *>(partial), static_cast<float2 *>(rowstat),
+                        static_cast<int2 *>(plan), accepted_len, out_tokens);
 }
 
 cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V,
@@ -434,9 +446,10 @@ cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B
     unsigned grid = 0;
     cudaError_t e = persistent_grid(k, items, &grid);
     if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, 0, s>>>(t, d, gamma, V, nrt, items, c, static_cast<const float2 *>(rowstat),
-                                static_cast<const int2 *>(plan), csum);
-    return cudaGetLastError();
+    const int64_t nwarps = int64_t(grid) * kWarps;
+    const int64_t per = (items + nwarps - 1) / nwarps;
+    return launch_after(k, grid, kThreads, 0, s, t, d, gamma, V, nrt, items, per, c,
+                        static_cast<const float2 *>(rowstat), static_cast<const int2 *>(plan), csum);
 }
 
 cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
@@ -445,18 +458,16 @@ cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamm
     const unsigned grid = unsigned((int64_t(B) * 32 + 127) / 128);
     auto k = pick(dtype, vec, draw_kernel<BF16, true>, draw_kernel<BF16, false>, draw_kernel<F32, true>,
                   draw_kernel<F32, false>);
-    k<<<grid, 128, 0, s>>>(t, d, B, gamma, V, ntile, nrt, c, seed, offset, static_cast<const float2 *>(partial),
-                           static_cast<const float2 *>(rowstat), static_cast<const int2 *>(plan), csum,
-                           out_tokens);
-    return cudaGetLastError();
+    return launch_after(k, grid, 128, 0, s, t, d, B, gamma, V, ntile, nrt, c, seed, offset,
+                        static_cast<const float2 *>(partial), static_cast<const float2 *>(rowstat),
+                        static_cast<const int2 *>(plan), csum, out_tokens);
 }
 
 cudaError_t launch_rowstats_finalize(int rows, int ntile, float c, float inv_t, const void *partial,
                                      float *m_out, float *lse_out, cudaStream_t s) {
-    const unsigned grid = unsigned((int64_t(rows) + 255) / 256);
-    rowstats_finalize_kernel<<<grid, 256, 0, s>>>(rows, ntile, c, inv_t,
-                                                  static_cast<const float2 *>(partial), m_out, lse_out);
-    return cudaGetLastError();
+    const unsigned grid = unsigned((int64_t(rows) * 32 + 255) / 256);
+    return launch_after(rowstats_finalize_kernel, grid, 256, 0, s, rows, ntile, c, inv_t,
+                        static_cast<const float2 *>(partial), m_out, lse_out);
 }
 
 cudaError_t launch_uniforms(uint64_t seed, uint64_t offset, int B, int positions, int purpose,
