@@ -35,8 +35,8 @@ SECONDARY = ["greedy_b512", "tree_b64"]
 METRIC = "verified seqs/s"
 UNIT = "seqs/s"
 FALLBACK_HBM_GBS = 6800.0
-DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "argmax_tiles_kernel",
-                   "tree": "argmax_tiles_kernel"}
+DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "max_tiles_kernel",
+                   "tree": "max_tiles_kernel"}
 STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
 STAGES = {"sample": ["row_stats", "decide", "residual_mass", "inverse_cdf"],
           "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"]}

@@ -152,12 +152,12 @@ sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_str
  * For callers that cannot hand the library device memory -- code running inside another
  * runtime's execution step whose framework owns every buffer, or a serving loop that must
  * not call cudaMalloc once it is running.  Same arguments, rules and results as
- * spec_verify_greedy, minus the workspace: the per-tile partials live in a fixed,
+ * spec_verify_greedy, minus the workspace: the per-tile maxima live in a fixed,
  * 256-byte-aligned device array of SV_NOALLOC_SCRATCH_BYTES that is part of the library and
  * stays resident on every GPU that loads it until the process exits.
- *   - Limit: B * (gamma + 1) * ceil(V / tile) * 8 <= SV_NOALLOC_SCRATCH_BYTES, with tile =
+ *   - Limit: B * (gamma + 1) * ceil(V / tile) * 4 <= SV_NOALLOC_SCRATCH_BYTES, with tile =
  *     2048 logits for bf16 and 1024 for fp32 (4 MiB covers, e.g., B = 512, gamma = 6,
- *     V = 152064 bf16: 2.2 MB).  Larger problems return SV_ERR_WORKSPACE before anything is
+ *     V = 152064 bf16: 1.1 MB).  Larger problems return SV_ERR_WORKSPACE before anything is
  *     enqueued.
  *   - The first call on a device looks up the array's device address (once per device,
  *     with that device current); make that first call before any stream capture.
@@ -195,7 +195,7 @@ sv_status spec_verify_uniforms(uint64_t seed, uint64_t offset, int B, int positi
  * spec_verify_sample / _greedy / _tree_greedy on this thread records events[0] on its
  * stream before its first kernel and events[s] after its s-th kernel (s = 1 .. n_events-1;
  * sampling has 4 kernels: row statistics, decide, residual masses, inverse-CDF draw; greedy
- * and tree have 2: argmax partials, finalize).  The events are cudaEvent_t handles created
+ * and tree have 2: tile maxima, finalize).  The events are cudaEvent_t handles created
  * and owned by the caller; recording them adds no synchronisation.  Pass NULL (or 0) to
  * turn it off.  Returns SV_ERR_INVALID_ARG for n_events < 0 or > 8.
  */

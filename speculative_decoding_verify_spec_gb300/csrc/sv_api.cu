@@ -35,8 +35,8 @@ struct Layout {
 };
 
 // Workspace regions (each 256-byte aligned):
-//   partial  per (row, 4 KB tile): float2 (M, S) for sampling / row stats, int2 (value,
-//            index) for greedy / tree;
+//   partial  per (row, 4 KB tile): float2 (M, S) for sampling / row stats, the float
+//            maximum for greedy / tree;
 //   rowstat  per row: float2 (M, S)                             (sampling only)
 //   plan     per sequence: int2 (stop row k, mode)              (sampling only)
 //   csum     per (sequence, 2 KB residual tile): residual mass  (sampling only)
@@ -187,10 +187,11 @@ sv_status spec_verify_greedy(const void *target_logits, int64_t t_batch_stride,
     void *partial = at(workspace, L.partial);
     cudaError_t e = mark(0, s);
     if (e == cudaSuccess)
-        e = sv::launch_argmax_tiles(dtype == SV_BF16, vec, t, gamma + 1, B, V, ntile, partial, s);
+        e = sv::launch_max_tiles(dtype == SV_BF16, vec, t, gamma + 1, B, V, ntile, partial, s);
     if (e == cudaSuccess) e = mark(1, s);
     if (e == cudaSuccess)
-        e = sv::launch_greedy_finalize(B, gamma, V, ntile, partial, draft_tokens, accepted_len,
+        e = sv::launch_greedy_finalize(dtype == SV_BF16, vec, t, B, gamma, V, ntile, partial, draft_tokens,
+                                       accepted_len,
                                        out_tokens, s);
     if (e == cudaSuccess) e = mark(2, s);
     return cuda_status(e);
@@ -220,10 +221,11 @@ sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_str
     void *partial = at(workspace, L.partial);
     cudaError_t e = mark(0, s);
     if (e == cudaSuccess)
-        e = sv::launch_argmax_tiles(dtype == SV_BF16, vec, t, N, B, V, ntile, partial, s);
+        e = sv::launch_max_tiles(dtype == SV_BF16, vec, t, N, B, V, ntile, partial, s);
     if (e == cudaSuccess) e = mark(1, s);
     if (e == cudaSuccess)
-        e = sv::launch_tree_finalize(B, N, V, ntile, partial, parent, node_tokens, max_depth,
+        e = sv::launch_tree_finalize(dtype == SV_BF16, vec, t, B, N, V, ntile, partial, parent, node_tokens,
+                                     max_depth,
                                      accepted_len, out_tokens, out_path, s);
     if (e == cudaSuccess) e = mark(2, s);
     return cuda_status(e);

@@ -10,12 +10,16 @@
 // Exercise 5, verify_tree_greedy).
 //
 // GPU decomposition:
-//   argmax_tiles     persistent: every 4 KB tile of every row, one warp per tile:
-//                    NaN-propagating max and its lowest index.
-//   greedy_finalize  one warp per sequence: merge tiles, longest matching prefix.
-//   tree_finalize    one CTA per sequence: merge tiles for all N nodes, validate the
+//   max_tiles        persistent: every 4 KB tile of every row, one warp per tile: the
+//                    tile's NaN-propagating maximum.
+//   greedy_finalize  one CTA per sequence, one warp per row: the row maximum and the lowest
+//                    tile holding it, then the first position of that value inside that one
+//                    tile (re-read, 4 KB); then the longest matching prefix.
+//   tree_finalize    one CTA per sequence: the same argmax for all N nodes, validate the
 //                    tree, accepted flags by walking each node's root path, deepest node
 //                    (lowest index on ties), write the path.
+// Searching for the index only inside the winning tile keeps the streaming pass as cheap
+// as a plain maximum.
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -28,7 +32,7 @@ __device__ __forceinline__ const char *row_ptr(const Logits &L, int bytes, int64
 
 template <class D, bool VEC>
 __global__ void __launch_bounds__(kThreads, 4)
-    argmax_tiles_kernel(Logits t, int R, int V, int ntile, int64_t items, int2 *__restrict__ partial) {
+    max_tiles_kernel(Logits t, int R, int V, int ntile, int64_t items, float *__restrict__ partial) {
     griddep_launch_next();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = int64_t(gridDim.x) * kWarps;
@@ -44,47 +48,59 @@ __global__ void __launch_bounds__(kThreads, 4)
             v[u] = e0 < len ? load_vec<D, VEC>(rp, c0, e0, len)
                             : make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
         }
-        // the tile's maximum first (NaN-propagating), then the lowest index holding it,
-        // branch-free in two steps: the first of this lane's vectors whose maximum is the
-        // tile max, then the first element of that vector equal to it (reverse scans with
-        // selects, so the last match written is the lowest index)
-        const float bm = warp_reduce(thread_max<D>(v), [](float a, float b) { return max_nan(a, b); });
-        int idx = kNoIndex;
-        if (bm == bm) {
-            int uhit = -1;
-#pragma unroll
-            for (int u = kTileVecs - 1; u >= 0; --u) {
-                float vm;
-                if constexpr (D::EPV == 8) {
-                    const uint32_t mw = vec_max_word<BF16>(v[u]);
-                    vm = max_nan(bf16_lo(mw), bf16_hi(mw));
-                } else {
-                    vm = max_nan(max_nan(__uint_as_float(v[u].x), __uint_as_float(v[u].y)),
-                                 max_nan(__uint_as_float(v[u].z), __uint_as_float(v[u].w)));
-                }
-                uhit = vm == bm ? u : uhit;
-            }
-            if (uhit >= 0) {
-                uint4 hv = v[0];
-#pragma unroll
-                for (int u = 1; u < kTileVecs; ++u) hv = uhit == u ? v[u] : hv;
-                const int e0 = (lane + 32 * uhit) * D::EPV;
-#pragma unroll
-                for (int e = D::EPV - 1; e >= 0; --e) {
-                    const bool hit = vec_elem<D>(hv, e) == bm && e0 + e < len;
-                    idx = hit ? int(c0) + e0 + e : idx;
-                }
-            }
-        }
-        idx = warp_reduce(idx, [](int a, int b) { return min(a, b); });
-        if (lane == 0) partial[w.it] = make_int2(__float_as_int(bm), idx);
+        const float m = warp_reduce(thread_max<D>(v), [](float a, float b) { return max_nan(a, b); });
+        if (lane == 0) partial[w.it] = m;
     }
 }
 
-// Greedy finalize, one CTA per sequence: warp w merges the tile partials of rows w, w + 8,
-// ...; warp 0 then finds the longest matching prefix.
+// The argmax of one row (one warp; every lane returns it): the largest tile maximum, on
+// ties the lowest tile (a NaN maximum marks bad data and absorbs everything), then the
+// first position of that value inside that tile, read again from the row.  Returns (value
+// bits, index).
+template <class D, bool VEC>
+__device__ int2 warp_row_argmax(const float *__restrict__ tmax, int ntile, const char *row, int V, int lane) {
+    int2 best = make_int2(__float_as_int(-__int_as_float(0x7f800000)), kNoIndex);
+    for (int q0 = lane; q0 < ntile; q0 += 128) {
+        float e[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) e[j] = q0 + 32 * j < ntile ? tmax[q0 + 32 * j] : -__int_as_float(0x7f800000);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (q0 + 32 * j < ntile) best = merge_argmax(best, make_int2(__float_as_int(e[j]), q0 + 32 * j));
+    }
+    best = warp_reduce(best, [](int2 a, int2 b) { return merge_argmax(a, b); });
+    const float bm = __int_as_float(best.x);
+    if (bm != bm) return make_int2(best.x, -1);
+    const int64_t c0 = int64_t(best.y) * tile_elems<D>();
+    const int len = unit_len(V, c0, tile_elems<D>());
+    uint4 v[kTileVecs];
+#pragma unroll
+    for (int u = 0; u < kTileVecs; ++u) {
+        const int e0 = (lane + 32 * u) * D::EPV;
+        v[u] = e0 < len ? load_vec<D, VEC>(row, c0, e0, len)
+                        : make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
+    }
+    // lane-local first match (lane l holds vectors l, l + 32, ... in index order), then the
+    // lowest over the lanes; reverse scans with selects keep the lowest match
+    int idx = kNoIndex;
+#pragma unroll
+    for (int u = kTileVecs - 1; u >= 0; --u) {
+        const int e0 = (lane + 32 * u) * D::EPV;
+#pragma unroll
+        for (int e = D::EPV - 1; e >= 0; --e) {
+            const bool hit = vec_elem<D>(v[u], e) == bm && e0 + e < len;
+            idx = hit ? int(c0) + e0 + e : idx;
+        }
+    }
+    idx = warp_reduce(idx, [](int a, int b) { return min(a, b); });
+    return make_int2(best.x, idx);
+}
+
+// Greedy finalize, one CTA per sequence: warp w finds the argmax of rows w, w + 8, ...;
+// warp 0 then finds the longest matching prefix.
+template <class D, bool VEC>
 __global__ void __launch_bounds__(kThreads)
-    greedy_finalize_kernel(int B, int gamma, int V, int ntile, const int2 *__restrict__ partial,
+    greedy_finalize_kernel(Logits t, int B, int gamma, int V, int ntile, const float *__restrict__ partial,
                            const int32_t *__restrict__ x, int32_t *__restrict__ accepted_len,
                            int32_t *__restrict__ out_tokens) {
     extern __shared__ int2 s_best[];  // [gamma + 1]
@@ -94,7 +110,8 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t seq = blockIdx.x;
     const int R = gamma + 1;
     for (int i = warp; i < R; i += kWarps) {
-        const int2 best = warp_merge_argmax(partial + (seq * R + i) * ntile, ntile, lane);
+        const int2 best = warp_row_argmax<D, VEC>(partial + (seq * R + i) * ntile, ntile,
+                                                  row_ptr(t, D::kBytes, seq, i), V, lane);
         if (lane == 0) s_best[i] = best;
     }
     __syncthreads();
@@ -132,8 +149,9 @@ __global__ void __launch_bounds__(kThreads)
 constexpr int kTreeThreads = 256;
 constexpr int kKeyShift = 11;  // node index < 2^11 (SV_MAX_TREE_NODES = 1024)
 
+template <class D, bool VEC>
 __global__ void __launch_bounds__(kTreeThreads)
-    tree_finalize_kernel(int B, int N, int V, int ntile, const int2 *__restrict__ partial,
+    tree_finalize_kernel(Logits t, int B, int N, int V, int ntile, const float *__restrict__ partial,
                          const int32_t *__restrict__ parent, const int32_t *__restrict__ node_tokens,
                          int max_depth, int32_t *__restrict__ accepted_len,
                          int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_path) {
@@ -155,7 +173,8 @@ __global__ void __launch_bounds__(kTreeThreads)
     }
     griddep_wait();
     for (int v = warp; v < N; v += kTreeThreads / 32) {  // node v's argmax: one warp per row
-        const int2 best = warp_merge_argmax(partial + (seq * N + v) * ntile, ntile, lane);
+        const int2 best = warp_row_argmax<D, VEC>(partial + (seq * N + v) * ntile, ntile,
+                                                  row_ptr(t, D::kBytes, seq, v), V, lane);
         if (lane == 0) {
             const float val = __int_as_float(best.x);
             seq_ok &= val == val;
@@ -211,33 +230,37 @@ __global__ void __launch_bounds__(kTreeThreads)
 
 }  // namespace
 
-cudaError_t launch_argmax_tiles(int dtype, bool vec, Logits t, int R, int B, int V, int ntile,
-                                void *partial, cudaStream_t s) {
+cudaError_t launch_max_tiles(int dtype, bool vec, Logits t, int R, int B, int V, int ntile, void *partial,
+                             cudaStream_t s) {
     const int64_t items = int64_t(B) * R * ntile;
-    auto k = dtype == 1 ? (vec ? argmax_tiles_kernel<BF16, true> : argmax_tiles_kernel<BF16, false>)
-                        : (vec ? argmax_tiles_kernel<F32, true> : argmax_tiles_kernel<F32, false>);
+    auto k = dtype == 1 ? (vec ? max_tiles_kernel<BF16, true> : max_tiles_kernel<BF16, false>)
+                        : (vec ? max_tiles_kernel<F32, true> : max_tiles_kernel<F32, false>);
     unsigned grid = 0;
     cudaError_t e = persistent_grid(k, items, &grid);
     if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, 0, s>>>(t, R, V, ntile, items, static_cast<int2 *>(partial));
+    k<<<grid, kThreads, 0, s>>>(t, R, V, ntile, items, static_cast<float *>(partial));
     return cudaGetLastError();
 }
 
-cudaError_t launch_greedy_finalize(int B, int gamma, int V, int ntile, const void *partial,
-                                   const int32_t *x, int32_t *accepted_len, int32_t *out_tokens,
-                                   cudaStream_t s) {
+cudaError_t launch_greedy_finalize(int dtype, bool vec, Logits t, int B, int gamma, int V, int ntile,
+                                   const void *partial, const int32_t *x, int32_t *accepted_len,
+                                   int32_t *out_tokens, cudaStream_t s) {
     const size_t smem = size_t(gamma + 1) * sizeof(int2);
-    return launch_after(greedy_finalize_kernel, unsigned(B), kThreads, smem, s, B, gamma, V, ntile,
-                        static_cast<const int2 *>(partial), x, accepted_len, out_tokens);
+    auto k = dtype == 1 ? (vec ? greedy_finalize_kernel<BF16, true> : greedy_finalize_kernel<BF16, false>)
+                        : (vec ? greedy_finalize_kernel<F32, true> : greedy_finalize_kernel<F32, false>);
+    return launch_after(k, unsigned(B), kThreads, smem, s, t, B, gamma, V, ntile,
+                        static_cast<const float *>(partial), x, accepted_len, out_tokens);
 }
 
-cudaError_t launch_tree_finalize(int B, int N, int V, int ntile, const void *partial,
-                                 const int32_t *parent, const int32_t *node_tokens, int max_depth,
-                                 int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
+cudaError_t launch_tree_finalize(int dtype, bool vec, Logits t, int B, int N, int V, int ntile,
+                                 const void *partial, const int32_t *parent, const int32_t *node_tokens,
+                                 int max_depth, int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
                                  cudaStream_t s) {
     const size_t smem = size_t(3) * N * sizeof(int);
-    return launch_after(tree_finalize_kernel, unsigned(B), kTreeThreads, smem, s, B, N, V, ntile,
-                        static_cast<const int2 *>(partial), parent, node_tokens, max_depth, accepted_len,
+    auto k = dtype == 1 ? (vec ? tree_finalize_kernel<BF16, true> : tree_finalize_kernel<BF16, false>)
+                        : (vec ? tree_finalize_kernel<F32, true> : tree_finalize_kernel<F32, false>);
+    return launch_after(k, unsigned(B), kTreeThreads, smem, s, t, B, N, V, ntile,
+                        static_cast<const float *>(partial), parent, node_tokens, max_depth, accepted_len,
                         out_tokens, out_path);
 }
 

@@ -41,15 +41,17 @@ cudaError_t launch_uniforms(uint64_t seed, uint64_t offset, int B, int positions
                             float *out, cudaStream_t s);
 
 // Greedy / tree path ------------------------------------------------------------------
-// Argmax partial (value, lowest index) per (row, 4 KB tile) of [B][R][V].
-cudaError_t launch_argmax_tiles(int dtype, bool vec, Logits t, int R, int B, int V, int ntile,
-                                void *partial, cudaStream_t s);
-cudaError_t launch_greedy_finalize(int B, int gamma, int V, int ntile, const void *partial,
-                                   const int32_t *x, int32_t *accepted_len, int32_t *out_tokens,
-                                   cudaStream_t s);
-cudaError_t launch_tree_finalize(int B, int N, int V, int ntile, const void *partial,
-                                 const int32_t *parent, const int32_t *node_tokens, int max_depth,
-                                 int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
+// The NaN-propagating maximum of every (row, 4 KB tile) of [B][R][V]: partial[row * ntile + tile].
+cudaError_t launch_max_tiles(int dtype, bool vec, Logits t, int R, int B, int V, int ntile, void *partial,
+                             cudaStream_t s);
+// Row argmax from the tile maxima (the first position of the maximum, searched in the
+// lowest tile that holds it), then the accept rule; both read t again for that one tile.
+cudaError_t launch_greedy_finalize(int dtype, bool vec, Logits t, int B, int gamma, int V, int ntile,
+                                   const void *partial, const int32_t *x, int32_t *accepted_len,
+                                   int32_t *out_tokens, cudaStream_t s);
+cudaError_t launch_tree_finalize(int dtype, bool vec, Logits t, int B, int N, int V, int ntile,
+                                 const void *partial, const int32_t *parent, const int32_t *node_tokens,
+                                 int max_depth, int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
                                  cudaStream_t s);
 
 }  // namespace sv

@@ -1,6 +1,6 @@
 // sv_noalloc.cu -- greedy verification for callers that cannot allocate device memory.
 //
-// spec_verify_greedy needs a caller-provided workspace for its per-tile argmax partials.
+// spec_verify_greedy needs a caller-provided workspace for its per-tile maxima.
 // Some callers have no way to provide one: code that runs inside another runtime's
 // execution step (a plugin or custom op whose host framework owns every device buffer and
 // forbids allocation while a request is in flight), or a serving loop that must never call
@@ -76,16 +76,16 @@ extern "C" sv_status spec_verify_greedy_noalloc(const void *target_logits, int64
         return SV_ERR_INVALID_ARG;
     const int ntile = noalloc_ntile(V, dtype);
     const int64_t partials = int64_t(B) * (gamma + 1) * ntile;
-    if (partials * int64_t(sizeof(int2)) > int64_t(kNoallocScratchBytes))
+    if (partials * int64_t(sizeof(float)) > int64_t(kNoallocScratchBytes))
         return SV_ERR_WORKSPACE;  // larger than the fixed scratch: use spec_verify_greedy
     void *scratch = nullptr;
     if (sv_status st = scratch_address(&scratch)) return st;
     const bool vec = noalloc_vec_ok(target_logits, t_batch_stride, t_row_stride, dtype);
     const sv::Logits t{target_logits, t_batch_stride, t_row_stride};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = sv::launch_argmax_tiles(dtype == SV_BF16, vec, t, gamma + 1, B, V, ntile, scratch, s);
+    cudaError_t e = sv::launch_max_tiles(dtype == SV_BF16, vec, t, gamma + 1, B, V, ntile, scratch, s);
     if (e == cudaSuccess)
-        e = sv::launch_greedy_finalize(B, gamma, V, ntile, scratch, draft_tokens, accepted_len,
-                                       out_tokens, s);
+        e = sv::launch_greedy_finalize(dtype == SV_BF16, vec, t, B, gamma, V, ntile, scratch, draft_tokens,
+                                       accepted_len, out_tokens, s);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
