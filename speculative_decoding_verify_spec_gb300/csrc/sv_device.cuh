@@ -95,6 +95,16 @@ __device__ __forceinline__ float vec_elem<BF16>(const uint4 &v, int e) {
     return (e & 1) ? bf16_hi(w) : bf16_lo(w);
 }
 
+// A 16-byte read-only load that is not kept in L1 and asks L2 to fetch the surrounding
+// 256 bytes: logits are read once, in long runs.
+__device__ __forceinline__ uint4 ld_stream(const char *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 // ------------------------------------------------------------------------------------
 // Loading one 16-byte vector of a unit (tile).  `e0` is the element offset of the vector
 // inside the unit that starts at element c0, `len` the number of real elements in it.  A whole in-range vector of
@@ -103,8 +113,7 @@ __device__ __forceinline__ float vec_elem<BF16>(const uint4 &v, int e) {
 // ------------------------------------------------------------------------------------
 template <class D, bool VEC>
 __device__ __forceinline__ uint4 load_vec(const char *row, int64_t c0, int e0, int len) {
-    if (VEC && e0 + D::EPV <= len)
-        return __ldg(reinterpret_cast<const uint4 *>(row + (c0 + e0) * D::kBytes));
+    if (VEC && e0 + D::EPV <= len) return ld_stream(row + (c0 + e0) * D::kBytes);
     uint32_t w[4] = {D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord};
     if constexpr (D::EPV == 4) {
 #pragma unroll
@@ -235,8 +244,9 @@ __device__ __forceinline__ T warp_reduce(T v, Op op) {
     return v;
 }
 
-// Block-wide reduction; every thread returns the result.  `scratch` holds kWarps values.
-template <class T, class Op>
+// Block-wide reduction over a CTA of NW warps; every thread returns the result.
+// `scratch` holds NW values.
+template <int NW, class T, class Op>
 __device__ __forceinline__ T block_reduce(T v, Op op, T *scratch) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     v = warp_reduce(v, op);
@@ -245,7 +255,7 @@ __device__ __forceinline__ T block_reduce(T v, Op op, T *scratch) {
     __syncthreads();
     T r = scratch[0];
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) r = op(r, scratch[w]);
+    for (int w = 1; w < NW; ++w) r = op(r, scratch[w]);
     return r;
 }
 

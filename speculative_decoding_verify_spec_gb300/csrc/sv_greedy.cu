@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kThreads)
     if (lane == 0) accepted_len[seq] = n;
 }
 
-constexpr int kTreeThreads = 256;
+constexpr int kTreeThreads = 512;
 constexpr int kKeyShift = 11;  // node index < 2^11 (SV_MAX_TREE_NODES = 1024)
 
 template <class D, bool VEC>
@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(kTreeThreads)
                          int max_depth, int32_t *__restrict__ accepted_len,
                          int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_path) {
     extern __shared__ int s_tree[];  // a[N], par[N], tok[N]
-    __shared__ int red[kWarps];
+    constexpr int kTreeWarps = kTreeThreads / 32;
+    __shared__ int red[kTreeWarps];
     griddep_launch_next();
     int *a = s_tree, *par = s_tree + N, *tok = s_tree + 2 * N;
     const int64_t seq = blockIdx.x;
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kTreeThreads)
         if (v > 0) seq_ok &= tk >= 0 && tk < V;
     }
     griddep_wait();
-    for (int v = warp; v < N; v += kTreeThreads / 32) {  // node v's argmax: one warp per row
+    for (int v = warp; v < N; v += kTreeWarps) {  // node v's argmax: one warp per row
         const int2 best = warp_row_argmax<D, VEC>(partial + (seq * N + v) * ntile, ntile,
                                                   row_ptr(t, D::kBytes, seq, v), V, lane);
         if (lane == 0) {
@@ -199,8 +200,8 @@ __global__ void __launch_bounds__(kTreeThreads)
             if (kept) best_key = max(best_key, (d << kKeyShift) | ((1 << kKeyShift) - 1 - v));
         }
     }
-    max_d = block_reduce(max_d, [](int x, int y) { return max(x, y); }, red);
-    best_key = block_reduce(best_key, [](int x, int y) { return max(x, y); }, red);
+    max_d = block_reduce<kTreeWarps>(max_d, [](int x, int y) { return max(x, y); }, red);
+    best_key = block_reduce<kTreeWarps>(best_key, [](int x, int y) { return max(x, y); }, red);
     if (threadIdx.x != 0) return;
 
     int32_t *out = out_tokens + seq * W;
