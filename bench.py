@@ -38,7 +38,7 @@ FALLBACK_HBM_GBS = 6800.0
 DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "max_tiles_kernel",
                    "tree": "max_tiles_kernel"}
 STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
-STAGES = {"sample": ["row_stats", "decide", "residual_mass", "inverse_cdf"],
+STAGES = {"sample": ["row_stats", "decide", "residual_mass", "inverse_cdf", "redraw"],
           "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"]}
 
 
@@ -258,7 +258,7 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
     call, outs = make_call(name, inputs, dev, **ov)
     nst = len(STAGES[mode])
     if mode == "sample" and cfg["gamma"] == 0:
-        nst = 4
+        nst = 5
     for _ in range(max(3, warmup)):
         call()
     torch.cuda.synchronize()
@@ -310,7 +310,7 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "bytes_per_launch": kb,
                      "traffic": committed_traffic(kernel, name)},
-        "gpu_launches": steps * (nst if mode != "sample" or cfg["gamma"] > 0 else 3),
+        "gpu_launches": steps * (nst if mode != "sample" or cfg["gamma"] > 0 else 4),
     }
     return res, inputs, call
 

@@ -190,11 +190,32 @@ sv_status spec_verify_uniforms(uint64_t seed, uint64_t offset, int B, int positi
                                int purpose, float *out, void *stream);
 
 /*
+ * Test hook: where spec_verify_sample keeps its re-draw bookkeeping inside a sampling
+ * workspace of these sizes (byte offset of an int32 array, (size_t)-1 for bad sizes).
+ *   [0] sequences the last call marked for the extended-precision re-draw: a draw whose
+ *       threshold u'R lies within 5e-7 R of a CDF boundary, or an accept test with
+ *       |u q - p| < 1e-6 max(p, u q) -- the comparisons fp32 could get wrong
+ *       ("The rule"; readings R2, R3).  At most 32 per call are redone; the rest keep the
+ *       fp32 result.
+ *   [3] SV_ERR_TIMEOUT if the re-draw gave up on a grid barrier (else 0).
+ * Read it after the call's stream has completed.
+ */
+size_t spec_verify_sample_redraw_offset(int B, int gamma, int V, sv_dtype dtype);
+
+/*
+ * Test hook: exp(y_hi[i] + y_lo[i]) for arguments <= 0 in the double-float arithmetic of
+ * the re-draw (result hi + lo, about 48 significant bits; 0 below -87).  Device arrays of n.
+ */
+sv_status spec_verify_exp_df(const float *y_hi, const float *y_lo, int n, float *out_hi, float *out_lo,
+                             void *stream);
+
+/*
  * Optional timing instrumentation for the CALLING THREAD (the only state the library
  * keeps, and it is thread-local).  With events != NULL, each later call of
  * spec_verify_sample / _greedy / _tree_greedy on this thread records events[0] on its
  * stream before its first kernel and events[s] after its s-th kernel (s = 1 .. n_events-1;
- * sampling has 4 kernels: row statistics, decide, residual masses, inverse-CDF draw; greedy
+ * sampling has 5 kernels: row statistics, decide, residual masses, inverse-CDF draw,
+ * extended-precision re-draw of near-boundary sequences; greedy
  * and tree have 2: tile maxima, finalize).  The events are cudaEvent_t handles created
  * and owned by the caller; recording them adds no synchronisation.  Pass NULL (or 0) to
  * turn it off.  Returns SV_ERR_INVALID_ARG for n_events < 0 or > 8.

@@ -61,6 +61,10 @@ def load_library() -> ctypes.CDLL:
         lib.spec_verify_uniforms.restype = i32
         lib.spec_verify_greedy_noalloc.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, P, P]
         lib.spec_verify_greedy_noalloc.restype = i32
+        lib.spec_verify_sample_redraw_offset.argtypes = [i32, i32, i32, i32]
+        lib.spec_verify_sample_redraw_offset.restype = sz
+        lib.spec_verify_exp_df.argtypes = [P, P, i32, P, P, P]
+        lib.spec_verify_exp_df.restype = i32
         lib.spec_verify_set_stage_events.argtypes = [P, i32]
         lib.spec_verify_set_stage_events.restype = i32
         lib.spec_verify_status_string.argtypes = [i32]
@@ -227,6 +231,30 @@ def spec_verify_uniforms(seed: int, offset: int, B: int, positions: int, purpose
                                   purpose, out.data_ptr(), _stream(out.device))
     _check(st, "spec_verify_uniforms")
     return out
+
+
+def sample_redraw_state(workspace: torch.Tensor, B: int, gamma: int, V: int, dtype: int):
+    """Test hook: (sequences marked for the extended-precision re-draw by the last sampling
+    call that used `workspace`, status of that re-draw); synchronises the device."""
+    lib = load_library()
+    off = lib.spec_verify_sample_redraw_offset(B, gamma, V, dtype)
+    if off == ctypes.c_size_t(-1).value:
+        raise ValueError("bad sizes")
+    torch.cuda.synchronize(workspace.device)
+    words = workspace.view(torch.uint8)[off:off + 16].clone().view(torch.int32).cpu()
+    return int(words[0]), int(words[3])
+
+
+def spec_verify_exp_df(y_hi: torch.Tensor, y_lo: torch.Tensor):
+    """Test hook: exp(y_hi + y_lo) in the re-draw's double-float arithmetic -> (hi, lo)."""
+    lib = load_library()
+    if y_hi.dtype != torch.float32 or y_lo.dtype != torch.float32 or y_hi.shape != y_lo.shape:
+        raise ValueError("y_hi, y_lo: fp32 tensors of one shape")
+    y_hi, y_lo = y_hi.contiguous(), y_lo.contiguous()
+    out_hi, out_lo = torch.empty_like(y_hi), torch.empty_like(y_lo)
+    _check(lib.spec_verify_exp_df(y_hi.data_ptr(), y_lo.data_ptr(), y_hi.numel(), out_hi.data_ptr(),
+                                  out_lo.data_ptr(), _stream(y_hi.device)), "spec_verify_exp_df")
+    return out_hi, out_lo
 
 
 def set_stage_events(events) -> None:

@@ -22,6 +22,10 @@ int res_tile_elems(sv_dtype d) {
 }
 int ntile_of(int V, sv_dtype d) { return int((int64_t(V) + tile_elems(d) - 1) / tile_elems(d)); }
 int nrt_of(int V, sv_dtype d) { return int((int64_t(V) + res_tile_elems(d) - 1) / res_tile_elems(d)); }
+int nref_of(int V, sv_dtype d) {
+    const int64_t ue = sv::refine_unit_elems(d == SV_BF16 ? 1 : 0);
+    return int((int64_t(V) + ue - 1) / ue);
+}
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // 16-byte vector loads are legal when the base and both strides keep every row aligned.
@@ -31,7 +35,9 @@ bool vec_ok(const void *p, int64_t sb, int64_t sr, sv_dtype d) {
 }
 
 struct Layout {
-    size_t partial = 0, rowstat = 0, plan = 0, csum = 0, total = 0;
+    size_t partial = 0, rowstat = 0, plan = 0, csum = 0;
+    size_t rflag = 0, rctl = 0, rlist = 0, rsum = 0, ramb = 0;  // re-draw (sampling)
+    size_t total = 0;
 };
 
 // Workspace regions (each 256-byte aligned):
@@ -40,6 +46,8 @@ struct Layout {
 //   rowstat  per row: float2 (M, S)                             (sampling only)
 //   plan     per sequence: int2 (stop row k, mode)              (sampling only)
 //   csum     per (sequence, 2 KB residual tile): residual mass  (sampling only)
+//   rflag, rctl, rlist (RefineInfo records), rsum, ramb: the extended-precision re-draw of near-boundary
+//            sequences (sampling only; see sv_internal.h)
 Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
     Layout L;
     if (B <= 0 || V <= 0 || rows < 0 || !dtype_ok(dtype)) return L;
@@ -61,6 +69,17 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
         off += up256(size_t(B) * 8);
         L.csum = off;
         off += up256(size_t(B) * size_t(nrt_of(V, dtype)) * 4);
+        const size_t nref = size_t(nref_of(V, dtype));
+        L.rflag = off;
+        off += up256(size_t(B) * 4);
+        L.rctl = off;
+        off += up256(size_t(sv::kRefineCtlWords) * 4);
+        L.rlist = off;
+        off += up256(size_t(sv::kMaxRefine) * sizeof(sv::RefineInfo));
+        L.rsum = off;
+        off += up256(size_t(sv::kMaxRefine) * size_t(sv::slot_df_entries(rows, int(nref))) * 8);
+        L.ramb = off;
+        off += up256(size_t(sv::kMaxRefine) * size_t(sv::slot_amb_ints(rows)) * 4);
     }
     L.total = off;
     return L;
@@ -151,17 +170,26 @@ sv_status spec_verify_sample(const void *target_logits, int64_t t_batch_stride,
     if (e == cudaSuccess)
         e = sv::launch_stats_tiles(dt, vec, t, gamma + 1, d, R, B, V, ntile, c, partial, s);
     if (e == cudaSuccess) e = mark(1, s);
+    int *rflag = reinterpret_cast<int *>(at(workspace, L.rflag));
+    int *rctl = reinterpret_cast<int *>(at(workspace, L.rctl));
+    sv::RefineInfo *rinfo = reinterpret_cast<sv::RefineInfo *>(at(workspace, L.rlist));
     if (e == cudaSuccess)
         e = sv::launch_decide(dt, t, d, B, gamma, V, ntile, c, draft_tokens, seed, offset, partial,
-                              rowstat, plan, accepted_len, out_tokens, s);
+                              rowstat, plan, accepted_len, out_tokens, rflag, rctl, s);
     if (e == cudaSuccess) e = mark(2, s);
     if (e == cudaSuccess && gamma > 0)
         e = sv::launch_residual_tiles(dt, vec, t, d, B, gamma, V, nrt, c, rowstat, plan, csum, s);
     if (e == cudaSuccess) e = mark(3, s);
     if (e == cudaSuccess)
         e = sv::launch_draw(dt, vec, t, d, B, gamma, V, ntile, nrt, c, seed, offset, partial, rowstat,
-                            plan, csum, out_tokens, s);
+                            plan, csum, out_tokens, rflag, rctl, rinfo,
+                            reinterpret_cast<int *>(at(workspace, L.ramb)), s);
     if (e == cudaSuccess) e = mark(4, s);
+    if (e == cudaSuccess)
+        e = sv::launch_refine(dt, vec, t, d, B, gamma, V, nref_of(V, dtype), temperature, seed, offset,
+                              draft_tokens, rowstat, plan, rctl, rinfo, at(workspace, L.rsum), at(workspace, L.ramb),
+                              accepted_len, out_tokens, s);
+    if (e == cudaSuccess) e = mark(5, s);
     return cuda_status(e);
 }
 
@@ -257,6 +285,19 @@ sv_status spec_verify_row_stats(const void *logits, int64_t batch_stride, int64_
     if (e == cudaSuccess)
         e = sv::launch_rowstats_finalize(B * rows_per_seq, ntile, c, inv_t, partial, m_out, lse_out, s);
     return cuda_status(e);
+}
+
+size_t spec_verify_sample_redraw_offset(int B, int gamma, int V, sv_dtype dtype) {
+    if (B <= 0 || gamma < 0 || V <= 0 || !dtype_ok(dtype)) return size_t(-1);
+    return layout(SV_MODE_SAMPLE, B, gamma, V, dtype).rctl;
+}
+
+sv_status spec_verify_exp_df(const float *y_hi, const float *y_lo, int n, float *out_hi, float *out_lo,
+                             void *stream) {
+    if (n < 0) return SV_ERR_INVALID_ARG;
+    if (n == 0) return SV_OK;
+    if (!y_hi || !y_lo || !out_hi || !out_lo) return SV_ERR_INVALID_ARG;
+    return cuda_status(sv::launch_exp_df(y_hi, y_lo, n, out_hi, out_lo, static_cast<cudaStream_t>(stream)));
 }
 
 sv_status spec_verify_set_stage_events(void *const *events, int n_events) {

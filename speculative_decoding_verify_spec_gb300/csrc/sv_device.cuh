@@ -105,6 +105,11 @@ __device__ __forceinline__ uint4 ld_stream(const char *p) {
     return r;
 }
 
+template <class D>
+__device__ __forceinline__ uint4 neg_inf_vec() {
+    return make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
+}
+
 // ------------------------------------------------------------------------------------
 // Loading one 16-byte vector of a unit (tile).  `e0` is the element offset of the vector
 // inside the unit that starts at element c0, `len` the number of real elements in it.  A whole in-range vector of
@@ -326,21 +331,29 @@ struct TileWalk {
 __device__ __forceinline__ void griddep_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Launches `kernel` so that it may start while the previous kernel on the stream drains.
+// Launches `kernel` so that it may start while the previous kernel on the stream drains;
+// a cooperative launch (every CTA resident at once) when asked.
 template <class... Params, class... Args>
-inline cudaError_t launch_after(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem,
-                                cudaStream_t s, Args &&...args) {
+inline cudaError_t launch_after_ex(bool cooperative, void (*kernel)(Params...), unsigned grid, unsigned block,
+                                   size_t smem, cudaStream_t s, Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cooperative ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+template <class... Params, class... Args>
+inline cudaError_t launch_after(void (*kernel)(Params...), unsigned grid, unsigned block, size_t smem,
+                                cudaStream_t s, Args &&...args) {
+    return launch_after_ex(false, kernel, grid, block, smem, s, std::forward<Args>(args)...);
 }
 
 // One warp merges the n tile partials of a row: lane l takes tiles l, l + 32, ... in order,

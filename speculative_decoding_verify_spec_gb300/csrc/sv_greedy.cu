@@ -26,10 +26,6 @@
 namespace sv {
 namespace {
 
-__device__ __forceinline__ const char *row_ptr(const Logits &L, int bytes, int64_t b, int64_t r) {
-    return static_cast<const char *>(L.ptr) + (b * L.batch_stride + r * L.row_stride) * bytes;
-}
-
 template <class D, bool VEC>
 __global__ void __launch_bounds__(kThreads, 4)
     max_tiles_kernel(Logits t, int R, int V, int ntile, int64_t items, float *__restrict__ partial) {

@@ -13,6 +13,32 @@ struct Logits {
     int64_t row_stride;
 };
 
+// Row r of sequence b as bytes (element size `bytes`).
+__host__ __device__ inline const char *row_ptr(const Logits &L, int bytes, int64_t b, int64_t r) {
+    return static_cast<const char *>(L.ptr) + (b * L.batch_stride + r * L.row_stride) * bytes;
+}
+
+// Extended-precision re-draw of near-boundary sampling sequences -----------------------
+// decide marks a sequence whose accept test had |u q - p| < kRefineAcceptWindow * max(p, u q)
+// (flag kRefineAccept); draw marks one whose threshold u'R lies within
+// kRefineCdfWindow * R of a CDF boundary or that needed a rounding fallback (kRefineDraw),
+// and appends every marked sequence to a list of at most kMaxRefine; refine redoes those in
+// double-float arithmetic.  Control words (int32, zeroed by decide every call):
+constexpr int kRefineCount = 0;     // sequences marked by this call (may exceed kMaxRefine)
+constexpr int kRefineBarCount = 1;  // grid barrier of the refine kernel
+constexpr int kRefineBarGen = 2;
+constexpr int kRefineStatus = 3;    // SV_ERR_TIMEOUT if a barrier of the refine kernel gave up
+constexpr int kRefineCtlWords = 8;
+constexpr int kMaxRefine = 32;
+constexpr int kRefineDraw = 1, kRefineAccept = 2;
+constexpr float kRefineAcceptWindow = 1e-6f;
+constexpr float kRefineCdfWindow = 2e-7f;  // 2.6x the largest fp32 CDF error measured (7.7e-8 of R)
+// What draw records about a listed sequence (the re-draw's first read).
+struct RefineInfo {
+    int seq, flag, k, mode;  // plan (k, mode) as decided in fp32
+    float Mt, St, Md, Sd;    // fp32 (max, sum) of target / draft row k (Md, Sd unused for a bonus draw)
+};
+
 // Sampling path -----------------------------------------------------------------------
 // Row statistics of B sequences of R = rows_a + rows_b rows: local rows [0, rows_a) come
 // from `a`, [rows_a, R) from `b` (row rows_a + i of b is row i of tensor b).  One partial
@@ -24,16 +50,37 @@ cudaError_t launch_stats_tiles(int dtype, bool vec, Logits a, int rows_a, Logits
 cudaError_t launch_decide(int dtype, Logits t, Logits d, int B, int gamma, int V, int ntile,
                           float c, const int32_t *x, uint64_t seed, uint64_t offset,
                           const void *partial, void *rowstat, void *plan, int32_t *accepted_len,
-                          int32_t *out_tokens, cudaStream_t s);
+                          int32_t *out_tokens, int *rflag, int *rctl, cudaStream_t s);
 // Residual mass sum_j (p_j - q_j)+ of every residual tile of the stop row (sequences that
 // rejected): csum[seq * nrt + tile].
 cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V,
                                   int nrt, float c, const void *rowstat, const void *plan, float *csum,
                                   cudaStream_t s);
-// Inverse-CDF draw of the final token on the stop row of every valid sequence.
+// Inverse-CDF draw of the final token on the stop row of every valid sequence; marks and
+// lists the sequences to redo in extended precision.
 cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
                         float c, uint64_t seed, uint64_t offset, const void *partial, const void *rowstat,
-                        const void *plan, const float *csum, int32_t *out_tokens, cudaStream_t s);
+                        const void *plan, const float *csum, int32_t *out_tokens, int *rflag, int *rctl,
+                        RefineInfo *rinfo, int *ramb, cudaStream_t s);
+// Logits per unit of the extended-precision re-draw (32 lanes x 2).
+inline int refine_unit_elems(int) { return 64; }
+// Per listed sequence the re-draw keeps (4 gamma + 1) x nref double-float unit sums and,
+// per row pair, an ambiguity list of 1 + kMaxAmbiguous ints (count first; draw clears the
+// counts of every slot it fills).
+constexpr int kMaxAmbiguous = 32;
+__host__ __device__ inline int64_t slot_df_entries(int gamma, int nref) { return int64_t(4 * gamma + 1) * nref; }
+__host__ __device__ inline int64_t slot_amb_ints(int gamma) {
+    return int64_t(gamma > 0 ? gamma : 1) * (1 + kMaxAmbiguous);
+}
+// The re-draw of the listed sequences (double-float arithmetic); a cooperative grid.
+// Scratch: rsum [kMaxRefine][slot_df_entries] (8 bytes each), ramb [kMaxRefine][slot_amb_ints].
+cudaError_t launch_refine(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int nref, float T,
+                          uint64_t seed, uint64_t offset, const int32_t *x, const void *rowstat, const void *plan,
+                          int *rctl, const RefineInfo *rinfo, void *rsum, void *ramb, int32_t *accepted_len,
+                          int32_t *out_tokens, cudaStream_t s);
+// Test hook: exp(hi + lo) in double-float for n arguments <= 0.
+cudaError_t launch_exp_df(const float *y_hi, const float *y_lo, int n, float *out_hi, float *out_lo,
+                          cudaStream_t s);
 // Test hook: (m, lse) per row from the partials.
 cudaError_t launch_rowstats_finalize(int rows, int ntile, float c, float inv_t, const void *partial,
                                      float *m_out, float *lse_out, cudaStream_t s);

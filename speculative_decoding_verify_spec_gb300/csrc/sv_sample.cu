@@ -26,15 +26,6 @@
 namespace sv {
 namespace {
 
-__device__ __forceinline__ const char *row_ptr(const Logits &L, int bytes, int64_t b, int64_t r) {
-    return static_cast<const char *>(L.ptr) + (b * L.batch_stride + r * L.row_stride) * bytes;
-}
-
-template <class D>
-__device__ __forceinline__ uint4 neg_inf_vec() {
-    return make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
-}
-
 // Unnormalised target weight 2^((t - M) c) = exp((t - M) / T) with a single rounding of
 // the (exact) difference times c.
 __device__ __forceinline__ float weight(float x, float M, float c) {
@@ -92,7 +83,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
                   const int32_t *__restrict__ x, uint64_t seed, uint64_t offset,
                   const float2 *__restrict__ partial, float2 *__restrict__ rowstat,
                   int2 *__restrict__ plan, int32_t *__restrict__ accepted_len,
-                  int32_t *__restrict__ out_tokens) {
+                  int32_t *__restrict__ out_tokens, int *__restrict__ rflag, int *__restrict__ rctl) {
     extern __shared__ float2 s_stat[];  // [2 gamma + 1]
     griddep_launch_next();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -111,6 +102,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
         }
     }
     griddep_wait();
+    if (blockIdx.x == 0 && threadIdx.x < kRefineCtlWords) rctl[threadIdx.x] = 0;  // this call's re-draw list
     for (int r = warp; r < R; r += kDecideWarps) {
         const float2 st = warp_merge_stats(partial + (seq * R + r) * ntile, ntile, c, lane);
         if (lane == 0) {
@@ -134,14 +126,18 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
         if (lane == 0) {
             accepted_len[seq] = -1;
             plan[seq] = make_int2(-1, -1);
+            rflag[seq] = 0;
         }
         return;
     }
 
+    // the scan; an accept test whose two sides u q and p are within the fp32 error of
+    // each other marks the sequence for the extended-precision re-draw
     int k = gamma;
+    bool near_any = false;
     for (int i0 = 0; i0 < gamma; i0 += 32) {
         const int i = i0 + lane;
-        bool reject = false;
+        bool reject = false, near = false;
         if (i < gamma) {
             const float2 st = s_stat[i];
             const float2 sd = s_stat[gamma + 1 + i];
@@ -155,8 +151,11 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
             const float q = weight(dx, sd.x, c) / sd.y;
             const float u = uniform01(seed, offset, uint32_t(seq), uint32_t(i), 0u);
             reject = !(u * q < p);
+            near = fabsf(u * q - p) < kRefineAcceptWindow * fmaxf(p, u * q);
         }
         const unsigned m = __ballot_sync(0xFFFFFFFFu, reject);
+        const unsigned performed = m ? ((2u << (__ffs(m) - 1)) - 1u) : 0xFFFFFFFFu;  // up to the first rejection
+        near_any |= (__ballot_sync(0xFFFFFFFFu, near) & performed) != 0u;
         if (m) {
             k = i0 + __ffs(m) - 1;
             break;
@@ -169,6 +168,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
     if (lane == 0) {
         accepted_len[seq] = k;
         plan[seq] = make_int2(k, k < gamma ? 1 : 0);
+        rflag[seq] = near_any ? kRefineAccept : 0;
     }
 }
 
@@ -178,8 +178,22 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
 // Persistent, with blocked work: warp w takes the items [w * per, (w + 1) * per), i.e.
 // runs of consecutive tiles of one or two sequences, so a sequence's plan and statistics
 // are read once per run and the warp's loads walk along the row.
+constexpr bool kResidualPrefetch = false;  // load tile i + 1 of a run while computing tile i (measured: no gain)
+constexpr int kResidualCtas = 4;           // resident CTAs per SM the kernel is built for
+
 template <class D, bool VEC>
-__global__ void __launch_bounds__(kThreads, 4)
+__device__ __forceinline__ void load_residual_tile(const char *tp, const char *dp, int64_t c0, int len, int lane,
+                                                   uint4 (&tv)[kResVecs], uint4 (&dv)[kResVecs]) {
+#pragma unroll
+    for (int u = 0; u < kResVecs; ++u) {
+        const int e0 = (lane + 32 * u) * D::EPV;
+        tv[u] = e0 < len ? load_vec<D, VEC>(tp, c0, e0, len) : neg_inf_vec<D>();
+        dv[u] = e0 < len ? load_vec<D, VEC>(dp, c0, e0, len) : neg_inf_vec<D>();
+    }
+}
+
+template <class D, bool VEC>
+__global__ void __launch_bounds__(kThreads, kResidualCtas)
     residual_tiles_kernel(Logits t, Logits d, int gamma, int V, int nrt, int64_t items, int64_t per, float c,
                           const float2 *__restrict__ rowstat, const int2 *__restrict__ plan,
                           float *__restrict__ csum) {
@@ -199,25 +213,37 @@ __global__ void __launch_bounds__(kThreads, 4)
             const float inv_st = 1.f / st.y, inv_sd = 1.f / sd.y;
             const char *tp = row_ptr(t, D::kBytes, seq, k);
             const char *dp = row_ptr(d, D::kBytes, seq, k);
+            constexpr int RE = res_tile_elems<D>();
+            uint4 tv[kResVecs], dv[kResVecs];
+            load_residual_tile<D, VEC>(tp, dp, (it - seq * nrt) * RE, unit_len(V, (it - seq * nrt) * RE, RE), lane, tv,
+                                       dv);
             for (; it < run_end; ++it) {
-                const int64_t c0 = (it - seq * nrt) * res_tile_elems<D>();
-                const int len = unit_len(V, c0, res_tile_elems<D>());
-                uint4 tv[kResVecs], dv[kResVecs];
-#pragma unroll
-                for (int u = 0; u < kResVecs; ++u) {
-                    const int e0 = (lane + 32 * u) * D::EPV;
-                    tv[u] = e0 < len ? load_vec<D, VEC>(tp, c0, e0, len) : neg_inf_vec<D>();
-                    dv[u] = e0 < len ? load_vec<D, VEC>(dp, c0, e0, len) : neg_inf_vec<D>();
+                uint4 ntv[kResVecs], ndv[kResVecs];
+                if (kResidualPrefetch && it + 1 < run_end) {
+                    const int64_t n0 = (it + 1 - seq * nrt) * RE;
+                    load_residual_tile<D, VEC>(tp, dp, n0, unit_len(V, n0, RE), lane, ntv, ndv);
                 }
                 float acc = 0.f;
 #pragma unroll
                 for (int u = 0; u < kResVecs; ++u)
 #pragma unroll
                     for (int e = 0; e < D::EPV; ++e)
-                        acc += residual_weight(vec_elem<D>(tv[u], e), vec_elem<D>(dv[u], e), c, st.x, inv_st,
-                                               sd.x, inv_sd);
+                        acc += residual_weight(vec_elem<D>(tv[u], e), vec_elem<D>(dv[u], e), c, st.x, inv_st, sd.x,
+                                               inv_sd);
                 const float mass = warp_reduce(acc, [](float x, float y) { return x + y; });
                 if (lane == 0) csum[it] = mass;
+                if (it + 1 < run_end) {
+                    if (kResidualPrefetch) {
+#pragma unroll
+                        for (int u = 0; u < kResVecs; ++u) {
+                            tv[u] = ntv[u];
+                            dv[u] = ndv[u];
+                        }
+                    } else {
+                        const int64_t n0 = (it + 1 - seq * nrt) * RE;
+                        load_residual_tile<D, VEC>(tp, dp, n0, unit_len(V, n0, RE), lane, tv, dv);
+                    }
+                }
             }
         }
         it = run_end;
@@ -236,7 +262,8 @@ __global__ void __launch_bounds__(128)
     draw_kernel(Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt, float c, uint64_t seed,
                 uint64_t offset, const float2 *__restrict__ partial, const float2 *__restrict__ rowstat,
                 const int2 *__restrict__ plan, const float *__restrict__ csum,
-                int32_t *__restrict__ out_tokens) {
+                int32_t *__restrict__ out_tokens, int *__restrict__ rflag, int *__restrict__ rctl,
+                RefineInfo *__restrict__ rinfo, int *__restrict__ ramb) {
     griddep_launch_next();
     griddep_wait();
     const int lane = threadIdx.x & 31;
@@ -255,14 +282,23 @@ __global__ void __launch_bounds__(128)
         return p.y * weight(p.x, st.x, c);  // mass of tile u under 2^((l - M) c)
     };
 
+    // this lane's first kKeep unit masses stay in registers for the walk below
+    constexpr int kKeep = 8;
+    float keep[kKeep];
     float total = 0.f, lane_sum = 0.f;
     int units = 0, per_lane = 0;
     for (int pass = 0; pass < 2; ++pass) {
         units = mode ? nrt : ntile;
         per_lane = (units + 31) / 32;
         lane_sum = 0.f;
-#pragma unroll 4
-        for (int q = 0; q < per_lane; ++q) {
+#pragma unroll
+        for (int q = 0; q < kKeep; ++q) {
+            const int u = lane * per_lane + q;
+            keep[q] = (q < per_lane && u < units) ? unit_mass(u) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < kKeep; ++q) lane_sum += keep[q];
+        for (int q = kKeep; q < per_lane; ++q) {
             const int u = lane * per_lane + q;
             if (u < units) lane_sum += unit_mass(u);
         }
@@ -276,29 +312,39 @@ __global__ void __launch_bounds__(128)
     // the unit holding the threshold: the first lane whose range crosses it, then inside it
     int unit = -1;
     float base = 0.f;
-    bool force_last = false;
+    bool force_last = false, unit_fallback = false;
     const unsigned crossing = __ballot_sync(0xFFFFFFFFu, incl > thr);
     if (crossing) {
         const int l = __ffs(crossing) - 1;
         if (lane == l) {
             float run = incl - lane_sum;
             int last_in_lane = lane * per_lane;
-            for (int q = 0; q < per_lane; ++q) {
+#pragma unroll
+            for (int q = 0; q < kKeep; ++q) {
+                const int u = lane * per_lane + q;
+                if (unit < 0 && q < per_lane && u < units) {
+                    last_in_lane = u;
+                    if (run + keep[q] > thr) unit = u;
+                    else run += keep[q];
+                }
+            }
+            for (int q = kKeep; q < per_lane && unit < 0; ++q) {
                 const int u = lane * per_lane + q;
                 if (u >= units) break;
                 last_in_lane = u;
                 const float m = unit_mass(u);
-                if (run + m > thr) {
-                    unit = u;
-                    break;
-                }
-                run += m;
+                if (run + m > thr) unit = u;
+                else run += m;
             }
-            if (unit < 0) unit = last_in_lane;  // rounding: stay inside this lane's units
+            if (unit < 0) {
+                unit = last_in_lane;  // rounding: stay inside this lane's units
+                unit_fallback = true;
+            }
             base = run;
         }
         unit = __shfl_sync(0xFFFFFFFFu, unit, l);
         base = __shfl_sync(0xFFFFFFFFu, base, l);
+        unit_fallback = __shfl_sync(0xFFFFFFFFu, unit_fallback, l);
     } else {  // rounding left the threshold at or above the total: the last unit with mass
         int lp = -1;
         for (int q = 0; q < per_lane; ++q) {
@@ -351,6 +397,7 @@ __global__ void __launch_bounds__(128)
     run.add(base);
     run.add(lincl - tsum);
     int cand = kNoIndex, lastpos = -1;
+    float gap = 0.f;  // distance from thr to the nearer of C_{j-1} and C_j at this lane's candidate
 #pragma unroll
     for (int v = 0; v < kTileVecs; ++v) {  // the same registers, the same arithmetic
         if (v < VPL) {
@@ -359,19 +406,43 @@ __global__ void __launch_bounds__(128)
             for (int e = 0; e < D::EPV; ++e) {
                 const int j = e0 + e;
                 const float w = w_at(tv[v], dv[v % kResVecs], e);
+                const float before = run.value();
                 run.add(w);
                 if (j < len) {
-                    if (!force_last && cand == kNoIndex && run.value() > thr) cand = j;
+                    if (!force_last && cand == kNoIndex && run.value() > thr) {
+                        cand = j;
+                        gap = fminf(thr - before, run.value() - thr);
+                    }
                     if (w > 0.f) lastpos = j;
                 }
             }
         }
     }
-    cand = warp_reduce(cand, [](int a, int b) { return min(a, b); });
+    const int first = warp_reduce(cand, [](int a, int b) { return min(a, b); });
     lastpos = warp_reduce(lastpos, [](int a, int b) { return max(a, b); });
-    int tok = cand != kNoIndex ? cand : lastpos;
+    int tok = first != kNoIndex ? first : lastpos;
     if (tok < 0) tok = 0;
-    if (lane == 0) out_tokens[seq * (gamma + 1) + k] = int32_t(u0 + tok);
+    // a draw whose threshold lies within the fp32 error of a CDF boundary (or that needed a
+    // rounding fallback, or a sequence decide marked) is redone in extended precision
+    const unsigned owner = __ballot_sync(0xFFFFFFFFu, cand == first && first != kNoIndex);
+    const float g = owner ? __shfl_sync(0xFFFFFFFFu, gap, __ffs(owner) - 1) : 0.f;
+    if (lane == 0) {
+        out_tokens[seq * (gamma + 1) + k] = int32_t(u0 + tok);
+        const bool near = first == kNoIndex || force_last || unit_fallback || mode != pl.y ||
+                          !(g >= kRefineCdfWindow * total);
+        int flag = rflag[seq];
+        if (near && flag == 0) flag = kRefineDraw;
+        if (flag != 0) {
+            rflag[seq] = flag;
+            const int slot = atomicAdd(rctl + kRefineCount, 1);
+            if (slot < kMaxRefine) {
+                const float2 sdk = pl.y == 1 ? rowstat[seq * R + gamma + 1 + k] : make_float2(0.f, 1.f);
+                rinfo[slot] = RefineInfo{int(seq), flag, k, pl.y, st.x, st.y, sdk.x, sdk.y};
+                int *amb = ramb + int64_t(slot) * slot_amb_ints(gamma);
+                for (int i = 0; i < (gamma > 0 ? gamma : 1); ++i) amb[i * (1 + kMaxAmbiguous)] = 0;
+            }
+        }
+    }
 }
 
 // ------------------------------------------------------------------------------------
@@ -429,12 +500,12 @@ cudaError_t launch_stats_tiles(int dtype, bool vec, Logits a, int rows_a, Logits
 cudaError_t launch_decide(int dtype, Logits t, Logits d, int B, int gamma, int V, int ntile,
                           float c, const int32_t *x, uint64_t seed, uint64_t offset,
                           const void *partial, void *rowstat, void *plan, int32_t *accepted_len,
-                          int32_t *out_tokens, cudaStream_t s) {
+                          int32_t *out_tokens, int *rflag, int *rctl, cudaStream_t s) {
     auto k = dtype == 1 ? decide_kernel<BF16> : decide_kernel<F32>;
     const size_t smem = size_t(2 * gamma + 1) * sizeof(float2);
     return launch_after(k, unsigned(B), kDecideWarps * 32, smem, s, t, d, B, gamma, V, ntile, c, x, seed, offset,
                         static_cast<const float2 *>(partial), static_cast<float2 *>(rowstat),
-                        static_cast<int2 *>(plan), accepted_len, out_tokens);
+                        static_cast<int2 *>(plan), accepted_len, out_tokens, rflag, rctl);
 }
 
 cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V,
@@ -454,13 +525,14 @@ cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B
 
 cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
                         float c, uint64_t seed, uint64_t offset, const void *partial, const void *rowstat,
-                        const void *plan, const float *csum, int32_t *out_tokens, cudaStream_t s) {
+                        const void *plan, const float *csum, int32_t *out_tokens, int *rflag, int *rctl,
+                        RefineInfo *rinfo, int *ramb, cudaStream_t s) {
     const unsigned grid = unsigned((int64_t(B) * 32 + 127) / 128);
     auto k = pick(dtype, vec, draw_kernel<BF16, true>, draw_kernel<BF16, false>, draw_kernel<F32, true>,
                   draw_kernel<F32, false>);
     return launch_after(k, grid, 128, 0, s, t, d, B, gamma, V, ntile, nrt, c, seed, offset,
                         static_cast<const float2 *>(partial), static_cast<const float2 *>(rowstat),
-                        static_cast<const int2 *>(plan), csum, out_tokens);
+                        static_cast<const int2 *>(plan), csum, out_tokens, rflag, rctl, rinfo, ramb);
 }
 
 cudaError_t launch_rowstats_finalize(int rows, int ntile, float c, float inv_t, const void *partial,

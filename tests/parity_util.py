@@ -27,6 +27,8 @@ def oracle_sample(target, draft, tokens, T, seed, offset=0, threads=None, diagno
     """The oracle over the whole batch, split over threads (each range keeps its global
     sequence index b0, which keys the uniforms).  Inputs may be CUDA tensors or the host
     arrays returned by host() (to convert once for many calls)."""
+    # the C-ABI call receives the temperature as a float: the oracle divides by that value
+    T = float(np.float32(T))
     t = target if isinstance(target, np.ndarray) else host(target)
     d = draft if isinstance(draft, np.ndarray) else host(draft)
     x = tokens if isinstance(tokens, np.ndarray) else tokens.cpu().numpy()
@@ -94,13 +96,13 @@ def compare_sample(acc, out, o_acc, o_out, o_flags, o_diag=None, label="", recor
     return n, mism, flg, mdiag
 
 
-def record_rates(label, n, mismatches, flagged, flags, mismatch_diag=()):
+def record_rates(label, n, mismatches, flagged, flags, mismatch_diag=(), **extra):
     """Append the flag / mismatch counts of a parity case to gpurun_out/parity_rates.jsonl."""
     out_dir = os.path.join(ROOT, "gpurun_out")
     os.makedirs(out_dir, exist_ok=True)
     rec = {"case": label, "sequences": n, "mismatches": mismatches, "flagged": flagged,
            "flag_accept": int(((flags & 1) != 0).sum()), "flag_cdf": int(((flags & 2) != 0).sum()),
            "flag_residual_small": int(((flags & 4) != 0).sum()),
-           "mismatch_diagnostics": list(mismatch_diag)[:50]}
+           "mismatch_diagnostics": list(mismatch_diag)[:50], **extra}
     with open(os.path.join(out_dir, "parity_rates.jsonl"), "a") as f:
         f.write(json.dumps(rec) + "\n")
