@@ -183,7 +183,7 @@ sv_status spec_verify_sample(const void *target_logits, int64_t t_batch_stride,
     if (e == cudaSuccess)
         e = sv::launch_draw(dt, vec, t, d, B, gamma, V, ntile, nrt, c, seed, offset, partial, rowstat,
                             plan, csum, out_tokens, rflag, rctl, rinfo,
-                            reinterpret_cast<int *>(at(workspace, L.ramb)), s);
+                            reinterpret_cast<int *>(at(workspace, L.ramb)), gamma > 0, s);
     if (e == cudaSuccess) e = mark(4, s);
     if (e == cudaSuccess)
         e = sv::launch_refine(dt, vec, t, d, B, gamma, V, nref_of(V, dtype), temperature, seed, offset,

@@ -61,7 +61,7 @@ cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B
 cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
                         float c, uint64_t seed, uint64_t offset, const void *partial, const void *rowstat,
                         const void *plan, const float *csum, int32_t *out_tokens, int *rflag, int *rctl,
-                        RefineInfo *rinfo, int *ramb, cudaStream_t s);
+                        RefineInfo *rinfo, int *ramb, bool early, cudaStream_t s);
 // Logits per unit of the extended-precision re-draw (32 lanes x 2).
 inline int refine_unit_elems(int) { return 64; }
 // Per listed sequence the re-draw keeps (4 gamma + 1) x nref double-float unit sums and,

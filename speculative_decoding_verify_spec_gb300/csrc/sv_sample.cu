@@ -43,6 +43,21 @@ __device__ __forceinline__ float residual_weight(float tj, float dj, float c, fl
     return fmaxf(__fsub_rn(p, q), 0.f);
 }
 
+// residual_weight on two elements: the exponent arguments and the two products with FP32x2
+// instructions, the difference p - q with one scalar subtraction per element.  A packed
+// p + (-q) is not safe: the code generator may fuse the product q into that addition
+// (one FFMA2, which keeps p's rounding error, so identical rows would leave ~1e-8 of
+// residual mass instead of exactly 0), and scalar arithmetic with explicit rounding is
+// never fused.  Each result equals residual_weight bit for bit.
+__device__ __forceinline__ float2 residual_weight2(float2 t2, float2 d2, float2 c2, float2 nmt2, float2 inv_st2,
+                                                   float2 nmd2, float2 inv_sd2) {
+    const float2 yt = __fmul2_rn(__fadd2_rn(t2, nmt2), c2);
+    const float2 yd = __fmul2_rn(__fadd2_rn(d2, nmd2), c2);
+    const float2 p = __fmul2_rn(make_float2(ex2(yt.x), ex2(yt.y)), inv_st2);
+    const float2 q = __fmul2_rn(make_float2(ex2(yd.x), ex2(yd.y)), inv_sd2);
+    return make_float2(fmaxf(__fsub_rn(p.x, q.x), 0.f), fmaxf(__fsub_rn(p.y, q.y), 0.f));
+}
+
 // ------------------------------------------------------------------------------------
 // Row statistics: partial[(seq * R + row) * ntile + tile] = (M, S) of that 4 KB tile, S
 // relative to the tile's own maximum.  Local rows [0, rows_a) come from a, the rest from bt.
@@ -177,7 +192,10 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
 // stop row, for the sequences that rejected (plan mode 1); other entries are not written.
 // Persistent, with blocked work: warp w takes the items [w * per, (w + 1) * per), i.e.
 // runs of consecutive tiles of one or two sequences, so a sequence's plan and statistics
-// are read once per run and the warp's loads walk along the row.
+// are read once per run and the warp's loads walk along the row.  The weights of element
+// pairs come from residual_weight2 (FP32x2), even and odd elements summed separately.
+// (Staging the tiles through shared memory with asynchronous copies made this kernel ~2 us
+// faster but the re-draw kernel that follows it ~10 us slower; measured, not kept.)
 constexpr bool kResidualPrefetch = false;  // load tile i + 1 of a run while computing tile i (measured: no gain)
 constexpr int kResidualCtas = 4;           // resident CTAs per SM the kernel is built for
 
@@ -197,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, kResidualCtas)
     residual_tiles_kernel(Logits t, Logits d, int gamma, int V, int nrt, int64_t items, int64_t per, float c,
                           const float2 *__restrict__ rowstat, const int2 *__restrict__ plan,
                           float *__restrict__ csum) {
-    griddep_launch_next();
     griddep_wait();
+    griddep_launch_next();  // after the wait: the draw's prologue may read what decide wrote
     const int lane = threadIdx.x & 31;
     const int R = 2 * gamma + 1;
     int64_t it = (int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5)) * per;
@@ -223,14 +241,27 @@ __global__ void __launch_bounds__(kThreads, kResidualCtas)
                     const int64_t n0 = (it + 1 - seq * nrt) * RE;
                     load_residual_tile<D, VEC>(tp, dp, n0, unit_len(V, n0, RE), lane, ntv, ndv);
                 }
-                float acc = 0.f;
+                float2 acc = make_float2(0.f, 0.f);
+                const float2 c2 = make_float2(c, c), nmt2 = make_float2(-st.x, -st.x),
+                             inv_st2 = make_float2(inv_st, inv_st), nmd2 = make_float2(-sd.x, -sd.x),
+                             inv_sd2 = make_float2(inv_sd, inv_sd);
 #pragma unroll
-                for (int u = 0; u < kResVecs; ++u)
+                for (int u = 0; u < kResVecs; ++u) {
+                    const uint32_t tw[4] = {tv[u].x, tv[u].y, tv[u].z, tv[u].w}, dw[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
 #pragma unroll
-                    for (int e = 0; e < D::EPV; ++e)
-                        acc += residual_weight(vec_elem<D>(tv[u], e), vec_elem<D>(dv[u], e), c, st.x, inv_st, sd.x,
-                                               inv_sd);
-                const float mass = warp_reduce(acc, [](float x, float y) { return x + y; });
+                    for (int q = 0; q < 4; q += (D::EPV == 8 ? 1 : 2)) {
+                        float2 t2, d2;
+                        if constexpr (D::EPV == 8) {
+                            t2 = make_float2(bf16_lo(tw[q]), bf16_hi(tw[q]));
+                            d2 = make_float2(bf16_lo(dw[q]), bf16_hi(dw[q]));
+                        } else {
+                            t2 = make_float2(__uint_as_float(tw[q]), __uint_as_float(tw[q + 1]));
+                            d2 = make_float2(__uint_as_float(dw[q]), __uint_as_float(dw[q + 1]));
+                        }
+                        acc = __fadd2_rn(acc, residual_weight2(t2, d2, c2, nmt2, inv_st2, nmd2, inv_sd2));
+                    }
+                }
+                const float mass = warp_reduce(acc.x + acc.y, [](float x, float y) { return x + y; });
                 if (lane == 0) csum[it] = mass;
                 if (it + 1 < run_end) {
                     if (kResidualPrefetch) {
@@ -263,17 +294,35 @@ __global__ void __launch_bounds__(128)
                 uint64_t offset, const float2 *__restrict__ partial, const float2 *__restrict__ rowstat,
                 const int2 *__restrict__ plan, const float *__restrict__ csum,
                 int32_t *__restrict__ out_tokens, int *__restrict__ rflag, int *__restrict__ rctl,
-                RefineInfo *__restrict__ rinfo, int *__restrict__ ramb) {
+                RefineInfo *__restrict__ rinfo, int *__restrict__ ramb, bool early) {
     griddep_launch_next();
-    griddep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t seq = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    if (seq >= B) return;
-    const int2 pl = plan[seq];
+    const bool live = seq < B;
+    const int R = 2 * gamma + 1;
+    // What decide wrote (plan, statistics, its re-draw mark) and the uniform.  With `early`
+    // (the residual kernel ran in between and let this grid start only after its own wait
+    // on decide) these loads go out before the wait for the residual masses.
+    int2 pl = make_int2(-1, -1);
+    float2 st = make_float2(0.f, 1.f), sdk = make_float2(0.f, 1.f);
+    int flag0 = 0;
+    float u1 = 0.f;
+    auto read_plan = [&]() {
+        pl = __ldcg(plan + seq);
+        if (pl.y >= 0) {
+            st = __ldcg(rowstat + seq * R + pl.x);
+            if (pl.y == 1) sdk = __ldcg(rowstat + seq * R + gamma + 1 + pl.x);
+            flag0 = __ldcg(rflag + seq);
+            u1 = uniform01(seed, offset, uint32_t(seq), uint32_t(pl.x), 1u);
+        }
+    };
+    if (live && early) read_plan();
+    griddep_wait();
+    if (!live) return;
+    if (!early) read_plan();
     if (pl.y < 0) return;  // invalid sequence: outputs already written by decide
-    const int k = pl.x, R = 2 * gamma + 1;
+    const int k = pl.x;
     int mode = pl.y;  // 1: residual after a rejection, 0: bonus draw from p
-    const float2 st = rowstat[seq * R + k];
     const float2 *prow = partial + (seq * R + k) * ntile;
     const float *crow = csum + seq * nrt;
     auto unit_mass = [&](int u) -> float {
@@ -306,7 +355,7 @@ __global__ void __launch_bounds__(128)
         if (mode == 1 && !(total > 0.f)) mode = 0;  // exact-zero residual: draw from p
         else break;
     }
-    const float thr = uniform01(seed, offset, uint32_t(seq), uint32_t(k), 1u) * total;
+    const float thr = u1 * total;
     const float incl = warp_inclusive_scan(lane_sum, lane);
 
     // the unit holding the threshold: the first lane whose range crosses it, then inside it
@@ -361,7 +410,7 @@ __global__ void __launch_bounds__(128)
     const int last_unit = (V - 1) / unit_elems;  // units past it hold no element of the row
     if (unit > last_unit) unit = last_unit;
     const int VPL = mode ? kResVecs : kTileVecs;
-    const float2 sd = mode ? rowstat[seq * R + gamma + 1 + k] : make_float2(0.f, 1.f);
+    const float2 sd = mode ? sdk : make_float2(0.f, 1.f);
     const float inv_st = 1.f / st.y, inv_sd = 1.f / sd.y;
     const char *tp = row_ptr(t, D::kBytes, seq, k);
     const char *dp = row_ptr(d, D::kBytes, seq, k);
@@ -430,13 +479,12 @@ __global__ void __launch_bounds__(128)
         out_tokens[seq * (gamma + 1) + k] = int32_t(u0 + tok);
         const bool near = first == kNoIndex || force_last || unit_fallback || mode != pl.y ||
                           !(g >= kRefineCdfWindow * total);
-        int flag = rflag[seq];
+        int flag = flag0;
         if (near && flag == 0) flag = kRefineDraw;
         if (flag != 0) {
             rflag[seq] = flag;
             const int slot = atomicAdd(rctl + kRefineCount, 1);
             if (slot < kMaxRefine) {
-                const float2 sdk = pl.y == 1 ? rowstat[seq * R + gamma + 1 + k] : make_float2(0.f, 1.f);
                 rinfo[slot] = RefineInfo{int(seq), flag, k, pl.y, st.x, st.y, sdk.x, sdk.y};
                 int *amb = ramb + int64_t(slot) * slot_amb_ints(gamma);
                 for (int i = 0; i < (gamma > 0 ? gamma : 1); ++i) amb[i * (1 + kMaxAmbiguous)] = 0;
@@ -526,13 +574,13 @@ cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B
 cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
                         float c, uint64_t seed, uint64_t offset, const void *partial, const void *rowstat,
                         const void *plan, const float *csum, int32_t *out_tokens, int *rflag, int *rctl,
-                        RefineInfo *rinfo, int *ramb, cudaStream_t s) {
+                        RefineInfo *rinfo, int *ramb, bool early, cudaStream_t s) {
     const unsigned grid = unsigned((int64_t(B) * 32 + 127) / 128);
     auto k = pick(dtype, vec, draw_kernel<BF16, true>, draw_kernel<BF16, false>, draw_kernel<F32, true>,
                   draw_kernel<F32, false>);
     return launch_after(k, grid, 128, 0, s, t, d, B, gamma, V, ntile, nrt, c, seed, offset,
                         static_cast<const float2 *>(partial), static_cast<const float2 *>(rowstat),
-                        static_cast<const int2 *>(plan), csum, out_tokens, rflag, rctl, rinfo, ramb);
+                        static_cast<const int2 *>(plan), csum, out_tokens, rflag, rctl, rinfo, ramb, early);
 }
 
 cudaError_t launch_rowstats_finalize(int rows, int ntile, float c, float inv_t, const void *partial,
