@@ -325,7 +325,9 @@ struct TileWalk {
 // Programmatic dependent launch.  Every kernel of a call first lets the next kernel of the
 // call be scheduled (its CTAs then wait in griddep_wait on SMs freed by this grid's tail),
 // then, before it reads anything an earlier kernel wrote, waits for the previous grid to
-// complete and flush.  Every CTA waits before it may exit, so a grid is only complete once
+// complete and flush.  A call's first kernel waits before any read at all (its predecessor
+// is the caller's kernel, which may signal its dependents before it has written the
+// logits), so across calls only the launch latency is hidden.  Every CTA waits before it may exit, so a grid is only complete once
 // its predecessor is -- completion is transitive along the call.  For a grid launched
 // without the attribute both instructions are no-ops.
 __device__ __forceinline__ void griddep_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

@@ -30,6 +30,7 @@ template <class D, bool VEC>
 __global__ void __launch_bounds__(kThreads, 4)
     max_tiles_kernel(Logits t, int R, int V, int ntile, int64_t items, float *__restrict__ partial) {
     griddep_launch_next();
+    griddep_wait();  // before any read: the caller's previous kernel may be writing the logits
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = int64_t(gridDim.x) * kWarps;
     for (TileWalk w(int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5), nwarps, R, ntile); w.it < items;
@@ -235,8 +236,7 @@ cudaError_t launch_max_tiles(int dtype, bool vec, Logits t, int R, int B, int V,
     unsigned grid = 0;
     cudaError_t e = persistent_grid(k, items, &grid);
     if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, 0, s>>>(t, R, V, ntile, items, static_cast<float *>(partial));
-    return cudaGetLastError();
+    return launch_after(k, grid, kThreads, 0, s, t, R, V, ntile, items, static_cast<float *>(partial));
 }
 
 cudaError_t launch_greedy_finalize(int dtype, bool vec, Logits t, int B, int gamma, int V, int ntile,

@@ -66,6 +66,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     stats_tiles_kernel(Logits a, int rows_a, Logits bt, int R, int V, int ntile, int64_t items, float c,
                        float2 *__restrict__ partial) {
     griddep_launch_next();
+    griddep_wait();  // before any read: the caller's previous kernel may be writing the logits
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = int64_t(gridDim.x) * kWarps;
     for (TileWalk w(int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5), nwarps, R, ntile); w.it < items;
@@ -541,8 +542,7 @@ cudaError_t launch_stats_tiles(int dtype, bool vec, Logits a, int rows_a, Logits
     unsigned grid = 0;
     cudaError_t e = persistent_grid(k, items, &grid);
     if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, 0, s>>>(a, rows_a, b, R, V, ntile, items, c, static_cast<float2 *>(partial));
-    return cudaGetLastError();
+    return launch_after(k, grid, kThreads, 0, s, a, rows_a, b, R, V, ntile, items, c, static_cast<float2 *>(partial));
 }
 
 cudaError_t launch_decide(int dtype, Logits t, Logits d, int B, int gamma, int V, int ntile,
