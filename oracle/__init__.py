@@ -64,6 +64,11 @@ def _bind(lib):
     lib.oracle_verify_tree_greedy.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, i32,
                                               P, P, P, P]
     lib.oracle_verify_tree_greedy.restype = i32
+    lib.oracle_verify_tree_sample.argtypes = [P, i64, i64, P, i64, i64, i32, i32, i32, i32, i32,
+                                              P, P, i32, dbl, i32, u64, u64, P, P, P, P]
+    lib.oracle_verify_tree_sample.restype = i32
+    lib.oracle_exact_probs_tree.argtypes = [P, P, P, P, i32, i32, dbl, i32, P]
+    lib.oracle_exact_probs_tree.restype = i32
     return lib
 
 
@@ -218,6 +223,48 @@ class Oracle:
         return acc, out, path, flags
 
 
+    def verify_tree_sample(self, target, draft, parent, node_tokens, max_depth, temperature,
+                           seed, offset=0, without_replacement=False, b0=0):
+        """Token-tree sampling verification (multi-round rejection); returns
+        (accepted_len[B], out_tokens[B, max_depth+1], out_path[B, max_depth+1], flags[B])."""
+        t, code, tsb, tsr = _logits(target)
+        d, dcode, dsb, dsr = _logits(draft)
+        B, N, V = t.shape
+        if dcode != code or d.shape != (B, N, V):
+            raise ValueError("draft logits must match the target's dtype and be [B, N, V]")
+        par = np.ascontiguousarray(np.asarray(parent, dtype=np.int32).reshape(N))
+        toks = np.ascontiguousarray(np.asarray(node_tokens, dtype=np.int32).reshape(B, N))
+        W = max_depth + 1
+        acc = np.zeros(B, np.int32)
+        out = np.zeros((B, W), np.int32)
+        path = np.zeros((B, W), np.int32)
+        flags = np.zeros(B, np.int32)
+        rc = self.lib.oracle_verify_tree_sample(_ptr(t), tsb, tsr, _ptr(d), dsb, dsr, code, B,
+                                                int(b0), N, V, _ptr(par), _ptr(toks),
+                                                int(max_depth), float(temperature),
+                                                int(bool(without_replacement)), int(seed),
+                                                int(offset), _ptr(acc), _ptr(out), _ptr(path),
+                                                _ptr(flags))
+        assert rc == 0
+        return acc, out, path, flags
+
+    def exact_probs_tree(self, t_logits, d_logits, parent, tokens, temperature,
+                         without_replacement=False) -> np.ndarray:
+        """Enumeration mode of the tree rule: P(final node = v, final token = j) as [N, V]."""
+        t = np.ascontiguousarray(np.asarray(t_logits, dtype=np.float64))
+        N, V = t.shape
+        d = np.ascontiguousarray(np.asarray(d_logits, dtype=np.float64).reshape(N, V))
+        par = np.ascontiguousarray(np.asarray(parent, dtype=np.int32).reshape(N))
+        x = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32).reshape(N))
+        prob = np.zeros((N, V), np.float64)
+        rc = self.lib.oracle_exact_probs_tree(_ptr(t), _ptr(d), _ptr(par), _ptr(x), N, V,
+                                              float(temperature), int(bool(without_replacement)),
+                                              _ptr(prob))
+        if rc != 0:
+            raise ValueError("invalid tree, row or token")
+        return prob
+
+
 def philox4x32_10(ctr, key):
     return _load().philox4x32_10(ctr, key)
 
@@ -246,6 +293,17 @@ def verify_greedy(target, draft_tokens):
 
 def verify_tree_greedy(target, parent, node_tokens, max_depth):
     return _load().verify_tree_greedy(target, parent, node_tokens, max_depth)
+
+
+def verify_tree_sample(target, draft, parent, node_tokens, max_depth, temperature, seed,
+                       offset=0, without_replacement=False, b0=0):
+    return _load().verify_tree_sample(target, draft, parent, node_tokens, max_depth, temperature,
+                                      seed, offset, without_replacement, b0)
+
+
+def exact_probs_tree(t_logits, d_logits, parent, tokens, temperature, without_replacement=False):
+    return _load().exact_probs_tree(t_logits, d_logits, parent, tokens, temperature,
+                                    without_replacement)
 
 
 def default() -> Oracle:

@@ -573,3 +573,259 @@ int oracle_verify_tree_greedy(const void *target, int64_t t_batch_stride, int64_
     free(l);
     return 0;
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* Token-tree SAMPLING verification: multi-round (recursive) rejection sampling
+ * [SD "Tree Attention: Verifying Many Candidates at Once", the paragraph after
+ * build_tree_attn (SpecInfer's rule)].  At an accepted node v with children c_1 < c_2 <
+ * ... (node-index order = the order the drafter drew them from q_v):
+ *   test c_r's token x with the single-candidate rule against the CURRENT (p, q):
+ *   accept iff u * q(x) < p(x), u = U(b, c_r - 1, 0); an accepted child becomes the new v;
+ *   a rejection replaces p by the residual (p - q)+ / ||(p - q)+||_1 and, when the
+ *   siblings were drawn without replacement, q by q with x removed, renormalised.
+ * When every child of v is rejected the final token is drawn from the last residual;
+ * at a leaf it is the bonus drawn from p_v; both with u' = U(b, v, 1) by inverse CDF.
+ * With a chain-shaped tree (node i's only child is i + 1) this is exactly
+ * oracle_verify_sample, uniforms included.
+ * Readings: a residual of mass 0 leaves p unchanged (flagged); without
+ * replacement a q with no mass left is 0 everywhere (a later sibling is then accepted iff
+ * p(x) > 0, and the residual is p).  Validity: every target row and the draft row of
+ * every node with children must be a distribution, every token in [0, V), the tree
+ * well-formed and no deeper than max_depth; otherwise the sequence (or, for the tree,
+ * every sequence) is -1.
+ *   target, draft: [B][N][V] (row v: the target's / drafter's logits after the path to v)
+ *   parent[N], node_tokens[B][N] as in oracle_verify_tree_greedy.
+ * Outputs (max_depth + 1 wide, -1 padded): accepted_len[b] = depth of the final node,
+ * out_tokens[b] = path tokens without the root then the final token, out_path[b] = node
+ * ids root..final node, flags[b] as in oracle_verify_sample.                           */
+/* ------------------------------------------------------------------------------------ */
+
+/* After a rejected candidate x: r <- (p - q)+ (returns its mass R), p <- r / R (unchanged
+ * if R == 0; *fell_back is set then), and without replacement q <- q without x,
+ * renormalised.                                                                         */
+static double reject_update(double *p, double *q, int V, int x, int without_replacement,
+                            double *r, int *fell_back)
+{
+    double R = 0.0;
+    for (int j = 0; j < V; ++j) {
+        double d = p[j] - q[j];
+        r[j] = d > 0.0 ? d : 0.0;
+        R += r[j];
+    }
+    *fell_back = !(R > 0.0);
+    if (R > 0.0)
+        for (int j = 0; j < V; ++j)
+            p[j] = r[j] / R;
+    if (without_replacement) {
+        q[x] = 0.0;
+        double Q = 0.0;
+        for (int j = 0; j < V; ++j)
+            Q += q[j];
+        for (int j = 0; j < V; ++j)
+            q[j] = Q > 0.0 ? q[j] / Q : 0.0;
+    }
+    return R;
+}
+
+/* depth[] of a well-formed tree no deeper than max_depth; returns 0 otherwise. */
+static int tree_depths(const int32_t *parent, int N, int max_depth, int *depth)
+{
+    if (N < 1 || parent[0] != -1)
+        return 0;
+    depth[0] = 0;
+    for (int v = 1; v < N; ++v) {
+        if (parent[v] < 0 || parent[v] >= v)
+            return 0;
+        depth[v] = depth[parent[v]] + 1;
+        if (depth[v] > max_depth)
+            return 0;
+    }
+    return 1;
+}
+
+int oracle_verify_tree_sample(const void *target, int64_t t_batch_stride, int64_t t_row_stride,
+                              const void *draft, int64_t d_batch_stride, int64_t d_row_stride,
+                              int dtype, int B, int b0, int N, int V, const int32_t *parent,
+                              const int32_t *node_tokens, int max_depth, double T,
+                              int without_replacement, uint64_t seed, uint64_t offset,
+                              int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
+                              int32_t *flags)
+{
+    int W = max_depth + 1;
+    for (int b = 0; b < B; ++b) {
+        accepted_len[b] = -1;
+        flags[b] = 0;
+        for (int i = 0; i < W; ++i) {
+            out_tokens[(int64_t)b * W + i] = -1;
+            if (out_path)
+                out_path[(int64_t)b * W + i] = -1;
+        }
+    }
+    size_t rowsz = sizeof(double) * (size_t)V;
+    int *depth = (int *)malloc(sizeof(int) * (size_t)N);
+    int *nchild = (int *)malloc(sizeof(int) * (size_t)N);
+    double *l = (double *)malloc(rowsz);
+    double *p = (double *)malloc(rowsz);
+    double *q = (double *)malloc(rowsz);
+    double *r = (double *)malloc(rowsz);
+    if (!depth || !nchild || !l || !p || !q || !r) {
+        free(depth);
+        free(nchild);
+        free(l);
+        free(p);
+        free(q);
+        free(r);
+        return -1;
+    }
+    int tree_ok = tree_depths(parent, N, max_depth, depth);
+    for (int v = 0; v < N; ++v)
+        nchild[v] = 0;
+    for (int v = 1; v < N && tree_ok; ++v)
+        nchild[parent[v]]++;
+    for (int b = 0; b < B && tree_ok; ++b) {
+        /* validity of every row the walk may read, and of every token */
+        int ok = 1;
+        for (int v = 0; v < N && ok; ++v) {
+            load_row(target, dtype, (int64_t)b * t_batch_stride + (int64_t)v * t_row_stride, V, l);
+            ok = softmax_row(l, V, T, p, NULL, NULL) == 0;
+            if (ok && nchild[v] > 0) {
+                load_row(draft, dtype, (int64_t)b * d_batch_stride + (int64_t)v * d_row_stride, V, l);
+                ok = softmax_row(l, V, T, q, NULL, NULL) == 0;
+            }
+        }
+        for (int v = 1; v < N && ok; ++v) {
+            int32_t tok = node_tokens[(int64_t)b * N + v];
+            ok = tok >= 0 && tok < V;
+        }
+        if (!ok)
+            continue;
+
+        /* the walk from the root; after a rejection r holds the unnormalised residual
+         * (p - q)+ of mass Rr that the final draw uses, exactly as the chain rule does */
+        int v = 0, rejected = 0;
+        double Rr = 0.0;
+        for (;;) {
+            rejected = 0;
+            load_row(target, dtype, (int64_t)b * t_batch_stride + (int64_t)v * t_row_stride, V, l);
+            softmax_row(l, V, T, p, NULL, NULL);
+            if (nchild[v] > 0) {
+                load_row(draft, dtype, (int64_t)b * d_batch_stride + (int64_t)v * d_row_stride, V, l);
+                softmax_row(l, V, T, q, NULL, NULL);
+            }
+            int next = -1;
+            for (int c = v + 1; c < N && next < 0; ++c) {
+                if (parent[c] != v)
+                    continue;
+                int x = node_tokens[(int64_t)b * N + c];
+                double u = oracle_uniform(seed, offset, (uint32_t)(b0 + b), (uint32_t)(c - 1), 0u);
+                if (q[x] > 0.0 && fabs(u - p[x] / q[x]) < ACCEPT_WINDOW)
+                    flags[b] |= FLAG_ACCEPT_NEAR_THRESHOLD;
+                if (u * q[x] < p[x]) {
+                    next = c; /* accepted */
+                } else {
+                    int fell_back = 0;
+                    Rr = reject_update(p, q, V, x, without_replacement, r, &fell_back);
+                    rejected = !fell_back;
+                    if (Rr < RESIDUAL_SMALL)
+                        flags[b] |= FLAG_RESIDUAL_NEAR_ZERO;
+                    if (fell_back)
+                        flags[b] |= FLAG_RESIDUAL_FALLBACK;
+                }
+            }
+            if (next < 0)
+                break;
+            v = next;
+        }
+
+        /* the final token: from the last residual after the children were all rejected,
+         * from p_v at a leaf (or where the last residual had no mass) */
+        double R = 0.0, margin = 0.0;
+        const double *w = p;
+        if (rejected) {
+            w = r;
+            R = Rr;
+        } else {
+            for (int j = 0; j < V; ++j)
+                R += p[j];
+        }
+        double u2 = oracle_uniform(seed, offset, (uint32_t)(b0 + b), (uint32_t)v, 1u);
+        int tok = inverse_cdf(w, V, R, u2, &margin);
+        if (margin < CDF_WINDOW)
+            flags[b] |= FLAG_CDF_NEAR_BOUNDARY;
+        int d = depth[v];
+        for (int w = v, s = d; s >= 0; --s) {
+            if (out_path)
+                out_path[(int64_t)b * W + s] = w;
+            if (s >= 1)
+                out_tokens[(int64_t)b * W + s - 1] = node_tokens[(int64_t)b * N + w];
+            w = parent[w];
+        }
+        out_tokens[(int64_t)b * W + d] = tok;
+        accepted_len[b] = d;
+    }
+    free(depth);
+    free(nchild);
+    free(l);
+    free(p);
+    free(q);
+    free(r);
+    return 0;
+}
+
+/* Enumeration mode for the tree rule: for one sequence with fixed rows and fixed tokens,
+ * prob[v * V + j] = P(the walk ends at node v and the final token is j), each uniform
+ * replaced by its branch weights.  Logits fp64 [N][V].  Returns -1 on an invalid input. */
+int oracle_exact_probs_tree(const double *t_logits, const double *d_logits, const int32_t *parent,
+                            const int32_t *tokens, int N, int V, double T, int without_replacement,
+                            double *prob)
+{
+    size_t rowsz = sizeof(double) * (size_t)V;
+    int *depth = (int *)malloc(sizeof(int) * (size_t)N);
+    double *reach = (double *)malloc(sizeof(double) * (size_t)N);
+    double *p = (double *)malloc(rowsz);
+    double *q = (double *)malloc(rowsz);
+    double *r = (double *)malloc(rowsz);
+    int rc = 0;
+    if (!depth || !reach || !p || !q || !r || !tree_depths(parent, N, N, depth)) {
+        rc = -1;
+        goto done;
+    }
+    for (int j = 0; j < N * V; ++j)
+        prob[j] = 0.0;
+    for (int v = 0; v < N; ++v)
+        reach[v] = v == 0 ? 1.0 : 0.0;
+    for (int v = 0; v < N; ++v) { /* parents come before children */
+        int has_child = 0;
+        for (int c = v + 1; c < N; ++c)
+            has_child |= parent[c] == v;
+        if (softmax_row(t_logits + (size_t)v * V, V, T, p, NULL, NULL) != 0 ||
+            (has_child && softmax_row(d_logits + (size_t)v * V, V, T, q, NULL, NULL) != 0)) {
+            rc = -1;
+            goto done;
+        }
+        double rest = 1.0; /* probability that the children tested so far were all rejected */
+        for (int c = v + 1; c < N; ++c) {
+            if (parent[c] != v)
+                continue;
+            int x = tokens[c];
+            if (x < 0 || x >= V) {
+                rc = -1;
+                goto done;
+            }
+            double a = accept_probability(p[x], q[x]);
+            reach[c] += reach[v] * rest * a;
+            rest *= 1.0 - a;
+            int fell_back = 0;
+            reject_update(p, q, V, x, without_replacement, r, &fell_back);
+        }
+        for (int j = 0; j < V; ++j)
+            prob[(size_t)v * V + j] += reach[v] * rest * p[j];
+    }
+done:
+    free(depth);
+    free(reach);
+    free(p);
+    free(q);
+    free(r);
+    return rc;
+}

@@ -440,6 +440,192 @@ def pin_tree_bruteforce(orc):
 
 
 # --------------------------------------------------------------------------------------
+# Token-tree sampling: multi-round rejection [SD "Tree Attention", the paragraph on
+# SpecInfer's rule].  The rule is lossless for a drafter that draws each node's children
+# from q at that node, with or without replacement.
+# --------------------------------------------------------------------------------------
+def _draw_law(q, k, without_replacement):
+    """Every ordered k-tuple of tokens a drafter draws from q, with its probability."""
+    V = len(q)
+    for xs in itertools.product(range(V), repeat=k):
+        pr, left, used = 1.0, 1.0, set()
+        for x in xs:
+            if without_replacement:
+                if x in used or left <= 0.0:
+                    pr = 0.0
+                    break
+                pr *= q[x] / left
+                left -= q[x]
+                used.add(x)
+            else:
+                pr *= q[x]
+        if pr > 0.0:
+            yield xs, pr
+
+
+def tree_round_law(orc, y, parent, V, T, wor, salt_p=11, salt_q=23, mask_p=0.0):
+    """Law of the tokens one tree round emits after prefix y, averaged over the drafter's
+    draws of every node's children and over the rule's uniforms (enumeration mode)."""
+    N = len(parent)
+    children = [[c for c in range(N) if parent[c] == v] for v in range(N)]
+
+    def path_tokens(v, tok):
+        out = []
+        while v != 0:
+            out.append(tok[v])
+            v = parent[v]
+        return tuple(reversed(out))
+
+    assignments = [({}, 1.0)]
+    for v in range(N):  # parents before children: path(v) is known when v's children are drawn
+        if not children[v]:
+            continue
+        grown = []
+        for tok, pr in assignments:
+            q = _softmax(_tiny_model(y + path_tokens(v, tok), V, salt_q, 1.5), T)
+            for xs, pq in _draw_law(q, len(children[v]), wor):
+                t2 = dict(tok)
+                t2.update(zip(children[v], xs))
+                grown.append((t2, pr * pq))
+        assignments = grown
+    law = {}
+    for tok, pr in assignments:
+        tokens = [0] + [tok[c] for c in range(1, N)]
+        t_rows = [_tiny_model(y + path_tokens(v, tok), V, salt_p, 1.5, mask_p) for v in range(N)]
+        d_rows = [_tiny_model(y + path_tokens(v, tok), V, salt_q, 1.5) for v in range(N)]
+        P = orc.exact_probs_tree(np.array(t_rows), np.array(d_rows), parent, tokens, T, wor)
+        for v in range(N):
+            for j in range(V):
+                if P[v, j] > 0.0:
+                    z = path_tokens(v, tok) + (j,)
+                    law[z] = law.get(z, 0.0) + pr * P[v, j]
+    return law
+
+
+def pin_tree_sample_lossless(orc, cases=(([-1, 0, 0], 3, 3, 0.8, False, 0.0),
+                                         ([-1, 0, 0], 3, 3, 0.8, True, 0.0),
+                                         ([-1, 0, 0, 0], 4, 2, 1.1, True, 0.25),
+                                         ([-1, 0, 0, 0], 3, 2, 1.0, True, 0.0),
+                                         ([-1, 0, 0, 1], 3, 3, 0.9, False, 0.3),
+                                         ([-1, 0, 1, 1, 0], 3, 3, 1.2, True, 0.0))):
+    """Composed rounds of the tree rule emit exactly the target model's law (< 1e-12)."""
+    for parent, V, L, T, wor, mask in cases:
+        got, frontier = {}, {(): 1.0}
+        while frontier:
+            nxt = {}
+            for y, w in frontier.items():
+                if len(y) >= L:
+                    got[y[:L]] = got.get(y[:L], 0.0) + w
+                    continue
+                for z, pz in tree_round_law(orc, y, parent, V, T, wor, mask_p=mask).items():
+                    nxt[y + z] = nxt.get(y + z, 0.0) + w * pz
+            frontier = nxt
+        want = target_law(V, L, T, mask_p=mask)
+        keys = set(got) | set(want)
+        err = max(abs(got.get(k, 0.0) - want.get(k, 0.0)) for k in keys)
+        assert err < 1e-12, (parent, V, L, T, wor, mask, err)
+
+
+def _children_draws(rs, q, n, k, without_replacement):
+    """n independent drafter draws of k ordered children from q ([n, k] tokens)."""
+    if not without_replacement:
+        return rs.choice(len(q), size=(n, k), p=q).astype(np.int32)
+    # Gumbel keys: sorting log q + G gives sequential sampling without replacement
+    with np.errstate(divide="ignore"):
+        keys = np.log(q)[None, :] + rs.gumbel(size=(n, len(q)))
+    return np.argsort(-keys, axis=1)[:, :k].astype(np.int32)
+
+
+def pin_tree_sample_chi2(orc, trials=200_000, V=5, T=0.9, alpha=1e-3):
+    """The Philox-driven tree sampler: over many rounds (fresh drafter draws and uniforms)
+    the first emitted token follows p at the root and, after child c is accepted, the
+    second follows p at c (chi-squared at alpha)."""
+    rs = np.random.RandomState(4343)
+    parent = [-1, 0, 0, 0]
+    t_rows = rs.normal(0, 1.5, (4, V)).astype(np.float32)
+    d_rows = rs.normal(0, 1.5, (4, V)).astype(np.float32)
+    t_rows[0, 1] = -np.inf  # a token the target never emits
+    p = [_softmax(t_rows[v].astype(np.float64), T) for v in range(4)]
+    q0 = _softmax(d_rows[0].astype(np.float64), T)
+    target = np.ascontiguousarray(np.broadcast_to(t_rows, (trials, 4, V)))
+    draft = np.ascontiguousarray(np.broadcast_to(d_rows, (trials, 4, V)))
+    for wor in (False, True):
+        toks = np.zeros((trials, 4), np.int32)
+        toks[:, 1:] = _children_draws(rs, q0, trials, 3, wor)
+        acc, out, path, _ = orc.verify_tree_sample(target, draft, parent, toks, 1, T, seed=77,
+                                                   offset=int(wor), without_replacement=wor)
+        assert ((acc == 0) | (acc == 1)).all()
+        live = p[0] > 0
+        cnt = np.bincount(out[:, 0], minlength=V)
+        assert (cnt[~live] == 0).all()
+        assert stats.chisquare(cnt[live], trials * p[0][live]).pvalue > alpha
+        for c in (1, 2, 3):  # the bonus after child c
+            sel = path[:, 1] == c
+            cnt = np.bincount(out[sel, 1], minlength=V)
+            assert stats.chisquare(cnt, sel.sum() * p[c]).pvalue > alpha
+
+
+def pin_chain_tree_sample_equals_chain(orc):
+    """On a chain-shaped tree the tree rule is the chain rule, uniforms included: the same
+    tokens, lengths and flags, bit for bit, in both sibling modes."""
+    rs = np.random.RandomState(31)
+    for gamma, V, T in ((1, 7, 1.0), (4, 40, 0.8), (6, 100, 1.3)):
+        B = 96
+        t = rs.normal(0, 2, (B, gamma + 1, V)).astype(np.float32)
+        d = (t[:, :gamma] + rs.normal(0, 1, (B, gamma, V))).astype(np.float32)
+        t[rs.rand(B, gamma + 1, V) < 0.1] = -np.inf
+        t[:, :, 0] = 0.0  # every row keeps a finite entry
+        x = np.array([[rs.choice(V, p=_softmax(d[b, i].astype(np.float64), T))
+                       for i in range(gamma)] for b in range(B)], np.int32)
+        acc, out, flags = orc.verify_sample(t, d, x, T, seed=5, offset=3)
+        parent = [-1] + list(range(gamma))
+        dd = np.concatenate([d, np.zeros((B, 1, V), np.float32)], axis=1)  # leaf row unused
+        toks = np.concatenate([np.zeros((B, 1), np.int32), x], axis=1)
+        for wor in (False, True):
+            acc2, out2, path2, flags2 = orc.verify_tree_sample(t, dd, parent, toks, gamma, T, 5, 3,
+                                                               without_replacement=wor)
+            assert (acc2 == acc).all() and (out2 == out).all() and (flags2 == flags).all()
+            for b in range(B):
+                assert list(path2[b, :acc[b] + 1]) == list(range(acc[b] + 1))
+
+
+def pin_tree_sample_invariants(orc):
+    """Outputs of random trees: a root path of parent-child steps, its node tokens, one
+    final token with positive weight, -1 padding; bad input gives -1."""
+    rs = np.random.RandomState(57)
+    for N, V in ((1, 3), (6, 4), (20, 9), (40, 30)):
+        B = 60
+        parent = random_tree(rs, N)
+        depth = [0] * N
+        for v in range(1, N):
+            depth[v] = depth[parent[v]] + 1
+        D = max(depth)
+        t = rs.normal(0, 2, (B, N, V)).astype(np.float32)
+        d = rs.normal(0, 2, (B, N, V)).astype(np.float32)
+        t[rs.rand(B, N, V) < 0.2] = -np.inf
+        t[:, :, V - 1] = 1.0
+        toks = rs.randint(0, V, (B, N)).astype(np.int32)
+        for wor in (False, True):
+            acc, out, path, _ = orc.verify_tree_sample(t, d, parent, toks, D, 0.9, 11, 0, wor)
+            for b in range(B):
+                k = acc[b]
+                assert 0 <= k <= D and path[b, 0] == 0 and (path[b, k + 1:] == -1).all()
+                for s in range(1, k + 1):
+                    assert parent[path[b, s]] == path[b, s - 1]
+                    assert out[b, s - 1] == toks[b, path[b, s]]
+                assert 0 <= out[b, k] < V and np.isfinite(t[b, path[b, k], out[b, k]])
+                assert (out[b, k + 1:] == -1).all()
+    t = np.zeros((3, 3, 4), np.float32)
+    d = np.zeros((3, 3, 4), np.float32)
+    t[0, 2, 1] = np.nan          # a target row
+    d[1, 0, :] = -np.inf         # the draft row of a node with children
+    toks = np.zeros((3, 3), np.int32)
+    toks[2, 1] = 4               # a token out of range
+    acc, out, path, _ = orc.verify_tree_sample(t, d, [-1, 0, 0], toks, 1, 1.0, 0)
+    assert (acc == -1).all() and (out == -1).all() and (path == -1).all()
+
+
+# --------------------------------------------------------------------------------------
 # P10: row max / log-sum-exp against scipy's logsumexp [SD apply_temperature]
 # --------------------------------------------------------------------------------------
 def pin_row_stats(orc):
@@ -465,4 +651,6 @@ ALL_PINS = [
     pin_identical_rows_accept_all, pin_one_hot_equals_greedy, pin_one_hot_draft_accept_prob,
     pin_round_invariants, pin_worked_example, pin_acceptance_rate, pin_greedy_textbook,
     pin_tree_printed_depths, pin_chain_tree_equals_greedy, pin_tree_bruteforce, pin_row_stats,
+    pin_tree_sample_lossless, pin_tree_sample_chi2, pin_chain_tree_sample_equals_chain,
+    pin_tree_sample_invariants,
 ]

@@ -14,6 +14,8 @@ import oracle_pins as pins
 
 chi2_quick = functools.partial(pins.pin_chi2_sampler, trials=200_000)
 chi2_quick.__name__ = "pin_chi2_sampler_quick"
+tree_chi2_quick = functools.partial(pins.pin_tree_sample_chi2, trials=100_000)
+tree_chi2_quick.__name__ = "pin_tree_sample_chi2_quick"
 
 MUTATIONS = [
     ("residual_sign", "double d = p[j] - q[j];\n            r[j] = d > 0.0 ? d : 0.0;",
@@ -49,6 +51,16 @@ MUTATIONS = [
      [pins.pin_tree_bruteforce]),
     ("lse_missing_temperature", "if (l[j] / T > m)\n            m = l[j] / T;",
      "if (l[j] > m)\n            m = l[j];", [pins.pin_row_stats]),
+    ("tree_siblings_against_original_p", "            p[j] = r[j] / R;", "            p[j] = p[j];",
+     [pins.pin_tree_sample_lossless, tree_chi2_quick]),
+    ("tree_q_not_renormalised", "q[j] = Q > 0.0 ? q[j] / Q : 0.0;", "q[j] = Q > 0.0 ? q[j] : 0.0;",
+     [pins.pin_tree_sample_lossless]),
+    ("tree_rejected_token_kept_in_q", "        q[x] = 0.0;", "        q[x] = q[x];",
+     [pins.pin_tree_sample_lossless]),
+    ("tree_uniform_index", "(uint32_t)(c - 1), 0u);", "(uint32_t)c, 0u);",
+     [pins.pin_chain_tree_sample_equals_chain]),
+    ("tree_sampler_accept_swapped", "if (u * q[x] < p[x]) {", "if (u * p[x] < q[x]) {",
+     [tree_chi2_quick, pins.pin_chain_tree_sample_equals_chain]),
 ]
 
 
