@@ -589,10 +589,11 @@ int oracle_verify_tree_greedy(const void *target, int64_t t_batch_stride, int64_
  * oracle_verify_sample, uniforms included.
  * Readings: a residual of mass 0 leaves p unchanged (flagged); without
  * replacement a q with no mass left is 0 everywhere (a later sibling is then accepted iff
- * p(x) > 0, and the residual is p).  Validity: every target row and the draft row of
- * every node with children must be a distribution, every token in [0, V), the tree
- * well-formed and no deeper than max_depth; otherwise the sequence (or, for the tree,
- * every sequence) is -1.
+ * p(x) > 0, and the residual is p).  Validity: every node token in [0, V) and every row
+ * the walk reads (the target row of each node it reaches, the draft row of each reached
+ * node that has children) a distribution -- a row the rule never reads cannot change the
+ * result; the tree well-formed and no deeper than max_depth.  Otherwise the sequence (or,
+ * for the tree, every sequence) is -1.
  *   target, draft: [B][N][V] (row v: the target's / drafter's logits after the path to v)
  *   parent[N], node_tokens[B][N] as in oracle_verify_tree_greedy.
  * Outputs (max_depth + 1 wide, -1 padded): accepted_len[b] = depth of the final node,
@@ -683,16 +684,8 @@ int oracle_verify_tree_sample(const void *target, int64_t t_batch_stride, int64_
     for (int v = 1; v < N && tree_ok; ++v)
         nchild[parent[v]]++;
     for (int b = 0; b < B && tree_ok; ++b) {
-        /* validity of every row the walk may read, and of every token */
+        /* every node token must be in range; rows are checked as the walk reads them */
         int ok = 1;
-        for (int v = 0; v < N && ok; ++v) {
-            load_row(target, dtype, (int64_t)b * t_batch_stride + (int64_t)v * t_row_stride, V, l);
-            ok = softmax_row(l, V, T, p, NULL, NULL) == 0;
-            if (ok && nchild[v] > 0) {
-                load_row(draft, dtype, (int64_t)b * d_batch_stride + (int64_t)v * d_row_stride, V, l);
-                ok = softmax_row(l, V, T, q, NULL, NULL) == 0;
-            }
-        }
         for (int v = 1; v < N && ok; ++v) {
             int32_t tok = node_tokens[(int64_t)b * N + v];
             ok = tok >= 0 && tok < V;
@@ -707,11 +700,13 @@ int oracle_verify_tree_sample(const void *target, int64_t t_batch_stride, int64_
         for (;;) {
             rejected = 0;
             load_row(target, dtype, (int64_t)b * t_batch_stride + (int64_t)v * t_row_stride, V, l);
-            softmax_row(l, V, T, p, NULL, NULL);
-            if (nchild[v] > 0) {
+            ok = softmax_row(l, V, T, p, NULL, NULL) == 0;
+            if (ok && nchild[v] > 0) {
                 load_row(draft, dtype, (int64_t)b * d_batch_stride + (int64_t)v * d_row_stride, V, l);
-                softmax_row(l, V, T, q, NULL, NULL);
+                ok = softmax_row(l, V, T, q, NULL, NULL) == 0;
             }
+            if (!ok)
+                break;
             int next = -1;
             for (int c = v + 1; c < N && next < 0; ++c) {
                 if (parent[c] != v)
@@ -737,6 +732,10 @@ int oracle_verify_tree_sample(const void *target, int64_t t_batch_stride, int64_
             v = next;
         }
 
+        if (!ok) {
+            flags[b] = 0;
+            continue;
+        }
         /* the final token: from the last residual after the children were all rejected,
          * from p_v at a leaf (or where the last residual had no mass) */
         double R = 0.0, margin = 0.0;

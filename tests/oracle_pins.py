@@ -617,12 +617,24 @@ def pin_tree_sample_invariants(orc):
                 assert (out[b, k + 1:] == -1).all()
     t = np.zeros((3, 3, 4), np.float32)
     d = np.zeros((3, 3, 4), np.float32)
-    t[0, 2, 1] = np.nan          # a target row
-    d[1, 0, :] = -np.inf         # the draft row of a node with children
+    t[0, 0, 1] = np.nan          # the root's target row
+    d[1, 0, :] = -np.inf         # the draft row of a reached node with children
     toks = np.zeros((3, 3), np.int32)
     toks[2, 1] = 4               # a token out of range
     acc, out, path, _ = orc.verify_tree_sample(t, d, [-1, 0, 0], toks, 1, 1.0, 0)
     assert (acc == -1).all() and (out == -1).all() and (path == -1).all()
+    # a row the walk never reads cannot matter: node 1's token has p = 0 at the root, so
+    # node 1 is always rejected and its child, node 2, never reached
+    t = rs.normal(0, 1, (40, 4, 6)).astype(np.float32)
+    d = rs.normal(0, 1, (40, 4, 6)).astype(np.float32)
+    t[:, 0, 3] = -np.inf
+    toks = np.tile(np.array([0, 3, 1, 2], np.int32), (40, 1))
+    ref = orc.verify_tree_sample(t, d, [-1, 0, 1, 0], toks, 2, 1.0, 9)
+    t[:, 2, :] = np.nan
+    d[:, 2, :] = np.nan
+    d[:, 1, :] = np.nan  # node 1 has a child but is never reached
+    got = orc.verify_tree_sample(t, d, [-1, 0, 1, 0], toks, 2, 1.0, 9)
+    assert all((a == b).all() for a, b in zip(ref, got)) and (ref[0] >= 0).all()
 
 
 # --------------------------------------------------------------------------------------
