@@ -31,15 +31,15 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "sample_b256"
-SECONDARY = ["greedy_b512", "tree_b64"]
+SECONDARY = ["greedy_b512", "tree_b64", "tree_sample_b64"]
 METRIC = "verified seqs/s"
 UNIT = "seqs/s"
 FALLBACK_HBM_GBS = 6800.0
 DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "max_tiles_kernel",
-                   "tree": "max_tiles_kernel"}
+                   "tree": "max_tiles_kernel", "tree_sample": "tree_sample_kernel"}
 STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
 STAGES = {"sample": ["row_stats", "decide", "residual_mass", "inverse_cdf", "redraw"],
-          "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"]}
+          "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"], "tree_sample": ["walk"]}
 
 
 def parse_args():
@@ -232,6 +232,23 @@ def make_call(name, inputs, dev, **ov):
             return sv.spec_verify_greedy(target, tokens, workspace=ws, accepted_len=acc, out_tokens=out)
         return call, (acc, out)
     N = cfg["N"]
+    if mode == "tree_sample":
+        ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_TREE_SAMPLE, B, N, V, dt),
+                         dtype=torch.uint8, device=dev)
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        out = torch.empty((B, inputs.max_depth + 1), dtype=torch.int32, device=dev)
+        path = torch.empty((B, inputs.max_depth + 1), dtype=torch.int32, device=dev)
+        step_counter = [0]
+
+        def call(target=inputs.target, tokens=inputs.node_tokens, draft=inputs.draft):
+            step_counter[0] += 1
+            return sv.spec_verify_tree_sample(target, draft, inputs.parent, tokens,
+                                              inputs.max_depth, inputs.temperature, inputs.seed,
+                                              step_counter[0],
+                                              without_replacement=inputs.without_replacement,
+                                              workspace=ws, accepted_len=acc, out_tokens=out,
+                                              out_path=path)
+        return call, (acc, out, path)
     ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_TREE, B, N, V, dt),
                      dtype=torch.uint8, device=dev)
     acc = torch.empty(B, dtype=torch.int32, device=dev)
@@ -312,6 +329,12 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
                      "traffic": committed_traffic(kernel, name)},
         "gpu_launches": steps * (nst if mode != "sample" or cfg["gamma"] > 0 else 4),
     }
+    if mode == "tree_sample":
+        # the walk reads only the rows of the nodes it reaches: the every-row byte count of
+        # the metric does not apply, and the kernel is bound by exponentials and latency
+        res.update({"hbm_gbs_step": None, "frac_of_8tbs_step": None, "roofline": None,
+                    "lazy": "one CTA per sequence reads only the rows of the nodes its walk reaches",
+                    "mean_path_nodes": float(acc[acc >= 0].mean().item() + 1) if (acc >= 0).any() else None})
     return res, inputs, call
 
 
@@ -326,8 +349,9 @@ def measure_e2e(name, inputs, steps, dev, **ov):
     mode = cfg["mode"]
     host_in = {}
     dev_in = {}
-    keys = ["target", "draft", "draft_tokens"] if mode == "sample" else (
-        ["target", "draft_tokens"] if mode == "greedy" else ["target", "node_tokens"])
+    keys = {"sample": ["target", "draft", "draft_tokens"], "greedy": ["target", "draft_tokens"],
+            "tree": ["target", "node_tokens"],
+            "tree_sample": ["target", "draft", "node_tokens"]}[mode]
     for k in keys:
         t = getattr(inputs, k)
         host_in[k] = t.cpu().pin_memory()
@@ -344,6 +368,8 @@ def measure_e2e(name, inputs, steps, dev, **ov):
             call(dev_in["target"], dev_in["draft"], dev_in["draft_tokens"])
         elif mode == "greedy":
             call(dev_in["target"], dev_in["draft_tokens"])
+        elif mode == "tree_sample":
+            call(dev_in["target"], dev_in["node_tokens"], dev_in["draft"])
         else:
             call(dev_in["target"], dev_in["node_tokens"])
         for h, o in zip(host_out, outs):
@@ -384,6 +410,13 @@ def oracle_run(name, inputs, threads):
     elif mode == "greedy":
         x = inputs.draft_tokens.cpu().numpy()
         fn = lambda r: orc.verify_greedy(t[r[0]:r[1]], x[r[0]:r[1]])
+    elif mode == "tree_sample":
+        d = oracle.as_oracle_logits(inputs.draft)
+        par = inputs.parent.cpu().numpy()
+        x = inputs.node_tokens.cpu().numpy()
+        fn = lambda r: orc.verify_tree_sample(t[r[0]:r[1]], d[r[0]:r[1]], par, x[r[0]:r[1]],
+                                              inputs.max_depth, inputs.temperature, inputs.seed, 0,
+                                              inputs.without_replacement, b0=r[0])
     else:
         par = inputs.parent.cpu().numpy()
         x = inputs.node_tokens.cpu().numpy()

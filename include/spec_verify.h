@@ -62,7 +62,8 @@ typedef enum {
     SV_MODE_SAMPLE = 0,    /* spec_verify_sample:      rows = gamma */
     SV_MODE_GREEDY = 1,    /* spec_verify_greedy:      rows = gamma */
     SV_MODE_TREE = 2,      /* spec_verify_tree_greedy: rows = N     */
-    SV_MODE_ROW_STATS = 3  /* spec_verify_row_stats:   rows = rows_per_seq */
+    SV_MODE_ROW_STATS = 3, /* spec_verify_row_stats:   rows = rows_per_seq */
+    SV_MODE_TREE_SAMPLE = 4 /* spec_verify_tree_sample: rows = N    */
 } sv_mode;
 
 /* Limits checked on the host (SV_ERR_INVALID_ARG beyond them). */
@@ -144,6 +145,40 @@ sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_str
                                   int max_depth, int32_t *accepted_len, int32_t *out_tokens,
                                   int32_t *out_path, void *workspace, size_t workspace_bytes,
                                   void *stream);
+
+/*
+ * Token-tree SAMPLING verification by multi-round (recursive) rejection [SD "Tree
+ * Attention", the paragraph on SpecInfer's rule].
+ *
+ *   target_logits  [B][N][V]  row v: the target's logits after the path to node v (p_v).
+ *   draft_logits   [B][N][V]  row v: the drafter's logits at node v (q_v), from which v's
+ *                             children were drawn; rows of leaves are never read.
+ *   parent, node_tokens, max_depth: as spec_verify_tree_greedy.  Children are tested in
+ *                             increasing node index (the order they were drawn).
+ *   temperature, seed, offset: as spec_verify_sample (applied to both models).
+ *   without_replacement       nonzero if each node's children were drawn from q_v without
+ *                             replacement (q is then renormalised over the untested ones).
+ * From the root: test the children of the current node in order with the single-candidate
+ * rule (accept child c iff u q(x) < p(x), u = U(b, c - 1, purpose 0)); an accepted child
+ * becomes the current node; a rejection replaces p by (p - q)+ normalised (and removes x
+ * from q without replacement).  When all children are rejected the final token is drawn
+ * from the last residual, at a leaf from p_v (inverse CDF, u' = U(b, v, purpose 1)).  A
+ * chain-shaped tree gives spec_verify_sample's rule.  Outputs as spec_verify_tree_greedy:
+ * accepted_len = depth of the final node, out_tokens = path tokens then the final token,
+ * out_path = node ids (may be NULL).  Rows are read lazily, one CTA per sequence: only the
+ * rows of the nodes the walk reaches.  A malformed or too deep tree makes every sequence
+ * -1; a token of b outside [0, V), or a row the walk reads that is not a distribution (NaN,
+ * +inf, no finite entry), makes sequence b -1.  Workspace: B * ceil(V / unit) floats
+ * (spec_verify_workspace_size(SV_MODE_TREE_SAMPLE, B, N, V, dtype)).
+ */
+sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_stride,
+                                  int64_t t_row_stride, const void *draft_logits,
+                                  int64_t d_batch_stride, int64_t d_row_stride, sv_dtype dtype,
+                                  int B, int N, int V, const int32_t *parent,
+                                  const int32_t *node_tokens, int max_depth, float temperature,
+                                  uint64_t seed, uint64_t offset, int without_replacement,
+                                  int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
+                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Greedy verification that allocates nothing and takes no workspace.  (The pages have no

@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     spec_verify_row_stats,
     spec_verify_sample,
     spec_verify_tree_greedy,
+    spec_verify_tree_sample,
     spec_verify_uniforms,
     spec_verify_workspace_size,
 )
@@ -23,6 +24,7 @@ __all__ = [
     "spec_verify_row_stats",
     "spec_verify_sample",
     "spec_verify_tree_greedy",
+    "spec_verify_tree_sample",
     "spec_verify_uniforms",
     "spec_verify_workspace_size",
 ]

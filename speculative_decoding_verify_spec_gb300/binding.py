@@ -17,7 +17,7 @@ import torch
 from . import _build
 
 SV_OK = 0
-MODE_SAMPLE, MODE_GREEDY, MODE_TREE, MODE_ROW_STATS = 0, 1, 2, 3
+MODE_SAMPLE, MODE_GREEDY, MODE_TREE, MODE_ROW_STATS, MODE_TREE_SAMPLE = 0, 1, 2, 3, 4
 FP32, BF16 = 0, 1
 
 _lock = threading.Lock()
@@ -55,6 +55,9 @@ def load_library() -> ctypes.CDLL:
         lib.spec_verify_tree_greedy.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, i32, P, P, P,
                                                 P, sz, P]
         lib.spec_verify_tree_greedy.restype = i32
+        lib.spec_verify_tree_sample.argtypes = [P, i64, i64, P, i64, i64, i32, i32, i32, i32, P, P, i32,
+                                                f32, u64, u64, i32, P, P, P, P, sz, P]
+        lib.spec_verify_tree_sample.restype = i32
         lib.spec_verify_row_stats.argtypes = [P, i64, i64, i32, i32, i32, i32, f32, P, P, P, sz, P]
         lib.spec_verify_row_stats.restype = i32
         lib.spec_verify_uniforms.argtypes = [u64, u64, i32, i32, i32, P, P]
@@ -203,6 +206,42 @@ def spec_verify_tree_greedy(target: torch.Tensor, parent: torch.Tensor, node_tok
                                      out_path.data_ptr() if out_path is not None else None,
                                      ws.data_ptr(), wsb, _stream(dev))
     _check(st, "spec_verify_tree_greedy")
+    return accepted_len, out_tokens, out_path
+
+
+def spec_verify_tree_sample(target: torch.Tensor, draft: torch.Tensor, parent: torch.Tensor,
+                            node_tokens: torch.Tensor, max_depth: int, temperature: float, seed: int,
+                            offset: int = 0, *, without_replacement: bool = False,
+                            with_path: bool = True, workspace=None, accepted_len=None,
+                            out_tokens=None, out_path=None):
+    """Token-tree sampling verification (multi-round rejection); returns (accepted_len [B],
+    out_tokens [B, D+1], out_path [B, D+1] or None)."""
+    lib = load_library()
+    tsb, tsr = _logits3(target, "target")
+    dsb, dsr = _logits3(draft, "draft")
+    B, N, V = target.shape
+    dt = _dtype_code(target)
+    if draft.dtype != target.dtype or tuple(draft.shape) != (B, N, V):
+        raise ValueError("draft must be [B, N, V] with the target's dtype")
+    par = _ints(parent, "parent", (N,))
+    tok = _ints(node_tokens, "node_tokens", (B, N))
+    dev = target.device
+    W = int(max_depth) + 1
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, W), dtype=torch.int32, device=dev)
+    if with_path and out_path is None:
+        out_path = torch.empty((B, W), dtype=torch.int32, device=dev)
+    ws, wsb = _workspace(MODE_TREE_SAMPLE, B, N, V, dt, dev, workspace)
+    st = lib.spec_verify_tree_sample(target.data_ptr(), tsb, tsr, draft.data_ptr(), dsb, dsr, dt, B,
+                                     N, V, par.data_ptr(), tok.data_ptr(), int(max_depth),
+                                     float(temperature), int(seed) & (2**64 - 1),
+                                     int(offset) & (2**64 - 1), int(bool(without_replacement)),
+                                     accepted_len.data_ptr(), out_tokens.data_ptr(),
+                                     out_path.data_ptr() if out_path is not None else None,
+                                     ws.data_ptr(), wsb, _stream(dev))
+    _check(st, "spec_verify_tree_sample")
     return accepted_len, out_tokens, out_path
 
 

@@ -1,0 +1,401 @@
+// sv_tree_sample.cu -- token-tree SAMPLING verification: multi-round (recursive) rejection.
+//
+// Method ("7.6 Speculative Decoding: Draft Models, Medusa, EAGLE & Lookahead", "Tree
+// Attention: Verifying Many Candidates at Once", the paragraph on SpecInfer's rule): at an
+// accepted node v the children are tested in order against the current (p, q) with the
+// single-candidate rule; a rejection replaces p by the normalised residual (p - q)+ and,
+// when the siblings were drawn without replacement, q by q without the rejected token,
+// renormalised; when every child is rejected the final token comes from the last
+// residual, at a leaf it is the bonus drawn from p at the leaf.
+//
+// The walk is sequential and data-dependent, so it runs lazily: one CTA per sequence
+// reads only the rows of the nodes it reaches.  p and q are never materialised.  With
+// p0 = softmax(t_v / T) and q0 = softmax(d_v / T), after r rejections
+//     p_r(j) = w_r(j) / D_r,   w_r(j) = max(p0(j) - a_r(j) q0(j), 0),
+//     q_r(j) = s_r q0(j)  (0 for a token removed from q),
+// where a_r(j) = A_r for every token still in q and the value A had when the token was
+// removed for the others.  A rejection at round r sets A_{r+1} = A_r + D_r s_r and
+// D_{r+1} = sum_j w_{r+1}(j) (one pass over the row pair); without replacement s_{r+1} =
+// 1 / (1 - the removed tokens' q0 mass).  (Induction on r: for a token still in q,
+// p_r - q_r = (max(p0 - A_r q0, 0) - D_r s_r q0) / D_r, whose positive part is
+// max(p0 - A_{r+1} q0, 0) / D_r.)  Each pass stores one mass per unit of res_tile_elems
+// logits, and the final draw walks those masses and then one unit, as the chain's draw.
+//
+// Arithmetic mirrors the chain sampler: weights 2^((x - M) c) with x - M exact, explicitly
+// rounded products, fp32 sums in a fixed order, Kahan prefixes inside the chosen unit.
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+constexpr int kTsThreads = 1024;
+constexpr int kTsWarps = kTsThreads / 32;
+constexpr int kMaxRemoved = 64;  // tokens removed from q at one node (without replacement)
+
+__device__ __forceinline__ float tweight(float x, float M, float c) { return ex2(__fmul_rn(__fsub_rn(x, M), c)); }
+
+// The state of the current node: its rows' statistics and the implicit (p, q).
+struct NodeState {
+    float Mt, inv_st, Md, inv_sd;  // (max, 1 / sum) of target row v and draft row v
+    float A, Dn, s;                // a coefficient, D_r, q's scale
+    float qrem;                    // removed tokens' q0 mass
+    int nrem;                      // tokens removed from q
+    bool has_q;                    // the draft row was read (v has children)
+};
+
+// w(j) of one logit pair under coefficient a (a = 0: p0 alone; the draft is not used).
+__device__ __forceinline__ float wgt(float tj, float dj, const NodeState &s, float a, float c) {
+    const float p = __fmul_rn(tweight(tj, s.Mt, c), s.inv_st);
+    if (a == 0.f) return p;
+    const float q = __fmul_rn(tweight(dj, s.Md, c), s.inv_sd);
+    return fmaxf(__fsub_rn(p, __fmul_rn(a, q)), 0.f);
+}
+
+template <class D, bool VEC>
+__device__ __forceinline__ void load_unit(const char *row, int64_t u0, int len, int lane, uint4 (&v)[kResVecs]) {
+#pragma unroll
+    for (int k = 0; k < kResVecs; ++k) {
+        const int e0 = (lane + 32 * k) * D::EPV;
+        v[k] = e0 < len ? load_vec<D, VEC>(row, u0, e0, len) : neg_inf_vec<D>();
+    }
+}
+
+}  // namespace
+
+// One CTA per sequence.  Shared: parent, tokens, child counts, depths, the path, the
+// removed tokens and their frozen coefficients, and the reduction scratch.
+template <class D, bool VEC>
+__global__ void __launch_bounds__(kTsThreads, 1)
+    tree_sample_kernel(Logits t, Logits d, int N, int V, const int32_t *__restrict__ parent,
+                       const int32_t *__restrict__ node_tokens, int max_depth, float c, uint64_t seed,
+                       uint64_t offset, int without_replacement, int nunit, float *__restrict__ umass,
+                       int32_t *__restrict__ accepted_len, int32_t *__restrict__ out_tokens,
+                       int32_t *__restrict__ out_path) {
+    extern __shared__ int s_int[];
+    int *s_par = s_int, *s_tok = s_int + N, *s_nch = s_int + 2 * N, *s_dep = s_int + 3 * N;
+    int *s_path = s_int + 4 * N;  // max_depth + 1
+    __shared__ int s_remtok[kMaxRemoved];
+    __shared__ float s_remcoef[kMaxRemoved];
+    __shared__ float2 s_stat[2][kTsWarps];
+    __shared__ float s_sum[kTsWarps];
+    __shared__ int s_flag;
+    __shared__ float s_tx[2];
+    griddep_launch_next();
+    griddep_wait();  // the caller's kernels may still be writing the inputs
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t seq = blockIdx.x;
+    const int W = max_depth + 1;
+    int32_t *out = out_tokens + seq * W;
+    int32_t *opath = out_path ? out_path + seq * W : nullptr;
+    float *um = umass + seq * int64_t(nunit);
+    constexpr int RE = res_tile_elems<D>();
+
+    // the tree and the tokens: parent[0] = -1, parent[v] in [0, v), depth <= max_depth
+    if (tid == 0) s_flag = 1;
+    __syncthreads();
+    for (int v = tid; v < N; v += kTsThreads) {
+        const int p = parent[v];
+        s_par[v] = p;
+        s_nch[v] = 0;
+        const int tk = v == 0 ? 0 : node_tokens[seq * N + v];
+        s_tok[v] = tk;
+        if ((v == 0 && p != -1) || (v > 0 && (p < 0 || p >= v)) || tk < 0 || tk >= V) s_flag = 0;
+    }
+    __syncthreads();
+    if (s_flag) {
+        for (int v = tid; v < N; v += kTsThreads) {
+            int dpt = 0;
+            for (int w = v; w != 0 && dpt <= max_depth; w = s_par[w]) ++dpt;
+            s_dep[v] = dpt;
+            if (dpt > max_depth) s_flag = 0;
+            if (v > 0) atomicAdd(&s_nch[s_par[v]], 1);
+        }
+    }
+    __syncthreads();
+    auto fail = [&]() {
+        for (int i = tid; i < W; i += kTsThreads) {
+            out[i] = -1;
+            if (opath) opath[i] = -1;
+        }
+        if (tid == 0) accepted_len[seq] = -1;
+    };
+    if (!s_flag) {
+        fail();
+        return;
+    }
+
+    // One pass over the units of row pair v: every warp takes units warp, warp + 32, ...;
+    // the unit masses go to um[], their total (fixed order) is returned to every thread.
+    // a = 0 reads the target row only.
+    auto mass_pass = [&](const char *tp, const char *dp, const NodeState &st, float a) -> float {
+        for (int u = warp; u < nunit; u += kTsWarps) {
+            const int64_t u0 = int64_t(u) * RE;
+            const int len = unit_len(V, u0, RE);
+            uint4 tv[kResVecs], dv[kResVecs];
+            load_unit<D, VEC>(tp, u0, len, lane, tv);
+            if (a != 0.f) load_unit<D, VEC>(dp, u0, len, lane, dv);
+            float acc = 0.f;
+#pragma unroll
+            for (int k = 0; k < kResVecs; ++k)
+#pragma unroll
+                for (int e = 0; e < D::EPV; ++e)
+                    acc += wgt(vec_elem<D>(tv[k], e), a != 0.f ? vec_elem<D>(dv[k], e) : 0.f, st, a, c);
+            acc = warp_reduce(acc, [](float x, float y) { return x + y; });
+            if (lane == 0) um[u] = acc;
+        }
+        __syncthreads();  // the unit masses of every warp
+        // tokens removed earlier keep their own coefficient: correct their units (thread 0)
+        if (tid == 0 && a != 0.f) {
+            for (int r = 0; r < st.nrem; ++r) {
+                if (s_remcoef[r] == a) continue;
+                const int j = s_remtok[r];
+                const float tj = load_elem<D>(tp, j), dj = load_elem<D>(dp, j);
+                um[j / RE] += wgt(tj, dj, st, s_remcoef[r], c) - wgt(tj, dj, st, a, c);
+            }
+        }
+        __syncthreads();
+        // total: lanes of warp 0 own contiguous runs of units, then a warp scan
+        if (warp == 0) {
+            const int per = (nunit + 31) / 32;
+            float ls = 0.f;
+            for (int q = 0; q < per; ++q) {
+                const int u = lane * per + q;
+                if (u < nunit) ls += um[u];
+            }
+            const float tot = __shfl_sync(0xFFFFFFFFu, warp_inclusive_scan(ls, lane), 31);
+            if (lane == 0) s_sum[0] = tot;
+        }
+        __syncthreads();
+        const float tot = s_sum[0];
+        __syncthreads();
+        return tot;
+    };
+
+    // (max, sum) of one row: warps reduce units, then a fixed-order merge; every thread
+    // returns (M, S) and whether the row is a distribution.
+    auto row_stats = [&](const char *row, int slot) -> float2 {
+        float2 ws = make_float2(-__int_as_float(0x7f800000), 0.f);
+        for (int u = warp; u < nunit; u += kTsWarps) {
+            const int64_t u0 = int64_t(u) * RE;
+            const int len = unit_len(V, u0, RE);
+            uint4 v[kResVecs];
+            load_unit<D, VEC>(row, u0, len, lane, v);
+            const float M = warp_reduce(thread_max<D>(v), [](float x, float y) { return max_nan(x, y); });
+            float S = 0.f;
+            if (is_finite(M)) S = warp_reduce(thread_sumexp<D>(v, c, M), [](float x, float y) { return x + y; });
+            ws = merge_stats(ws, make_float2(M, S), c);
+        }
+        if (lane == 0) s_stat[slot][warp] = ws;
+        __syncthreads();
+        float2 r = s_stat[slot][0];
+        for (int w = 1; w < kTsWarps; ++w) r = merge_stats(r, s_stat[slot][w], c);
+        __syncthreads();
+        return r;
+    };
+
+    int v = 0, depth = 0;
+    if (tid == 0) s_path[0] = 0;
+    NodeState st{};
+    for (;;) {
+        const char *tp = row_ptr(t, D::kBytes, seq, v);
+        const char *dp = row_ptr(d, D::kBytes, seq, v);
+        st.has_q = s_nch[v] > 0;
+        const float2 ts = row_stats(tp, 0);
+        float2 ds = make_float2(0.f, 1.f);
+        if (st.has_q) ds = row_stats(dp, 1);
+        if (!is_finite(ts.x) || (st.has_q && !is_finite(ds.x))) {  // not a distribution (R11)
+            fail();
+            return;
+        }
+        st.Mt = ts.x;
+        st.inv_st = 1.f / ts.y;
+        st.Md = ds.x;
+        st.inv_sd = 1.f / ds.y;
+        st.A = 0.f;
+        st.Dn = 1.f;
+        st.s = 1.f;
+        st.qrem = 0.f;
+        st.nrem = 0;
+        bool residual_ready = false;  // um[] holds the masses of the current w
+        float last_total = 0.f;       // ... and their total
+        int next = -1;
+        for (int cnode = v + 1; cnode < N && next < 0; ++cnode) {
+            if (s_par[cnode] != v) continue;
+            const int x = s_tok[cnode];
+            if (tid == 0) {
+                s_tx[0] = load_elem<D>(tp, x);
+                s_tx[1] = load_elem<D>(dp, x);
+            }
+            __syncthreads();
+            const float tx = s_tx[0], dx = s_tx[1];
+            __syncthreads();
+            // the current p(x) and q(x)
+            float ax = st.A;
+            bool removed = false;
+            for (int r = 0; r < st.nrem; ++r)
+                if (s_remtok[r] == x) {
+                    ax = s_remcoef[r];
+                    removed = true;
+                }
+            const float p0x = __fmul_rn(tweight(tx, st.Mt, c), st.inv_st);
+            const float q0x = __fmul_rn(tweight(dx, st.Md, c), st.inv_sd);
+            const float wx = ax == 0.f ? p0x : fmaxf(__fsub_rn(p0x, __fmul_rn(ax, q0x)), 0.f);
+            const float px = wx / st.Dn;
+            const float qx = removed ? 0.f : __fmul_rn(st.s, q0x);
+            const float u = uniform01(seed, offset, uint32_t(seq), uint32_t(cnode - 1), 0u);
+            if (u * qx < px) {  // accepted
+                next = cnode;
+                break;
+            }
+            // rejected: A grows by D s (q's current scale), x leaves q without replacement
+            const float Anew = __fadd_rn(st.A, __fmul_rn(st.Dn, st.s));
+            NodeState ns = st;
+            if (without_replacement && !removed && st.nrem < kMaxRemoved) {
+                if (tid == 0) {
+                    s_remtok[st.nrem] = x;
+                    s_remcoef[st.nrem] = Anew;
+                }
+                ns.nrem = st.nrem + 1;
+                ns.qrem = __fadd_rn(st.qrem, q0x);
+                ns.s = ns.qrem < 1.f ? 1.f / __fsub_rn(1.f, ns.qrem) : 0.f;
+            }
+            __syncthreads();
+            const float F = mass_pass(tp, dp, ns, Anew);
+            if (F > 0.f) {
+                ns.A = Anew;
+                ns.Dn = F;
+                residual_ready = true;
+                last_total = F;
+            } else {  // no residual mass: p stays (the removal from q still happens)
+                ns.A = st.A;
+                ns.Dn = st.Dn;
+                residual_ready = false;
+                if (without_replacement && ns.nrem > st.nrem && tid == 0) s_remcoef[st.nrem] = st.A;
+            }
+            st = ns;
+            __syncthreads();
+        }
+        if (next >= 0) {
+            ++depth;
+            if (tid == 0) s_path[depth] = next;
+            v = next;
+            continue;
+        }
+        // the final token at v: from w under the current state (the last residual, or p)
+        const float total = residual_ready ? last_total : mass_pass(tp, dp, st, st.A);
+        if (warp == 0) {
+            const float u2 = uniform01(seed, offset, uint32_t(seq), uint32_t(v), 1u);
+            const float thr = u2 * total;
+            const int per = (nunit + 31) / 32;
+            float ls = 0.f;
+            for (int q = 0; q < per; ++q) {
+                const int uu = lane * per + q;
+                if (uu < nunit) ls += um[uu];
+            }
+            const float incl = warp_inclusive_scan(ls, lane);
+            int unit = -1;
+            float base = 0.f;
+            bool force_last = false;
+            const unsigned crossing = __ballot_sync(0xFFFFFFFFu, incl > thr);
+            if (crossing) {
+                const int l = __ffs(crossing) - 1;
+                if (lane == l) {
+                    float run = incl - ls;
+                    int last_in_lane = lane * per;
+                    for (int q = 0; q < per && unit < 0; ++q) {
+                        const int uu = lane * per + q;
+                        if (uu >= nunit) break;
+                        last_in_lane = uu;
+                        if (run + um[uu] > thr) unit = uu;
+                        else run += um[uu];
+                    }
+                    if (unit < 0) unit = last_in_lane;
+                    base = run;
+                }
+                unit = __shfl_sync(0xFFFFFFFFu, unit, l);
+                base = __shfl_sync(0xFFFFFFFFu, base, l);
+            } else {  // rounding left the threshold at or above the total: the last unit with mass
+                int lp = -1;
+                for (int q = 0; q < per; ++q) {
+                    const int uu = lane * per + q;
+                    if (uu < nunit && um[uu] > 0.f) lp = uu;
+                }
+                lp = warp_reduce(lp, [](int a, int b) { return max(a, b); });
+                unit = lp >= 0 ? lp : 0;
+                force_last = true;
+            }
+            // inside the unit: lane l owns the contiguous vectors [l kResVecs, (l + 1) kResVecs)
+            const int64_t u0 = int64_t(unit) * RE;
+            const int len = unit_len(V, u0, RE);
+            uint4 tv[kResVecs], dv[kResVecs];
+#pragma unroll
+            for (int k = 0; k < kResVecs; ++k) {
+                const int e0 = (lane * kResVecs + k) * D::EPV;
+                tv[k] = e0 < len ? load_vec<D, VEC>(tp, u0, e0, len) : neg_inf_vec<D>();
+                dv[k] = (st.A != 0.f && e0 < len) ? load_vec<D, VEC>(dp, u0, e0, len) : neg_inf_vec<D>();
+            }
+            auto w_at = [&](int k, int e) -> float {
+                const int j = int(u0) + (lane * kResVecs + k) * D::EPV + e;
+                float a = st.A;
+                for (int r = 0; r < st.nrem; ++r)
+                    if (s_remtok[r] == j) a = s_remcoef[r];
+                return wgt(vec_elem<D>(tv[k], e), st.A != 0.f ? vec_elem<D>(dv[k], e) : 0.f, st, a, c);
+            };
+            Kahan lsum;
+#pragma unroll
+            for (int k = 0; k < kResVecs; ++k)
+#pragma unroll
+                for (int e = 0; e < D::EPV; ++e) lsum.add(w_at(k, e));
+            const float tsum = lsum.value();
+            const float lincl = warp_inclusive_scan(tsum, lane);
+            Kahan run;
+            run.add(base);
+            run.add(lincl - tsum);
+            int cand = kNoIndex, lastpos = -1;
+#pragma unroll
+            for (int k = 0; k < kResVecs; ++k)
+#pragma unroll
+                for (int e = 0; e < D::EPV; ++e) {
+                    const int j = (lane * kResVecs + k) * D::EPV + e;
+                    const float w = w_at(k, e);
+                    run.add(w);
+                    if (j < len) {
+                        if (!force_last && cand == kNoIndex && run.value() > thr) cand = j;
+                        if (w > 0.f) lastpos = j;
+                    }
+                }
+            const int first = warp_reduce(cand, [](int a, int b) { return min(a, b); });
+            lastpos = warp_reduce(lastpos, [](int a, int b) { return max(a, b); });
+            int tok = first != kNoIndex ? first : lastpos;
+            if (tok < 0) tok = 0;
+            if (lane == 0) s_tx[0] = __int_as_float(int(u0) + tok);
+        }
+        __syncthreads();
+        break;
+    }
+    // outputs: the path (root .. v), its tokens, the final token, -1 padding
+    const int tok = __float_as_int(s_tx[0]);
+    for (int i = tid; i < W; i += kTsThreads) {
+        int o = -1, pth = -1;
+        if (i <= depth) pth = s_path[i];
+        if (i < depth) o = s_tok[s_path[i + 1]];
+        else if (i == depth) o = tok;
+        out[i] = o;
+        if (opath) opath[i] = pth;
+    }
+    if (tid == 0) accepted_len[seq] = depth;
+}
+
+cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, const int32_t *parent,
+                               const int32_t *node_tokens, int max_depth, float c, uint64_t seed, uint64_t offset,
+                               int without_replacement, int nunit, float *umass, int32_t *accepted_len,
+                               int32_t *out_tokens, int32_t *out_path, cudaStream_t s) {
+    const size_t smem = size_t(4 * N + max_depth + 1) * sizeof(int);
+    auto k = dtype == 1 ? (vec ? tree_sample_kernel<BF16, true> : tree_sample_kernel<BF16, false>)
+                        : (vec ? tree_sample_kernel<F32, true> : tree_sample_kernel<F32, false>);
+    return launch_after(k, unsigned(B), kTsThreads, smem, s, t, d, N, V, parent, node_tokens, max_depth, c, seed,
+                        offset, without_replacement, nunit, umass, accepted_len, out_tokens, out_path);
+}
+
+}  // namespace sv

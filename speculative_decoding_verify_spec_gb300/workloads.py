@@ -21,6 +21,10 @@ Workloads (vocabulary sizes, draft lengths and distributions as specified for th
   tree_b64       tree,     B=64,  N=64 nodes (depth 6, fanouts 4,3,2,2,1,1 pruned to 64 nodes),
                  V=128256, bf16, t ~ N(0,2^2); per internal node one random child carries the
                  parent's argmax w.p. 0.7, every other child a uniform token
+  tree_sample_b64  token-tree sampling (multi-round rejection) on the same tree, B=64,
+                 V=128256, bf16, t ~ N(0,2^2) at every node, d = 0.8 t + N(0,1), T=1; every
+                 internal node's children are a drafter's draws from softmax(d_v / T) without
+                 replacement (Gumbel top-k, in draw order)
 """
 from __future__ import annotations
 
@@ -38,6 +42,9 @@ WORKLOADS = {
     "greedy_b512": dict(mode="greedy", B=512, gamma=6, V=152064, dtype="bf16", input_seed=1004),
     "tree_b64": dict(mode="tree", B=64, N=64, V=128256, dtype="bf16", input_seed=1005,
                      branching=(4, 3, 2, 2, 1, 1)),
+    "tree_sample_b64": dict(mode="tree_sample", B=64, N=64, V=128256, dtype="bf16",
+                            input_seed=1006, verify_seed=0x5EED + 6, temperature=1.0,
+                            branching=(4, 3, 2, 2, 1, 1), without_replacement=True),
 }
 
 DESCRIPTIONS = {
@@ -46,6 +53,8 @@ DESCRIPTIONS = {
     "sample_b256": "sampling verify B=256 V=128256 gamma=8 bf16 T=0.7 (5% peaked rows)",
     "greedy_b512": "greedy verify B=512 V=152064 gamma=6 bf16",
     "tree_b64": "greedy token-tree verify B=64 N=64 depth=6 V=128256 bf16",
+    "tree_sample_b64": ("token-tree sampling verify (multi-round rejection) B=64 N=64 depth=6 "
+                        "V=128256 bf16 T=1.0, children drawn from q without replacement"),
 }
 
 
@@ -218,6 +227,64 @@ def make_tree(B, V, dtype="bf16", seed=1, device="cpu", branching=(4, 3, 2, 2, 1
     return TreeInputs(t.contiguous(), par_t, tokens.contiguous(), max(depth), list(depth))
 
 
+@dataclass
+class TreeSampleInputs:
+    target: torch.Tensor        # [B, N, V]
+    draft: torch.Tensor         # [B, N, V]
+    parent: torch.Tensor        # [N] int32
+    node_tokens: torch.Tensor   # [B, N] int32
+    max_depth: int
+    temperature: float
+    seed: int
+    without_replacement: bool
+    depth: list = field(default_factory=list)
+
+
+def draw_children(draft_over_T: torch.Tensor, k: int, without_replacement: bool, g, device):
+    """k ordered children per row drawn from softmax(draft_over_T) ([rows, k] int32): a
+    drafter's draws, by Gumbel-max (with replacement, k independent draws) or Gumbel
+    top-k (without replacement: the keys sorted descending give the draw order)."""
+    if not without_replacement:
+        return torch.stack([_gumbel_draw(draft_over_T, g, device) for _ in range(k)], dim=-1)
+    u = torch.rand(draft_over_T.shape, generator=g, device=device, dtype=torch.float32)
+    u = u.clamp_(min=1e-20, max=1.0 - 1e-7)
+    keys = draft_over_T + (-torch.log(-torch.log(u)))
+    return torch.topk(keys, k, dim=-1, sorted=True).indices.to(torch.int32)
+
+
+def make_tree_sample(B, V, dtype="bf16", seed=1, verify_seed=0, device="cpu",
+                     branching=(4, 3, 2, 2, 1, 1), N=64, temperature=1.0,
+                     without_replacement=True, target_std=2.0, draft_scale=0.8, noise_std=1.0,
+                     parent=None):
+    """Tree-sampling inputs: target and draft logits at every node of the pruned tree (or a
+    given parent list), every internal node's children drawn from q at that node."""
+    if parent is None:
+        parent, depth = tree_shape(branching, N)
+    else:
+        depth = [0] * len(parent)
+        for v in range(1, len(parent)):
+            depth[v] = depth[parent[v]] + 1
+    N = len(parent)
+    g = _gen(seed, device)
+    t32 = _randn((B, N, V), g, device, target_std)
+    d32 = draft_scale * t32 + _randn((B, N, V), g, device, noise_std)
+    t, d = _round(t32, dtype), _round(d32, dtype)
+    del t32, d32
+    tokens = torch.zeros((B, N), device=device, dtype=torch.int32)
+    children = [[] for _ in range(N)]
+    for v in range(1, N):
+        children[parent[v]].append(v)
+    for v in range(N):
+        if children[v]:
+            drawn = draw_children(d[:, v].float() / temperature, len(children[v]),
+                                  without_replacement, g, device)
+            tokens[:, children[v]] = drawn
+    par_t = torch.tensor(parent, dtype=torch.int32, device=device)
+    return TreeSampleInputs(t.contiguous(), d.contiguous(), par_t, tokens.contiguous(),
+                            max(depth), float(temperature), int(verify_seed),
+                            bool(without_replacement), list(depth))
+
+
 def make(name: str, device="cpu", **overrides):
     """Inputs of a named workload (shapes may be overridden to make a smaller case)."""
     cfg = dict(WORKLOADS[name])
@@ -236,6 +303,10 @@ def make(name: str, device="cpu", **overrides):
     if mode == "greedy":
         return make_greedy(cfg["B"], cfg["gamma"], cfg["V"], cfg["dtype"], cfg["input_seed"],
                            device)
+    if mode == "tree_sample":
+        return make_tree_sample(cfg["B"], cfg["V"], cfg["dtype"], cfg["input_seed"],
+                                cfg["verify_seed"], device, tuple(cfg["branching"]), cfg["N"],
+                                cfg["temperature"], cfg["without_replacement"])
     return make_tree(cfg["B"], cfg["V"], cfg["dtype"], cfg["input_seed"], device,
                      tuple(cfg["branching"]), cfg["N"])
 
@@ -256,6 +327,9 @@ def logical_bytes(name: str, **overrides) -> int:
     N = cfg["N"]
     _, depth = tree_shape(tuple(cfg["branching"]), N)
     D = max(depth)
+    if cfg["mode"] == "tree_sample":  # every target row and the draft rows of internal nodes
+        internal = len(set(tree_shape(tuple(cfg["branching"]), N)[0][1:]))
+        return B * (N + internal) * V * s + 4 * B * N + 4 * N + 4 * B * (2 * D + 3)
     return B * N * V * s + 4 * B * N + 4 * N + 4 * B * (2 * D + 3)
 
 

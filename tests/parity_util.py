@@ -72,6 +72,48 @@ def oracle_tree(target, parent, tokens, max_depth, threads=None):
     return tuple(np.concatenate([p[i] for p in parts]) for i in range(4))
 
 
+def oracle_tree_sample(target, draft, parent, tokens, max_depth, T, seed, offset=0,
+                       without_replacement=False, threads=None):
+    """The tree-sampling oracle over the whole batch, split over threads (global sequence
+    index b0 keys the uniforms)."""
+    T = float(np.float32(T))
+    t = target if isinstance(target, np.ndarray) else host(target)
+    d = draft if isinstance(draft, np.ndarray) else host(draft)
+    B = t.shape[0]
+    par = np.asarray(parent.cpu().numpy() if torch.is_tensor(parent) else parent, np.int32)
+    x = tokens if isinstance(tokens, np.ndarray) else tokens.cpu().numpy()
+    x = x.astype(np.int32).reshape(B, -1)
+    threads = threads or min(16, os.cpu_count() or 1)
+    orc = oracle.default()
+
+    def run(rg):
+        s, e = rg
+        return orc.verify_tree_sample(t[s:e], d[s:e], par, x[s:e], max_depth, T, seed, offset,
+                                      without_replacement, b0=s)
+
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(run, _ranges(B, threads)))
+    return tuple(np.concatenate([p[i] for p in parts]) for i in range(4))
+
+
+def compare_tree_sample(acc, out, path, o_acc, o_out, o_path, o_flags, label="", record=True):
+    """Lengths, tokens and paths must agree wherever the oracle raised no flag; returns
+    (n, mismatches, flagged)."""
+    acc, out, path = acc.cpu().numpy(), out.cpu().numpy(), path.cpu().numpy()
+    same = (acc == o_acc) & (out == o_out).all(1) & (path == o_path).all(1)
+    flagged = o_flags != 0
+    bad = ~same & ~flagged
+    if bad.any():
+        i = int(np.nonzero(bad)[0][0])
+        raise AssertionError(f"{label}: unflagged mismatch at sequence {i}: gpu acc={acc[i]} "
+                             f"out={out[i].tolist()} path={path[i].tolist()} oracle acc={o_acc[i]} "
+                             f"out={o_out[i].tolist()} path={o_path[i].tolist()}")
+    n, mism, flg = len(acc), int((~same).sum()), int(flagged.sum())
+    if record:
+        record_rates(label, n, mism, flg, o_flags)
+    return n, mism, flg
+
+
 def compare_sample(acc, out, o_acc, o_out, o_flags, o_diag=None, label="", record=None):
     """Tokens and lengths must agree wherever the oracle raised no flag; returns
     (n, mismatches, flagged, diagnostics of the mismatched sequences)."""
