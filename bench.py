@@ -31,15 +31,19 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "sample_b256"
-SECONDARY = ["greedy_b512", "tree_b64", "tree_sample_b64"]
+SECONDARY = ["greedy_b512", "tree_b64", "tree_sample_b64", "sample_b256_lazy", "greedy_b512_lazy",
+             "tree_b64_lazy"]
 METRIC = "verified seqs/s"
 UNIT = "seqs/s"
 FALLBACK_HBM_GBS = 6800.0
 DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "max_tiles_kernel",
-                   "tree": "max_tiles_kernel", "tree_sample": "tree_sample_kernel"}
+                   "tree": "max_tiles_kernel", "tree_sample": "tree_sample_kernel",
+                   "sample_lazy": "tree_sample_kernel", "greedy_lazy": "greedy_walk_kernel",
+                   "tree_lazy": "greedy_walk_kernel"}
 STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
 STAGES = {"sample": ["row_stats", "decide", "residual_mass", "inverse_cdf", "redraw"],
-          "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"], "tree_sample": ["walk"]}
+          "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"], "tree_sample": ["walk"],
+          "sample_lazy": ["walk"], "greedy_lazy": ["walk"], "tree_lazy": ["walk"]}
 
 
 def parse_args():
@@ -207,6 +211,38 @@ def make_call(name, inputs, dev, **ov):
     mode = cfg["mode"]
     B, V = cfg["B"], cfg["V"]
     dt = binding.BF16 if cfg["dtype"] == "bf16" else binding.FP32
+    lazy = cfg.get("lazy", False)
+    if mode == "sample" and lazy:
+        g = cfg["gamma"]
+        ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_SAMPLE_LAZY, B, g, V, dt),
+                         dtype=torch.uint8, device=dev)
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        out = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+        step_counter = [0]
+
+        def call(target=inputs.target, draft=inputs.draft, tokens=inputs.draft_tokens):
+            step_counter[0] += 1
+            return sv.spec_verify_sample_lazy(target, draft, tokens, inputs.temperature, inputs.seed,
+                                              step_counter[0], workspace=ws, accepted_len=acc,
+                                              out_tokens=out)
+        return call, (acc, out)
+    if mode == "greedy" and lazy:
+        g = cfg["gamma"]
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        out = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+
+        def call(target=inputs.target, tokens=inputs.draft_tokens):
+            return sv.spec_verify_greedy_lazy(target, tokens, accepted_len=acc, out_tokens=out)
+        return call, (acc, out)
+    if mode == "tree" and lazy:
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        out = torch.empty((B, inputs.max_depth + 1), dtype=torch.int32, device=dev)
+        path = torch.empty((B, inputs.max_depth + 1), dtype=torch.int32, device=dev)
+
+        def call(target=inputs.target, tokens=inputs.node_tokens):
+            return sv.spec_verify_tree_greedy_lazy(target, inputs.parent, tokens, inputs.max_depth,
+                                                   accepted_len=acc, out_tokens=out, out_path=path)
+        return call, (acc, out, path)
     if mode == "sample":
         g = cfg["gamma"]
         ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_SAMPLE, B, g, V, dt),
@@ -273,6 +309,8 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
     mode = cfg["mode"]
     inputs = W.make(name, device=dev, input_seed=cfg["input_seed"] + 7919 * rank, **ov)
     call, outs = make_call(name, inputs, dev, **ov)
+    if cfg.get("lazy"):
+        mode = mode + "_lazy"
     nst = len(STAGES[mode])
     if mode == "sample" and cfg["gamma"] == 0:
         nst = 5
@@ -335,6 +373,28 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
         res.update({"hbm_gbs_step": None, "frac_of_8tbs_step": None, "roofline": None,
                     "lazy": "one CTA per sequence reads only the rows of the nodes its walk reaches",
                     "mean_path_nodes": float(acc[acc >= 0].mean().item() + 1) if (acc >= 0).any() else None})
+    if mode.endswith("_lazy"):
+        # bytes the walks read in the last step, from its outputs: chain greedy reads rows
+        # 0..k; tree greedy the rows of the accepted nodes (at least the path); chain
+        # sampling the (max, sum) pass over target rows 0..k and draft rows 0..min(k, gamma-1),
+        # then a residual pass over 2 rows (k < gamma) or a bonus pass over 1 row
+        s = 2 if cfg["dtype"] == "bf16" else 4
+        a = outs[0].long().cpu()
+        a = a[a >= 0]
+        if mode == "sample_lazy":
+            g = cfg["gamma"]
+            rows_read = ((a + 1) + torch.clamp(a + 1, max=g) + torch.where(a < g, 2, 1)).sum().item()
+        else:
+            rows_read = (a + 1).sum().item()
+        lb = rows_read * cfg["V"] * s
+        res.update({"hbm_gbs_step": None, "frac_of_8tbs_step": None,
+                    "lazy": "one CTA per sequence reads only the rows the rule needs",
+                    "rows_read_per_step": rows_read,
+                    "roofline": {"bound": "hbm", "kernel": kernel, "achieved": lb / (ms_step / 1e3) / 1e9,
+                                 "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                                 "frac": lb / (ms_step / 1e3) / 1e9 / peak, "bytes_per_launch": lb,
+                                 "traffic": None,
+                                 "note": "bytes the walks read (a lower bound for tree greedy), over the step time"}})
     return res, inputs, call
 
 

@@ -63,7 +63,8 @@ typedef enum {
     SV_MODE_GREEDY = 1,    /* spec_verify_greedy:      rows = gamma */
     SV_MODE_TREE = 2,      /* spec_verify_tree_greedy: rows = N     */
     SV_MODE_ROW_STATS = 3, /* spec_verify_row_stats:   rows = rows_per_seq */
-    SV_MODE_TREE_SAMPLE = 4 /* spec_verify_tree_sample: rows = N    */
+    SV_MODE_TREE_SAMPLE = 4, /* spec_verify_tree_sample: rows = N   */
+    SV_MODE_SAMPLE_LAZY = 5  /* spec_verify_sample_lazy: rows = gamma */
 } sv_mode;
 
 /* Limits checked on the host (SV_ERR_INVALID_ARG beyond them). */
@@ -179,6 +180,42 @@ sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_str
                                   uint64_t seed, uint64_t offset, int without_replacement,
                                   int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * LAZY verification: the same rules, reading only the rows that can change the result.
+ * The rows after the first rejection, or beside the accepted nodes of a tree, never reach
+ * the result; these entries run one CTA per sequence that walks the rule and reads the rows
+ * it needs as it goes (one pass per row, plus one residual pass per rejection when
+ * sampling).  They return exactly what the full entries return whenever every row is a
+ * distribution (sampling) or NaN-free (greedy); a bad row the walk never reads does not
+ * invalidate the sequence.  Outputs, arguments and errors as the full entries.
+ *
+ *   spec_verify_sample_lazy       the chain rule of spec_verify_sample (the tree rule of
+ *                                 spec_verify_tree_sample on the chain v -> v + 1, whose
+ *                                 uniforms are the chain's); workspace:
+ *                                 spec_verify_workspace_size(SV_MODE_SAMPLE_LAZY, B, gamma,
+ *                                 V, dtype) bytes.
+ *   spec_verify_greedy_lazy       the rule of spec_verify_greedy; no workspace.
+ *   spec_verify_tree_greedy_lazy  the rule of spec_verify_tree_greedy (every accepted node's
+ *                                 row is read, so the deepest-node rule is unchanged); no
+ *                                 workspace.
+ */
+sv_status spec_verify_sample_lazy(const void *target_logits, int64_t t_batch_stride,
+                                  int64_t t_row_stride, const void *draft_logits,
+                                  int64_t d_batch_stride, int64_t d_row_stride, sv_dtype dtype,
+                                  int B, int gamma, int V, const int32_t *draft_tokens,
+                                  float temperature, uint64_t seed, uint64_t offset,
+                                  int32_t *accepted_len, int32_t *out_tokens, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+sv_status spec_verify_greedy_lazy(const void *target_logits, int64_t t_batch_stride,
+                                  int64_t t_row_stride, sv_dtype dtype, int B, int gamma, int V,
+                                  const int32_t *draft_tokens, int32_t *accepted_len,
+                                  int32_t *out_tokens, void *stream);
+sv_status spec_verify_tree_greedy_lazy(const void *target_logits, int64_t t_batch_stride,
+                                       int64_t t_row_stride, sv_dtype dtype, int B, int N, int V,
+                                       const int32_t *parent, const int32_t *node_tokens,
+                                       int max_depth, int32_t *accepted_len, int32_t *out_tokens,
+                                       int32_t *out_path, void *stream);
 
 /*
  * Greedy verification that allocates nothing and takes no workspace.  (The pages have no

@@ -9,9 +9,12 @@ from .binding import (  # noqa: F401
     SpecVerifyError,
     load_library,
     spec_verify_greedy,
+    spec_verify_greedy_lazy,
     spec_verify_row_stats,
     spec_verify_sample,
+    spec_verify_sample_lazy,
     spec_verify_tree_greedy,
+    spec_verify_tree_greedy_lazy,
     spec_verify_tree_sample,
     spec_verify_uniforms,
     spec_verify_workspace_size,
@@ -21,9 +24,12 @@ __all__ = [
     "SpecVerifyError",
     "load_library",
     "spec_verify_greedy",
+    "spec_verify_greedy_lazy",
     "spec_verify_row_stats",
     "spec_verify_sample",
+    "spec_verify_sample_lazy",
     "spec_verify_tree_greedy",
+    "spec_verify_tree_greedy_lazy",
     "spec_verify_tree_sample",
     "spec_verify_uniforms",
     "spec_verify_workspace_size",

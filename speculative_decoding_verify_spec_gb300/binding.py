@@ -17,7 +17,7 @@ import torch
 from . import _build
 
 SV_OK = 0
-MODE_SAMPLE, MODE_GREEDY, MODE_TREE, MODE_ROW_STATS, MODE_TREE_SAMPLE = 0, 1, 2, 3, 4
+MODE_SAMPLE, MODE_GREEDY, MODE_TREE, MODE_ROW_STATS, MODE_TREE_SAMPLE, MODE_SAMPLE_LAZY = 0, 1, 2, 3, 4, 5
 FP32, BF16 = 0, 1
 
 _lock = threading.Lock()
@@ -58,6 +58,13 @@ def load_library() -> ctypes.CDLL:
         lib.spec_verify_tree_sample.argtypes = [P, i64, i64, P, i64, i64, i32, i32, i32, i32, P, P, i32,
                                                 f32, u64, u64, i32, P, P, P, P, sz, P]
         lib.spec_verify_tree_sample.restype = i32
+        lib.spec_verify_sample_lazy.argtypes = [P, i64, i64, P, i64, i64, i32, i32, i32, i32, P, f32, u64,
+                                                u64, P, P, P, sz, P]
+        lib.spec_verify_sample_lazy.restype = i32
+        lib.spec_verify_greedy_lazy.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, P, P]
+        lib.spec_verify_greedy_lazy.restype = i32
+        lib.spec_verify_tree_greedy_lazy.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, i32, P, P, P, P]
+        lib.spec_verify_tree_greedy_lazy.restype = i32
         lib.spec_verify_row_stats.argtypes = [P, i64, i64, i32, i32, i32, i32, f32, P, P, P, sz, P]
         lib.spec_verify_row_stats.restype = i32
         lib.spec_verify_uniforms.argtypes = [u64, u64, i32, i32, i32, P, P]
@@ -242,6 +249,90 @@ def spec_verify_tree_sample(target: torch.Tensor, draft: torch.Tensor, parent: t
                                      out_path.data_ptr() if out_path is not None else None,
                                      ws.data_ptr(), wsb, _stream(dev))
     _check(st, "spec_verify_tree_sample")
+    return accepted_len, out_tokens, out_path
+
+
+def spec_verify_sample_lazy(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor,
+                            temperature: float, seed: int, offset: int = 0, *, workspace=None,
+                            accepted_len=None, out_tokens=None):
+    """Lazy sampling verification (reads rows up to the stop point); returns (accepted_len
+    [B], out_tokens [B, gamma+1]) -- spec_verify_sample's outputs."""
+    lib = load_library()
+    tsb, tsr = _logits3(target, "target")
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    dt = _dtype_code(target)
+    if gamma > 0:
+        dsb, dsr = _logits3(draft, "draft")
+        if draft.dtype != target.dtype or tuple(draft.shape) != (B, gamma, V):
+            raise ValueError("draft must be [B, gamma, V] with the target's dtype")
+        dptr = draft.data_ptr()
+        x = _ints(draft_tokens, "draft_tokens", (B, gamma))
+        xptr = x.data_ptr()
+    else:
+        dsb = dsr = 0
+        dptr = xptr = None
+    dev = target.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    ws, wsb = _workspace(MODE_SAMPLE_LAZY, B, gamma, V, dt, dev, workspace)
+    st = lib.spec_verify_sample_lazy(target.data_ptr(), tsb, tsr, dptr, dsb, dsr, dt, B, gamma, V, xptr,
+                                     float(temperature), int(seed) & (2**64 - 1),
+                                     int(offset) & (2**64 - 1), accepted_len.data_ptr(),
+                                     out_tokens.data_ptr(), ws.data_ptr(), wsb, _stream(dev))
+    _check(st, "spec_verify_sample_lazy")
+    return accepted_len, out_tokens
+
+
+def spec_verify_greedy_lazy(target: torch.Tensor, draft_tokens: torch.Tensor, *, accepted_len=None,
+                            out_tokens=None):
+    """Lazy greedy verification (reads rows up to the first mismatch); returns
+    spec_verify_greedy's outputs."""
+    lib = load_library()
+    tsb, tsr = _logits3(target, "target")
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    dt = _dtype_code(target)
+    x = _ints(draft_tokens, "draft_tokens", (B, gamma)) if gamma > 0 else None
+    dev = target.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    st = lib.spec_verify_greedy_lazy(target.data_ptr(), tsb, tsr, dt, B, gamma, V,
+                                     x.data_ptr() if x is not None else None, accepted_len.data_ptr(),
+                                     out_tokens.data_ptr(), _stream(dev))
+    _check(st, "spec_verify_greedy_lazy")
+    return accepted_len, out_tokens
+
+
+def spec_verify_tree_greedy_lazy(target: torch.Tensor, parent: torch.Tensor, node_tokens: torch.Tensor,
+                                 max_depth: int, *, with_path: bool = True, accepted_len=None,
+                                 out_tokens=None, out_path=None):
+    """Lazy greedy tree verification (reads the rows of accepted nodes only); returns
+    spec_verify_tree_greedy's outputs."""
+    lib = load_library()
+    tsb, tsr = _logits3(target, "target")
+    B, N, V = target.shape
+    dt = _dtype_code(target)
+    par = _ints(parent, "parent", (N,))
+    tok = _ints(node_tokens, "node_tokens", (B, N))
+    dev = target.device
+    W = int(max_depth) + 1
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, W), dtype=torch.int32, device=dev)
+    if with_path and out_path is None:
+        out_path = torch.empty((B, W), dtype=torch.int32, device=dev)
+    st = lib.spec_verify_tree_greedy_lazy(target.data_ptr(), tsb, tsr, dt, B, N, V, par.data_ptr(),
+                                          tok.data_ptr(), int(max_depth), accepted_len.data_ptr(),
+                                          out_tokens.data_ptr(),
+                                          out_path.data_ptr() if out_path is not None else None,
+                                          _stream(dev))
+    _check(st, "spec_verify_tree_greedy_lazy")
     return accepted_len, out_tokens, out_path
 
 

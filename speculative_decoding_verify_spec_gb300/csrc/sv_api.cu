@@ -59,6 +59,7 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
     case SV_MODE_TREE:
     case SV_MODE_ROW_STATS: R = size_t(rows); break;
     case SV_MODE_TREE_SAMPLE:  // unit masses of the node being walked, per sequence
+    case SV_MODE_SAMPLE_LAZY:
         L.partial = 0;
         L.total = up256(size_t(B) * size_t(nrt_of(V, dtype)) * 4);
         return L;
@@ -291,10 +292,83 @@ sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_str
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = mark(0, s);
     if (e == cudaSuccess)
-        e = sv::launch_tree_sample(dtype == SV_BF16, vec, t, d, B, N, V, parent, node_tokens, max_depth, c, seed,
+        e = sv::launch_tree_sample(dtype == SV_BF16, vec, t, d, B, N, V, false, parent, node_tokens, max_depth, c,
+                                   seed,
                                    offset, without_replacement, nrt_of(V, dtype),
                                    reinterpret_cast<float *>(at(workspace, 0)), accepted_len, out_tokens,
                                    out_path, s);
+    if (e == cudaSuccess) e = mark(1, s);
+    return cuda_status(e);
+}
+
+sv_status spec_verify_sample_lazy(const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride,
+                                  const void *draft_logits, int64_t d_batch_stride, int64_t d_row_stride,
+                                  sv_dtype dtype, int B, int gamma, int V, const int32_t *draft_tokens,
+                                  float temperature, uint64_t seed, uint64_t offset, int32_t *accepted_len,
+                                  int32_t *out_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!dtype_ok(dtype)) return SV_ERR_UNSUPPORTED;
+    if (B < 0 || gamma < 0 || gamma > SV_MAX_GAMMA || V < 1 || V > SV_MAX_VOCAB)
+        return SV_ERR_INVALID_ARG;
+    if (t_batch_stride < 0 || t_row_stride < 0 || d_batch_stride < 0 || d_row_stride < 0)
+        return SV_ERR_INVALID_ARG;
+    if (!(temperature > 0.f) || !std::isfinite(temperature)) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !accepted_len || !out_tokens) return SV_ERR_INVALID_ARG;
+    if (gamma > 0 && (!draft_logits || !draft_tokens)) return SV_ERR_INVALID_ARG;
+    const Layout L = layout(SV_MODE_SAMPLE_LAZY, B, gamma, V, dtype);
+    if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
+    const bool vec = vec_ok(target_logits, t_batch_stride, t_row_stride, dtype) &&
+                     (gamma == 0 || vec_ok(draft_logits, d_batch_stride, d_row_stride, dtype));
+    const Logits t{target_logits, t_batch_stride, t_row_stride};
+    const Logits d{gamma > 0 ? draft_logits : target_logits, d_batch_stride, d_row_stride};
+    const float c = float(1.4426950408889634 / double(temperature));  // log2(e) / T
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = mark(0, s);
+    if (e == cudaSuccess)
+        e = sv::launch_tree_sample(dtype == SV_BF16, vec, t, d, B, gamma + 1, V, true, nullptr, draft_tokens, gamma,
+                                   c, seed, offset, 0, nrt_of(V, dtype), reinterpret_cast<float *>(at(workspace, 0)),
+                                   accepted_len, out_tokens, nullptr, s);
+    if (e == cudaSuccess) e = mark(1, s);
+    return cuda_status(e);
+}
+
+sv_status spec_verify_greedy_lazy(const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride,
+                                  sv_dtype dtype, int B, int gamma, int V, const int32_t *draft_tokens,
+                                  int32_t *accepted_len, int32_t *out_tokens, void *stream) {
+    if (!dtype_ok(dtype)) return SV_ERR_UNSUPPORTED;
+    if (B < 0 || gamma < 0 || gamma > SV_MAX_GAMMA || V < 1 || V > SV_MAX_VOCAB || t_batch_stride < 0 ||
+        t_row_stride < 0)
+        return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !accepted_len || !out_tokens || (gamma > 0 && !draft_tokens)) return SV_ERR_INVALID_ARG;
+    const bool vec = vec_ok(target_logits, t_batch_stride, t_row_stride, dtype);
+    const Logits t{target_logits, t_batch_stride, t_row_stride};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = mark(0, s);
+    if (e == cudaSuccess)
+        e = sv::launch_greedy_walk(dtype == SV_BF16, vec, t, B, gamma + 1, V, true, nullptr, draft_tokens, gamma,
+                                   accepted_len, out_tokens, nullptr, s);
+    if (e == cudaSuccess) e = mark(1, s);
+    return cuda_status(e);
+}
+
+sv_status spec_verify_tree_greedy_lazy(const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride,
+                                       sv_dtype dtype, int B, int N, int V, const int32_t *parent,
+                                       const int32_t *node_tokens, int max_depth, int32_t *accepted_len,
+                                       int32_t *out_tokens, int32_t *out_path, void *stream) {
+    if (!dtype_ok(dtype)) return SV_ERR_UNSUPPORTED;
+    if (B < 0 || N < 1 || N > SV_MAX_TREE_NODES || V < 1 || V > SV_MAX_VOCAB)
+        return SV_ERR_INVALID_ARG;
+    if (max_depth < 0 || max_depth >= N || t_batch_stride < 0 || t_row_stride < 0) return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!target_logits || !parent || !node_tokens || !accepted_len || !out_tokens) return SV_ERR_INVALID_ARG;
+    const bool vec = vec_ok(target_logits, t_batch_stride, t_row_stride, dtype);
+    const Logits t{target_logits, t_batch_stride, t_row_stride};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = mark(0, s);
+    if (e == cudaSuccess)
+        e = sv::launch_greedy_walk(dtype == SV_BF16, vec, t, B, N, V, false, parent, node_tokens, max_depth,
+                                   accepted_len, out_tokens, out_path, s);
     if (e == cudaSuccess) e = mark(1, s);
     return cuda_status(e);
 }

@@ -1,0 +1,178 @@
+// sv_lazy.cu -- lazy greedy verification: read only the rows whose argmax decides something.
+//
+// Method ("7.6 Speculative Decoding: Draft Models, Medusa, EAGLE & Lookahead", "Extending
+// to a chain" at temperature 0 and "Tree Attention" / Exercise 5 verify_tree_greedy; the
+// greedy rule of "Medusa, EAGLE and self-speculation", speculative_greedy): node v != 0 is
+// accepted when its token equals the argmax of its parent's row and its parent is
+// accepted; the deepest accepted node (lowest index among equally deep ones) ends the path
+// and its row's argmax is the bonus.  A chain is the tree whose node v has parent v - 1.
+//
+// Only accepted nodes' rows can change the result (a row decides its children's
+// acceptance and, for the deepest accepted node, the bonus), so one CTA per sequence walks
+// the accepted nodes in index order -- parents come before children -- and reads exactly
+// those rows.  Each row's argmax is the two-step search of the full path: the largest
+// 4 KB-tile maximum (lowest tile on ties, NaN absorbing), then the first position of that
+// value inside that tile.
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+constexpr int kLzThreads = 1024;
+constexpr int kLzWarps = kLzThreads / 32;
+
+}  // namespace
+
+// chain: parent(v) = v - 1 and node v's token is tokens[seq * (N - 1) + v - 1] (draft
+// tokens [B][gamma], N = gamma + 1); otherwise parent[N] and node_tokens [B][N].
+template <class D, bool VEC>
+__global__ void __launch_bounds__(kLzThreads, 1)
+    greedy_walk_kernel(Logits t, int N, int V, bool chain, const int32_t *__restrict__ parent,
+                       const int32_t *__restrict__ tokens, int max_depth, int32_t *__restrict__ accepted_len,
+                       int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_path) {
+    extern __shared__ int s_int[];
+    int *s_par = s_int, *s_tok = s_int + N, *s_dep = s_int + 2 * N, *s_acc = s_int + 3 * N;
+    int *s_arg = s_int + 4 * N;  // argmax of each accepted node's row
+    int *s_path = s_int + 5 * N;  // max_depth + 1
+    __shared__ int2 s_best[kLzWarps];
+    __shared__ int s_flag, s_tile, s_idx;
+    griddep_launch_next();
+    griddep_wait();  // the caller's kernels may still be writing the inputs
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t seq = blockIdx.x;
+    const int W = max_depth + 1;
+    int32_t *out = out_tokens + seq * W;
+    int32_t *opath = out_path ? out_path + seq * W : nullptr;
+    constexpr int TE = tile_elems<D>();
+    const int ntile = int((int64_t(V) + TE - 1) / TE);
+
+    if (tid == 0) s_flag = 1;
+    __syncthreads();
+    for (int v = tid; v < N; v += kLzThreads) {
+        const int p = chain ? v - 1 : parent[v];
+        const int tk = v == 0 ? 0 : (chain ? tokens[seq * (N - 1) + v - 1] : tokens[seq * N + v]);
+        s_par[v] = p;
+        s_tok[v] = tk;
+        s_acc[v] = v == 0;
+        if ((v == 0 && p != -1) || (v > 0 && (p < 0 || p >= v)) || tk < 0 || tk >= V) s_flag = 0;
+    }
+    __syncthreads();
+    if (s_flag) {
+        for (int v = tid; v < N; v += kLzThreads) {
+            int dpt = 0;
+            for (int w = v; w != 0 && dpt <= max_depth; w = s_par[w]) ++dpt;
+            s_dep[v] = dpt;
+            if (dpt > max_depth) s_flag = 0;
+        }
+    }
+    __syncthreads();
+    auto fail = [&]() {
+        for (int i = tid; i < W; i += kLzThreads) {
+            out[i] = -1;
+            if (opath) opath[i] = -1;
+        }
+        if (tid == 0) accepted_len[seq] = -1;
+    };
+    if (!s_flag) {
+        fail();
+        return;
+    }
+
+    // the argmax of row v (every thread returns it; -1 for a row with a NaN)
+    auto row_argmax = [&](int v) -> int {
+        const char *row = row_ptr(t, D::kBytes, seq, v);
+        int2 best = make_int2(__float_as_int(-__int_as_float(0x7f800000)), kNoIndex);  // (max bits, tile)
+        for (int tile = warp; tile < ntile; tile += kLzWarps) {
+            const int64_t c0 = int64_t(tile) * TE;
+            const int len = unit_len(V, c0, TE);
+            uint4 vv[kTileVecs];
+#pragma unroll
+            for (int u = 0; u < kTileVecs; ++u) {
+                const int e0 = (lane + 32 * u) * D::EPV;
+                vv[u] = e0 < len ? load_vec<D, VEC>(row, c0, e0, len) : neg_inf_vec<D>();
+            }
+            const float m = warp_reduce(thread_max<D>(vv), [](float a, float b) { return max_nan(a, b); });
+            best = merge_argmax(best, make_int2(__float_as_int(m), tile));
+        }
+        if (lane == 0) s_best[warp] = best;
+        __syncthreads();
+        if (tid == 0) {
+            int2 b = s_best[0];
+            for (int w = 1; w < kLzWarps; ++w) b = merge_argmax(b, s_best[w]);
+            const float bm = __int_as_float(b.x);
+            s_tile = bm != bm ? -1 : b.y;
+            s_best[0] = b;
+        }
+        __syncthreads();
+        const int tile = s_tile;
+        const float bm = __int_as_float(s_best[0].x);
+        if (warp == 0 && tile >= 0) {  // the first position of the maximum inside that tile
+            const int64_t c0 = int64_t(tile) * TE;
+            const int len = unit_len(V, c0, TE);
+            uint4 vv[kTileVecs];
+#pragma unroll
+            for (int u = 0; u < kTileVecs; ++u) {
+                const int e0 = (lane + 32 * u) * D::EPV;
+                vv[u] = e0 < len ? load_vec<D, VEC>(row, c0, e0, len) : neg_inf_vec<D>();
+            }
+            int idx = kNoIndex;
+#pragma unroll
+            for (int u = kTileVecs - 1; u >= 0; --u) {
+                const int e0 = (lane + 32 * u) * D::EPV;
+#pragma unroll
+                for (int e = D::EPV - 1; e >= 0; --e) {
+                    const bool hit = vec_elem<D>(vv[u], e) == bm && e0 + e < len;
+                    idx = hit ? int(c0) + e0 + e : idx;
+                }
+            }
+            idx = warp_reduce(idx, [](int a, int b) { return min(a, b); });
+            if (lane == 0) s_idx = idx;
+        }
+        __syncthreads();
+        const int r = tile >= 0 ? s_idx : -1;
+        __syncthreads();
+        return r;
+    };
+
+    // accepted nodes in index order: their rows decide their children and the bonus
+    int best = 0;
+    for (int v = 0; v < N; ++v) {
+        if (!s_acc[v]) continue;  // uniform: written before the last barrier
+        const int a = row_argmax(v);
+        if (a < 0) {  // a NaN in a row the rule reads
+            fail();
+            return;
+        }
+        if (tid == 0) s_arg[v] = a;
+        for (int c = v + 1 + tid; c < N; c += kLzThreads)
+            if (s_par[c] == v && s_tok[c] == a) s_acc[c] = 1;
+        if (s_dep[v] > s_dep[best]) best = v;
+        __syncthreads();
+    }
+    // outputs: the path root .. best, its tokens, the bonus argmax(best), -1 padding
+    const int depth = s_dep[best];
+    if (tid == 0)
+        for (int s = depth, node = best; s >= 0; --s) {
+            s_path[s] = node;
+            node = s_par[node];
+        }
+    __syncthreads();
+    for (int i = tid; i < W; i += kLzThreads) {
+        if (opath) opath[i] = i <= depth ? s_path[i] : -1;
+        out[i] = i < depth ? s_tok[s_path[i + 1]] : (i == depth ? s_arg[best] : -1);
+    }
+    if (tid == 0) accepted_len[seq] = depth;
+}
+
+cudaError_t launch_greedy_walk(int dtype, bool vec, Logits t, int B, int N, int V, bool chain, const int32_t *parent,
+                               const int32_t *tokens, int max_depth, int32_t *accepted_len, int32_t *out_tokens,
+                               int32_t *out_path, cudaStream_t s) {
+    const size_t smem = size_t(5 * N + max_depth + 1) * sizeof(int);
+    auto k = dtype == 1 ? (vec ? greedy_walk_kernel<BF16, true> : greedy_walk_kernel<BF16, false>)
+                        : (vec ? greedy_walk_kernel<F32, true> : greedy_walk_kernel<F32, false>);
+    return launch_after(k, unsigned(B), kLzThreads, smem, s, t, N, V, chain, parent, tokens, max_depth, accepted_len,
+                        out_tokens, out_path);
+}
+
+}  // namespace sv

@@ -64,10 +64,12 @@ __device__ __forceinline__ void load_unit(const char *row, int64_t u0, int len, 
 }  // namespace
 
 // One CTA per sequence.  Shared: parent, tokens, child counts, depths, the path, the
-// removed tokens and their frozen coefficients, and the reduction scratch.
+// removed tokens and their frozen coefficients, and the reduction scratch.  chain: the
+// tree whose node v has parent v - 1 and token node_tokens[seq * (N - 1) + v - 1] (the
+// chain rule of spec_verify_sample, read lazily).
 template <class D, bool VEC>
 __global__ void __launch_bounds__(kTsThreads, 1)
-    tree_sample_kernel(Logits t, Logits d, int N, int V, const int32_t *__restrict__ parent,
+    tree_sample_kernel(Logits t, Logits d, int N, int V, bool chain, const int32_t *__restrict__ parent,
                        const int32_t *__restrict__ node_tokens, int max_depth, float c, uint64_t seed,
                        uint64_t offset, int without_replacement, int nunit, float *__restrict__ umass,
                        int32_t *__restrict__ accepted_len, int32_t *__restrict__ out_tokens,
@@ -95,10 +97,10 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     if (tid == 0) s_flag = 1;
     __syncthreads();
     for (int v = tid; v < N; v += kTsThreads) {
-        const int p = parent[v];
+        const int p = chain ? v - 1 : parent[v];
         s_par[v] = p;
         s_nch[v] = 0;
-        const int tk = v == 0 ? 0 : node_tokens[seq * N + v];
+        const int tk = v == 0 ? 0 : (chain ? node_tokens[seq * (N - 1) + v - 1] : node_tokens[seq * N + v]);
         s_tok[v] = tk;
         if ((v == 0 && p != -1) || (v > 0 && (p < 0 || p >= v)) || tk < 0 || tk >= V) s_flag = 0;
     }
@@ -387,14 +389,16 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     if (tid == 0) accepted_len[seq] = depth;
 }
 
-cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, const int32_t *parent,
+cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, bool chain,
+                               const int32_t *parent,
                                const int32_t *node_tokens, int max_depth, float c, uint64_t seed, uint64_t offset,
                                int without_replacement, int nunit, float *umass, int32_t *accepted_len,
                                int32_t *out_tokens, int32_t *out_path, cudaStream_t s) {
     const size_t smem = size_t(4 * N + max_depth + 1) * sizeof(int);
     auto k = dtype == 1 ? (vec ? tree_sample_kernel<BF16, true> : tree_sample_kernel<BF16, false>)
                         : (vec ? tree_sample_kernel<F32, true> : tree_sample_kernel<F32, false>);
-    return launch_after(k, unsigned(B), kTsThreads, smem, s, t, d, N, V, parent, node_tokens, max_depth, c, seed,
+    return launch_after(k, unsigned(B), kTsThreads, smem, s, t, d, N, V, chain, parent, node_tokens, max_depth, c,
+                        seed,
                         offset, without_replacement, nunit, umass, accepted_len, out_tokens, out_path);
 }
 

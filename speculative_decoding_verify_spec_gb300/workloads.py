@@ -46,6 +46,9 @@ WORKLOADS = {
                             input_seed=1006, verify_seed=0x5EED + 6, temperature=1.0,
                             branching=(4, 3, 2, 2, 1, 1), without_replacement=True),
 }
+# the same inputs, verified by the lazy entries (rows read only where the rule needs them)
+for _base in ("sample_b256", "greedy_b512", "tree_b64"):
+    WORKLOADS[_base + "_lazy"] = dict(WORKLOADS[_base], lazy=True, base=_base)
 
 DESCRIPTIONS = {
     "sample_b1": "sampling verify B=1 V=1000 gamma=4 fp32 T=1.0",
@@ -56,6 +59,8 @@ DESCRIPTIONS = {
     "tree_sample_b64": ("token-tree sampling verify (multi-round rejection) B=64 N=64 depth=6 "
                         "V=128256 bf16 T=1.0, children drawn from q without replacement"),
 }
+for _base in ("sample_b256", "greedy_b512", "tree_b64"):
+    DESCRIPTIONS[_base + "_lazy"] = DESCRIPTIONS[_base] + ", lazy (rows read only where the rule needs them)"
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -289,6 +294,7 @@ def make(name: str, device="cpu", **overrides):
     """Inputs of a named workload (shapes may be overridden to make a smaller case)."""
     cfg = dict(WORKLOADS[name])
     cfg.update(overrides)
+    name = cfg.get("base", name)
     mode = cfg["mode"]
     if mode == "sample":
         common = dict(B=cfg["B"], gamma=cfg["gamma"], V=cfg["V"], dtype=cfg["dtype"],
