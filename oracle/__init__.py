@@ -69,6 +69,8 @@ def _bind(lib):
     lib.oracle_verify_tree_sample.restype = i32
     lib.oracle_exact_probs_tree.argtypes = [P, P, P, P, i32, i32, dbl, i32, P]
     lib.oracle_exact_probs_tree.restype = i32
+    lib.oracle_ngram_draft.argtypes = [P, i64, P, i32, i32, i32, i32, P, P]
+    lib.oracle_ngram_draft.restype = i32
     return lib
 
 
@@ -265,6 +267,21 @@ class Oracle:
         return prob
 
 
+    def ngram_draft(self, history, lengths, n, k, pad):
+        """Prompt-lookup drafts of a [B, T] int32 history with lengths[B]; returns
+        (drafts [B, k] (-1 padded), counts [B])."""
+        h = np.ascontiguousarray(np.asarray(history, dtype=np.int32))
+        B, T = h.shape
+        L = np.ascontiguousarray(np.asarray(lengths, dtype=np.int32).reshape(B))
+        drafts = np.zeros((B, k), np.int32)
+        count = np.zeros(B, np.int32)
+        rc = self.lib.oracle_ngram_draft(_ptr(h), T, _ptr(L), B, int(n), int(k), int(bool(pad)),
+                                         _ptr(drafts), _ptr(count))
+        if rc != 0:
+            raise ValueError("n must be >= 1 and k >= 0")
+        return drafts, count
+
+
 def philox4x32_10(ctr, key):
     return _load().philox4x32_10(ctr, key)
 
@@ -304,6 +321,10 @@ def verify_tree_sample(target, draft, parent, node_tokens, max_depth, temperatur
 def exact_probs_tree(t_logits, d_logits, parent, tokens, temperature, without_replacement=False):
     return _load().exact_probs_tree(t_logits, d_logits, parent, tokens, temperature,
                                     without_replacement)
+
+
+def ngram_draft(history, lengths, n, k, pad):
+    return _load().ngram_draft(history, lengths, n, k, pad)
 
 
 def default() -> Oracle:

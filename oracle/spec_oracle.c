@@ -828,3 +828,47 @@ done:
     free(r);
     return rc;
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* Prompt-lookup (n-gram) drafting [MS lookup_draft; SD Exercise 4 ngram_draft].
+ * history: [B][stride] tokens, len[b] of them valid.  For each sequence:
+ *   tail  = its last n tokens;
+ *   match = the largest i in [0, len - n - 1] with history[i + t] == tail[t] for every t
+ *           (the most recent EARLIER occurrence; the continuation starts at i + n <= len - 1);
+ *   drafts[m] = history[match + n + m] for m = 0, 1, ... while match + n + m < len, at most k;
+ *   pad != 0 (Exercise 4's fallback): the remaining slots, or all k when there is no match,
+ *           repeat the last token, so k tokens are always proposed (for len >= 1).
+ * count[b] = the number of drafts; unused slots are -1.  Exercise 4 is n = 1, pad = 1;
+ * lookup_draft is pad = 0 (n = 3, k = 4 in the page's example).                        */
+/* ------------------------------------------------------------------------------------ */
+int oracle_ngram_draft(const int32_t *history, int64_t stride, const int32_t *len, int B, int n, int k, int pad,
+                       int32_t *drafts, int32_t *count)
+{
+    if (n < 1 || k < 0)
+        return -1;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *h = history + (int64_t)b * stride;
+        int L = len[b];
+        int32_t *out = drafts + (int64_t)b * k;
+        for (int m = 0; m < k; ++m)
+            out[m] = -1;
+        count[b] = 0;
+        int match = -1;
+        for (int i = L - n - 1; i >= 0 && match < 0; --i) { /* right to left: the first hit is the latest */
+            int same = 1;
+            for (int t = 0; t < n && same; ++t)
+                same = h[i + t] == h[L - n + t];
+            if (same)
+                match = i;
+        }
+        int c = 0;
+        if (match >= 0)
+            for (; c < k && match + n + c < L; ++c)
+                out[c] = h[match + n + c];
+        if (pad && L >= 1)
+            for (; c < k; ++c)
+                out[c] = h[L - 1];
+        count[b] = c;
+    }
+    return 0;
+}

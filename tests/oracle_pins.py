@@ -638,6 +638,48 @@ def pin_tree_sample_invariants(orc):
 
 
 # --------------------------------------------------------------------------------------
+# Prompt-lookup (n-gram) drafting [MS lookup_draft; SD Exercise 4 ngram_draft]
+# --------------------------------------------------------------------------------------
+def pin_ngram_worked_examples(orc):
+    """Drafts worked by hand from the pages' definitions (tests/golden)."""
+    with open(os.path.join(GOLDEN, "ngram_draft_examples.txt")) as f:
+        cases = [ln.rstrip("\n") for ln in f if ln.strip() and not ln.startswith("#")]
+    assert len(cases) >= 10
+    for ln in cases:
+        head, hist, want = (s.split() for s in ln.split("|"))
+        n, k, pad = (int(x) for x in head)
+        h = np.array([[int(x) for x in hist]], np.int32)
+        drafts, count = orc.ngram_draft(h, [h.shape[1]], n, k, pad)
+        want = [int(x) for x in want]
+        assert count[0] == len(want) and list(drafts[0, :len(want)]) == want, (ln, drafts, count)
+        assert (drafts[0, len(want):] == -1).all()
+
+
+def pin_ngram_bruteforce(orc):
+    """On random small-alphabet histories (ragged lengths, padded rows): the draft is the
+    continuation of the latest earlier occurrence of the tail -- every later start in the
+    search range fails to match -- and nothing is proposed without one (unless padded)."""
+    rs = np.random.RandomState(61)
+    for n, k, pad, alpha in ((1, 4, 1, 3), (1, 5, 0, 8), (2, 4, 0, 3), (3, 4, 0, 2), (4, 7, 1, 2)):
+        B, T = 300, 40
+        h = rs.randint(0, alpha, (B, T)).astype(np.int32)
+        L = rs.randint(0, T + 1, B).astype(np.int32)
+        drafts, count = orc.ngram_draft(h, L, n, k, pad)
+        for b in range(B):
+            seq = list(h[b, :L[b]])
+            starts = [i for i in range(0, len(seq) - n) if seq[i:i + n] == seq[len(seq) - n:]]
+            if starts:
+                i = max(starts)
+                cont = seq[i + n:i + n + k]
+            else:
+                cont = []
+            if pad and seq:
+                cont = cont + [seq[-1]] * (k - len(cont))
+            assert count[b] == len(cont) and list(drafts[b, :len(cont)]) == cont, (b, seq)
+            assert (drafts[b, len(cont):] == -1).all()
+
+
+# --------------------------------------------------------------------------------------
 # P10: row max / log-sum-exp against scipy's logsumexp [SD apply_temperature]
 # --------------------------------------------------------------------------------------
 def pin_row_stats(orc):
@@ -664,5 +706,5 @@ ALL_PINS = [
     pin_round_invariants, pin_worked_example, pin_acceptance_rate, pin_greedy_textbook,
     pin_tree_printed_depths, pin_chain_tree_equals_greedy, pin_tree_bruteforce, pin_row_stats,
     pin_tree_sample_lossless, pin_tree_sample_chi2, pin_chain_tree_sample_equals_chain,
-    pin_tree_sample_invariants,
+    pin_tree_sample_invariants, pin_ngram_worked_examples, pin_ngram_bruteforce,
 ]

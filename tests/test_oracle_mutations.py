@@ -61,6 +61,15 @@ MUTATIONS = [
      [pins.pin_chain_tree_sample_equals_chain]),
     ("tree_sampler_accept_swapped", "if (u * q[x] < p[x]) {", "if (u * p[x] < q[x]) {",
      [tree_chi2_quick, pins.pin_chain_tree_sample_equals_chain]),
+    ("ngram_earliest_match", "for (int i = L - n - 1; i >= 0 && match < 0; --i) {",
+     "for (int i = 0; i <= L - n - 1 && match < 0; ++i) {",
+     [pins.pin_ngram_worked_examples, pins.pin_ngram_bruteforce]),
+    ("ngram_tail_matches_itself", "for (int i = L - n - 1; i >= 0 && match < 0; --i) {",
+     "for (int i = L - n; i >= 0 && match < 0; --i) {",
+     [pins.pin_ngram_worked_examples, pins.pin_ngram_bruteforce]),
+    ("ngram_no_fallback", "        if (pad && L >= 1)\n            for (; c < k; ++c)",
+     "        if (0 && pad && L >= 1)\n            for (; c < k; ++c)",
+     [pins.pin_ngram_worked_examples, pins.pin_ngram_bruteforce]),
 ]
 
 
