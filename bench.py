@@ -32,18 +32,18 @@ if ROOT not in sys.path:
 
 DEFAULT_WORKLOAD = "sample_b256"
 SECONDARY = ["greedy_b512", "tree_b64", "tree_sample_b64", "sample_b256_lazy", "greedy_b512_lazy",
-             "tree_b64_lazy"]
+             "tree_b64_lazy", "ngram_b256"]
 METRIC = "verified seqs/s"
 UNIT = "seqs/s"
 FALLBACK_HBM_GBS = 6800.0
 DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "max_tiles_kernel",
                    "tree": "max_tiles_kernel", "tree_sample": "tree_sample_kernel",
                    "sample_lazy": "tree_sample_kernel", "greedy_lazy": "greedy_walk_kernel",
-                   "tree_lazy": "greedy_walk_kernel"}
+                   "tree_lazy": "greedy_walk_kernel", "ngram": "ngram_draft_kernel"}
 STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
 STAGES = {"sample": ["row_stats", "decide", "residual_mass", "inverse_cdf", "redraw"],
           "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"], "tree_sample": ["walk"],
-          "sample_lazy": ["walk"], "greedy_lazy": ["walk"], "tree_lazy": ["walk"]}
+          "sample_lazy": ["walk"], "greedy_lazy": ["walk"], "tree_lazy": ["walk"], "ngram": ["draft"]}
 
 
 def parse_args():
@@ -195,6 +195,8 @@ def kernel_bytes(name: str, **ov) -> int:
     """Algorithmic bytes of the dominant kernel per launch: every logit it streams, once."""
     from speculative_decoding_verify_spec_gb300 import workloads as W
     cfg = W.WORKLOADS[name]
+    if cfg["mode"] == "ngram":
+        return W.logical_bytes(name, **ov)
     s = 2 if cfg["dtype"] == "bf16" else 4
     return W.rows(name, **ov) * cfg["V"] * s
 
@@ -212,6 +214,13 @@ def make_call(name, inputs, dev, **ov):
     B, V = cfg["B"], cfg["V"]
     dt = binding.BF16 if cfg["dtype"] == "bf16" else binding.FP32
     lazy = cfg.get("lazy", False)
+    if mode == "ngram":
+        drafts = torch.empty((B, cfg["k"]), dtype=torch.int32, device=dev)
+        count = torch.empty(B, dtype=torch.int32, device=dev)
+
+        def call(history=inputs.history, lengths=inputs.lengths):
+            return sv.spec_ngram_draft(history, lengths, inputs.n, inputs.k, inputs.pad, drafts=drafts, count=count)
+        return call, (count, drafts)
     if mode == "sample" and lazy:
         g = cfg["gamma"]
         ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_SAMPLE_LAZY, B, g, V, dt),
@@ -373,6 +382,10 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
         res.update({"hbm_gbs_step": None, "frac_of_8tbs_step": None, "roofline": None,
                     "lazy": "one CTA per sequence reads only the rows of the nodes its walk reaches",
                     "mean_path_nodes": float(acc[acc >= 0].mean().item() + 1) if (acc >= 0).any() else None})
+    if mode == "ngram":
+        res.update({"rows_per_s": None, "roofline": None, "mean_accepted_len": None,
+                    "mean_drafts": float(outs[0].float().mean().item()),
+                    "bytes_note": "every history token once; the search stops at the first chunk holding a match"})
     if mode.endswith("_lazy"):
         # bytes the walks read in the last step, from its outputs: chain greedy reads rows
         # 0..k; tree greedy the rows of the accepted nodes (at least the path); chain

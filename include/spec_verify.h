@@ -218,6 +218,25 @@ sv_status spec_verify_tree_greedy_lazy(const void *target_logits, int64_t t_batc
                                        int32_t *out_path, void *stream);
 
 /*
+ * Prompt-lookup (n-gram) drafting [MS lookup_draft; SD Exercise 4 ngram_draft]: the drafts
+ * that the verification entries take, from the token history itself.
+ *
+ *   history  [B][stride] int32   each sequence's tokens so far, lengths[b] of them valid
+ *                                (a length outside [0, stride] is clamped to it).
+ *   n        1 .. 64             the n-gram: the sequence's last n tokens (the tail).
+ *   k        0 .. SV_MAX_GAMMA   tokens to propose.
+ *   pad      nonzero: always propose k tokens, filling with the last token (Exercise 4).
+ * The drafts are the tokens that followed the tail's most recent earlier occurrence (a
+ * start i <= len - n - 1 whose n tokens equal the tail), at most k of them; none without a
+ * match (or with len < n + 1) unless padded.  Outputs: drafts [B][k] (-1 in unused slots),
+ * count [B].  The drafter's q is one-hot on each draft: verify with spec_verify_greedy, or
+ * with spec_verify_sample given draft rows that are -inf except at the draft token.
+ * No workspace; one CTA per sequence searches from the end of the history backwards.
+ */
+sv_status spec_ngram_draft(const int32_t *history, int64_t stride, const int32_t *lengths, int B, int n,
+                           int k, int pad, int32_t *drafts, int32_t *count, void *stream);
+
+/*
  * Greedy verification that allocates nothing and takes no workspace.  (The pages have no
  * counterpart: this is a deployment variant of spec_verify_greedy.)
  *

@@ -8,6 +8,7 @@ generators shared by tests and bench (``workloads``).
 from .binding import (  # noqa: F401
     SpecVerifyError,
     load_library,
+    spec_ngram_draft,
     spec_verify_greedy,
     spec_verify_greedy_lazy,
     spec_verify_row_stats,
@@ -23,6 +24,7 @@ from .binding import (  # noqa: F401
 __all__ = [
     "SpecVerifyError",
     "load_library",
+    "spec_ngram_draft",
     "spec_verify_greedy",
     "spec_verify_greedy_lazy",
     "spec_verify_row_stats",

@@ -65,6 +65,8 @@ def load_library() -> ctypes.CDLL:
         lib.spec_verify_greedy_lazy.restype = i32
         lib.spec_verify_tree_greedy_lazy.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, i32, P, P, P, P]
         lib.spec_verify_tree_greedy_lazy.restype = i32
+        lib.spec_ngram_draft.argtypes = [P, i64, P, i32, i32, i32, i32, P, P, P]
+        lib.spec_ngram_draft.restype = i32
         lib.spec_verify_row_stats.argtypes = [P, i64, i64, i32, i32, i32, i32, f32, P, P, P, sz, P]
         lib.spec_verify_row_stats.restype = i32
         lib.spec_verify_uniforms.argtypes = [u64, u64, i32, i32, i32, P, P]
@@ -334,6 +336,26 @@ def spec_verify_tree_greedy_lazy(target: torch.Tensor, parent: torch.Tensor, nod
                                           _stream(dev))
     _check(st, "spec_verify_tree_greedy_lazy")
     return accepted_len, out_tokens, out_path
+
+
+def spec_ngram_draft(history: torch.Tensor, lengths: torch.Tensor, n: int, k: int, pad: bool = False,
+                     *, drafts=None, count=None):
+    """Prompt-lookup drafts of a [B, T] int32 history with lengths [B]; returns (drafts
+    [B, k] int32, -1 in unused slots, count [B] int32)."""
+    lib = load_library()
+    if history.dim() != 2 or history.dtype != torch.int32 or history.stride(1) != 1:
+        raise ValueError("history must be a [B, T] int32 tensor with contiguous rows")
+    B, T = history.shape
+    L = _ints(lengths, "lengths", (B,))
+    dev = history.device
+    if drafts is None:
+        drafts = torch.empty((B, int(k)), dtype=torch.int32, device=dev)
+    if count is None:
+        count = torch.empty(B, dtype=torch.int32, device=dev)
+    st = lib.spec_ngram_draft(history.data_ptr(), history.stride(0), L.data_ptr(), B, int(n), int(k),
+                              int(bool(pad)), drafts.data_ptr(), count.data_ptr(), _stream(dev))
+    _check(st, "spec_ngram_draft")
+    return drafts, count
 
 
 def spec_verify_row_stats(logits: torch.Tensor, temperature: float = 1.0, *, workspace=None):

@@ -373,6 +373,16 @@ sv_status spec_verify_tree_greedy_lazy(const void *target_logits, int64_t t_batc
     return cuda_status(e);
 }
 
+sv_status spec_ngram_draft(const int32_t *history, int64_t stride, const int32_t *lengths, int B, int n, int k,
+                           int pad, int32_t *drafts, int32_t *count, void *stream) {
+    if (B < 0 || n < 1 || n > sv::kMaxNgram || k < 0 || k > SV_MAX_GAMMA || stride < 0 || stride > (1 << 30))
+        return SV_ERR_INVALID_ARG;
+    if (B == 0) return SV_OK;
+    if (!history || !lengths || !count || (k > 0 && !drafts)) return SV_ERR_INVALID_ARG;
+    return cuda_status(sv::launch_ngram_draft(history, stride, lengths, B, n, k, pad, drafts, count,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 sv_status spec_verify_row_stats(const void *logits, int64_t batch_stride, int64_t row_stride,
                                 sv_dtype dtype, int B, int rows_per_seq, int V,
                                 float temperature, float *m_out, float *lse_out,

@@ -76,6 +76,10 @@ cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, i
 cudaError_t launch_greedy_walk(int dtype, bool vec, Logits t, int B, int N, int V, bool chain, const int32_t *parent,
                                const int32_t *tokens, int max_depth, int32_t *accepted_len, int32_t *out_tokens,
                                int32_t *out_path, cudaStream_t s);
+// Prompt-lookup drafting: history [B][stride] with lengths[B]; drafts [B][k], count [B].
+constexpr int kMaxNgram = 64;
+cudaError_t launch_ngram_draft(const int32_t *history, int64_t stride, const int32_t *lengths, int B, int n, int k,
+                               int pad, int32_t *drafts, int32_t *count, cudaStream_t s);
 // Logits per unit of the extended-precision re-draw (32 lanes x 2).
 inline int refine_unit_elems(int) { return 64; }
 // Per listed sequence the re-draw keeps (4 gamma + 1) x nref double-float unit sums and,

@@ -46,6 +46,7 @@ WORKLOADS = {
                             input_seed=1006, verify_seed=0x5EED + 6, temperature=1.0,
                             branching=(4, 3, 2, 2, 1, 1), without_replacement=True),
 }
+WORKLOADS["ngram_b256"] = dict(mode="ngram", B=256, T=16384, V=128256, n=3, k=8, pad=False, input_seed=1007)
 # the same inputs, verified by the lazy entries (rows read only where the rule needs them)
 for _base in ("sample_b256", "greedy_b512", "tree_b64"):
     WORKLOADS[_base + "_lazy"] = dict(WORKLOADS[_base], lazy=True, base=_base)
@@ -59,6 +60,8 @@ DESCRIPTIONS = {
     "tree_sample_b64": ("token-tree sampling verify (multi-round rejection) B=64 N=64 depth=6 "
                         "V=128256 bf16 T=1.0, children drawn from q without replacement"),
 }
+DESCRIPTIONS["ngram_b256"] = ("prompt-lookup drafting B=256 histories of up to 16384 tokens (V=128256, copy-heavy), "
+                              "n=3, k=8")
 for _base in ("sample_b256", "greedy_b512", "tree_b64"):
     DESCRIPTIONS[_base + "_lazy"] = DESCRIPTIONS[_base] + ", lazy (rows read only where the rule needs them)"
 
@@ -290,6 +293,41 @@ def make_tree_sample(B, V, dtype="bf16", seed=1, verify_seed=0, device="cpu",
                             bool(without_replacement), list(depth))
 
 
+@dataclass
+class NgramInputs:
+    history: torch.Tensor   # [B, T] int32
+    lengths: torch.Tensor   # [B] int32
+    n: int
+    k: int
+    pad: bool
+
+
+def make_ngram(B, T, V, n=3, k=8, pad=False, seed=1, device="cpu", copies=64, span=(16, 64),
+               tail_copy=0.8):
+    """Copy-heavy token histories: uniform tokens into which `copies` spans of earlier text
+    are copied (the repetition prompt lookup exploits); with probability tail_copy the last
+    span of a history repeats an earlier one, so its tail usually has an earlier occurrence.
+    Lengths are ragged in [T - 1024, T]."""
+    import numpy as np
+    rs = np.random.RandomState(seed)
+    h = rs.randint(0, V, (B, T)).astype(np.int32)
+    lengths = (T - rs.randint(0, min(1024, T), B)).astype(np.int32)
+    for b in range(B):
+        L = int(lengths[b])
+        for _ in range(copies):
+            ln = int(rs.randint(span[0], span[1] + 1))
+            if L <= 2 * ln + 1:
+                break
+            dst = int(rs.randint(ln, L - ln))
+            src = int(rs.randint(0, dst - ln + 1))
+            h[b, dst:dst + ln] = h[b, src:src + ln]
+        if rs.rand() < tail_copy and L > 2 * span[1] + 1:
+            ln = span[1]
+            src = int(rs.randint(0, L - 2 * ln))
+            h[b, L - ln:L] = h[b, src:src + ln]
+    return NgramInputs(torch.from_numpy(h).to(device), torch.from_numpy(lengths).to(device), n, k, pad)
+
+
 def make(name: str, device="cpu", **overrides):
     """Inputs of a named workload (shapes may be overridden to make a smaller case)."""
     cfg = dict(WORKLOADS[name])
@@ -309,6 +347,8 @@ def make(name: str, device="cpu", **overrides):
     if mode == "greedy":
         return make_greedy(cfg["B"], cfg["gamma"], cfg["V"], cfg["dtype"], cfg["input_seed"],
                            device)
+    if mode == "ngram":
+        return make_ngram(cfg["B"], cfg["T"], cfg["V"], cfg["n"], cfg["k"], cfg["pad"], cfg["input_seed"], device)
     if mode == "tree_sample":
         return make_tree_sample(cfg["B"], cfg["V"], cfg["dtype"], cfg["input_seed"],
                                 cfg["verify_seed"], device, tuple(cfg["branching"]), cfg["N"],
@@ -319,9 +359,11 @@ def make(name: str, device="cpu", **overrides):
 
 def logical_bytes(name: str, **overrides) -> int:
     """Bytes the metric counts for one verify call: every logit once plus the small
-    integer inputs and outputs."""
+    integer inputs and outputs (for the drafter: every history token once, and the drafts)."""
     cfg = dict(WORKLOADS[name])
     cfg.update(overrides)
+    if cfg["mode"] == "ngram":
+        return cfg["B"] * (cfg["T"] * 4 + 4 + cfg["k"] * 4 + 4)
     s = 2 if cfg["dtype"] == "bf16" else 4
     B, V = cfg["B"], cfg["V"]
     if cfg["mode"] == "sample":
@@ -348,6 +390,8 @@ def units(name: str, **overrides) -> int:
 def rows(name: str, **overrides) -> int:
     cfg = dict(WORKLOADS[name])
     cfg.update(overrides)
+    if cfg["mode"] == "ngram":
+        return cfg["B"]
     if cfg["mode"] == "sample":
         return cfg["B"] * (2 * cfg["gamma"] + 1)
     if cfg["mode"] == "greedy":
