@@ -58,10 +58,11 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
     case SV_MODE_GREEDY: R = size_t(rows) + 1; break;
     case SV_MODE_TREE:
     case SV_MODE_ROW_STATS: R = size_t(rows); break;
-    case SV_MODE_TREE_SAMPLE:  // unit masses of the node being walked, per sequence
+    case SV_MODE_TREE_SAMPLE:  // unit masses of the node being walked, then per-CTA row statistics
     case SV_MODE_SAMPLE_LAZY:
         L.partial = 0;
-        L.total = up256(size_t(B) * size_t(nrt_of(V, dtype)) * 4);
+        L.rowstat = up256(size_t(B) * size_t(nrt_of(V, dtype)) * 4);
+        L.total = L.rowstat + up256(size_t(B) * sv::kTreeSampleCluster * 2 * 8);
         return L;
     default: return L;
     }
@@ -295,7 +296,8 @@ sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_str
         e = sv::launch_tree_sample(dtype == SV_BF16, vec, t, d, B, N, V, false, parent, node_tokens, max_depth, c,
                                    seed,
                                    offset, without_replacement, nrt_of(V, dtype),
-                                   reinterpret_cast<float *>(at(workspace, 0)), accepted_len, out_tokens,
+                                   reinterpret_cast<float *>(at(workspace, 0)),
+                                   reinterpret_cast<float2 *>(at(workspace, L.rowstat)), accepted_len, out_tokens,
                                    out_path, s);
     if (e == cudaSuccess) e = mark(1, s);
     return cuda_status(e);
@@ -327,7 +329,8 @@ sv_status spec_verify_sample_lazy(const void *target_logits, int64_t t_batch_str
     if (e == cudaSuccess)
         e = sv::launch_tree_sample(dtype == SV_BF16, vec, t, d, B, gamma + 1, V, true, nullptr, draft_tokens, gamma,
                                    c, seed, offset, 0, nrt_of(V, dtype), reinterpret_cast<float *>(at(workspace, 0)),
-                                   accepted_len, out_tokens, nullptr, s);
+                                   reinterpret_cast<float2 *>(at(workspace, L.rowstat)), accepted_len, out_tokens,
+                                   nullptr, s);
     if (e == cudaSuccess) e = mark(1, s);
     return cuda_status(e);
 }

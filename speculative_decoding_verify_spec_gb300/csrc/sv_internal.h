@@ -65,12 +65,12 @@ cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamm
 // Token-tree sampling (multi-round rejection), one CTA per sequence reading the rows of the
 // nodes its walk reaches; with chain, the tree whose node v has parent v - 1 and token
 // node_tokens[b][v - 1] ([B][N - 1]).  c = log2(e) / T; umass: [B][nunit] floats of
-// scratch, nunit = ceil(V / res_tile_elems).
+// scratch, nunit = ceil(V / res_tile_elems); cstat: [B][kTreeSampleCluster][2] float2.
+constexpr int kTreeSampleCluster = 4;  // at most this many CTAs (SMs) per sequence of the walk
 cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, bool chain,
-                               const int32_t *parent,
-                               const int32_t *node_tokens, int max_depth, float c, uint64_t seed, uint64_t offset,
-                               int without_replacement, int nunit, float *umass, int32_t *accepted_len,
-                               int32_t *out_tokens, int32_t *out_path, cudaStream_t s);
+                               const int32_t *parent, const int32_t *node_tokens, int max_depth, float c, uint64_t seed,
+                               uint64_t offset, int without_replacement, int nunit, float *umass, float2 *cstat,
+                               int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path, cudaStream_t s);
 // Lazy greedy verification, one CTA per sequence reading only the rows of accepted nodes:
 // a tree (parent[N], tokens [B][N]) or, with chain, the chain of draft tokens [B][N - 1].
 cudaError_t launch_greedy_walk(int dtype, bool vec, Logits t, int B, int N, int V, bool chain, const int32_t *parent,

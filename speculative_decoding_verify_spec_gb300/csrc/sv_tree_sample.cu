@@ -33,6 +33,28 @@ constexpr int kTsThreads = 1024;
 constexpr int kTsWarps = kTsThreads / 32;
 constexpr int kMaxRemoved = 64;  // tokens removed from q at one node (without replacement)
 
+// All threads of the sequence's cluster (or CTA).  The .release / .acquire barrier orders
+// the threads' memory operations at cluster scope, so unit masses and statistics written
+// before it by one CTA are seen after it by the others.
+template <int CS>
+__device__ __forceinline__ void csync() {
+    if constexpr (CS > 1) {
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    } else {
+        __syncthreads();
+    }
+}
+template <int CS>
+__device__ __forceinline__ int cluster_rank() {
+    if constexpr (CS > 1) {
+        unsigned r;
+        asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+        return int(r);
+    } else {
+        return 0;
+    }
+}
+
 __device__ __forceinline__ float tweight(float x, float M, float c) { return ex2(__fmul_rn(__fsub_rn(x, M), c)); }
 
 // The state of the current node: its rows' statistics and the implicit (p, q).
@@ -63,15 +85,18 @@ __device__ __forceinline__ void load_unit(const char *row, int64_t u0, int len, 
 
 }  // namespace
 
-// One CTA per sequence.  Shared: parent, tokens, child counts, depths, the path, the
+// One cluster of CS CTAs per sequence: every CTA runs the same walk, takes every CS-th
+// unit of each pass, and merges the CTAs' partials in rank order after a cluster barrier,
+// so all of them take the same decisions; rank 0 draws and writes the outputs.  cstat:
+// [B][CS][2] per-CTA row statistics.  Shared: parent, tokens, child counts, depths, the path, the
 // removed tokens and their frozen coefficients, and the reduction scratch.  chain: the
 // tree whose node v has parent v - 1 and token node_tokens[seq * (N - 1) + v - 1] (the
 // chain rule of spec_verify_sample, read lazily).
-template <class D, bool VEC>
+template <class D, bool VEC, int CS>
 __global__ void __launch_bounds__(kTsThreads, 1)
     tree_sample_kernel(Logits t, Logits d, int N, int V, bool chain, const int32_t *__restrict__ parent,
                        const int32_t *__restrict__ node_tokens, int max_depth, float c, uint64_t seed,
-                       uint64_t offset, int without_replacement, int nunit, float *__restrict__ umass,
+                       uint64_t offset, int without_replacement, int nunit, float *umass, float2 *cstat,
                        int32_t *__restrict__ accepted_len, int32_t *__restrict__ out_tokens,
                        int32_t *__restrict__ out_path) {
     extern __shared__ int s_int[];
@@ -86,7 +111,9 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     griddep_launch_next();
     griddep_wait();  // the caller's kernels may still be writing the inputs
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t seq = blockIdx.x;
+    const int64_t seq = blockIdx.x / CS;
+    const int rank = cluster_rank<CS>();
+    const int gw = rank * kTsWarps + warp;  // this warp among the cluster's
     const int W = max_depth + 1;
     int32_t *out = out_tokens + seq * W;
     int32_t *opath = out_path ? out_path + seq * W : nullptr;
@@ -116,6 +143,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     }
     __syncthreads();
     auto fail = [&]() {
+        if (rank != 0) return;
         for (int i = tid; i < W; i += kTsThreads) {
             out[i] = -1;
             if (opath) opath[i] = -1;
@@ -131,7 +159,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     // the unit masses go to um[], their total (fixed order) is returned to every thread.
     // a = 0 reads the target row only.
     auto mass_pass = [&](const char *tp, const char *dp, const NodeState &st, float a) -> float {
-        for (int u = warp; u < nunit; u += kTsWarps) {
+        for (int u = gw; u < nunit; u += CS * kTsWarps) {
             const int64_t u0 = int64_t(u) * RE;
             const int len = unit_len(V, u0, RE);
             uint4 tv[kResVecs], dv[kResVecs];
@@ -146,9 +174,9 @@ __global__ void __launch_bounds__(kTsThreads, 1)
             acc = warp_reduce(acc, [](float x, float y) { return x + y; });
             if (lane == 0) um[u] = acc;
         }
-        __syncthreads();  // the unit masses of every warp
-        // tokens removed earlier keep their own coefficient: correct their units (thread 0)
-        if (tid == 0 && a != 0.f) {
+        csync<CS>();  // the unit masses of every warp of the cluster
+        // tokens removed earlier keep their own coefficient: correct their units (rank 0)
+        if (rank == 0 && tid == 0 && a != 0.f) {
             for (int r = 0; r < st.nrem; ++r) {
                 if (s_remcoef[r] == a) continue;
                 const int j = s_remtok[r];
@@ -156,7 +184,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
                 um[j / RE] += wgt(tj, dj, st, s_remcoef[r], c) - wgt(tj, dj, st, a, c);
             }
         }
-        __syncthreads();
+        csync<CS>();
         // total: lanes of warp 0 own contiguous runs of units, then a warp scan
         if (warp == 0) {
             const int per = (nunit + 31) / 32;
@@ -170,7 +198,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
         }
         __syncthreads();
         const float tot = s_sum[0];
-        __syncthreads();
+        csync<CS>();  // every CTA has read um[] before any may start the next pass
         return tot;
     };
 
@@ -178,7 +206,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     // returns (M, S) and whether the row is a distribution.
     auto row_stats = [&](const char *row, int slot) -> float2 {
         float2 ws = make_float2(-__int_as_float(0x7f800000), 0.f);
-        for (int u = warp; u < nunit; u += kTsWarps) {
+        for (int u = gw; u < nunit; u += CS * kTsWarps) {
             const int64_t u0 = int64_t(u) * RE;
             const int len = unit_len(V, u0, RE);
             uint4 v[kResVecs];
@@ -192,7 +220,16 @@ __global__ void __launch_bounds__(kTsThreads, 1)
         __syncthreads();
         float2 r = s_stat[slot][0];
         for (int w = 1; w < kTsWarps; ++w) r = merge_stats(r, s_stat[slot][w], c);
-        __syncthreads();
+        if constexpr (CS > 1) {  // the CTAs' statistics, merged in rank order by each CTA
+            float2 *cs = cstat + seq * CS * 2;
+            if (tid == 0) cs[rank * 2 + slot] = r;
+            csync<CS>();
+            r = cs[slot];
+            for (int k = 1; k < CS; ++k) r = merge_stats(r, cs[k * 2 + slot], c);
+            csync<CS>();  // read by every CTA before the next statistics overwrite them
+        } else {
+            __syncthreads();
+        }
         return r;
     };
 
@@ -286,7 +323,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
         }
         // the final token at v: from w under the current state (the last residual, or p)
         const float total = residual_ready ? last_total : mass_pass(tp, dp, st, st.A);
-        if (warp == 0) {
+        if (warp == 0 && rank == 0) {
             const float u2 = uniform01(seed, offset, uint32_t(seq), uint32_t(v), 1u);
             const float thr = u2 * total;
             const int per = (nunit + 31) / 32;
@@ -376,6 +413,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
         __syncthreads();
         break;
     }
+    if (rank != 0) return;
     // outputs: the path (root .. v), its tokens, the final token, -1 padding
     const int tok = __float_as_int(s_tx[0]);
     for (int i = tid; i < W; i += kTsThreads) {
@@ -389,17 +427,54 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     if (tid == 0) accepted_len[seq] = depth;
 }
 
-cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, bool chain,
-                               const int32_t *parent,
-                               const int32_t *node_tokens, int max_depth, float c, uint64_t seed, uint64_t offset,
-                               int without_replacement, int nunit, float *umass, int32_t *accepted_len,
-                               int32_t *out_tokens, int32_t *out_path, cudaStream_t s) {
+namespace {
+template <int CS>
+cudaError_t launch_walk(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, bool chain, const int32_t *parent,
+                        const int32_t *node_tokens, int max_depth, float c, uint64_t seed, uint64_t offset,
+                        int without_replacement, int nunit, float *umass, float2 *cstat, int32_t *accepted_len,
+                        int32_t *out_tokens, int32_t *out_path, cudaStream_t s) {
     const size_t smem = size_t(4 * N + max_depth + 1) * sizeof(int);
-    auto k = dtype == 1 ? (vec ? tree_sample_kernel<BF16, true> : tree_sample_kernel<BF16, false>)
-                        : (vec ? tree_sample_kernel<F32, true> : tree_sample_kernel<F32, false>);
-    return launch_after(k, unsigned(B), kTsThreads, smem, s, t, d, N, V, chain, parent, node_tokens, max_depth, c,
-                        seed,
-                        offset, without_replacement, nunit, umass, accepted_len, out_tokens, out_path);
+    auto k = dtype == 1 ? (vec ? tree_sample_kernel<BF16, true, CS> : tree_sample_kernel<BF16, false, CS>)
+                        : (vec ? tree_sample_kernel<F32, true, CS> : tree_sample_kernel<F32, false, CS>);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(B) * CS);
+    cfg.blockDim = dim3(kTsThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CS;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CS > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, k, t, d, N, V, chain, parent, node_tokens, max_depth, c, seed, offset,
+                              without_replacement, nunit, umass, cstat, accepted_len, out_tokens, out_path);
+}
+}  // namespace
+
+// The cluster size: as many SMs per sequence as keep every sequence's cluster resident at
+// once (a pass is a few unit loads per warp, so a second wave of clusters costs more than
+// a wider cluster saves).
+cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, bool chain,
+                               const int32_t *parent, const int32_t *node_tokens, int max_depth, float c, uint64_t seed,
+                               uint64_t offset, int without_replacement, int nunit, float *umass, float2 *cstat,
+                               int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path, cudaStream_t s) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    static_assert(kTreeSampleCluster == 4, "the statistics scratch is sized for clusters of up to 4");
+    if (int64_t(B) * 4 <= sms)
+        return launch_walk<4>(dtype, vec, t, d, B, N, V, chain, parent, node_tokens, max_depth, c, seed, offset,
+                              without_replacement, nunit, umass, cstat, accepted_len, out_tokens, out_path, s);
+    if (int64_t(B) * 2 <= sms)
+        return launch_walk<2>(dtype, vec, t, d, B, N, V, chain, parent, node_tokens, max_depth, c, seed, offset,
+                              without_replacement, nunit, umass, cstat, accepted_len, out_tokens, out_path, s);
+    return launch_walk<1>(dtype, vec, t, d, B, N, V, chain, parent, node_tokens, max_depth, c, seed, offset,
+                          without_replacement, nunit, umass, cstat, accepted_len, out_tokens, out_path, s);
 }
 
 }  // namespace sv
