@@ -42,8 +42,8 @@ DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "max_tiles_kernel",
                    "tree_lazy": "greedy_walk_kernel", "ngram": "ngram_draft_kernel"}
 STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
 STAGES = {"sample": ["row_stats", "decide", "residual_mass", "inverse_cdf", "redraw"],
-          "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"], "tree_sample": ["walk"],
-          "sample_lazy": ["walk"], "greedy_lazy": ["walk"], "tree_lazy": ["walk"], "ngram": ["draft"]}
+          "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"], "tree_sample": ["walk", "rewalk_exp", "rewalk"],
+          "sample_lazy": ["walk", "rewalk_exp", "rewalk"], "greedy_lazy": ["walk"], "tree_lazy": ["walk"], "ngram": ["draft"]}
 
 
 def parse_args():

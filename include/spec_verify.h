@@ -169,8 +169,15 @@ sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_str
  * out_path = node ids (may be NULL).  Rows are read lazily, one CTA per sequence: only the
  * rows of the nodes the walk reaches.  A malformed or too deep tree makes every sequence
  * -1; a token of b outside [0, V), or a row the walk reads that is not a distribution (NaN,
- * +inf, no finite entry), makes sequence b -1.  Workspace: B * ceil(V / unit) floats
- * (spec_verify_workspace_size(SV_MODE_TREE_SAMPLE, B, N, V, dtype)).
+ * +inf, no finite entry), makes sequence b -1.  The walk decides in fp32 and marks the
+ * sequences where one decision came within a few fp32 errors of flipping; two more kernels
+ * walk the marked ones again (the first 8 per call, in index order) in double-float
+ * arithmetic and rewrite their outputs, so the result is the exact rule's except where a
+ * decision is closer than ~1e-12 to its boundary (spec_verify_walk_redraw_offset).
+ * Workspace: spec_verify_workspace_size(SV_MODE_TREE_SAMPLE, B, N, V, dtype) bytes, about
+ * 128 V min(N, 8) bytes: the re-walk keeps the double-float exponentials of the rows of up
+ * to 8 reached nodes for each of 8 sequences (115 MB at N = 64, V = 128256 with
+ * max_depth = 6 needing 7 of the 8 positions; the size assumes 8).
  */
 sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_stride,
                                   int64_t t_row_stride, const void *draft_logits,
@@ -192,7 +199,8 @@ sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_str
  *
  *   spec_verify_sample_lazy       the chain rule of spec_verify_sample (the tree rule of
  *                                 spec_verify_tree_sample on the chain v -> v + 1, whose
- *                                 uniforms are the chain's); workspace:
+ *                                 uniforms are the chain's, with its double-float re-walk
+ *                                 of marked sequences); workspace:
  *                                 spec_verify_workspace_size(SV_MODE_SAMPLE_LAZY, B, gamma,
  *                                 V, dtype) bytes.
  *   spec_verify_greedy_lazy       the rule of spec_verify_greedy; no workspace.
@@ -284,7 +292,7 @@ sv_status spec_verify_uniforms(uint64_t seed, uint64_t offset, int B, int positi
  * Test hook: where spec_verify_sample keeps its re-draw bookkeeping inside a sampling
  * workspace of these sizes (byte offset of an int32 array, (size_t)-1 for bad sizes).
  *   [0] sequences the last call marked for the extended-precision re-draw: a draw whose
- *       threshold u'R lies within 5e-7 R of a CDF boundary, or an accept test with
+ *       threshold u'R lies within 2e-7 R of a CDF boundary, or an accept test with
  *       |u q - p| < 1e-6 max(p, u q) -- the comparisons fp32 could get wrong
  *       ("The rule"; readings R2, R3).  At most 32 per call are redone; the rest keep the
  *       fp32 result.
@@ -292,6 +300,23 @@ sv_status spec_verify_uniforms(uint64_t seed, uint64_t offset, int B, int positi
  * Read it after the call's stream has completed.
  */
 size_t spec_verify_sample_redraw_offset(int B, int gamma, int V, sv_dtype dtype);
+
+/*
+ * Test hook: where spec_verify_tree_sample (mode SV_MODE_TREE_SAMPLE, rows = N) and
+ * spec_verify_sample_lazy (SV_MODE_SAMPLE_LAZY, rows = gamma) keep their re-walk
+ * bookkeeping inside a workspace of these sizes: the byte offset of an int32 array
+ * ((size_t)-1 for another mode or bad sizes), read after the call's stream has completed:
+ *   [0] sequences the last call marked: an accept test with |u q - p| below 1e-6 of
+ *       max(p, u q) plus the size of p's terms, a residual mass below 1e-6 (1 + A), less
+ *       than 1e-5 of q's mass left, or a final draw whose threshold lies within 3e-7 of
+ *       the draw's total mass from a CDF boundary (A: the walk's rejection coefficient;
+ *       p after r rejections is max(p0 - A q0, 0) normalised);
+ *   [3] 0 (no wait of the re-walk can time out: it meets at hardware cluster barriers);
+ *   [4] sequences re-walked (the first 8 marked);
+ *   [8 + b] 1 if sequence b was marked, else 0;
+ *   [8 + B + b] nodes of sequence b's walk recorded for the re-walk (at most 8).
+ */
+size_t spec_verify_walk_redraw_offset(sv_mode mode, int B, int rows, int V, sv_dtype dtype);
 
 /*
  * Test hook: exp(y_hi[i] + y_lo[i]) for arguments <= 0 in the double-float arithmetic of
@@ -303,13 +328,14 @@ sv_status spec_verify_exp_df(const float *y_hi, const float *y_lo, int n, float 
 /*
  * Optional timing instrumentation for the CALLING THREAD (the only state the library
  * keeps, and it is thread-local).  With events != NULL, each later call of
- * spec_verify_sample / _greedy / _tree_greedy on this thread records events[0] on its
- * stream before its first kernel and events[s] after its s-th kernel (s = 1 .. n_events-1;
- * sampling has 5 kernels: row statistics, decide, residual masses, inverse-CDF draw,
- * extended-precision re-draw of near-boundary sequences; greedy
- * and tree have 2: tile maxima, finalize).  The events are cudaEvent_t handles created
- * and owned by the caller; recording them adds no synchronisation.  Pass NULL (or 0) to
- * turn it off.  Returns SV_ERR_INVALID_ARG for n_events < 0 or > 8.
+ * spec_verify_sample / _greedy / _tree_greedy / _tree_sample / _sample_lazy on this thread
+ * records events[0] on its stream before its first kernel and events[s] after its s-th
+ * kernel (s = 1 .. n_events-1; sampling has 5 kernels: row statistics, decide, residual
+ * masses, inverse-CDF draw, extended-precision re-draw of near-boundary sequences; greedy
+ * and tree have 2: tile maxima, finalize; tree sampling and lazy sampling have 3: the
+ * walk, the re-walk's exponentials, the re-walk).  The events are cudaEvent_t handles created and owned by the
+ * caller; recording them adds no synchronisation.  Pass NULL (or 0) to turn it off.
+ * Returns SV_ERR_INVALID_ARG for n_events < 0 or > 8.
  */
 sv_status spec_verify_set_stage_events(void *const *events, int n_events);
 

@@ -75,6 +75,8 @@ def load_library() -> ctypes.CDLL:
         lib.spec_verify_greedy_noalloc.restype = i32
         lib.spec_verify_sample_redraw_offset.argtypes = [i32, i32, i32, i32]
         lib.spec_verify_sample_redraw_offset.restype = sz
+        lib.spec_verify_walk_redraw_offset.argtypes = [i32, i32, i32, i32, i32]
+        lib.spec_verify_walk_redraw_offset.restype = sz
         lib.spec_verify_exp_df.argtypes = [P, P, i32, P, P, P]
         lib.spec_verify_exp_df.restype = i32
         lib.spec_verify_set_stage_events.argtypes = [P, i32]
@@ -395,6 +397,20 @@ def sample_redraw_state(workspace: torch.Tensor, B: int, gamma: int, V: int, dty
     torch.cuda.synchronize(workspace.device)
     words = workspace.view(torch.uint8)[off:off + 16].clone().view(torch.int32).cpu()
     return int(words[0]), int(words[3])
+
+
+def walk_redraw_state(workspace: torch.Tensor, mode: int, B: int, rows: int, V: int, dtype: int):
+    """Test hook: the re-walk bookkeeping of the last tree-sampling (mode MODE_TREE_SAMPLE,
+    rows = N) or lazy sampling (MODE_SAMPLE_LAZY, rows = gamma) call that used `workspace`:
+    (sequences marked, sequences re-walked, status, per-sequence marks as a numpy array);
+    synchronises the device."""
+    lib = load_library()
+    off = lib.spec_verify_walk_redraw_offset(mode, B, rows, V, dtype)
+    if off == ctypes.c_size_t(-1).value:
+        raise ValueError("bad mode or sizes")
+    torch.cuda.synchronize(workspace.device)
+    words = workspace.view(torch.uint8)[off:off + 4 * (8 + B)].clone().view(torch.int32).cpu().numpy()
+    return int(words[0]), int(words[4]), int(words[3]), words[8:8 + B].copy()
 
 
 def spec_verify_exp_df(y_hi: torch.Tensor, y_lo: torch.Tensor):

@@ -37,6 +37,7 @@ bool vec_ok(const void *p, int64_t sb, int64_t sr, sv_dtype d) {
 struct Layout {
     size_t partial = 0, rowstat = 0, plan = 0, csum = 0;
     size_t rflag = 0, rctl = 0, rlist = 0, rsum = 0, ramb = 0;  // re-draw (sampling)
+    size_t rec = 0, et = 0, us = 0, npos = 0, um = 0, pmax = 0, pcnt = 0;  // re-walk (tree sampling; rctl, rsum too)
     size_t total = 0;
 };
 
@@ -48,6 +49,19 @@ struct Layout {
 //   csum     per (sequence, 2 KB residual tile): residual mass  (sampling only)
 //   rflag, rctl, rlist (RefineInfo records), rsum, ramb: the extended-precision re-draw of near-boundary
 //            sequences (sampling only; see sv_internal.h)
+// Tree sampling and lazy sampling: the walk's unit masses (partial) and per-CTA row
+// statistics (rowstat), then the re-walk's control block, marks and record lengths (rctl),
+// records (rec), stored exponentials and their unit sums (et, us), support counts (npos),
+// unit masses (um), per-CTA sums (rsum), maxima (pmax) and counts (pcnt); see
+// sv_internal.h.  The exponentials dominate: 16 V bytes per recorded node and listed
+// sequence.
+// Recorded positions of the tree-sampling walk: max_depth + 1 <= N (tree) or gamma + 1
+// (lazy chain), at most kTreeRecNodes.
+int rec_positions(sv_mode mode, int rows) {
+    return mode == SV_MODE_TREE_SAMPLE ? (rows < sv::kTreeRecNodes ? rows : sv::kTreeRecNodes)
+                                       : sv::tree_rec_nodes(rows);
+}
+
 Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
     Layout L;
     if (B <= 0 || V <= 0 || rows < 0 || !dtype_ok(dtype)) return L;
@@ -58,12 +72,35 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
     case SV_MODE_GREEDY: R = size_t(rows) + 1; break;
     case SV_MODE_TREE:
     case SV_MODE_ROW_STATS: R = size_t(rows); break;
-    case SV_MODE_TREE_SAMPLE:  // unit masses of the node being walked, then per-CTA row statistics
-    case SV_MODE_SAMPLE_LAZY:
+    case SV_MODE_TREE_SAMPLE:
+    case SV_MODE_SAMPLE_LAZY: {
         L.partial = 0;
-        L.rowstat = up256(size_t(B) * size_t(nrt_of(V, dtype)) * 4);
-        L.total = L.rowstat + up256(size_t(B) * sv::kTreeSampleCluster * 2 * 8);
+        size_t off = up256(size_t(B) * size_t(nrt_of(V, dtype)) * 4);
+        L.rowstat = off;
+        off += up256(size_t(B) * sv::kTreeSampleCluster * 2 * 8);
+        const size_t K = size_t(rec_positions(mode, rows));
+        const size_t nu = size_t(sv::tree_refine_units(V)), S = sv::kMaxTreeRefine, C = sv::kTreeRefineCluster;
+        L.rctl = off;
+        off += up256((size_t(sv::kTrCtlWords) + 2 * size_t(B)) * 4);
+        L.rec = off;
+        off += up256(size_t(B) * K * 16);
+        L.et = off;
+        off += up256(S * K * 2 * size_t(V) * 8);
+        L.us = off;
+        off += up256(S * K * 2 * nu * 8);
+        L.npos = off;
+        off += up256(S * K * 4);
+        L.um = off;
+        off += up256(S * nu * 8);
+        L.rsum = off;
+        off += up256(S * 2 * C * 2 * 8);
+        L.pmax = off;
+        off += up256(S * C * 2 * 4);
+        L.pcnt = off;
+        off += up256(S * C * 4);
+        L.total = off;
         return L;
+    }
     default: return L;
     }
     L.partial = 0;
@@ -101,6 +138,22 @@ sv_status check_workspace(const Layout &L, void *ws, size_t bytes) {
 char *at(void *ws, size_t off) { return static_cast<char *>(ws) + off; }
 
 sv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
+
+sv::TreeRefineWs tree_refine_ws(const Layout &L, void *ws, int B) {
+    sv::TreeRefineWs r;
+    r.ctl = reinterpret_cast<int *>(at(ws, L.rctl));
+    r.mark = r.ctl + sv::kTrCtlWords;
+    r.rlen = r.mark + B;
+    r.rec = reinterpret_cast<float4 *>(at(ws, L.rec));
+    r.et = reinterpret_cast<sv::df *>(at(ws, L.et));
+    r.us = reinterpret_cast<sv::df *>(at(ws, L.us));
+    r.npos = reinterpret_cast<int *>(at(ws, L.npos));
+    r.um = reinterpret_cast<sv::df *>(at(ws, L.um));
+    r.part = reinterpret_cast<sv::df *>(at(ws, L.rsum));
+    r.pmax = reinterpret_cast<float *>(at(ws, L.pmax));
+    r.pcnt = reinterpret_cast<int *>(at(ws, L.pcnt));
+    return r;
+}
 
 // Tile counts (and every partial index) stay below 2^31.
 bool tiles_fit(int B, int64_t R, int ntile) { return int64_t(B) * R * ntile <= kMaxGrid; }
@@ -291,15 +344,22 @@ sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_str
     const Logits d{draft_logits, d_batch_stride, d_row_stride};
     const float c = float(1.4426950408889634 / double(temperature));  // log2(e) / T
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const sv::TreeRefineWs rw = tree_refine_ws(L, workspace, B);
+    const int K = sv::tree_rec_nodes(max_depth);
     cudaError_t e = mark(0, s);
     if (e == cudaSuccess)
         e = sv::launch_tree_sample(dtype == SV_BF16, vec, t, d, B, N, V, false, parent, node_tokens, max_depth, c,
-                                   seed,
-                                   offset, without_replacement, nrt_of(V, dtype),
+                                   seed, offset, without_replacement, nrt_of(V, dtype),
                                    reinterpret_cast<float *>(at(workspace, 0)),
-                                   reinterpret_cast<float2 *>(at(workspace, L.rowstat)), accepted_len, out_tokens,
-                                   out_path, s);
+                                   reinterpret_cast<float2 *>(at(workspace, L.rowstat)), rw, K, accepted_len,
+                                   out_tokens, out_path, s);
     if (e == cudaSuccess) e = mark(1, s);
+    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, rw, s);
+    if (e == cudaSuccess) e = mark(2, s);
+    if (e == cudaSuccess)
+        e = sv::launch_tree_rewalk(dtype == SV_BF16, t, d, B, N, V, false, parent, node_tokens, max_depth, temperature,
+                                   seed, offset, without_replacement, K, rw, accepted_len, out_tokens, out_path, s);
+    if (e == cudaSuccess) e = mark(3, s);
     return cuda_status(e);
 }
 
@@ -325,13 +385,21 @@ sv_status spec_verify_sample_lazy(const void *target_logits, int64_t t_batch_str
     const Logits d{gamma > 0 ? draft_logits : target_logits, d_batch_stride, d_row_stride};
     const float c = float(1.4426950408889634 / double(temperature));  // log2(e) / T
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const sv::TreeRefineWs rw = tree_refine_ws(L, workspace, B);
+    const int K = sv::tree_rec_nodes(gamma);
     cudaError_t e = mark(0, s);
     if (e == cudaSuccess)
         e = sv::launch_tree_sample(dtype == SV_BF16, vec, t, d, B, gamma + 1, V, true, nullptr, draft_tokens, gamma,
                                    c, seed, offset, 0, nrt_of(V, dtype), reinterpret_cast<float *>(at(workspace, 0)),
-                                   reinterpret_cast<float2 *>(at(workspace, L.rowstat)), accepted_len, out_tokens,
-                                   nullptr, s);
+                                   reinterpret_cast<float2 *>(at(workspace, L.rowstat)), rw, K, accepted_len,
+                                   out_tokens, nullptr, s);
     if (e == cudaSuccess) e = mark(1, s);
+    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, rw, s);
+    if (e == cudaSuccess) e = mark(2, s);
+    if (e == cudaSuccess)
+        e = sv::launch_tree_rewalk(dtype == SV_BF16, t, d, B, gamma + 1, V, true, nullptr, draft_tokens, gamma,
+                                   temperature, seed, offset, 0, K, rw, accepted_len, out_tokens, nullptr, s);
+    if (e == cudaSuccess) e = mark(3, s);
     return cuda_status(e);
 }
 
@@ -417,6 +485,13 @@ sv_status spec_verify_row_stats(const void *logits, int64_t batch_stride, int64_
 size_t spec_verify_sample_redraw_offset(int B, int gamma, int V, sv_dtype dtype) {
     if (B <= 0 || gamma < 0 || V <= 0 || !dtype_ok(dtype)) return size_t(-1);
     return layout(SV_MODE_SAMPLE, B, gamma, V, dtype).rctl;
+}
+
+size_t spec_verify_walk_redraw_offset(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
+    if ((mode != SV_MODE_TREE_SAMPLE && mode != SV_MODE_SAMPLE_LAZY) || B <= 0 || rows < 0 || V <= 0 ||
+        !dtype_ok(dtype))
+        return size_t(-1);
+    return layout(mode, B, rows, V, dtype).rctl;
 }
 
 sv_status spec_verify_exp_df(const float *y_hi, const float *y_lo, int n, float *out_hi, float *out_lo,

@@ -333,6 +333,28 @@ struct TileWalk {
 __device__ __forceinline__ void griddep_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// All threads of a thread-block cluster of CS CTAs (CS = 1: the CTA).  The .release /
+// .acquire barrier orders the threads' memory operations at cluster scope, so what one CTA
+// wrote before it (shared or global) is seen after it by the others.
+template <int CS>
+__device__ __forceinline__ void csync() {
+    if constexpr (CS > 1) {
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    } else {
+        __syncthreads();
+    }
+}
+template <int CS>
+__device__ __forceinline__ int cluster_rank() {
+    if constexpr (CS > 1) {
+        unsigned r;
+        asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+        return int(r);
+    } else {
+        return 0;
+    }
+}
+
 // Launches `kernel` so that it may start while the previous kernel on the stream drains;
 // a cooperative launch (every CTA resident at once) when asked.
 template <class... Params, class... Args>

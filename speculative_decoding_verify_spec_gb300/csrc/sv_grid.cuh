@@ -1,0 +1,56 @@
+// sv_grid.cuh -- a bounded grid-wide barrier for the cooperative re-draw kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+namespace sv {
+
+constexpr uint64_t kBarrierLimitNs = 2000000000ull;  // give up a grid barrier after 2 s
+
+// Control words of a grid barrier inside an int32 control block.
+constexpr int kBarCount = 1, kBarGen = 2, kBarStatus = 3;
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Grid barrier for a cooperative launch (all CTAs resident).  ctl[kBarCount] must be 0
+// before the first barrier of a launch (the generation word may hold anything).  Returns
+// false, after recording SV_ERR_TIMEOUT in ctl[kBarStatus], if the other CTAs did not
+// arrive within the limit.
+__device__ inline bool grid_barrier(int *ctl) {
+    __shared__ int ok_s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        volatile int *gen = ctl + kBarGen;
+        const int g = *gen;
+        int ok = 1;
+        __threadfence();
+        if (atomicAdd(ctl + kBarCount, 1) == int(gridDim.x) - 1) {
+            atomicExch(ctl + kBarCount, 0);
+            __threadfence();
+            atomicAdd(ctl + kBarGen, 1);
+        } else {
+            const uint64_t t0 = global_ns();
+            for (uint32_t i = 0; *gen == g; ++i) {
+                if ((i & 63) == 63 && global_ns() - t0 > kBarrierLimitNs) {
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+        __threadfence();
+        if (!ok) atomicExch(ctl + kBarStatus, int(SV_ERR_TIMEOUT));
+        ok_s = ok;
+    }
+    __syncthreads();
+    return ok_s != 0;
+}
+
+}  // namespace sv

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace sv {
@@ -62,15 +63,69 @@ cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamm
                         float c, uint64_t seed, uint64_t offset, const void *partial, const void *rowstat,
                         const void *plan, const float *csum, int32_t *out_tokens, int *rflag, int *rctl,
                         RefineInfo *rinfo, int *ramb, bool early, cudaStream_t s);
+// Extended-precision re-walk of near-boundary tree-sampling sequences -----------------
+// The walk marks sequence b (mark[b] = 1, else 0, every call) when one of its fp32
+// decisions came near enough to flipping: an accept test with |u q - p| below
+// kTreeAcceptWindow x (max(p, u q) + the size of p's terms), a residual mass below
+// kTreeMassWindow x (1 + A), less than kTreeQMassWindow of q's mass left, more removed
+// tokens than it tracks, or a final draw whose threshold lies within kTreeCdfWindow x
+// (total + A) of a CDF boundary (A: the walk's coefficient; total: the draw's mass; the
+// draw's prefixes are fp64 sums of the fp32 weights, so the gap is that of the weights'
+// own rounding, measured below 7e-9 (total + A) on the workloads).  It records
+// the first kTreeRecNodes nodes it reached (rec: node, M_t, M_d, has children; rlen: how
+// many).  The re-walk redoes the first kMaxTreeRefine marked sequences in double-float
+// arithmetic.  Control block (int32, zeroed by the walk; words other than these stay 0):
+constexpr int kTrMarked = 0;  // sequences the last call marked
+constexpr int kTrRedone = 4;  // sequences redone (the first kMaxTreeRefine marked, in index order)
+constexpr int kTrCtlWords = 8;
+constexpr int kMaxTreeRefine = 8;
+constexpr int kTreeRecNodes = 8;
+constexpr float kTreeAcceptWindow = 1e-6f;
+constexpr float kTreeMassWindow = 1e-6f;
+constexpr float kTreeQMassWindow = 1e-5f;
+constexpr float kTreeCdfWindow = 4e-8f;
+constexpr int kTreeRefineCluster = 16;  // at most this many CTAs of the re-walk's cluster per sequence
+struct df;
+// Workspace of the re-walk, K = min(max_depth + 1, kTreeRecNodes) positions, nunit =
+// tree_refine_units(V):  ctl [kTrCtlWords]; mark, rlen [B]; rec [B][K] float4;
+// et [kMaxTreeRefine][K][2][V] and us [kMaxTreeRefine][K][2][nunit] double-float (the
+// exponentials of the recorded rows and their unit sums); npos [kMaxTreeRefine][K] int;
+// um [kMaxTreeRefine][nunit], part [kMaxTreeRefine][2][cluster][2] double-float; pmax
+// [kMaxTreeRefine][cluster][2] float; pcnt [kMaxTreeRefine][cluster] int.
+struct TreeRefineWs {
+    int *ctl, *mark, *rlen;
+    float4 *rec;
+    df *et, *us;
+    int *npos;
+    df *um, *part;
+    float *pmax;
+    int *pcnt;
+};
+constexpr int kTreeRefineUnit = 256;  // logits per unit of the re-walk's passes (one warp)
+__host__ __device__ inline int tree_refine_units(int V) {
+    return int((int64_t(V) + kTreeRefineUnit - 1) / kTreeRefineUnit);
+}
+inline int tree_rec_nodes(int max_depth) { return max_depth + 1 < kTreeRecNodes ? max_depth + 1 : kTreeRecNodes; }
+inline size_t tree_refine_smem(int N, int max_depth) { return size_t(13 * N + max_depth + 1) * 4; }
+// The exponentials of the listed sequences' recorded rows (every resident CTA), then the
+// re-walk (one cluster of 16 CTAs per listed sequence where the device holds one, else 8).
+cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws,
+                            cudaStream_t s);
+cudaError_t launch_tree_rewalk(int dtype, Logits t, Logits d, int B, int N, int V, bool chain, const int32_t *parent,
+                               const int32_t *node_tokens, int max_depth, float T, uint64_t seed, uint64_t offset,
+                               int without_replacement, int K, TreeRefineWs ws, int32_t *accepted_len,
+                               int32_t *out_tokens, int32_t *out_path, cudaStream_t s);
 // Token-tree sampling (multi-round rejection), one CTA per sequence reading the rows of the
 // nodes its walk reaches; with chain, the tree whose node v has parent v - 1 and token
 // node_tokens[b][v - 1] ([B][N - 1]).  c = log2(e) / T; umass: [B][nunit] floats of
-// scratch, nunit = ceil(V / res_tile_elems); cstat: [B][kTreeSampleCluster][2] float2.
+// scratch, nunit = ceil(V / res_tile_elems); cstat: [B][kTreeSampleCluster][2] float2;
+// rw, K: the re-walk's control block, marks and records (below).
 constexpr int kTreeSampleCluster = 4;  // at most this many CTAs (SMs) per sequence of the walk
 cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, bool chain,
                                const int32_t *parent, const int32_t *node_tokens, int max_depth, float c, uint64_t seed,
                                uint64_t offset, int without_replacement, int nunit, float *umass, float2 *cstat,
-                               int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path, cudaStream_t s);
+                               TreeRefineWs rw, int K, int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
+                               cudaStream_t s);
 // Lazy greedy verification, one CTA per sequence reading only the rows of accepted nodes:
 // a tree (parent[N], tokens [B][N]) or, with chain, the chain of draft tokens [B][N - 1].
 cudaError_t launch_greedy_walk(int dtype, bool vec, Logits t, int B, int N, int V, bool chain, const int32_t *parent,

@@ -27,61 +27,16 @@
 #include "spec_verify.h"
 #include "sv_device.cuh"
 #include "sv_df.cuh"
+#include "sv_grid.cuh"
 #include "sv_internal.h"
 
 namespace sv {
 namespace {
 
-constexpr uint64_t kBarrierLimitNs = 2000000000ull;  // give up a grid barrier after 2 s
-
-__device__ __forceinline__ uint64_t global_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Grid barrier for a cooperative launch (all CTAs resident).  Returns false, after
-// recording SV_ERR_TIMEOUT, if the other CTAs did not arrive within the limit.
-__device__ bool grid_barrier(int *ctl) {
-    __shared__ int ok_s;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        volatile int *gen = ctl + kRefineBarGen;
-        const int g = *gen;
-        int ok = 1;
-        __threadfence();
-        if (atomicAdd(ctl + kRefineBarCount, 1) == int(gridDim.x) - 1) {
-            atomicExch(ctl + kRefineBarCount, 0);
-            __threadfence();
-            atomicAdd(ctl + kRefineBarGen, 1);
-        } else {
-            const uint64_t t0 = global_ns();
-            for (uint32_t i = 0; *gen == g; ++i) {
-                if ((i & 63) == 63 && global_ns() - t0 > kBarrierLimitNs) {
-                    ok = 0;
-                    break;
-                }
-                __nanosleep(64);
-            }
-        }
-        __threadfence();
-        if (!ok) atomicExch(ctl + kRefineStatus, int(SV_ERR_TIMEOUT));
-        ok_s = ok;
-    }
-    __syncthreads();
-    return ok_s != 0;
-}
-
 constexpr int kRefLane = 2;             // logits per lane in a re-draw unit
 constexpr int kRefUnit = 32 * kRefLane;  // 64 logits per unit (one warp)
 constexpr int kRefBatch = 8;             // loads issued together in the per-sequence stage
 constexpr float kSignBand = 2e-6f;       // relative band around S_t / S_d left to the exact pass
-
-// exp((x - M) / T) for x <= M: x - M exactly (TwoSum), times 1/T in double-float.
-__device__ __forceinline__ df weight_df(float x, float M, df inv_t) {
-    if (!(x > -__int_as_float(0x7f800000))) return df{0.f, 0.f};  // a masked (-inf) logit
-    return exp_df(df_mul(two_sum(x, -M), inv_t));
-}
 
 // Block-wide double-float sum / inclusive scan (kThreads threads, index order = thread
 // order).  `sm` holds kWarps values.

@@ -22,8 +22,9 @@
 // logits, and the final draw walks those masses and then one unit, as the chain's draw.
 //
 // Arithmetic mirrors the chain sampler: weights 2^((x - M) c) with x - M exact, explicitly
-// rounded products, fp32 sums in a fixed order, Kahan prefixes inside the chosen unit.
+// rounded products, fp32 sums in a fixed order; the final draw's prefixes in fp64.
 #include "sv_device.cuh"
+#include "sv_df.cuh"
 #include "sv_internal.h"
 
 namespace sv {
@@ -33,27 +34,17 @@ constexpr int kTsThreads = 1024;
 constexpr int kTsWarps = kTsThreads / 32;
 constexpr int kMaxRemoved = 64;  // tokens removed from q at one node (without replacement)
 
-// All threads of the sequence's cluster (or CTA).  The .release / .acquire barrier orders
-// the threads' memory operations at cluster scope, so unit masses and statistics written
-// before it by one CTA are seen after it by the others.
-template <int CS>
-__device__ __forceinline__ void csync() {
-    if constexpr (CS > 1) {
-        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-    } else {
-        __syncthreads();
+// A running sum of fp32 terms kept as an unevaluated pair (hi, lo): TwoSum on the high
+// parts, the errors gathered in lo -- ~2^-48 relative at the lengths the draw sums.
+struct PairSum {
+    float hi = 0.f, lo = 0.f;
+    __device__ __forceinline__ void add(float x) {
+        const df s = two_sum(hi, x);
+        hi = s.hi;
+        lo = __fadd_rn(lo, s.lo);
     }
-}
-template <int CS>
-__device__ __forceinline__ int cluster_rank() {
-    if constexpr (CS > 1) {
-        unsigned r;
-        asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-        return int(r);
-    } else {
-        return 0;
-    }
-}
+    __device__ __forceinline__ df value() const { return fast_two_sum(hi, lo); }
+};
 
 __device__ __forceinline__ float tweight(float x, float M, float c) { return ex2(__fmul_rn(__fsub_rn(x, M), c)); }
 
@@ -97,8 +88,8 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     tree_sample_kernel(Logits t, Logits d, int N, int V, bool chain, const int32_t *__restrict__ parent,
                        const int32_t *__restrict__ node_tokens, int max_depth, float c, uint64_t seed,
                        uint64_t offset, int without_replacement, int nunit, float *umass, float2 *cstat,
-                       int32_t *__restrict__ accepted_len, int32_t *__restrict__ out_tokens,
-                       int32_t *__restrict__ out_path) {
+                       TreeRefineWs rw, int K, int32_t *__restrict__ accepted_len,
+                       int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_path) {
     extern __shared__ int s_int[];
     int *s_par = s_int, *s_tok = s_int + N, *s_nch = s_int + 2 * N, *s_dep = s_int + 3 * N;
     int *s_path = s_int + 4 * N;  // max_depth + 1
@@ -107,6 +98,8 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     __shared__ float2 s_stat[2][kTsWarps];
     __shared__ float s_sum[kTsWarps];
     __shared__ int s_flag;
+    __shared__ int s_near;  // a decision came near flipping in fp32: the re-walk redoes the sequence
+    __shared__ int s_nrec;  // nodes recorded for the re-walk
     __shared__ float s_tx[2];
     griddep_launch_next();
     griddep_wait();  // the caller's kernels may still be writing the inputs
@@ -120,8 +113,16 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     float *um = umass + seq * int64_t(nunit);
     constexpr int RE = res_tile_elems<D>();
 
+    if (blockIdx.x == 0) {  // the re-walk's control words and counters (it starts after this grid)
+        if (tid < kTrCtlWords) rw.ctl[tid] = 0;
+        for (int i = tid; i < kMaxTreeRefine * K; i += kTsThreads) rw.npos[i] = 0;
+    }
     // the tree and the tokens: parent[0] = -1, parent[v] in [0, v), depth <= max_depth
-    if (tid == 0) s_flag = 1;
+    if (tid == 0) {
+        s_flag = 1;
+        s_near = 0;
+        s_nrec = 0;
+    }
     __syncthreads();
     for (int v = tid; v < N; v += kTsThreads) {
         const int p = chain ? v - 1 : parent[v];
@@ -148,7 +149,11 @@ __global__ void __launch_bounds__(kTsThreads, 1)
             out[i] = -1;
             if (opath) opath[i] = -1;
         }
-        if (tid == 0) accepted_len[seq] = -1;
+        if (tid == 0) {
+            accepted_len[seq] = -1;
+            rw.mark[seq] = s_near;  // a near decision may have led to this row
+            rw.rlen[seq] = s_nrec;
+        }
     };
     if (!s_flag) {
         fail();
@@ -247,6 +252,10 @@ __global__ void __launch_bounds__(kTsThreads, 1)
             fail();
             return;
         }
+        if (rank == 0 && tid == 0 && depth < K) {  // the node and its rows' maxima, for the re-walk
+            rw.rec[seq * K + depth] = make_float4(__int_as_float(v), ts.x, st.has_q ? ds.x : 0.f, st.has_q ? 1.f : 0.f);
+            s_nrec = depth + 1;
+        }
         st.Mt = ts.x;
         st.inv_st = 1.f / ts.y;
         st.Md = ds.x;
@@ -283,13 +292,19 @@ __global__ void __launch_bounds__(kTsThreads, 1)
             const float px = wx / st.Dn;
             const float qx = removed ? 0.f : __fmul_rn(st.s, q0x);
             const float u = uniform01(seed, offset, uint32_t(seq), uint32_t(cnode - 1), 0u);
-            if (u * qx < px) {  // accepted
+            const float uq = u * qx;
+            // p's error: its own terms' rounding and D's, relative to D (both shrink with D)
+            if (tid == 0 &&
+                fabsf(uq - px) < kTreeAcceptWindow * (fmaxf(px, uq) + __fdividef(p0x + ax * q0x + px * st.A, st.Dn)))
+                s_near = 1;
+            if (uq < px) {  // accepted
                 next = cnode;
                 break;
             }
             // rejected: A grows by D s (q's current scale), x leaves q without replacement
             const float Anew = __fadd_rn(st.A, __fmul_rn(st.Dn, st.s));
             NodeState ns = st;
+            if (tid == 0 && without_replacement && !removed && st.nrem >= kMaxRemoved) s_near = 1;
             if (without_replacement && !removed && st.nrem < kMaxRemoved) {
                 if (tid == 0) {
                     s_remtok[st.nrem] = x;
@@ -298,9 +313,11 @@ __global__ void __launch_bounds__(kTsThreads, 1)
                 ns.nrem = st.nrem + 1;
                 ns.qrem = __fadd_rn(st.qrem, q0x);
                 ns.s = ns.qrem < 1.f ? 1.f / __fsub_rn(1.f, ns.qrem) : 0.f;
+                if (tid == 0 && !(ns.qrem < 1.f - kTreeQMassWindow)) s_near = 1;
             }
             __syncthreads();
             const float F = mass_pass(tp, dp, ns, Anew);
+            if (tid == 0 && !(F > kTreeMassWindow * (1.f + Anew))) s_near = 1;
             if (F > 0.f) {
                 ns.A = Anew;
                 ns.Dn = F;
@@ -323,37 +340,45 @@ __global__ void __launch_bounds__(kTsThreads, 1)
         }
         // the final token at v: from w under the current state (the last residual, or p)
         const float total = residual_ready ? last_total : mass_pass(tp, dp, st, st.A);
+        (void)total;
         if (warp == 0 && rank == 0) {
+            // The prefixes and the threshold in double-float (sums of the fp32 weights good to
+            // ~2^-48): the comparison is then limited by the weights' own rounding, not by the
+            // resolution of an fp32 running sum, and near-boundary draws are rarer.
             const float u2 = uniform01(seed, offset, uint32_t(seq), uint32_t(v), 1u);
-            const float thr = u2 * total;
             const int per = (nunit + 31) / 32;
-            float ls = 0.f;
+            PairSum lacc;
             for (int q = 0; q < per; ++q) {
                 const int uu = lane * per + q;
-                if (uu < nunit) ls += um[uu];
+                if (uu < nunit) lacc.add(um[uu]);
             }
-            const float incl = warp_inclusive_scan(ls, lane);
+            const df incl = df_warp_scan(lacc.value(), lane);
+            const df totd = df_shfl(incl, 31);
+            const df thr = df_mul_f(totd, u2);
             int unit = -1;
-            float base = 0.f;
+            df base = df{0.f, 0.f};
             bool force_last = false;
-            const unsigned crossing = __ballot_sync(0xFFFFFFFFu, incl > thr);
+            const unsigned crossing = __ballot_sync(0xFFFFFFFFu, df_gt(incl, thr));
             if (crossing) {
                 const int l = __ffs(crossing) - 1;
+                df excl = df_shfl_up(incl, 1);
+                if (lane == 0) excl = df{0.f, 0.f};
                 if (lane == l) {
-                    float run = incl - ls;
+                    df run = excl;
                     int last_in_lane = lane * per;
                     for (int q = 0; q < per && unit < 0; ++q) {
                         const int uu = lane * per + q;
                         if (uu >= nunit) break;
                         last_in_lane = uu;
-                        if (run + um[uu] > thr) unit = uu;
-                        else run += um[uu];
+                        const df nx = df_add(run, df_from(um[uu]));
+                        if (df_gt(nx, thr)) unit = uu;
+                        else run = nx;
                     }
                     if (unit < 0) unit = last_in_lane;
                     base = run;
                 }
                 unit = __shfl_sync(0xFFFFFFFFu, unit, l);
-                base = __shfl_sync(0xFFFFFFFFu, base, l);
+                base = df_shfl(base, l);
             } else {  // rounding left the threshold at or above the total: the last unit with mass
                 int lp = -1;
                 for (int q = 0; q < per; ++q) {
@@ -381,30 +406,48 @@ __global__ void __launch_bounds__(kTsThreads, 1)
                     if (s_remtok[r] == j) a = s_remcoef[r];
                 return wgt(vec_elem<D>(tv[k], e), st.A != 0.f ? vec_elem<D>(dv[k], e) : 0.f, st, a, c);
             };
-            Kahan lsum;
-#pragma unroll
-            for (int k = 0; k < kResVecs; ++k)
-#pragma unroll
-                for (int e = 0; e < D::EPV; ++e) lsum.add(w_at(k, e));
-            const float tsum = lsum.value();
-            const float lincl = warp_inclusive_scan(tsum, lane);
-            Kahan run;
-            run.add(base);
-            run.add(lincl - tsum);
-            int cand = kNoIndex, lastpos = -1;
+            PairSum lsum;
+            int lastpos = -1;
 #pragma unroll
             for (int k = 0; k < kResVecs; ++k)
 #pragma unroll
                 for (int e = 0; e < D::EPV; ++e) {
                     const int j = (lane * kResVecs + k) * D::EPV + e;
                     const float w = w_at(k, e);
-                    run.add(w);
-                    if (j < len) {
-                        if (!force_last && cand == kNoIndex && run.value() > thr) cand = j;
-                        if (w > 0.f) lastpos = j;
-                    }
+                    lsum.add(w);
+                    if (j < len && w > 0.f) lastpos = j;
                 }
-            const int first = warp_reduce(cand, [](int a, int b) { return min(a, b); });
+            const df lincl = df_warp_scan(lsum.value(), lane);
+            df lexcl = df_shfl_up(lincl, 1);
+            if (lane == 0) lexcl = df{0.f, 0.f};
+            // the lane whose run crosses thr, then its logits one per lane and a second scan
+            constexpr int NE = kResVecs * D::EPV;  // logits per lane
+            int first = kNoIndex;
+            float gap = 0.f;  // distance of thr to the chosen token's CDF boundaries
+            const unsigned lb = force_last ? 0u : __ballot_sync(0xFFFFFFFFu, df_gt(df_add(base, lincl), thr));
+            if (lb) {
+                const int l3 = __ffs(lb) - 1;
+                const int j = l3 * NE + lane;
+                float w = 0.f;
+                if (lane < NE && j < len) {
+                    float a = st.A;
+                    for (int r = 0; r < st.nrem; ++r)
+                        if (s_remtok[r] == int(u0) + j) a = s_remcoef[r];
+                    w = wgt(load_elem<D>(tp, u0 + j), st.A != 0.f ? load_elem<D>(dp, u0 + j) : 0.f, st, a, c);
+                }
+                const df start = df_add(base, df_shfl(lexcl, l3));
+                const df above = df_sub(df_add(start, df_warp_scan(df_from(w), lane)), thr);  // C_j - thr
+                const unsigned eb = __ballot_sync(0xFFFFFFFFu, lane < NE && j < len && df_pos(above));
+                if (eb) {
+                    const int le = __ffs(eb) - 1;
+                    first = l3 * NE + le;
+                    const float ah = __shfl_sync(0xFFFFFFFFu, above.hi, le);
+                    const float wl = __shfl_sync(0xFFFFFFFFu, w, le);
+                    gap = fminf(__fsub_rn(wl, ah), ah);  // thr - C_{j-1} = w - (C_j - thr)
+                }
+            }
+            if (lane == 0 && (first == kNoIndex || force_last || !(gap >= kTreeCdfWindow * (totd.hi + st.A))))
+                s_near = 1;
             lastpos = warp_reduce(lastpos, [](int a, int b) { return max(a, b); });
             int tok = first != kNoIndex ? first : lastpos;
             if (tok < 0) tok = 0;
@@ -414,6 +457,10 @@ __global__ void __launch_bounds__(kTsThreads, 1)
         break;
     }
     if (rank != 0) return;
+    if (tid == 0) {
+        rw.mark[seq] = s_near;
+        rw.rlen[seq] = s_nrec;
+    }
     // outputs: the path (root .. v), its tokens, the final token, -1 padding
     const int tok = __float_as_int(s_tx[0]);
     for (int i = tid; i < W; i += kTsThreads) {
@@ -431,8 +478,8 @@ namespace {
 template <int CS>
 cudaError_t launch_walk(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, bool chain, const int32_t *parent,
                         const int32_t *node_tokens, int max_depth, float c, uint64_t seed, uint64_t offset,
-                        int without_replacement, int nunit, float *umass, float2 *cstat, int32_t *accepted_len,
-                        int32_t *out_tokens, int32_t *out_path, cudaStream_t s) {
+                        int without_replacement, int nunit, float *umass, float2 *cstat, TreeRefineWs rw, int K,
+                        int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path, cudaStream_t s) {
     const size_t smem = size_t(4 * N + max_depth + 1) * sizeof(int);
     auto k = dtype == 1 ? (vec ? tree_sample_kernel<BF16, true, CS> : tree_sample_kernel<BF16, false, CS>)
                         : (vec ? tree_sample_kernel<F32, true, CS> : tree_sample_kernel<F32, false, CS>);
@@ -451,7 +498,7 @@ cudaError_t launch_walk(int dtype, bool vec, Logits t, Logits d, int B, int N, i
     cfg.attrs = attr;
     cfg.numAttrs = CS > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, k, t, d, N, V, chain, parent, node_tokens, max_depth, c, seed, offset,
-                              without_replacement, nunit, umass, cstat, accepted_len, out_tokens, out_path);
+                              without_replacement, nunit, umass, cstat, rw, K, accepted_len, out_tokens, out_path);
 }
 }  // namespace
 
@@ -461,7 +508,8 @@ cudaError_t launch_walk(int dtype, bool vec, Logits t, Logits d, int B, int N, i
 cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, bool chain,
                                const int32_t *parent, const int32_t *node_tokens, int max_depth, float c, uint64_t seed,
                                uint64_t offset, int without_replacement, int nunit, float *umass, float2 *cstat,
-                               int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path, cudaStream_t s) {
+                               TreeRefineWs rw, int K, int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
+                               cudaStream_t s) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -469,12 +517,12 @@ cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, i
     static_assert(kTreeSampleCluster == 4, "the statistics scratch is sized for clusters of up to 4");
     if (int64_t(B) * 4 <= sms)
         return launch_walk<4>(dtype, vec, t, d, B, N, V, chain, parent, node_tokens, max_depth, c, seed, offset,
-                              without_replacement, nunit, umass, cstat, accepted_len, out_tokens, out_path, s);
+                              without_replacement, nunit, umass, cstat, rw, K, accepted_len, out_tokens, out_path, s);
     if (int64_t(B) * 2 <= sms)
         return launch_walk<2>(dtype, vec, t, d, B, N, V, chain, parent, node_tokens, max_depth, c, seed, offset,
-                              without_replacement, nunit, umass, cstat, accepted_len, out_tokens, out_path, s);
+                              without_replacement, nunit, umass, cstat, rw, K, accepted_len, out_tokens, out_path, s);
     return launch_walk<1>(dtype, vec, t, d, B, N, V, chain, parent, node_tokens, max_depth, c, seed, offset,
-                          without_replacement, nunit, umass, cstat, accepted_len, out_tokens, out_path, s);
+                          without_replacement, nunit, umass, cstat, rw, K, accepted_len, out_tokens, out_path, s);
 }
 
 }  // namespace sv

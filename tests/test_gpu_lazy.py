@@ -11,9 +11,10 @@ import pytest
 import torch
 
 import speculative_decoding_verify_spec_gb300 as sv
+from speculative_decoding_verify_spec_gb300 import binding
 from speculative_decoding_verify_spec_gb300 import workloads as W
 
-from parity_util import compare_sample, oracle_greedy, oracle_sample, oracle_tree
+from parity_util import compare_sample, host, oracle_greedy, oracle_sample, oracle_tree, record_rates
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -119,3 +120,30 @@ def test_sample_lazy_small_and_edge_cases():
     d = s.target[:, :4].contiguous()
     acc, out = sv.spec_verify_sample_lazy(s.target, d, s.draft_tokens, 1.0, 5)
     assert (acc == 4).all()
+
+
+def test_sample_lazy_disagreements_are_below_one_in_ten_thousand():
+    """40 rounds of the B=256 workload through the lazy entry: fewer than 0.01 % of the
+    10,240 sequences disagree with the oracle; the double-float re-walk ran."""
+    s = W.make("sample_b256", device=DEV)
+    B, G1, V = s.target.shape
+    ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_SAMPLE_LAZY, B, G1 - 1, V, binding.BF16),
+                     dtype=torch.uint8, device=DEV)
+    t, d, x = host(s.target), host(s.draft), s.draft_tokens.cpu().numpy()
+    total = mism = flg = marked = 0
+    flags = []
+    for off in range(1, 41):
+        acc, out = sv.spec_verify_sample_lazy(s.target, s.draft, s.draft_tokens, s.temperature, s.seed, off,
+                                              workspace=ws)
+        m, r, status, _ = binding.walk_redraw_state(ws, binding.MODE_SAMPLE_LAZY, B, G1 - 1, V, binding.BF16)
+        assert status == 0 and r == min(m, 8)
+        marked += m
+        o = oracle_sample(t, d, x, s.temperature, s.seed, off, diagnostics=True)
+        n, mm, f, _ = compare_sample(acc, out, *o, label=f"lazy sample_b256 offset {off}")
+        total, mism, flg = total + n, mism + mm, flg + f
+        flags.append(o[2])
+    record_rates("lazy sample_b256 x40 rounds", total, mism, flg, np.concatenate(flags), redraw_marked=marked)
+    assert total == 10240
+    assert marked > 0
+    assert mism < 1e-4 * total, (mism, total)
+
