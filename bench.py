@@ -212,7 +212,6 @@ def make_call(name, inputs, dev, **ov):
     cfg.update(ov)
     mode = cfg["mode"]
     B, V = cfg["B"], cfg["V"]
-    dt = binding.BF16 if cfg["dtype"] == "bf16" else binding.FP32
     lazy = cfg.get("lazy", False)
     if mode == "ngram":
         drafts = torch.empty((B, cfg["k"]), dtype=torch.int32, device=dev)
@@ -221,6 +220,7 @@ def make_call(name, inputs, dev, **ov):
         def call(history=inputs.history, lengths=inputs.lengths):
             return sv.spec_ngram_draft(history, lengths, inputs.n, inputs.k, inputs.pad, drafts=drafts, count=count)
         return call, (count, drafts)
+    dt = binding.BF16 if cfg["dtype"] == "bf16" else binding.FP32
     if mode == "sample" and lazy:
         g = cfg["gamma"]
         ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_SAMPLE_LAZY, B, g, V, dt),
