@@ -70,6 +70,9 @@ def _bind(lib):
     lib.oracle_exact_probs_tree.argtypes = [P, P, P, P, i32, i32, dbl, i32, P]
     lib.oracle_exact_probs_tree.restype = i32
     lib.oracle_ngram_draft.argtypes = [P, i64, P, i32, i32, i32, i32, P, P]
+    lib.oracle_verify_typical.argtypes = [P, i64, i64, i32, i32, i32, i32, i32, P, dbl, dbl, dbl,
+                                          u64, u64, P, P, P, P]
+    lib.oracle_verify_typical.restype = ctypes.c_int
     lib.oracle_ngram_draft.restype = i32
     return lib
 
@@ -267,6 +270,25 @@ class Oracle:
         return prob
 
 
+    def verify_typical(self, target, draft_tokens, temperature, epsilon, delta, seed, offset=0,
+                       b0=0):
+        """Typical acceptance; returns (accepted_len[B], out_tokens[B, gamma+1], flags[B],
+        entropy[B, gamma+1] (H of each row the rule read, NaN elsewhere))."""
+        t, code, tsb, tsr = _logits(target)
+        B, G1, V = t.shape
+        gamma = G1 - 1
+        x = np.ascontiguousarray(np.asarray(draft_tokens, dtype=np.int32).reshape(B, gamma))
+        acc = np.zeros(B, np.int32)
+        out = np.zeros((B, G1), np.int32)
+        flags = np.zeros(B, np.int32)
+        H = np.zeros((B, G1), np.float64)
+        rc = self.lib.oracle_verify_typical(_ptr(t), tsb, tsr, code, B, int(b0), gamma, V, _ptr(x),
+                                            float(temperature), float(epsilon), float(delta),
+                                            int(seed), int(offset), _ptr(acc), _ptr(out), _ptr(flags),
+                                            _ptr(H))
+        assert rc == 0
+        return acc, out, flags, H
+
     def ngram_draft(self, history, lengths, n, k, pad):
         """Prompt-lookup drafts of a [B, T] int32 history with lengths[B]; returns
         (drafts [B, k] (-1 padded), counts [B])."""
@@ -321,6 +343,10 @@ def verify_tree_sample(target, draft, parent, node_tokens, max_depth, temperatur
 def exact_probs_tree(t_logits, d_logits, parent, tokens, temperature, without_replacement=False):
     return _load().exact_probs_tree(t_logits, d_logits, parent, tokens, temperature,
                                     without_replacement)
+
+
+def verify_typical(target, draft_tokens, temperature, epsilon, delta, seed, offset=0, b0=0):
+    return _load().verify_typical(target, draft_tokens, temperature, epsilon, delta, seed, offset, b0)
 
 
 def ngram_draft(history, lengths, n, k, pad):

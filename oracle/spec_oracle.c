@@ -20,6 +20,8 @@
  *         argmax at the stop row).
  *   [HB]  "Speculative Decoding: Draft Models, EAGLE, and How to Actually Use It"
  *         -- "The Algorithm" (steps 1-4 and the worked p/q example).
+ *         The "Medusa" paragraph and the closing note on typical acceptance (a
+ *         threshold scaled by the step's entropy; oracle_verify_typical).
  *   [PH]  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3"
  *         (SC'11): the Philox4x32-10 counter-based generator.
  *
@@ -827,6 +829,103 @@ done:
     free(q);
     free(r);
     return rc;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Typical acceptance [SD "Medusa" paragraph ("accepts any token whose target probability
+ * exceeds a threshold") and the closing note on typical acceptance ("a threshold that
+ * scales with the step's entropy"; not distribution-preserving)].  The pages fix neither
+ * the form nor the constants; the reading taken (R20):
+ *   p_i   = softmax(t_i / T)                                   (rows i = 0 .. gamma)
+ *   H_i   = -sum_j p_i(j) ln p_i(j)                            (0 ln 0 = 0)
+ *   tau_i = min(epsilon, delta * exp(-H_i))                    (exp(-H): 1 / perplexity)
+ *   draft x_i is accepted iff p_i(x_i) > tau_i, left to right; the first failure k ends the
+ *   prefix (k = gamma if none fails) and the token at k is drawn from p_k itself (no
+ *   residual: the rule does not preserve the target law anyway), by the inverse CDF with
+ *   u' = U(b, k, purpose 1).
+ * Rows are read as the rule needs them (0 .. k): a bad row past the stop does not count.
+ * A token outside [0, V) or a row read that is not a distribution gives -1.
+ * Outputs as oracle_verify_sample; entropy [B][gamma+1] (or NULL): H_i of the rows read,
+ * NAN elsewhere.  Flags: FLAG_ACCEPT_NEAR_THRESHOLD when |p - tau| < 1e-5 max(p, tau) in a
+ * test performed, FLAG_CDF_NEAR_BOUNDARY as for sampling.                              */
+/* ------------------------------------------------------------------------------------ */
+int oracle_verify_typical(const void *target, int64_t t_batch_stride, int64_t t_row_stride,
+                          int dtype, int B, int b0, int gamma, int V, const int32_t *draft_tokens,
+                          double T, double epsilon, double delta, uint64_t seed, uint64_t offset,
+                          int32_t *accepted_len, int32_t *out_tokens, int32_t *flags,
+                          double *entropy)
+{
+    double *l = (double *)malloc(sizeof(double) * (size_t)V);
+    double *p = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!l || !p) {
+        free(l);
+        free(p);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        int32_t *out = out_tokens + (int64_t)b * (gamma + 1);
+        const int32_t *x = draft_tokens + (int64_t)b * gamma;
+        for (int i = 0; i <= gamma; ++i) {
+            out[i] = -1;
+            if (entropy)
+                entropy[(int64_t)b * (gamma + 1) + i] = NAN;
+        }
+        accepted_len[b] = -1;
+        flags[b] = 0;
+        int ok = 1;
+        for (int i = 0; i < gamma && ok; ++i)
+            ok = x[i] >= 0 && x[i] < V;
+        if (!ok)
+            continue;
+        int k = -1;
+        for (int i = 0; i <= gamma; ++i) {
+            load_row(target, dtype, (int64_t)b * t_batch_stride + (int64_t)i * t_row_stride, V, l);
+            if (softmax_row(l, V, T, p, NULL, NULL) != 0) {
+                ok = 0;
+                break;
+            }
+            double H = 0.0;
+            for (int j = 0; j < V; ++j)
+                if (p[j] > 0.0)
+                    H -= p[j] * log(p[j]);
+            if (entropy)
+                entropy[(int64_t)b * (gamma + 1) + i] = H;
+            if (i == gamma) {
+                k = gamma;
+                break;
+            }
+            double tau = delta * exp(-H);
+            if (epsilon < tau)
+                tau = epsilon;
+            double px = p[x[i]];
+            double big = px > tau ? px : tau;
+            if (fabs(px - tau) < ACCEPT_WINDOW * big)
+                flags[b] |= FLAG_ACCEPT_NEAR_THRESHOLD;
+            if (!(px > tau)) {
+                k = i;
+                break;
+            }
+        }
+        if (!ok) {
+            flags[b] = 0;
+            continue;
+        }
+        /* p holds p_k: the final token from it */
+        double R = 0.0, margin = 0.0;
+        for (int j = 0; j < V; ++j)
+            R += p[j];
+        double u2 = oracle_uniform(seed, offset, (uint32_t)(b0 + b), (uint32_t)k, 1u);
+        int tok = inverse_cdf(p, V, R, u2, &margin);
+        if (margin < CDF_WINDOW)
+            flags[b] |= FLAG_CDF_NEAR_BOUNDARY;
+        for (int i = 0; i < k; ++i)
+            out[i] = x[i];
+        out[k] = tok;
+        accepted_len[b] = k;
+    }
+    free(l);
+    free(p);
+    return 0;
 }
 
 /* ------------------------------------------------------------------------------------ */

@@ -700,6 +700,111 @@ def pin_row_stats(orc):
     assert not valid.any()
 
 
+# --------------------------------------------------------------------------------------
+# Typical acceptance [SD "Medusa" paragraph and the note on typical acceptance: accept a
+# draft whose target probability exceeds a threshold scaled by the step's entropy].  The
+# rule's form is a reading (threshold min(epsilon, delta exp(-H)); parity of the constants
+# unpinned); these pins fix what does not depend on the constants.
+# --------------------------------------------------------------------------------------
+def _typical_case(rows, T=1.0):
+    """Target [1, len(rows), V] from logit rows; draft i = the argmax of row i (finite)."""
+    t = np.stack([np.asarray(r, np.float64) for r in rows])[None].astype(np.float32)
+    x = np.array([[int(np.argmax(r)) for r in rows[:-1]]], np.int32)
+    return t, x
+
+
+def pin_typical_entropy(orc):
+    """The entropy the rule reads is the textbook one: ln V for a uniform row, 0 for a
+    one-hot row, scipy.stats.entropy (natural log) of softmax(t / T) for random and
+    partly masked rows.  epsilon = 0 makes the threshold 0, so every row is read."""
+    V, T = 37, 0.8
+    rs = np.random.RandomState(71)
+    hot = np.full(V, -np.inf)
+    hot[5] = 0.0
+    masked = rs.randn(V) * 2
+    masked[rs.rand(V) < 0.4] = -np.inf
+    masked[3] = 1.0
+    rows = [np.zeros(V), hot, rs.randn(V) * 3, masked, rs.randn(V)]
+    t, x = _typical_case(rows, T)
+    acc, out, flags, H = orc.verify_typical(t, x, T, 0.0, 0.3, 5, 0)
+    assert acc[0] == len(rows) - 1, acc
+    want = [np.log(V), 0.0] + [stats.entropy(_softmax(t[0, i], T)) for i in range(2, len(rows))]
+    assert np.allclose(H[0], want, rtol=1e-12, atol=1e-12), (H[0], want)
+
+
+def pin_typical_threshold_closed_forms(orc):
+    """Uniform rows (p(x) = 1/V, H = ln V, threshold min(epsilon, delta / V)) and one-hot
+    rows (p(x) = 1, H = 0, threshold min(epsilon, delta)): the first draft is accepted
+    exactly on the side of each closed-form threshold; equality rejects (strict >)."""
+    V, G = 40, 3
+    uni = [np.zeros(V)] * (G + 1)
+    t, x = _typical_case(uni)
+    for eps, delta, accept in ((1.0, 0.99, True), (1.0, 1.01, False), (0.99 / V, 100.0, True),
+                               (1.01 / V, 100.0, False)):
+        acc, _, _, _ = orc.verify_typical(t, x, 1.0, eps, delta, 3, 0)
+        assert (acc[0] == G) == accept and (acc[0] == 0) == (not accept), (eps, delta, acc)
+    hot = np.full(V, -np.inf)
+    hot[7] = 2.0
+    t, x = _typical_case([hot] * (G + 1))
+    for eps, delta, want in ((1.0, 1.0, 0), (0.5, 2.0, G), (2.0, 0.999, G), (1.0, 5.0, 0)):
+        acc, out, _, _ = orc.verify_typical(t, x, 1.0, eps, delta, 3, 0)
+        assert acc[0] == want and out[0, want] == 7, (eps, delta, acc, out)
+
+
+def pin_typical_zero_threshold(orc):
+    """epsilon = 0: a draft is accepted exactly when its logit is finite, so the prefix
+    ends at the first draft the target rules out (a -inf logit)."""
+    rs = np.random.RandomState(72)
+    B, G, V = 400, 5, 23
+    t = (rs.randn(B, G + 1, V) * 2).astype(np.float32)
+    t[rs.rand(B, G + 1, V) < 0.3] = -np.inf
+    t[:, :, 0] = 0.0  # every row stays a distribution
+    x = rs.randint(0, V, (B, G)).astype(np.int32)
+    acc, out, _, _ = orc.verify_typical(t, x, 1.0, 0.0, 0.5, 9, 0)
+    for b in range(B):
+        dead = [i for i in range(G) if t[b, i, x[b, i]] == -np.inf]
+        k = dead[0] if dead else G
+        assert acc[b] == k and list(out[b, :k]) == list(x[b, :k]), (b, acc[b], k)
+        assert np.isfinite(t[b, k, out[b, k]]) and (out[b, k + 1:] == -1).all()
+
+
+def pin_typical_draw_law(orc, trials=200_000, V=5, G=2, T=0.9, alpha=1e-3):
+    """The token at the stop is drawn from p at the stop row: with every draft rejected
+    (epsilon = delta = 2) the first token's law is p_0; with every draft accepted
+    (epsilon = 0, finite rows) the bonus's law is p_gamma (chi-squared over Philox draws)."""
+    t, _ = _chi2_rows(V, G)
+    rows = np.ascontiguousarray(np.broadcast_to(t[:G + 1][None], (trials, G + 1, V)))
+    x = np.zeros((trials, G), np.int32)
+    for eps, delta, k in ((2.0, 2.0, 0), (0.0, 0.5, G)):
+        acc, out, _, _ = orc.verify_typical(rows, x, T, eps, delta, 0xBEEF, 0)
+        assert (acc == k).all(), (eps, np.unique(acc))
+        obs = np.bincount(out[:, k], minlength=V)
+        _, pv = stats.chisquare(obs, _softmax(t[k], T) * trials)
+        assert pv > alpha, (k, pv, obs / trials)
+
+
+def pin_typical_lazy_rows(orc):
+    """Rows are read up to the stop: a NaN row past it leaves the result unchanged, a NaN
+    row the rule reads, or a draft token out of range, gives -1."""
+    rs = np.random.RandomState(73)
+    G, V = 4, 30
+    t = (rs.randn(1, G + 1, V) * 2).astype(np.float32)
+    x = np.zeros((1, G), np.int32)
+    t[0, 0, 0] = -np.inf  # the first draft is ruled out: the stop is row 0
+    acc, out, _, _ = orc.verify_typical(t, x, 1.0, 0.0, 0.3, 4, 0)
+    assert acc[0] == 0
+    t2 = t.copy()
+    t2[0, 2, 5] = np.nan
+    acc2, out2, _, H2 = orc.verify_typical(t2, x, 1.0, 0.0, 0.3, 4, 0)
+    assert acc2[0] == 0 and (out2 == out).all() and np.isnan(H2[0, 1:]).all()
+    t3 = t.copy()
+    t3[0, 0, 9] = np.nan
+    acc3, out3, _, _ = orc.verify_typical(t3, x, 1.0, 0.0, 0.3, 4, 0)
+    assert acc3[0] == -1 and (out3 == -1).all()
+    acc4, _, _, _ = orc.verify_typical(t, np.full((1, G), V, np.int32), 1.0, 0.0, 0.3, 4, 0)
+    assert acc4[0] == -1
+
+
 ALL_PINS = [
     pin_philox_kat, pin_uniform_definition, pin_bruteforce_lossless, pin_chi2_sampler,
     pin_identical_rows_accept_all, pin_one_hot_equals_greedy, pin_one_hot_draft_accept_prob,
@@ -707,4 +812,6 @@ ALL_PINS = [
     pin_tree_printed_depths, pin_chain_tree_equals_greedy, pin_tree_bruteforce, pin_row_stats,
     pin_tree_sample_lossless, pin_tree_sample_chi2, pin_chain_tree_sample_equals_chain,
     pin_tree_sample_invariants, pin_ngram_worked_examples, pin_ngram_bruteforce,
+    pin_typical_entropy, pin_typical_threshold_closed_forms, pin_typical_zero_threshold,
+    pin_typical_draw_law, pin_typical_lazy_rows,
 ]

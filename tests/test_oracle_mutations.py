@@ -70,6 +70,17 @@ MUTATIONS = [
     ("ngram_no_fallback", "        if (pad && L >= 1)\n            for (; c < k; ++c)",
      "        if (0 && pad && L >= 1)\n            for (; c < k; ++c)",
      [pins.pin_ngram_worked_examples, pins.pin_ngram_bruteforce]),
+    ("typical_entropy_in_bits", "H -= p[j] * log(p[j]);", "H -= p[j] * log2(p[j]);",
+     [pins.pin_typical_entropy, pins.pin_typical_threshold_closed_forms]),
+    ("typical_entropy_sign", "double tau = delta * exp(-H);", "double tau = delta * exp(H);",
+     [pins.pin_typical_threshold_closed_forms]),
+    ("typical_threshold_max", "if (epsilon < tau)\n                tau = epsilon;",
+     "if (epsilon > tau)\n                tau = epsilon;", [pins.pin_typical_threshold_closed_forms]),
+    ("typical_accept_on_equality", "if (!(px > tau)) {", "if (!(px >= tau)) {",
+     [pins.pin_typical_threshold_closed_forms]),
+    ("typical_stop_off_by_one", "                k = i;\n                break;",
+     "                k = i + 1 > gamma ? gamma : i + 1;\n                break;",
+     [pins.pin_typical_zero_threshold, pins.pin_typical_draw_law]),
 ]
 
 
