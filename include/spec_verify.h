@@ -64,7 +64,8 @@ typedef enum {
     SV_MODE_TREE = 2,      /* spec_verify_tree_greedy: rows = N     */
     SV_MODE_ROW_STATS = 3, /* spec_verify_row_stats:   rows = rows_per_seq */
     SV_MODE_TREE_SAMPLE = 4, /* spec_verify_tree_sample: rows = N   */
-    SV_MODE_SAMPLE_LAZY = 5  /* spec_verify_sample_lazy: rows = gamma */
+    SV_MODE_SAMPLE_LAZY = 5, /* spec_verify_sample_lazy: rows = gamma */
+    SV_MODE_TYPICAL = 6      /* spec_verify_typical:     rows = gamma */
 } sv_mode;
 
 /* Limits checked on the host (SV_ERR_INVALID_ARG beyond them). */
@@ -226,6 +227,33 @@ sv_status spec_verify_tree_greedy_lazy(const void *target_logits, int64_t t_batc
                                        int32_t *out_path, void *stream);
 
 /*
+ * TYPICAL ACCEPTANCE (Medusa's relaxed rule) [SD the Medusa paragraph and the closing note
+ * on typical acceptance: accept a draft whose target probability exceeds a threshold that
+ * scales with the step's entropy; not distribution-preserving].  The pages give no form
+ * or constants; this entry takes
+ *   p_i = softmax(t_i / T),  H_i = -sum_j p_i(j) ln p_i(j),  tau_i = min(epsilon, delta e^-H_i),
+ * accepts draft x_i while p_i(x_i) > tau_i (left to right), and draws the token at the
+ * first failure k (or the bonus at k = gamma) from p_k itself by the inverse CDF with
+ * u' = U(b, k, purpose 1) as spec_verify_sample does.
+ *   target_logits  [B][gamma+1][V]  as spec_verify_sample (no draft logits are read).
+ *   draft_tokens   [B][gamma] int32 (may be NULL when gamma == 0).
+ *   temperature > 0; epsilon >= 0, delta >= 0 finite (epsilon = 0 accepts every draft the
+ *   target gives positive probability).
+ * Outputs as spec_verify_sample.  Rows are read lazily, one CTA per sequence: rows 0 .. k
+ * only; a token outside [0, V) or a row read that is not a distribution gives -1.  The
+ * accept tests are taken in fp32; a final draw whose threshold lies within 1e-6 of the row's
+ * mass from a CDF boundary is redone in double-float arithmetic (the first 8 per call, by
+ * two more kernels; spec_verify_walk_redraw_offset with SV_MODE_TYPICAL reports them).
+ * Workspace: spec_verify_workspace_size(SV_MODE_TYPICAL, B, gamma, V, dtype) bytes (~128 V
+ * bytes of re-draw scratch plus 4 bytes per 1024 logits per sequence).
+ */
+sv_status spec_verify_typical(const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride,
+                              sv_dtype dtype, int B, int gamma, int V, const int32_t *draft_tokens,
+                              float temperature, float epsilon, float delta, uint64_t seed,
+                              uint64_t offset, int32_t *accepted_len, int32_t *out_tokens,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Prompt-lookup (n-gram) drafting [MS lookup_draft; SD Exercise 4 ngram_draft]: the drafts
  * that the verification entries take, from the token history itself.
  *
@@ -302,9 +330,11 @@ sv_status spec_verify_uniforms(uint64_t seed, uint64_t offset, int B, int positi
 size_t spec_verify_sample_redraw_offset(int B, int gamma, int V, sv_dtype dtype);
 
 /*
- * Test hook: where spec_verify_tree_sample (mode SV_MODE_TREE_SAMPLE, rows = N) and
- * spec_verify_sample_lazy (SV_MODE_SAMPLE_LAZY, rows = gamma) keep their re-walk
- * bookkeeping inside a workspace of these sizes: the byte offset of an int32 array
+ * Test hook: where spec_verify_tree_sample (mode SV_MODE_TREE_SAMPLE, rows = N),
+ * spec_verify_sample_lazy (SV_MODE_SAMPLE_LAZY, rows = gamma) and spec_verify_typical
+ * (SV_MODE_TYPICAL, rows = gamma; its marks are near-boundary final draws, its record
+ * length 1) keep their re-walk / re-draw bookkeeping inside a workspace of these sizes:
+ * the byte offset of an int32 array
  * ((size_t)-1 for another mode or bad sizes), read after the call's stream has completed:
  *   [0] sequences the last call marked: an accept test with |u q - p| below 1e-6 of
  *       max(p, u q) plus the size of p's terms, a residual mass below 1e-6 (1 + A), less
@@ -328,12 +358,13 @@ sv_status spec_verify_exp_df(const float *y_hi, const float *y_lo, int n, float 
 /*
  * Optional timing instrumentation for the CALLING THREAD (the only state the library
  * keeps, and it is thread-local).  With events != NULL, each later call of
- * spec_verify_sample / _greedy / _tree_greedy / _tree_sample / _sample_lazy on this thread
+ * spec_verify_sample / _greedy / _tree_greedy / _tree_sample / _sample_lazy / _typical on this thread
  * records events[0] on its stream before its first kernel and events[s] after its s-th
  * kernel (s = 1 .. n_events-1; sampling has 5 kernels: row statistics, decide, residual
  * masses, inverse-CDF draw, extended-precision re-draw of near-boundary sequences; greedy
  * and tree have 2: tile maxima, finalize; tree sampling and lazy sampling have 3: the
- * walk, the re-walk's exponentials, the re-walk).  The events are cudaEvent_t handles created and owned by the
+ * walk, the re-walk's exponentials, the re-walk; typical acceptance has 3: the walk, the
+ * re-draw's exponentials, the re-draw).  The events are cudaEvent_t handles created and owned by the
  * caller; recording them adds no synchronisation.  Pass NULL (or 0) to turn it off.
  * Returns SV_ERR_INVALID_ARG for n_events < 0 or > 8.
  */

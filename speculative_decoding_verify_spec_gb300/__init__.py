@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     spec_ngram_draft,
     spec_verify_greedy,
     spec_verify_greedy_lazy,
+    spec_verify_typical,
     spec_verify_row_stats,
     spec_verify_sample,
     spec_verify_sample_lazy,
@@ -27,6 +28,7 @@ __all__ = [
     "spec_ngram_draft",
     "spec_verify_greedy",
     "spec_verify_greedy_lazy",
+    "spec_verify_typical",
     "spec_verify_row_stats",
     "spec_verify_sample",
     "spec_verify_sample_lazy",

@@ -17,7 +17,7 @@ import torch
 from . import _build
 
 SV_OK = 0
-MODE_SAMPLE, MODE_GREEDY, MODE_TREE, MODE_ROW_STATS, MODE_TREE_SAMPLE, MODE_SAMPLE_LAZY = 0, 1, 2, 3, 4, 5
+MODE_SAMPLE, MODE_GREEDY, MODE_TREE, MODE_ROW_STATS, MODE_TREE_SAMPLE, MODE_SAMPLE_LAZY, MODE_TYPICAL = range(7)
 FP32, BF16 = 0, 1
 
 _lock = threading.Lock()
@@ -63,6 +63,9 @@ def load_library() -> ctypes.CDLL:
         lib.spec_verify_sample_lazy.restype = i32
         lib.spec_verify_greedy_lazy.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, P, P]
         lib.spec_verify_greedy_lazy.restype = i32
+        lib.spec_verify_typical.argtypes = [P, i64, i64, i32, i32, i32, i32, P, f32, f32, f32, u64, u64, P, P, P,
+                                            sz, P]
+        lib.spec_verify_typical.restype = i32
         lib.spec_verify_tree_greedy_lazy.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, i32, P, P, P, P]
         lib.spec_verify_tree_greedy_lazy.restype = i32
         lib.spec_ngram_draft.argtypes = [P, i64, P, i32, i32, i32, i32, P, P, P]
@@ -287,6 +290,33 @@ def spec_verify_sample_lazy(target: torch.Tensor, draft: torch.Tensor, draft_tok
                                      int(offset) & (2**64 - 1), accepted_len.data_ptr(),
                                      out_tokens.data_ptr(), ws.data_ptr(), wsb, _stream(dev))
     _check(st, "spec_verify_sample_lazy")
+    return accepted_len, out_tokens
+
+
+def spec_verify_typical(target: torch.Tensor, draft_tokens: torch.Tensor, temperature: float, epsilon: float,
+                        delta: float, seed: int, offset: int = 0, *, workspace=None, accepted_len=None,
+                        out_tokens=None):
+    """Typical acceptance (threshold min(epsilon, delta exp(-H)) on the target probability);
+    returns (accepted_len [B], out_tokens [B, gamma+1]) -- spec_verify_sample's outputs."""
+    lib = load_library()
+    tsb, tsr = _logits3(target, "target")
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    dt = _dtype_code(target)
+    xptr = None
+    if gamma > 0:
+        x = _ints(draft_tokens, "draft_tokens", (B, gamma))
+        xptr = x.data_ptr()
+    dev = target.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    ws, wsb = _workspace(MODE_TYPICAL, B, gamma, V, dt, dev, workspace)
+    st = lib.spec_verify_typical(target.data_ptr(), tsb, tsr, dt, B, gamma, V, xptr, float(temperature),
+                                 float(epsilon), float(delta), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                 accepted_len.data_ptr(), out_tokens.data_ptr(), ws.data_ptr(), wsb, _stream(dev))
+    _check(st, "spec_verify_typical")
     return accepted_len, out_tokens
 
 

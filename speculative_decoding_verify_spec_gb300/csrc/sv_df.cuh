@@ -74,6 +74,18 @@ __device__ __forceinline__ df df_div(df x, df y) {
 }
 __device__ __forceinline__ df df_div_f(df x, float y) { return df_div(x, df_from(y)); }
 
+// A running sum of fp32 terms kept as an unevaluated pair (hi, lo): TwoSum on the high
+// parts, the errors gathered in lo -- ~2^-48 relative at the lengths the draws sum.
+struct PairSum {
+    float hi = 0.f, lo = 0.f;
+    __device__ __forceinline__ void add(float x) {
+        const df s = two_sum(hi, x);
+        hi = s.hi;
+        lo = __fadd_rn(lo, s.lo);
+    }
+    __device__ __forceinline__ df value() const { return fast_two_sum(hi, lo); }
+};
+
 // A running sum of double-float terms: TwoSum on the high parts, the low parts and the
 // rounding errors gathered in one float -- about 2^-48 relative for sums of a few tens of
 // terms of one sign, at half the cost of df_add.

@@ -212,6 +212,85 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// The double-float re-draw of typical acceptance's final token: CTA j takes listed sequence
+// j, whose stop row k the typical walk recorded (one position); tree_exp_kernel stored that
+// row's exponentials e(j) = exp((t_j - M) / T) and unit sums.  The token is the first j with
+// e(0) + ... + e(j) > u' x S (u' = U(b, k, purpose 1)): the unit by a warp search over the
+// unit sums, then inside the unit as the re-walk's draw does.  Only out_tokens[b][k]
+// changes (the accepted prefix was decided by the walk).
+__global__ void __launch_bounds__(kThreads)
+    typical_redraw_kernel(int B, int gamma, int V, uint64_t seed, uint64_t offset, TreeRefineWs ws,
+                          int32_t *__restrict__ out_tokens) {
+    __shared__ int s_seq[kMaxTreeRefine];
+    __shared__ unsigned s_bal[kWarps];
+    __shared__ int s_cnt[2];
+    griddep_launch_next();
+    griddep_wait();  // the exponentials of the stop rows
+    int total_marked = 0;
+    const int n = list_marked(ws.mark, B, s_seq, s_bal, s_cnt, &total_marked);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        ws.ctl[kTrMarked] = total_marked;
+        ws.ctl[kTrRedone] = n;
+    }
+    const int j = blockIdx.x;
+    if (j >= n || threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    const int64_t seq = s_seq[j];
+    const int k = __float_as_int(__ldcg(ws.rec + seq).x);  // one recorded position: the stop row
+    const int nunit = tree_refine_units(V);
+    const df *E = ws.et + int64_t(j) * 2 * V;  // slot j, position 0, target row
+    const df *U = ws.us + int64_t(j) * 2 * nunit;
+    const float u2 = uniform01(seed, offset, uint32_t(seq), uint32_t(k), 1u);
+    const df thr = df_mul_f(warp_total(U, 1, nunit, lane), u2);
+    df run;
+    bool force;
+    int u = warp_search(U, 1, nunit, df_zero(), thr, false, &run, &force, lane);
+    if (u < 0) u = 0;
+    const int64_t j0 = int64_t(u) * kTrUnit + lane * kTrLane;
+    df w[kTrLane];
+    DfSum lsum;
+    int lastpos = -1;
+#pragma unroll
+    for (int e = 0; e < kTrLane; ++e) {
+        w[e] = j0 + e < V ? ldcg_df(E + j0 + e) : df_zero();
+        if (j0 + e < V) {
+            lsum.add(w[e]);
+            if (df_pos(w[e])) lastpos = int(j0) + e;
+        }
+    }
+    lastpos = warp_reduce(lastpos, [](int a, int b) { return max(a, b); });
+    int tok = lastpos;
+    if (!force) {
+        const df incl = df_warp_scan(lsum.value(), lane);
+        df excl = df_shfl_up(incl, 1);
+        if (lane == 0) excl = df_zero();
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, df_gt(df_add(run, incl), thr));
+        if (bal) {
+            const int l = __ffs(bal) - 1;
+            int cand = -1, lpos = -1;
+            df r2 = df_add(run, excl);
+#pragma unroll
+            for (int e = 0; e < kTrLane; ++e) {
+                const df nx = df_add(r2, w[e]);
+                if (cand < 0 && df_gt(nx, thr)) cand = int(j0) + e;
+                if (df_pos(w[e])) lpos = int(j0) + e;
+                r2 = nx;
+            }
+            if (cand < 0) cand = lpos;
+            cand = __shfl_sync(0xFFFFFFFFu, cand, l);
+            if (cand >= 0) tok = cand;
+        }
+    }
+    if (tok < 0) tok = int(int64_t(u) * kTrUnit);
+    if (lane == 0) out_tokens[seq * (gamma + 1) + k] = tok;
+}
+
+cudaError_t launch_typical_redraw(int B, int gamma, int V, uint64_t seed, uint64_t offset, TreeRefineWs ws,
+                                  int32_t *out_tokens, cudaStream_t s) {
+    return launch_after(typical_redraw_kernel, unsigned(kMaxTreeRefine), kThreads, 0, s, B, gamma, V, seed, offset,
+                        ws, out_tokens);
+}
+
 // The re-walk: cluster j (CS CTAs) takes listed sequence j.
 template <class D, int CS>
 __global__ void __launch_bounds__(kRwThreads, 1)

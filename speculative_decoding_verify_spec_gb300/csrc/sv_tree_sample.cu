@@ -34,18 +34,6 @@ constexpr int kTsThreads = 1024;
 constexpr int kTsWarps = kTsThreads / 32;
 constexpr int kMaxRemoved = 64;  // tokens removed from q at one node (without replacement)
 
-// A running sum of fp32 terms kept as an unevaluated pair (hi, lo): TwoSum on the high
-// parts, the errors gathered in lo -- ~2^-48 relative at the lengths the draw sums.
-struct PairSum {
-    float hi = 0.f, lo = 0.f;
-    __device__ __forceinline__ void add(float x) {
-        const df s = two_sum(hi, x);
-        hi = s.hi;
-        lo = __fadd_rn(lo, s.lo);
-    }
-    __device__ __forceinline__ df value() const { return fast_two_sum(hi, lo); }
-};
-
 __device__ __forceinline__ float tweight(float x, float M, float c) { return ex2(__fmul_rn(__fsub_rn(x, M), c)); }
 
 // The state of the current node: its rows' statistics and the implicit (p, q).

@@ -50,6 +50,9 @@ WORKLOADS["ngram_b256"] = dict(mode="ngram", B=256, T=16384, V=128256, n=3, k=8,
 # the same inputs, verified by the lazy entries (rows read only where the rule needs them)
 for _base in ("sample_b256", "greedy_b512", "tree_b64"):
     WORKLOADS[_base + "_lazy"] = dict(WORKLOADS[_base], lazy=True, base=_base)
+# the B=256 sampling inputs under typical acceptance (target rows only; the threshold's
+# constants are workload parameters chosen for a mid-range acceptance -- the pages give none)
+WORKLOADS["typical_b256"] = dict(WORKLOADS["sample_b256"], typical=True, base="sample_b256", epsilon=0.1, delta=0.3)
 
 DESCRIPTIONS = {
     "sample_b1": "sampling verify B=1 V=1000 gamma=4 fp32 T=1.0",
@@ -64,6 +67,8 @@ DESCRIPTIONS["ngram_b256"] = ("prompt-lookup drafting B=256 histories of up to 1
                               "n=3, k=8")
 for _base in ("sample_b256", "greedy_b512", "tree_b64"):
     DESCRIPTIONS[_base + "_lazy"] = DESCRIPTIONS[_base] + ", lazy (rows read only where the rule needs them)"
+DESCRIPTIONS["typical_b256"] = ("typical acceptance B=256 V=128256 gamma=8 bf16 T=0.7, threshold "
+                                "min(0.1, 0.3 exp(-H)), the sampling workload's target rows and drafts")
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -366,6 +371,9 @@ def logical_bytes(name: str, **overrides) -> int:
         return cfg["B"] * (cfg["T"] * 4 + 4 + cfg["k"] * 4 + 4)
     s = 2 if cfg["dtype"] == "bf16" else 4
     B, V = cfg["B"], cfg["V"]
+    if cfg["mode"] == "sample" and cfg.get("typical"):  # target rows only
+        g = cfg["gamma"]
+        return B * (g + 1) * V * s + 4 * B * g + 4 * B * (g + 2)
     if cfg["mode"] == "sample":
         g = cfg["gamma"]
         return B * (2 * g + 1) * V * s + 4 * B * g + 4 * B * (g + 2)
@@ -393,7 +401,7 @@ def rows(name: str, **overrides) -> int:
     if cfg["mode"] == "ngram":
         return cfg["B"]
     if cfg["mode"] == "sample":
-        return cfg["B"] * (2 * cfg["gamma"] + 1)
+        return cfg["B"] * ((1 if cfg.get("typical") else 2) * cfg["gamma"] + 1)
     if cfg["mode"] == "greedy":
         return cfg["B"] * (cfg["gamma"] + 1)
     return cfg["B"] * cfg["N"]

@@ -770,12 +770,13 @@ def pin_typical_zero_threshold(orc):
 
 def pin_typical_draw_law(orc, trials=200_000, V=5, G=2, T=0.9, alpha=1e-3):
     """The token at the stop is drawn from p at the stop row: with every draft rejected
-    (epsilon = delta = 2) the first token's law is p_0; with every draft accepted
-    (epsilon = 0, finite rows) the bonus's law is p_gamma (chi-squared over Philox draws)."""
+    (threshold min(2, 1e30 e^-H) = 2 > any probability) the first token's law is p_0; with
+    every draft accepted (epsilon = 0, finite rows) the bonus's law is p_gamma (chi-squared
+    over Philox draws)."""
     t, _ = _chi2_rows(V, G)
     rows = np.ascontiguousarray(np.broadcast_to(t[:G + 1][None], (trials, G + 1, V)))
     x = np.zeros((trials, G), np.int32)
-    for eps, delta, k in ((2.0, 2.0, 0), (0.0, 0.5, G)):
+    for eps, delta, k in ((2.0, 1e30, 0), (0.0, 0.5, G)):
         acc, out, _, _ = orc.verify_typical(rows, x, T, eps, delta, 0xBEEF, 0)
         assert (acc == k).all(), (eps, np.unique(acc))
         obs = np.bincount(out[:, k], minlength=V)
