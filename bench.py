@@ -31,7 +31,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "sample_b256"
-SECONDARY = ["greedy_b512", "tree_b64", "tree_sample_b64", "sample_b256_lazy", "typical_b256", "greedy_b512_lazy",
+SECONDARY = ["greedy_b512", "tree_b64", "tree_sample_b64", "sample_b256_lazy", "typical_b256", "onehot_b256",
+             "greedy_b512_lazy",
              "tree_b64_lazy", "ngram_b256"]
 METRIC = "verified seqs/s"
 UNIT = "seqs/s"
@@ -40,12 +41,12 @@ DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "max_tiles_kernel",
                    "tree": "max_tiles_kernel", "tree_sample": "tree_sample_kernel",
                    "sample_lazy": "tree_sample_kernel", "greedy_lazy": "greedy_walk_kernel",
                    "tree_lazy": "greedy_walk_kernel", "ngram": "ngram_draft_kernel",
-                   "typical": "typical_walk_kernel"}
+                   "typical": "typical_walk_kernel", "onehot": "typical_walk_kernel"}
 STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
 STAGES = {"sample": ["row_stats", "decide", "residual_mass", "inverse_cdf", "redraw"],
           "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"], "tree_sample": ["walk", "rewalk_exp", "rewalk"],
           "sample_lazy": ["walk", "rewalk_exp", "rewalk"], "greedy_lazy": ["walk"], "tree_lazy": ["walk"], "ngram": ["draft"],
-          "typical": ["walk", "redraw_exp", "redraw"]}
+          "typical": ["walk", "redraw_exp", "redraw"], "onehot": ["walk", "redraw_exp", "redraw"]}
 
 
 def parse_args():
@@ -237,6 +238,19 @@ def make_call(name, inputs, dev, **ov):
                                           inputs.seed, step_counter[0], workspace=ws, accepted_len=acc,
                                           out_tokens=out)
         return call, (acc, out)
+    if mode == "sample" and cfg.get("onehot"):
+        g = cfg["gamma"]
+        ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_SAMPLE_ONEHOT, B, g, V, dt),
+                         dtype=torch.uint8, device=dev)
+        acc = torch.empty(B, dtype=torch.int32, device=dev)
+        out = torch.empty((B, g + 1), dtype=torch.int32, device=dev)
+        step_counter = [0]
+
+        def call(target=inputs.target, tokens=inputs.draft_tokens):
+            step_counter[0] += 1
+            return sv.spec_verify_sample_onehot(target, tokens, inputs.temperature, inputs.seed, step_counter[0],
+                                                workspace=ws, accepted_len=acc, out_tokens=out)
+        return call, (acc, out)
     if mode == "sample" and lazy:
         g = cfg["gamma"]
         ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_SAMPLE_LAZY, B, g, V, dt),
@@ -338,6 +352,8 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
         mode = mode + "_lazy"
     if cfg.get("typical"):
         mode = "typical"
+    if cfg.get("onehot"):
+        mode = "onehot"
     nst = len(STAGES[mode])
     if mode == "sample" and cfg["gamma"] == 0:
         nst = 5
@@ -404,7 +420,7 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
         res.update({"rows_per_s": None, "roofline": None, "mean_accepted_len": None,
                     "mean_drafts": float(outs[0].float().mean().item()),
                     "bytes_note": "every history token once; the search stops at the first chunk holding a match"})
-    if mode.endswith("_lazy") or mode == "typical":
+    if mode.endswith("_lazy") or mode in ("typical", "onehot"):
         # bytes the walks read in the last step, from its outputs: chain greedy reads rows
         # 0..k; tree greedy the rows of the accepted nodes (at least the path); chain
         # sampling the (max, sum) pass over target rows 0..k and draft rows 0..min(k, gamma-1),
@@ -415,7 +431,7 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
         if mode == "sample_lazy":
             g = cfg["gamma"]
             rows_read = ((a + 1) + torch.clamp(a + 1, max=g) + torch.where(a < g, 2, 1)).sum().item()
-        elif mode == "typical":  # target rows 0..k, then row k again for the draw
+        elif mode in ("typical", "onehot"):  # target rows 0..k, then row k again for the draw
             rows_read = (a + 2).sum().item()
         else:
             rows_read = (a + 1).sum().item()

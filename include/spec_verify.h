@@ -65,7 +65,8 @@ typedef enum {
     SV_MODE_ROW_STATS = 3, /* spec_verify_row_stats:   rows = rows_per_seq */
     SV_MODE_TREE_SAMPLE = 4, /* spec_verify_tree_sample: rows = N   */
     SV_MODE_SAMPLE_LAZY = 5, /* spec_verify_sample_lazy: rows = gamma */
-    SV_MODE_TYPICAL = 6      /* spec_verify_typical:     rows = gamma */
+    SV_MODE_TYPICAL = 6,     /* spec_verify_typical:     rows = gamma */
+    SV_MODE_SAMPLE_ONEHOT = 7 /* spec_verify_sample_onehot: rows = gamma */
 } sv_mode;
 
 /* Limits checked on the host (SV_ERR_INVALID_ARG beyond them). */
@@ -254,6 +255,26 @@ sv_status spec_verify_typical(const void *target_logits, int64_t t_batch_stride,
                               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * SAMPLING verification against a ONE-HOT draft distribution: the drafter proposed x_i
+ * with q_i(x_i) = 1 (a prompt-lookup / n-gram drafter, spec_ngram_draft).  The rule of
+ * spec_verify_sample with that q [SD "The rule"; the one-hot case of the chain]: accept x_i
+ * iff u_i < p_i(x_i) (u_i = U(b, i, purpose 0)); at the first rejection k the residual
+ * (p_k - q_k)+ is p_k without x_k, from which the final token is drawn (u' = U(b, k,
+ * purpose 1)); the bonus from p_gamma when every draft is accepted.  It equals
+ * spec_verify_sample given draft rows that are -inf except 0 at x_i, without those rows.
+ *   target_logits  [B][gamma+1][V] as spec_verify_sample; draft_tokens [B][gamma] (may be
+ *                  NULL when gamma == 0); temperature > 0 (applied to p).
+ * Outputs, errors and the lazy row reads as spec_verify_typical (one CTA per sequence,
+ * rows 0 .. k; near-boundary final draws redone in double-float).  Workspace:
+ * spec_verify_workspace_size(SV_MODE_SAMPLE_ONEHOT, B, gamma, V, dtype) bytes.
+ */
+sv_status spec_verify_sample_onehot(const void *target_logits, int64_t t_batch_stride,
+                                    int64_t t_row_stride, sv_dtype dtype, int B, int gamma, int V,
+                                    const int32_t *draft_tokens, float temperature, uint64_t seed,
+                                    uint64_t offset, int32_t *accepted_len, int32_t *out_tokens,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Prompt-lookup (n-gram) drafting [MS lookup_draft; SD Exercise 4 ngram_draft]: the drafts
  * that the verification entries take, from the token history itself.
  *
@@ -265,8 +286,8 @@ sv_status spec_verify_typical(const void *target_logits, int64_t t_batch_stride,
  * The drafts are the tokens that followed the tail's most recent earlier occurrence (a
  * start i <= len - n - 1 whose n tokens equal the tail), at most k of them; none without a
  * match (or with len < n + 1) unless padded.  Outputs: drafts [B][k] (-1 in unused slots),
- * count [B].  The drafter's q is one-hot on each draft: verify with spec_verify_greedy, or
- * with spec_verify_sample given draft rows that are -inf except at the draft token.
+ * count [B].  The drafter's q is one-hot on each draft: verify with spec_verify_greedy or
+ * spec_verify_sample_onehot.
  * No workspace; one CTA per sequence searches from the end of the history backwards.
  */
 sv_status spec_ngram_draft(const int32_t *history, int64_t stride, const int32_t *lengths, int B, int n,
@@ -331,9 +352,9 @@ size_t spec_verify_sample_redraw_offset(int B, int gamma, int V, sv_dtype dtype)
 
 /*
  * Test hook: where spec_verify_tree_sample (mode SV_MODE_TREE_SAMPLE, rows = N),
- * spec_verify_sample_lazy (SV_MODE_SAMPLE_LAZY, rows = gamma) and spec_verify_typical
- * (SV_MODE_TYPICAL, rows = gamma; its marks are near-boundary final draws, its record
- * length 1) keep their re-walk / re-draw bookkeeping inside a workspace of these sizes:
+ * spec_verify_sample_lazy (SV_MODE_SAMPLE_LAZY, rows = gamma), spec_verify_typical
+ * (SV_MODE_TYPICAL) and spec_verify_sample_onehot (SV_MODE_SAMPLE_ONEHOT; rows = gamma;
+ * their marks are near-boundary final draws, their record length 1) keep their re-walk / re-draw bookkeeping inside a workspace of these sizes:
  * the byte offset of an int32 array
  * ((size_t)-1 for another mode or bad sizes), read after the call's stream has completed:
  *   [0] sequences the last call marked: an accept test with |u q - p| below 1e-6 of
@@ -358,13 +379,14 @@ sv_status spec_verify_exp_df(const float *y_hi, const float *y_lo, int n, float 
 /*
  * Optional timing instrumentation for the CALLING THREAD (the only state the library
  * keeps, and it is thread-local).  With events != NULL, each later call of
- * spec_verify_sample / _greedy / _tree_greedy / _tree_sample / _sample_lazy / _typical on this thread
+ * spec_verify_sample / _greedy / _tree_greedy / _tree_sample / _sample_lazy / _typical /
+ * _sample_onehot on this thread
  * records events[0] on its stream before its first kernel and events[s] after its s-th
  * kernel (s = 1 .. n_events-1; sampling has 5 kernels: row statistics, decide, residual
  * masses, inverse-CDF draw, extended-precision re-draw of near-boundary sequences; greedy
  * and tree have 2: tile maxima, finalize; tree sampling and lazy sampling have 3: the
- * walk, the re-walk's exponentials, the re-walk; typical acceptance has 3: the walk, the
- * re-draw's exponentials, the re-draw).  The events are cudaEvent_t handles created and owned by the
+ * walk, the re-walk's exponentials, the re-walk; typical acceptance and one-hot sampling
+ * have 3: the walk, the re-draw's exponentials, the re-draw).  The events are cudaEvent_t handles created and owned by the
  * caller; recording them adds no synchronisation.  Pass NULL (or 0) to turn it off.
  * Returns SV_ERR_INVALID_ARG for n_events < 0 or > 8.
  */

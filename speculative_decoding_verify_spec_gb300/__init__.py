@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     spec_verify_greedy,
     spec_verify_greedy_lazy,
     spec_verify_typical,
+    spec_verify_sample_onehot,
     spec_verify_row_stats,
     spec_verify_sample,
     spec_verify_sample_lazy,
@@ -29,6 +30,7 @@ __all__ = [
     "spec_verify_greedy",
     "spec_verify_greedy_lazy",
     "spec_verify_typical",
+    "spec_verify_sample_onehot",
     "spec_verify_row_stats",
     "spec_verify_sample",
     "spec_verify_sample_lazy",

@@ -17,7 +17,8 @@ import torch
 from . import _build
 
 SV_OK = 0
-MODE_SAMPLE, MODE_GREEDY, MODE_TREE, MODE_ROW_STATS, MODE_TREE_SAMPLE, MODE_SAMPLE_LAZY, MODE_TYPICAL = range(7)
+(MODE_SAMPLE, MODE_GREEDY, MODE_TREE, MODE_ROW_STATS, MODE_TREE_SAMPLE, MODE_SAMPLE_LAZY, MODE_TYPICAL,
+ MODE_SAMPLE_ONEHOT) = range(8)
 FP32, BF16 = 0, 1
 
 _lock = threading.Lock()
@@ -66,6 +67,8 @@ def load_library() -> ctypes.CDLL:
         lib.spec_verify_typical.argtypes = [P, i64, i64, i32, i32, i32, i32, P, f32, f32, f32, u64, u64, P, P, P,
                                             sz, P]
         lib.spec_verify_typical.restype = i32
+        lib.spec_verify_sample_onehot.argtypes = [P, i64, i64, i32, i32, i32, i32, P, f32, u64, u64, P, P, P, sz, P]
+        lib.spec_verify_sample_onehot.restype = i32
         lib.spec_verify_tree_greedy_lazy.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, i32, P, P, P, P]
         lib.spec_verify_tree_greedy_lazy.restype = i32
         lib.spec_ngram_draft.argtypes = [P, i64, P, i32, i32, i32, i32, P, P, P]
@@ -317,6 +320,33 @@ def spec_verify_typical(target: torch.Tensor, draft_tokens: torch.Tensor, temper
                                  float(epsilon), float(delta), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
                                  accepted_len.data_ptr(), out_tokens.data_ptr(), ws.data_ptr(), wsb, _stream(dev))
     _check(st, "spec_verify_typical")
+    return accepted_len, out_tokens
+
+
+def spec_verify_sample_onehot(target: torch.Tensor, draft_tokens: torch.Tensor, temperature: float, seed: int,
+                              offset: int = 0, *, workspace=None, accepted_len=None, out_tokens=None):
+    """Sampling verification of drafts whose draft distribution is one-hot (a prompt-lookup
+    drafter's); returns (accepted_len [B], out_tokens [B, gamma+1]) -- spec_verify_sample's
+    outputs for draft rows that are -inf except at each draft."""
+    lib = load_library()
+    tsb, tsr = _logits3(target, "target")
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    dt = _dtype_code(target)
+    xptr = None
+    if gamma > 0:
+        x = _ints(draft_tokens, "draft_tokens", (B, gamma))
+        xptr = x.data_ptr()
+    dev = target.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    ws, wsb = _workspace(MODE_SAMPLE_ONEHOT, B, gamma, V, dt, dev, workspace)
+    st = lib.spec_verify_sample_onehot(target.data_ptr(), tsb, tsr, dt, B, gamma, V, xptr, float(temperature),
+                                       int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), accepted_len.data_ptr(),
+                                       out_tokens.data_ptr(), ws.data_ptr(), wsb, _stream(dev))
+    _check(st, "spec_verify_sample_onehot")
     return accepted_len, out_tokens
 
 

@@ -73,13 +73,15 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
     case SV_MODE_TREE:
     case SV_MODE_ROW_STATS: R = size_t(rows); break;
     case SV_MODE_TYPICAL:  // the unit masses of each stop row, then the re-draw (one position)
+    case SV_MODE_SAMPLE_ONEHOT:
     case SV_MODE_TREE_SAMPLE:
     case SV_MODE_SAMPLE_LAZY: {
         L.partial = 0;
         size_t off = up256(size_t(B) * size_t(nrt_of(V, dtype)) * 4);
         L.rowstat = off;
         off += up256(size_t(B) * sv::kTreeSampleCluster * 2 * 8);
-        const size_t K = mode == SV_MODE_TYPICAL ? 1 : size_t(rec_positions(mode, rows));
+        const size_t K =
+            (mode == SV_MODE_TYPICAL || mode == SV_MODE_SAMPLE_ONEHOT) ? 1 : size_t(rec_positions(mode, rows));
         const size_t nu = size_t(sv::tree_refine_units(V)), S = sv::kMaxTreeRefine, C = sv::kTreeRefineCluster;
         L.rctl = off;
         off += up256((size_t(sv::kTrCtlWords) + 2 * size_t(B)) * 4);
@@ -404,10 +406,15 @@ sv_status spec_verify_sample_lazy(const void *target_logits, int64_t t_batch_str
     return cuda_status(e);
 }
 
-sv_status spec_verify_typical(const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride, sv_dtype dtype,
-                              int B, int gamma, int V, const int32_t *draft_tokens, float temperature, float epsilon,
-                              float delta, uint64_t seed, uint64_t offset, int32_t *accepted_len,
-                              int32_t *out_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+// The target-only walks: typical acceptance (onehot = 0) or sampling against a one-hot q
+// (onehot = 1).  Both share the workspace layout of SV_MODE_TYPICAL.
+sv_status target_walk(int onehot, const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride,
+                      sv_dtype dtype, int B, int gamma, int V, const int32_t *draft_tokens, float temperature,
+                      float epsilon, float delta, uint64_t seed, uint64_t offset, int32_t *accepted_len,
+                      int32_t *out_tokens, void *workspace, size_t workspace_bytes, void *stream) {
     if (!dtype_ok(dtype)) return SV_ERR_UNSUPPORTED;
     if (B < 0 || gamma < 0 || gamma > SV_MAX_GAMMA || V < 1 || V > SV_MAX_VOCAB || t_batch_stride < 0 ||
         t_row_stride < 0)
@@ -417,7 +424,7 @@ sv_status spec_verify_typical(const void *target_logits, int64_t t_batch_stride,
         return SV_ERR_INVALID_ARG;
     if (B == 0) return SV_OK;
     if (!target_logits || !accepted_len || !out_tokens || (gamma > 0 && !draft_tokens)) return SV_ERR_INVALID_ARG;
-    const Layout L = layout(SV_MODE_TYPICAL, B, gamma, V, dtype);
+    const Layout L = layout(onehot ? SV_MODE_SAMPLE_ONEHOT : SV_MODE_TYPICAL, B, gamma, V, dtype);
     if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
     const sv::TreeRefineWs rw = tree_refine_ws(L, workspace, B);
     const bool vec = vec_ok(target_logits, t_batch_stride, t_row_stride, dtype);
@@ -427,16 +434,34 @@ sv_status spec_verify_typical(const void *target_logits, int64_t t_batch_stride,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = mark(0, s);
     if (e == cudaSuccess)
-        e = sv::launch_typical(dtype == SV_BF16, vec, t, B, gamma, V, draft_tokens, c, c_lo, epsilon, delta, seed,
-                               offset,
-                               nrt_of(V, dtype), reinterpret_cast<float *>(at(workspace, L.partial)), rw, accepted_len,
-                               out_tokens, s);
+        e = sv::launch_typical(dtype == SV_BF16, vec, t, B, gamma, V, draft_tokens, c, c_lo, onehot, epsilon, delta,
+                               seed, offset, nrt_of(V, dtype), reinterpret_cast<float *>(at(workspace, L.partial)), rw,
+                               accepted_len, out_tokens, s);
     if (e == cudaSuccess) e = mark(1, s);
     if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, t, B, V, temperature, 1, rw, s);
     if (e == cudaSuccess) e = mark(2, s);
     if (e == cudaSuccess) e = sv::launch_typical_redraw(B, gamma, V, seed, offset, rw, out_tokens, s);
     if (e == cudaSuccess) e = mark(3, s);
     return cuda_status(e);
+}
+}  // namespace
+
+extern "C" {
+
+sv_status spec_verify_typical(const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride, sv_dtype dtype,
+                              int B, int gamma, int V, const int32_t *draft_tokens, float temperature, float epsilon,
+                              float delta, uint64_t seed, uint64_t offset, int32_t *accepted_len,
+                              int32_t *out_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+    return target_walk(0, target_logits, t_batch_stride, t_row_stride, dtype, B, gamma, V, draft_tokens, temperature,
+                       epsilon, delta, seed, offset, accepted_len, out_tokens, workspace, workspace_bytes, stream);
+}
+
+sv_status spec_verify_sample_onehot(const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride,
+                                    sv_dtype dtype, int B, int gamma, int V, const int32_t *draft_tokens,
+                                    float temperature, uint64_t seed, uint64_t offset, int32_t *accepted_len,
+                                    int32_t *out_tokens, void *workspace, size_t workspace_bytes, void *stream) {
+    return target_walk(1, target_logits, t_batch_stride, t_row_stride, dtype, B, gamma, V, draft_tokens, temperature,
+                       0.f, 0.f, seed, offset, accepted_len, out_tokens, workspace, workspace_bytes, stream);
 }
 
 sv_status spec_verify_greedy_lazy(const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride,
@@ -524,7 +549,8 @@ size_t spec_verify_sample_redraw_offset(int B, int gamma, int V, sv_dtype dtype)
 }
 
 size_t spec_verify_walk_redraw_offset(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
-    if ((mode != SV_MODE_TREE_SAMPLE && mode != SV_MODE_SAMPLE_LAZY && mode != SV_MODE_TYPICAL) || B <= 0 ||
+    if ((mode != SV_MODE_TREE_SAMPLE && mode != SV_MODE_SAMPLE_LAZY && mode != SV_MODE_TYPICAL &&
+         mode != SV_MODE_SAMPLE_ONEHOT) || B <= 0 ||
         rows < 0 || V <= 0 ||
         !dtype_ok(dtype))
         return size_t(-1);

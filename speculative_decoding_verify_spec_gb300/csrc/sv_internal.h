@@ -131,12 +131,14 @@ cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, i
 cudaError_t launch_greedy_walk(int dtype, bool vec, Logits t, int B, int N, int V, bool chain, const int32_t *parent,
                                const int32_t *tokens, int max_depth, int32_t *accepted_len, int32_t *out_tokens,
                                int32_t *out_path, cudaStream_t s);
-// Typical acceptance, one CTA per sequence reading target rows 0 .. stop: tokens [B][gamma],
+// Typical acceptance (onehot = 0) or sampling verification against a one-hot q (onehot =
+// 1), one CTA per sequence reading target rows 0 .. stop: tokens [B][gamma],
 // c + c_lo = log2(e) / T (the low part for the draw's weights); umass: [B][nunit] floats of
 // scratch, nunit = ceil(V / res_tile_elems).
 cudaError_t launch_typical(int dtype, bool vec, Logits t, int B, int gamma, int V, const int32_t *tokens, float c,
-                           float c_lo, float epsilon, float delta, uint64_t seed, uint64_t offset, int nunit, float *umass,
-                           TreeRefineWs rw, int32_t *accepted_len, int32_t *out_tokens, cudaStream_t s);
+                           float c_lo, int onehot, float epsilon, float delta, uint64_t seed, uint64_t offset,
+                           int nunit, float *umass, TreeRefineWs rw, int32_t *accepted_len, int32_t *out_tokens,
+                           cudaStream_t s);
 // The double-float re-draw of the typical walk's marked final tokens (one recorded position
 // per sequence: the stop row), after launch_tree_exp with K = 1.
 cudaError_t launch_typical_redraw(int B, int gamma, int V, uint64_t seed, uint64_t offset, TreeRefineWs ws,

@@ -111,15 +111,21 @@ __device__ df exp_unit(const char *row, float M, df inv_t, int V, int u, df *E, 
 // lane's own run).  *run_out = the prefix before i.  With no crossing (rounding left thr
 // at or above the sum) or `force` set: the last i with a positive value, *force_out = true
 // (-1 if every value is 0).  Every lane returns the same.
+// Entry ex_i (if >= 0) is read as vals[ex_i] - ex_v (a unit sum without one excluded term).
+__device__ __forceinline__ df entry(const df *vals, int stride, int i, int ex_i, df ex_v) {
+    const df v = ldcg_df(vals + int64_t(i) * stride);
+    return i == ex_i ? df_sub(v, ex_v) : v;
+}
+
 __device__ int warp_search(const df *vals, int stride, int n, df base, df thr, bool force, df *run_out,
-                           bool *force_out, int lane) {
+                           bool *force_out, int lane, int ex_i = -1, df ex_v = df{0.f, 0.f}) {
     const int per = (n + 31) / 32;
     df ls = df_zero();
     int lastpos = -1;
     for (int q = 0; q < per; ++q) {
         const int i = lane * per + q;
         if (i < n) {
-            const df v = ldcg_df(vals + int64_t(i) * stride);
+            const df v = entry(vals, stride, i, ex_i, ex_v);
             ls = df_add(ls, v);
             if (df_pos(v)) lastpos = i;
         }
@@ -137,7 +143,7 @@ __device__ int warp_search(const df *vals, int stride, int n, df base, df thr, b
                 for (int q = 0; q < per; ++q) {
                     const int i = lane * per + q;
                     if (i >= n) break;
-                    const df nx = df_add(run, ldcg_df(vals + int64_t(i) * stride));
+                    const df nx = df_add(run, entry(vals, stride, i, ex_i, ex_v));
                     if (df_gt(nx, thr)) {
                         found = i;
                         break;
@@ -160,12 +166,12 @@ __device__ int warp_search(const df *vals, int stride, int n, df base, df thr, b
 }
 
 // The sum of n values in warp_search's order (every lane returns it).
-__device__ df warp_total(const df *vals, int stride, int n, int lane) {
+__device__ df warp_total(const df *vals, int stride, int n, int lane, int ex_i = -1, df ex_v = df{0.f, 0.f}) {
     const int per = (n + 31) / 32;
     df ls = df_zero();
     for (int q = 0; q < per; ++q) {
         const int i = lane * per + q;
-        if (i < n) ls = df_add(ls, ldcg_df(vals + int64_t(i) * stride));
+        if (i < n) ls = df_add(ls, entry(vals, stride, i, ex_i, ex_v));
     }
     return df_shfl(df_warp_scan(ls, lane), 31);
 }
@@ -212,12 +218,13 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
-// The double-float re-draw of typical acceptance's final token: CTA j takes listed sequence
-// j, whose stop row k the typical walk recorded (one position); tree_exp_kernel stored that
+// The double-float re-draw of the target-only walk's final token (typical acceptance, or
+// one-hot q): CTA j takes listed sequence j, whose stop row k the walk recorded (one
+// position, with the token a one-hot q's residual excludes); tree_exp_kernel stored that
 // row's exponentials e(j) = exp((t_j - M) / T) and unit sums.  The token is the first j with
-// e(0) + ... + e(j) > u' x S (u' = U(b, k, purpose 1)): the unit by a warp search over the
-// unit sums, then inside the unit as the re-walk's draw does.  Only out_tokens[b][k]
-// changes (the accepted prefix was decided by the walk).
+// e(0) + ... + e(j) > u' x S over the included logits (u' = U(b, k, purpose 1)): the unit by
+// a warp search over the unit sums, then inside the unit as the re-walk's draw does.  Only
+// out_tokens[b][k] changes (the accepted prefix was decided by the walk).
 __global__ void __launch_bounds__(kThreads)
     typical_redraw_kernel(int B, int gamma, int V, uint64_t seed, uint64_t offset, TreeRefineWs ws,
                           int32_t *__restrict__ out_tokens) {
@@ -236,15 +243,19 @@ __global__ void __launch_bounds__(kThreads)
     if (j >= n || threadIdx.x >= 32) return;
     const int lane = threadIdx.x;
     const int64_t seq = s_seq[j];
-    const int k = __float_as_int(__ldcg(ws.rec + seq).x);  // one recorded position: the stop row
+    const float4 rec = __ldcg(ws.rec + seq);  // one recorded position: the stop row
+    const int k = __float_as_int(rec.x);
+    const int xk = __float_as_int(rec.z);  // a token the draw excludes (one-hot q), else -1
     const int nunit = tree_refine_units(V);
     const df *E = ws.et + int64_t(j) * 2 * V;  // slot j, position 0, target row
     const df *U = ws.us + int64_t(j) * 2 * nunit;
+    const int ex_u = xk >= 0 ? xk / kTrUnit : -1;
+    const df ex_v = xk >= 0 ? ldcg_df(E + xk) : df_zero();
     const float u2 = uniform01(seed, offset, uint32_t(seq), uint32_t(k), 1u);
-    const df thr = df_mul_f(warp_total(U, 1, nunit, lane), u2);
+    const df thr = df_mul_f(warp_total(U, 1, nunit, lane, ex_u, ex_v), u2);
     df run;
     bool force;
-    int u = warp_search(U, 1, nunit, df_zero(), thr, false, &run, &force, lane);
+    int u = warp_search(U, 1, nunit, df_zero(), thr, false, &run, &force, lane, ex_u, ex_v);
     if (u < 0) u = 0;
     const int64_t j0 = int64_t(u) * kTrUnit + lane * kTrLane;
     df w[kTrLane];
@@ -252,7 +263,7 @@ __global__ void __launch_bounds__(kThreads)
     int lastpos = -1;
 #pragma unroll
     for (int e = 0; e < kTrLane; ++e) {
-        w[e] = j0 + e < V ? ldcg_df(E + j0 + e) : df_zero();
+        w[e] = (j0 + e < V && j0 + e != xk) ? ldcg_df(E + j0 + e) : df_zero();
         if (j0 + e < V) {
             lsum.add(w[e]);
             if (df_pos(w[e])) lastpos = int(j0) + e;

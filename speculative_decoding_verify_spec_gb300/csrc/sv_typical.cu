@@ -1,4 +1,6 @@
-// sv_typical.cu -- typical acceptance (Medusa's relaxed rule), lazily, one CTA per sequence.
+// sv_typical.cu -- verification rules that read target rows only, lazily, one CTA per
+// sequence: typical acceptance (Medusa's relaxed rule) and sampling verification against a
+// one-hot draft distribution (the prompt-lookup drafter's q).
 //
 // Method ("7.6 Speculative Decoding: Draft Models, Medusa, EAGLE & Lookahead", the Medusa
 // paragraph and the closing note on typical acceptance): a draft token is accepted when its
@@ -6,6 +8,11 @@
 // does not preserve the target law.  The form taken (the pages give no constants):
 // tau_i = min(epsilon, delta exp(-H(p_i))) with p_i = softmax(t_i / T); the first draft with
 // p_i(x_i) <= tau_i ends the prefix and the token at the stop is drawn from p itself.
+//
+// With a one-hot q (q_i(x_i) = 1) the chain rule of "The rule" becomes: accept x_i iff
+// u_i < p_i(x_i) (u_i = U(b, i, purpose 0)); at the first rejection k the residual
+// (p_k - q_k)+ is p_k with x_k removed, so the final token is drawn from p_k without x_k;
+// the bonus at k = gamma from p_gamma.  No draft logits exist or are read.
 //
 // The rule needs rows 0 .. k only.  Per row read, one pass gives (M, S, Z): the maximum,
 // S = sum 2^a and Z = sum 2^a a with a = (x - M) log2(e) / T, merged across units with the
@@ -62,8 +69,8 @@ __device__ __forceinline__ Stat3 merge3(const Stat3 &a, const Stat3 &b, float c)
 template <class D, bool VEC>
 __global__ void __launch_bounds__(kTyThreads, 1)
     typical_walk_kernel(Logits t, int gamma, int V, const int32_t *__restrict__ tokens, float c, float c_lo,
-                        float epsilon,
-                        float delta, uint64_t seed, uint64_t offset, int nunit, float *umass, TreeRefineWs rw,
+                        int onehot, float epsilon, float delta, uint64_t seed, uint64_t offset, int nunit,
+                        float *umass, TreeRefineWs rw,
                         int32_t *__restrict__ accepted_len, int32_t *__restrict__ out_tokens) {
     __shared__ Stat3 s_st[kTyWarps];
     __shared__ Stat3 s_row;
@@ -157,13 +164,20 @@ __global__ void __launch_bounds__(kTyThreads, 1)
         }
         if (i == gamma) break;
         const float px = __fdiv_rn(ex2(__fmul_rn(__fsub_rn(load_elem<D>(row, x[i]), st.M), c)), st.S);
-        const float H = __fsub_rn(logf(st.S), __fdiv_rn(0.69314718f * st.Z, st.S));
-        const float tau = fminf(epsilon, delta * expf(-H));
-        if (!(px > tau)) {
+        bool accept;
+        if (onehot) {  // u q(x) < p(x) with q(x) = 1
+            accept = uniform01(seed, offset, uint32_t(seq), uint32_t(i), 0u) < px;
+        } else {
+            const float H = __fsub_rn(logf(st.S), __fdiv_rn(0.69314718f * st.Z, st.S));
+            accept = px > fminf(epsilon, delta * expf(-H));
+        }
+        if (!accept) {
             k = i;
             break;
         }
     }
+    // one-hot q after a rejection: the residual is p_k without the rejected token
+    const int xk = (onehot && k < gamma) ? x[k] : -1;
 
     // the final token from p_k: unit masses, then the draw
     const char *row = row_ptr(t, D::kBytes, seq, k);
@@ -181,8 +195,10 @@ __global__ void __launch_bounds__(kTyThreads, 1)
 #pragma unroll
         for (int q = 0; q < kResVecs; ++q)
 #pragma unroll
-            for (int e = 0; e < D::EPV; ++e)
-                acc += pweight(vec_elem<D>(v[q], e), st.M, c, c_lo, inv_s);
+            for (int e = 0; e < D::EPV; ++e) {
+                const int j = int(u0) + (lane + 32 * q) * D::EPV + e;
+                acc += j == xk ? 0.f : pweight(vec_elem<D>(v[q], e), st.M, c, c_lo, inv_s);
+            }
         acc = warp_reduce(acc, [](float a, float b) { return a + b; });
         if (lane == 0) um[u] = acc;
     }
@@ -244,7 +260,7 @@ __global__ void __launch_bounds__(kTyThreads, 1)
             const uint4 vv = e0 < len ? load_vec<D, VEC>(row, u0, e0, len) : neg_inf_vec<D>();
 #pragma unroll
             for (int e = 0; e < D::EPV; ++e) {
-                const float w = pweight(vec_elem<D>(vv, e), st.M, c, c_lo, inv_s);
+                const float w = int(u0) + e0 + e == xk ? 0.f : pweight(vec_elem<D>(vv, e), st.M, c, c_lo, inv_s);
                 lsum.add(w);
                 if (e0 + e < len && w > 0.f) lastpos = e0 + e;
             }
@@ -258,7 +274,7 @@ __global__ void __launch_bounds__(kTyThreads, 1)
         if (lb) {
             const int l3 = __ffs(lb) - 1;
             const int j = l3 * NE + lane;
-            const float w = (lane < NE && j < len)
+            const float w = (lane < NE && j < len && int(u0) + j != xk)
                                 ? pweight(load_elem<D>(row, u0 + j), st.M, c, c_lo, inv_s)
                                 : 0.f;
             const df start = df_add(base, df_shfl(lexcl, l3));
@@ -286,16 +302,18 @@ __global__ void __launch_bounds__(kTyThreads, 1)
         accepted_len[seq] = k;
         rw.mark[seq] = s_near;
         rw.rlen[seq] = 1;  // the stop row and its maximum, for the re-draw
-        rw.rec[seq] = make_float4(__int_as_float(k), st.M, 0.f, 0.f);
+        rw.rec[seq] = make_float4(__int_as_float(k), st.M, __int_as_float(xk), 0.f);  // .z: the excluded token
     }
 }
 
 cudaError_t launch_typical(int dtype, bool vec, Logits t, int B, int gamma, int V, const int32_t *tokens, float c,
-                           float c_lo, float epsilon, float delta, uint64_t seed, uint64_t offset, int nunit, float *umass,
-                           TreeRefineWs rw, int32_t *accepted_len, int32_t *out_tokens, cudaStream_t s) {
+                           float c_lo, int onehot, float epsilon, float delta, uint64_t seed, uint64_t offset,
+                           int nunit, float *umass, TreeRefineWs rw, int32_t *accepted_len, int32_t *out_tokens,
+                           cudaStream_t s) {
     auto k = dtype == 1 ? (vec ? typical_walk_kernel<BF16, true> : typical_walk_kernel<BF16, false>)
                         : (vec ? typical_walk_kernel<F32, true> : typical_walk_kernel<F32, false>);
-    return launch_after(k, unsigned(B), kTyThreads, 0, s, t, gamma, V, tokens, c, c_lo, epsilon, delta, seed, offset,
+    return launch_after(k, unsigned(B), kTyThreads, 0, s, t, gamma, V, tokens, c, c_lo, onehot, epsilon, delta, seed,
+                        offset,
                         nunit, umass, rw, accepted_len, out_tokens);
 }
 

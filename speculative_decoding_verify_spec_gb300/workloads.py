@@ -53,6 +53,8 @@ for _base in ("sample_b256", "greedy_b512", "tree_b64"):
 # the B=256 sampling inputs under typical acceptance (target rows only; the threshold's
 # constants are workload parameters chosen for a mid-range acceptance -- the pages give none)
 WORKLOADS["typical_b256"] = dict(WORKLOADS["sample_b256"], typical=True, base="sample_b256", epsilon=0.1, delta=0.3)
+# ... and verified by sampling against a one-hot q (a prompt-lookup drafter's): target rows only
+WORKLOADS["onehot_b256"] = dict(WORKLOADS["sample_b256"], onehot=True, base="sample_b256")
 
 DESCRIPTIONS = {
     "sample_b1": "sampling verify B=1 V=1000 gamma=4 fp32 T=1.0",
@@ -69,6 +71,8 @@ for _base in ("sample_b256", "greedy_b512", "tree_b64"):
     DESCRIPTIONS[_base + "_lazy"] = DESCRIPTIONS[_base] + ", lazy (rows read only where the rule needs them)"
 DESCRIPTIONS["typical_b256"] = ("typical acceptance B=256 V=128256 gamma=8 bf16 T=0.7, threshold "
                                 "min(0.1, 0.3 exp(-H)), the sampling workload's target rows and drafts")
+DESCRIPTIONS["onehot_b256"] = ("sampling verify against a one-hot q B=256 V=128256 gamma=8 bf16 T=0.7, "
+                               "the sampling workload's target rows and drafts")
 
 
 def _gen(seed: int, device) -> torch.Generator:
@@ -371,7 +375,7 @@ def logical_bytes(name: str, **overrides) -> int:
         return cfg["B"] * (cfg["T"] * 4 + 4 + cfg["k"] * 4 + 4)
     s = 2 if cfg["dtype"] == "bf16" else 4
     B, V = cfg["B"], cfg["V"]
-    if cfg["mode"] == "sample" and cfg.get("typical"):  # target rows only
+    if cfg["mode"] == "sample" and (cfg.get("typical") or cfg.get("onehot")):  # target rows only
         g = cfg["gamma"]
         return B * (g + 1) * V * s + 4 * B * g + 4 * B * (g + 2)
     if cfg["mode"] == "sample":
@@ -401,7 +405,7 @@ def rows(name: str, **overrides) -> int:
     if cfg["mode"] == "ngram":
         return cfg["B"]
     if cfg["mode"] == "sample":
-        return cfg["B"] * ((1 if cfg.get("typical") else 2) * cfg["gamma"] + 1)
+        return cfg["B"] * ((1 if cfg.get("typical") or cfg.get("onehot") else 2) * cfg["gamma"] + 1)
     if cfg["mode"] == "greedy":
         return cfg["B"] * (cfg["gamma"] + 1)
     return cfg["B"] * cfg["N"]

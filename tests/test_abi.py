@@ -63,7 +63,10 @@ def test_workspace_sizes(lib):
     assert ws(1, 512, 6, 152064, 1) >= 512 * 7 * 75 * 8
     assert ws(2, 64, 64, 128256, 1) >= 64 * 64 * 63 * 8
     assert ws(0, 0, 8, 1000, 0) == 0
-    assert ws(7, 1, 1, 1, 0) == 0
+    assert ws(8, 1, 1, 1, 0) == 0  # an unknown mode
+    # typical acceptance / one-hot sampling: 4 bytes per residual unit per sequence, plus the
+    # double-float re-draw scratch (the stop rows' exponentials: 8 slots x 2 rows x V x 8 B)
+    assert ws(6, 256, 8, 128256, 1) == ws(7, 256, 8, 128256, 1) >= 256 * 126 * 4 + 8 * 2 * 128256 * 8
 
 
 P = ctypes.c_void_p
