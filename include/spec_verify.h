@@ -341,7 +341,8 @@ sv_status spec_verify_uniforms(uint64_t seed, uint64_t offset, int B, int positi
  * Test hook: where spec_verify_sample keeps its re-draw bookkeeping inside a sampling
  * workspace of these sizes (byte offset of an int32 array, (size_t)-1 for bad sizes).
  *   [0] sequences the last call marked for the extended-precision re-draw: a draw whose
- *       threshold u'R lies within 2e-7 R of a CDF boundary, or an accept test with
+ *       threshold u'R lies within 2e-7 R (a bonus draw) or 6e-8 R (a residual draw) of a
+ *       CDF boundary, or an accept test with
  *       |u q - p| < 1e-6 max(p, u q) -- the comparisons fp32 could get wrong
  *       ("The rule"; readings R2, R3).  At most 32 per call are redone; the rest keep the
  *       fp32 result.

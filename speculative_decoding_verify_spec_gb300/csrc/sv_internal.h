@@ -33,7 +33,11 @@ constexpr int kRefineCtlWords = 8;
 constexpr int kMaxRefine = 32;
 constexpr int kRefineDraw = 1, kRefineAccept = 2;
 constexpr float kRefineAcceptWindow = 1e-6f;
-constexpr float kRefineCdfWindow = 2e-7f;  // 2.6x the largest fp32 CDF error measured (7.7e-8 of R)
+// Draw prefixes are double-float, so the gap is limited by the unit masses' own fp32 error:
+// a bonus draw's units are row-statistics tiles rescaled by one exponential each (~1e-7 of a
+// tile's mass, the same for every logit of it), a residual draw's are direct sums.
+constexpr float kRefineCdfWindow = 2e-7f;      // bonus draw from p (mode 0)
+constexpr float kRefineCdfWindowRes = 6e-8f;   // residual draw (mode 1)
 // What draw records about a listed sequence (the re-draw's first read).
 struct RefineInfo {
     int seq, flag, k, mode;  // plan (k, mode) as decided in fp32

@@ -21,6 +21,7 @@
 //                   the tiles of p for a bonus draw), then an in-order scan inside the chosen
 //                   unit held in registers; the first j with C_j > u' R.
 #include "sv_device.cuh"
+#include "sv_df.cuh"
 #include "sv_internal.h"
 
 namespace sv {
@@ -332,59 +333,64 @@ __global__ void __launch_bounds__(128)
         return p.y * weight(p.x, st.x, c);  // mass of tile u under 2^((l - M) c)
     };
 
-    // this lane's first kKeep unit masses stay in registers for the walk below
+    // this lane's first kKeep unit masses stay in registers for the walk below.  The prefixes
+    // and the threshold are double-float (pair sums of the fp32 masses): the comparison is
+    // then limited by the weights' own rounding, not by an fp32 running sum's resolution.
     constexpr int kKeep = 8;
     float keep[kKeep];
-    float total = 0.f, lane_sum = 0.f;
+    df totd = df{0.f, 0.f}, incl = df{0.f, 0.f};
     int units = 0, per_lane = 0;
     for (int pass = 0; pass < 2; ++pass) {
         units = mode ? nrt : ntile;
         per_lane = (units + 31) / 32;
-        lane_sum = 0.f;
+        PairSum lacc;
 #pragma unroll
         for (int q = 0; q < kKeep; ++q) {
             const int u = lane * per_lane + q;
             keep[q] = (q < per_lane && u < units) ? unit_mass(u) : 0.f;
         }
 #pragma unroll
-        for (int q = 0; q < kKeep; ++q) lane_sum += keep[q];
+        for (int q = 0; q < kKeep; ++q) lacc.add(keep[q]);
         for (int q = kKeep; q < per_lane; ++q) {
             const int u = lane * per_lane + q;
-            if (u < units) lane_sum += unit_mass(u);
+            if (u < units) lacc.add(unit_mass(u));
         }
-        total = __shfl_sync(0xFFFFFFFFu, warp_inclusive_scan(lane_sum, lane), 31);
-        if (mode == 1 && !(total > 0.f)) mode = 0;  // exact-zero residual: draw from p
+        incl = df_warp_scan(lacc.value(), lane);
+        totd = df_shfl(incl, 31);
+        if (mode == 1 && !(totd.hi > 0.f)) mode = 0;  // exact-zero residual: draw from p
         else break;
     }
-    const float thr = u1 * total;
-    const float incl = warp_inclusive_scan(lane_sum, lane);
+    const df thr = df_mul_f(totd, u1);
 
     // the unit holding the threshold: the first lane whose range crosses it, then inside it
     int unit = -1;
-    float base = 0.f;
+    df base = df{0.f, 0.f};
     bool force_last = false, unit_fallback = false;
-    const unsigned crossing = __ballot_sync(0xFFFFFFFFu, incl > thr);
+    const unsigned crossing = __ballot_sync(0xFFFFFFFFu, df_gt(incl, thr));
     if (crossing) {
         const int l = __ffs(crossing) - 1;
+        df excl = df_shfl_up(incl, 1);
+        if (lane == 0) excl = df{0.f, 0.f};
         if (lane == l) {
-            float run = incl - lane_sum;
+            df run = excl;
             int last_in_lane = lane * per_lane;
 #pragma unroll
             for (int q = 0; q < kKeep; ++q) {
                 const int u = lane * per_lane + q;
                 if (unit < 0 && q < per_lane && u < units) {
                     last_in_lane = u;
-                    if (run + keep[q] > thr) unit = u;
-                    else run += keep[q];
+                    const df nx = df_add(run, df_from(keep[q]));
+                    if (df_gt(nx, thr)) unit = u;
+                    else run = nx;
                 }
             }
             for (int q = kKeep; q < per_lane && unit < 0; ++q) {
                 const int u = lane * per_lane + q;
                 if (u >= units) break;
                 last_in_lane = u;
-                const float m = unit_mass(u);
-                if (run + m > thr) unit = u;
-                else run += m;
+                const df nx = df_add(run, df_from(unit_mass(u)));
+                if (df_gt(nx, thr)) unit = u;
+                else run = nx;
             }
             if (unit < 0) {
                 unit = last_in_lane;  // rounding: stay inside this lane's units
@@ -393,7 +399,7 @@ __global__ void __launch_bounds__(128)
             base = run;
         }
         unit = __shfl_sync(0xFFFFFFFFu, unit, l);
-        base = __shfl_sync(0xFFFFFFFFu, base, l);
+        base = df_shfl(base, l);
         unit_fallback = __shfl_sync(0xFFFFFFFFu, unit_fallback, l);
     } else {  // rounding left the threshold at or above the total: the last unit with mass
         int lp = -1;
@@ -433,53 +439,78 @@ __global__ void __launch_bounds__(128)
         return mode ? residual_weight(tj, vec_elem<D>(d4, e), c, st.x, inv_st, sd.x, inv_sd)
                     : weight(tj, st.x, c);
     };
-    Kahan lsum;
+    PairSum lsum;
+    int lastpos = -1;
 #pragma unroll
     for (int v = 0; v < kTileVecs; ++v) {
-        if (v < VPL) {
-#pragma unroll
-            for (int e = 0; e < D::EPV; ++e) lsum.add(w_at(tv[v], dv[v % kResVecs], e));
-        }
-    }
-    const float tsum = lsum.value();
-    const float lincl = warp_inclusive_scan(tsum, lane);
-    Kahan run;
-    run.add(base);
-    run.add(lincl - tsum);
-    int cand = kNoIndex, lastpos = -1;
-    float gap = 0.f;  // distance from thr to the nearer of C_{j-1} and C_j at this lane's candidate
-#pragma unroll
-    for (int v = 0; v < kTileVecs; ++v) {  // the same registers, the same arithmetic
         if (v < VPL) {
             const int e0 = (lane * VPL + v) * D::EPV;
 #pragma unroll
             for (int e = 0; e < D::EPV; ++e) {
-                const int j = e0 + e;
                 const float w = w_at(tv[v], dv[v % kResVecs], e);
-                const float before = run.value();
-                run.add(w);
-                if (j < len) {
-                    if (!force_last && cand == kNoIndex && run.value() > thr) {
-                        cand = j;
-                        gap = fminf(thr - before, run.value() - thr);
-                    }
-                    if (w > 0.f) lastpos = j;
-                }
+                lsum.add(w);
+                if (e0 + e < len && w > 0.f) lastpos = e0 + e;
             }
         }
     }
-    const int first = warp_reduce(cand, [](int a, int b) { return min(a, b); });
+    const df lincl = df_warp_scan(lsum.value(), lane);
+    df lexcl = df_shfl_up(lincl, 1);
+    if (lane == 0) lexcl = df{0.f, 0.f};
+    // the lane whose run crosses thr, then its logits spread over the warp (one or two per
+    // lane, the same arithmetic from the same bits) and a second scan
+    int first = kNoIndex;
+    float g = 0.f;  // distance from thr to the nearer of C_{j-1} and C_j of the drawn j
+    const unsigned lb = force_last ? 0u : __ballot_sync(0xFFFFFFFFu, df_gt(df_add(base, lincl), thr));
+    if (lb) {
+        const int l3 = __ffs(lb) - 1;
+        const int NE = VPL * D::EPV;        // logits per lane of the unit
+        const int ne2 = (NE + 31) / 32;     // ... per lane of this scan (1 or 2)
+        const float inv_t1 = inv_st, inv_d1 = inv_sd;
+        float w2[2] = {0.f, 0.f};
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int j = l3 * NE + lane * ne2 + r;
+            if (r < ne2 && lane * ne2 + r < NE && j < len) {
+                const float tj = load_elem<D>(tp, u0 + j);
+                w2[r] = mode ? residual_weight(tj, load_elem<D>(dp, u0 + j), c, st.x, inv_t1, sd.x, inv_d1)
+                             : weight(tj, st.x, c);
+            }
+        }
+        PairSum ps;
+        ps.add(w2[0]);
+        ps.add(w2[1]);
+        const df e_incl = df_warp_scan(ps.value(), lane);
+        const df start = df_add(base, df_shfl(lexcl, l3));
+        const unsigned eb = __ballot_sync(0xFFFFFFFFu, df_pos(df_sub(df_add(start, e_incl), thr)));
+        if (eb) {
+            const int l4 = __ffs(eb) - 1;
+            df run2 = df_add(start, df_shfl(df_shfl_up(e_incl, 1), l4));
+            if (l4 == 0) run2 = start;
+            const float wa = __shfl_sync(0xFFFFFFFFu, w2[0], l4), wb = __shfl_sync(0xFFFFFFFFu, w2[1], l4);
+            const df a0 = df_sub(df_add(run2, df_from(wa)), thr);  // C - thr after the first logit
+            int r = 0;
+            float w = wa;
+            df above = a0;
+            if (!df_pos(a0) && ne2 > 1) {
+                r = 1;
+                w = wb;
+                above = df_sub(df_add(df_add(run2, df_from(wa)), df_from(wb)), thr);
+            }
+            if (df_pos(above)) {
+                first = l3 * NE + l4 * ne2 + r;
+                g = fminf(__fsub_rn(w, above.hi), above.hi);  // thr - C_{j-1} = w - (C_j - thr)
+            }
+        }
+    }
     lastpos = warp_reduce(lastpos, [](int a, int b) { return max(a, b); });
     int tok = first != kNoIndex ? first : lastpos;
     if (tok < 0) tok = 0;
-    // a draw whose threshold lies within the fp32 error of a CDF boundary (or that needed a
-    // rounding fallback, or a sequence decide marked) is redone in extended precision
-    const unsigned owner = __ballot_sync(0xFFFFFFFFu, cand == first && first != kNoIndex);
-    const float g = owner ? __shfl_sync(0xFFFFFFFFu, gap, __ffs(owner) - 1) : 0.f;
+    // a draw whose threshold lies within the fp32 weights' error of a CDF boundary (or that
+    // needed a rounding fallback, or a sequence decide marked) is redone in extended precision
     if (lane == 0) {
         out_tokens[seq * (gamma + 1) + k] = int32_t(u0 + tok);
         const bool near = first == kNoIndex || force_last || unit_fallback || mode != pl.y ||
-                          !(g >= kRefineCdfWindow * total);
+                          !(g >= (mode ? kRefineCdfWindowRes : kRefineCdfWindow) * totd.hi);
         int flag = flag0;
         if (near && flag == 0) flag = kRefineDraw;
         if (flag != 0) {
