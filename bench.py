@@ -337,7 +337,45 @@ def make_call(name, inputs, dev, **ov):
     return call, (acc, out, path)
 
 
-def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
+def step_distribution(call, n=200):
+    """Per-step times (ms) of n calls, each bracketed by its own events: p10 / p50 / p90."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    t = sorted(a.elapsed_time(b) for a, b in evs)
+    return {"p10_ms": t[n // 10], "p50_ms": t[n // 2], "p90_ms": t[(9 * n) // 10], "steps": n}
+
+
+def graph_time(call, per_graph=20, replays=50):
+    """The same calls captured in one CUDA graph (per_graph calls, each with its own
+    offset) and replayed: ms per call."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            call()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(per_graph):
+            call()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(replays):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (replays * per_graph)
+
+
+def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None, detail=False):
     import torch
     from speculative_decoding_verify_spec_gb300 import binding
     from speculative_decoding_verify_spec_gb300 import workloads as W
@@ -388,6 +426,15 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
     torch.cuda.synchronize()
     stage_ms = [sum(ev[k][s].elapsed_time(ev[k][s + 1]) for k in range(ksteps)) / ksteps
                 for s in range(nst)]
+    extra = {}
+    if detail:  # the per-step spread, and the same step replayed from a CUDA graph
+        extra["step_spread"] = step_distribution(call)
+        try:
+            gms = graph_time(call)
+            extra["graph"] = {"ms_per_step": gms, "value": world * cfg["B"] / (gms / 1e3),
+                              "note": "20 calls (20 offsets) captured in one graph, replayed 50 times"}
+        except Exception as exc:  # capture is reported, not required
+            extra["graph"] = {"error": f"{type(exc).__name__}: {exc}"[:200]}
     ms_step = ms_max / steps
     B = cfg["B"]
     value = world * B / (ms_step / 1e3)
@@ -409,6 +456,7 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None):
                      "bytes_per_launch": kb,
                      "traffic": committed_traffic(kernel, name)},
         "gpu_launches": steps * (nst if mode != "sample" or cfg["gamma"] > 0 else 4),
+        **extra,
     }
     if mode == "tree_sample":
         # the walk reads only the rows of the nodes it reaches: the every-row byte count of
@@ -561,7 +609,7 @@ def run_ours(args):
     clocks.start()
     ov = {} if args.batch is None else {"B": args.batch}
     main, inputs, _ = measure(args.workload, args.steps, args.warmup, rank, world, dev, peak,
-                              peak_kind, args.batch)
+                              peak_kind, args.batch, detail=True)
     clk = clocks.stop()
     modes = {}
     if not args.no_modes:
@@ -597,6 +645,7 @@ def run_ours(args):
             "rows_per_s": main["rows_per_s"], "hbm_gbs": main["hbm_gbs_step"],
             "frac_of_8tbs": main["frac_of_8tbs_step"],
             "mean_accepted_len": main["mean_accepted_len"], "stages_ms": main["stages_ms"],
+            "step_spread": main.get("step_spread"), "graph": main.get("graph"),
             "roofline": main["roofline"], "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": main["gpu_launches"], "clocks": clk, "modes": modes,
         }
