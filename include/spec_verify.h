@@ -371,6 +371,15 @@ size_t spec_verify_sample_redraw_offset(int B, int gamma, int V, sv_dtype dtype)
 size_t spec_verify_walk_redraw_offset(sv_mode mode, int B, int rows, int V, sv_dtype dtype);
 
 /*
+ * Test hook of the one software wait (the re-draw's bounded grid barrier): one CTA meets
+ * the barrier expecting expected_arrivals (1 or 2) CTAs.  With 2 nobody else arrives: the
+ * wait gives up after limit_us (at most 5 s) and writes SV_ERR_TIMEOUT to ctl[3]; with 1 it
+ * passes at once and ctl[3] is 0.  ctl: a device int32 array of 8 the call overwrites.
+ * The kernel returns either way, so the context stays usable.
+ */
+sv_status spec_verify_wait_selftest(int *ctl, int expected_arrivals, uint32_t limit_us, void *stream);
+
+/*
  * Test hook: exp(y_hi[i] + y_lo[i]) for arguments <= 0 in the double-float arithmetic of
  * the re-draw (result hi + lo, about 48 significant bits; 0 below -87).  Device arrays of n.
  */

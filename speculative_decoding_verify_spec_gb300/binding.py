@@ -83,6 +83,8 @@ def load_library() -> ctypes.CDLL:
         lib.spec_verify_sample_redraw_offset.restype = sz
         lib.spec_verify_walk_redraw_offset.argtypes = [i32, i32, i32, i32, i32]
         lib.spec_verify_walk_redraw_offset.restype = sz
+        lib.spec_verify_wait_selftest.argtypes = [P, i32, ctypes.c_uint32, P]
+        lib.spec_verify_wait_selftest.restype = i32
         lib.spec_verify_exp_df.argtypes = [P, P, i32, P, P, P]
         lib.spec_verify_exp_df.restype = i32
         lib.spec_verify_set_stage_events.argtypes = [P, i32]
@@ -471,6 +473,17 @@ def walk_redraw_state(workspace: torch.Tensor, mode: int, B: int, rows: int, V: 
     torch.cuda.synchronize(workspace.device)
     words = workspace.view(torch.uint8)[off:off + 4 * (8 + B)].clone().view(torch.int32).cpu().numpy()
     return int(words[0]), int(words[4]), int(words[3]), words[8:8 + B].copy()
+
+
+def wait_selftest(expected_arrivals: int, limit_us: int, device="cuda:0") -> int:
+    """Test hook: run the re-draw's bounded grid barrier in one CTA expecting
+    `expected_arrivals` CTAs; returns the status word it leaves (4 = SV_ERR_TIMEOUT)."""
+    lib = load_library()
+    ctl = torch.zeros(8, dtype=torch.int32, device=device)
+    _check(lib.spec_verify_wait_selftest(ctl.data_ptr(), int(expected_arrivals), int(limit_us),
+                                         _stream(torch.device(device))), "spec_verify_wait_selftest")
+    torch.cuda.synchronize(device)
+    return int(ctl[3].item())
 
 
 def spec_verify_exp_df(y_hi: torch.Tensor, y_lo: torch.Tensor):

@@ -557,6 +557,12 @@ size_t spec_verify_walk_redraw_offset(sv_mode mode, int B, int rows, int V, sv_d
     return layout(mode, B, rows, V, dtype).rctl;
 }
 
+sv_status spec_verify_wait_selftest(int *ctl, int expected_arrivals, uint32_t limit_us, void *stream) {
+    if (!ctl || expected_arrivals < 1 || expected_arrivals > 2 || limit_us > 5000000u) return SV_ERR_INVALID_ARG;
+    return cuda_status(sv::launch_wait_selftest(ctl, expected_arrivals, uint64_t(limit_us) * 1000u,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 sv_status spec_verify_exp_df(const float *y_hi, const float *y_lo, int n, float *out_hi, float *out_lo,
                              void *stream) {
     if (n < 0) return SV_ERR_INVALID_ARG;

@@ -1,4 +1,4 @@
-// sv_grid.cuh -- a bounded grid-wide barrier for the cooperative re-draw kernels.
+// sv_grid.cuh -- a bounded grid-wide barrier for the cooperative re-draw kernel.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -19,11 +19,12 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Grid barrier for a cooperative launch (all CTAs resident).  ctl[kBarCount] must be 0
-// before the first barrier of a launch (the generation word may hold anything).  Returns
-// false, after recording SV_ERR_TIMEOUT in ctl[kBarStatus], if the other CTAs did not
-// arrive within the limit.
-__device__ inline bool grid_barrier(int *ctl) {
+// Grid barrier for a cooperative launch (all CTAs resident): waits until `expected` CTAs
+// (the grid by default) have arrived.  ctl[kBarCount] must be 0 before the first barrier of
+// a launch (the generation word may hold anything).  Returns false, after recording
+// SV_ERR_TIMEOUT in ctl[kBarStatus], if the others did not arrive within limit_ns.
+__device__ inline bool grid_barrier(int *ctl, int expected = -1, uint64_t limit_ns = kBarrierLimitNs) {
+    if (expected < 0) expected = int(gridDim.x);
     __shared__ int ok_s;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -31,14 +32,14 @@ __device__ inline bool grid_barrier(int *ctl) {
         const int g = *gen;
         int ok = 1;
         __threadfence();
-        if (atomicAdd(ctl + kBarCount, 1) == int(gridDim.x) - 1) {
+        if (atomicAdd(ctl + kBarCount, 1) == expected - 1) {
             atomicExch(ctl + kBarCount, 0);
             __threadfence();
             atomicAdd(ctl + kBarGen, 1);
         } else {
             const uint64_t t0 = global_ns();
             for (uint32_t i = 0; *gen == g; ++i) {
-                if ((i & 63) == 63 && global_ns() - t0 > kBarrierLimitNs) {
+                if ((i & 63) == 63 && global_ns() - t0 > limit_ns) {
                     ok = 0;
                     break;
                 }

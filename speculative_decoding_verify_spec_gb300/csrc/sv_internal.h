@@ -168,6 +168,8 @@ cudaError_t launch_refine(int dtype, bool vec, Logits t, Logits d, int B, int ga
                           uint64_t seed, uint64_t offset, const int32_t *x, const void *rowstat, const void *plan,
                           int *rctl, const RefineInfo *rinfo, void *rsum, void *ramb, int32_t *accepted_len,
                           int32_t *out_tokens, cudaStream_t s);
+// Test hook: one CTA through the re-draw's grid barrier expecting `expected` arrivals.
+cudaError_t launch_wait_selftest(int *ctl, int expected, uint64_t limit_ns, cudaStream_t s);
 // Test hook: exp(hi + lo) in double-float for n arguments <= 0.
 cudaError_t launch_exp_df(const float *y_hi, const float *y_lo, int n, float *out_hi, float *out_lo,
                           cudaStream_t s);

@@ -420,6 +420,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
+// Test hook of the bounded wait: one CTA meets the re-draw's grid barrier expecting
+// `expected` arrivals; with more than one nobody else comes, the wait runs out after
+// limit_ns and records SV_ERR_TIMEOUT in ctl[kBarStatus] (the same path a stalled re-draw
+// takes).
+__global__ void wait_selftest_kernel(int *ctl, int expected, uint64_t limit_ns) {
+    if (threadIdx.x == 0) {
+        ctl[kBarCount] = 0;
+        ctl[kBarStatus] = 0;
+    }
+    __syncthreads();
+    grid_barrier(ctl, expected, limit_ns);
+}
+
 __global__ void exp_df_kernel(const float *__restrict__ y_hi, const float *__restrict__ y_lo, int n,
                               float *__restrict__ out_hi, float *__restrict__ out_lo) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -445,6 +458,11 @@ cudaError_t launch_refine(int dtype, bool vec, Logits t, Logits d, int B, int ga
     return launch_after_ex(true, k, grid, kThreads, 0, s, t, d, gamma, V, nref, T, seed, offset, x,
                            static_cast<const float2 *>(rowstat), rctl, rinfo, static_cast<df *>(rsum),
                            static_cast<int *>(ramb), accepted_len, out_tokens);
+}
+
+cudaError_t launch_wait_selftest(int *ctl, int expected, uint64_t limit_ns, cudaStream_t s) {
+    wait_selftest_kernel<<<1, 32, 0, s>>>(ctl, expected, limit_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_exp_df(const float *y_hi, const float *y_lo, int n, float *out_hi, float *out_lo,
