@@ -546,8 +546,9 @@ def measure_e2e(name, inputs, steps, dev, **ov):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
-def oracle_run(name, inputs, threads):
-    """The oracle over a batch, one thread per range of sequences."""
+def oracle_run(name, inputs, threads, limit=None):
+    """The oracle over a batch (its first `limit` sequences if given), one thread per range
+    of sequences."""
     import numpy as np
     import oracle
     from speculative_decoding_verify_spec_gb300 import workloads as W
@@ -556,7 +557,7 @@ def oracle_run(name, inputs, threads):
     mode = cfg["mode"]
     orc = oracle.default()
     t = oracle.as_oracle_logits(inputs.target)
-    B = t.shape[0]
+    B = t.shape[0] if limit is None else min(limit, t.shape[0])
     step = max(1, (B + threads - 1) // threads)
     ranges = [(s, min(B, s + step)) for s in range(0, B, step)]
     if mode == "sample":
@@ -588,9 +589,15 @@ def cpu_baseline(name, inputs):
     t0 = time.perf_counter()
     B, used = oracle_run(name, inputs, cores)
     dt = time.perf_counter() - t0
+    n1 = 16  # and single-threaded, on the batch's first sequences
+    t1 = time.perf_counter()
+    B1, _ = oracle_run(name, inputs, 1, limit=n1)
+    dt1 = time.perf_counter() - t1
     return {"value": B / dt, "unit": UNIT, "cores": min(cores, used), "kind": "oracle",
             "sample": f"the full batch of {B} sequences of the same workload, once "
-                      f"({dt:.2f} s wall on {min(cores, used)} threads)"}
+                      f"({dt:.2f} s wall on {min(cores, used)} threads)",
+            "single_thread": {"value": B1 / dt1, "unit": UNIT, "cores": 1,
+                              "sample": f"the first {B1} sequences of the batch ({dt1:.2f} s wall)"}}
 
 
 def run_ours(args):
