@@ -43,6 +43,7 @@ DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "max_tiles_kernel",
                    "tree_lazy": "greedy_walk_kernel", "ngram": "ngram_draft_kernel",
                    "typical": "typical_walk_kernel", "onehot": "typical_walk_kernel"}
 STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
+ACCEPT_STEPS = 16  # untimed steps whose accepted lengths and re-draw counts are read back
 STAGES = {"sample": ["row_stats", "decide", "residual_mass", "inverse_cdf", "redraw"],
           "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"], "tree_sample": ["walk", "rewalk_exp", "rewalk"],
           "sample_lazy": ["walk", "rewalk_exp", "rewalk"], "greedy_lazy": ["walk"], "tree_lazy": ["walk"], "ngram": ["draft"],
@@ -237,6 +238,7 @@ def make_call(name, inputs, dev, **ov):
             return sv.spec_verify_typical(target, tokens, inputs.temperature, cfg["epsilon"], cfg["delta"],
                                           inputs.seed, step_counter[0], workspace=ws, accepted_len=acc,
                                           out_tokens=out)
+        call.redraw_state = lambda: binding.walk_redraw_state(ws, binding.MODE_TYPICAL, B, g, V, dt)[:3]
         return call, (acc, out)
     if mode == "sample" and cfg.get("onehot"):
         g = cfg["gamma"]
@@ -250,6 +252,7 @@ def make_call(name, inputs, dev, **ov):
             step_counter[0] += 1
             return sv.spec_verify_sample_onehot(target, tokens, inputs.temperature, inputs.seed, step_counter[0],
                                                 workspace=ws, accepted_len=acc, out_tokens=out)
+        call.redraw_state = lambda: binding.walk_redraw_state(ws, binding.MODE_SAMPLE_ONEHOT, B, g, V, dt)[:3]
         return call, (acc, out)
     if mode == "sample" and lazy:
         g = cfg["gamma"]
@@ -264,6 +267,7 @@ def make_call(name, inputs, dev, **ov):
             return sv.spec_verify_sample_lazy(target, draft, tokens, inputs.temperature, inputs.seed,
                                               step_counter[0], workspace=ws, accepted_len=acc,
                                               out_tokens=out)
+        call.redraw_state = lambda: binding.walk_redraw_state(ws, binding.MODE_SAMPLE_LAZY, B, g, V, dt)[:3]
         return call, (acc, out)
     if mode == "greedy" and lazy:
         g = cfg["gamma"]
@@ -295,6 +299,11 @@ def make_call(name, inputs, dev, **ov):
             return sv.spec_verify_sample(target, draft, tokens, inputs.temperature, inputs.seed,
                                          step_counter[0], workspace=ws, accepted_len=acc,
                                          out_tokens=out)
+
+        def chain_state():  # the re-draw takes the first 32 marked sequences (the library's list)
+            m, status = binding.sample_redraw_state(ws, B, g, V, dt)
+            return m, min(m, 32), status
+        call.redraw_state = chain_state
         return call, (acc, out)
     if mode == "greedy":
         g = cfg["gamma"]
@@ -323,6 +332,7 @@ def make_call(name, inputs, dev, **ov):
                                               without_replacement=inputs.without_replacement,
                                               workspace=ws, accepted_len=acc, out_tokens=out,
                                               out_path=path)
+        call.redraw_state = lambda: binding.walk_redraw_state(ws, binding.MODE_TREE_SAMPLE, B, N, V, dt)[:3]
         return call, (acc, out, path)
     ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_TREE, B, N, V, dt),
                      dtype=torch.uint8, device=dev)
@@ -335,6 +345,34 @@ def make_call(name, inputs, dev, **ov):
                                           workspace=ws, accepted_len=acc, out_tokens=out,
                                           out_path=path)
     return call, (acc, out, path)
+
+
+def acceptance_stats(call, acc, steps):
+    """Untimed: the accepted-length histogram over `steps` further calls (each with its own
+    offset where the rule samples), and for the sampling rules how many sequences the
+    extended-precision pass had to re-do -- the GPU's counterpart of the oracle's
+    tolerance flags."""
+    import torch
+    seen = []
+    marked = redone = 0
+    status = []
+    for _ in range(steps):
+        call()
+        seen.append(acc.long().clone())
+        if hasattr(call, "redraw_state"):
+            m, r, st = call.redraw_state()
+            marked += m
+            redone += r
+            status.append(st)
+    seqs = steps * acc.numel()
+    hist = torch.bincount(torch.cat(seen) + 1).cpu()  # bin 0 counts invalid sequences (-1)
+    out = {"steps": steps, "sequences": seqs, "invalid": int(hist[0]),
+           "accepted_len_hist": [int(x) for x in hist[1:]],
+           "mean_accepted_len": float((hist[1:] * torch.arange(len(hist) - 1)).sum()) / max(1, seqs - int(hist[0]))}
+    if hasattr(call, "redraw_state"):
+        out.update({"redraw_marked": marked, "redraw_redone": redone, "redraw_rate": marked / seqs,
+                    "redraw_status_nonzero": sum(1 for x in status if x != 0)})
+    return out
 
 
 def step_distribution(call, n=200):
@@ -427,6 +465,11 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None, 
     stage_ms = [sum(ev[k][s].elapsed_time(ev[k][s + 1]) for k in range(ksteps)) / ksteps
                 for s in range(nst)]
     extra = {}
+    if mode != "ngram":
+        try:  # reported beside the timings, never in place of them
+            extra["acceptance"] = acceptance_stats(call, outs[0], ACCEPT_STEPS)
+        except Exception as exc:
+            extra["acceptance"] = {"error": f"{type(exc).__name__}: {exc}"[:200]}
     if detail:  # the per-step spread, and the same step replayed from a CUDA graph
         extra["step_spread"] = step_distribution(call)
         try:
@@ -548,7 +591,7 @@ def measure_e2e(name, inputs, steps, dev, **ov):
 
 def oracle_run(name, inputs, threads, limit=None):
     """The oracle over a batch (its first `limit` sequences if given), one thread per range
-    of sequences."""
+    of sequences; returns (sequences, threads used, accepted_len or None, flags or None)."""
     import numpy as np
     import oracle
     from speculative_decoding_verify_spec_gb300 import workloads as W
@@ -556,48 +599,105 @@ def oracle_run(name, inputs, threads, limit=None):
     cfg = W.WORKLOADS[name]
     mode = cfg["mode"]
     orc = oracle.default()
-    t = oracle.as_oracle_logits(inputs.target)
-    B = t.shape[0] if limit is None else min(limit, t.shape[0])
+    if mode == "ngram":
+        h = inputs.history.cpu().numpy()
+        L = np.clip(inputs.lengths.cpu().numpy(), 0, h.shape[1])
+        B = h.shape[0] if limit is None else min(limit, h.shape[0])
+        fn = lambda r: orc.ngram_draft(h[r[0]:r[1]], L[r[0]:r[1]], inputs.n, inputs.k, inputs.pad)
+    else:
+        t = oracle.as_oracle_logits(inputs.target)
+        B = t.shape[0] if limit is None else min(limit, t.shape[0])
     step = max(1, (B + threads - 1) // threads)
     ranges = [(s, min(B, s + step)) for s in range(0, B, step)]
-    if mode == "sample":
+    T, seed = getattr(inputs, "temperature", None), getattr(inputs, "seed", None)
+    if mode == "sample" and cfg.get("typical"):
+        x = inputs.draft_tokens.cpu().numpy()
+
+        def fn(r):
+            acc, _, flags, _ = orc.verify_typical(t[r[0]:r[1]], x[r[0]:r[1]], T, cfg["epsilon"], cfg["delta"],
+                                                  seed, 0, b0=r[0])
+            return acc, flags
+    elif mode == "sample" and cfg.get("onehot"):
+        x = inputs.draft_tokens.cpu().numpy()
+        g, V = x.shape[1], t.shape[2]
+
+        def fn(r):  # q one-hot on each draft token: -inf everywhere else, in the target's form
+            n = r[1] - r[0]
+            if t.dtype == np.uint16:
+                d = np.full((n, g, V), 0xFF80, np.uint16)  # bf16 -inf
+            else:
+                d = np.full((n, g, V), -np.inf, np.float32)
+            if g:
+                d[np.arange(n)[:, None], np.arange(g)[None, :], x[r[0]:r[1]]] = 0
+            acc, _, flags = orc.verify_sample(t[r[0]:r[1]], d, x[r[0]:r[1]], T, seed, 0, b0=r[0])
+            return acc, flags
+    elif mode == "sample":
         d = oracle.as_oracle_logits(inputs.draft)
         x = inputs.draft_tokens.cpu().numpy()
-        fn = lambda r: orc.verify_sample(t[r[0]:r[1]], d[r[0]:r[1]], x[r[0]:r[1]],
-                                         inputs.temperature, inputs.seed, 0, b0=r[0])
+
+        def fn(r):
+            acc, _, flags = orc.verify_sample(t[r[0]:r[1]], d[r[0]:r[1]], x[r[0]:r[1]], T, seed, 0, b0=r[0])
+            return acc, flags
     elif mode == "greedy":
         x = inputs.draft_tokens.cpu().numpy()
-        fn = lambda r: orc.verify_greedy(t[r[0]:r[1]], x[r[0]:r[1]])
+        fn = lambda r: (orc.verify_greedy(t[r[0]:r[1]], x[r[0]:r[1]])[0], None)
     elif mode == "tree_sample":
         d = oracle.as_oracle_logits(inputs.draft)
         par = inputs.parent.cpu().numpy()
         x = inputs.node_tokens.cpu().numpy()
-        fn = lambda r: orc.verify_tree_sample(t[r[0]:r[1]], d[r[0]:r[1]], par, x[r[0]:r[1]],
-                                              inputs.max_depth, inputs.temperature, inputs.seed, 0,
-                                              inputs.without_replacement, b0=r[0])
-    else:
+
+        def fn(r):
+            acc, _, _, flags = orc.verify_tree_sample(t[r[0]:r[1]], d[r[0]:r[1]], par, x[r[0]:r[1]],
+                                                      inputs.max_depth, T, seed, 0,
+                                                      inputs.without_replacement, b0=r[0])
+            return acc, flags
+    elif mode == "tree":
         par = inputs.parent.cpu().numpy()
         x = inputs.node_tokens.cpu().numpy()
-        fn = lambda r: orc.verify_tree_greedy(t[r[0]:r[1]], par, x[r[0]:r[1]], inputs.max_depth)
+
+        def fn(r):
+            acc, _, _, flags = orc.verify_tree_greedy(t[r[0]:r[1]], par, x[r[0]:r[1]], inputs.max_depth)
+            return acc, flags
     with ThreadPoolExecutor(threads) as ex:
-        list(ex.map(fn, ranges))
-    return B, len(ranges)
+        res = list(ex.map(fn, ranges))
+    if mode == "ngram" or not res:
+        return B, len(ranges), None, None
+    acc = np.concatenate([r[0] for r in res])
+    flags = np.concatenate([r[1] for r in res]) if res[0][1] is not None else None
+    return B, len(ranges), acc, flags
+
+
+def oracle_acceptance(acc, flags):
+    """Accepted-length histogram of an oracle run and how many sequences it flagged as
+    decided within its tolerance of a threshold or CDF boundary."""
+    import numpy as np
+
+    acc = np.asarray(acc)
+    valid = acc[acc >= 0]
+    out = {"sequences": int(acc.size), "invalid": int((acc < 0).sum()),
+           "accepted_len_hist": [int(x) for x in np.bincount(valid)] if valid.size else [],
+           "mean_accepted_len": float(valid.mean()) if valid.size else None}
+    if flags is not None:
+        n = int((np.asarray(flags) != 0).sum())
+        out.update({"oracle_flags": n, "oracle_flag_rate": n / max(1, acc.size)})
+    return out
 
 
 def cpu_baseline(name, inputs):
     cores = os.cpu_count() or 1
     t0 = time.perf_counter()
-    B, used = oracle_run(name, inputs, cores)
+    B, used, acc, flags = oracle_run(name, inputs, cores)
     dt = time.perf_counter() - t0
     n1 = 16  # and single-threaded, on the batch's first sequences
     t1 = time.perf_counter()
-    B1, _ = oracle_run(name, inputs, 1, limit=n1)
+    B1, _, _, _ = oracle_run(name, inputs, 1, limit=n1)
     dt1 = time.perf_counter() - t1
     return {"value": B / dt, "unit": UNIT, "cores": min(cores, used), "kind": "oracle",
             "sample": f"the full batch of {B} sequences of the same workload, once "
                       f"({dt:.2f} s wall on {min(cores, used)} threads)",
             "single_thread": {"value": B1 / dt1, "unit": UNIT, "cores": 1,
-                              "sample": f"the first {B1} sequences of the batch ({dt1:.2f} s wall)"}}
+                              "sample": f"the first {B1} sequences of the batch ({dt1:.2f} s wall)"},
+            "acceptance": oracle_acceptance(acc, flags) if acc is not None else None}
 
 
 def run_ours(args):
@@ -644,14 +744,15 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded generators, resident in HBM)",
             "config": {"workload": W.DESCRIPTIONS[args.workload], "B": cfg["B"],
-                       "gamma": cfg.get("gamma"), "V": cfg["V"], "logits": cfg["dtype"],
+                       "gamma": cfg.get("gamma"), "V": cfg["V"], "logits": cfg.get("dtype"),
                        "temperature": cfg.get("temperature"),
                        "l2": f"inputs larger than L2 ({W.logical_bytes(args.workload, **ov) / 1e9:.2f} GB "
                              "read per step), no flush",
                        "parallelism": f"replicas x{world} (independent batches per GPU)"},
             "rows_per_s": main["rows_per_s"], "hbm_gbs": main["hbm_gbs_step"],
             "frac_of_8tbs": main["frac_of_8tbs_step"],
-            "mean_accepted_len": main["mean_accepted_len"], "stages_ms": main["stages_ms"],
+            "mean_accepted_len": main["mean_accepted_len"], "acceptance": main.get("acceptance"),
+            "stages_ms": main["stages_ms"],
             "step_spread": main.get("step_spread"), "graph": main.get("graph"),
             "roofline": main["roofline"], "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": main["gpu_launches"], "clocks": clk, "modes": modes,
@@ -683,7 +784,7 @@ def run_reference(args):
         oracle_run(name, inputs, cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_run(name, inputs, cores)
+        _, _, acc, flags = oracle_run(name, inputs, cores)
     dt = time.perf_counter() - t0
     value = args.steps * per_step / dt
     line = {
@@ -692,10 +793,11 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded generators)",
         "config": {"workload": W.DESCRIPTIONS[name], "B": cfg["B"], "gamma": cfg.get("gamma"),
-                   "V": cfg["V"], "logits": cfg["dtype"]},
+                   "V": cfg["V"], "logits": cfg.get("dtype")},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, per_step), "kind": "oracle",
                          "sample": f"{per_step} sequences of the workload per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "acceptance": oracle_acceptance(acc, flags) if args.steps > 0 and acc is not None else None,
     }
     print(json.dumps(line), flush=True)
 
