@@ -23,6 +23,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 from concurrent.futures import ThreadPoolExecutor
 
@@ -114,15 +115,23 @@ class ClockSampler:
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{self.gpu}.csv")
-            self.f = open(self.path, "w")
+            out_dir = os.environ.get("SV_BENCH_OUT")  # where to keep the raw samples, if anywhere
+            if out_dir:
+                os.makedirs(out_dir, exist_ok=True)
+                self.path = os.path.join(out_dir, f"clocks_gpu{self.gpu}.csv")
+                self.f = open(self.path, "w")
+            else:
+                self.f = tempfile.NamedTemporaryFile("w", suffix=".csv", delete=False)
+                self.path = self.f.name
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader", "-lms", "100"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
             time.sleep(0.3)
-        except Exception:
+        except Exception:  # no nvidia-smi: no clock record
             self.proc = None
+            if self.path and not os.environ.get("SV_BENCH_OUT"):
+                self.f.close()
+                os.unlink(self.path)
 
     def stop(self):
         if self.proc is None:
@@ -136,7 +145,11 @@ class ClockSampler:
         self.f.close()
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.readlines()
+        if not os.environ.get("SV_BENCH_OUT"):
+            os.unlink(self.path)
+        for line in lines:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue

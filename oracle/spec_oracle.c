@@ -25,7 +25,7 @@
  *   [PH]  Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3"
  *         (SC'11): the Philox4x32-10 counter-based generator.
  *
- * Readings where the pages leave a step open (each is listed in the design doc):
+ * Readings taken where the pages leave a step open:
  *   - uniforms: Philox4x32-10, key = seed, counter = (4*i + purpose, b, offset lo, offset hi),
  *     word 0, u = (w >> 8) * 2^-24 (exactly representable in fp32 and fp64).
  *   - accept test: u * q(x) < p(x)  (the page's strict "r < accept_prob" with the division
@@ -589,7 +589,7 @@ int oracle_verify_tree_greedy(const void *target, int64_t t_batch_stride, int64_
  * at a leaf it is the bonus drawn from p_v; both with u' = U(b, v, 1) by inverse CDF.
  * With a chain-shaped tree (node i's only child is i + 1) this is exactly
  * oracle_verify_sample, uniforms included.
- * Readings (DESIGN.md): a residual of mass 0 leaves p unchanged (flagged); without
+ * Readings: a residual of mass 0 leaves p unchanged (flagged); without
  * replacement a q with no mass left is 0 everywhere (a later sibling is then accepted iff
  * p(x) > 0, and the residual is p).  Validity: every node token in [0, V) and every row
  * the walk reads (the target row of each node it reaches, the draft row of each reached
@@ -835,7 +835,7 @@ done:
 /* Typical acceptance [SD "Medusa" paragraph ("accepts any token whose target probability
  * exceeds a threshold") and the closing note on typical acceptance ("a threshold that
  * scales with the step's entropy"; not distribution-preserving)].  The pages fix neither
- * the form nor the constants; the reading taken (R20):
+ * the form nor the constants; the reading taken:
  *   p_i   = softmax(t_i / T)                                   (rows i = 0 .. gamma)
  *   H_i   = -sum_j p_i(j) ln p_i(j)                            (0 ln 0 = 0)
  *   tau_i = min(epsilon, delta * exp(-H_i))                    (exp(-H): 1 / perplexity)

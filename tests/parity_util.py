@@ -139,12 +139,16 @@ def compare_sample(acc, out, o_acc, o_out, o_flags, o_diag=None, label="", recor
 
 
 def record_rates(label, n, mismatches, flagged, flags, mismatch_diag=(), **extra):
-    """Append the flag / mismatch counts of a parity case to gpurun_out/parity_rates.jsonl."""
-    out_dir = os.path.join(ROOT, "gpurun_out")
-    os.makedirs(out_dir, exist_ok=True)
+    """Append the flag / mismatch counts of a parity case, as one JSON line, to the file that
+    the SV_PARITY_LOG environment variable names (nothing is kept when it is unset)."""
+    path = os.environ.get("SV_PARITY_LOG")
+    if not path:
+        return
+    if os.path.dirname(path):
+        os.makedirs(os.path.dirname(path), exist_ok=True)
     rec = {"case": label, "sequences": n, "mismatches": mismatches, "flagged": flagged,
            "flag_accept": int(((flags & 1) != 0).sum()), "flag_cdf": int(((flags & 2) != 0).sum()),
            "flag_residual_small": int(((flags & 4) != 0).sum()),
            "mismatch_diagnostics": list(mismatch_diag)[:50], **extra}
-    with open(os.path.join(out_dir, "parity_rates.jsonl"), "a") as f:
+    with open(path, "a") as f:
         f.write(json.dumps(rec) + "\n")
