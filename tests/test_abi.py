@@ -141,3 +141,100 @@ def test_binding_refuses_cpu_tensors():
     t = torch.zeros(1, 2, 8)
     with pytest.raises(ValueError):
         binding.spec_verify_greedy(t, torch.zeros(1, 1, dtype=torch.int32))
+
+
+def test_tree_sample_and_lazy_entries_reject_bad_arguments(lib):
+    ts = lib.spec_verify_tree_sample
+    # t tsb tsr d dsb dsr dtype B N V parent tokens max_depth T seed off wr acc out path ws wsb stream
+    base = [P(16), 0, 0, P(16), 0, 0, 1, 1, 7, 5, P(16), P(16), 2, 1.0, 0, 0, 1, P(16), P(16), P(16),
+            P(256), 1 << 20, None]
+
+    def call(fn, args, **at):
+        a = list(args)
+        for i, v in at.items():
+            a[int(i[1:])] = v
+        return fn(*a)
+    assert call(ts, base, a6=9) == 2                     # unknown dtype
+    assert call(ts, base, a8=0) == 1                     # N < 1
+    assert call(ts, base, a8=5000) == 1                  # N above the limit
+    assert call(ts, base, a12=7) == 1                    # max_depth must be < N
+    assert call(ts, base, a2=-3) == 1                    # negative stride
+    assert call(ts, base, a13=0.0) == 1                  # temperature must be > 0
+    assert call(ts, base, a13=float("inf")) == 1
+    assert call(ts, base, a10=None) == 1                 # no parent array
+    assert call(ts, base, a3=None) == 1                  # no draft logits
+    assert call(ts, base, a20=None) == 5                 # no workspace
+    assert call(ts, base, a7=0) == 0                     # empty batch
+    sl = lib.spec_verify_sample_lazy
+    # t tsb tsr d dsb dsr dtype B gamma V x T seed off acc out ws wsb stream
+    lz = [P(16), 0, 0, P(16), 0, 0, 1, 1, 2, 5, P(16), 1.0, 0, 0, P(16), P(16), P(256), 1 << 20, None]
+    assert call(sl, lz, a8=-1) == 1
+    assert call(sl, lz, a8=2000) == 1
+    assert call(sl, lz, a11=float("nan")) == 1
+    assert call(sl, lz, a10=None) == 1                   # drafts needed when gamma > 0
+    assert call(sl, lz, a16=P(8)) == 5                   # misaligned workspace
+    assert call(sl, lz, a7=0) == 0
+    gl = lib.spec_verify_greedy_lazy
+    assert gl(P(16), 0, 0, 1, 1, 2, 0, P(16), P(16), P(16), None) == 1      # V < 1
+    assert gl(P(16), 0, 0, 1, 1, 2, 5, None, P(16), P(16), None) == 1       # no drafts
+    assert gl(P(16), 0, 0, 3, 1, 2, 5, P(16), P(16), P(16), None) == 2      # unknown dtype
+    assert gl(P(16), 0, 0, 1, 0, 2, 5, P(16), P(16), P(16), None) == 0
+    tl = lib.spec_verify_tree_greedy_lazy
+    assert tl(P(16), 0, 0, 1, 1, 7, 5, P(16), P(16), 7, P(16), P(16), P(16), None) == 1  # depth >= N
+    assert tl(P(16), 0, 0, 1, 1, 7, 5, None, P(16), 2, P(16), P(16), P(16), None) == 1   # no parent
+    assert tl(P(16), 0, 0, 1, 0, 7, 5, P(16), P(16), 2, P(16), P(16), P(16), None) == 0
+
+
+def test_target_only_rules_reject_bad_arguments(lib):
+    ty = lib.spec_verify_typical
+    # t tsb tsr dtype B gamma V x T eps delta seed off acc out ws wsb stream
+    base = [P(16), 0, 0, 1, 1, 2, 5, P(16), 1.0, 0.1, 0.3, 0, 0, P(16), P(16), P(256), 1 << 20, None]
+
+    def call(fn, args, **at):
+        a = list(args)
+        for i, v in at.items():
+            a[int(i[1:])] = v
+        return fn(*a)
+    assert call(ty, base, a9=-0.1) == 1                  # epsilon must be >= 0
+    assert call(ty, base, a10=float("nan")) == 1         # delta must be finite
+    assert call(ty, base, a10=float("inf")) == 1
+    assert call(ty, base, a8=0.0) == 1
+    assert call(ty, base, a7=None) == 1
+    assert call(ty, base, a3=5) == 2
+    assert call(ty, base, a16=8) == 5                    # workspace too small
+    assert call(ty, base, a4=0) == 0
+    oh = lib.spec_verify_sample_onehot
+    # t tsb tsr dtype B gamma V x T seed off acc out ws wsb stream
+    ob = [P(16), 0, 0, 1, 1, 2, 5, P(16), 1.0, 0, 0, P(16), P(16), P(256), 1 << 20, None]
+    assert call(oh, ob, a5=-1) == 1
+    assert call(oh, ob, a8=-1.0) == 1
+    assert call(oh, ob, a11=None) == 1                   # no accepted_len
+    assert call(oh, ob, a13=None) == 5
+    assert call(oh, ob, a4=0) == 0
+
+
+def test_drafter_and_hooks_reject_bad_arguments(lib):
+    ng = lib.spec_ngram_draft
+    # history stride lengths B n k pad drafts count stream
+    assert ng(P(16), 8, P(16), 1, 0, 4, 0, P(16), P(16), None) == 1          # n < 1
+    assert ng(P(16), 8, P(16), 1, 3, -1, 0, P(16), P(16), None) == 1         # k < 0
+    assert ng(P(16), -8, P(16), 1, 3, 4, 0, P(16), P(16), None) == 1         # negative stride
+    assert ng(P(16), 8, None, 1, 3, 4, 0, P(16), P(16), None) == 1           # no lengths
+    assert ng(P(16), 8, P(16), 1, 3, 4, 0, None, P(16), None) == 1           # drafts needed when k > 0
+    assert ng(P(16), 8, P(16), 0, 3, 4, 0, P(16), P(16), None) == 0          # empty batch
+    rs = lib.spec_verify_row_stats
+    assert rs(P(16), 0, 0, 1, 1, 0, 5, 1.0, P(16), P(16), P(256), 1 << 20, None) == 1   # rows < 1
+    assert rs(P(16), 0, 0, 1, 1, 1, 5, 0.0, P(16), P(16), P(256), 1 << 20, None) == 1   # T = 0
+    assert rs(P(16), 0, 0, 1, 1, 1, 5, 1.0, None, P(16), P(256), 1 << 20, None) == 1    # no output
+    assert rs(P(16), 0, 0, 4, 1, 1, 5, 1.0, P(16), P(16), P(256), 1 << 20, None) == 2
+    assert rs(P(16), 0, 0, 1, 0, 1, 5, 1.0, P(16), P(16), P(256), 1 << 20, None) == 0
+    assert lib.spec_verify_exp_df(P(16), P(16), -1, P(16), P(16), None) == 1
+    assert lib.spec_verify_exp_df(None, None, 0, None, None, None) == 0
+    assert lib.spec_verify_exp_df(None, P(16), 4, P(16), P(16), None) == 1
+    assert lib.spec_verify_wait_selftest(None, 1, 1000, None) == 1
+    assert lib.spec_verify_wait_selftest(P(16), 0, 1000, None) == 1          # at least one arrival
+    assert lib.spec_verify_wait_selftest(P(16), 3, 1000, None) == 1          # at most two
+    assert lib.spec_verify_wait_selftest(P(16), 2, 6_000_000, None) == 1     # limit above 5 s
+    assert lib.spec_verify_set_stage_events(None, -1) == 1
+    assert lib.spec_verify_set_stage_events(None, 9) == 1
+    assert lib.spec_verify_set_stage_events(None, 0) == 0                    # clears the list
