@@ -18,8 +18,9 @@
  *
  * Conventions shared by every entry point
  *   - Every array argument is a DEVICE pointer; the caller owns all memory.  The library
- *     allocates nothing and keeps no state between calls (apart from the optional,
- *     thread-local timing events of spec_verify_set_stage_events).
+ *     allocates nothing and keeps no state between calls, apart from the optional,
+ *     thread-local timing events of spec_verify_set_stage_events and the fixed scratch
+ *     array of spec_verify_greedy_noalloc.
  *   - Logits are [B][rows][V] with a contiguous last axis.  Strides are in ELEMENTS and may
  *     be 0 (broadcast).  Rows are read with 16-byte vector loads when the base pointer and
  *     both strides (times the element size) are multiples of 16 bytes, else element-wise.
@@ -33,8 +34,9 @@
  *     token of that sequence = -1.  Other sequences are unaffected.
  *   - `workspace` is caller-provided device scratch of at least
  *     spec_verify_workspace_size(...) bytes, 16-byte aligned.  Its contents need no
- *     initialisation and are meaningless after the call.  Calls that run concurrently
- *     need distinct workspaces.
+ *     initialisation.  After the call only the re-draw counts that the test hooks
+ *     spec_verify_sample_redraw_offset / spec_verify_walk_redraw_offset locate mean
+ *     anything.  Calls that run concurrently need distinct workspaces.
  *   - A round emits accepted_len[b] + 1 tokens (always >= 1) [SD "Extending to a chain"].
  */
 #ifndef SPEC_VERIFY_H
@@ -168,8 +170,8 @@ sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_str
  * from the last residual, at a leaf from p_v (inverse CDF, u' = U(b, v, purpose 1)).  A
  * chain-shaped tree gives spec_verify_sample's rule.  Outputs as spec_verify_tree_greedy:
  * accepted_len = depth of the final node, out_tokens = path tokens then the final token,
- * out_path = node ids (may be NULL).  Rows are read lazily, one CTA per sequence: only the
- * rows of the nodes the walk reaches.  A malformed or too deep tree makes every sequence
+ * out_path = node ids (may be NULL).  Rows are read lazily, one cluster of 1, 2 or 4 CTAs
+ * per sequence: only the rows of the nodes the walk reaches.  A malformed or too deep tree makes every sequence
  * -1; a token of b outside [0, V), or a row the walk reads that is not a distribution (NaN,
  * +inf, no finite entry), makes sequence b -1.  The walk decides in fp32 and marks the
  * sequences where one decision came within a few fp32 errors of flipping; two more kernels
