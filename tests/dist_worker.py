@@ -5,7 +5,6 @@ import os
 def run(rank, world, port, out_q):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
                       WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
-    import numpy as np
     import torch.distributed as dist
 
     import bench

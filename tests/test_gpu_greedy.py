@@ -4,11 +4,10 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 import speculative_decoding_verify_spec_gb300 as sv
 from speculative_decoding_verify_spec_gb300 import workloads as W
 
-from parity_util import host, oracle_greedy, oracle_tree
+from parity_util import oracle_greedy, oracle_tree
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"

@@ -3,7 +3,6 @@ host can read (and the context stays usable), and every verify entry point can b
 in a CUDA graph and replayed with the same results as an eager call."""
 import time
 
-import numpy as np
 import pytest
 import torch
 
