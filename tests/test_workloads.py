@@ -44,3 +44,51 @@ def test_tree_shape_counts():
 def test_logical_bytes_formula():
     assert W.logical_bytes("sample_b256") == 256 * 17 * 128256 * 2 + 4 * 256 * 8 + 4 * 256 * 10
     assert W.logical_bytes("greedy_b512") == 512 * 7 * 152064 * 2 + 4 * 512 * 6 + 4 * 512 * 8
+
+
+def test_metric_bytes_match_the_printed_sizes():
+    # the metric's bytes: every logit once plus the small integer inputs and outputs,
+    # against the sizes printed beside the five workloads (to their last printed digit)
+    assert W.logical_bytes("sample_b1") == 1 * 9 * 1000 * 4 + 4 * 4 + 4 * 6
+    assert abs(W.logical_bytes("sample_b64") / 1e6 - 45.06) < 0.01
+    assert abs(W.logical_bytes("sample_b256") / 1e9 - 1.1163) < 1e-4
+    assert abs(W.logical_bytes("greedy_b512") / 1e9 - 1.0900) < 1e-4
+    assert abs(W.logical_bytes("tree_b64") / 1e9 - 1.0507) < 1e-4
+
+
+def test_rows_and_target_only_bytes():
+    assert W.rows("sample_b256") == 256 * 17
+    assert W.rows("typical_b256") == W.rows("onehot_b256") == 256 * 9     # no draft rows
+    assert W.rows("greedy_b512") == 512 * 7 and W.rows("tree_b64") == 64 * 64
+    assert W.logical_bytes("typical_b256") == 256 * 9 * 128256 * 2 + 4 * 256 * 8 + 4 * 256 * 10
+    assert W.logical_bytes("onehot_b256") == W.logical_bytes("typical_b256")
+    assert W.logical_bytes("ngram_b256") == 256 * (16384 * 4 + 4 + 8 * 4 + 4)
+
+
+def test_tree_sample_children_are_distinct_draws():
+    s = W.make("tree_sample_b64", B=6, V=40)
+    par = s.parent.tolist()
+    assert s.target.shape == (6, 64, 40) and s.draft.shape == (6, 64, 40)
+    assert s.without_replacement and s.max_depth == 6
+    for v in range(64):
+        kids = [c for c in range(1, 64) if par[c] == v]
+        if len(kids) > 1:  # without replacement: siblings carry distinct tokens
+            toks = s.node_tokens[:, kids]
+            for b in range(6):
+                assert len(set(toks[b].tolist())) == len(kids)
+    assert ((s.node_tokens[:, 1:] >= 0) & (s.node_tokens[:, 1:] < 40)).all()
+
+
+def test_ngram_histories_are_ragged_and_copy_heavy():
+    g = W.make("ngram_b256", B=16, T=4096)
+    L = g.lengths
+    assert g.history.shape == (16, 4096) and g.history.dtype == torch.int32
+    assert ((L >= 4096 - 1024) & (L <= 4096)).all() and len(set(L.tolist())) > 1
+    assert ((g.history >= 0) & (g.history < 128256)).all()
+    # most tails have an earlier occurrence (the last span repeats earlier text w.p. 0.8)
+    hits = 0
+    for b in range(16):
+        h, n = g.history[b, :int(L[b])].tolist(), g.n
+        tail = h[-n:]
+        hits += any(h[i:i + n] == tail for i in range(len(h) - n))
+    assert hits >= 8
