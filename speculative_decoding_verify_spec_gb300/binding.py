@@ -119,12 +119,31 @@ def _logits3(t: torch.Tensor, name: str):
     return t.stride(0), t.stride(1)
 
 
-def _ints(t: torch.Tensor, name: str, shape) -> torch.Tensor:
+def _ints(t: torch.Tensor, name: str, shape, dev=None) -> torch.Tensor:
     if not t.is_cuda or t.dtype != torch.int32:
         raise ValueError(f"{name} must be an int32 CUDA tensor")
+    if dev is not None and t.device != dev:
+        raise ValueError(f"{name} must be on {dev}, got {t.device}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     return t.contiguous()
+
+
+def _out(t, name: str, shape, dev) -> torch.Tensor:
+    """A caller-provided int32 output, checked (the kernels write it in place), or a new one."""
+    if t is None:
+        return torch.empty(tuple(shape), dtype=torch.int32, device=dev)
+    if not t.is_cuda or t.device != dev or t.dtype != torch.int32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous int32 tensor on {dev}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _like(t: torch.Tensor, ref: torch.Tensor, name: str):
+    """A second logits tensor: on the target's device, with its dtype."""
+    if t.device != ref.device or t.dtype != ref.dtype:
+        raise ValueError(f"{name} must be on {ref.device} with dtype {ref.dtype}")
 
 
 def _stream(device) -> int:
@@ -139,6 +158,8 @@ def _workspace(mode, B, rows, V, dtype, device, workspace):
     n = spec_verify_workspace_size(mode, B, rows, V, dtype)
     if workspace is None:
         workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=device)
+    elif not workspace.is_cuda or workspace.device != device or not workspace.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {device}")
     elif workspace.numel() * workspace.element_size() < n:
         raise ValueError(f"workspace too small: need {n} bytes")
     return workspace, workspace.numel() * workspace.element_size()
@@ -155,19 +176,18 @@ def spec_verify_sample(target: torch.Tensor, draft: torch.Tensor, draft_tokens: 
     dt = _dtype_code(target)
     if gamma > 0:
         dsb, dsr = _logits3(draft, "draft")
-        if draft.dtype != target.dtype or tuple(draft.shape) != (B, gamma, V):
+        _like(draft, target, "draft")
+        if tuple(draft.shape) != (B, gamma, V):
             raise ValueError("draft must be [B, gamma, V] with the target's dtype")
         dptr = draft.data_ptr()
-        x = _ints(draft_tokens, "draft_tokens", (B, gamma))
+        x = _ints(draft_tokens, "draft_tokens", (B, gamma), target.device)
         xptr = x.data_ptr()
     else:
         dsb = dsr = 0
         dptr = xptr = None
     dev = target.device
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    accepted_len = _out(accepted_len, "accepted_len", (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", (B, G1), dev)
     ws, wsb = _workspace(MODE_SAMPLE, B, gamma, V, dt, dev, workspace)
     st = lib.spec_verify_sample(target.data_ptr(), tsb, tsr, dptr, dsb, dsr, dt, B, gamma, V, xptr,
                                 float(temperature), int(seed) & (2**64 - 1),
@@ -185,12 +205,10 @@ def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, *, work
     B, G1, V = target.shape
     gamma = G1 - 1
     dt = _dtype_code(target)
-    x = _ints(draft_tokens, "draft_tokens", (B, gamma)) if gamma > 0 else None
+    x = _ints(draft_tokens, "draft_tokens", (B, gamma), target.device) if gamma > 0 else None
     dev = target.device
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    accepted_len = _out(accepted_len, "accepted_len", (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", (B, G1), dev)
     ws, wsb = _workspace(MODE_GREEDY, B, gamma, V, dt, dev, workspace)
     st = lib.spec_verify_greedy(target.data_ptr(), tsb, tsr, dt, B, gamma, V,
                                 x.data_ptr() if x is not None else None, accepted_len.data_ptr(),
@@ -208,16 +226,14 @@ def spec_verify_tree_greedy(target: torch.Tensor, parent: torch.Tensor, node_tok
     tsb, tsr = _logits3(target, "target")
     B, N, V = target.shape
     dt = _dtype_code(target)
-    par = _ints(parent, "parent", (N,))
-    tok = _ints(node_tokens, "node_tokens", (B, N))
+    par = _ints(parent, "parent", (N,), target.device)
+    tok = _ints(node_tokens, "node_tokens", (B, N), target.device)
     dev = target.device
     W = int(max_depth) + 1
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, W), dtype=torch.int32, device=dev)
-    if with_path and out_path is None:
-        out_path = torch.empty((B, W), dtype=torch.int32, device=dev)
+    accepted_len = _out(accepted_len, "accepted_len", (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", (B, W), dev)
+    if with_path or out_path is not None:
+        out_path = _out(out_path, "out_path", (B, W), dev)
     ws, wsb = _workspace(MODE_TREE, B, N, V, dt, dev, workspace)
     st = lib.spec_verify_tree_greedy(target.data_ptr(), tsb, tsr, dt, B, N, V, par.data_ptr(),
                                      tok.data_ptr(), int(max_depth), accepted_len.data_ptr(),
@@ -240,18 +256,17 @@ def spec_verify_tree_sample(target: torch.Tensor, draft: torch.Tensor, parent: t
     dsb, dsr = _logits3(draft, "draft")
     B, N, V = target.shape
     dt = _dtype_code(target)
-    if draft.dtype != target.dtype or tuple(draft.shape) != (B, N, V):
+    _like(draft, target, "draft")
+    if tuple(draft.shape) != (B, N, V):
         raise ValueError("draft must be [B, N, V] with the target's dtype")
-    par = _ints(parent, "parent", (N,))
-    tok = _ints(node_tokens, "node_tokens", (B, N))
+    par = _ints(parent, "parent", (N,), target.device)
+    tok = _ints(node_tokens, "node_tokens", (B, N), target.device)
     dev = target.device
     W = int(max_depth) + 1
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, W), dtype=torch.int32, device=dev)
-    if with_path and out_path is None:
-        out_path = torch.empty((B, W), dtype=torch.int32, device=dev)
+    accepted_len = _out(accepted_len, "accepted_len", (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", (B, W), dev)
+    if with_path or out_path is not None:
+        out_path = _out(out_path, "out_path", (B, W), dev)
     ws, wsb = _workspace(MODE_TREE_SAMPLE, B, N, V, dt, dev, workspace)
     st = lib.spec_verify_tree_sample(target.data_ptr(), tsb, tsr, draft.data_ptr(), dsb, dsr, dt, B,
                                      N, V, par.data_ptr(), tok.data_ptr(), int(max_depth),
@@ -276,19 +291,18 @@ def spec_verify_sample_lazy(target: torch.Tensor, draft: torch.Tensor, draft_tok
     dt = _dtype_code(target)
     if gamma > 0:
         dsb, dsr = _logits3(draft, "draft")
-        if draft.dtype != target.dtype or tuple(draft.shape) != (B, gamma, V):
+        _like(draft, target, "draft")
+        if tuple(draft.shape) != (B, gamma, V):
             raise ValueError("draft must be [B, gamma, V] with the target's dtype")
         dptr = draft.data_ptr()
-        x = _ints(draft_tokens, "draft_tokens", (B, gamma))
+        x = _ints(draft_tokens, "draft_tokens", (B, gamma), target.device)
         xptr = x.data_ptr()
     else:
         dsb = dsr = 0
         dptr = xptr = None
     dev = target.device
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    accepted_len = _out(accepted_len, "accepted_len", (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", (B, G1), dev)
     ws, wsb = _workspace(MODE_SAMPLE_LAZY, B, gamma, V, dt, dev, workspace)
     st = lib.spec_verify_sample_lazy(target.data_ptr(), tsb, tsr, dptr, dsb, dsr, dt, B, gamma, V, xptr,
                                      float(temperature), int(seed) & (2**64 - 1),
@@ -310,13 +324,11 @@ def spec_verify_typical(target: torch.Tensor, draft_tokens: torch.Tensor, temper
     dt = _dtype_code(target)
     xptr = None
     if gamma > 0:
-        x = _ints(draft_tokens, "draft_tokens", (B, gamma))
+        x = _ints(draft_tokens, "draft_tokens", (B, gamma), target.device)
         xptr = x.data_ptr()
     dev = target.device
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    accepted_len = _out(accepted_len, "accepted_len", (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", (B, G1), dev)
     ws, wsb = _workspace(MODE_TYPICAL, B, gamma, V, dt, dev, workspace)
     st = lib.spec_verify_typical(target.data_ptr(), tsb, tsr, dt, B, gamma, V, xptr, float(temperature),
                                  float(epsilon), float(delta), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
@@ -337,13 +349,11 @@ def spec_verify_sample_onehot(target: torch.Tensor, draft_tokens: torch.Tensor, 
     dt = _dtype_code(target)
     xptr = None
     if gamma > 0:
-        x = _ints(draft_tokens, "draft_tokens", (B, gamma))
+        x = _ints(draft_tokens, "draft_tokens", (B, gamma), target.device)
         xptr = x.data_ptr()
     dev = target.device
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    accepted_len = _out(accepted_len, "accepted_len", (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", (B, G1), dev)
     ws, wsb = _workspace(MODE_SAMPLE_ONEHOT, B, gamma, V, dt, dev, workspace)
     st = lib.spec_verify_sample_onehot(target.data_ptr(), tsb, tsr, dt, B, gamma, V, xptr, float(temperature),
                                        int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), accepted_len.data_ptr(),
@@ -361,12 +371,10 @@ def spec_verify_greedy_lazy(target: torch.Tensor, draft_tokens: torch.Tensor, *,
     B, G1, V = target.shape
     gamma = G1 - 1
     dt = _dtype_code(target)
-    x = _ints(draft_tokens, "draft_tokens", (B, gamma)) if gamma > 0 else None
+    x = _ints(draft_tokens, "draft_tokens", (B, gamma), target.device) if gamma > 0 else None
     dev = target.device
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    accepted_len = _out(accepted_len, "accepted_len", (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", (B, G1), dev)
     st = lib.spec_verify_greedy_lazy(target.data_ptr(), tsb, tsr, dt, B, gamma, V,
                                      x.data_ptr() if x is not None else None, accepted_len.data_ptr(),
                                      out_tokens.data_ptr(), _stream(dev))
@@ -383,16 +391,14 @@ def spec_verify_tree_greedy_lazy(target: torch.Tensor, parent: torch.Tensor, nod
     tsb, tsr = _logits3(target, "target")
     B, N, V = target.shape
     dt = _dtype_code(target)
-    par = _ints(parent, "parent", (N,))
-    tok = _ints(node_tokens, "node_tokens", (B, N))
+    par = _ints(parent, "parent", (N,), target.device)
+    tok = _ints(node_tokens, "node_tokens", (B, N), target.device)
     dev = target.device
     W = int(max_depth) + 1
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, W), dtype=torch.int32, device=dev)
-    if with_path and out_path is None:
-        out_path = torch.empty((B, W), dtype=torch.int32, device=dev)
+    accepted_len = _out(accepted_len, "accepted_len", (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", (B, W), dev)
+    if with_path or out_path is not None:
+        out_path = _out(out_path, "out_path", (B, W), dev)
     st = lib.spec_verify_tree_greedy_lazy(target.data_ptr(), tsb, tsr, dt, B, N, V, par.data_ptr(),
                                           tok.data_ptr(), int(max_depth), accepted_len.data_ptr(),
                                           out_tokens.data_ptr(),
@@ -407,15 +413,13 @@ def spec_ngram_draft(history: torch.Tensor, lengths: torch.Tensor, n: int, k: in
     """Prompt-lookup drafts of a [B, T] int32 history with lengths [B]; returns (drafts
     [B, k] int32, -1 in unused slots, count [B] int32)."""
     lib = load_library()
-    if history.dim() != 2 or history.dtype != torch.int32 or history.stride(1) != 1:
-        raise ValueError("history must be a [B, T] int32 tensor with contiguous rows")
+    if not history.is_cuda or history.dim() != 2 or history.dtype != torch.int32 or history.stride(1) != 1:
+        raise ValueError("history must be a [B, T] int32 CUDA tensor with contiguous rows")
     B, T = history.shape
-    L = _ints(lengths, "lengths", (B,))
     dev = history.device
-    if drafts is None:
-        drafts = torch.empty((B, int(k)), dtype=torch.int32, device=dev)
-    if count is None:
-        count = torch.empty(B, dtype=torch.int32, device=dev)
+    L = _ints(lengths, "lengths", (B,), dev)
+    drafts = _out(drafts, "drafts", (B, max(int(k), 0)), dev)
+    count = _out(count, "count", (B,), dev)
     st = lib.spec_ngram_draft(history.data_ptr(), history.stride(0), L.data_ptr(), B, int(n), int(k),
                               int(bool(pad)), drafts.data_ptr(), count.data_ptr(), _stream(dev))
     _check(st, "spec_ngram_draft")
@@ -523,12 +527,10 @@ def spec_verify_greedy_noalloc(target: torch.Tensor, draft_tokens: torch.Tensor,
     B, G1, V = target.shape
     gamma = G1 - 1
     dt = _dtype_code(target)
-    x = _ints(draft_tokens, "draft_tokens", (B, gamma)) if gamma > 0 else None
+    x = _ints(draft_tokens, "draft_tokens", (B, gamma), target.device) if gamma > 0 else None
     dev = target.device
-    if accepted_len is None:
-        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
-    if out_tokens is None:
-        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    accepted_len = _out(accepted_len, "accepted_len", (B,), dev)
+    out_tokens = _out(out_tokens, "out_tokens", (B, G1), dev)
     st = lib.spec_verify_greedy_noalloc(target.data_ptr(), tsb, tsr, dt, B, gamma, V,
                                         x.data_ptr() if x is not None else None,
                                         accepted_len.data_ptr(), out_tokens.data_ptr(),

@@ -137,10 +137,45 @@ def test_uniform_hook_rejects_bad_purpose(lib):
 
 
 def test_binding_refuses_cpu_tensors():
+    """No entry has a CPU path: host tensors are refused before the library is called."""
     import torch
-    t = torch.zeros(1, 2, 8)
+    t = torch.zeros(2, 3, 8)
+    x = torch.zeros(2, 2, dtype=torch.int32)
+    tt = torch.zeros(2, 3, 8)
+    par = torch.tensor([-1, 0, 0], dtype=torch.int32)
+    tok = torch.zeros(2, 3, dtype=torch.int32)
+    calls = [
+        lambda: binding.spec_verify_greedy(t, x),
+        lambda: binding.spec_verify_sample(t, t[:, :2], x, 1.0, 0),
+        lambda: binding.spec_verify_tree_greedy(tt, par, tok, 1),
+        lambda: binding.spec_verify_tree_sample(tt, tt, par, tok, 1, 1.0, 0),
+        lambda: binding.spec_verify_sample_lazy(t, t[:, :2], x, 1.0, 0),
+        lambda: binding.spec_verify_greedy_lazy(t, x),
+        lambda: binding.spec_verify_tree_greedy_lazy(tt, par, tok, 1),
+        lambda: binding.spec_verify_typical(t, x, 1.0, 0.1, 0.3, 0),
+        lambda: binding.spec_verify_sample_onehot(t, x, 1.0, 0),
+        lambda: binding.spec_verify_greedy_noalloc(t, x),
+        lambda: binding.spec_verify_row_stats(t),
+        lambda: binding.spec_ngram_draft(torch.zeros(2, 16, dtype=torch.int32),
+                                         torch.full((2,), 16, dtype=torch.int32), 3, 4),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError):
+            call()
+
+
+def test_binding_checks_caller_provided_outputs():
+    """Outputs and workspaces passed in are written in place by the kernels, so anything
+    but a contiguous int32 tensor of the right shape on the call's device is refused."""
+    import torch
+    dev = torch.device("cuda", 0)
     with pytest.raises(ValueError):
-        binding.spec_verify_greedy(t, torch.zeros(1, 1, dtype=torch.int32))
+        binding._out(torch.zeros(4, dtype=torch.int32), "accepted_len", (4,), dev)   # host memory
+    assert binding._out(None, "x", (2, 3), torch.device("cpu")).shape == (2, 3)      # allocated when absent
+    with pytest.raises(ValueError):
+        binding._workspace(binding.MODE_GREEDY, 1, 1, 8, binding.FP32, dev, torch.zeros(1 << 16, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        binding._like(torch.zeros(1, 1, 4, dtype=torch.bfloat16), torch.zeros(1, 1, 4), "draft")
 
 
 def test_tree_sample_and_lazy_entries_reject_bad_arguments(lib):
