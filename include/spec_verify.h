@@ -54,7 +54,7 @@ typedef enum {
     SV_ERR_INVALID_ARG = 1, /* a size, stride, pointer or temperature is out of range */
     SV_ERR_UNSUPPORTED = 2, /* dtype or mode not supported */
     SV_ERR_CUDA = 3,        /* a CUDA launch failed; see cudaGetLastError semantics */
-    SV_ERR_TIMEOUT = 4,     /* reserved: a bounded device wait gave up */
+    SV_ERR_TIMEOUT = 4,     /* a bounded device wait gave up (re-draw status words) */
     SV_ERR_WORKSPACE = 5    /* workspace NULL, too small or not 16-byte aligned */
 } sv_status;
 
