@@ -277,7 +277,7 @@ def test_drafter_and_hooks_reject_bad_arguments(lib):
 
 def test_binding_constants_match_the_header():
     text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "spec_verify.h")).read(), flags=re.S)
-    values = {k: int(v) for k, v in re.findall(r"\b(SV_[A-Z_]+)\s*=\s*(\d+)", text)}
+    values = {k: int(v) for k, v in re.findall(r"\b(SV_[A-Z0-9_]+)\s*=\s*(\d+)", text)}
     assert values["SV_OK"] == binding.SV_OK
     assert (values["SV_FP32"], values["SV_BF16"]) == (binding.FP32, binding.BF16)
     for name in ("SAMPLE", "GREEDY", "TREE", "ROW_STATS", "TREE_SAMPLE", "SAMPLE_LAZY", "TYPICAL",
