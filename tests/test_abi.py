@@ -284,3 +284,14 @@ def test_binding_constants_match_the_header():
                  "SAMPLE_ONEHOT"):
         assert values["SV_MODE_" + name] == getattr(binding, "MODE_" + name), name
     assert values["SV_ERR_TIMEOUT"] == 4  # the status the bounded-wait test expects
+
+
+def test_package_exports_every_entry_point():
+    import speculative_decoding_verify_spec_gb300 as sv
+    public = [n for n in dir(binding) if n.startswith(("spec_verify_", "spec_ngram_"))
+              and n not in ("spec_verify_exp_df", "spec_verify_uniforms")]
+    hooks = {"spec_verify_exp_df"}  # test hooks stay in the binding module
+    for n in public:
+        assert n in sv.__all__ or n in hooks, n
+    for n in sv.__all__:
+        assert hasattr(sv, n), n
