@@ -51,3 +51,26 @@ def test_hbm_peak_reads_measured_file():
             assert peak == float(json.load(f)["hbm_gbs"]) and kind == "measured"
     else:
         assert (peak, kind) == (bench.FALLBACK_HBM_GBS, "fallback")
+
+
+def test_oracle_legs_run_every_workload():
+    """The CPU legs (cpu_baseline, --impl reference) call the oracle's rule for each
+    workload: small versions of every one run, and report a histogram and flags where the
+    rule has them."""
+    from speculative_decoding_verify_spec_gb300 import workloads as W
+    import __graft_entry__
+
+    __graft_entry__._build_oracle()
+    for name in W.WORKLOADS:
+        mode = W.WORKLOADS[name]["mode"]
+        ov = {"B": 3, "T": 600} if mode == "ngram" else {"B": 3, "V": 300}
+        inputs = W.make(name, device="cpu", **ov)
+        B, used, acc, flags = bench.oracle_run(name, inputs, 2)
+        assert B == 3 and 1 <= used <= 2, name
+        if mode == "ngram":
+            assert acc is None and flags is None
+            continue
+        assert acc.shape == (3,) and (acc >= -1).all(), name
+        out = bench.oracle_acceptance(acc, flags)
+        assert sum(out["accepted_len_hist"]) + out["invalid"] == 3, name
+        assert ("oracle_flags" in out) == (mode != "greedy"), name
