@@ -45,7 +45,7 @@ DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "max_tiles_kernel",
                    "typical": "typical_walk_kernel", "onehot": "typical_walk_kernel"}
 STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
 ACCEPT_STEPS = 16  # untimed steps whose accepted lengths and re-draw counts are read back
-STAGES = {"sample": ["row_stats", "decide", "residual_mass", "inverse_cdf", "redraw"],
+STAGES = {"sample": ["row_stats", "decide", "residual_mass", "draw_redraw"],
           "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"], "tree_sample": ["walk", "rewalk_exp", "rewalk"],
           "sample_lazy": ["walk", "rewalk_exp", "rewalk"], "greedy_lazy": ["walk"], "tree_lazy": ["walk"], "ngram": ["draft"],
           "typical": ["walk", "redraw_exp", "redraw"], "onehot": ["walk", "redraw_exp", "redraw"]}
@@ -251,7 +251,7 @@ def make_call(name, inputs, dev, **ov):
             return sv.spec_verify_typical(target, tokens, inputs.temperature, cfg["epsilon"], cfg["delta"],
                                           inputs.seed, step_counter[0], workspace=ws, accepted_len=acc,
                                           out_tokens=out)
-        call.redraw_state = lambda: binding.walk_redraw_state(ws, binding.MODE_TYPICAL, B, g, V, dt)[:3]
+        call.redraw_state = lambda: binding.call_status(ws, binding.MODE_TYPICAL, B, g, V, dt)[:3]
         return call, (acc, out)
     if mode == "sample" and cfg.get("onehot"):
         g = cfg["gamma"]
@@ -265,7 +265,7 @@ def make_call(name, inputs, dev, **ov):
             step_counter[0] += 1
             return sv.spec_verify_sample_onehot(target, tokens, inputs.temperature, inputs.seed, step_counter[0],
                                                 workspace=ws, accepted_len=acc, out_tokens=out)
-        call.redraw_state = lambda: binding.walk_redraw_state(ws, binding.MODE_SAMPLE_ONEHOT, B, g, V, dt)[:3]
+        call.redraw_state = lambda: binding.call_status(ws, binding.MODE_SAMPLE_ONEHOT, B, g, V, dt)[:3]
         return call, (acc, out)
     if mode == "sample" and lazy:
         g = cfg["gamma"]
@@ -280,7 +280,7 @@ def make_call(name, inputs, dev, **ov):
             return sv.spec_verify_sample_lazy(target, draft, tokens, inputs.temperature, inputs.seed,
                                               step_counter[0], workspace=ws, accepted_len=acc,
                                               out_tokens=out)
-        call.redraw_state = lambda: binding.walk_redraw_state(ws, binding.MODE_SAMPLE_LAZY, B, g, V, dt)[:3]
+        call.redraw_state = lambda: binding.call_status(ws, binding.MODE_SAMPLE_LAZY, B, g, V, dt)[:3]
         return call, (acc, out)
     if mode == "greedy" and lazy:
         g = cfg["gamma"]
@@ -313,10 +313,7 @@ def make_call(name, inputs, dev, **ov):
                                          step_counter[0], workspace=ws, accepted_len=acc,
                                          out_tokens=out)
 
-        def chain_state():  # the re-draw takes the first 32 marked sequences (the library's list)
-            m, status = binding.sample_redraw_state(ws, B, g, V, dt)
-            return m, min(m, 32), status
-        call.redraw_state = chain_state
+        call.redraw_state = lambda: binding.call_status(ws, binding.MODE_SAMPLE, B, g, V, dt)[:3]
         return call, (acc, out)
     if mode == "greedy":
         g = cfg["gamma"]
@@ -345,7 +342,7 @@ def make_call(name, inputs, dev, **ov):
                                               without_replacement=inputs.without_replacement,
                                               workspace=ws, accepted_len=acc, out_tokens=out,
                                               out_path=path)
-        call.redraw_state = lambda: binding.walk_redraw_state(ws, binding.MODE_TREE_SAMPLE, B, N, V, dt)[:3]
+        call.redraw_state = lambda: binding.call_status(ws, binding.MODE_TREE_SAMPLE, B, N, V, dt)[:3]
         return call, (acc, out, path)
     ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_TREE, B, N, V, dt),
                      dtype=torch.uint8, device=dev)

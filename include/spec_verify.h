@@ -34,9 +34,14 @@
  *     token of that sequence = -1.  Other sequences are unaffected.
  *   - `workspace` is caller-provided device scratch of at least
  *     spec_verify_workspace_size(...) bytes, 16-byte aligned.  Its contents need no
- *     initialisation.  After the call only the re-draw counts that the test hooks
- *     spec_verify_sample_redraw_offset / spec_verify_walk_redraw_offset locate mean
- *     anything.  Calls that run concurrently need distinct workspaces.
+ *     initialisation.  After the call only the status words that spec_verify_status_offset
+ *     locates mean anything.  Calls that run concurrently need distinct workspaces.
+ *   - The sampling entries decide in fp32 and redo EVERY sequence whose fp32 decision came
+ *     near enough to its boundary to be in doubt in double-float arithmetic (~48 bits), so
+ *     their result is the exact rule's except where a comparison's exact margin is below
+ *     ~1e-12 relative.  Their device-side outcome (sequences marked, sequences redone, and a
+ *     status that is SV_OK unless a bounded device wait gave up) is in the workspace at
+ *     spec_verify_status_offset once the stream has completed.
  *   - A round emits accepted_len[b] + 1 tokens (always >= 1) [SD "Extending to a chain"].
  */
 #ifndef SPEC_VERIFY_H
@@ -175,13 +180,13 @@ sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_str
  * -1; a token of b outside [0, V), or a row the walk reads that is not a distribution (NaN,
  * +inf, no finite entry), makes sequence b -1.  The walk decides in fp32 and marks the
  * sequences where one decision came within a few fp32 errors of flipping; two more kernels
- * walk the marked ones again (the first 8 per call, in index order) in double-float
- * arithmetic and rewrite their outputs, so the result is the exact rule's except where a
- * decision is closer than ~1e-12 to its boundary (spec_verify_walk_redraw_offset).
- * Workspace: spec_verify_workspace_size(SV_MODE_TREE_SAMPLE, B, N, V, dtype) bytes, about
- * 128 V min(N, 8) bytes: the re-walk keeps the double-float exponentials of the rows of up
- * to 8 reached nodes for each of 8 sequences (115 MB at N = 64, V = 128256 with
- * max_depth = 6 needing 7 of the 8 positions; the size assumes 8).
+ * walk every marked one again in double-float arithmetic and rewrite its outputs, so the
+ * result is the exact rule's except where a decision is closer than ~1e-12 to its boundary
+ * (spec_verify_status_offset).  Workspace: spec_verify_workspace_size(SV_MODE_TREE_SAMPLE,
+ * B, N, V, dtype) bytes, about 128 V min(N, 8) bytes: eight clusters re-walk the marked
+ * sequences, the first eight with the double-float exponentials of up to 8 reached nodes
+ * precomputed by the whole grid (115 MB at N = 64, V = 128256 with max_depth = 6 needing 7
+ * of the 8 positions; the size assumes 8), later ones computing them in the cluster.
  */
 sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_stride,
                                   int64_t t_row_stride, const void *draft_logits,
@@ -244,11 +249,11 @@ sv_status spec_verify_tree_greedy_lazy(const void *target_logits, int64_t t_batc
  *   target gives positive probability).
  * Outputs as spec_verify_sample.  Rows are read lazily, one CTA per sequence: rows 0 .. k
  * only; a token outside [0, V) or a row read that is not a distribution gives -1.  The
- * accept tests are taken in fp32; a final draw whose threshold lies within 1e-6 of the row's
- * mass from a CDF boundary is redone in double-float arithmetic (the first 8 per call, by
- * two more kernels; spec_verify_walk_redraw_offset with SV_MODE_TYPICAL reports them).
- * Workspace: spec_verify_workspace_size(SV_MODE_TYPICAL, B, gamma, V, dtype) bytes (~128 V
- * bytes of re-draw scratch plus 4 bytes per 1024 logits per sequence).
+ * accept tests are taken in fp32; every final draw whose threshold lies within 1e-6 of the
+ * row's mass from a CDF boundary is redone in double-float arithmetic by two more kernels
+ * (spec_verify_status_offset with SV_MODE_TYPICAL reports them).  Workspace:
+ * spec_verify_workspace_size(SV_MODE_TYPICAL, B, gamma, V, dtype) bytes (per sequence 4
+ * bytes per 1024 logits and 8 bytes per 256 logits of re-draw unit sums).
  */
 sv_status spec_verify_typical(const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride,
                               sv_dtype dtype, int B, int gamma, int V, const int32_t *draft_tokens,
@@ -340,44 +345,33 @@ sv_status spec_verify_uniforms(uint64_t seed, uint64_t offset, int B, int positi
                                int purpose, float *out, void *stream);
 
 /*
- * Test hook: where spec_verify_sample keeps its re-draw bookkeeping inside a sampling
- * workspace of these sizes (byte offset of an int32 array, (size_t)-1 for bad sizes).
- *   [0] sequences the last call marked for the extended-precision re-draw: a draw whose
- *       threshold u'R lies within 2e-7 R (a bonus draw) or 6e-8 R (a residual draw) of a
- *       CDF boundary, or an accept test with
- *       |u q - p| < 1e-6 max(p, u q) -- the comparisons fp32 could get wrong
- *       ("The rule"; readings R2, R3).  At most 32 per call are redone; the rest keep the
- *       fp32 result.
- *   [3] SV_ERR_TIMEOUT if the re-draw gave up on a grid barrier (else 0).
- * Read it after the call's stream has completed.
+ * Where a sampling call keeps its device-side outcome inside its workspace: the byte offset
+ * of an int32 array ((size_t)-1 for a mode without one -- greedy, tree greedy, row
+ * statistics -- or bad sizes).  Modes and rows as spec_verify_workspace_size:
+ * SV_MODE_SAMPLE, SV_MODE_TREE_SAMPLE, SV_MODE_SAMPLE_LAZY, SV_MODE_TYPICAL and
+ * SV_MODE_SAMPLE_ONEHOT.  Read it after the call's stream has completed:
+ *   [0]      sequences the call marked: an fp32 decision near enough to its boundary to be
+ *            in doubt -- an accept test with |u q - p| below 1e-6 of max(p, u q) (plus, for
+ *            the tree walk, the size of p's terms), a draw whose threshold lies within a few
+ *            1e-8 .. 1e-6 of the draw's total mass from a CDF boundary, a residual mass or a
+ *            remaining q mass too small to trust, or a rounding fallback ("The rule";
+ *            readings R2, R3, R14);
+ *   [3]      SV_OK, or SV_ERR_TIMEOUT if a bounded wait of the chain re-draw gave up (2 s:
+ *            only when the GPU cannot hold its grid, e.g. another kernel holds every SM) --
+ *            the sequences it did not finish keep their fp32 result;
+ *   [4]      sequences redone in double-float arithmetic (equal to [0] unless [3] is set);
+ *   [8 + b]  nonzero if sequence b was marked.
  */
-size_t spec_verify_sample_redraw_offset(int B, int gamma, int V, sv_dtype dtype);
+size_t spec_verify_status_offset(sv_mode mode, int B, int rows, int V, sv_dtype dtype);
 
 /*
- * Test hook: where spec_verify_tree_sample (mode SV_MODE_TREE_SAMPLE, rows = N),
- * spec_verify_sample_lazy (SV_MODE_SAMPLE_LAZY, rows = gamma), spec_verify_typical
- * (SV_MODE_TYPICAL) and spec_verify_sample_onehot (SV_MODE_SAMPLE_ONEHOT; rows = gamma;
- * their marks are near-boundary final draws, their record length 1) keep their re-walk / re-draw bookkeeping inside a workspace of these sizes:
- * the byte offset of an int32 array
- * ((size_t)-1 for another mode or bad sizes), read after the call's stream has completed:
- *   [0] sequences the last call marked: an accept test with |u q - p| below 1e-6 of
- *       max(p, u q) plus the size of p's terms, a residual mass below 1e-6 (1 + A), less
- *       than 1e-5 of q's mass left, or a final draw whose threshold lies within 3e-7 of
- *       the draw's total mass from a CDF boundary (A: the walk's rejection coefficient;
- *       p after r rejections is max(p0 - A q0, 0) normalised);
- *   [3] 0 (no wait of the re-walk can time out: it meets at hardware cluster barriers);
- *   [4] sequences re-walked (the first 8 marked);
- *   [8 + b] 1 if sequence b was marked, else 0;
- *   [8 + B + b] nodes of sequence b's walk recorded for the re-walk (at most 8).
- */
-size_t spec_verify_walk_redraw_offset(sv_mode mode, int B, int rows, int V, sv_dtype dtype);
-
-/*
- * Test hook of the one software wait (the re-draw's bounded grid barrier): one CTA meets
- * the barrier expecting expected_arrivals (1 or 2) CTAs.  With 2 nobody else arrives: the
- * wait gives up after limit_us (at most 5 s) and writes SV_ERR_TIMEOUT to ctl[3]; with 1 it
- * passes at once and ctl[3] is 0.  ctl: a device int32 array of 8 the call overwrites.
- * The kernel returns either way, so the context stays usable.
+ * Test hook of the library's software waits (the chain re-draw's bounded wait for a flag
+ * another warp sets, and the bounded grid barrier): one CTA waits for a flag and then meets
+ * the barrier expecting expected_arrivals (1 or 2) CTAs.  With 1 the CTA sets the flag
+ * itself and passes both at once (ctl[3] = 0).  With 2 nobody sets the flag and nobody
+ * else arrives: each wait gives up after limit_us (at most 5 s) and SV_ERR_TIMEOUT is
+ * written to ctl[3].  ctl: a device int32 array of 8 the call overwrites.  The kernel
+ * returns either way, so the context stays usable.
  */
 sv_status spec_verify_wait_selftest(int *ctl, int expected_arrivals, uint32_t limit_us, void *stream);
 
@@ -394,8 +388,9 @@ sv_status spec_verify_exp_df(const float *y_hi, const float *y_lo, int n, float 
  * spec_verify_sample / _greedy / _tree_greedy / _tree_sample / _sample_lazy / _typical /
  * _sample_onehot on this thread
  * records events[0] on its stream before its first kernel and events[s] after its s-th
- * kernel (s = 1 .. n_events-1; sampling has 5 kernels: row statistics, decide, residual
- * masses, inverse-CDF draw, extended-precision re-draw of near-boundary sequences; greedy
+ * kernel (s = 1 .. n_events-1; sampling has 4 kernels: row statistics, decide, residual
+ * masses, and the inverse-CDF draw with the extended-precision re-draw of near-boundary
+ * sequences (one cooperative grid); greedy
  * and tree have 2: tile maxima, finalize; tree sampling and lazy sampling have 3: the
  * walk, the re-walk's exponentials, the re-walk; typical acceptance and one-hot sampling
  * have 3: the walk, the re-draw's exponentials, the re-draw).  The events are cudaEvent_t handles created and owned by the

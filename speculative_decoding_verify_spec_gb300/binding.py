@@ -79,10 +79,8 @@ def load_library() -> ctypes.CDLL:
         lib.spec_verify_uniforms.restype = i32
         lib.spec_verify_greedy_noalloc.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, P, P]
         lib.spec_verify_greedy_noalloc.restype = i32
-        lib.spec_verify_sample_redraw_offset.argtypes = [i32, i32, i32, i32]
-        lib.spec_verify_sample_redraw_offset.restype = sz
-        lib.spec_verify_walk_redraw_offset.argtypes = [i32, i32, i32, i32, i32]
-        lib.spec_verify_walk_redraw_offset.restype = sz
+        lib.spec_verify_status_offset.argtypes = [i32, i32, i32, i32, i32]
+        lib.spec_verify_status_offset.restype = sz
         lib.spec_verify_wait_selftest.argtypes = [P, i32, ctypes.c_uint32, P]
         lib.spec_verify_wait_selftest.restype = i32
         lib.spec_verify_exp_df.argtypes = [P, P, i32, P, P, P]
@@ -453,25 +451,13 @@ def spec_verify_uniforms(seed: int, offset: int, B: int, positions: int, purpose
     return out
 
 
-def sample_redraw_state(workspace: torch.Tensor, B: int, gamma: int, V: int, dtype: int):
-    """Test hook: (sequences marked for the extended-precision re-draw by the last sampling
-    call that used `workspace`, status of that re-draw); synchronises the device."""
+def call_status(workspace: torch.Tensor, mode: int, B: int, rows: int, V: int, dtype: int):
+    """The device-side outcome of the last sampling call (mode MODE_SAMPLE, MODE_TREE_SAMPLE,
+    MODE_SAMPLE_LAZY, MODE_TYPICAL or MODE_SAMPLE_ONEHOT; rows as for the workspace size)
+    that used `workspace`: (sequences marked for the extended-precision pass, sequences
+    redone, status, per-sequence marks as a numpy array).  Synchronises the device."""
     lib = load_library()
-    off = lib.spec_verify_sample_redraw_offset(B, gamma, V, dtype)
-    if off == ctypes.c_size_t(-1).value:
-        raise ValueError("bad sizes")
-    torch.cuda.synchronize(workspace.device)
-    words = workspace.view(torch.uint8)[off:off + 16].clone().view(torch.int32).cpu()
-    return int(words[0]), int(words[3])
-
-
-def walk_redraw_state(workspace: torch.Tensor, mode: int, B: int, rows: int, V: int, dtype: int):
-    """Test hook: the re-walk bookkeeping of the last tree-sampling (mode MODE_TREE_SAMPLE,
-    rows = N) or lazy sampling (MODE_SAMPLE_LAZY, rows = gamma) call that used `workspace`:
-    (sequences marked, sequences re-walked, status, per-sequence marks as a numpy array);
-    synchronises the device."""
-    lib = load_library()
-    off = lib.spec_verify_walk_redraw_offset(mode, B, rows, V, dtype)
+    off = lib.spec_verify_status_offset(mode, B, rows, V, dtype)
     if off == ctypes.c_size_t(-1).value:
         raise ValueError("bad mode or sizes")
     torch.cuda.synchronize(workspace.device)
@@ -480,8 +466,9 @@ def walk_redraw_state(workspace: torch.Tensor, mode: int, B: int, rows: int, V: 
 
 
 def wait_selftest(expected_arrivals: int, limit_us: int, device="cuda:0") -> int:
-    """Test hook: run the re-draw's bounded grid barrier in one CTA expecting
-    `expected_arrivals` CTAs; returns the status word it leaves (4 = SV_ERR_TIMEOUT)."""
+    """Test hook: one CTA waits for a flag (set by itself when expected_arrivals is 1) and
+    meets the bounded grid barrier expecting `expected_arrivals` CTAs; returns the status
+    word it leaves (4 = SV_ERR_TIMEOUT)."""
     lib = load_library()
     ctl = torch.zeros(8, dtype=torch.int32, device=device)
     _check(lib.spec_verify_wait_selftest(ctl.data_ptr(), int(expected_arrivals), int(limit_us),

@@ -22,10 +22,6 @@ int res_tile_elems(sv_dtype d) {
 }
 int ntile_of(int V, sv_dtype d) { return int((int64_t(V) + tile_elems(d) - 1) / tile_elems(d)); }
 int nrt_of(int V, sv_dtype d) { return int((int64_t(V) + res_tile_elems(d) - 1) / res_tile_elems(d)); }
-int nref_of(int V, sv_dtype d) {
-    const int64_t ue = sv::refine_unit_elems(d == SV_BF16 ? 1 : 0);
-    return int((int64_t(V) + ue - 1) / ue);
-}
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // 16-byte vector loads are legal when the base and both strides keep every row aligned.
@@ -36,7 +32,7 @@ bool vec_ok(const void *p, int64_t sb, int64_t sr, sv_dtype d) {
 
 struct Layout {
     size_t partial = 0, rowstat = 0, plan = 0, csum = 0;
-    size_t rflag = 0, rctl = 0, rlist = 0, rsum = 0, ramb = 0;  // re-draw (sampling)
+    size_t rctl = 0, rbar = 0, rlist = 0, rsum = 0, ramb = 0, rresc = 0;  // re-draw: control + marks, barrier, records, scratch
     size_t rec = 0, et = 0, us = 0, npos = 0, um = 0, pmax = 0, pcnt = 0;  // re-walk (tree sampling; rctl, rsum too)
     size_t total = 0;
 };
@@ -47,8 +43,13 @@ struct Layout {
 //   rowstat  per row: float2 (M, S)                             (sampling only)
 //   plan     per sequence: int2 (stop row k, mode)              (sampling only)
 //   csum     per (sequence, 2 KB residual tile): residual mass  (sampling only)
-//   rflag, rctl, rlist (RefineInfo records), rsum, ramb: the extended-precision re-draw of near-boundary
-//            sequences (sampling only; see sv_internal.h)
+//   rctl     the re-draw's control words, then the per-sequence marks rflag[B];
+//   rbar     the words of the re-draw's grid barrier;
+//   rlist    2 B RefineInfo records (main list, rescan list);
+//   rsum, ramb, rresc  the re-draw's scratch: per main-list sequence 5 x refine_units(V)
+//            double-float unit sums and refine_units(V) near-logit counts; kRescanChunk x
+//            (2 gamma + 1) x refine_units(V) unit sums for the rescan list (sampling only; see
+//            sv_internal.h): the re-draw of every near-boundary sequence
 // Tree sampling and lazy sampling: the walk's unit masses (partial) and per-CTA row
 // statistics (rowstat), then the re-walk's control block, marks and record lengths (rctl),
 // records (rec), stored exponentials and their unit sums (et, us), support counts (npos),
@@ -87,10 +88,11 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
         off += up256((size_t(sv::kTrCtlWords) + 2 * size_t(B)) * 4);
         L.rec = off;
         off += up256(size_t(B) * K * 16);
+        const bool per_seq = mode == SV_MODE_TYPICAL || mode == SV_MODE_SAMPLE_ONEHOT;  // unit sums per sequence
         L.et = off;
-        off += up256(S * K * 2 * size_t(V) * 8);
+        off += per_seq ? 0 : up256(S * K * 2 * size_t(V) * 8);
         L.us = off;
-        off += up256(S * K * 2 * nu * 8);
+        off += up256(per_seq ? size_t(B) * nu * 8 : S * K * 2 * nu * 8);
         L.npos = off;
         off += up256(S * K * 4);
         L.um = off;
@@ -115,17 +117,19 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
         off += up256(size_t(B) * 8);
         L.csum = off;
         off += up256(size_t(B) * size_t(nrt_of(V, dtype)) * 4);
-        const size_t nref = size_t(nref_of(V, dtype));
-        L.rflag = off;
-        off += up256(size_t(B) * 4);
         L.rctl = off;
+        off += up256((size_t(sv::kRefineCtlWords) + size_t(B)) * 4);
+        L.rbar = off;
         off += up256(size_t(sv::kRefineCtlWords) * 4);
         L.rlist = off;
-        off += up256(size_t(sv::kMaxRefine) * sizeof(sv::RefineInfo));
+        off += up256(size_t(2) * B * sizeof(sv::RefineInfo));
+        const size_t nu = size_t(sv::refine_units(V));
         L.rsum = off;
-        off += up256(size_t(sv::kMaxRefine) * size_t(sv::slot_df_entries(rows, int(nref))) * 8);
+        off += up256(size_t(B) * 5 * nu * 8);
         L.ramb = off;
-        off += up256(size_t(sv::kMaxRefine) * size_t(sv::slot_amb_ints(rows)) * 4);
+        off += up256(size_t(B) * nu * 4);
+        L.rresc = off;
+        off += up256(size_t(sv::kRescanChunk) * (size_t(2) * rows + 1) * nu * 8);
     }
     L.total = off;
     return L;
@@ -232,26 +236,23 @@ sv_status spec_verify_sample(const void *target_logits, int64_t t_batch_stride,
     if (e == cudaSuccess)
         e = sv::launch_stats_tiles(dt, vec, t, gamma + 1, d, R, B, V, ntile, c, partial, s);
     if (e == cudaSuccess) e = mark(1, s);
-    int *rflag = reinterpret_cast<int *>(at(workspace, L.rflag));
     int *rctl = reinterpret_cast<int *>(at(workspace, L.rctl));
+    int *rflag = rctl + sv::kRefineCtlWords;
+    int *rbar = reinterpret_cast<int *>(at(workspace, L.rbar));
     sv::RefineInfo *rinfo = reinterpret_cast<sv::RefineInfo *>(at(workspace, L.rlist));
     if (e == cudaSuccess)
         e = sv::launch_decide(dt, t, d, B, gamma, V, ntile, c, draft_tokens, seed, offset, partial,
-                              rowstat, plan, accepted_len, out_tokens, rflag, rctl, s);
+                              rowstat, plan, accepted_len, out_tokens, rflag, rctl, rbar, s);
     if (e == cudaSuccess) e = mark(2, s);
     if (e == cudaSuccess && gamma > 0)
         e = sv::launch_residual_tiles(dt, vec, t, d, B, gamma, V, nrt, c, rowstat, plan, csum, s);
     if (e == cudaSuccess) e = mark(3, s);
     if (e == cudaSuccess)
-        e = sv::launch_draw(dt, vec, t, d, B, gamma, V, ntile, nrt, c, seed, offset, partial, rowstat,
-                            plan, csum, out_tokens, rflag, rctl, rinfo,
-                            reinterpret_cast<int *>(at(workspace, L.ramb)), gamma > 0, s);
+        e = sv::launch_draw_refine(dt, vec, t, d, B, gamma, V, ntile, nrt, c, temperature, seed, offset, draft_tokens,
+                                   partial, rowstat, plan, csum, accepted_len, out_tokens, rctl, rbar, rinfo,
+                                   at(workspace, L.rsum), reinterpret_cast<int *>(at(workspace, L.ramb)),
+                                   at(workspace, L.rresc), gamma > 0, s);
     if (e == cudaSuccess) e = mark(4, s);
-    if (e == cudaSuccess)
-        e = sv::launch_refine(dt, vec, t, d, B, gamma, V, nref_of(V, dtype), temperature, seed, offset,
-                              draft_tokens, rowstat, plan, rctl, rinfo, at(workspace, L.rsum), at(workspace, L.ramb),
-                              accepted_len, out_tokens, s);
-    if (e == cudaSuccess) e = mark(5, s);
     return cuda_status(e);
 }
 
@@ -357,7 +358,7 @@ sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_str
                                    reinterpret_cast<float2 *>(at(workspace, L.rowstat)), rw, K, accepted_len,
                                    out_tokens, out_path, s);
     if (e == cudaSuccess) e = mark(1, s);
-    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, rw, s);
+    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, false, rw, s);
     if (e == cudaSuccess) e = mark(2, s);
     if (e == cudaSuccess)
         e = sv::launch_tree_rewalk(dtype == SV_BF16, t, d, B, N, V, false, parent, node_tokens, max_depth, temperature,
@@ -397,7 +398,7 @@ sv_status spec_verify_sample_lazy(const void *target_logits, int64_t t_batch_str
                                    reinterpret_cast<float2 *>(at(workspace, L.rowstat)), rw, K, accepted_len,
                                    out_tokens, nullptr, s);
     if (e == cudaSuccess) e = mark(1, s);
-    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, rw, s);
+    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, false, rw, s);
     if (e == cudaSuccess) e = mark(2, s);
     if (e == cudaSuccess)
         e = sv::launch_tree_rewalk(dtype == SV_BF16, t, d, B, gamma + 1, V, true, nullptr, draft_tokens, gamma,
@@ -438,9 +439,9 @@ sv_status target_walk(int onehot, const void *target_logits, int64_t t_batch_str
                                seed, offset, nrt_of(V, dtype), reinterpret_cast<float *>(at(workspace, L.partial)), rw,
                                accepted_len, out_tokens, s);
     if (e == cudaSuccess) e = mark(1, s);
-    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, t, B, V, temperature, 1, rw, s);
+    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, t, B, V, temperature, 1, true, rw, s);
     if (e == cudaSuccess) e = mark(2, s);
-    if (e == cudaSuccess) e = sv::launch_typical_redraw(B, gamma, V, seed, offset, rw, out_tokens, s);
+    if (e == cudaSuccess) e = sv::launch_typical_redraw(dtype == SV_BF16, t, B, gamma, V, temperature, seed, offset, rw, out_tokens, s);
     if (e == cudaSuccess) e = mark(3, s);
     return cuda_status(e);
 }
@@ -543,16 +544,10 @@ sv_status spec_verify_row_stats(const void *logits, int64_t batch_stride, int64_
     return cuda_status(e);
 }
 
-size_t spec_verify_sample_redraw_offset(int B, int gamma, int V, sv_dtype dtype) {
-    if (B <= 0 || gamma < 0 || V <= 0 || !dtype_ok(dtype)) return size_t(-1);
-    return layout(SV_MODE_SAMPLE, B, gamma, V, dtype).rctl;
-}
-
-size_t spec_verify_walk_redraw_offset(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
-    if ((mode != SV_MODE_TREE_SAMPLE && mode != SV_MODE_SAMPLE_LAZY && mode != SV_MODE_TYPICAL &&
-         mode != SV_MODE_SAMPLE_ONEHOT) || B <= 0 ||
-        rows < 0 || V <= 0 ||
-        !dtype_ok(dtype))
+size_t spec_verify_status_offset(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
+    if ((mode != SV_MODE_SAMPLE && mode != SV_MODE_TREE_SAMPLE && mode != SV_MODE_SAMPLE_LAZY &&
+         mode != SV_MODE_TYPICAL && mode != SV_MODE_SAMPLE_ONEHOT) ||
+        B <= 0 || rows < 0 || V <= 0 || !dtype_ok(dtype))
         return size_t(-1);
     return layout(mode, B, rows, V, dtype).rctl;
 }

@@ -149,9 +149,13 @@ static __constant__ float2 kExp2Sixteenths[16] = {
     {0x1.ea4afap+0f, 0x1.52486cp-27f},
 };
 
-// exp(y) for -87 <= y <= 0 (see the header comment); 0 below -87.
-__device__ __forceinline__ df exp_df(df y) {
-    if (!(y.hi >= -87.f)) return df{0.f, 0.f};
+// exp(y) for -87 <= y <= 0 (see the header comment); 0 below -87.  Branch-free (the argument
+// is clamped and the result selected at the end), so the independent exponentials of a
+// thread interleave in the instruction stream.  tab(j) returns 2^(j/16) as (hi, lo).
+template <class Tab>
+__device__ __forceinline__ df exp_df_core(df y, Tab tab) {
+    const bool live = y.hi >= -87.f;
+    if (!live) y = df{-87.f, 0.f};
     constexpr float k16InvLn2 = 0x1.715476p+4f;
     // ln2 / 16 = C1 + C2 + C3; C1 has 13 significant bits and |kk| < 2^11, so kk * C1 is exact
     constexpr float kC1 = 0x1.62ep-5f, kC2 = 0x1.0bfbe8p-19f, kC3 = 0x1.cf79acp-44f;
@@ -172,17 +176,34 @@ __device__ __forceinline__ df exp_df(df y) {
     e = df_add(r, e);
     e = df_add(df_from(1.f), e);
     const int ki = int(kk);
-    const float2 tj = kExp2Sixteenths[ki & 15];
+    const float2 tj = tab(ki & 15);
     e = df_mul(e, df{tj.x, tj.y});
     const float scale = __int_as_float(((ki >> 4) + 127) << 23);  // 2^floor(kk/16) >= 2^-126
-    return df{__fmul_rn(e.hi, scale), __fmul_rn(e.lo, scale)};
+    return live ? df{__fmul_rn(e.hi, scale), __fmul_rn(e.lo, scale)} : df{0.f, 0.f};
+}
+__device__ __forceinline__ df exp_df(df y) {
+    return exp_df_core(y, [](int j) { return kExp2Sixteenths[j]; });
+}
+// The same value with the table fetched by warp shuffles instead of divergent constant
+// loads: every lane of the warp calls it together; tj = kExp2Sixteenths[lane & 15].
+__device__ __forceinline__ df exp_df_warp(df y, float2 tj) {
+    return exp_df_core(y, [&](int j) {
+        return make_float2(__shfl_sync(0xFFFFFFFFu, tj.x, j), __shfl_sync(0xFFFFFFFFu, tj.y, j));
+    });
 }
 
 // exp((x - M) / T) for a logit x <= M (inv_t = 1 / T): x - M exactly (TwoSum), the product
 // and the exponential in double-float; a -inf logit gives 0.
 __device__ __forceinline__ df weight_df(float x, float M, df inv_t) {
-    if (!(x > -__int_as_float(0x7f800000))) return df{0.f, 0.f};  // a masked (-inf) logit
-    return exp_df(df_mul(two_sum(x, -M), inv_t));
+    const bool masked = !(x > -__int_as_float(0x7f800000));
+    const df e = exp_df(df_mul(two_sum(masked ? M : x, -M), inv_t));
+    return masked ? df{0.f, 0.f} : e;
+}
+// weight_df for a whole warp at once (see exp_df_warp).
+__device__ __forceinline__ df weight_df_warp(float x, float M, df inv_t, float2 tj) {
+    const bool masked = !(x > -__int_as_float(0x7f800000));
+    const df e = exp_df_warp(df_mul(two_sum(masked ? M : x, -M), inv_t), tj);
+    return masked ? df{0.f, 0.f} : e;
 }
 
 }  // namespace sv

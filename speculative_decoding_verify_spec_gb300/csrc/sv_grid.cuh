@@ -1,4 +1,5 @@
-// sv_grid.cuh -- a bounded grid-wide barrier for the cooperative re-draw kernel.
+// sv_grid.cuh -- bounded device-side waits: a flag set by another warp of the grid, and a
+// grid-wide barrier for cooperative launches.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -17,6 +18,32 @@ __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// A load with acquire semantics at device scope (sees what a release -- a fence then a
+// store or atomic -- made visible before it).
+__device__ __forceinline__ int ld_acquire(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits until *p is nonzero and returns it.  Gives up after limit_ns: records
+// SV_ERR_TIMEOUT in *status and returns 0.  Only for flags that a warp already running
+// (never itself waiting) will set.
+__device__ inline int wait_nonzero(const int *p, int *status, uint64_t limit_ns) {
+    int v = ld_acquire(p);
+    if (v) return v;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        __nanosleep(128);
+        v = ld_acquire(p);
+        if (v) return v;
+        if ((i & 15) == 15 && global_ns() - t0 > limit_ns) {
+            atomicExch(status, int(SV_ERR_TIMEOUT));
+            return 0;
+        }
+    }
 }
 
 // Grid barrier for a cooperative launch (all CTAs resident): waits until `expected` CTAs

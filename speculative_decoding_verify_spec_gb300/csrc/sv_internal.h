@@ -23,14 +23,16 @@ __host__ __device__ inline const char *row_ptr(const Logits &L, int bytes, int64
 // decide marks a sequence whose accept test had |u q - p| < kRefineAcceptWindow * max(p, u q)
 // (flag kRefineAccept); draw marks one whose threshold u'R lies within
 // kRefineCdfWindow * R of a CDF boundary or that needed a rounding fallback (kRefineDraw),
-// and appends every marked sequence to a list of at most kMaxRefine; refine redoes those in
-// double-float arithmetic.  Control words (int32, zeroed by decide every call):
-constexpr int kRefineCount = 0;     // sequences marked by this call (may exceed kMaxRefine)
-constexpr int kRefineBarCount = 1;  // grid barrier of the refine kernel
-constexpr int kRefineBarGen = 2;
-constexpr int kRefineStatus = 3;    // SV_ERR_TIMEOUT if a barrier of the refine kernel gave up
+// and lists every marked sequence: those with kRefineAccept on the rescan list (entries B ..
+// 2B - 1 of the records), the others on the main list (entries 0 .. B - 1); refine redoes
+// all of them in double-float arithmetic.  Control block (int32, zeroed by decide every
+// call), followed by the per-sequence marks rflag[B]:
+constexpr int kRefineCount = 0;     // sequences marked by this call
+constexpr int kRefineMain = 1;      // entries on the main list
+constexpr int kRefineAll = 2;       // entries on the rescan list
+constexpr int kRefineStatus = 3;    // SV_ERR_TIMEOUT if a bounded wait of the re-draw gave up
+constexpr int kRefineRedone = 4;    // sequences whose final token the re-draw wrote
 constexpr int kRefineCtlWords = 8;
-constexpr int kMaxRefine = 32;
 constexpr int kRefineDraw = 1, kRefineAccept = 2;
 constexpr float kRefineAcceptWindow = 1e-6f;
 // Draw prefixes are double-float, so the gap is limited by the unit masses' own fp32 error:
@@ -38,11 +40,25 @@ constexpr float kRefineAcceptWindow = 1e-6f;
 // tile's mass, the same for every logit of it), a residual draw's are direct sums.
 constexpr float kRefineCdfWindow = 2e-7f;      // bonus draw from p (mode 0)
 constexpr float kRefineCdfWindowRes = 6e-8f;   // residual draw (mode 1)
+// Every draw window also holds kTokenWindow x min(1, S - 1) / S for each row the weights
+// come from (S = sum 2^y, y = (x - M) c <= 0): one fp32 weight 2^y is off by at most ~2.5e-7
+// (ex2.approx's own error, measured at 1.42e-7 relative over [-40, 0], plus the argument's
+// rounding, 2^y |y| <= 0.53, and the product with 1 / S), except the row maximum's,
+// 2^0 = 1 exactly; so one other token of weight up to min(1, S - 1) can move a boundary by
+// that much -- on a row carried by a few tokens more than the windows above, which are set
+// by the many small, independent errors of spread-out rows.
+constexpr float kTokenWindow = 3e-7f;
+__host__ __device__ inline float token_window(float S) { return kTokenWindow * fminf(1.f, S - 1.f) / S; }
 // What draw records about a listed sequence (the re-draw's first read).
 struct RefineInfo {
     int seq, flag, k, mode;  // plan (k, mode) as decided in fp32
     float Mt, St, Md, Sd;    // fp32 (max, sum) of target / draft row k (Md, Sd unused for a bonus draw)
 };
+// Re-draw scratch (units of 64 logits, refine_units(V) of them per row): per main-list
+// sequence 5 rows of double-float unit sums and one of near-logit counts; the rescan list
+// is taken kRescanChunk sequences at a time, (2 gamma + 1) rows of unit sums each.
+constexpr int kRescanChunk = 16;
+inline int64_t refine_units(int V) { return (int64_t(V) + 63) / 64; }
 
 // Sampling path -----------------------------------------------------------------------
 // Row statistics of B sequences of R = rows_a + rows_b rows: local rows [0, rows_a) come
@@ -55,18 +71,20 @@ cudaError_t launch_stats_tiles(int dtype, bool vec, Logits a, int rows_a, Logits
 cudaError_t launch_decide(int dtype, Logits t, Logits d, int B, int gamma, int V, int ntile,
                           float c, const int32_t *x, uint64_t seed, uint64_t offset,
                           const void *partial, void *rowstat, void *plan, int32_t *accepted_len,
-                          int32_t *out_tokens, int *rflag, int *rctl, cudaStream_t s);
+                          int32_t *out_tokens, int *rflag, int *rctl, int *rbar, cudaStream_t s);
 // Residual mass sum_j (p_j - q_j)+ of every residual tile of the stop row (sequences that
 // rejected): csum[seq * nrt + tile].
 cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V,
                                   int nrt, float c, const void *rowstat, const void *plan, float *csum,
                                   cudaStream_t s);
-// Inverse-CDF draw of the final token on the stop row of every valid sequence; marks and
-// lists the sequences to redo in extended precision.
-cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
-                        float c, uint64_t seed, uint64_t offset, const void *partial, const void *rowstat,
-                        const void *plan, const float *csum, int32_t *out_tokens, int *rflag, int *rctl,
-                        RefineInfo *rinfo, int *ramb, bool early, cudaStream_t s);
+// Inverse-CDF draw of the final token on the stop row of every valid sequence, then the
+// extended-precision re-draw of every sequence it or decide marked (one cooperative grid;
+// rbar: its grid barrier's words; rsum, ramb, rresc: the re-draw's scratch, see above).
+cudaError_t launch_draw_refine(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
+                               float c, float T, uint64_t seed, uint64_t offset, const int32_t *x, const void *partial,
+                               const void *rowstat, const void *plan, const float *csum, int32_t *accepted_len,
+                               int32_t *out_tokens, int *rctl, int *rbar, RefineInfo *rinfo, void *rsum, int *ramb,
+                               void *rresc, bool early, cudaStream_t s);
 // Extended-precision re-walk of near-boundary tree-sampling sequences -----------------
 // The walk marks sequence b (mark[b] = 1, else 0, every call) when one of its fp32
 // decisions came near enough to flipping: an accept test with |u q - p| below
@@ -77,10 +95,11 @@ cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamm
 // draw's prefixes are fp64 sums of the fp32 weights, so the gap is that of the weights'
 // own rounding, measured below 7e-9 (total + A) on the workloads).  It records
 // the first kTreeRecNodes nodes it reached (rec: node, M_t, M_d, has children; rlen: how
-// many).  The re-walk redoes the first kMaxTreeRefine marked sequences in double-float
-// arithmetic.  Control block (int32, zeroed by the walk; words other than these stay 0):
+// many).  The re-walk redoes every marked sequence in double-float arithmetic:
+// kMaxTreeRefine clusters, the first kMaxTreeRefine marked sequences with exponentials the
+// whole grid precomputed (slots), later ones computing them in their cluster.  Control block (int32, zeroed by the walk; words other than these stay 0):
 constexpr int kTrMarked = 0;  // sequences the last call marked
-constexpr int kTrRedone = 4;  // sequences redone (the first kMaxTreeRefine marked, in index order)
+constexpr int kTrRedone = 4;  // sequences redone (every marked one)
 constexpr int kTrCtlWords = 8;
 constexpr int kMaxTreeRefine = 8;
 constexpr int kTreeRecNodes = 8;
@@ -113,8 +132,8 @@ inline int tree_rec_nodes(int max_depth) { return max_depth + 1 < kTreeRecNodes 
 inline size_t tree_refine_smem(int N, int max_depth) { return size_t(13 * N + max_depth + 1) * 4; }
 // The exponentials of the listed sequences' recorded rows (every resident CTA), then the
 // re-walk (one cluster of 16 CTAs per listed sequence where the device holds one, else 8).
-cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws,
-                            cudaStream_t s);
+cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, bool per_seq,
+                            TreeRefineWs ws, cudaStream_t s);
 cudaError_t launch_tree_rewalk(int dtype, Logits t, Logits d, int B, int N, int V, bool chain, const int32_t *parent,
                                const int32_t *node_tokens, int max_depth, float T, uint64_t seed, uint64_t offset,
                                int without_replacement, int K, TreeRefineWs ws, int32_t *accepted_len,
@@ -144,30 +163,15 @@ cudaError_t launch_typical(int dtype, bool vec, Logits t, int B, int gamma, int 
                            int nunit, float *umass, TreeRefineWs rw, int32_t *accepted_len, int32_t *out_tokens,
                            cudaStream_t s);
 // The double-float re-draw of the typical walk's marked final tokens (one recorded position
-// per sequence: the stop row), after launch_tree_exp with K = 1.
-cudaError_t launch_typical_redraw(int B, int gamma, int V, uint64_t seed, uint64_t offset, TreeRefineWs ws,
-                                  int32_t *out_tokens, cudaStream_t s);
+// per sequence: the stop row), after launch_tree_exp with K = 1 and per_seq (every marked
+// sequence, us[B][nunit]).
+cudaError_t launch_typical_redraw(int dtype, Logits t, int B, int gamma, int V, float T, uint64_t seed,
+                                  uint64_t offset, TreeRefineWs ws, int32_t *out_tokens, cudaStream_t s);
 constexpr float kTypicalCdfWindow = 1e-6f;  // marks a typical draw this close (x total) to a CDF boundary
 // Prompt-lookup drafting: history [B][stride] with lengths[B]; drafts [B][k], count [B].
 constexpr int kMaxNgram = 64;
 cudaError_t launch_ngram_draft(const int32_t *history, int64_t stride, const int32_t *lengths, int B, int n, int k,
                                int pad, int32_t *drafts, int32_t *count, cudaStream_t s);
-// Logits per unit of the extended-precision re-draw (32 lanes x 2).
-inline int refine_unit_elems(int) { return 64; }
-// Per listed sequence the re-draw keeps (4 gamma + 1) x nref double-float unit sums and,
-// per row pair, an ambiguity list of 1 + kMaxAmbiguous ints (count first; draw clears the
-// counts of every slot it fills).
-constexpr int kMaxAmbiguous = 32;
-__host__ __device__ inline int64_t slot_df_entries(int gamma, int nref) { return int64_t(4 * gamma + 1) * nref; }
-__host__ __device__ inline int64_t slot_amb_ints(int gamma) {
-    return int64_t(gamma > 0 ? gamma : 1) * (1 + kMaxAmbiguous);
-}
-// The re-draw of the listed sequences (double-float arithmetic); a cooperative grid.
-// Scratch: rsum [kMaxRefine][slot_df_entries] (8 bytes each), ramb [kMaxRefine][slot_amb_ints].
-cudaError_t launch_refine(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int nref, float T,
-                          uint64_t seed, uint64_t offset, const int32_t *x, const void *rowstat, const void *plan,
-                          int *rctl, const RefineInfo *rinfo, void *rsum, void *ramb, int32_t *accepted_len,
-                          int32_t *out_tokens, cudaStream_t s);
 // Test hook: one CTA through the re-draw's grid barrier expecting `expected` arrivals.
 cudaError_t launch_wait_selftest(int *ctl, int expected, uint64_t limit_ns, cudaStream_t s);
 // Test hook: exp(hi + lo) in double-float for n arguments <= 0.

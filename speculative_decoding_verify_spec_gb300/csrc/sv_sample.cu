@@ -23,6 +23,7 @@
 #include "sv_device.cuh"
 #include "sv_df.cuh"
 #include "sv_internal.h"
+#include "sv_refine.cuh"
 
 namespace sv {
 namespace {
@@ -100,7 +101,8 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
                   const int32_t *__restrict__ x, uint64_t seed, uint64_t offset,
                   const float2 *__restrict__ partial, float2 *__restrict__ rowstat,
                   int2 *__restrict__ plan, int32_t *__restrict__ accepted_len,
-                  int32_t *__restrict__ out_tokens, int *__restrict__ rflag, int *__restrict__ rctl) {
+                  int32_t *__restrict__ out_tokens, int *__restrict__ rflag, int *__restrict__ rctl,
+                  int *__restrict__ rbar) {
     extern __shared__ float2 s_stat[];  // [2 gamma + 1]
     griddep_launch_next();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -119,7 +121,10 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
         }
     }
     griddep_wait();
-    if (blockIdx.x == 0 && threadIdx.x < kRefineCtlWords) rctl[threadIdx.x] = 0;  // this call's re-draw list
+    if (blockIdx.x == 0 && threadIdx.x < kRefineCtlWords) {  // this call's re-draw lists and barrier
+        rctl[threadIdx.x] = 0;
+        rbar[threadIdx.x] = 0;
+    }
     for (int r = warp; r < R; r += kDecideWarps) {
         const float2 st = warp_merge_stats(partial + (seq * R + r) * ntile, ntile, c, lane);
         if (lane == 0) {
@@ -284,44 +289,22 @@ __global__ void __launch_bounds__(kThreads, kResidualCtas)
 }
 
 // ------------------------------------------------------------------------------------
-// The inverse-CDF draw, one warp per sequence.  Units: mode 1 the residual tiles of the
+// The inverse-CDF draw of one sequence by one warp.  Units: mode 1 the residual tiles of the
 // stop row (masses from residual_tiles), mode 0 the tiles of p (mass S_u 2^((M_u - M) c)
 // from the row-statistics partials).  A zero residual falls back to p.  Lane l owns the
 // contiguous units [l * per_lane, (l + 1) * per_lane); inside the chosen unit lane l holds
 // a contiguous run of its vectors in registers, summed once and scanned once with the same
-// arithmetic, so both passes see the same bits.
+// arithmetic, so both passes see the same bits.  pl, st, sdk, flag0, u1: what decide wrote
+// for the sequence (plan, statistics of its stop rows, its mark) and the draw's uniform.
 template <class D, bool VEC>
-__global__ void __launch_bounds__(128)
-    draw_kernel(Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt, float c, uint64_t seed,
-                uint64_t offset, const float2 *__restrict__ partial, const float2 *__restrict__ rowstat,
-                const int2 *__restrict__ plan, const float *__restrict__ csum,
-                int32_t *__restrict__ out_tokens, int *__restrict__ rflag, int *__restrict__ rctl,
-                RefineInfo *__restrict__ rinfo, int *__restrict__ ramb, bool early) {
-    griddep_launch_next();
-    const int lane = threadIdx.x & 31;
-    const int64_t seq = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const bool live = seq < B;
+__device__ __forceinline__ void draw_sequence(Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
+                                              float c, const float2 *__restrict__ partial,
+                                              const float *__restrict__ csum, int32_t *__restrict__ out_tokens,
+                                              int *__restrict__ rflag, int *__restrict__ rctl,
+                                              RefineInfo *__restrict__ rinfo, int64_t seq, int2 pl, float2 st,
+                                              float2 sdk, int flag0, float u1,
+                                              int lane) {
     const int R = 2 * gamma + 1;
-    // What decide wrote (plan, statistics, its re-draw mark) and the uniform.  With `early`
-    // (the residual kernel ran in between and let this grid start only after its own wait
-    // on decide) these loads go out before the wait for the residual masses.
-    int2 pl = make_int2(-1, -1);
-    float2 st = make_float2(0.f, 1.f), sdk = make_float2(0.f, 1.f);
-    int flag0 = 0;
-    float u1 = 0.f;
-    auto read_plan = [&]() {
-        pl = __ldcg(plan + seq);
-        if (pl.y >= 0) {
-            st = __ldcg(rowstat + seq * R + pl.x);
-            if (pl.y == 1) sdk = __ldcg(rowstat + seq * R + gamma + 1 + pl.x);
-            flag0 = __ldcg(rflag + seq);
-            u1 = uniform01(seed, offset, uint32_t(seq), uint32_t(pl.x), 1u);
-        }
-    };
-    if (live && early) read_plan();
-    griddep_wait();
-    if (!live) return;
-    if (!early) read_plan();
     if (pl.y < 0) return;  // invalid sequence: outputs already written by decide
     const int k = pl.x;
     int mode = pl.y;  // 1: residual after a rejection, 0: bonus draw from p
@@ -510,19 +493,69 @@ __global__ void __launch_bounds__(128)
     if (lane == 0) {
         out_tokens[seq * (gamma + 1) + k] = int32_t(u0 + tok);
         const bool near = first == kNoIndex || force_last || unit_fallback || mode != pl.y ||
-                          !(g >= (mode ? kRefineCdfWindowRes : kRefineCdfWindow) * totd.hi);
+                          !(g >= (mode ? kRefineCdfWindowRes * totd.hi + token_window(st.y) + token_window(sd.y)
+                                       : kRefineCdfWindow * totd.hi + kTokenWindow * fminf(1.f, st.y - 1.f)));
+        // (mode 0 weighs in units of the row maximum's weight, not of S)
         int flag = flag0;
         if (near && flag == 0) flag = kRefineDraw;
-        if (flag != 0) {
+        if (flag != 0) {  // listed: a marked accept test on the rescan list, a draw on the main list
             rflag[seq] = flag;
-            const int slot = atomicAdd(rctl + kRefineCount, 1);
-            if (slot < kMaxRefine) {
-                rinfo[slot] = RefineInfo{int(seq), flag, k, pl.y, st.x, st.y, sdk.x, sdk.y};
-                int *amb = ramb + int64_t(slot) * slot_amb_ints(gamma);
-                for (int i = 0; i < (gamma > 0 ? gamma : 1); ++i) amb[i * (1 + kMaxAmbiguous)] = 0;
-            }
+            atomicAdd(rctl + kRefineCount, 1);
+            const int e = (flag & kRefineAccept) ? B + atomicAdd(rctl + kRefineAll, 1) : atomicAdd(rctl + kRefineMain, 1);
+            rinfo[e] = RefineInfo{int(seq), flag, k, pl.y, st.x, st.y, sdk.x, sdk.y};
         }
     }
+}
+
+// ------------------------------------------------------------------------------------
+// The draws and the re-draw in one cooperative grid (every CTA resident): each warp draws
+// its sequences (grid-stride), then every CTA runs the re-draw's phases, which start with a
+// grid barrier and end at once when no sequence was marked.  With `early` (the residual
+// kernel ran in between and let this grid start only after its own wait on decide) a warp's
+// first plan is read before the wait for the residual masses.
+template <class D, bool VEC>
+__global__ void __launch_bounds__(kThreads, 2)
+    draw_refine_kernel(Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt, float c, float T,
+                       uint64_t seed, uint64_t offset, const int32_t *__restrict__ x,
+                       const float2 *__restrict__ partial, const float2 *__restrict__ rowstat,
+                       const int2 *__restrict__ plan, const float *__restrict__ csum,
+                       int32_t *__restrict__ accepted_len, int32_t *__restrict__ out_tokens, int *__restrict__ rctl,
+                       int *__restrict__ rbar, RefineInfo *__restrict__ rinfo, df *__restrict__ rsum,
+                       int *__restrict__ ramb, df *__restrict__ rresc, bool early) {
+    __shared__ RefineSmem sm;
+    griddep_launch_next();
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int64_t nw = (int64_t(gridDim.x) * kThreads) >> 5;
+    const int R = 2 * gamma + 1;
+    int *rflag = rctl + kRefineCtlWords;
+    int2 pl = make_int2(-1, -1);
+    float2 st = make_float2(0.f, 1.f), sdk = make_float2(0.f, 1.f);
+    int flag0 = 0;
+    float u1 = 0.f;
+    auto read_plan = [&](int64_t seq) {
+        pl = __ldcg(plan + seq);
+        st = make_float2(0.f, 1.f);
+        sdk = make_float2(0.f, 1.f);
+        flag0 = 0;
+        if (pl.y >= 0) {
+            st = __ldcg(rowstat + seq * R + pl.x);
+            if (pl.y == 1) sdk = __ldcg(rowstat + seq * R + gamma + 1 + pl.x);
+            flag0 = __ldcg(rflag + seq);
+            u1 = uniform01(seed, offset, uint32_t(seq), uint32_t(pl.x), 1u);
+        }
+    };
+    if (gw < B && early) read_plan(gw);
+    griddep_wait();
+    for (int64_t seq = gw; seq < B; seq += nw) {
+        if (!(early && seq == gw)) read_plan(seq);
+        if (pl.y >= 0)  // (an invalid sequence's outputs were written by decide)
+            draw_sequence<D, VEC>(t, d, B, gamma, V, ntile, nrt, c, partial, csum, out_tokens, rflag, rctl, rinfo,
+                                  seq, pl, st, sdk, flag0, u1, lane);
+    }
+    const RefineArgs ra{t, d, B, gamma, V, T, seed, offset, x, rowstat, rctl, rbar, rinfo, rsum, ramb, rresc,
+                        accepted_len, out_tokens};
+    refine_phases<D>(ra, sm);
 }
 
 // ------------------------------------------------------------------------------------
@@ -579,12 +612,12 @@ cudaError_t launch_stats_tiles(int dtype, bool vec, Logits a, int rows_a, Logits
 cudaError_t launch_decide(int dtype, Logits t, Logits d, int B, int gamma, int V, int ntile,
                           float c, const int32_t *x, uint64_t seed, uint64_t offset,
                           const void *partial, void *rowstat, void *plan, int32_t *accepted_len,
-                          int32_t *out_tokens, int *rflag, int *rctl, cudaStream_t s) {
+                          int32_t *out_tokens, int *rflag, int *rctl, int *rbar, cudaStream_t s) {
     auto k = dtype == 1 ? decide_kernel<BF16> : decide_kernel<F32>;
     const size_t smem = size_t(2 * gamma + 1) * sizeof(float2);
     return launch_after(k, unsigned(B), kDecideWarps * 32, smem, s, t, d, B, gamma, V, ntile, c, x, seed, offset,
                         static_cast<const float2 *>(partial), static_cast<float2 *>(rowstat),
-                        static_cast<int2 *>(plan), accepted_len, out_tokens, rflag, rctl);
+                        static_cast<int2 *>(plan), accepted_len, out_tokens, rflag, rctl, rbar);
 }
 
 cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V,
@@ -602,16 +635,20 @@ cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B
                         static_cast<const float2 *>(rowstat), static_cast<const int2 *>(plan), csum);
 }
 
-cudaError_t launch_draw(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
-                        float c, uint64_t seed, uint64_t offset, const void *partial, const void *rowstat,
-                        const void *plan, const float *csum, int32_t *out_tokens, int *rflag, int *rctl,
-                        RefineInfo *rinfo, int *ramb, bool early, cudaStream_t s) {
-    const unsigned grid = unsigned((int64_t(B) * 32 + 127) / 128);
-    auto k = pick(dtype, vec, draw_kernel<BF16, true>, draw_kernel<BF16, false>, draw_kernel<F32, true>,
-                  draw_kernel<F32, false>);
-    return launch_after(k, grid, 128, 0, s, t, d, B, gamma, V, ntile, nrt, c, seed, offset,
-                        static_cast<const float2 *>(partial), static_cast<const float2 *>(rowstat),
-                        static_cast<const int2 *>(plan), csum, out_tokens, rflag, rctl, rinfo, ramb, early);
+cudaError_t launch_draw_refine(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
+                               float c, float T, uint64_t seed, uint64_t offset, const int32_t *x, const void *partial,
+                               const void *rowstat, const void *plan, const float *csum, int32_t *accepted_len,
+                               int32_t *out_tokens, int *rctl, int *rbar, RefineInfo *rinfo, void *rsum, int *ramb,
+                               void *rresc, bool early, cudaStream_t s) {
+    auto k = pick(dtype, vec, draw_refine_kernel<BF16, true>, draw_refine_kernel<BF16, false>,
+                  draw_refine_kernel<F32, true>, draw_refine_kernel<F32, false>);
+    unsigned grid = 0;  // every resident slot, at most one warp per sequence for the draws
+    cudaError_t e = persistent_grid(k, int64_t(1) << 40, &grid);
+    if (e != cudaSuccess) return e;
+    return launch_after_ex(true, k, grid, kThreads, 0, s, t, d, B, gamma, V, ntile, nrt, c, T, seed, offset, x,
+                           static_cast<const float2 *>(partial), static_cast<const float2 *>(rowstat),
+                           static_cast<const int2 *>(plan), csum, accepted_len, out_tokens, rctl, rbar, rinfo,
+                           static_cast<df *>(rsum), ramb, static_cast<df *>(rresc), early);
 }
 
 cudaError_t launch_rowstats_finalize(int rows, int ntile, float c, float inv_t, const void *partial,

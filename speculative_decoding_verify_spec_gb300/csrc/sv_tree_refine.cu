@@ -5,15 +5,19 @@
 // Once", SpecInfer's rule; "The rule" for the single test).  A comparison whose two sides
 // lie closer than the fp32 error may come out the other way than in exact arithmetic, and
 // every later decision depends on it, so the walk marks such a sequence and records the
-// nodes it reached with their rows' maxima; these kernels walk the first kMaxTreeRefine
-// marked sequences (index order) again from the root in double-float arithmetic
+// nodes it reached with their rows' maxima; these kernels walk every marked sequence
+// (index order) again from the root in double-float arithmetic
 // (sv_df.cuh, ~48 bits; the arithmetic of the chain's re-draw), which settles every
 // comparison whose exact margin is above ~1e-12.
 //
-//   tree_exp_kernel     the whole grid: for every recorded node of every listed sequence,
-//                       e_t(j) = exp((t_j - M_t) / T) and e_d(j) of its target and draft
-//                       rows, stored with their 256-logit unit sums and q's support size;
-//   tree_rewalk_kernel  one thread-block cluster per listed sequence, its CTAs owning
+//   tree_exp_kernel     the whole grid: for every recorded node of the first eight marked
+//                       sequences, e_t(j) = exp((t_j - M_t) / T) and e_d(j) of its target
+//                       and draft rows, stored with their 256-logit unit sums and q's
+//                       support size (for the target-only rules: the unit sums of every
+//                       marked sequence's stop row);
+//   tree_rewalk_kernel  eight thread-block clusters, each taking every eighth marked
+//                       sequence in turn (the first one with those stored values, later ones
+//                       computing them in the cluster), its CTAs owning
 //                       contiguous runs of units and meeting at hardware cluster barriers:
 //                       the rows' sums S_t, S_d, the child tests, one pass per rejection
 //                       for the residual weights in S_t units
@@ -28,6 +32,7 @@
 #include "spec_verify.h"
 #include "sv_device.cuh"
 #include "sv_df.cuh"
+#include "sv_dfwalk.cuh"
 #include "sv_internal.h"
 
 namespace sv {
@@ -37,19 +42,6 @@ constexpr int kTrUnit = kTreeRefineUnit;  // logits per unit (one warp)
 constexpr int kTrLane = kTrUnit / 32;     // logits per lane in a unit (contiguous)
 constexpr int kRwThreads = 512;
 constexpr int kRwWarps = kRwThreads / 32;
-
-__device__ __forceinline__ df ldcg_df(const df *p) {
-    const float2 v = __ldcg(reinterpret_cast<const float2 *>(p));
-    return df{v.x, v.y};
-}
-__device__ __forceinline__ void st_df(df *p, df v) { *reinterpret_cast<float2 *>(p) = make_float2(v.hi, v.lo); }
-__device__ __forceinline__ df df_zero() { return df{0.f, 0.f}; }
-
-// W(j) = max(e_t - ar e_d, 0), ar = a_j rho.
-__device__ __forceinline__ df resid_w(df et, df ed, df ar) {
-    const df w = df_sub(et, df_mul(ar, ed));
-    return df_pos(w) ? w : df_zero();
-}
 
 // The listed sequences: the first kMaxTreeRefine with mark[b] != 0, in index order, into
 // s_seq; returns how many are listed, *total = how many are marked.  Every CTA builds the
@@ -83,119 +75,95 @@ __device__ int list_marked(const int *mark, int B, int *s_seq, unsigned *s_bal, 
     return s_cnt[0];
 }
 
+// The n-th marked sequence (0-based, index order), or -1 if fewer are marked; *total = how
+// many are marked.  Every CTA computes the same.  s_bal: one word per warp of the CTA.
+__device__ int nth_marked(const int *mark, int B, int n, unsigned *s_bal, int *s_cnt, int *total) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    if (tid == 0) {
+        s_cnt[0] = -1;
+        s_cnt[1] = 0;
+    }
+    for (int base = 0; base < B; base += blockDim.x) {
+        const int sq = base + tid;
+        const int f = sq < B ? __ldcg(mark + sq) : 0;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, f != 0);
+        if (lane == 0) s_bal[warp] = bal;
+        __syncthreads();
+        if (tid == 0) {
+            for (int w = 0; w < nw; ++w) {
+                const unsigned m = s_bal[w];
+                const int c = __popc(m);
+                if (s_cnt[0] < 0 && n >= s_cnt[1] && n < s_cnt[1] + c) {
+                    unsigned mm = m;
+                    for (int q = 0; q < n - s_cnt[1]; ++q) mm &= mm - 1;
+                    s_cnt[0] = base + w * 32 + __ffs(mm) - 1;
+                }
+                s_cnt[1] += c;
+            }
+        }
+        __syncthreads();
+    }
+    *total = s_cnt[1];
+    const int r = s_cnt[0];
+    __syncthreads();  // read by every thread before the next call overwrites it
+    return r;
+}
+
 // One unit of one row: e(j) = exp((x_j - M) / T) for its logits, stored; returns (to every
 // lane) the unit sum, in lane order (lane sums, then a warp scan), and the number of
 // positive e(j) in *cnt.
 template <class D>
 __device__ df exp_unit(const char *row, float M, df inv_t, int V, int u, df *E, int *cnt, int lane) {
     const int64_t j0 = int64_t(u) * kTrUnit + lane * kTrLane;
-    float x[kTrLane];  // the loads first, all in flight together
-#pragma unroll
-    for (int e = 0; e < kTrLane; ++e) x[e] = j0 + e < V ? load_elem<D>(row, j0 + e) : 0.f;
-    DfSum ls;
+    df w[kDfLane];
+    unit_exps<D>(row, M, inv_t, V, u, lane, w);  // 0 past the row's end
     int c = 0;
 #pragma unroll
     for (int e = 0; e < kTrLane; ++e)
         if (j0 + e < V) {
-            const df w = weight_df(x[e], M, inv_t);
-            st_df(E + j0 + e, w);
-            ls.add(w);
-            c += df_pos(w) ? 1 : 0;
+            st_df(E + j0 + e, w[e]);
+            c += df_pos(w[e]) ? 1 : 0;
         }
     *cnt = warp_reduce(c, [](int a, int b) { return a + b; });
-    return df_shfl(df_warp_scan(ls.value(), lane), 31);
-}
-
-// Warp-level search over n values (vals[i * stride]) in index order: the first i with
-// base + vals[0] + ... + vals[i] > thr (lanes own contiguous runs: a lane prefix, then the
-// lane's own run).  *run_out = the prefix before i.  With no crossing (rounding left thr
-// at or above the sum) or `force` set: the last i with a positive value, *force_out = true
-// (-1 if every value is 0).  Every lane returns the same.
-// Entry ex_i (if >= 0) is read as vals[ex_i] - ex_v (a unit sum without one excluded term).
-__device__ __forceinline__ df entry(const df *vals, int stride, int i, int ex_i, df ex_v) {
-    const df v = ldcg_df(vals + int64_t(i) * stride);
-    return i == ex_i ? df_sub(v, ex_v) : v;
-}
-
-__device__ int warp_search(const df *vals, int stride, int n, df base, df thr, bool force, df *run_out,
-                           bool *force_out, int lane, int ex_i = -1, df ex_v = df{0.f, 0.f}) {
-    const int per = (n + 31) / 32;
-    df ls = df_zero();
-    int lastpos = -1;
-    for (int q = 0; q < per; ++q) {
-        const int i = lane * per + q;
-        if (i < n) {
-            const df v = entry(vals, stride, i, ex_i, ex_v);
-            ls = df_add(ls, v);
-            if (df_pos(v)) lastpos = i;
-        }
-    }
-    if (!force) {
-        const df incl = df_warp_scan(ls, lane);
-        df excl = df_shfl_up(incl, 1);
-        if (lane == 0) excl = df_zero();
-        const unsigned bal = __ballot_sync(0xFFFFFFFFu, df_gt(df_add(base, incl), thr));
-        if (bal) {
-            const int l = __ffs(bal) - 1;
-            int found = -1;
-            df run = df_add(base, excl);
-            if (lane == l) {
-                for (int q = 0; q < per; ++q) {
-                    const int i = lane * per + q;
-                    if (i >= n) break;
-                    const df nx = df_add(run, entry(vals, stride, i, ex_i, ex_v));
-                    if (df_gt(nx, thr)) {
-                        found = i;
-                        break;
-                    }
-                    run = nx;
-                }
-            }
-            found = __shfl_sync(0xFFFFFFFFu, found, l);
-            run = df_shfl(run, l);
-            if (found >= 0) {
-                *run_out = run;
-                *force_out = false;
-                return found;
-            }
-        }
-    }
-    *run_out = df_zero();
-    *force_out = true;
-    return warp_reduce(lastpos, [](int a, int b) { return max(a, b); });
-}
-
-// The sum of n values in warp_search's order (every lane returns it).
-__device__ df warp_total(const df *vals, int stride, int n, int lane, int ex_i = -1, df ex_v = df{0.f, 0.f}) {
-    const int per = (n + 31) / 32;
-    df ls = df_zero();
-    for (int q = 0; q < per; ++q) {
-        const int i = lane * per + q;
-        if (i < n) ls = df_add(ls, entry(vals, stride, i, ex_i, ex_v));
-    }
-    return df_shfl(df_warp_scan(ls, lane), 31);
+    return unit_sum(w, lane);
 }
 
 }  // namespace
 
-// The exponentials of the recorded nodes of every listed sequence (grid-stride over
-// (slot, position, row, unit), one warp per unit).
+// The exponentials of the recorded nodes of the first kMaxTreeRefine marked sequences
+// (grid-stride over (slot, position, row, unit), one warp per unit).  per_seq (the
+// target-only walks, one recorded row per sequence): the unit sums of the recorded row of
+// EVERY marked sequence instead, stored per sequence (us[b][nunit]), no exponentials.
 template <class D>
 __global__ void __launch_bounds__(kThreads)
-    tree_exp_kernel(Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws) {
+    tree_exp_kernel(Logits t, Logits d, int B, int V, float T, int K, bool per_seq, TreeRefineWs ws) {
     __shared__ int s_seq[kMaxTreeRefine];
     __shared__ unsigned s_bal[kWarps];
     __shared__ int s_cnt[2];
     griddep_launch_next();
     griddep_wait();  // the walk's marks and records
-    int total = 0;
-    const int n = list_marked(ws.mark, B, s_seq, s_bal, s_cnt, &total);
-    if (n == 0) return;
     const int lane = threadIdx.x & 31;
     const int nunit = tree_refine_units(V);
     const df inv_t = df_div(df_from(1.f), df_from(T));
-    const int64_t items = int64_t(n) * K * 2 * nunit;
     const int64_t nw = int64_t(gridDim.x) * kWarps;
+    if (per_seq) {
+        const int64_t items = int64_t(B) * nunit;
+        for (int64_t it = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); it < items; it += nw) {
+            const int64_t seq = it / nunit;
+            const int u = int(it - seq * nunit);
+            if (!__ldcg(ws.mark + seq)) continue;  // (uniform over the warp)
+            const float4 rec = __ldcg(ws.rec + seq);
+            df w[kDfLane];
+            unit_exps<D>(row_ptr(t, D::kBytes, seq, __float_as_int(rec.x)), rec.y, inv_t, V, u, lane, w);
+            const df us = unit_sum(w, lane);
+            if (lane == 0) st_df(ws.us + seq * nunit + u, us);
+        }
+        return;
+    }
+    int total = 0;
+    const int n = list_marked(ws.mark, B, s_seq, s_bal, s_cnt, &total);
+    if (n == 0) return;
+    const int64_t items = int64_t(n) * K * 2 * nunit;
     for (int64_t it = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); it < items; it += nw) {
         const int u = int(it % nunit);
         const int64_t rest = it / nunit;
@@ -219,90 +187,59 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // The double-float re-draw of the target-only walk's final token (typical acceptance, or
-// one-hot q): CTA j takes listed sequence j, whose stop row k the walk recorded (one
-// position, with the token a one-hot q's residual excludes); tree_exp_kernel stored that
-// row's exponentials e(j) = exp((t_j - M) / T) and unit sums.  The token is the first j with
-// e(0) + ... + e(j) > u' x S over the included logits (u' = U(b, k, purpose 1)): the unit by
-// a warp search over the unit sums, then inside the unit as the re-walk's draw does.  Only
-// out_tokens[b][k] changes (the accepted prefix was decided by the walk).
+// one-hot q), one warp per marked sequence -- every marked sequence.  The walk recorded the
+// stop row k (one position, with the token a one-hot q's residual excludes) and
+// tree_exp_kernel stored the unit sums of e(j) = exp((t_j - M) / T) over that row.  The
+// token is the first j with e(0) + ... + e(j) > u' x S over the included logits (u' = U(b,
+// k, purpose 1)): the unit by a warp search over the unit sums, then inside the unit (its
+// exponentials again) as the re-walk's draw does.  Only out_tokens[b][k] changes (the
+// accepted prefix was decided by the walk).
+template <class D>
 __global__ void __launch_bounds__(kThreads)
-    typical_redraw_kernel(int B, int gamma, int V, uint64_t seed, uint64_t offset, TreeRefineWs ws,
+    typical_redraw_kernel(Logits t, int B, int gamma, int V, float T, uint64_t seed, uint64_t offset, TreeRefineWs ws,
                           int32_t *__restrict__ out_tokens) {
-    __shared__ int s_seq[kMaxTreeRefine];
-    __shared__ unsigned s_bal[kWarps];
-    __shared__ int s_cnt[2];
     griddep_launch_next();
-    griddep_wait();  // the exponentials of the stop rows
-    int total_marked = 0;
-    const int n = list_marked(ws.mark, B, s_seq, s_bal, s_cnt, &total_marked);
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        ws.ctl[kTrMarked] = total_marked;
-        ws.ctl[kTrRedone] = n;
-    }
-    const int j = blockIdx.x;
-    if (j >= n || threadIdx.x >= 32) return;
-    const int lane = threadIdx.x;
-    const int64_t seq = s_seq[j];
+    griddep_wait();  // the unit sums of the stop rows
+    const int lane = threadIdx.x & 31;
+    const int64_t seq = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    if (seq >= B || !__ldcg(ws.mark + seq)) return;
     const float4 rec = __ldcg(ws.rec + seq);  // one recorded position: the stop row
     const int k = __float_as_int(rec.x);
     const int xk = __float_as_int(rec.z);  // a token the draw excludes (one-hot q), else -1
     const int nunit = tree_refine_units(V);
-    const df *E = ws.et + int64_t(j) * 2 * V;  // slot j, position 0, target row
-    const df *U = ws.us + int64_t(j) * 2 * nunit;
-    const int ex_u = xk >= 0 ? xk / kTrUnit : -1;
-    const df ex_v = xk >= 0 ? ldcg_df(E + xk) : df_zero();
+    const df inv_t = df_div(df_from(1.f), df_from(T));
+    const char *row = row_ptr(t, D::kBytes, seq, k);
+    const df *U = ws.us + seq * nunit;
+    const int ex_u = xk >= 0 ? xk / kDfUnit : -1;
+    const df ex_v = xk >= 0 ? weight1_df(load_elem<D>(row, xk), rec.y, inv_t) : df_zero();
     const float u2 = uniform01(seed, offset, uint32_t(seq), uint32_t(k), 1u);
     const df thr = df_mul_f(warp_total(U, 1, nunit, lane, ex_u, ex_v), u2);
     df run;
     bool force;
     int u = warp_search(U, 1, nunit, df_zero(), thr, false, &run, &force, lane, ex_u, ex_v);
     if (u < 0) u = 0;
-    const int64_t j0 = int64_t(u) * kTrUnit + lane * kTrLane;
-    df w[kTrLane];
-    DfSum lsum;
-    int lastpos = -1;
+    df w[kDfLane];
+    unit_exps<D>(row, rec.y, inv_t, V, u, lane, w);
+    const int64_t j0 = int64_t(u) * kDfUnit + lane * kDfLane;
 #pragma unroll
-    for (int e = 0; e < kTrLane; ++e) {
-        w[e] = (j0 + e < V && j0 + e != xk) ? ldcg_df(E + j0 + e) : df_zero();
-        if (j0 + e < V) {
-            lsum.add(w[e]);
-            if (df_pos(w[e])) lastpos = int(j0) + e;
-        }
+    for (int e = 0; e < kDfLane; ++e)
+        if (j0 + e == xk) w[e] = df_zero();
+    const int tok = unit_pick(w, int64_t(u) * kDfUnit, j0, V, run, thr, force, lane);
+    if (lane == 0) {
+        out_tokens[seq * (gamma + 1) + k] = tok;
+        atomicAdd(ws.ctl + kTrMarked, 1);
+        atomicAdd(ws.ctl + kTrRedone, 1);
     }
-    lastpos = warp_reduce(lastpos, [](int a, int b) { return max(a, b); });
-    int tok = lastpos;
-    if (!force) {
-        const df incl = df_warp_scan(lsum.value(), lane);
-        df excl = df_shfl_up(incl, 1);
-        if (lane == 0) excl = df_zero();
-        const unsigned bal = __ballot_sync(0xFFFFFFFFu, df_gt(df_add(run, incl), thr));
-        if (bal) {
-            const int l = __ffs(bal) - 1;
-            int cand = -1, lpos = -1;
-            df r2 = df_add(run, excl);
-#pragma unroll
-            for (int e = 0; e < kTrLane; ++e) {
-                const df nx = df_add(r2, w[e]);
-                if (cand < 0 && df_gt(nx, thr)) cand = int(j0) + e;
-                if (df_pos(w[e])) lpos = int(j0) + e;
-                r2 = nx;
-            }
-            if (cand < 0) cand = lpos;
-            cand = __shfl_sync(0xFFFFFFFFu, cand, l);
-            if (cand >= 0) tok = cand;
-        }
-    }
-    if (tok < 0) tok = int(int64_t(u) * kTrUnit);
-    if (lane == 0) out_tokens[seq * (gamma + 1) + k] = tok;
 }
 
-cudaError_t launch_typical_redraw(int B, int gamma, int V, uint64_t seed, uint64_t offset, TreeRefineWs ws,
-                                  int32_t *out_tokens, cudaStream_t s) {
-    return launch_after(typical_redraw_kernel, unsigned(kMaxTreeRefine), kThreads, 0, s, B, gamma, V, seed, offset,
-                        ws, out_tokens);
+cudaError_t launch_typical_redraw(int dtype, Logits t, int B, int gamma, int V, float T, uint64_t seed,
+                                  uint64_t offset, TreeRefineWs ws, int32_t *out_tokens, cudaStream_t s) {
+    auto k = dtype == 1 ? typical_redraw_kernel<BF16> : typical_redraw_kernel<F32>;
+    return launch_after(k, unsigned((int64_t(B) * 32 + kThreads - 1) / kThreads), kThreads, 0, s, t, B, gamma, V, T,
+                        seed, offset, ws, out_tokens);
 }
 
-// The re-walk: cluster j (CS CTAs) takes listed sequence j.
+// The re-walk: cluster j (CS CTAs) takes the marked sequences of rank j, j + 8, j + 16, ...
 template <class D, int CS>
 __global__ void __launch_bounds__(kRwThreads, 1)
     tree_rewalk_kernel(Logits t, Logits d, int B, int N, int V, bool chain, const int32_t *__restrict__ parent,
@@ -319,7 +256,6 @@ __global__ void __launch_bounds__(kRwThreads, 1)
     df *s_remcoef = reinterpret_cast<df *>(s_int + 5 * N + max_depth + 1);
     df *s_lcoef = s_remcoef + N;
     df *s_cxt = s_lcoef + N, *s_cxd = s_cxt + N;
-    __shared__ int s_seq[kMaxTreeRefine];
     __shared__ unsigned s_bal[kRwWarps];
     __shared__ int s_cnt[2];
     __shared__ df s_wsum[2][kRwWarps];
@@ -333,27 +269,24 @@ __global__ void __launch_bounds__(kRwThreads, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int j = int(blockIdx.x) / CS;
     const int rank = cluster_rank<CS>();
-    int total_marked = 0;
-    const int n = list_marked(ws.mark, B, s_seq, s_bal, s_cnt, &total_marked);
-    if (blockIdx.x == 0 && tid == 0) {
-        ws.ctl[kTrMarked] = total_marked;
-        ws.ctl[kTrRedone] = n;
-    }
-    if (j >= n) return;  // the whole cluster
-    const int64_t seq = s_seq[j];
     const int nunit = tree_refine_units(V);
     auto unit_lo = [&](int c) { return int(int64_t(c) * nunit / CS); };
     const int u_lo = unit_lo(rank), u_hi = unit_lo(rank + 1);
     const int64_t e_lo = int64_t(u_lo) * kTrUnit, e_hi = int64_t(u_hi) * kTrUnit;
     const df inv_t = df_div(df_from(1.f), df_from(T));
     const int W = max_depth + 1;
-    int32_t *out = out_tokens + seq * W;
-    int32_t *opath = out_path ? out_path + seq * W : nullptr;
     df *um = ws.um + int64_t(j) * nunit;            // unit masses of the current pass
     df *cpart = ws.part + int64_t(j) * 2 * CS * 2;  // [2 buffers][CS][2]
     float *cpmax = ws.pmax + int64_t(j) * CS * 2;
     int *ccnt = ws.pcnt + int64_t(j) * CS;
-    const int rlen = __ldcg(ws.rlen + seq);
+
+  // One marked sequence, walked again.  allow_cache: slot j holds its recorded rows'
+  // exponentials (the first kMaxTreeRefine marked sequences); otherwise the cluster
+  // computes every row's maxima and exponentials itself.
+  auto walk_one = [&](int64_t seq, bool allow_cache) {
+    int32_t *out = out_tokens + seq * W;
+    int32_t *opath = out_path ? out_path + seq * W : nullptr;
+    const int rlen = allow_cache ? __ldcg(ws.rlen + seq) : 0;
 
     // the tree (the walk checked it before marking the sequence)
     if (tid == 0) s_flag = 1;
@@ -718,14 +651,28 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         if (tid == 0) accepted_len[seq] = depth;
         return;
     }
+  };
+
+    // cluster j takes the marked sequences of rank j, j + G, j + 2 G, ... (index order; G
+    // clusters), the first of them with slot j's stored exponentials
+    const int G = int(gridDim.x) / CS;
+    for (int iter = 0;; ++iter) {
+        int total_marked = 0;
+        const int64_t seq = nth_marked(ws.mark, B, j + iter * G, s_bal, s_cnt, &total_marked);
+        if (iter == 0 && blockIdx.x == 0 && tid == 0) ws.ctl[kTrMarked] = total_marked;
+        if (seq < 0) break;  // (the whole cluster)
+        walk_one(seq, iter == 0);
+        csync<CS>();  // every CTA is done with the slot's scratch before the next sequence
+        if (rank == 0 && tid == 0) atomicAdd(ws.ctl + kTrRedone, 1);
+    }
 }
 
-cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws,
-                            cudaStream_t s) {
+cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, bool per_seq,
+                            TreeRefineWs ws, cudaStream_t s) {
     auto ke = dtype == 1 ? tree_exp_kernel<BF16> : tree_exp_kernel<F32>;
     unsigned grid = 0;  // every resident CTA
     cudaError_t e = persistent_grid(ke, int64_t(1) << 40, &grid);
-    if (e == cudaSuccess) e = launch_after(ke, grid, kThreads, 0, s, t, d, B, V, T, K, ws);
+    if (e == cudaSuccess) e = launch_after(ke, grid, kThreads, 0, s, t, d, B, V, T, K, per_seq, ws);
     return e;
 }
 

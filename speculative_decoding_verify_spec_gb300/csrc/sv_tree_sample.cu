@@ -434,7 +434,10 @@ __global__ void __launch_bounds__(kTsThreads, 1)
                     gap = fminf(__fsub_rn(wl, ah), ah);  // thr - C_{j-1} = w - (C_j - thr)
                 }
             }
-            if (lane == 0 && (first == kNoIndex || force_last || !(gap >= kTreeCdfWindow * (totd.hi + st.A))))
+            // (p0's terms from target row v, A q0's from draft row v)
+            const float win = kTreeCdfWindow * (totd.hi + st.A) + token_window(1.f / st.inv_st) +
+                              (st.A != 0.f ? st.A * token_window(1.f / st.inv_sd) : 0.f);
+            if (lane == 0 && (first == kNoIndex || force_last || !(gap >= win)))
                 s_near = 1;
             lastpos = warp_reduce(lastpos, [](int a, int b) { return max(a, b); });
             int tok = first != kNoIndex ? first : lastpos;

@@ -290,7 +290,8 @@ __global__ void __launch_bounds__(kTyThreads, 1)
         }
         // fp32 weights (~1e-7 each) cannot settle a threshold this close: the double-float
         // re-draw redoes it
-        if (lane == 0 && (first < 0 || force_last || !(gap >= kTypicalCdfWindow * totd.hi))) s_near = 1;
+        if (lane == 0 && (first < 0 || force_last || !(gap >= kTypicalCdfWindow * totd.hi + token_window(st.S))))
+            s_near = 1;
         lastpos = warp_reduce(lastpos, [](int a, int b) { return max(a, b); });
         int tok = first >= 0 ? first : lastpos;
         if (tok < 0) tok = 0;

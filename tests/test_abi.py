@@ -64,18 +64,22 @@ def test_workspace_sizes(lib):
     assert ws(2, 64, 64, 128256, 1) >= 64 * 64 * 63 * 8
     assert ws(0, 0, 8, 1000, 0) == 0
     assert ws(8, 1, 1, 1, 0) == 0  # an unknown mode
-    # the re-walk / re-draw bookkeeping offsets: modes 4-7 only, inside their workspaces
-    off = lib.spec_verify_walk_redraw_offset
+    # the re-draw of every marked sequence: per sequence 5 rows of double-float unit sums and
+    # one of counts (64-logit units), plus the control words, marks and 2 B records
+    assert n >= 256 * 5 * 2004 * 8 + 256 * 2004 * 4 + 4 * (8 + 256)
+    # the status words: every sampling mode (0, 4-7), inside its workspace; none elsewhere
+    off = lib.spec_verify_status_offset
     off.restype = ctypes.c_size_t
     none = ctypes.c_size_t(-1).value
-    for mode in (4, 5, 6, 7):
+    for mode in (0, 4, 5, 6, 7):
         o = off(mode, 64, 8, 32000, 1)
-        assert o != none and o % 256 == 0 and o + 4 * (8 + 2 * 64) <= ws(mode, 64, 8, 32000, 1)
-    for mode in (0, 1, 2, 3, 8):
+        assert o != none and o % 256 == 0 and o + 4 * (8 + 64) <= ws(mode, 64, 8, 32000, 1)
+    for mode in (1, 2, 3, 8):
         assert off(mode, 64, 8, 32000, 1) == none
+    assert off(0, 0, 8, 32000, 1) == none and off(0, 4, 8, 0, 1) == none and off(0, 4, 8, 10, 5) == none
     # typical acceptance / one-hot sampling: 4 bytes per residual unit per sequence, plus the
-    # double-float re-draw scratch (the stop rows' exponentials: 8 slots x 2 rows x V x 8 B)
-    assert ws(6, 256, 8, 128256, 1) == ws(7, 256, 8, 128256, 1) >= 256 * 126 * 4 + 8 * 2 * 128256 * 8
+    # re-draw's unit sums of every sequence's stop row (8 bytes per 256 logits)
+    assert ws(6, 256, 8, 128256, 1) == ws(7, 256, 8, 128256, 1) >= 256 * 126 * 4 + 256 * 501 * 8
 
 
 P = ctypes.c_void_p

@@ -243,8 +243,8 @@ def test_disagreements_are_below_one_in_ten_thousand():
         for off in range(1, rounds + 1):
             acc, out = sv.spec_verify_sample(s.target, s.draft, s.draft_tokens, s.temperature,
                                              s.seed, off, workspace=ws)
-            n_marked, status = binding.sample_redraw_state(ws, B, G1 - 1, V, binding.BF16)
-            assert status == 0
+            n_marked, n_redone, status, _ = binding.call_status(ws, binding.MODE_SAMPLE, B, G1 - 1, V, binding.BF16)
+            assert status == 0 and n_redone == n_marked
             marked += n_marked
             o = oracle_sample(t, d, x, s.temperature, s.seed, off, diagnostics=True)
             n, m, f, md = compare_sample(acc, out, *o, label=f"{name} offset {off}")
