@@ -385,8 +385,8 @@ sv_status spec_verify_exp_df(const float *y_hi, const float *y_lo, int n, float 
 /*
  * Optional timing instrumentation for the CALLING THREAD (the only state the library
  * keeps, and it is thread-local).  With events != NULL, each later call of
- * spec_verify_sample / _greedy / _tree_greedy / _tree_sample / _sample_lazy / _typical /
- * _sample_onehot on this thread
+ * spec_verify_sample / _greedy / _greedy_noalloc / _tree_greedy / _tree_sample / _sample_lazy /
+ * _typical / _sample_onehot on this thread
  * records events[0] on its stream before its first kernel and events[s] after its s-th
  * kernel (s = 1 .. n_events-1; sampling has 4 kernels: row statistics, decide, residual
  * masses, and the inverse-CDF draw with the extended-precision re-draw of near-boundary

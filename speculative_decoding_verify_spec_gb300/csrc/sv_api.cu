@@ -14,21 +14,15 @@ using sv::Logits;
 
 constexpr int64_t kMaxGrid = 0x7FFFFFFF;
 
+using sv::ntile_of;
+using sv::vec_ok;
+
 bool dtype_ok(sv_dtype d) { return d == SV_FP32 || d == SV_BF16; }
-int elem_bytes(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
-int tile_elems(sv_dtype d) { return d == SV_BF16 ? sv::tile_elems<sv::BF16>() : sv::tile_elems<sv::F32>(); }
 int res_tile_elems(sv_dtype d) {
     return d == SV_BF16 ? sv::res_tile_elems<sv::BF16>() : sv::res_tile_elems<sv::F32>();
 }
-int ntile_of(int V, sv_dtype d) { return int((int64_t(V) + tile_elems(d) - 1) / tile_elems(d)); }
 int nrt_of(int V, sv_dtype d) { return int((int64_t(V) + res_tile_elems(d) - 1) / res_tile_elems(d)); }
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
-
-// 16-byte vector loads are legal when the base and both strides keep every row aligned.
-bool vec_ok(const void *p, int64_t sb, int64_t sr, sv_dtype d) {
-    const int64_t e = elem_bytes(d);
-    return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((sb * e) % 16 == 0) && ((sr * e) % 16 == 0);
-}
 
 struct Layout {
     size_t partial = 0, rowstat = 0, plan = 0, csum = 0;
@@ -170,14 +164,16 @@ constexpr int kMaxStageEvents = 8;
 thread_local cudaEvent_t t_events[kMaxStageEvents];
 thread_local int t_nevents = 0;
 
-// Records event `s` of the calling thread's list, if there is one; stage 0 is "before the
-// first kernel".
-cudaError_t mark(int s, cudaStream_t stream) {
+cudaError_t mark(int s, cudaStream_t stream) { return sv::mark_stage(s, stream); }
+
+}  // namespace
+
+namespace sv {
+cudaError_t mark_stage(int s, cudaStream_t stream) {
     if (s < t_nevents && t_events[s] != nullptr) return cudaEventRecord(t_events[s], stream);
     return cudaSuccess;
 }
-
-}  // namespace
+}  // namespace sv
 
 extern "C" {
 

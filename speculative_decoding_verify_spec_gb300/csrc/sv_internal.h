@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "spec_verify.h"
+
 namespace sv {
 
 // One logits tensor [B][rows][V] (strides in elements) of element type dtype (0 fp32, 1 bf16).
@@ -182,6 +184,20 @@ cudaError_t launch_rowstats_finalize(int rows, int ntile, float c, float inv_t, 
                                      float *m_out, float *lse_out, cudaStream_t s);
 cudaError_t launch_uniforms(uint64_t seed, uint64_t offset, int B, int positions, int purpose,
                             float *out, cudaStream_t s);
+
+// Host-side helpers shared by the entry points ----------------------------------------
+inline int elem_bytes(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
+// Logits per 4 KB tile of the streaming kernels (32 lanes x 8 sixteen-byte vectors).
+inline int tile_elems_of(sv_dtype d) { return 32 * 8 * (16 / elem_bytes(d)); }
+inline int ntile_of(int V, sv_dtype d) { return int((int64_t(V) + tile_elems_of(d) - 1) / tile_elems_of(d)); }
+// 16-byte vector loads are legal when the base and both strides keep every row aligned.
+inline bool vec_ok(const void *p, int64_t sb, int64_t sr, sv_dtype d) {
+    const int64_t e = elem_bytes(d);
+    return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((sb * e) % 16 == 0) && ((sr * e) % 16 == 0);
+}
+// Records stage event s of the calling thread's list (spec_verify_set_stage_events), if any;
+// stage 0 is "before the first kernel".
+cudaError_t mark_stage(int s, cudaStream_t stream);
 
 // Greedy / tree path ------------------------------------------------------------------
 // The NaN-propagating maximum of every (row, 4 KB tile) of [B][R][V]: partial[row * ntile + tile].

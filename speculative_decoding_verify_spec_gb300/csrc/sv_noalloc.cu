@@ -48,18 +48,6 @@ sv_status scratch_address(void **addr) {
     return SV_OK;
 }
 
-int noalloc_elem_bytes(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }
-
-int noalloc_ntile(int V, sv_dtype d) {
-    const int64_t te = d == SV_BF16 ? sv::tile_elems<sv::BF16>() : sv::tile_elems<sv::F32>();
-    return int((int64_t(V) + te - 1) / te);
-}
-
-bool noalloc_vec_ok(const void *p, int64_t sb, int64_t sr, sv_dtype d) {
-    const int64_t e = noalloc_elem_bytes(d);
-    return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((sb * e) % 16 == 0) && ((sr * e) % 16 == 0);
-}
-
 }  // namespace
 
 extern "C" sv_status spec_verify_greedy_noalloc(const void *target_logits, int64_t t_batch_stride,
@@ -74,18 +62,21 @@ extern "C" sv_status spec_verify_greedy_noalloc(const void *target_logits, int64
     if (B == 0) return SV_OK;
     if (!target_logits || !accepted_len || !out_tokens || (gamma > 0 && !draft_tokens))
         return SV_ERR_INVALID_ARG;
-    const int ntile = noalloc_ntile(V, dtype);
+    const int ntile = sv::ntile_of(V, dtype);
     const int64_t partials = int64_t(B) * (gamma + 1) * ntile;
     if (partials * int64_t(sizeof(float)) > int64_t(kNoallocScratchBytes))
         return SV_ERR_WORKSPACE;  // larger than the fixed scratch: use spec_verify_greedy
     void *scratch = nullptr;
     if (sv_status st = scratch_address(&scratch)) return st;
-    const bool vec = noalloc_vec_ok(target_logits, t_batch_stride, t_row_stride, dtype);
+    const bool vec = sv::vec_ok(target_logits, t_batch_stride, t_row_stride, dtype);
     const sv::Logits t{target_logits, t_batch_stride, t_row_stride};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = sv::launch_max_tiles(dtype == SV_BF16, vec, t, gamma + 1, B, V, ntile, scratch, s);
+    cudaError_t e = sv::mark_stage(0, s);  // the same stage events as spec_verify_greedy
+    if (e == cudaSuccess) e = sv::launch_max_tiles(dtype == SV_BF16, vec, t, gamma + 1, B, V, ntile, scratch, s);
+    if (e == cudaSuccess) e = sv::mark_stage(1, s);
     if (e == cudaSuccess)
         e = sv::launch_greedy_finalize(dtype == SV_BF16, vec, t, B, gamma, V, ntile, scratch, draft_tokens,
                                        accepted_len, out_tokens, s);
+    if (e == cudaSuccess) e = sv::mark_stage(2, s);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
