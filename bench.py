@@ -41,15 +41,15 @@ UNIT = "seqs/s"
 FALLBACK_HBM_GBS = 6800.0
 DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "max_tiles_kernel",
                    "tree": "max_tiles_kernel", "tree_sample": "tree_sample_kernel",
-                   "sample_lazy": "tree_sample_kernel", "greedy_lazy": "greedy_walk_kernel",
+                   "sample_lazy": "level_kernel", "greedy_lazy": "greedy_walk_kernel",
                    "tree_lazy": "greedy_walk_kernel", "ngram": "ngram_draft_kernel",
-                   "typical": "typical_walk_kernel", "onehot": "typical_walk_kernel"}
+                   "typical": "level_kernel", "onehot": "level_kernel"}
 STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
 ACCEPT_STEPS = 16  # untimed steps whose accepted lengths and re-draw counts are read back
 STAGES = {"sample": ["row_stats", "decide", "residual_mass", "draw_redraw"],
           "greedy": ["argmax", "finalize"], "tree": ["argmax", "finalize"], "tree_sample": ["walk", "rewalk_exp", "rewalk"],
-          "sample_lazy": ["walk", "rewalk_exp", "rewalk"], "greedy_lazy": ["walk"], "tree_lazy": ["walk"], "ngram": ["draft"],
-          "typical": ["walk", "redraw_exp", "redraw"], "onehot": ["walk", "redraw_exp", "redraw"]}
+          "sample_lazy": ["walk", "residual_mass", "draw_redraw"], "greedy_lazy": ["walk"], "tree_lazy": ["walk"],
+          "ngram": ["draft"], "typical": ["walk", "draw_redraw"], "onehot": ["walk", "draw_redraw"]}
 
 
 def parse_args():
@@ -549,29 +549,34 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None, 
                     "mean_drafts": float(outs[0].float().mean().item()),
                     "bytes_note": "every history token once; the search stops at the first chunk holding a match"})
     if mode.endswith("_lazy") or mode in ("typical", "onehot"):
-        # bytes the walks read in the last step, from its outputs: chain greedy reads rows
-        # 0..k; tree greedy the rows of the accepted nodes (at least the path); chain
-        # sampling the (max, sum) pass over target rows 0..k and draft rows 0..min(k, gamma-1),
-        # then a residual pass over 2 rows (k < gamma) or a bonus pass over 1 row
+        # bytes the walk kernel needs to read in the last step, from its outputs: chain greedy
+        # reads rows 0..k, tree greedy the rows of the accepted nodes (at least the path), the
+        # level walks target rows 0..k (and for the sampling chain draft rows
+        # 0..min(k, gamma-1)); the sampling chain's step then reads 2 rows for the residual
+        # (k < gamma) or 1 for the bonus, the other level walks row k once more for the draw
         s = 2 if cfg["dtype"] == "bf16" else 4
         a = outs[0].long().cpu()
         a = a[a >= 0]
         if mode == "sample_lazy":
             g = cfg["gamma"]
-            rows_read = ((a + 1) + torch.clamp(a + 1, max=g) + torch.where(a < g, 2, 1)).sum().item()
-        elif mode in ("typical", "onehot"):  # target rows 0..k, then row k again for the draw
-            rows_read = (a + 2).sum().item()
+            walk_rows = ((a + 1) + torch.clamp(a + 1, max=g)).sum().item()
+            step_rows = walk_rows + torch.where(a < g, 2, 1).sum().item()
+        elif mode in ("typical", "onehot"):
+            walk_rows = (a + 1).sum().item()
+            step_rows = walk_rows + a.numel()
         else:
-            rows_read = (a + 1).sum().item()
-        lb = rows_read * cfg["V"] * s
-        res.update({"hbm_gbs_step": None, "frac_of_8tbs_step": None,
-                    "lazy": "one CTA per sequence reads only the rows the rule needs",
-                    "rows_read_per_step": rows_read,
-                    "roofline": {"bound": "hbm", "kernel": kernel, "achieved": lb / (ms_step / 1e3) / 1e9,
-                                 "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                                 "frac": lb / (ms_step / 1e3) / 1e9 / peak, "bytes_per_launch": lb,
-                                 "traffic": None,
-                                 "note": "bytes the walks read (a lower bound for tree greedy), over the step time"}})
+            walk_rows = step_rows = (a + 1).sum().item()
+        lb, sb = walk_rows * cfg["V"] * s, step_rows * cfg["V"] * s
+        level = kernel == "level_kernel"
+        res.update({"hbm_gbs_step": sb / (ms_step / 1e3) / 1e9, "frac_of_8tbs_step": sb / (ms_step / 1e3) / 8e12,
+                    "lazy": ("a level-synchronous walk over the whole GPU reads only the rows the rule needs"
+                             if level else "one CTA per sequence reads only the rows the rule needs"),
+                    "rows_read_per_step": step_rows,
+                    "roofline": {"bound": "hbm", "kernel": kernel, "achieved": lb / (dom_ms / 1e3) / 1e9,
+                                 "peak": peak, "peak_kind": peak_kind + " copy (read+write) bandwidth",
+                                 "unit": "GB/s", "frac": lb / (dom_ms / 1e3) / 1e9 / peak, "bytes_per_launch": lb,
+                                 "traffic": committed_traffic(kernel, name),
+                                 "note": "bytes the walk needs (a lower bound for tree greedy) over the walk's time"}})
     return res, inputs, call
 
 
@@ -589,6 +594,9 @@ def measure_e2e(name, inputs, steps, dev, **ov):
     keys = {"sample": ["target", "draft", "draft_tokens"], "greedy": ["target", "draft_tokens"],
             "tree": ["target", "node_tokens"],
             "tree_sample": ["target", "draft", "node_tokens"]}[mode]
+    target_only = bool(cfg.get("typical") or cfg.get("onehot"))  # no draft logits
+    if target_only:
+        keys = ["target", "draft_tokens"]
     for k in keys:
         t = getattr(inputs, k)
         host_in[k] = t.cpu().pin_memory()
@@ -601,7 +609,9 @@ def measure_e2e(name, inputs, steps, dev, **ov):
     def step():
         for k in keys:
             dev_in[k].copy_(host_in[k], non_blocking=True)
-        if mode == "sample":
+        if target_only:
+            call(dev_in["target"], dev_in["draft_tokens"])
+        elif mode == "sample":
             call(dev_in["target"], dev_in["draft"], dev_in["draft_tokens"])
         elif mode == "greedy":
             call(dev_in["target"], dev_in["draft_tokens"])

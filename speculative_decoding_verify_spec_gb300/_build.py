@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libspecverify.so")
 OBJ_DIR = os.path.join(ROOT, "_build")
 SOURCES = ["sv_api.cu", "sv_sample.cu", "sv_greedy.cu", "sv_refine.cu", "sv_tree_sample.cu", "sv_tree_refine.cu",
-           "sv_lazy.cu", "sv_ngram.cu", "sv_noalloc.cu", "sv_typical.cu"]
+           "sv_lazy.cu", "sv_ngram.cu", "sv_noalloc.cu", "sv_level.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -28,6 +28,7 @@ struct Layout {
     size_t partial = 0, rowstat = 0, plan = 0, csum = 0;
     size_t rctl = 0, rbar = 0, rlist = 0, rsum = 0, ramb = 0, rresc = 0;  // re-draw: control + marks, barrier, records, scratch
     size_t rec = 0, et = 0, us = 0, npos = 0, um = 0, pmax = 0, pcnt = 0;  // re-walk (tree sampling; rctl, rsum too)
+    size_t zpart = 0, lctl = 0, lact = 0, tcnt = 0, lstate = 0, lavail = 0;  // the level walks
     size_t total = 0;
 };
 
@@ -63,30 +64,28 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
     const size_t ntile = size_t(ntile_of(V, dtype));
     size_t R = 0;
     switch (mode) {
-    case SV_MODE_SAMPLE: R = size_t(2) * rows + 1; break;
+    case SV_MODE_SAMPLE:
+    case SV_MODE_SAMPLE_LAZY: R = size_t(2) * rows + 1; break;
+    case SV_MODE_TYPICAL:
+    case SV_MODE_SAMPLE_ONEHOT: R = size_t(rows) + 1; break;
     case SV_MODE_GREEDY: R = size_t(rows) + 1; break;
     case SV_MODE_TREE:
     case SV_MODE_ROW_STATS: R = size_t(rows); break;
-    case SV_MODE_TYPICAL:  // the unit masses of each stop row, then the re-draw (one position)
-    case SV_MODE_SAMPLE_ONEHOT:
-    case SV_MODE_TREE_SAMPLE:
-    case SV_MODE_SAMPLE_LAZY: {
+    case SV_MODE_TREE_SAMPLE: {
         L.partial = 0;
         size_t off = up256(size_t(B) * size_t(nrt_of(V, dtype)) * 4);
         L.rowstat = off;
         off += up256(size_t(B) * sv::kTreeSampleCluster * 2 * 8);
-        const size_t K =
-            (mode == SV_MODE_TYPICAL || mode == SV_MODE_SAMPLE_ONEHOT) ? 1 : size_t(rec_positions(mode, rows));
+        const size_t K = size_t(rec_positions(mode, rows));
         const size_t nu = size_t(sv::tree_refine_units(V)), S = sv::kMaxTreeRefine, C = sv::kTreeRefineCluster;
         L.rctl = off;
         off += up256((size_t(sv::kTrCtlWords) + 2 * size_t(B)) * 4);
         L.rec = off;
         off += up256(size_t(B) * K * 16);
-        const bool per_seq = mode == SV_MODE_TYPICAL || mode == SV_MODE_SAMPLE_ONEHOT;  // unit sums per sequence
         L.et = off;
-        off += per_seq ? 0 : up256(S * K * 2 * size_t(V) * 8);
+        off += up256(S * K * 2 * size_t(V) * 8);
         L.us = off;
-        off += up256(per_seq ? size_t(B) * nu * 8 : S * K * 2 * nu * 8);
+        off += up256(S * K * 2 * nu * 8);
         L.npos = off;
         off += up256(S * K * 4);
         L.um = off;
@@ -104,7 +103,9 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
     }
     L.partial = 0;
     size_t off = up256(size_t(B) * R * ntile * 8);
-    if (mode == SV_MODE_SAMPLE) {
+    const bool sampling = mode == SV_MODE_SAMPLE || mode == SV_MODE_SAMPLE_LAZY || mode == SV_MODE_TYPICAL ||
+                          mode == SV_MODE_SAMPLE_ONEHOT;
+    if (sampling) {
         L.rowstat = off;
         off += up256(size_t(B) * R * 8);
         L.plan = off;
@@ -123,7 +124,23 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
         L.ramb = off;
         off += up256(size_t(B) * nu * 4);
         L.rresc = off;
-        off += up256(size_t(sv::kRescanChunk) * (size_t(2) * rows + 1) * nu * 8);
+        off += up256(size_t(sv::kRescanChunk) * R * nu * 8);
+    }
+    if (sampling && mode != SV_MODE_SAMPLE) {  // the level walk's own words
+        if (mode == SV_MODE_TYPICAL) {
+            L.zpart = off;
+            off += up256(size_t(B) * R * ntile * 4);
+        }
+        L.lctl = off;
+        off += up256((size_t(8) + rows + 2) * 4);
+        L.lact = off;
+        off += up256(size_t(2) * B * 4);
+        L.tcnt = off;
+        off += up256(size_t(B) * 4);
+        L.lstate = off;
+        off += up256(size_t(B) * 4);
+        L.lavail = off;
+        off += up256(size_t(B) * 4);
     }
     L.total = off;
     return L;
@@ -166,6 +183,79 @@ thread_local int t_nevents = 0;
 
 cudaError_t mark(int s, cudaStream_t stream) { return sv::mark_stage(s, stream); }
 
+}  // namespace
+
+namespace {
+// The lazy walks of the sampling chain, of a one-hot q and of typical acceptance: the level
+// kernel reads rows 0 .. k of each sequence and plans its draw; then (the chain only) the
+// residual masses of the stop rows; then the draw with the double-float re-draw of every
+// near-boundary sequence.  Arguments already checked, except the workspace.
+sv_status level_walk(int rule, sv_mode mode, const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride,
+                     const void *draft_logits, int64_t d_batch_stride, int64_t d_row_stride, sv_dtype dtype, int B,
+                     int gamma, int V, const int32_t *draft_tokens, float temperature, float epsilon, float delta,
+                     uint64_t seed, uint64_t offset, int32_t *accepted_len, int32_t *out_tokens, void *workspace,
+                     size_t workspace_bytes, void *stream) {
+    const Layout L = layout(mode, B, gamma, V, dtype);
+    if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
+    const bool chain = rule == sv::kRuleSample;
+    const int ntile = ntile_of(V, dtype), nrt = nrt_of(V, dtype);
+    if (!tiles_fit(B, chain ? 2 * int64_t(gamma) + 1 : int64_t(gamma) + 1, ntile)) return SV_ERR_INVALID_ARG;
+    const bool vec = vec_ok(target_logits, t_batch_stride, t_row_stride, dtype) &&
+                     (!chain || gamma == 0 || vec_ok(draft_logits, d_batch_stride, d_row_stride, dtype));
+    const Logits t{target_logits, t_batch_stride, t_row_stride};
+    const Logits d{chain && gamma > 0 ? draft_logits : target_logits, d_batch_stride, d_row_stride};
+    const float c = float(1.4426950408889634 / double(temperature));  // log2(e) / T
+    const int dt = dtype == SV_BF16 ? 1 : 0;
+    const int R = chain ? 2 * gamma + 1 : gamma + 1;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int *rctl = reinterpret_cast<int *>(at(workspace, L.rctl));
+    int *rbar = reinterpret_cast<int *>(at(workspace, L.rbar));
+    int *lavail = reinterpret_cast<int *>(at(workspace, L.lavail));
+    sv::LevelArgs la;
+    la.t = t;
+    la.d = d;
+    la.B = B;
+    la.gamma = gamma;
+    la.V = V;
+    la.ntile = ntile;
+    la.R = R;
+    la.c = c;
+    la.x = draft_tokens;
+    la.seed = seed;
+    la.offset = offset;
+    la.epsilon = epsilon;
+    la.delta = delta;
+    la.partial = reinterpret_cast<float2 *>(at(workspace, L.partial));
+    la.zpart = reinterpret_cast<float *>(at(workspace, L.zpart));
+    la.rowstat = reinterpret_cast<float2 *>(at(workspace, L.rowstat));
+    la.plan = reinterpret_cast<int2 *>(at(workspace, L.plan));
+    la.accepted_len = accepted_len;
+    la.out_tokens = out_tokens;
+    la.rctl = rctl;
+    la.rbar = rbar;
+    la.lctl = reinterpret_cast<int *>(at(workspace, L.lctl));
+    la.lact = reinterpret_cast<int *>(at(workspace, L.lact));
+    la.tcnt = reinterpret_cast<int *>(at(workspace, L.tcnt));
+    la.lstate = reinterpret_cast<int *>(at(workspace, L.lstate));
+    la.lavail = lavail;
+    float *csum = reinterpret_cast<float *>(at(workspace, L.csum));
+    cudaError_t e = mark(0, s);
+    if (e == cudaSuccess) e = sv::launch_level(rule, dt, vec, la, s);
+    if (e == cudaSuccess) e = mark(1, s);
+    int st = 2;
+    if (e == cudaSuccess && chain && gamma > 0) {
+        e = sv::launch_residual_tiles(dt, vec, t, d, B, gamma, V, nrt, c, la.rowstat, la.plan, csum, s);
+        if (e == cudaSuccess) e = mark(st++, s);
+    }
+    if (e == cudaSuccess)
+        e = sv::launch_draw_refine(dt, vec, t, d, B, gamma, V, ntile, nrt, c, temperature, seed, offset, rule, R, lavail,
+                                   draft_tokens, la.partial, la.rowstat, la.plan, csum, accepted_len, out_tokens, rctl,
+                                   rbar, reinterpret_cast<sv::RefineInfo *>(at(workspace, L.rlist)),
+                                   at(workspace, L.rsum), reinterpret_cast<int *>(at(workspace, L.ramb)),
+                                   at(workspace, L.rresc), chain && gamma > 0, s);
+    if (e == cudaSuccess) e = mark(st, s);
+    return cuda_status(e);
+}
 }  // namespace
 
 namespace sv {
@@ -244,8 +334,9 @@ sv_status spec_verify_sample(const void *target_logits, int64_t t_batch_stride,
         e = sv::launch_residual_tiles(dt, vec, t, d, B, gamma, V, nrt, c, rowstat, plan, csum, s);
     if (e == cudaSuccess) e = mark(3, s);
     if (e == cudaSuccess)
-        e = sv::launch_draw_refine(dt, vec, t, d, B, gamma, V, ntile, nrt, c, temperature, seed, offset, draft_tokens,
-                                   partial, rowstat, plan, csum, accepted_len, out_tokens, rctl, rbar, rinfo,
+        e = sv::launch_draw_refine(dt, vec, t, d, B, gamma, V, ntile, nrt, c, temperature, seed, offset,
+                                   sv::kRuleSample, R, nullptr, draft_tokens, partial, rowstat, plan, csum, accepted_len,
+                                   out_tokens, rctl, rbar, rinfo,
                                    at(workspace, L.rsum), reinterpret_cast<int *>(at(workspace, L.ramb)),
                                    at(workspace, L.rresc), gamma > 0, s);
     if (e == cudaSuccess) e = mark(4, s);
@@ -354,7 +445,7 @@ sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_str
                                    reinterpret_cast<float2 *>(at(workspace, L.rowstat)), rw, K, accepted_len,
                                    out_tokens, out_path, s);
     if (e == cudaSuccess) e = mark(1, s);
-    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, false, rw, s);
+    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, rw, s);
     if (e == cudaSuccess) e = mark(2, s);
     if (e == cudaSuccess)
         e = sv::launch_tree_rewalk(dtype == SV_BF16, t, d, B, N, V, false, parent, node_tokens, max_depth, temperature,
@@ -377,37 +468,16 @@ sv_status spec_verify_sample_lazy(const void *target_logits, int64_t t_batch_str
     if (B == 0) return SV_OK;
     if (!target_logits || !accepted_len || !out_tokens) return SV_ERR_INVALID_ARG;
     if (gamma > 0 && (!draft_logits || !draft_tokens)) return SV_ERR_INVALID_ARG;
-    const Layout L = layout(SV_MODE_SAMPLE_LAZY, B, gamma, V, dtype);
-    if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
-    const bool vec = vec_ok(target_logits, t_batch_stride, t_row_stride, dtype) &&
-                     (gamma == 0 || vec_ok(draft_logits, d_batch_stride, d_row_stride, dtype));
-    const Logits t{target_logits, t_batch_stride, t_row_stride};
-    const Logits d{gamma > 0 ? draft_logits : target_logits, d_batch_stride, d_row_stride};
-    const float c = float(1.4426950408889634 / double(temperature));  // log2(e) / T
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const sv::TreeRefineWs rw = tree_refine_ws(L, workspace, B);
-    const int K = sv::tree_rec_nodes(gamma);
-    cudaError_t e = mark(0, s);
-    if (e == cudaSuccess)
-        e = sv::launch_tree_sample(dtype == SV_BF16, vec, t, d, B, gamma + 1, V, true, nullptr, draft_tokens, gamma,
-                                   c, seed, offset, 0, nrt_of(V, dtype), reinterpret_cast<float *>(at(workspace, 0)),
-                                   reinterpret_cast<float2 *>(at(workspace, L.rowstat)), rw, K, accepted_len,
-                                   out_tokens, nullptr, s);
-    if (e == cudaSuccess) e = mark(1, s);
-    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, false, rw, s);
-    if (e == cudaSuccess) e = mark(2, s);
-    if (e == cudaSuccess)
-        e = sv::launch_tree_rewalk(dtype == SV_BF16, t, d, B, gamma + 1, V, true, nullptr, draft_tokens, gamma,
-                                   temperature, seed, offset, 0, K, rw, accepted_len, out_tokens, nullptr, s);
-    if (e == cudaSuccess) e = mark(3, s);
-    return cuda_status(e);
+    return level_walk(sv::kRuleSample, SV_MODE_SAMPLE_LAZY, target_logits, t_batch_stride, t_row_stride,
+                      draft_logits, d_batch_stride, d_row_stride, dtype, B, gamma, V, draft_tokens, temperature, 0.f,
+                      0.f, seed, offset, accepted_len, out_tokens, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"
 
 namespace {
 // The target-only walks: typical acceptance (onehot = 0) or sampling against a one-hot q
-// (onehot = 1).  Both share the workspace layout of SV_MODE_TYPICAL.
+// (onehot = 1).
 sv_status target_walk(int onehot, const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride,
                       sv_dtype dtype, int B, int gamma, int V, const int32_t *draft_tokens, float temperature,
                       float epsilon, float delta, uint64_t seed, uint64_t offset, int32_t *accepted_len,
@@ -421,25 +491,10 @@ sv_status target_walk(int onehot, const void *target_logits, int64_t t_batch_str
         return SV_ERR_INVALID_ARG;
     if (B == 0) return SV_OK;
     if (!target_logits || !accepted_len || !out_tokens || (gamma > 0 && !draft_tokens)) return SV_ERR_INVALID_ARG;
-    const Layout L = layout(onehot ? SV_MODE_SAMPLE_ONEHOT : SV_MODE_TYPICAL, B, gamma, V, dtype);
-    if (sv_status st = check_workspace(L, workspace, workspace_bytes)) return st;
-    const sv::TreeRefineWs rw = tree_refine_ws(L, workspace, B);
-    const bool vec = vec_ok(target_logits, t_batch_stride, t_row_stride, dtype);
-    const Logits t{target_logits, t_batch_stride, t_row_stride};
-    const double cd = 1.4426950408889634 / double(temperature);  // log2(e) / T
-    const float c = float(cd), c_lo = float(cd - double(c));
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = mark(0, s);
-    if (e == cudaSuccess)
-        e = sv::launch_typical(dtype == SV_BF16, vec, t, B, gamma, V, draft_tokens, c, c_lo, onehot, epsilon, delta,
-                               seed, offset, nrt_of(V, dtype), reinterpret_cast<float *>(at(workspace, L.partial)), rw,
-                               accepted_len, out_tokens, s);
-    if (e == cudaSuccess) e = mark(1, s);
-    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, t, B, V, temperature, 1, true, rw, s);
-    if (e == cudaSuccess) e = mark(2, s);
-    if (e == cudaSuccess) e = sv::launch_typical_redraw(dtype == SV_BF16, t, B, gamma, V, temperature, seed, offset, rw, out_tokens, s);
-    if (e == cudaSuccess) e = mark(3, s);
-    return cuda_status(e);
+    return level_walk(onehot ? sv::kRuleOnehot : sv::kRuleTypical, onehot ? SV_MODE_SAMPLE_ONEHOT : SV_MODE_TYPICAL,
+                      target_logits, t_batch_stride, t_row_stride, nullptr, 0, 0, dtype, B, gamma, V, draft_tokens,
+                      temperature, epsilon, delta, seed, offset, accepted_len, out_tokens, workspace, workspace_bytes,
+                      stream);
 }
 }  // namespace
 

@@ -381,13 +381,17 @@ inline cudaError_t launch_after(void (*kernel)(Params...), unsigned grid, unsign
 }
 
 // One warp merges the n tile partials of a row: lane l takes tiles l, l + 32, ... in order,
-// then the lanes combine in a fixed butterfly.  Every lane returns the row's result.
+// then the lanes combine in a fixed butterfly.  Every lane returns the row's result.  L2:
+// read the partials at L2 (written by other SMs in the same kernel, after a fence).
+template <bool L2 = false>
 __device__ __forceinline__ float2 warp_merge_stats(const float2 *__restrict__ p, int n, float c, int lane) {
     float2 s = make_float2(-__int_as_float(0x7f800000), 0.f);
     for (int q0 = lane; q0 < n; q0 += 128) {
         float2 e[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) e[j] = q0 + 32 * j < n ? p[q0 + 32 * j] : make_float2(-__int_as_float(0x7f800000), 0.f);
+        for (int j = 0; j < 4; ++j)
+            e[j] = q0 + 32 * j < n ? (L2 ? __ldcg(p + q0 + 32 * j) : p[q0 + 32 * j])
+                                   : make_float2(-__int_as_float(0x7f800000), 0.f);
 #pragma unroll
         for (int j = 0; j < 4; ++j) s = merge_stats(s, e[j], c);
     }

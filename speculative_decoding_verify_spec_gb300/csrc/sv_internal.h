@@ -21,6 +21,11 @@ __host__ __device__ inline const char *row_ptr(const Logits &L, int bytes, int64
     return static_cast<const char *>(L.ptr) + (b * L.batch_stride + r * L.row_stride) * bytes;
 }
 
+// The sampling rules that share the draw and the re-draw: the chain (residual (p - q)+ after a
+// rejection), a one-hot draft distribution (p without the rejected token), typical
+// acceptance (the token at the stop drawn from p itself).
+constexpr int kRuleSample = 0, kRuleOnehot = 1, kRuleTypical = 2;
+
 // Extended-precision re-draw of near-boundary sampling sequences -----------------------
 // decide marks a sequence whose accept test had |u q - p| < kRefineAcceptWindow * max(p, u q)
 // (flag kRefineAccept); draw marks one whose threshold u'R lies within
@@ -82,8 +87,12 @@ cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B
 // Inverse-CDF draw of the final token on the stop row of every valid sequence, then the
 // extended-precision re-draw of every sequence it or decide marked (one cooperative grid;
 // rbar: its grid barrier's words; rsum, ramb, rresc: the re-draw's scratch, see above).
+// rule: kRuleSample / kRuleOnehot / kRuleTypical (which rows the rescan reads, and its test);
+// R: rows per sequence in partial / rowstat; lavail: rows a lazy walk read per sequence
+// (NULL: all of them).
 cudaError_t launch_draw_refine(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
-                               float c, float T, uint64_t seed, uint64_t offset, const int32_t *x, const void *partial,
+                               float c, float T, uint64_t seed, uint64_t offset, int rule, int R, const int *lavail,
+                               const int32_t *x, const void *partial,
                                const void *rowstat, const void *plan, const float *csum, int32_t *accepted_len,
                                int32_t *out_tokens, int *rctl, int *rbar, RefineInfo *rinfo, void *rsum, int *ramb,
                                void *rresc, bool early, cudaStream_t s);
@@ -134,8 +143,8 @@ inline int tree_rec_nodes(int max_depth) { return max_depth + 1 < kTreeRecNodes 
 inline size_t tree_refine_smem(int N, int max_depth) { return size_t(13 * N + max_depth + 1) * 4; }
 // The exponentials of the listed sequences' recorded rows (every resident CTA), then the
 // re-walk (one cluster of 16 CTAs per listed sequence where the device holds one, else 8).
-cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, bool per_seq,
-                            TreeRefineWs ws, cudaStream_t s);
+cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws,
+                            cudaStream_t s);
 cudaError_t launch_tree_rewalk(int dtype, Logits t, Logits d, int B, int N, int V, bool chain, const int32_t *parent,
                                const int32_t *node_tokens, int max_depth, float T, uint64_t seed, uint64_t offset,
                                int without_replacement, int K, TreeRefineWs ws, int32_t *accepted_len,
@@ -156,20 +165,6 @@ cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, i
 cudaError_t launch_greedy_walk(int dtype, bool vec, Logits t, int B, int N, int V, bool chain, const int32_t *parent,
                                const int32_t *tokens, int max_depth, int32_t *accepted_len, int32_t *out_tokens,
                                int32_t *out_path, cudaStream_t s);
-// Typical acceptance (onehot = 0) or sampling verification against a one-hot q (onehot =
-// 1), one CTA per sequence reading target rows 0 .. stop: tokens [B][gamma],
-// c + c_lo = log2(e) / T (the low part for the draw's weights); umass: [B][nunit] floats of
-// scratch, nunit = ceil(V / res_tile_elems).
-cudaError_t launch_typical(int dtype, bool vec, Logits t, int B, int gamma, int V, const int32_t *tokens, float c,
-                           float c_lo, int onehot, float epsilon, float delta, uint64_t seed, uint64_t offset,
-                           int nunit, float *umass, TreeRefineWs rw, int32_t *accepted_len, int32_t *out_tokens,
-                           cudaStream_t s);
-// The double-float re-draw of the typical walk's marked final tokens (one recorded position
-// per sequence: the stop row), after launch_tree_exp with K = 1 and per_seq (every marked
-// sequence, us[B][nunit]).
-cudaError_t launch_typical_redraw(int dtype, Logits t, int B, int gamma, int V, float T, uint64_t seed,
-                                  uint64_t offset, TreeRefineWs ws, int32_t *out_tokens, cudaStream_t s);
-constexpr float kTypicalCdfWindow = 1e-6f;  // marks a typical draw this close (x total) to a CDF boundary
 // Prompt-lookup drafting: history [B][stride] with lengths[B]; drafts [B][k], count [B].
 constexpr int kMaxNgram = 64;
 cudaError_t launch_ngram_draft(const int32_t *history, int64_t stride, const int32_t *lengths, int B, int n, int k,
@@ -184,6 +179,32 @@ cudaError_t launch_rowstats_finalize(int rows, int ntile, float c, float inv_t, 
                                      float *m_out, float *lse_out, cudaStream_t s);
 cudaError_t launch_uniforms(uint64_t seed, uint64_t offset, int B, int positions, int purpose,
                             float *out, cudaStream_t s);
+
+// Level-synchronous lazy walks (sv_level.cu) --------------------------------------------
+struct LevelArgs {
+    Logits t, d;                     // d: draft rows (the sampling chain only)
+    int B, gamma, V, ntile;
+    int R;                           // rows per sequence in partial / rowstat: 2 gamma + 1 (chain), else gamma + 1
+    float c;                         // log2(e) / T
+    const int32_t *x;                // draft tokens [B][gamma]
+    uint64_t seed, offset;
+    float epsilon, delta;            // typical acceptance's threshold
+    float2 *partial;                 // [B][R][ntile] (M, S) per 4 KB tile
+    float *zpart;                    // [B][R][ntile] Z per tile (typical acceptance)
+    float2 *rowstat;                 // [B][R] (M, S) of every row read
+    int2 *plan;                      // [B] (stop row, kind of draw: 0 from p, 1 residual, 2 p without x_k)
+    int32_t *accepted_len, *out_tokens;
+    int *rctl, *rbar;                // the draw kernel's re-draw control words and barrier (zeroed here)
+    int *lctl;                       // [8] this kernel's grid barrier, then [gamma + 2] level list lengths
+    int *lact;                       // [2][B] the sequences of the current and the next level
+    int *tcnt;                       // [B] tiles of the current step counted in
+    int *lstate;                     // [B] bit 0 walking, bit 1 marked for the rescan
+    int *lavail;                     // [B] rows 0 .. lavail - 1 read (what the rescan may use)
+};
+// The walk (a cooperative grid, one CTA of 768 threads per SM), after zeroing lctl's
+// barrier words and list lengths and tcnt.  A step fetches one level's rows, or every
+// remaining level's once that is at most 64 MB, and the finishing warp walks them in order.
+cudaError_t launch_level(int rule, int dtype, bool vec, const LevelArgs &a, cudaStream_t s);
 
 // Host-side helpers shared by the entry points ----------------------------------------
 inline int elem_bytes(sv_dtype d) { return d == SV_BF16 ? 2 : 4; }

@@ -41,6 +41,9 @@ namespace sv {
 struct RefineArgs {
     Logits t, d;
     int B, gamma, V;
+    int rule;                   // kRuleSample, kRuleOnehot or kRuleTypical
+    int R;                      // rows per sequence in rowstat: 2 gamma + 1 (chain), else gamma + 1
+    const int *lavail;          // rows 0 .. lavail[b] - 1 read by a lazy walk (NULL: every row)
     float T;
     uint64_t seed, offset;
     const int32_t *x;           // draft tokens [B][gamma]
@@ -74,6 +77,12 @@ __device__ __forceinline__ df ldcg_df(const df *p) {
 }
 __device__ __forceinline__ void st_df(df *p, df v) { *reinterpret_cast<float2 *>(p) = make_float2(v.hi, v.lo); }
 __device__ __forceinline__ df df_zero() { return df{0.f, 0.f}; }
+// A record written by another SM earlier in this grid: read at L2.
+__device__ __forceinline__ RefineInfo ldcg_info(const RefineInfo *p) {
+    const int4 a = __ldcg(reinterpret_cast<const int4 *>(p)), b = __ldcg(reinterpret_cast<const int4 *>(p) + 1);
+    return RefineInfo{a.x, a.y, a.z, a.w, __int_as_float(b.x), __int_as_float(b.y), __int_as_float(b.z),
+                      __int_as_float(b.w)};
+}
 
 // exp((x_j - M) / T) of this lane's logits of unit u (0 past the row's end).  Every lane of
 // the warp calls it together (the exponential's table comes by shuffle); tj = this lane's
@@ -276,7 +285,8 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
     if (!barrier()) return;  // every draw done, the lists complete
     const int nall = __ldcg(a.rctl + kRefineAll);
     if (__ldcg(a.rctl + kRefineMain) + nall == 0) return;  // (the same for every CTA)
-    const int gamma = a.gamma, V = a.V, B = a.B, R = 2 * gamma + 1;
+    const int gamma = a.gamma, V = a.V, B = a.B, R = a.R;
+    const bool onehot = a.rule == kRuleOnehot;
     const int nu = (V + kUnit - 1) / kUnit;
     const int64_t gw = (int64_t(blockIdx.x) * kThreads + tid) >> 5;
     const int64_t nw = (int64_t(gridDim.x) * kThreads) >> 5;
@@ -293,7 +303,7 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
     // The token inside unit u (warp 0 computes; every thread returns it): the weights of
     // target row k, or with resid the residual weights of row pair k.
     auto pick = [&](int64_t seq, int k, float Mt, float Md, df rho, bool with_resid, int u, df b0, df thr,
-                    bool force) -> int {
+                    bool force, int ex = -1) -> int {
         if (warp == 0) {
             df w[kLane];
             if (with_resid) {
@@ -303,6 +313,9 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
                 for (int e = 0; e < kLane; ++e) w[e] = resid(w[e], wd[e], rho);
             } else {
                 lane_exps<D>(trow(seq, k), Mt, inv_t, V, u, lane, tj, w);
+#pragma unroll
+                for (int e = 0; e < kLane; ++e)
+                    if (int64_t(u) * kUnit + lane * kLane + e == ex) w[e] = df_zero();  // the excluded token
             }
             const int tok = unit_pick(w, u, V, b0, thr, force, lane);
             if (lane == 0) sm.unit = tok;
@@ -325,7 +338,9 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
             const int c = int(it / (int64_t(R) * nu));
             const int loc = int(it - int64_t(c) * R * nu);
             const int ri = loc / nu, u = loc - ri * nu;
-            const int64_t seq = a.rinfo[B + c0 + c].seq;
+            const int64_t seq = ldcg_info(a.rinfo + B + c0 + c).seq;
+            const int avail = a.lavail ? __ldcg(a.lavail + seq) : gamma + 1;
+            if ((ri <= gamma ? ri : ri - gamma - 1) >= avail) continue;  // a row the lazy walk did not read
             df w[kLane];
             lane_exps<D>(stat_row(seq, ri), a.rowstat[seq * R + ri].x, inv_t, V, u, lane, tj, w);
             const df s = warp_sum_ordered(df_add(w[0], w[1]), lane);
@@ -333,20 +348,31 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
         }
         if (!barrier()) return;
         for (int c = blockIdx.x; c < nc; c += gridDim.x) {
-            RefineInfo info = a.rinfo[B + c0 + c];
+            RefineInfo info = ldcg_info(a.rinfo + B + c0 + c);
             const int64_t seq = info.seq;
             const df *rs = a.rresc + int64_t(c) * R * nu;
+            const int avail = a.lavail ? __ldcg(a.lavail + seq) : gamma + 1;
             int k2 = gamma;
-            for (int i = 0; i < gamma; ++i) {  // u e_d(x) S_t < e_t(x) S_d, left to right
-                df St, Sd;
+            bool bad = false;  // the walk reaches a row the lazy walk could not read (not a distribution)
+            for (int i = 0; i < gamma; ++i) {  // u e_d(x) S_t < e_t(x) S_d (one-hot: u S_t < e_t(x)), left to right
+                if (i >= avail) {
+                    bad = true;
+                    break;
+                }
+                df St, Sd = df_from(1.f);
                 block_sum2(nu, [&](int q) { return ldcg_df(rs + int64_t(i) * nu + q); },
-                           [&](int q) { return ldcg_df(rs + int64_t(gamma + 1 + i) * nu + q); }, &St, &Sd, sm);
+                           [&](int q) { return onehot ? df_zero() : ldcg_df(rs + int64_t(gamma + 1 + i) * nu + q); },
+                           &St, &Sd, sm);
                 if (tid == 0) {
                     const int32_t xi = a.x[seq * gamma + i];
                     const df et = weight_df(load_elem<D>(trow(seq, i), xi), a.rowstat[seq * R + i].x, inv_t);
-                    const df ed = weight_df(load_elem<D>(drow(seq, i), xi), a.rowstat[seq * R + gamma + 1 + i].x, inv_t);
                     const float uu = uniform01(a.seed, a.offset, uint32_t(seq), uint32_t(i), 0u);
-                    sm.i0 = df_lt(df_mul_f(df_mul(ed, St), uu), df_mul(et, Sd)) ? 0 : 1;
+                    if (onehot) {
+                        sm.i0 = df_lt(df_mul_f(St, uu), et) ? 0 : 1;
+                    } else {
+                        const df ed = weight_df(load_elem<D>(drow(seq, i), xi), a.rowstat[seq * R + gamma + 1 + i].x, inv_t);
+                        sm.i0 = df_lt(df_mul_f(df_mul(ed, St), uu), df_mul(et, Sd)) ? 0 : 1;
+                    }
                 }
                 __syncthreads();
                 const int rejected = sm.i0;
@@ -356,13 +382,17 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
                     break;
                 }
             }
+            if (k2 == gamma && gamma >= avail) bad = true;
             int32_t *out = a.out_tokens + seq * (gamma + 1);
             for (int i = tid; i <= gamma; i += kThreads) {
-                if (i < k2) out[i] = a.x[seq * gamma + i];
+                if (bad) out[i] = -1;
+                else if (i < k2) out[i] = a.x[seq * gamma + i];
                 else if (i > k2) out[i] = -1;
             }
-            if (tid == 0) a.accepted_len[seq] = k2;
-            if (k2 == gamma) {  // every draft accepted: the bonus draw from p_gamma, now
+            if (tid == 0) a.accepted_len[seq] = bad ? -1 : k2;
+            if (bad) {
+                if (tid == 0) atomicAdd(a.rctl + kRefineRedone, 1);
+            } else if (k2 == gamma) {  // every draft accepted: the bonus draw from p_gamma, now
                 df total, thr, b0;
                 bool force;
                 const int u = block_search(nu, uniform01(a.seed, a.offset, uint32_t(seq), uint32_t(gamma), 1u),
@@ -372,7 +402,7 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
                 if (tid == 0) finish(seq, gamma, tok);
             } else if (tid == 0) {  // a residual draw at the new stop row: onto the main list
                 info.k = k2;
-                info.mode = 1;
+                info.mode = onehot ? 2 : 1;
                 a.rinfo[atomicAdd(a.rctl + kRefineMain, 1)] = info;
             }
             __syncthreads();
@@ -386,13 +416,13 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
     const int64_t na = int64_t(nmain) * nu;
     for (int64_t it = gw; it < na; it += nw) {
         const int e = int(it / nu), u = int(it - int64_t(e) * nu);
-        const RefineInfo info = a.rinfo[e];
+        const RefineInfo info = ldcg_info(a.rinfo + e);
         const int64_t seq = info.seq;
         const int k = info.k;
         df *S = a.rsum + e * slot;
         const float2 st = a.rowstat[seq * R + k];
         df wt[kLane];
-        if (info.mode == 0) {  // a bonus draw: the target row's sums only
+        if (info.mode != 1) {  // a draw from p (a bonus draw, or p without a one-hot q's token): its sums only
             lane_exps<D>(trow(seq, k), st.x, inv_t, V, u, lane, tj, wt);
             const df at = warp_sum_ordered(df_add(wt[0], wt[1]), lane);
             if (lane == 0) st_df(S + u, at);
@@ -431,7 +461,7 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
 
     // F: one CTA per main-list sequence, the draw.
     for (int e = blockIdx.x; e < nmain; e += gridDim.x) {
-        const RefineInfo info = a.rinfo[e];
+        const RefineInfo info = ldcg_info(a.rinfo + e);
         const int64_t seq = info.seq;
         const int k = info.k;
         const df *S = a.rsum + e * slot;
@@ -486,6 +516,14 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
                 },
                 &total, &thr, &b0, &force, sm);
             if (df_pos(total)) tok = pick(seq, k, st.x, sd.x, rho, true, u, b0, thr, force);
+        }
+        if (tok < 0 && info.mode == 2) {  // p without the token a one-hot q put all its mass on
+            const int ex = a.x[seq * gamma + k], ex_u = ex / kUnit;
+            const df ex_w = weight_df(load_elem<D>(trow(seq, k), ex), st.x, inv_t);
+            const int u = block_search(
+                nu, u2, [&](int q) { return q == ex_u ? df_sub(all_t(q), ex_w) : all_t(q); }, &total, &thr, &b0, &force,
+                sm);
+            if (df_pos(total)) tok = pick(seq, k, st.x, 0.f, df_zero(), false, u, b0, thr, force, ex);
         }
         if (tok < 0) {  // a bonus draw, or no residual mass at all: the draw from p on row k
             const int u = block_search(nu, u2, all_t, &total, &thr, &b0, &force, sm);

@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, kResidualCtas)
         const int64_t seq = it / nrt;
         const int64_t run_end = (seq + 1) * nrt < end ? (seq + 1) * nrt : end;
         const int2 pl = plan[seq];
-        if (pl.y == 1) {  // uniform over the warp
+        if (pl.y == 1 && pl.x >= 0 && pl.x < gamma) {  // uniform over the warp (a plan out of range: no work)
             const int k = pl.x;
             const float2 st = rowstat[seq * R + k], sd = rowstat[seq * R + gamma + 1 + k];
             const float inv_st = 1.f / st.y, inv_sd = 1.f / sd.y;
@@ -298,22 +298,28 @@ __global__ void __launch_bounds__(kThreads, kResidualCtas)
 // for the sequence (plan, statistics of its stop rows, its mark) and the draw's uniform.
 template <class D, bool VEC>
 __device__ __forceinline__ void draw_sequence(Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
-                                              float c, const float2 *__restrict__ partial,
+                                              int R, const int32_t *__restrict__ x, float c,
+                                              const float2 *__restrict__ partial,
                                               const float *__restrict__ csum, int32_t *__restrict__ out_tokens,
                                               int *__restrict__ rflag, int *__restrict__ rctl,
                                               RefineInfo *__restrict__ rinfo, int64_t seq, int2 pl, float2 st,
                                               float2 sdk, int flag0, float u1,
                                               int lane) {
-    const int R = 2 * gamma + 1;
     if (pl.y < 0) return;  // invalid sequence: outputs already written by decide
     const int k = pl.x;
-    int mode = pl.y;  // 1: residual after a rejection, 0: bonus draw from p
+    int mode = pl.y == 1 ? 1 : 0;  // 1: residual after a rejection, 0: a draw from p
+    // pl.y == 2 (a one-hot q rejected x_k): the draw from p without x_k, i.e. its tile's mass
+    // less x_k's weight and x_k's own weight 0
+    int ex = pl.y == 2 ? x[seq * gamma + k] : -1;
+    const float w_ex = ex >= 0 ? weight(load_elem<D>(row_ptr(t, D::kBytes, seq, k), ex), st.x, c) : 0.f;
+    const int ex_tile = ex >= 0 ? ex / tile_elems<D>() : -1;
     const float2 *prow = partial + (seq * R + k) * ntile;
     const float *crow = csum + seq * nrt;
     auto unit_mass = [&](int u) -> float {
         if (mode) return crow[u];
         const float2 p = prow[u];
-        return p.y * weight(p.x, st.x, c);  // mass of tile u under 2^((l - M) c)
+        const float m = p.y * weight(p.x, st.x, c);  // mass of tile u under 2^((l - M) c)
+        return u == ex_tile ? fmaxf(__fsub_rn(m, w_ex), 0.f) : m;
     };
 
     // this lane's first kKeep unit masses stay in registers for the walk below.  The prefixes
@@ -340,8 +346,12 @@ __device__ __forceinline__ void draw_sequence(Logits t, Logits d, int B, int gam
         }
         incl = df_warp_scan(lacc.value(), lane);
         totd = df_shfl(incl, 31);
-        if (mode == 1 && !(totd.hi > 0.f)) mode = 0;  // exact-zero residual: draw from p
-        else break;
+        if ((mode == 1 || ex >= 0) && !(totd.hi > 0.f)) {  // exact-zero residual: draw from p
+            mode = 0;
+            ex = -1;
+        } else {
+            break;
+        }
     }
     const df thr = df_mul_f(totd, u1);
 
@@ -417,10 +427,10 @@ __device__ __forceinline__ void draw_sequence(Logits t, Logits d, int B, int gam
         const int e0 = (lane * VPL + v) * D::EPV;
         dv[v] = (mode && e0 < len) ? load_vec<D, VEC>(dp, u0, e0, len) : neg_inf_vec<D>();
     }
-    auto w_at = [&](const uint4 &t4, const uint4 &d4, int e) -> float {
+    auto w_at = [&](const uint4 &t4, const uint4 &d4, int e, int j) -> float {  // j: index in the unit
         const float tj = vec_elem<D>(t4, e);
         return mode ? residual_weight(tj, vec_elem<D>(d4, e), c, st.x, inv_st, sd.x, inv_sd)
-                    : weight(tj, st.x, c);
+                    : (u0 + j == ex ? 0.f : weight(tj, st.x, c));
     };
     PairSum lsum;
     int lastpos = -1;
@@ -430,7 +440,7 @@ __device__ __forceinline__ void draw_sequence(Logits t, Logits d, int B, int gam
             const int e0 = (lane * VPL + v) * D::EPV;
 #pragma unroll
             for (int e = 0; e < D::EPV; ++e) {
-                const float w = w_at(tv[v], dv[v % kResVecs], e);
+                const float w = w_at(tv[v], dv[v % kResVecs], e, e0 + e);
                 lsum.add(w);
                 if (e0 + e < len && w > 0.f) lastpos = e0 + e;
             }
@@ -456,7 +466,7 @@ __device__ __forceinline__ void draw_sequence(Logits t, Logits d, int B, int gam
             if (r < ne2 && lane * ne2 + r < NE && j < len) {
                 const float tj = load_elem<D>(tp, u0 + j);
                 w2[r] = mode ? residual_weight(tj, load_elem<D>(dp, u0 + j), c, st.x, inv_t1, sd.x, inv_d1)
-                             : weight(tj, st.x, c);
+                             : (u0 + j == ex ? 0.f : weight(tj, st.x, c));
             }
         }
         PairSum ps;
@@ -492,10 +502,12 @@ __device__ __forceinline__ void draw_sequence(Logits t, Logits d, int B, int gam
     // needed a rounding fallback, or a sequence decide marked) is redone in extended precision
     if (lane == 0) {
         out_tokens[seq * (gamma + 1) + k] = int32_t(u0 + tok);
-        const bool near = first == kNoIndex || force_last || unit_fallback || mode != pl.y ||
+        const bool fell_back = (pl.y == 1 && mode == 0) || (pl.y == 2 && ex < 0);  // no residual mass
+        // (a draw from p weighs in units of the row maximum's weight, not of S; without x_k its
+        // tile's mass carries the subtraction's rounding too)
+        const bool near = first == kNoIndex || force_last || unit_fallback || fell_back ||
                           !(g >= (mode ? kRefineCdfWindowRes * totd.hi + token_window(st.y) + token_window(sd.y)
-                                       : kRefineCdfWindow * totd.hi + kTokenWindow * fminf(1.f, st.y - 1.f)));
-        // (mode 0 weighs in units of the row maximum's weight, not of S)
+                                       : kRefineCdfWindow * totd.hi + kTokenWindow * (fminf(1.f, st.y - 1.f) + w_ex)));
         int flag = flag0;
         if (near && flag == 0) flag = kRefineDraw;
         if (flag != 0) {  // listed: a marked accept test on the rescan list, a draw on the main list
@@ -516,8 +528,9 @@ __device__ __forceinline__ void draw_sequence(Logits t, Logits d, int B, int gam
 template <class D, bool VEC>
 __global__ void __launch_bounds__(kThreads, 2)
     draw_refine_kernel(Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt, float c, float T,
-                       uint64_t seed, uint64_t offset, const int32_t *__restrict__ x,
-                       const float2 *__restrict__ partial, const float2 *__restrict__ rowstat,
+                       uint64_t seed, uint64_t offset, int rule, int R, const int *__restrict__ lavail,
+                       const int32_t *__restrict__ x, const float2 *__restrict__ partial,
+                       const float2 *__restrict__ rowstat,
                        const int2 *__restrict__ plan, const float *__restrict__ csum,
                        int32_t *__restrict__ accepted_len, int32_t *__restrict__ out_tokens, int *__restrict__ rctl,
                        int *__restrict__ rbar, RefineInfo *__restrict__ rinfo, df *__restrict__ rsum,
@@ -527,7 +540,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int lane = threadIdx.x & 31;
     const int64_t gw = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int64_t nw = (int64_t(gridDim.x) * kThreads) >> 5;
-    const int R = 2 * gamma + 1;
     int *rflag = rctl + kRefineCtlWords;
     int2 pl = make_int2(-1, -1);
     float2 st = make_float2(0.f, 1.f), sdk = make_float2(0.f, 1.f);
@@ -535,6 +547,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     float u1 = 0.f;
     auto read_plan = [&](int64_t seq) {
         pl = __ldcg(plan + seq);
+        // a plan out of range (only if the kernel that writes plans stopped early) draws nothing
+        if (pl.x < 0 || pl.x > gamma || pl.y < 0 || pl.y > 2 || (pl.y == 1 && pl.x == gamma)) pl = make_int2(-1, -1);
         st = make_float2(0.f, 1.f);
         sdk = make_float2(0.f, 1.f);
         flag0 = 0;
@@ -550,11 +564,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int64_t seq = gw; seq < B; seq += nw) {
         if (!(early && seq == gw)) read_plan(seq);
         if (pl.y >= 0)  // (an invalid sequence's outputs were written by decide)
-            draw_sequence<D, VEC>(t, d, B, gamma, V, ntile, nrt, c, partial, csum, out_tokens, rflag, rctl, rinfo,
-                                  seq, pl, st, sdk, flag0, u1, lane);
+            draw_sequence<D, VEC>(t, d, B, gamma, V, ntile, nrt, R, x, c, partial, csum, out_tokens, rflag, rctl,
+                                  rinfo, seq, pl, st, sdk, flag0, u1, lane);
     }
-    const RefineArgs ra{t, d, B, gamma, V, T, seed, offset, x, rowstat, rctl, rbar, rinfo, rsum, ramb, rresc,
-                        accepted_len, out_tokens};
+    const RefineArgs ra{t, d, B, gamma, V, rule, R, lavail, T, seed, offset, x, rowstat, rctl, rbar, rinfo, rsum,
+                        ramb, rresc, accepted_len, out_tokens};
     refine_phases<D>(ra, sm);
 }
 
@@ -636,7 +650,8 @@ cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B
 }
 
 cudaError_t launch_draw_refine(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,
-                               float c, float T, uint64_t seed, uint64_t offset, const int32_t *x, const void *partial,
+                               float c, float T, uint64_t seed, uint64_t offset, int rule, int R, const int *lavail,
+                               const int32_t *x, const void *partial,
                                const void *rowstat, const void *plan, const float *csum, int32_t *accepted_len,
                                int32_t *out_tokens, int *rctl, int *rbar, RefineInfo *rinfo, void *rsum, int *ramb,
                                void *rresc, bool early, cudaStream_t s) {
@@ -645,7 +660,8 @@ cudaError_t launch_draw_refine(int dtype, bool vec, Logits t, Logits d, int B, i
     unsigned grid = 0;  // every resident slot, at most one warp per sequence for the draws
     cudaError_t e = persistent_grid(k, int64_t(1) << 40, &grid);
     if (e != cudaSuccess) return e;
-    return launch_after_ex(true, k, grid, kThreads, 0, s, t, d, B, gamma, V, ntile, nrt, c, T, seed, offset, x,
+    return launch_after_ex(true, k, grid, kThreads, 0, s, t, d, B, gamma, V, ntile, nrt, c, T, seed, offset, rule, R,
+                           lavail, x,
                            static_cast<const float2 *>(partial), static_cast<const float2 *>(rowstat),
                            static_cast<const int2 *>(plan), csum, accepted_len, out_tokens, rctl, rbar, rinfo,
                            static_cast<df *>(rsum), ramb, static_cast<df *>(rresc), early);

@@ -13,8 +13,7 @@
 //   tree_exp_kernel     the whole grid: for every recorded node of the first eight marked
 //                       sequences, e_t(j) = exp((t_j - M_t) / T) and e_d(j) of its target
 //                       and draft rows, stored with their 256-logit unit sums and q's
-//                       support size (for the target-only rules: the unit sums of every
-//                       marked sequence's stop row);
+//                       support size;
 //   tree_rewalk_kernel  eight thread-block clusters, each taking every eighth marked
 //                       sequence in turn (the first one with those stored values, later ones
 //                       computing them in the cluster), its CTAs owning
@@ -131,12 +130,10 @@ __device__ df exp_unit(const char *row, float M, df inv_t, int V, int u, df *E, 
 }  // namespace
 
 // The exponentials of the recorded nodes of the first kMaxTreeRefine marked sequences
-// (grid-stride over (slot, position, row, unit), one warp per unit).  per_seq (the
-// target-only walks, one recorded row per sequence): the unit sums of the recorded row of
-// EVERY marked sequence instead, stored per sequence (us[b][nunit]), no exponentials.
+// (grid-stride over (slot, position, row, unit), one warp per unit).
 template <class D>
 __global__ void __launch_bounds__(kThreads)
-    tree_exp_kernel(Logits t, Logits d, int B, int V, float T, int K, bool per_seq, TreeRefineWs ws) {
+    tree_exp_kernel(Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws) {
     __shared__ int s_seq[kMaxTreeRefine];
     __shared__ unsigned s_bal[kWarps];
     __shared__ int s_cnt[2];
@@ -146,20 +143,6 @@ __global__ void __launch_bounds__(kThreads)
     const int nunit = tree_refine_units(V);
     const df inv_t = df_div(df_from(1.f), df_from(T));
     const int64_t nw = int64_t(gridDim.x) * kWarps;
-    if (per_seq) {
-        const int64_t items = int64_t(B) * nunit;
-        for (int64_t it = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); it < items; it += nw) {
-            const int64_t seq = it / nunit;
-            const int u = int(it - seq * nunit);
-            if (!__ldcg(ws.mark + seq)) continue;  // (uniform over the warp)
-            const float4 rec = __ldcg(ws.rec + seq);
-            df w[kDfLane];
-            unit_exps<D>(row_ptr(t, D::kBytes, seq, __float_as_int(rec.x)), rec.y, inv_t, V, u, lane, w);
-            const df us = unit_sum(w, lane);
-            if (lane == 0) st_df(ws.us + seq * nunit + u, us);
-        }
-        return;
-    }
     int total = 0;
     const int n = list_marked(ws.mark, B, s_seq, s_bal, s_cnt, &total);
     if (n == 0) return;
@@ -184,59 +167,6 @@ __global__ void __launch_bounds__(kThreads)
             if (r == 1 && cnt) atomicAdd(ws.npos + int64_t(j) * K + k, cnt);
         }
     }
-}
-
-// The double-float re-draw of the target-only walk's final token (typical acceptance, or
-// one-hot q), one warp per marked sequence -- every marked sequence.  The walk recorded the
-// stop row k (one position, with the token a one-hot q's residual excludes) and
-// tree_exp_kernel stored the unit sums of e(j) = exp((t_j - M) / T) over that row.  The
-// token is the first j with e(0) + ... + e(j) > u' x S over the included logits (u' = U(b,
-// k, purpose 1)): the unit by a warp search over the unit sums, then inside the unit (its
-// exponentials again) as the re-walk's draw does.  Only out_tokens[b][k] changes (the
-// accepted prefix was decided by the walk).
-template <class D>
-__global__ void __launch_bounds__(kThreads)
-    typical_redraw_kernel(Logits t, int B, int gamma, int V, float T, uint64_t seed, uint64_t offset, TreeRefineWs ws,
-                          int32_t *__restrict__ out_tokens) {
-    griddep_launch_next();
-    griddep_wait();  // the unit sums of the stop rows
-    const int lane = threadIdx.x & 31;
-    const int64_t seq = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-    if (seq >= B || !__ldcg(ws.mark + seq)) return;
-    const float4 rec = __ldcg(ws.rec + seq);  // one recorded position: the stop row
-    const int k = __float_as_int(rec.x);
-    const int xk = __float_as_int(rec.z);  // a token the draw excludes (one-hot q), else -1
-    const int nunit = tree_refine_units(V);
-    const df inv_t = df_div(df_from(1.f), df_from(T));
-    const char *row = row_ptr(t, D::kBytes, seq, k);
-    const df *U = ws.us + seq * nunit;
-    const int ex_u = xk >= 0 ? xk / kDfUnit : -1;
-    const df ex_v = xk >= 0 ? weight1_df(load_elem<D>(row, xk), rec.y, inv_t) : df_zero();
-    const float u2 = uniform01(seed, offset, uint32_t(seq), uint32_t(k), 1u);
-    const df thr = df_mul_f(warp_total(U, 1, nunit, lane, ex_u, ex_v), u2);
-    df run;
-    bool force;
-    int u = warp_search(U, 1, nunit, df_zero(), thr, false, &run, &force, lane, ex_u, ex_v);
-    if (u < 0) u = 0;
-    df w[kDfLane];
-    unit_exps<D>(row, rec.y, inv_t, V, u, lane, w);
-    const int64_t j0 = int64_t(u) * kDfUnit + lane * kDfLane;
-#pragma unroll
-    for (int e = 0; e < kDfLane; ++e)
-        if (j0 + e == xk) w[e] = df_zero();
-    const int tok = unit_pick(w, int64_t(u) * kDfUnit, j0, V, run, thr, force, lane);
-    if (lane == 0) {
-        out_tokens[seq * (gamma + 1) + k] = tok;
-        atomicAdd(ws.ctl + kTrMarked, 1);
-        atomicAdd(ws.ctl + kTrRedone, 1);
-    }
-}
-
-cudaError_t launch_typical_redraw(int dtype, Logits t, int B, int gamma, int V, float T, uint64_t seed,
-                                  uint64_t offset, TreeRefineWs ws, int32_t *out_tokens, cudaStream_t s) {
-    auto k = dtype == 1 ? typical_redraw_kernel<BF16> : typical_redraw_kernel<F32>;
-    return launch_after(k, unsigned((int64_t(B) * 32 + kThreads - 1) / kThreads), kThreads, 0, s, t, B, gamma, V, T,
-                        seed, offset, ws, out_tokens);
 }
 
 // The re-walk: cluster j (CS CTAs) takes the marked sequences of rank j, j + 8, j + 16, ...
@@ -667,12 +597,12 @@ __global__ void __launch_bounds__(kRwThreads, 1)
     }
 }
 
-cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, bool per_seq,
-                            TreeRefineWs ws, cudaStream_t s) {
+cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws,
+                            cudaStream_t s) {
     auto ke = dtype == 1 ? tree_exp_kernel<BF16> : tree_exp_kernel<F32>;
     unsigned grid = 0;  // every resident CTA
     cudaError_t e = persistent_grid(ke, int64_t(1) << 40, &grid);
-    if (e == cudaSuccess) e = launch_after(ke, grid, kThreads, 0, s, t, d, B, V, T, K, per_seq, ws);
+    if (e == cudaSuccess) e = launch_after(ke, grid, kThreads, 0, s, t, d, B, V, T, K, ws);
     return e;
 }
 

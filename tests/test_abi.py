@@ -77,9 +77,13 @@ def test_workspace_sizes(lib):
     for mode in (1, 2, 3, 8):
         assert off(mode, 64, 8, 32000, 1) == none
     assert off(0, 0, 8, 32000, 1) == none and off(0, 4, 8, 0, 1) == none and off(0, 4, 8, 10, 5) == none
-    # typical acceptance / one-hot sampling: 4 bytes per residual unit per sequence, plus the
-    # re-draw's unit sums of every sequence's stop row (8 bytes per 256 logits)
-    assert ws(6, 256, 8, 128256, 1) == ws(7, 256, 8, 128256, 1) >= 256 * 126 * 4 + 256 * 501 * 8
+    # the lazy walks (chain sampling, typical, one-hot): the sampling layout for their rows
+    # (2 gamma + 1, or gamma + 1 target rows), plus the walk's lists and counters; typical
+    # acceptance adds one float per tile for the entropy's moment
+    assert ws(5, 256, 8, 128256, 1) >= ws(0, 256, 8, 128256, 1) + 4 * 5 * 256
+    one_hot = ws(7, 256, 8, 128256, 1)
+    assert one_hot >= 256 * 9 * 63 * 8 + 256 * 5 * 2004 * 8
+    assert ws(6, 256, 8, 128256, 1) >= one_hot + 256 * 9 * 63 * 4
 
 
 P = ctypes.c_void_p
