@@ -177,16 +177,23 @@ __device__ __forceinline__ int block_search(int n, float u, Val val, df *total, 
     if (int(threadIdx.x) == first) {  // walk this thread's run in the order it was summed
         df r = first > 0 ? sm.incl[first - 1] : df_zero();
         int unit = -1, last = first * per;
-        for (int q = 0; q < per; ++q) {
-            const int i = first * per + q;
-            if (i >= n) break;
-            last = i;
-            const df nx = df_add(r, val(i));
-            if (df_gt(nx, *thr)) {
-                unit = i;
-                break;
+        for (int q0 = 0; q0 < per && unit < 0; q0 += kBatch) {  // a batch's loads in flight together
+            df v[kBatch];
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                const int i = first * per + q0 + q;
+                v[q] = (q0 + q < per && i < n) ? val(i) : df_zero();
             }
-            r = nx;
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                const int i = first * per + q0 + q;
+                if (unit < 0 && q0 + q < per && i < n) {
+                    last = i;
+                    const df nx = df_add(r, v[q]);
+                    if (df_gt(nx, *thr)) unit = i;
+                    else r = nx;
+                }
+            }
         }
         sm.unit = unit >= 0 ? unit : last;
         sm.base = r;
@@ -403,6 +410,12 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
             } else if (tid == 0) {  // a residual draw at the new stop row: onto the main list
                 info.k = k2;
                 info.mode = onehot ? 2 : 1;
+                const float2 st2 = a.rowstat[seq * R + k2];
+                const float2 sd2 = onehot ? make_float2(0.f, 1.f) : a.rowstat[seq * R + gamma + 1 + k2];
+                info.Mt = st2.x;
+                info.St = st2.y;
+                info.Md = sd2.x;
+                info.Sd = sd2.y;
                 a.rinfo[atomicAdd(a.rctl + kRefineMain, 1)] = info;
             }
             __syncthreads();
@@ -420,7 +433,7 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
         const int64_t seq = info.seq;
         const int k = info.k;
         df *S = a.rsum + e * slot;
-        const float2 st = a.rowstat[seq * R + k];
+        const float2 st = make_float2(info.Mt, info.St);  // the draw's copy of rowstat (no extra read)
         df wt[kLane];
         if (info.mode != 1) {  // a draw from p (a bonus draw, or p without a one-hot q's token): its sums only
             lane_exps<D>(trow(seq, k), st.x, inv_t, V, u, lane, tj, wt);
@@ -428,7 +441,7 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
             if (lane == 0) st_df(S + u, at);
             continue;
         }
-        const float2 sd = a.rowstat[seq * R + gamma + 1 + k];
+        const float2 sd = make_float2(info.Md, info.Sd);
         df wd[kLane];
         lane_exps2<D>(trow(seq, k), st.x, drow(seq, k), sd.x, inv_t, V, u, lane, tj, wt, wd);
         const df at = warp_sum_ordered(df_add(wt[0], wt[1]), lane);
@@ -468,13 +481,13 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
         df *fix = a.rsum + e * slot + 4 * int64_t(nu);
         const int *near = a.ramb + int64_t(e) * nu;
         const float u2 = uniform01(a.seed, a.offset, uint32_t(seq), uint32_t(k), 1u);
-        const float2 st = a.rowstat[seq * R + k];
+        const float2 st = make_float2(info.Mt, info.St);
         auto all_t = [&](int q) { return ldcg_df(S + q); };
         df total, thr, b0;
         bool force;
         int tok = -1;
         if (info.mode == 1) {
-            const float2 sd = a.rowstat[seq * R + gamma + 1 + k];
+            const float2 sd = make_float2(info.Md, info.Sd);
             df St, Sd;
             block_sum2(nu, all_t, [&](int q) { return ldcg_df(S + nu + q); }, &St, &Sd, sm);
             const df rho = df_div(St, Sd);
