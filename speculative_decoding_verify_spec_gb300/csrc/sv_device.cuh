@@ -355,6 +355,21 @@ __device__ __forceinline__ int cluster_rank() {
     }
 }
 
+// Distributed shared memory: the address of this CTA's shared variable *p in the shared
+// memory of cluster CTA `rank`, and 32-bit loads from such an address.
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, int rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(r)
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ int ld_dsmem(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Launches `kernel` so that it may start while the previous kernel on the stream drains;
 // a cooperative launch (every CTA resident at once) when asked.
 template <class... Params, class... Args>

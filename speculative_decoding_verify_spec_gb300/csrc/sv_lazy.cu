@@ -8,11 +8,13 @@
 // and its row's argmax is the bonus.  A chain is the tree whose node v has parent v - 1.
 //
 // Only accepted nodes' rows can change the result (a row decides its children's
-// acceptance and, for the deepest accepted node, the bonus), so one CTA per sequence walks
-// the accepted nodes in index order -- parents come before children -- and reads exactly
-// those rows.  Each row's argmax is the two-step search of the full path: the largest
-// 4 KB-tile maximum (lowest tile on ties, NaN absorbing), then the first position of that
-// value inside that tile.
+// acceptance and, for the deepest accepted node, the bonus), so a cluster of CS CTAs per
+// sequence (CS = 1 .. 8, as many SMs as the batch leaves for each sequence) walks the
+// accepted nodes in index order -- parents come before children -- and reads exactly those
+// rows, each CTA its share of a row's tiles.  Each row's argmax is the two-step search of
+// the full path: the largest 4 KB-tile maximum (lowest tile on ties, NaN absorbing), merged
+// over the cluster through distributed shared memory, then the first position of that value
+// inside that tile, found by the warp that read it.
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -26,7 +28,7 @@ constexpr int kLzWarps = kLzThreads / 32;
 
 // chain: parent(v) = v - 1 and node v's token is tokens[seq * (N - 1) + v - 1] (draft
 // tokens [B][gamma], N = gamma + 1); otherwise parent[N] and node_tokens [B][N].
-template <class D, bool VEC>
+template <class D, bool VEC, int CS>
 __global__ void __launch_bounds__(kLzThreads, 1)
     greedy_walk_kernel(Logits t, int N, int V, bool chain, const int32_t *__restrict__ parent,
                        const int32_t *__restrict__ tokens, int max_depth, int32_t *__restrict__ accepted_len,
@@ -36,16 +38,19 @@ __global__ void __launch_bounds__(kLzThreads, 1)
     int *s_arg = s_int + 4 * N;  // argmax of each accepted node's row
     int *s_path = s_int + 5 * N;  // max_depth + 1
     __shared__ int2 s_best[kLzWarps];
-    __shared__ int s_flag, s_tile, s_idx;
+    __shared__ int s_cbest[2];  // this CTA's best (max bits, tile) of the current row
+    __shared__ int s_flag, s_idx;
     griddep_launch_next();
     griddep_wait();  // the caller's kernels may still be writing the inputs
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t seq = blockIdx.x;
+    const int rank = cluster_rank<CS>();
+    const int64_t seq = blockIdx.x / CS;
     const int W = max_depth + 1;
     int32_t *out = out_tokens + seq * W;
     int32_t *opath = out_path ? out_path + seq * W : nullptr;
     constexpr int TE = tile_elems<D>();
     const int ntile = int((int64_t(V) + TE - 1) / TE);
+    const bool writer = rank == 0;  // one CTA of the cluster writes the outputs
 
     if (tid == 0) s_flag = 1;
     __syncthreads();
@@ -68,30 +73,36 @@ __global__ void __launch_bounds__(kLzThreads, 1)
     }
     __syncthreads();
     auto fail = [&]() {
+        if (!writer) return;
         for (int i = tid; i < W; i += kLzThreads) {
             out[i] = -1;
             if (opath) opath[i] = -1;
         }
         if (tid == 0) accepted_len[seq] = -1;
     };
-    if (!s_flag) {
+    if (!s_flag) {  // (the same in every CTA of the cluster: no shared memory was read remotely)
         fail();
         return;
     }
 
-    // the argmax of row v (every thread returns it; -1 for a row with a NaN)
+    // The argmax of row v (every thread returns it; -1 for a row with a NaN).  Warp g of the
+    // cluster (g = rank * kLzWarps + warp) takes tiles g, g + CS * kLzWarps, ...; it keeps
+    // its last tile, which is its only one whenever the row has at most CS * kLzWarps tiles.
+    const int gwarp = rank * kLzWarps + warp;
     auto row_argmax = [&](int v) -> int {
         const char *row = row_ptr(t, D::kBytes, seq, v);
         int2 best = make_int2(__float_as_int(-__int_as_float(0x7f800000)), kNoIndex);  // (max bits, tile)
-        for (int tile = warp; tile < ntile; tile += kLzWarps) {
+        uint4 vv[kTileVecs];
+        int held = -1;  // the tile whose logits vv holds
+        for (int tile = gwarp; tile < ntile; tile += CS * kLzWarps) {
             const int64_t c0 = int64_t(tile) * TE;
             const int len = unit_len(V, c0, TE);
-            uint4 vv[kTileVecs];
 #pragma unroll
             for (int u = 0; u < kTileVecs; ++u) {
                 const int e0 = (lane + 32 * u) * D::EPV;
                 vv[u] = e0 < len ? load_vec<D, VEC>(row, c0, e0, len) : neg_inf_vec<D>();
             }
+            held = tile;
             const float m = warp_reduce(thread_max<D>(vv), [](float a, float b) { return max_nan(a, b); });
             best = merge_argmax(best, make_int2(__float_as_int(m), tile));
         }
@@ -100,21 +111,29 @@ __global__ void __launch_bounds__(kLzThreads, 1)
         if (tid == 0) {
             int2 b = s_best[0];
             for (int w = 1; w < kLzWarps; ++w) b = merge_argmax(b, s_best[w]);
-            const float bm = __int_as_float(b.x);
-            s_tile = bm != bm ? -1 : b.y;
-            s_best[0] = b;
+            s_cbest[0] = b.x;
+            s_cbest[1] = b.y;
         }
-        __syncthreads();
-        const int tile = s_tile;
-        const float bm = __int_as_float(s_best[0].x);
-        if (warp == 0 && tile >= 0) {  // the first position of the maximum inside that tile
+        csync<CS>();  // every CTA's best is written
+        int2 b = make_int2(s_cbest[0], s_cbest[1]);
+        if constexpr (CS > 1) {
+            b = make_int2(ld_dsmem(dsmem_addr(&s_cbest[0], 0)), ld_dsmem(dsmem_addr(&s_cbest[1], 0)));
+            for (int r = 1; r < CS; ++r)
+                b = merge_argmax(b, make_int2(ld_dsmem(dsmem_addr(&s_cbest[0], r)), ld_dsmem(dsmem_addr(&s_cbest[1], r))));
+        }
+        const float bm = __int_as_float(b.x);
+        const int tile = bm != bm ? -1 : b.y;
+        // the first position of the maximum inside that tile, by the warp that read it
+        const bool owner = tile >= 0 && (tile % (CS * kLzWarps)) == gwarp;
+        if (owner) {
             const int64_t c0 = int64_t(tile) * TE;
             const int len = unit_len(V, c0, TE);
-            uint4 vv[kTileVecs];
+            if (held != tile) {
 #pragma unroll
-            for (int u = 0; u < kTileVecs; ++u) {
-                const int e0 = (lane + 32 * u) * D::EPV;
-                vv[u] = e0 < len ? load_vec<D, VEC>(row, c0, e0, len) : neg_inf_vec<D>();
+                for (int u = 0; u < kTileVecs; ++u) {
+                    const int e0 = (lane + 32 * u) * D::EPV;
+                    vv[u] = e0 < len ? load_vec<D, VEC>(row, c0, e0, len) : neg_inf_vec<D>();
+                }
             }
             int idx = kNoIndex;
 #pragma unroll
@@ -126,12 +145,16 @@ __global__ void __launch_bounds__(kLzThreads, 1)
                     idx = hit ? int(c0) + e0 + e : idx;
                 }
             }
-            idx = warp_reduce(idx, [](int a, int b) { return min(a, b); });
+            idx = warp_reduce(idx, [](int a, int c) { return min(a, c); });
             if (lane == 0) s_idx = idx;
         }
-        __syncthreads();
-        const int r = tile >= 0 ? s_idx : -1;
-        __syncthreads();
+        csync<CS>();  // the index is written (and every CTA is done reading the bests)
+        int r = -1;
+        if (tile >= 0) {
+            const int orank = (tile % (CS * kLzWarps)) / kLzWarps;
+            if constexpr (CS > 1) r = ld_dsmem(dsmem_addr(&s_idx, orank));
+            else r = s_idx;
+        }
         return r;
     };
 
@@ -141,6 +164,7 @@ __global__ void __launch_bounds__(kLzThreads, 1)
         if (!s_acc[v]) continue;  // uniform: written before the last barrier
         const int a = row_argmax(v);
         if (a < 0) {  // a NaN in a row the rule reads
+            csync<CS>();  // no CTA leaves while another may still read its shared memory
             fail();
             return;
         }
@@ -150,6 +174,8 @@ __global__ void __launch_bounds__(kLzThreads, 1)
         if (s_dep[v] > s_dep[best]) best = v;
         __syncthreads();
     }
+    csync<CS>();  // the last index read of the cluster is done
+    if (!writer) return;
     // outputs: the path root .. best, its tokens, the bonus argmax(best), -1 padding
     const int depth = s_dep[best];
     if (tid == 0)
@@ -165,14 +191,46 @@ __global__ void __launch_bounds__(kLzThreads, 1)
     if (tid == 0) accepted_len[seq] = depth;
 }
 
+template <int CS>
+cudaError_t launch_walk_cs(int dtype, bool vec, Logits t, int B, int N, int V, bool chain, const int32_t *parent,
+                           const int32_t *tokens, int max_depth, int32_t *accepted_len, int32_t *out_tokens,
+                           int32_t *out_path, size_t smem, cudaStream_t s) {
+    auto k = dtype == 1 ? (vec ? greedy_walk_kernel<BF16, true, CS> : greedy_walk_kernel<BF16, false, CS>)
+                        : (vec ? greedy_walk_kernel<F32, true, CS> : greedy_walk_kernel<F32, false, CS>);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(B) * CS);
+    cfg.blockDim = dim3(kLzThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CS;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CS > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, k, t, N, V, chain, parent, tokens, max_depth, accepted_len, out_tokens, out_path);
+}
+
 cudaError_t launch_greedy_walk(int dtype, bool vec, Logits t, int B, int N, int V, bool chain, const int32_t *parent,
                                const int32_t *tokens, int max_depth, int32_t *accepted_len, int32_t *out_tokens,
                                int32_t *out_path, cudaStream_t s) {
     const size_t smem = size_t(5 * N + max_depth + 1) * sizeof(int);
-    auto k = dtype == 1 ? (vec ? greedy_walk_kernel<BF16, true> : greedy_walk_kernel<BF16, false>)
-                        : (vec ? greedy_walk_kernel<F32, true> : greedy_walk_kernel<F32, false>);
-    return launch_after(k, unsigned(B), kLzThreads, smem, s, t, N, V, chain, parent, tokens, max_depth, accepted_len,
-                        out_tokens, out_path);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // CTAs per sequence: the most (a power of two, at most 8) that still fit one wave
+    int cs = 1;
+    while (cs < 8 && int64_t(B) * cs * 2 <= sms) cs *= 2;
+    switch (cs) {
+    case 8: return launch_walk_cs<8>(dtype, vec, t, B, N, V, chain, parent, tokens, max_depth, accepted_len, out_tokens, out_path, smem, s);
+    case 4: return launch_walk_cs<4>(dtype, vec, t, B, N, V, chain, parent, tokens, max_depth, accepted_len, out_tokens, out_path, smem, s);
+    case 2: return launch_walk_cs<2>(dtype, vec, t, B, N, V, chain, parent, tokens, max_depth, accepted_len, out_tokens, out_path, smem, s);
+    default: return launch_walk_cs<1>(dtype, vec, t, B, N, V, chain, parent, tokens, max_depth, accepted_len, out_tokens, out_path, smem, s);
+    }
 }
 
 }  // namespace sv
