@@ -60,7 +60,8 @@ typedef enum {
     SV_ERR_UNSUPPORTED = 2, /* dtype or mode not supported */
     SV_ERR_CUDA = 3,        /* a CUDA launch failed; see cudaGetLastError semantics */
     SV_ERR_TIMEOUT = 4,     /* a bounded device wait gave up (re-draw status words) */
-    SV_ERR_WORKSPACE = 5    /* workspace NULL, too small or not 16-byte aligned */
+    SV_ERR_WORKSPACE = 5,   /* workspace NULL, too small or not 16-byte aligned */
+    SV_ERR_CHECK = 6        /* bounds-checked build only: an internal index left its extent */
 } sv_status;
 
 typedef enum { SV_FP32 = 0, SV_BF16 = 1 } sv_dtype;
@@ -390,14 +391,35 @@ sv_status spec_verify_exp_df(const float *y_hi, const float *y_lo, int n, float 
  * records events[0] on its stream before its first kernel and events[s] after its s-th
  * kernel (s = 1 .. n_events-1; sampling has 4 kernels: row statistics, decide, residual
  * masses, and the inverse-CDF draw with the extended-precision re-draw of near-boundary
- * sequences (one cooperative grid); greedy
- * and tree have 2: tile maxima, finalize; tree sampling and lazy sampling have 3: the
- * walk, the re-walk's exponentials, the re-walk; typical acceptance and one-hot sampling
- * have 3: the walk, the re-draw's exponentials, the re-draw).  The events are cudaEvent_t handles created and owned by the
- * caller; recording them adds no synchronisation.  Pass NULL (or 0) to turn it off.
+ * sequences (one cooperative grid); greedy and tree have 2: tile maxima, finalize; the lazy
+ * greedy walks have 1; tree sampling has 3: the walk, the re-walk's exponentials, the
+ * re-walk; lazy sampling has 3: the level walk, residual masses, the draw with its re-draw;
+ * typical acceptance and one-hot sampling have 2: the level walk, the draw with its
+ * re-draw).  The events are cudaEvent_t handles created and owned by the caller; recording
+ * them adds no synchronisation.  Pass NULL (or 0) to turn it off.
  * Returns SV_ERR_INVALID_ARG for n_events < 0 or > 8.
  */
 sv_status spec_verify_set_stage_events(void *const *events, int n_events);
+
+/*
+ * The bounds-checked build (the library compiled with -DSV_CHECKS; a debugging aid, not the
+ * product build).  Its kernels check every index into the buffers the library sizes itself
+ * -- the workspace regions (tile partials, row statistics, plans, residual masses, re-draw
+ * records and unit sums, level lists and counters), tile and unit counts, tree node ids,
+ * n-gram positions and the rows of accepted_len / out_tokens -- against the extent the
+ * library knows, skip an access outside it and record the first such violation in a
+ * device-side word.  This call waits for the current device, copies that word into info
+ * (may be NULL): info[0] = site (a 16-bit tag of the source file's name << 16 | line),
+ * info[1] = the offending index, info[2] = the extent (both clamped to int32), info[3] =
+ * the number of violations; then clears it.  Returns SV_OK when nothing was recorded,
+ * SV_ERR_CHECK when something was, SV_ERR_CUDA if the copy failed, and SV_ERR_UNSUPPORTED
+ * (info zeroed) in the normal build.
+ */
+sv_status spec_verify_check_word(int32_t *info);
+/* Test hook of the bounds-checked build: one kernel that checks `index` against `extent`
+ * (and accesses no memory), so that a test can see a violation recorded and reported by
+ * spec_verify_check_word.  SV_ERR_UNSUPPORTED in the normal build. */
+sv_status spec_verify_check_selftest(int64_t index, int64_t extent);
 
 /* A static, human-readable name for a status code. */
 const char *spec_verify_status_string(sv_status status);

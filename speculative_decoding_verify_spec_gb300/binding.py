@@ -30,7 +30,8 @@ class SpecVerifyError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """The product library, or the build named by SV_LIBRARY (e.g. the bounds-checked one)."""
+    return os.environ.get("SV_LIBRARY") or _build.LIB_PATH
 
 
 def load_library() -> ctypes.CDLL:
@@ -91,6 +92,10 @@ def load_library() -> ctypes.CDLL:
         lib.spec_verify_status_string.restype = ctypes.c_char_p
         lib.spec_verify_version.argtypes = []
         lib.spec_verify_version.restype = i32
+        lib.spec_verify_check_word.argtypes = [P]
+        lib.spec_verify_check_word.restype = i32
+        lib.spec_verify_check_selftest.argtypes = [i64, i64]
+        lib.spec_verify_check_selftest.restype = i32
         _lib = lib
         return lib
 
@@ -463,6 +468,30 @@ def call_status(workspace: torch.Tensor, mode: int, B: int, rows: int, V: int, d
     torch.cuda.synchronize(workspace.device)
     words = workspace.view(torch.uint8)[off:off + 4 * (8 + B)].clone().view(torch.int32).cpu().numpy()
     return int(words[0]), int(words[4]), int(words[3]), words[8:8 + B].copy()
+
+
+def check_word():
+    """The bounds-checked build's violation record (see spec_verify_check_word): (status,
+    [site, index, extent, count]); status SV_ERR_UNSUPPORTED from the product build.  The
+    site's high 16 bits are file_tag() of the source file's base name, the low 16 its line."""
+    lib = load_library()
+    info = (ctypes.c_int32 * 4)()
+    st = lib.spec_verify_check_word(info)
+    return int(st), [int(v) for v in info]
+
+
+def check_selftest(index: int, extent: int) -> int:
+    """Bounds-checked build: one check of index against extent on the device (no memory
+    access); returns the launch status (SV_ERR_UNSUPPORTED from the product build)."""
+    return int(load_library().spec_verify_check_selftest(index, extent))
+
+
+def file_tag(name: str) -> int:
+    """The 16-bit tag the bounds-checked build gives a source file (FNV-1a, folded)."""
+    h = 2166136261
+    for ch in name.encode():
+        h = ((h ^ ch) * 16777619) & 0xFFFFFFFF
+    return (h >> 16) ^ (h & 0xFFFF)
 
 
 def wait_selftest(expected_arrivals: int, limit_us: int, device="cuda:0") -> int:

@@ -5,6 +5,7 @@
 #include <cstdint>
 
 #include "spec_verify.h"
+#include "sv_checks.cuh"
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -258,6 +259,25 @@ sv_status level_walk(int rule, sv_mode mode, const void *target_logits, int64_t 
 }
 }  // namespace
 
+#ifdef SV_CHECKS
+namespace sv {
+__device__ int g_check[4];
+__device__ bool check_fail(uint32_t site, int64_t idx, int64_t n) {
+    auto clamp32 = [](int64_t v) { return int(v > 0x7FFFFFFF ? 0x7FFFFFFF : (v < -0x7FFFFFFF ? -0x7FFFFFFF : v)); };
+    if (atomicCAS(&g_check[0], 0, int(site)) == 0) {
+        g_check[1] = clamp32(idx);
+        g_check[2] = clamp32(n);
+    }
+    atomicAdd(&g_check[3], 1);
+    return false;
+}
+// One check of `index` against `extent` and nothing else (no memory is accessed).
+__global__ void check_selftest_kernel(int64_t index, int64_t extent) {
+    if (threadIdx.x == 0) (void)SV_IN(index, extent);
+}
+}  // namespace sv
+#endif
+
 namespace sv {
 cudaError_t mark_stage(int s, cudaStream_t stream) {
     if (s < t_nevents && t_events[s] != nullptr) return cudaEventRecord(t_events[s], stream);
@@ -269,6 +289,34 @@ extern "C" {
 
 int spec_verify_version(void) { return 100; }
 
+sv_status spec_verify_check_word(int32_t *info) {
+#ifdef SV_CHECKS
+    int h[4] = {0, 0, 0, 0};
+    const int z[4] = {0, 0, 0, 0};
+    if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpyFromSymbol(h, sv::g_check, sizeof(h)) != cudaSuccess ||
+        cudaMemcpyToSymbol(sv::g_check, z, sizeof(z)) != cudaSuccess)
+        return SV_ERR_CUDA;
+    if (info)
+        for (int i = 0; i < 4; ++i) info[i] = h[i];
+    return h[0] != 0 ? SV_ERR_CHECK : SV_OK;
+#else
+    if (info)
+        for (int i = 0; i < 4; ++i) info[i] = 0;
+    return SV_ERR_UNSUPPORTED;
+#endif
+}
+
+sv_status spec_verify_check_selftest(int64_t index, int64_t extent) {
+#ifdef SV_CHECKS
+    sv::check_selftest_kernel<<<1, 32>>>(index, extent);
+    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+#else
+    (void)index;
+    (void)extent;
+    return SV_ERR_UNSUPPORTED;
+#endif
+}
+
 const char *spec_verify_status_string(sv_status s) {
     switch (s) {
     case SV_OK: return "ok";
@@ -277,6 +325,7 @@ const char *spec_verify_status_string(sv_status s) {
     case SV_ERR_CUDA: return "CUDA launch failed";
     case SV_ERR_TIMEOUT: return "a bounded device wait gave up";
     case SV_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case SV_ERR_CHECK: return "an internal index left its extent (bounds-checked build)";
     }
     return "unknown status";
 }

@@ -20,6 +20,7 @@
 //                    (lowest index on ties), write the path.
 // Searching for the index only inside the winning tile keeps the streaming pass as cheap
 // as a plain maximum.
+#include "sv_checks.cuh"
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -46,7 +47,7 @@ __global__ void __launch_bounds__(kThreads, 4)
                             : make_uint4(D::kNegInfWord, D::kNegInfWord, D::kNegInfWord, D::kNegInfWord);
         }
         const float m = warp_reduce(thread_max<D>(v), [](float a, float b) { return max_nan(a, b); });
-        if (lane == 0) partial[w.it] = m;
+        if (lane == 0 && SV_IN(w.it, items)) partial[w.it] = m;
     }
 }
 
@@ -107,6 +108,7 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t seq = blockIdx.x;
     const int R = gamma + 1;
     for (int i = warp; i < R; i += kWarps) {
+        if (!SV_IN((seq * R + i + 1) * ntile - 1, int64_t(B) * R * ntile)) continue;
         const int2 best = warp_row_argmax<D, VEC>(partial + (seq * R + i) * ntile, ntile,
                                                   row_ptr(t, D::kBytes, seq, i), V, lane);
         if (lane == 0) s_best[i] = best;
@@ -139,6 +141,7 @@ __global__ void __launch_bounds__(kThreads)
             break;
         }
     }
+    if (!SV_IN(n, R)) return;
     for (int i = lane; i < R; i += 32) out[i] = i < n ? x[seq * gamma + i] : (i == n ? s_best[n].y : -1);
     if (lane == 0) accepted_len[seq] = n;
 }
@@ -171,6 +174,7 @@ __global__ void __launch_bounds__(kTreeThreads)
     }
     griddep_wait();
     for (int v = warp; v < N; v += kTreeWarps) {  // node v's argmax: one warp per row
+        if (!SV_IN((seq * N + v + 1) * ntile - 1, int64_t(B) * N * ntile)) continue;
         const int2 best = warp_row_argmax<D, VEC>(partial + (seq * N + v) * ntile, ntile,
                                                   row_ptr(t, D::kBytes, seq, v), V, lane);
         if (lane == 0) {
@@ -189,6 +193,7 @@ __global__ void __launch_bounds__(kTreeThreads)
             bool kept = true;
             while (w != 0) {
                 const int p = par[w];
+                if (!SV_IN(p, N)) break;
                 kept = kept && tok[w] == a[p];
                 w = p;
                 ++d;
@@ -213,12 +218,14 @@ __global__ void __launch_bounds__(kTreeThreads)
     }
     const int d = best_key >> kKeyShift;
     const int vstar = (1 << kKeyShift) - 1 - (best_key & ((1 << kKeyShift) - 1));
+    if (!SV_IN(vstar, N) || !SV_IN(d, W)) return;
     for (int s = d + 1; s < W; ++s) {
         out[s] = -1;
         if (path) path[s] = -1;
     }
     out[d] = a[vstar];  // the bonus: argmax of the deepest kept node's row
     for (int s = d, w = vstar; s >= 0; --s) {
+        if (!SV_IN(w, N)) break;
         if (path) path[s] = w;
         if (s >= 1) out[s - 1] = tok[w];
         w = par[w];

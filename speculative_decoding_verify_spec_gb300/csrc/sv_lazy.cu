@@ -15,6 +15,7 @@
 // the full path: the largest 4 KB-tile maximum (lowest tile on ties, NaN absorbing), merged
 // over the cluster through distributed shared memory, then the first position of that value
 // inside that tile, found by the warp that read it.
+#include "sv_checks.cuh"
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -66,7 +67,7 @@ __global__ void __launch_bounds__(kLzThreads, 1)
     if (s_flag) {
         for (int v = tid; v < N; v += kLzThreads) {
             int dpt = 0;
-            for (int w = v; w != 0 && dpt <= max_depth; w = s_par[w]) ++dpt;
+            for (int w = v; w != 0 && dpt <= max_depth && SV_IN(w, N); w = s_par[w]) ++dpt;
             s_dep[v] = dpt;
             if (dpt > max_depth) s_flag = 0;
         }
@@ -178,15 +179,16 @@ __global__ void __launch_bounds__(kLzThreads, 1)
     if (!writer) return;
     // outputs: the path root .. best, its tokens, the bonus argmax(best), -1 padding
     const int depth = s_dep[best];
+    if (!SV_IN(depth, W)) return;
     if (tid == 0)
-        for (int s = depth, node = best; s >= 0; --s) {
+        for (int s = depth, node = best; s >= 0 && SV_IN(node, N); --s) {
             s_path[s] = node;
             node = s_par[node];
         }
     __syncthreads();
     for (int i = tid; i < W; i += kLzThreads) {
         if (opath) opath[i] = i <= depth ? s_path[i] : -1;
-        out[i] = i < depth ? s_tok[s_path[i + 1]] : (i == depth ? s_arg[best] : -1);
+        out[i] = i < depth ? (SV_IN(s_path[i + 1], N) ? s_tok[s_path[i + 1]] : -1) : (i == depth ? s_arg[best] : -1);
     }
     if (tid == 0) accepted_len[seq] = depth;
 }

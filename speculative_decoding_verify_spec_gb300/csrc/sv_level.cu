@@ -23,6 +23,7 @@
 // A sequence whose accept test came near its threshold (marked for the double-float rescan)
 // keeps streaming every later row, so the rescan finds whichever stop the exact test gives;
 // the rows it could use are counted in lavail.
+#include "sv_checks.cuh"
 #include "sv_device.cuh"
 #include "sv_grid.cuh"
 #include "sv_internal.h"
@@ -89,6 +90,11 @@ __device__ __forceinline__ bool level_decide(const LevelArgs &a, int64_t seq, in
     int32_t *out = a.out_tokens + seq * (G + 1);
     const int64_t rt = seq * R + i, rd = seq * R + G + 1 + i;  // rowstat rows of target / draft row i
     const bool has_d = RULE == kRuleSample && i < G;
+    if (!SV_IN(seq, a.B) || !SV_IN((rt + 1) * a.ntile - 1, int64_t(a.B) * R * a.ntile) ||
+        (has_d && !SV_IN((rd + 1) * a.ntile - 1, int64_t(a.B) * R * a.ntile))) {
+        state = 0;
+        return false;
+    }
     // the accept test's operands go out first: they do not depend on the statistics
     float tx = 0.f, dx = 0.f;
     int32_t xi = 0;
@@ -204,6 +210,7 @@ __global__ void __launch_bounds__(kLvThreads, 1) level_kernel(LevelArgs a) {
     for (int step = 0; i <= G; ++step) {
         const int n = step == 0 ? a.B : __ldcg(a.lctl + 8 + step);
         if (n == 0) break;  // (the same for every CTA)
+        if (!SV_IN(n - 1, a.B)) break;
         const int *list = a.lact + (step & 1) * int64_t(a.B);
         // levels fetched this step: one, or every remaining one once that is little work
         const int left = G + 1 - i;
@@ -263,7 +270,7 @@ __global__ void __launch_bounds__(kLvThreads, 1) level_kernel(LevelArgs a) {
             }
             const int64_t slot = rr * a.ntile + tile;
             if (it + kLvWarps < hi) issue(it + kLvWarps);
-            if (lane == 0) {
+            if (lane == 0 && SV_IN(slot, int64_t(a.B) * a.R * a.ntile)) {
                 a.partial[slot] = make_float2(M, S);
                 if constexpr (RULE == kRuleTypical) a.zpart[slot] = Z;
             }
@@ -282,7 +289,7 @@ __global__ void __launch_bounds__(kLvThreads, 1) level_kernel(LevelArgs a) {
                     const int cnt = int(b1 - b0);
                     const int64_t seq = seq_of(ai);
                     int *ctr = a.tcnt + seq;
-                    if (atom_add_acq_rel(ctr, cnt) + cnt == int(ups)) {
+                    if (SV_IN(seq, a.B) && atom_add_acq_rel(ctr, cnt) + cnt == int(ups)) {
                         *ctr = 0;  // for the next step (after the grid barrier)
                         s_dec[atomicAdd(&s_nd, 1)] = int(seq);
                     }
@@ -295,8 +302,10 @@ __global__ void __launch_bounds__(kLvThreads, 1) level_kernel(LevelArgs a) {
                     for (int j = i; j < i + s && more; ++j) more = level_decide<D, RULE>(a, seq, j, lane, state);
                     if (lane == 0) {
                         a.lstate[seq] = state;
-                        if (more && i + s <= G)
-                            a.lact[((step + 1) & 1) * int64_t(a.B) + atomicAdd(a.lctl + 8 + step + 1, 1)] = int(seq);
+                        if (more && i + s <= G && SV_IN(step + 1, G + 2)) {
+                            const int pos = atomicAdd(a.lctl + 8 + step + 1, 1);
+                            if (SV_IN(pos, a.B)) a.lact[((step + 1) & 1) * int64_t(a.B) + pos] = int(seq);
+                        }
                     }
                 }
                 __syncthreads();  // s_nd is reset for the next chunk

@@ -12,6 +12,7 @@
 // of kChunk starts; consecutive threads test consecutive starts (coalesced loads, the n
 // tokens of a start mostly served by L1), and the first chunk holding a match ends the
 // search -- on copy-heavy text the latest occurrence is usually near the end.
+#include "sv_checks.cuh"
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -36,7 +37,7 @@ __global__ void __launch_bounds__(kNgThreads)
     const int32_t *h = history + seq * stride;
     const int64_t Lr = lengths[seq];
     const int L = int(Lr < 0 ? 0 : (Lr > stride ? stride : Lr));  // a length past the row is clamped to it
-    if (tid < n && L >= n) s_tail[tid] = h[L - n + tid];
+    if (tid < n && L >= n && SV_IN(tid, kMaxNgram) && SV_IN(L - n + tid, stride)) s_tail[tid] = h[L - n + tid];
     __syncthreads();
     int best = -1;
     for (int hi = L - n - 1; hi >= 0 && best < 0; hi -= kChunk) {  // uniform over the CTA
@@ -44,7 +45,7 @@ __global__ void __launch_bounds__(kNgThreads)
         int local = -1;
         for (int i = hi - tid; i >= lo && local < 0; i -= kNgThreads) {  // descending: the first hit is the latest
             bool same = true;
-            for (int t = 0; t < n && same; ++t) same = __ldg(h + i + t) == s_tail[t];
+            for (int t = 0; t < n && same && SV_IN(i + t, L); ++t) same = __ldg(h + i + t) == s_tail[t];
             if (same) local = i;
         }
         local = warp_reduce(local, [](int a, int b) { return max(a, b); });
@@ -61,7 +62,8 @@ __global__ void __launch_bounds__(kNgThreads)
     if (best >= 0) avail = min(k, L - (best + n));
     const int c = pad && L >= 1 ? k : avail;
     for (int m = tid; m < k; m += kNgThreads)
-        out[m] = m < avail ? __ldg(h + best + n + m) : (m < c ? __ldg(h + L - 1) : -1);
+        out[m] = m < avail ? (SV_IN(best + n + m, L) ? __ldg(h + best + n + m) : -1)
+                           : (m < c ? (SV_IN(L - 1, stride) ? __ldg(h + L - 1) : -1) : -1);
     if (tid == 0) count[seq] = c;
 }
 

@@ -31,6 +31,7 @@
 #pragma once
 
 #include "spec_verify.h"
+#include "sv_checks.cuh"
 #include "sv_device.cuh"
 #include "sv_df.cuh"
 #include "sv_grid.cuh"
@@ -333,7 +334,7 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
         return tok;
     };
     auto finish = [&](int64_t seq, int k, int tok) {  // thread 0
-        a.out_tokens[seq * (gamma + 1) + k] = int32_t(tok);
+        if (SV_IN(seq * (gamma + 1) + k, int64_t(B) * (gamma + 1))) a.out_tokens[seq * (gamma + 1) + k] = int32_t(tok);
         atomicAdd(a.rctl + kRefineRedone, 1);
     };
 
@@ -345,7 +346,10 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
             const int c = int(it / (int64_t(R) * nu));
             const int loc = int(it - int64_t(c) * R * nu);
             const int ri = loc / nu, u = loc - ri * nu;
+            if (!SV_IN(B + c0 + c, 2 * int64_t(B))) continue;
             const int64_t seq = ldcg_info(a.rinfo + B + c0 + c).seq;
+            if (!SV_IN(seq * R + ri, int64_t(B) * R) || !SV_IN((int64_t(c) * R + ri) * nu + u, int64_t(kRescanChunk) * R * nu))
+                continue;
             const int avail = a.lavail ? __ldcg(a.lavail + seq) : gamma + 1;
             if ((ri <= gamma ? ri : ri - gamma - 1) >= avail) continue;  // a row the lazy walk did not read
             df w[kLane];
@@ -355,8 +359,10 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
         }
         if (!barrier()) return;
         for (int c = blockIdx.x; c < nc; c += gridDim.x) {
+            if (!SV_IN(B + c0 + c, 2 * int64_t(B))) continue;  // (uniform over the CTA)
             RefineInfo info = ldcg_info(a.rinfo + B + c0 + c);
             const int64_t seq = info.seq;
+            if (!SV_IN(seq, B)) continue;
             const df *rs = a.rresc + int64_t(c) * R * nu;
             const int avail = a.lavail ? __ldcg(a.lavail + seq) : gamma + 1;
             int k2 = gamma;
@@ -410,13 +416,14 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
             } else if (tid == 0) {  // a residual draw at the new stop row: onto the main list
                 info.k = k2;
                 info.mode = onehot ? 2 : 1;
+                const int pos = atomicAdd(a.rctl + kRefineMain, 1);
                 const float2 st2 = a.rowstat[seq * R + k2];
                 const float2 sd2 = onehot ? make_float2(0.f, 1.f) : a.rowstat[seq * R + gamma + 1 + k2];
                 info.Mt = st2.x;
                 info.St = st2.y;
                 info.Md = sd2.x;
                 info.Sd = sd2.y;
-                a.rinfo[atomicAdd(a.rctl + kRefineMain, 1)] = info;
+                if (SV_IN(pos, B)) a.rinfo[pos] = info;
             }
             __syncthreads();
         }
@@ -429,8 +436,10 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
     const int64_t na = int64_t(nmain) * nu;
     for (int64_t it = gw; it < na; it += nw) {
         const int e = int(it / nu), u = int(it - int64_t(e) * nu);
+        if (!SV_IN(e, B)) continue;
         const RefineInfo info = ldcg_info(a.rinfo + e);
         const int64_t seq = info.seq;
+        if (!SV_IN(seq, B) || !SV_IN(info.k, gamma + 1)) continue;
         const int k = info.k;
         df *S = a.rsum + e * slot;
         const float2 st = make_float2(info.Mt, info.St);  // the draw's copy of rowstat (no extra read)
@@ -474,8 +483,10 @@ __device__ void refine_phases(const RefineArgs &a, RefineSmem &sm) {
 
     // F: one CTA per main-list sequence, the draw.
     for (int e = blockIdx.x; e < nmain; e += gridDim.x) {
+        if (!SV_IN(e, B)) continue;  // (uniform over the CTA)
         const RefineInfo info = ldcg_info(a.rinfo + e);
         const int64_t seq = info.seq;
+        if (!SV_IN(seq, B) || !SV_IN(info.k, gamma + 1)) continue;
         const int k = info.k;
         const df *S = a.rsum + e * slot;
         df *fix = a.rsum + e * slot + 4 * int64_t(nu);

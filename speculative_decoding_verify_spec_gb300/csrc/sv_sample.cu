@@ -20,6 +20,7 @@
 //   draw            one warp per sequence: prefix over the unit masses (residual tiles, or
 //                   the tiles of p for a bonus draw), then an in-order scan inside the chosen
 //                   unit held in registers; the first j with C_j > u' R.
+#include "sv_checks.cuh"
 #include "sv_device.cuh"
 #include "sv_df.cuh"
 #include "sv_internal.h"
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 4)
         const float M = warp_reduce(thread_max<D>(v), [](float x, float y) { return max_nan(x, y); });
         float S = 0.f;
         if (is_finite(M)) S = warp_reduce(thread_sumexp<D>(v, c, M), [](float x, float y) { return x + y; });
-        if (lane == 0) partial[w.it] = make_float2(M, S);
+        if (lane == 0 && SV_IN(w.it, items)) partial[w.it] = make_float2(M, S);
     }
 }
 
@@ -126,10 +127,11 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
         rbar[threadIdx.x] = 0;
     }
     for (int r = warp; r < R; r += kDecideWarps) {
-        const float2 st = warp_merge_stats(partial + (seq * R + r) * ntile, ntile, c, lane);
+        const bool in = SV_IN((seq * R + r + 1) * ntile - 1, int64_t(B) * R * ntile);
+        const float2 st = in ? warp_merge_stats(partial + (seq * R + r) * ntile, ntile, c, lane) : make_float2(0.f, 1.f);
         if (lane == 0) {
             s_stat[r] = st;
-            rowstat[seq * R + r] = st;
+            if (SV_IN(seq * R + r, int64_t(B) * R)) rowstat[seq * R + r] = st;
         }
     }
     __syncthreads();
@@ -143,6 +145,7 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
     }
     ok = __all_sync(0xFFFFFFFFu, ok);
     int32_t *out = out_tokens + seq * (gamma + 1);
+    if (!SV_IN(seq, B)) return;
     if (!ok) {
         for (int i = lane; i <= gamma; i += 32) out[i] = -1;
         if (lane == 0) {
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, kResidualCtas)
     while (it < end) {
         const int64_t seq = it / nrt;
         const int64_t run_end = (seq + 1) * nrt < end ? (seq + 1) * nrt : end;
-        const int2 pl = plan[seq];
+        const int2 pl = SV_IN(seq, items / nrt) ? plan[seq] : make_int2(-1, -1);
         if (pl.y == 1 && pl.x >= 0 && pl.x < gamma) {  // uniform over the warp (a plan out of range: no work)
             const int k = pl.x;
             const float2 st = rowstat[seq * R + k], sd = rowstat[seq * R + gamma + 1 + k];
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, kResidualCtas)
                     }
                 }
                 const float mass = warp_reduce(acc.x + acc.y, [](float x, float y) { return x + y; });
-                if (lane == 0) csum[it] = mass;
+                if (lane == 0 && SV_IN(it, items)) csum[it] = mass;
                 if (it + 1 < run_end) {
                     if (kResidualPrefetch) {
 #pragma unroll
@@ -310,13 +313,15 @@ __device__ __forceinline__ void draw_sequence(Logits t, Logits d, int B, int gam
     int mode = pl.y == 1 ? 1 : 0;  // 1: residual after a rejection, 0: a draw from p
     // pl.y == 2 (a one-hot q rejected x_k): the draw from p without x_k, i.e. its tile's mass
     // less x_k's weight and x_k's own weight 0
-    int ex = pl.y == 2 ? x[seq * gamma + k] : -1;
+    int ex = pl.y == 2 && SV_IN(seq * gamma + k, int64_t(B) * gamma) ? x[seq * gamma + k] : -1;
+    if (ex >= 0 && !SV_IN(ex, V)) ex = -1;
     const float w_ex = ex >= 0 ? weight(load_elem<D>(row_ptr(t, D::kBytes, seq, k), ex), st.x, c) : 0.f;
     const int ex_tile = ex >= 0 ? ex / tile_elems<D>() : -1;
     const float2 *prow = partial + (seq * R + k) * ntile;
     const float *crow = csum + seq * nrt;
     auto unit_mass = [&](int u) -> float {
-        if (mode) return crow[u];
+        if (mode) return SV_IN(seq * nrt + u, int64_t(B) * nrt) ? crow[u] : 0.f;
+        if (!SV_IN((seq * R + k) * ntile + u, int64_t(B) * R * ntile)) return 0.f;
         const float2 p = prow[u];
         const float m = p.y * weight(p.x, st.x, c);  // mass of tile u under 2^((l - M) c)
         return u == ex_tile ? fmaxf(__fsub_rn(m, w_ex), 0.f) : m;
@@ -501,7 +506,7 @@ __device__ __forceinline__ void draw_sequence(Logits t, Logits d, int B, int gam
     // a draw whose threshold lies within the fp32 weights' error of a CDF boundary (or that
     // needed a rounding fallback, or a sequence decide marked) is redone in extended precision
     if (lane == 0) {
-        out_tokens[seq * (gamma + 1) + k] = int32_t(u0 + tok);
+        if (SV_IN(seq * (gamma + 1) + k, int64_t(B) * (gamma + 1))) out_tokens[seq * (gamma + 1) + k] = int32_t(u0 + tok);
         const bool fell_back = (pl.y == 1 && mode == 0) || (pl.y == 2 && ex < 0);  // no residual mass
         // (a draw from p weighs in units of the row maximum's weight, not of S; without x_k its
         // tile's mass carries the subtraction's rounding too)
@@ -514,7 +519,7 @@ __device__ __forceinline__ void draw_sequence(Logits t, Logits d, int B, int gam
             rflag[seq] = flag;
             atomicAdd(rctl + kRefineCount, 1);
             const int e = (flag & kRefineAccept) ? B + atomicAdd(rctl + kRefineAll, 1) : atomicAdd(rctl + kRefineMain, 1);
-            rinfo[e] = RefineInfo{int(seq), flag, k, pl.y, st.x, st.y, sdk.x, sdk.y};
+            if (SV_IN(e, 2 * int64_t(B))) rinfo[e] = RefineInfo{int(seq), flag, k, pl.y, st.x, st.y, sdk.x, sdk.y};
         }
     }
 }
@@ -552,7 +557,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         st = make_float2(0.f, 1.f);
         sdk = make_float2(0.f, 1.f);
         flag0 = 0;
-        if (pl.y >= 0) {
+        if (pl.y >= 0 && SV_IN(seq * R + pl.x, int64_t(B) * R) &&
+            (pl.y != 1 || SV_IN(seq * R + gamma + 1 + pl.x, int64_t(B) * R))) {
             st = __ldcg(rowstat + seq * R + pl.x);
             if (pl.y == 1) sdk = __ldcg(rowstat + seq * R + gamma + 1 + pl.x);
             flag0 = __ldcg(rflag + seq);

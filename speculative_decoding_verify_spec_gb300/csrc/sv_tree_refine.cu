@@ -29,6 +29,7 @@
 // A token's q-mass is exactly zero when its exponential is (a -inf draft logit, or one more
 // than 87 T below the row maximum); q is out of mass once every token with mass has left.
 #include "spec_verify.h"
+#include "sv_checks.cuh"
 #include "sv_device.cuh"
 #include "sv_df.cuh"
 #include "sv_dfwalk.cuh"
@@ -154,6 +155,7 @@ __global__ void __launch_bounds__(kThreads)
         const int k = int((rest / 2) % K);
         const int j = int(rest / (2 * int64_t(K)));
         const int64_t seq = s_seq[j];
+        if (!SV_IN(seq, B) || !SV_IN(j, kMaxTreeRefine)) continue;
         if (k >= __ldcg(ws.rlen + seq)) continue;  // (uniform over the warp)
         const float4 rec = __ldcg(ws.rec + seq * K + k);
         const int node = __float_as_int(rec.x);
@@ -469,7 +471,7 @@ __global__ void __launch_bounds__(kRwThreads, 1)
             df s_new = s;
             const bool add = without_replacement && !removed;
             if (add) {
-                if (tid == 0) {
+                if (tid == 0 && SV_IN(nrem, N)) {
                     s_remtok[nrem] = x;
                     s_remcoef[nrem] = Anew;
                 }
@@ -494,7 +496,7 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         }
         if (next >= 0) {
             ++depth;
-            if (tid == 0 && depth <= max_depth) s_path[depth] = next;
+            if (tid == 0 && depth <= max_depth && SV_IN(next, N)) s_path[depth] = next;
             __syncthreads();
             if (depth > max_depth) {  // (the walk checked the depths; never taken)
                 fail();
@@ -573,7 +575,7 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         for (int i = tid; i < W; i += kRwThreads) {
             int o = -1, pth = -1;
             if (i <= depth) pth = s_path[i];
-            if (i < depth) o = s_tok[s_path[i + 1]];
+            if (i < depth) o = SV_IN(s_path[i + 1], N) ? s_tok[s_path[i + 1]] : -1;
             else if (i == depth) o = tok;
             out[i] = o;
             if (opath) opath[i] = pth;
@@ -590,7 +592,7 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         int total_marked = 0;
         const int64_t seq = nth_marked(ws.mark, B, j + iter * G, s_bal, s_cnt, &total_marked);
         if (iter == 0 && blockIdx.x == 0 && tid == 0) ws.ctl[kTrMarked] = total_marked;
-        if (seq < 0) break;  // (the whole cluster)
+        if (seq < 0 || !SV_IN(seq, B)) break;  // (the whole cluster)
         walk_one(seq, iter == 0);
         csync<CS>();  // every CTA is done with the slot's scratch before the next sequence
         if (rank == 0 && tid == 0) atomicAdd(ws.ctl + kTrRedone, 1);

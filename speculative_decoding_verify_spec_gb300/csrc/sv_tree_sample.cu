@@ -23,6 +23,7 @@
 //
 // Arithmetic mirrors the chain sampler: weights 2^((x - M) c) with x - M exact, explicitly
 // rounded products, fp32 sums in a fixed order; the final draw's prefixes in fp64.
+#include "sv_checks.cuh"
 #include "sv_device.cuh"
 #include "sv_df.cuh"
 #include "sv_internal.h"
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
                 for (int e = 0; e < D::EPV; ++e)
                     acc += wgt(vec_elem<D>(tv[k], e), a != 0.f ? vec_elem<D>(dv[k], e) : 0.f, st, a, c);
             acc = warp_reduce(acc, [](float x, float y) { return x + y; });
-            if (lane == 0) um[u] = acc;
+            if (lane == 0 && SV_IN(u, nunit)) um[u] = acc;
         }
         csync<CS>();  // the unit masses of every warp of the cluster
         // tokens removed earlier keep their own coefficient: correct their units (rank 0)
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
                 if (s_remcoef[r] == a) continue;
                 const int j = s_remtok[r];
                 const float tj = load_elem<D>(tp, j), dj = load_elem<D>(dp, j);
-                um[j / RE] += wgt(tj, dj, st, s_remcoef[r], c) - wgt(tj, dj, st, a, c);
+                if (SV_IN(j / RE, nunit)) um[j / RE] += wgt(tj, dj, st, s_remcoef[r], c) - wgt(tj, dj, st, a, c);
             }
         }
         csync<CS>();
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
             fail();
             return;
         }
-        if (rank == 0 && tid == 0 && depth < K) {  // the node and its rows' maxima, for the re-walk
+        if (rank == 0 && tid == 0 && depth < K && SV_IN(v, N)) {  // the node and its rows' maxima, for the re-walk
             rw.rec[seq * K + depth] = make_float4(__int_as_float(v), ts.x, st.has_q ? ds.x : 0.f, st.has_q ? 1.f : 0.f);
             s_nrec = depth + 1;
         }
@@ -322,6 +323,10 @@ __global__ void __launch_bounds__(kTsThreads, 1)
         }
         if (next >= 0) {
             ++depth;
+            if (!SV_IN(depth, W) || !SV_IN(next, N)) {  // (the same in every thread)
+                fail();
+                return;
+            }
             if (tid == 0) s_path[depth] = next;
             v = next;
             continue;
@@ -457,7 +462,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     for (int i = tid; i < W; i += kTsThreads) {
         int o = -1, pth = -1;
         if (i <= depth) pth = s_path[i];
-        if (i < depth) o = s_tok[s_path[i + 1]];
+        if (i < depth) o = SV_IN(s_path[i + 1], N) ? s_tok[s_path[i + 1]] : -1;
         else if (i == depth) o = tok;
         out[i] = o;
         if (opath) opath[i] = pth;

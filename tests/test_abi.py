@@ -303,3 +303,22 @@ def test_package_exports_every_entry_point():
         assert n in sv.__all__ or n in hooks, n
     for n in sv.__all__:
         assert hasattr(sv, n), n
+
+
+def test_product_build_has_no_check_word(lib):
+    info = (ctypes.c_int32 * 4)(7, 7, 7, 7)
+    assert lib.spec_verify_check_word(info) == 2  # SV_ERR_UNSUPPORTED, no device access
+    assert list(info) == [0, 0, 0, 0]
+    assert lib.spec_verify_check_word(None) == 2
+    assert lib.spec_verify_check_selftest(ctypes.c_int64(5), ctypes.c_int64(3)) == 2
+    assert lib.spec_verify_status_string(6) == b"an internal index left its extent (bounds-checked build)"
+
+
+def test_file_tags_follow_fnv1a():
+    # FNV-1a (32-bit) reference values: "" -> 0x811c9dc5, "a" -> 0xe40c292c, "foobar" -> 0xbf9cf968
+    fold = lambda h: (h >> 16) ^ (h & 0xFFFF)
+    assert binding.file_tag("") == fold(0x811C9DC5)
+    assert binding.file_tag("a") == fold(0xE40C292C)
+    assert binding.file_tag("foobar") == fold(0xBF9CF968)
+    names = [f for f in os.listdir(os.path.join(_build.CSRC)) if f.endswith((".cu", ".cuh"))]
+    assert len({binding.file_tag(f) for f in names}) == len(names)  # the tags tell the files apart
