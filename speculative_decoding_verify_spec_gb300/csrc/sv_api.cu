@@ -29,7 +29,7 @@ struct Layout {
     size_t partial = 0, rowstat = 0, plan = 0, csum = 0;
     size_t rctl = 0, rbar = 0, rlist = 0, rsum = 0, ramb = 0, rresc = 0;  // re-draw: control + marks, barrier, records, scratch
     size_t rec = 0, et = 0, us = 0, npos = 0, um = 0, pmax = 0, pcnt = 0;  // re-walk (tree sampling; rctl, rsum too)
-    size_t zpart = 0, lctl = 0, lact = 0, tcnt = 0, lstate = 0, lavail = 0;  // the level walks
+    size_t zpart = 0, xval = 0, lctl = 0, lact = 0, tcnt = 0, lstate = 0, lavail = 0;  // the level walks
     size_t total = 0;
 };
 
@@ -132,6 +132,8 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
             L.zpart = off;
             off += up256(size_t(B) * R * ntile * 4);
         }
+        L.xval = off;
+        off += up256(size_t(B) * R * 4);
         L.lctl = off;
         off += up256((size_t(8) + rows + 2) * 4);
         L.lact = off;
@@ -228,6 +230,7 @@ sv_status level_walk(int rule, sv_mode mode, const void *target_logits, int64_t 
     la.delta = delta;
     la.partial = reinterpret_cast<float2 *>(at(workspace, L.partial));
     la.zpart = reinterpret_cast<float *>(at(workspace, L.zpart));
+    la.xval = reinterpret_cast<float *>(at(workspace, L.xval));
     la.rowstat = reinterpret_cast<float2 *>(at(workspace, L.rowstat));
     la.plan = reinterpret_cast<int2 *>(at(workspace, L.plan));
     la.accepted_len = accepted_len;

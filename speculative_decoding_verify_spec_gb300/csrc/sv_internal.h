@@ -191,6 +191,7 @@ struct LevelArgs {
     float epsilon, delta;            // typical acceptance's threshold
     float2 *partial;                 // [B][R][ntile] (M, S) per 4 KB tile
     float *zpart;                    // [B][R][ntile] Z per tile (typical acceptance)
+    float *xval;                     // [B][R] the logit at the draft token of each row read
     float2 *rowstat;                 // [B][R] (M, S) of every row read
     int2 *plan;                      // [B] (stop row, kind of draw: 0 from p, 1 residual, 2 p without x_k)
     int32_t *accepted_len, *out_tokens;

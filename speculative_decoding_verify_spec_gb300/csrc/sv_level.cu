@@ -80,41 +80,59 @@ __device__ __forceinline__ int atom_add_acq_rel(int *p, int v) {
     return old;
 }
 
-// The decision of sequence seq at level i (one row of each kind), by the warp that finished
-// the tiles of its rows; state: bit 0 walking, bit 1 marked (0 once the sequence neither
-// walks on nor needs more rows, for the rescan).  Returns state != 0.
+// What the decision of one level needs, gathered by any warp: the merged statistics of the
+// level's rows (the target row's Z too for typical acceptance) and the logits at the draft
+// token, which the tile pass recorded in xval.  `state` rides along in the first level's
+// record.
+struct LvStat {
+    float2 st, sd;
+    float zt, tx, dx;
+    int state;
+};
 template <class D, int RULE>
-__device__ __forceinline__ bool level_decide(const LevelArgs &a, int64_t seq, int i, int lane, int &state) {
+__device__ __forceinline__ LvStat level_gather(const LevelArgs &a, int64_t seq, int i, int lane) {
+    const int G = a.gamma, R = a.R;
+    const int64_t rt = seq * R + i, rd = seq * R + G + 1 + i;  // rows of target / draft row i
+    const bool has_d = RULE == kRuleSample && i < G;
+    LvStat g;
+    g.st = make_float2(0.f, 1.f);
+    g.sd = make_float2(0.f, 1.f);
+    g.zt = g.tx = g.dx = 0.f;
+    g.state = 0;
+    if (!SV_IN((rt + 1) * a.ntile - 1, int64_t(a.B) * R * a.ntile) ||
+        (has_d && !SV_IN((rd + 1) * a.ntile - 1, int64_t(a.B) * R * a.ntile)))
+        return g;
+    if (i < G) {  // the accept test's operands
+        g.tx = __ldcg(a.xval + rt);
+        if (has_d) g.dx = __ldcg(a.xval + rd);
+    }
+    if constexpr (RULE == kRuleTypical) {
+        const Stat3 s3 = warp_merge_stats3(a.partial + rt * a.ntile, a.zpart + rt * a.ntile, a.ntile, a.c, lane);
+        g.st = make_float2(s3.M, s3.S);
+        g.zt = s3.Z;
+    } else {
+        g.st = warp_merge_stats<true>(a.partial + rt * a.ntile, a.ntile, a.c, lane);
+    }
+    if (has_d) g.sd = warp_merge_stats<true>(a.partial + rd * a.ntile, a.ntile, a.c, lane);
+    return g;
+}
+
+// The decision of sequence seq at level i from its gathered record g (one warp); state:
+// bit 0 walking, bit 1 marked (0 once the sequence neither walks on nor needs more rows,
+// for the rescan).  Returns state != 0.
+template <class D, int RULE>
+__device__ __forceinline__ bool level_decide(const LevelArgs &a, int64_t seq, int i, int lane, int &state,
+                                             const LvStat &g) {
     const int G = a.gamma, R = a.R;
     int *rflag = a.rctl + kRefineCtlWords;
     int32_t *out = a.out_tokens + seq * (G + 1);
-    const int64_t rt = seq * R + i, rd = seq * R + G + 1 + i;  // rowstat rows of target / draft row i
+    const int64_t rt = seq * R + i, rd = seq * R + G + 1 + i;
     const bool has_d = RULE == kRuleSample && i < G;
-    if (!SV_IN(seq, a.B) || !SV_IN((rt + 1) * a.ntile - 1, int64_t(a.B) * R * a.ntile) ||
-        (has_d && !SV_IN((rd + 1) * a.ntile - 1, int64_t(a.B) * R * a.ntile))) {
+    if (!SV_IN(seq, a.B)) {
         state = 0;
         return false;
     }
-    // the accept test's operands go out first: they do not depend on the statistics
-    float tx = 0.f, dx = 0.f;
-    int32_t xi = 0;
-    if ((state & 1) && i < G) {
-        xi = a.x[seq * G + i];
-        if (xi >= 0 && xi < a.V) {
-            tx = load_elem<D>(row_ptr(a.t, D::kBytes, seq, i), xi);
-            if (has_d) dx = load_elem<D>(row_ptr(a.d, D::kBytes, seq, i), xi);
-        }
-    }
-    float2 st, sd = make_float2(0.f, 1.f);
-    float zt = 0.f;
-    if constexpr (RULE == kRuleTypical) {
-        const Stat3 s3 = warp_merge_stats3(a.partial + rt * a.ntile, a.zpart + rt * a.ntile, a.ntile, a.c, lane);
-        st = make_float2(s3.M, s3.S);
-        zt = s3.Z;
-    } else {
-        st = warp_merge_stats<true>(a.partial + rt * a.ntile, a.ntile, a.c, lane);
-    }
-    if (has_d) sd = warp_merge_stats<true>(a.partial + rd * a.ntile, a.ntile, a.c, lane);
+    const float2 st = g.st, sd = g.sd;
     if (i == 0) {  // the tokens: all in [0, V), else the sequence is invalid
         bool ok = true;
         for (int q = lane; q < G; q += 32) {
@@ -151,10 +169,10 @@ __device__ __forceinline__ bool level_decide(const LevelArgs &a, int64_t seq, in
         int stop = -1, kind = 0;
         bool near = false;
         if (i < G) {
-            const float p = ex2(__fmul_rn(__fsub_rn(tx, st.x), a.c)) / st.y;
+            const float p = ex2(__fmul_rn(__fsub_rn(g.tx, st.x), a.c)) / st.y;
             bool reject;
             if constexpr (RULE == kRuleSample) {
-                const float q = ex2(__fmul_rn(__fsub_rn(dx, sd.x), a.c)) / sd.y;
+                const float q = ex2(__fmul_rn(__fsub_rn(g.dx, sd.x), a.c)) / sd.y;
                 const float u = uniform01(a.seed, a.offset, uint32_t(seq), uint32_t(i), 0u);
                 reject = !(u * q < p);
                 near = fabsf(u * q - p) < kRefineAcceptWindow * fmaxf(p, u * q);
@@ -163,7 +181,7 @@ __device__ __forceinline__ bool level_decide(const LevelArgs &a, int64_t seq, in
                 reject = !(u < p);
                 near = fabsf(u - p) < kRefineAcceptWindow * fmaxf(p, u);
             } else {  // typical: H = ln S - ln 2 Z / S (natural log, p = 2^a / S)
-                const float H = __fsub_rn(logf(st.y), __fdiv_rn(0.69314718f * zt, st.y));
+                const float H = __fsub_rn(logf(st.y), __fdiv_rn(0.69314718f * g.zt, st.y));
                 reject = !(p > fminf(a.epsilon, a.delta * expf(-H)));
             }
             if (near) state |= 2;
@@ -191,12 +209,15 @@ __device__ __forceinline__ bool level_decide(const LevelArgs &a, int64_t seq, in
 }
 
 constexpr int64_t kSpecBytes = 64 << 20;  // a level fetches every remaining row once that is this little
+constexpr float kStepBytes = 32e6f;       // what one more step costs, in bytes streamed (~5 us)
 constexpr int kLvWarps = kLvThreads / 32;
+constexpr int kLvRecords = 512;  // gathered level records a CTA holds at once
 
 template <class D, bool VEC, int RULE>
 __global__ void __launch_bounds__(kLvThreads, 1) level_kernel(LevelArgs a) {
     __shared__ int s_nd;             // sequences this CTA completed in the current chunk
     __shared__ int s_dec[kLvThreads];
+    __shared__ LvStat s_lv[kLvRecords];
     griddep_launch_next();
     griddep_wait();  // before any read: the caller's previous kernel may be writing the inputs
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -206,16 +227,36 @@ __global__ void __launch_bounds__(kLvThreads, 1) level_kernel(LevelArgs a) {
     }
     const int G = a.gamma;
     const bool two = RULE == kRuleSample;  // a target and a draft row per level below gamma
-    int i = 0;
+    int i = 0, n_prev = a.B, s_prev = 1;
     for (int step = 0; i <= G; ++step) {
         const int n = step == 0 ? a.B : __ldcg(a.lctl + 8 + step);
         if (n == 0) break;  // (the same for every CTA)
         if (!SV_IN(n - 1, a.B)) break;
         const int *list = a.lact + (step & 1) * int64_t(a.B);
-        // levels fetched this step: one, or every remaining one once that is little work
+        // levels fetched this step: every remaining one once that is little work; else one,
+        // and more while the rows read for sequences that will have stopped before them
+        // (estimated from the fraction that went on per level so far) stay below what a step
+        // of its own costs
         const int left = G + 1 - i;
         const int64_t rows_left = two ? 2 * int64_t(left) - 1 : left;
-        const int s = int64_t(n) * rows_left * a.ntile * 4096 <= kSpecBytes ? left : 1;
+        int s = 1;
+        if (int64_t(n) * rows_left * a.ntile * 4096 <= kSpecBytes) {
+            s = left;
+        } else if (step > 0) {
+            const float go_on = powf(float(n) / float(n_prev), 1.f / float(s_prev));
+            const float level_bytes = float(two ? 2 : 1) * float(a.ntile) * 4096.f;
+            float waste = 0.f, reach = 1.f;
+            while (s < left) {
+                reach *= go_on;  // share of the n sequences still walking s levels on
+                const float w = float(n) * (1.f - reach) * level_bytes;
+                if (waste + w > kStepBytes) break;
+                waste += w;
+                ++s;
+            }
+        }
+        s = min(s, kLvRecords);  // a sequence's levels of one step fit the CTA's records
+        n_prev = n;
+        s_prev = s;
         const int nr = two ? 2 * s - (i + s - 1 == G ? 1 : 0) : s;  // rows per sequence this step
         const uint32_t ups = uint32_t(nr) * uint32_t(a.ntile);     // items (tiles) per sequence
         const uint64_t items = uint64_t(n) * ups;
@@ -227,8 +268,8 @@ __global__ void __launch_bounds__(kLvThreads, 1) level_kernel(LevelArgs a) {
         // The tile loop is software-pipelined: the next item's loads go out before this
         // item's sums.
         uint4 v[kTileVecs];
-        int64_t rr = 0;
-        int tile = 0;
+        int64_t rr = 0, c0 = 0;
+        int tile = 0, len = 0, xi = -1;
         auto issue = [&](uint64_t it) {
             const uint32_t ai = uint32_t(it / ups);
             const int local = int(it - uint64_t(ai) * ups);
@@ -239,8 +280,9 @@ __global__ void __launch_bounds__(kLvThreads, 1) level_kernel(LevelArgs a) {
             const int64_t seq = seq_of(ai);
             rr = seq * a.R + (is_d ? G + 1 + lv : lv);
             const char *rp = is_d ? row_ptr(a.d, D::kBytes, seq, lv) : row_ptr(a.t, D::kBytes, seq, lv);
-            const int64_t c0 = int64_t(tile) * tile_elems<D>();
-            const int len = unit_len(a.V, c0, tile_elems<D>());
+            c0 = int64_t(tile) * tile_elems<D>();
+            len = unit_len(a.V, c0, tile_elems<D>());
+            xi = lv < G ? __ldg(a.x + seq * G + lv) : -1;  // the draft token whose logit this row gives
 #pragma unroll
             for (int u = 0; u < kTileVecs; ++u) {
                 const int e0 = (lane + 32 * u) * D::EPV;
@@ -269,11 +311,29 @@ __global__ void __launch_bounds__(kLvThreads, 1) level_kernel(LevelArgs a) {
                 if (is_finite(M)) S = warp_reduce(thread_sumexp<D>(v, a.c, M), [](float x, float y) { return x + y; });
             }
             const int64_t slot = rr * a.ntile + tile;
+            // the logit at the draft token, if this tile holds it (by the lane that holds it)
+            const int64_t xr = int64_t(xi) - c0;
+            const int64_t xrow = rr;
+            int xl = -1;
+            float xv = 0.f;
+            if (xi >= 0 && xr >= 0 && xr < len) {
+                const int vi = int(xr) / D::EPV, e = int(xr) - vi * D::EPV;  // vector, element in it
+                const int wi = D::EPV == 8 ? e >> 1 : e;                         // 32-bit word in the vector
+                xl = vi & 31;
+                uint32_t w = 0;
+#pragma unroll
+                for (int u = 0; u < kTileVecs; ++u) {  // (no dynamic index into v: it stays in registers)
+                    const uint32_t wu = wi == 0 ? v[u].x : wi == 1 ? v[u].y : wi == 2 ? v[u].z : v[u].w;
+                    w = u == (vi >> 5) ? wu : w;
+                }
+                xv = D::EPV == 8 ? ((e & 1) ? bf16_hi(w) : bf16_lo(w)) : __uint_as_float(w);
+            }
             if (it + kLvWarps < hi) issue(it + kLvWarps);
             if (lane == 0 && SV_IN(slot, int64_t(a.B) * a.R * a.ntile)) {
                 a.partial[slot] = make_float2(M, S);
                 if constexpr (RULE == kRuleTypical) a.zpart[slot] = Z;
             }
+            if (lane == xl && SV_IN(xrow, int64_t(a.B) * a.R)) a.xval[xrow] = xv;
         }
         __syncthreads();  // every partial of this CTA's range is written
         // Count this CTA's tiles on the counter of each sequence it touched; the CTA whose count
@@ -295,18 +355,34 @@ __global__ void __launch_bounds__(kLvThreads, 1) level_kernel(LevelArgs a) {
                     }
                 }
                 __syncthreads();
-                for (int q = warp; q < s_nd; q += kLvWarps) {
-                    const int64_t seq = s_dec[q];
-                    int state = i == 0 ? 1 : __ldcg(a.lstate + seq);
-                    bool more = true;
-                    for (int j = i; j < i + s && more; ++j) more = level_decide<D, RULE>(a, seq, j, lane, state);
-                    if (lane == 0) {
-                        a.lstate[seq] = state;
-                        if (more && i + s <= G && SV_IN(step + 1, G + 2)) {
-                            const int pos = atomicAdd(a.lctl + 8 + step + 1, 1);
-                            if (SV_IN(pos, a.B)) a.lact[((step + 1) & 1) * int64_t(a.B) + pos] = int(seq);
+                // the records of every (sequence, level) this CTA completed, gathered by all
+                // warps at once; then a warp per sequence walks its levels in order
+                const int nd = s_nd, per_grp = max(1, kLvRecords / s);
+                for (int g0 = 0; g0 < nd; g0 += per_grp) {
+                    const int ng = min(per_grp, nd - g0);
+                    for (int e = warp; e < ng * s; e += kLvWarps) {
+                        const int q = e / s, j = e - q * s;
+                        const int64_t seq = s_dec[g0 + q];
+                        LvStat g = level_gather<D, RULE>(a, seq, i + j, lane);
+                        if (j == 0) g.state = i == 0 ? 1 : __ldcg(a.lstate + seq);
+                        if (lane == 0) s_lv[e] = g;
+                    }
+                    __syncthreads();
+                    for (int q = warp; q < ng; q += kLvWarps) {
+                        const int64_t seq = s_dec[g0 + q];
+                        int state = s_lv[q * s].state;
+                        bool more = true;
+                        for (int j = 0; j < s && more; ++j)
+                            more = level_decide<D, RULE>(a, seq, i + j, lane, state, s_lv[q * s + j]);
+                        if (lane == 0) {
+                            a.lstate[seq] = state;
+                            if (more && i + s <= G && SV_IN(step + 1, G + 2)) {
+                                const int pos = atomicAdd(a.lctl + 8 + step + 1, 1);
+                                if (SV_IN(pos, a.B)) a.lact[((step + 1) & 1) * int64_t(a.B) + pos] = int(seq);
+                            }
                         }
                     }
+                    __syncthreads();
                 }
                 __syncthreads();  // s_nd is reset for the next chunk
             }
