@@ -593,7 +593,7 @@ def measure_e2e(name, inputs, steps, dev, **ov):
     dev_in = {}
     keys = {"sample": ["target", "draft", "draft_tokens"], "greedy": ["target", "draft_tokens"],
             "tree": ["target", "node_tokens"],
-            "tree_sample": ["target", "draft", "node_tokens"]}[mode]
+            "tree_sample": ["target", "draft", "node_tokens"], "ngram": ["history", "lengths"]}[mode]
     target_only = bool(cfg.get("typical") or cfg.get("onehot"))  # no draft logits
     if target_only:
         keys = ["target", "draft_tokens"]
@@ -609,7 +609,9 @@ def measure_e2e(name, inputs, steps, dev, **ov):
     def step():
         for k in keys:
             dev_in[k].copy_(host_in[k], non_blocking=True)
-        if target_only:
+        if mode == "ngram":
+            call(dev_in["history"], dev_in["lengths"])
+        elif target_only:
             call(dev_in["target"], dev_in["draft_tokens"])
         elif mode == "sample":
             call(dev_in["target"], dev_in["draft"], dev_in["draft_tokens"])
@@ -773,7 +775,8 @@ def compact_line(line, main, modes, workload):
             "clocks")
     out = {k: line[k] for k in keep}
     out["config"] = {k: v for k, v in out["config"].items() if k in ("workload", "l2")}
-    out["roofline"] = {k: v for k, v in out["roofline"].items() if k != "bytes_per_launch"}
+    if out["roofline"] is not None:
+        out["roofline"] = {k: v for k, v in out["roofline"].items() if k != "bytes_per_launch"}
     e2e = line["e2e"]
     out["e2e"] = {k: e2e[k] for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
     cpu = line.get("cpu_baseline")

@@ -170,15 +170,20 @@ __global__ void __launch_bounds__(kTsThreads, 1)
         }
         csync<CS>();  // the unit masses of every warp of the cluster
         // tokens removed earlier keep their own coefficient: correct their units (rank 0)
-        if (rank == 0 && tid == 0 && a != 0.f) {
-            for (int r = 0; r < st.nrem; ++r) {
-                if (s_remcoef[r] == a) continue;
-                const int j = s_remtok[r];
-                const float tj = load_elem<D>(tp, j), dj = load_elem<D>(dp, j);
-                if (SV_IN(j / RE, nunit)) um[j / RE] += wgt(tj, dj, st, s_remcoef[r], c) - wgt(tj, dj, st, a, c);
+        bool fix = false;  // (the same in every thread of the cluster)
+        if (a != 0.f)
+            for (int r = 0; r < st.nrem; ++r) fix |= s_remcoef[r] != a;
+        if (fix) {
+            if (rank == 0 && tid == 0) {
+                for (int r = 0; r < st.nrem; ++r) {
+                    if (s_remcoef[r] == a) continue;
+                    const int j = s_remtok[r];
+                    const float tj = load_elem<D>(tp, j), dj = load_elem<D>(dp, j);
+                    if (SV_IN(j / RE, nunit)) um[j / RE] += wgt(tj, dj, st, s_remcoef[r], c) - wgt(tj, dj, st, a, c);
+                }
             }
+            csync<CS>();
         }
-        csync<CS>();
         // total: lanes of warp 0 own contiguous runs of units, then a warp scan
         if (warp == 0) {
             const int per = (nunit + 31) / 32;
@@ -196,35 +201,57 @@ __global__ void __launch_bounds__(kTsThreads, 1)
         return tot;
     };
 
-    // (max, sum) of one row: warps reduce units, then a fixed-order merge; every thread
-    // returns (M, S) and whether the row is a distribution.
-    auto row_stats = [&](const char *row, int slot) -> float2 {
-        float2 ws = make_float2(-__int_as_float(0x7f800000), 0.f);
+    // (max, sum) of the target row and, with two, of the draft row, in one pass (both rows'
+    // loads in flight together): warps reduce units, then a fixed-order merge per row; every
+    // thread returns the target row's (M, S) and *ds the draft row's ((0, 1) without two).
+    auto row_stats2 = [&](const char *tp, const char *dp, bool two, float2 *ds) -> float2 {
+        float2 wt = make_float2(-__int_as_float(0x7f800000), 0.f), wd = wt;
         for (int u = gw; u < nunit; u += CS * kTsWarps) {
             const int64_t u0 = int64_t(u) * RE;
             const int len = unit_len(V, u0, RE);
-            uint4 v[kResVecs];
-            load_unit<D, VEC>(row, u0, len, lane, v);
-            const float M = warp_reduce(thread_max<D>(v), [](float x, float y) { return max_nan(x, y); });
-            float S = 0.f;
-            if (is_finite(M)) S = warp_reduce(thread_sumexp<D>(v, c, M), [](float x, float y) { return x + y; });
-            ws = merge_stats(ws, make_float2(M, S), c);
+            uint4 vt[kResVecs], vd[kResVecs];
+            load_unit<D, VEC>(tp, u0, len, lane, vt);
+            if (two) load_unit<D, VEC>(dp, u0, len, lane, vd);
+            const float Mt = warp_reduce(thread_max<D>(vt), [](float x, float y) { return max_nan(x, y); });
+            float St = 0.f;
+            if (is_finite(Mt)) St = warp_reduce(thread_sumexp<D>(vt, c, Mt), [](float x, float y) { return x + y; });
+            wt = merge_stats(wt, make_float2(Mt, St), c);
+            if (two) {
+                const float Md = warp_reduce(thread_max<D>(vd), [](float x, float y) { return max_nan(x, y); });
+                float Sd = 0.f;
+                if (is_finite(Md)) Sd = warp_reduce(thread_sumexp<D>(vd, c, Md), [](float x, float y) { return x + y; });
+                wd = merge_stats(wd, make_float2(Md, Sd), c);
+            }
         }
-        if (lane == 0) s_stat[slot][warp] = ws;
+        if (lane == 0) {
+            s_stat[0][warp] = wt;
+            s_stat[1][warp] = wd;
+        }
         __syncthreads();
-        float2 r = s_stat[slot][0];
-        for (int w = 1; w < kTsWarps; ++w) r = merge_stats(r, s_stat[slot][w], c);
+        float2 rt = s_stat[0][0], rd = s_stat[1][0];
+        for (int w = 1; w < kTsWarps; ++w) {
+            rt = merge_stats(rt, s_stat[0][w], c);
+            rd = merge_stats(rd, s_stat[1][w], c);
+        }
         if constexpr (CS > 1) {  // the CTAs' statistics, merged in rank order by each CTA
             float2 *cs = cstat + seq * CS * 2;
-            if (tid == 0) cs[rank * 2 + slot] = r;
+            if (tid == 0) {
+                cs[rank * 2] = rt;
+                cs[rank * 2 + 1] = rd;
+            }
             csync<CS>();
-            r = cs[slot];
-            for (int k = 1; k < CS; ++k) r = merge_stats(r, cs[k * 2 + slot], c);
+            rt = cs[0];
+            rd = cs[1];
+            for (int k = 1; k < CS; ++k) {
+                rt = merge_stats(rt, cs[k * 2], c);
+                rd = merge_stats(rd, cs[k * 2 + 1], c);
+            }
             csync<CS>();  // read by every CTA before the next statistics overwrite them
         } else {
             __syncthreads();
         }
-        return r;
+        *ds = two ? rd : make_float2(0.f, 1.f);
+        return rt;
     };
 
     int v = 0, depth = 0;
@@ -234,9 +261,8 @@ __global__ void __launch_bounds__(kTsThreads, 1)
         const char *tp = row_ptr(t, D::kBytes, seq, v);
         const char *dp = row_ptr(d, D::kBytes, seq, v);
         st.has_q = s_nch[v] > 0;
-        const float2 ts = row_stats(tp, 0);
-        float2 ds = make_float2(0.f, 1.f);
-        if (st.has_q) ds = row_stats(dp, 1);
+        float2 ds;
+        const float2 ts = row_stats2(tp, dp, st.has_q, &ds);
         if (!is_finite(ts.x) || (st.has_q && !is_finite(ds.x))) {  // not a distribution (R11)
             fail();
             return;
