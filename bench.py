@@ -542,7 +542,7 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None, 
         # the walk reads only the rows of the nodes it reaches: the every-row byte count of
         # the metric does not apply, and the kernel is bound by exponentials and latency
         res.update({"hbm_gbs_step": None, "frac_of_8tbs_step": None, "roofline": None,
-                    "lazy": "one CTA per sequence reads only the rows of the nodes its walk reaches",
+                    "lazy": "a cluster of CTAs per sequence reads only the rows of the nodes its walk reaches",
                     "mean_path_nodes": float(acc[acc >= 0].mean().item() + 1) if (acc >= 0).any() else None})
     if mode == "ngram":
         res.update({"rows_per_s": None, "roofline": None, "mean_accepted_len": None,
@@ -570,7 +570,8 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None, 
         level = kernel == "level_kernel"
         res.update({"hbm_gbs_step": sb / (ms_step / 1e3) / 1e9, "frac_of_8tbs_step": sb / (ms_step / 1e3) / 8e12,
                     "lazy": ("a level-synchronous walk over the whole GPU reads only the rows the rule needs"
-                             if level else "one CTA per sequence reads only the rows the rule needs"),
+                             if level else "a cluster of CTAs per sequence (one CTA when the batch fills the GPU) "
+                             "reads only the rows the rule needs"),
                     "rows_read_per_step": step_rows,
                     "roofline": {"bound": "hbm", "kernel": kernel, "achieved": lb / (dom_ms / 1e3) / 1e9,
                                  "peak": peak, "peak_kind": peak_kind + " copy (read+write) bandwidth",

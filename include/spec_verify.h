@@ -201,22 +201,29 @@ sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_str
 /*
  * LAZY verification: the same rules, reading only the rows that can change the result.
  * The rows after the first rejection, or beside the accepted nodes of a tree, never reach
- * the result; these entries run one CTA per sequence that walks the rule and reads the rows
- * it needs as it goes (one pass per row, plus one residual pass per rejection when
- * sampling).  They return exactly what the full entries return whenever every row is a
- * distribution (sampling) or NaN-free (greedy); a bad row the walk never reads does not
- * invalidate the sequence.  Outputs, arguments and errors as the full entries.
+ * the result; these entries walk the rule and read the rows it needs as it goes.  They
+ * return exactly what the full entries return whenever every row is a distribution
+ * (sampling) or NaN-free (greedy); a bad row the walk never reads does not invalidate the
+ * sequence.  Outputs, arguments and errors as the full entries.
  *
- *   spec_verify_sample_lazy       the chain rule of spec_verify_sample (the tree rule of
- *                                 spec_verify_tree_sample on the chain v -> v + 1, whose
- *                                 uniforms are the chain's, with its double-float re-walk
- *                                 of marked sequences); workspace:
+ *   spec_verify_sample_lazy       the chain rule of spec_verify_sample, walked level by
+ *                                 level over the whole GPU: at level i every sequence still
+ *                                 walking streams its target row i and draft row i (one
+ *                                 contiguous range of tiles per CTA), the CTA that completes
+ *                                 a sequence takes its accept test, and a grid barrier ends
+ *                                 the level (several levels at once when the rows of
+ *                                 sequences that will have stopped cost less than a level of
+ *                                 its own).  The residual masses and the draw, with the
+ *                                 double-float re-draw of every marked sequence, are
+ *                                 spec_verify_sample's kernels.  Workspace:
  *                                 spec_verify_workspace_size(SV_MODE_SAMPLE_LAZY, B, gamma,
  *                                 V, dtype) bytes.
  *   spec_verify_greedy_lazy       the rule of spec_verify_greedy; no workspace.
  *   spec_verify_tree_greedy_lazy  the rule of spec_verify_tree_greedy (every accepted node's
  *                                 row is read, so the deepest-node rule is unchanged); no
- *                                 workspace.
+ *                                 workspace.  Both greedy walks give a sequence a cluster of
+ *                                 up to 8 CTAs while the batch leaves SMs free (one CTA
+ *                                 otherwise), each CTA reading its share of a row's tiles.
  */
 sv_status spec_verify_sample_lazy(const void *target_logits, int64_t t_batch_stride,
                                   int64_t t_row_stride, const void *draft_logits,
@@ -248,13 +255,13 @@ sv_status spec_verify_tree_greedy_lazy(const void *target_logits, int64_t t_batc
  *   draft_tokens   [B][gamma] int32 (may be NULL when gamma == 0).
  *   temperature > 0; epsilon >= 0, delta >= 0 finite (epsilon = 0 accepts every draft the
  *   target gives positive probability).
- * Outputs as spec_verify_sample.  Rows are read lazily, one CTA per sequence: rows 0 .. k
- * only; a token outside [0, V) or a row read that is not a distribution gives -1.  The
- * accept tests are taken in fp32; every final draw whose threshold lies within 1e-6 of the
- * row's mass from a CDF boundary is redone in double-float arithmetic by two more kernels
+ * Outputs as spec_verify_sample.  Rows are read lazily by the level walk of
+ * spec_verify_sample_lazy (each tile also sums the entropy's Z): rows 0 .. k only; a token
+ * outside [0, V) or a row read that is not a distribution gives -1.  The accept tests are
+ * taken in fp32; the final draw is spec_verify_sample's, and every draw whose threshold
+ * lies within the fp32 error of a CDF boundary is redone in double-float arithmetic
  * (spec_verify_status_offset with SV_MODE_TYPICAL reports them).  Workspace:
- * spec_verify_workspace_size(SV_MODE_TYPICAL, B, gamma, V, dtype) bytes (per sequence 4
- * bytes per 1024 logits and 8 bytes per 256 logits of re-draw unit sums).
+ * spec_verify_workspace_size(SV_MODE_TYPICAL, B, gamma, V, dtype) bytes.
  */
 sv_status spec_verify_typical(const void *target_logits, int64_t t_batch_stride, int64_t t_row_stride,
                               sv_dtype dtype, int B, int gamma, int V, const int32_t *draft_tokens,
@@ -272,8 +279,8 @@ sv_status spec_verify_typical(const void *target_logits, int64_t t_batch_stride,
  * spec_verify_sample given draft rows that are -inf except 0 at x_i, without those rows.
  *   target_logits  [B][gamma+1][V] as spec_verify_sample; draft_tokens [B][gamma] (may be
  *                  NULL when gamma == 0); temperature > 0 (applied to p).
- * Outputs, errors and the lazy row reads as spec_verify_typical (one CTA per sequence,
- * rows 0 .. k; near-boundary final draws redone in double-float).  Workspace:
+ * Outputs, errors and the lazy row reads as spec_verify_typical (the level walk, rows
+ * 0 .. k; near-boundary accept tests and final draws redone in double-float).  Workspace:
  * spec_verify_workspace_size(SV_MODE_SAMPLE_ONEHOT, B, gamma, V, dtype) bytes.
  */
 sv_status spec_verify_sample_onehot(const void *target_logits, int64_t t_batch_stride,
