@@ -497,7 +497,7 @@ sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_str
                                    reinterpret_cast<float2 *>(at(workspace, L.rowstat)), rw, K, accepted_len,
                                    out_tokens, out_path, s);
     if (e == cudaSuccess) e = mark(1, s);
-    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, rw, s);
+    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, rw, accepted_len, s);
     if (e == cudaSuccess) e = mark(2, s);
     if (e == cudaSuccess)
         e = sv::launch_tree_rewalk(dtype == SV_BF16, t, d, B, N, V, false, parent, node_tokens, max_depth, temperature,

@@ -109,6 +109,10 @@ cudaError_t launch_draw_refine(int dtype, bool vec, Logits t, Logits d, int B, i
 // many).  The re-walk redoes every marked sequence in double-float arithmetic:
 // kMaxTreeRefine clusters, the first kMaxTreeRefine marked sequences with exponentials the
 // whole grid precomputed (slots), later ones computing them in their cluster.  Control block (int32, zeroed by the walk; words other than these stay 0):
+// Mark bits of a tree walk: a decision on the path came near flipping (the re-walk starts
+// at the root), or only the final draw at the reached node did (the path is certain: the
+// re-walk starts at that node).
+constexpr int kTrMarkPath = 1, kTrMarkFinal = 2;
 constexpr int kTrMarked = 0;  // sequences the last call marked
 constexpr int kTrRedone = 4;  // sequences redone (every marked one)
 constexpr int kTrCtlWords = 8;
@@ -141,10 +145,12 @@ __host__ __device__ inline int tree_refine_units(int V) {
 }
 inline int tree_rec_nodes(int max_depth) { return max_depth + 1 < kTreeRecNodes ? max_depth + 1 : kTreeRecNodes; }
 inline size_t tree_refine_smem(int N, int max_depth) { return size_t(13 * N + max_depth + 1) * 4; }
-// The exponentials of the listed sequences' recorded rows (every resident CTA), then the
-// re-walk (one cluster of 16 CTAs per listed sequence where the device holds one, else 8).
+// The exponentials of the listed sequences' recorded rows (every resident CTA; for a
+// sequence marked only at its final draw, the reached node's rows alone), then the re-walk
+// (one cluster of 16 CTAs per listed sequence where the device holds one, else 8).
+// accepted_len: the walk's outputs (the depth it reached).
 cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws,
-                            cudaStream_t s);
+                            const int32_t *accepted_len, cudaStream_t s);
 cudaError_t launch_tree_rewalk(int dtype, Logits t, Logits d, int B, int N, int V, bool chain, const int32_t *parent,
                                const int32_t *node_tokens, int max_depth, float T, uint64_t seed, uint64_t offset,
                                int without_replacement, int K, TreeRefineWs ws, int32_t *accepted_len,

@@ -128,13 +128,21 @@ __device__ df exp_unit(const char *row, float M, df inv_t, int V, int u, df *E, 
     return unit_sum(w, lane);
 }
 
+// A sequence the walk marked only at its final draw, with the path recorded down to the
+// node it reached (depth acc < K, acc + 1 records): its path is certain, so the re-walk
+// starts at that node.
+__device__ __forceinline__ bool final_only(int mark, int rlen, int acc, int K) {
+    return mark == kTrMarkFinal && acc >= 0 && acc < K && rlen == acc + 1;
+}
+
 }  // namespace
 
 // The exponentials of the recorded nodes of the first kMaxTreeRefine marked sequences
 // (grid-stride over (slot, position, row, unit), one warp per unit).
 template <class D>
 __global__ void __launch_bounds__(kThreads)
-    tree_exp_kernel(Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws) {
+    tree_exp_kernel(Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws,
+                    const int32_t *__restrict__ accepted_len) {
     __shared__ int s_seq[kMaxTreeRefine];
     __shared__ unsigned s_bal[kWarps];
     __shared__ int s_cnt[2];
@@ -156,7 +164,10 @@ __global__ void __launch_bounds__(kThreads)
         const int j = int(rest / (2 * int64_t(K)));
         const int64_t seq = s_seq[j];
         if (!SV_IN(seq, B) || !SV_IN(j, kMaxTreeRefine)) continue;
-        if (k >= __ldcg(ws.rlen + seq)) continue;  // (uniform over the warp)
+        const int rlen = __ldcg(ws.rlen + seq);
+        if (k >= rlen) continue;  // (uniform over the warp)
+        // marked only at the final draw: the reached node's rows alone
+        if (k != rlen - 1 && final_only(__ldcg(ws.mark + seq), rlen, __ldcg(accepted_len + seq), K)) continue;
         const float4 rec = __ldcg(ws.rec + seq * K + k);
         const int node = __float_as_int(rec.x);
         if (r == 1 && rec.w == 0.f) continue;  // a leaf: no draft row
@@ -276,7 +287,19 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         __syncthreads();
     };
 
+    // Marked only at its final draw, with the path recorded: start at the node the walk
+    // reached (its path, every decision on it taken outside the fp32 error, is certain).
     int v = 0, depth = 0, buf = 0;
+    {
+        const int rl = __ldcg(ws.rlen + seq), acc = __ldcg(accepted_len + seq);
+        if (final_only(__ldcg(ws.mark + seq), rl, acc, K)) {
+            for (int i = tid; i <= acc; i += kRwThreads) s_path[i] = __float_as_int(__ldcg(ws.rec + seq * K + i).x);
+            depth = acc;
+            v = __float_as_int(__ldcg(ws.rec + seq * K + acc).x);
+            if (!SV_IN(v, N)) v = 0, depth = 0;
+            __syncthreads();
+        }
+    }
     for (;;) {
         const char *tp = row_ptr(t, D::kBytes, seq, v);
         const char *dp = row_ptr(d, D::kBytes, seq, v);
@@ -600,11 +623,11 @@ __global__ void __launch_bounds__(kRwThreads, 1)
 }
 
 cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws,
-                            cudaStream_t s) {
+                            const int32_t *accepted_len, cudaStream_t s) {
     auto ke = dtype == 1 ? tree_exp_kernel<BF16> : tree_exp_kernel<F32>;
     unsigned grid = 0;  // every resident CTA
     cudaError_t e = persistent_grid(ke, int64_t(1) << 40, &grid);
-    if (e == cudaSuccess) e = launch_after(ke, grid, kThreads, 0, s, t, d, B, V, T, K, ws);
+    if (e == cudaSuccess) e = launch_after(ke, grid, kThreads, 0, s, t, d, B, V, T, K, ws, accepted_len);
     return e;
 }
 

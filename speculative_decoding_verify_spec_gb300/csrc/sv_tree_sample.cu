@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     __shared__ float2 s_stat[2][kTsWarps];
     __shared__ float s_sum[kTsWarps];
     __shared__ int s_flag;
-    __shared__ int s_near;  // a decision came near flipping in fp32: the re-walk redoes the sequence
+    __shared__ int s_near;  // kTrMark* bits: a decision came near flipping in fp32 (the re-walk redoes it)
     __shared__ int s_nrec;  // nodes recorded for the re-walk
     __shared__ float s_tx[2];
     griddep_launch_next();
@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
             // p's error: its own terms' rounding and D's, relative to D (both shrink with D)
             if (tid == 0 &&
                 fabsf(uq - px) < kTreeAcceptWindow * (fmaxf(px, uq) + __fdividef(p0x + ax * q0x + px * st.A, st.Dn)))
-                s_near = 1;
+                s_near |= kTrMarkPath;
             if (uq < px) {  // accepted
                 next = cnode;
                 break;
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
             // rejected: A grows by D s (q's current scale), x leaves q without replacement
             const float Anew = __fadd_rn(st.A, __fmul_rn(st.Dn, st.s));
             NodeState ns = st;
-            if (tid == 0 && without_replacement && !removed && st.nrem >= kMaxRemoved) s_near = 1;
+            if (tid == 0 && without_replacement && !removed && st.nrem >= kMaxRemoved) s_near |= kTrMarkPath;
             if (without_replacement && !removed && st.nrem < kMaxRemoved) {
                 if (tid == 0) {
                     s_remtok[st.nrem] = x;
@@ -328,11 +328,11 @@ __global__ void __launch_bounds__(kTsThreads, 1)
                 ns.nrem = st.nrem + 1;
                 ns.qrem = __fadd_rn(st.qrem, q0x);
                 ns.s = ns.qrem < 1.f ? 1.f / __fsub_rn(1.f, ns.qrem) : 0.f;
-                if (tid == 0 && !(ns.qrem < 1.f - kTreeQMassWindow)) s_near = 1;
+                if (tid == 0 && !(ns.qrem < 1.f - kTreeQMassWindow)) s_near |= kTrMarkPath;
             }
             __syncthreads();
             const float F = mass_pass(tp, dp, ns, Anew);
-            if (tid == 0 && !(F > kTreeMassWindow * (1.f + Anew))) s_near = 1;
+            if (tid == 0 && !(F > kTreeMassWindow * (1.f + Anew))) s_near |= kTrMarkPath;
             if (F > 0.f) {
                 ns.A = Anew;
                 ns.Dn = F;
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
             const float win = kTreeCdfWindow * (totd.hi + st.A) + token_window(1.f / st.inv_st) +
                               (st.A != 0.f ? st.A * token_window(1.f / st.inv_sd) : 0.f);
             if (lane == 0 && (first == kNoIndex || force_last || !(gap >= win)))
-                s_near = 1;
+                s_near |= kTrMarkFinal;
             lastpos = warp_reduce(lastpos, [](int a, int b) { return max(a, b); });
             int tok = first != kNoIndex ? first : lastpos;
             if (tok < 0) tok = 0;
