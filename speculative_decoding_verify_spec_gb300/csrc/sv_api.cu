@@ -491,7 +491,7 @@ sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_str
     const int K = sv::tree_rec_nodes(max_depth);
     cudaError_t e = mark(0, s);
     if (e == cudaSuccess)
-        e = sv::launch_tree_sample(dtype == SV_BF16, vec, t, d, B, N, V, false, parent, node_tokens, max_depth, c,
+        e = sv::launch_tree_sample(dtype == SV_BF16, vec, t, d, B, N, V, parent, node_tokens, max_depth, c,
                                    seed, offset, without_replacement, nrt_of(V, dtype),
                                    reinterpret_cast<float *>(at(workspace, 0)),
                                    reinterpret_cast<float2 *>(at(workspace, L.rowstat)), rw, K, accepted_len,
@@ -500,7 +500,7 @@ sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_str
     if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, rw, accepted_len, s);
     if (e == cudaSuccess) e = mark(2, s);
     if (e == cudaSuccess)
-        e = sv::launch_tree_rewalk(dtype == SV_BF16, t, d, B, N, V, false, parent, node_tokens, max_depth, temperature,
+        e = sv::launch_tree_rewalk(dtype == SV_BF16, t, d, B, N, V, parent, node_tokens, max_depth, temperature,
                                    seed, offset, without_replacement, K, rw, accepted_len, out_tokens, out_path, s);
     if (e == cudaSuccess) e = mark(3, s);
     return cuda_status(e);

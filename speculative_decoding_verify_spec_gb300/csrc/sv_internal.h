@@ -151,17 +151,16 @@ inline size_t tree_refine_smem(int N, int max_depth) { return size_t(13 * N + ma
 // accepted_len: the walk's outputs (the depth it reached).
 cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws,
                             const int32_t *accepted_len, cudaStream_t s);
-cudaError_t launch_tree_rewalk(int dtype, Logits t, Logits d, int B, int N, int V, bool chain, const int32_t *parent,
+cudaError_t launch_tree_rewalk(int dtype, Logits t, Logits d, int B, int N, int V, const int32_t *parent,
                                const int32_t *node_tokens, int max_depth, float T, uint64_t seed, uint64_t offset,
                                int without_replacement, int K, TreeRefineWs ws, int32_t *accepted_len,
                                int32_t *out_tokens, int32_t *out_path, cudaStream_t s);
-// Token-tree sampling (multi-round rejection), one CTA per sequence reading the rows of the
-// nodes its walk reaches; with chain, the tree whose node v has parent v - 1 and token
-// node_tokens[b][v - 1] ([B][N - 1]).  c = log2(e) / T; umass: [B][nunit] floats of
+// Token-tree sampling (multi-round rejection), a cluster of CTAs per sequence reading the
+// rows of the nodes its walk reaches.  c = log2(e) / T; umass: [B][nunit] floats of
 // scratch, nunit = ceil(V / res_tile_elems); cstat: [B][kTreeSampleCluster][2] float2;
 // rw, K: the re-walk's control block, marks and records (below).
 constexpr int kTreeSampleCluster = 4;  // at most this many CTAs (SMs) per sequence of the walk
-cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, bool chain,
+cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, int N, int V,
                                const int32_t *parent, const int32_t *node_tokens, int max_depth, float c, uint64_t seed,
                                uint64_t offset, int without_replacement, int nunit, float *umass, float2 *cstat,
                                TreeRefineWs rw, int K, int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,

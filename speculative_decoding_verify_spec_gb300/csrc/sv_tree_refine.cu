@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kThreads)
 // The re-walk: cluster j (CS CTAs) takes the marked sequences of rank j, j + 8, j + 16, ...
 template <class D, int CS>
 __global__ void __launch_bounds__(kRwThreads, 1)
-    tree_rewalk_kernel(Logits t, Logits d, int B, int N, int V, bool chain, const int32_t *__restrict__ parent,
+    tree_rewalk_kernel(Logits t, Logits d, int B, int N, int V, const int32_t *__restrict__ parent,
                        const int32_t *__restrict__ node_tokens, int max_depth, float T, uint64_t seed,
                        uint64_t offset, int without_replacement, int K, TreeRefineWs ws,
                        int32_t *__restrict__ accepted_len, int32_t *__restrict__ out_tokens,
@@ -235,8 +235,8 @@ __global__ void __launch_bounds__(kRwThreads, 1)
     if (tid == 0) s_flag = 1;
     __syncthreads();
     for (int v = tid; v < N; v += kRwThreads) {
-        const int p = chain ? v - 1 : parent[v];
-        const int tk = v == 0 ? 0 : (chain ? node_tokens[seq * (N - 1) + v - 1] : node_tokens[seq * N + v]);
+        const int p = parent[v];
+        const int tk = v == 0 ? 0 : node_tokens[seq * N + v];
         s_par[v] = p;
         s_tok[v] = tk;
         s_nch[v] = 0;
@@ -633,7 +633,7 @@ cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T
 
 namespace {
 template <int CS>
-cudaError_t launch_rewalk(int dtype, Logits t, Logits d, int B, int N, int V, bool chain, const int32_t *parent,
+cudaError_t launch_rewalk(int dtype, Logits t, Logits d, int B, int N, int V, const int32_t *parent,
                           const int32_t *node_tokens, int max_depth, float T, uint64_t seed, uint64_t offset,
                           int without_replacement, int K, TreeRefineWs ws, int32_t *accepted_len, int32_t *out_tokens,
                           int32_t *out_path, cudaStream_t s, bool probe, int *fits) {
@@ -661,25 +661,25 @@ cudaError_t launch_rewalk(int dtype, Logits t, Logits d, int B, int N, int V, bo
         cfg.numAttrs = 1;
         return cudaOccupancyMaxActiveClusters(fits, kw, &cfg);
     }
-    return cudaLaunchKernelEx(&cfg, kw, t, d, B, N, V, chain, parent, node_tokens, max_depth, T, seed, offset,
+    return cudaLaunchKernelEx(&cfg, kw, t, d, B, N, V, parent, node_tokens, max_depth, T, seed, offset,
                               without_replacement, K, ws, accepted_len, out_tokens, out_path);
 }
 }  // namespace
 
 // Clusters of 16 CTAs where the device can hold one (a non-portable size), else of 8.
-cudaError_t launch_tree_rewalk(int dtype, Logits t, Logits d, int B, int N, int V, bool chain, const int32_t *parent,
+cudaError_t launch_tree_rewalk(int dtype, Logits t, Logits d, int B, int N, int V, const int32_t *parent,
                                const int32_t *node_tokens, int max_depth, float T, uint64_t seed, uint64_t offset,
                                int without_replacement, int K, TreeRefineWs ws, int32_t *accepted_len,
                                int32_t *out_tokens, int32_t *out_path, cudaStream_t s) {
     static_assert(kTreeRefineCluster == 16, "the per-sequence scratch is sized for clusters of up to 16");
     int fits = 0;
-    cudaError_t e = launch_rewalk<16>(dtype, t, d, B, N, V, chain, parent, node_tokens, max_depth, T, seed, offset,
+    cudaError_t e = launch_rewalk<16>(dtype, t, d, B, N, V, parent, node_tokens, max_depth, T, seed, offset,
                                       without_replacement, K, ws, accepted_len, out_tokens, out_path, s, true, &fits);
     if (e == cudaSuccess && fits >= 1)
-        return launch_rewalk<16>(dtype, t, d, B, N, V, chain, parent, node_tokens, max_depth, T, seed, offset,
+        return launch_rewalk<16>(dtype, t, d, B, N, V, parent, node_tokens, max_depth, T, seed, offset,
                                  without_replacement, K, ws, accepted_len, out_tokens, out_path, s, false, nullptr);
     (void)cudaGetLastError();  // a refused size is not an error of this call
-    return launch_rewalk<8>(dtype, t, d, B, N, V, chain, parent, node_tokens, max_depth, T, seed, offset,
+    return launch_rewalk<8>(dtype, t, d, B, N, V, parent, node_tokens, max_depth, T, seed, offset,
                             without_replacement, K, ws, accepted_len, out_tokens, out_path, s, false, nullptr);
 }
 

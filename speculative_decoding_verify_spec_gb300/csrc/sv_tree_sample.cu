@@ -69,12 +69,10 @@ __device__ __forceinline__ void load_unit(const char *row, int64_t u0, int len, 
 // unit of each pass, and merges the CTAs' partials in rank order after a cluster barrier,
 // so all of them take the same decisions; rank 0 draws and writes the outputs.  cstat:
 // [B][CS][2] per-CTA row statistics.  Shared: parent, tokens, child counts, depths, the path, the
-// removed tokens and their frozen coefficients, and the reduction scratch.  chain: the
-// tree whose node v has parent v - 1 and token node_tokens[seq * (N - 1) + v - 1] (the
-// chain rule of spec_verify_sample, read lazily).
+// removed tokens and their frozen coefficients, and the reduction scratch.
 template <class D, bool VEC, int CS>
 __global__ void __launch_bounds__(kTsThreads, 1)
-    tree_sample_kernel(Logits t, Logits d, int N, int V, bool chain, const int32_t *__restrict__ parent,
+    tree_sample_kernel(Logits t, Logits d, int N, int V, const int32_t *__restrict__ parent,
                        const int32_t *__restrict__ node_tokens, int max_depth, float c, uint64_t seed,
                        uint64_t offset, int without_replacement, int nunit, float *umass, float2 *cstat,
                        TreeRefineWs rw, int K, int32_t *__restrict__ accepted_len,
@@ -114,10 +112,10 @@ __global__ void __launch_bounds__(kTsThreads, 1)
     }
     __syncthreads();
     for (int v = tid; v < N; v += kTsThreads) {
-        const int p = chain ? v - 1 : parent[v];
+        const int p = parent[v];
         s_par[v] = p;
         s_nch[v] = 0;
-        const int tk = v == 0 ? 0 : (chain ? node_tokens[seq * (N - 1) + v - 1] : node_tokens[seq * N + v]);
+        const int tk = v == 0 ? 0 : node_tokens[seq * N + v];
         s_tok[v] = tk;
         if ((v == 0 && p != -1) || (v > 0 && (p < 0 || p >= v)) || tk < 0 || tk >= V) s_flag = 0;
     }
@@ -498,7 +496,7 @@ __global__ void __launch_bounds__(kTsThreads, 1)
 
 namespace {
 template <int CS>
-cudaError_t launch_walk(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, bool chain, const int32_t *parent,
+cudaError_t launch_walk(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, const int32_t *parent,
                         const int32_t *node_tokens, int max_depth, float c, uint64_t seed, uint64_t offset,
                         int without_replacement, int nunit, float *umass, float2 *cstat, TreeRefineWs rw, int K,
                         int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path, cudaStream_t s) {
@@ -519,7 +517,7 @@ cudaError_t launch_walk(int dtype, bool vec, Logits t, Logits d, int B, int N, i
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = CS > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, k, t, d, N, V, chain, parent, node_tokens, max_depth, c, seed, offset,
+    return cudaLaunchKernelEx(&cfg, k, t, d, N, V, parent, node_tokens, max_depth, c, seed, offset,
                               without_replacement, nunit, umass, cstat, rw, K, accepted_len, out_tokens, out_path);
 }
 }  // namespace
@@ -527,7 +525,7 @@ cudaError_t launch_walk(int dtype, bool vec, Logits t, Logits d, int B, int N, i
 // The cluster size: as many SMs per sequence as keep every sequence's cluster resident at
 // once (a pass is a few unit loads per warp, so a second wave of clusters costs more than
 // a wider cluster saves).
-cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, int N, int V, bool chain,
+cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, int N, int V,
                                const int32_t *parent, const int32_t *node_tokens, int max_depth, float c, uint64_t seed,
                                uint64_t offset, int without_replacement, int nunit, float *umass, float2 *cstat,
                                TreeRefineWs rw, int K, int32_t *accepted_len, int32_t *out_tokens, int32_t *out_path,
@@ -538,12 +536,12 @@ cudaError_t launch_tree_sample(int dtype, bool vec, Logits t, Logits d, int B, i
     if (e != cudaSuccess) return e;
     static_assert(kTreeSampleCluster == 4, "the statistics scratch is sized for clusters of up to 4");
     if (int64_t(B) * 4 <= sms)
-        return launch_walk<4>(dtype, vec, t, d, B, N, V, chain, parent, node_tokens, max_depth, c, seed, offset,
+        return launch_walk<4>(dtype, vec, t, d, B, N, V, parent, node_tokens, max_depth, c, seed, offset,
                               without_replacement, nunit, umass, cstat, rw, K, accepted_len, out_tokens, out_path, s);
     if (int64_t(B) * 2 <= sms)
-        return launch_walk<2>(dtype, vec, t, d, B, N, V, chain, parent, node_tokens, max_depth, c, seed, offset,
+        return launch_walk<2>(dtype, vec, t, d, B, N, V, parent, node_tokens, max_depth, c, seed, offset,
                               without_replacement, nunit, umass, cstat, rw, K, accepted_len, out_tokens, out_path, s);
-    return launch_walk<1>(dtype, vec, t, d, B, N, V, chain, parent, node_tokens, max_depth, c, seed, offset,
+    return launch_walk<1>(dtype, vec, t, d, B, N, V, parent, node_tokens, max_depth, c, seed, offset,
                           without_replacement, nunit, umass, cstat, rw, K, accepted_len, out_tokens, out_path, s);
 }
 
