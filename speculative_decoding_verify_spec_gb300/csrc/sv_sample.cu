@@ -20,6 +20,8 @@
 //   draw            one warp per sequence: prefix over the unit masses (residual tiles, or
 //                   the tiles of p for a bonus draw), then an in-order scan inside the chosen
 //                   unit held in registers; the first j with C_j > u' R.
+#include <algorithm>
+
 #include "sv_checks.cuh"
 #include "sv_device.cuh"
 #include "sv_df.cuh"
@@ -663,8 +665,12 @@ cudaError_t launch_draw_refine(int dtype, bool vec, Logits t, Logits d, int B, i
                                void *rresc, bool early, cudaStream_t s) {
     auto k = pick(dtype, vec, draw_refine_kernel<BF16, true>, draw_refine_kernel<BF16, false>,
                   draw_refine_kernel<F32, true>, draw_refine_kernel<F32, false>);
-    unsigned grid = 0;  // every resident slot, at most one warp per sequence for the draws
-    cudaError_t e = persistent_grid(k, int64_t(1) << 40, &grid);
+    // every resident slot, or fewer for a small problem: a warp per sequence for the draws
+    // and a warp per two units of a listed row pair for the re-draw's grid-wide phase (a
+    // grid of one or two CTAs meets at its barriers at once)
+    unsigned grid = 0;
+    const int64_t warps = std::max<int64_t>(B, int64_t(B) * refine_units(V) / 2);
+    cudaError_t e = persistent_grid(k, warps, &grid);
     if (e != cudaSuccess) return e;
     return launch_after_ex(true, k, grid, kThreads, 0, s, t, d, B, gamma, V, ntile, nrt, c, T, seed, offset, rule, R,
                            lavail, x,
