@@ -44,6 +44,10 @@ DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "max_tiles_kernel",
                    "sample_lazy": "level_kernel", "greedy_lazy": "greedy_walk_kernel",
                    "tree_lazy": "greedy_walk_kernel", "ngram": "ngram_draft_kernel",
                    "typical": "level_kernel", "onehot": "level_kernel"}
+# one sequence with few tiles runs as one kernel (single_sample_kernel): its stage events
+# 2..4 are recorded right after it
+DOMINANT_BY_WORKLOAD = {"sample_b1": "single_sample_kernel"}
+STAGES_BY_WORKLOAD = {"sample_b1": ["one_kernel", "none_1", "none_2", "none_3"]}
 STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
 ACCEPT_STEPS = 16  # untimed steps whose accepted lengths and re-draw counts are read back
 STAGES = {"sample": ["row_stats", "decide", "residual_mass", "draw_redraw"],
@@ -521,14 +525,15 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None, 
     kb = kernel_bytes(name, **ov)
     dom_ms = stage_ms[0]
     achieved = kb / (dom_ms / 1e3) / 1e9
-    kernel = DOMINANT_KERNEL[mode]
+    kernel = DOMINANT_BY_WORKLOAD.get(name, DOMINANT_KERNEL[mode])
+    stage_names = STAGES_BY_WORKLOAD.get(name, STAGES[mode])
     acc = outs[0].float()
     res = {
         "workload": W.DESCRIPTIONS[name], "value": value, "unit": UNIT, "ms_per_step": ms_step,
         "steps": steps, "rows_per_s": world * W.rows(name, **ov) / (ms_step / 1e3),
         "hbm_gbs_step": logical / (ms_step / 1e3) / 1e9,
         "frac_of_8tbs_step": logical / (ms_step / 1e3) / 8e12,
-        "stages_ms": dict(zip(STAGES[mode], stage_ms)), "l2": l2_note,
+        "stages_ms": dict(zip(stage_names, stage_ms)), "l2": l2_note,
         "mean_accepted_len": float(acc[acc >= 0].mean().item()) if (acc >= 0).any() else None,
         "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind + " copy (read+write) bandwidth", "unit": "GB/s",

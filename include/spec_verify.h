@@ -398,7 +398,9 @@ sv_status spec_verify_exp_df(const float *y_hi, const float *y_lo, int n, float 
  * records events[0] on its stream before its first kernel and events[s] after its s-th
  * kernel (s = 1 .. n_events-1; sampling has 4 kernels: row statistics, decide, residual
  * masses, and the inverse-CDF draw with the extended-precision re-draw of near-boundary
- * sequences (one cooperative grid); greedy and tree have 2: tile maxima, finalize; the lazy
+ * sequences (one cooperative grid); a sampling call with B = 1 and (2 gamma + 1) row tiles
+ * of at most 256 runs all four stages in one kernel of one thread block, and records
+ * events[2..4] right after it; greedy and tree have 2: tile maxima, finalize; the lazy
  * greedy walks have 1; tree sampling has 3: the walk, the re-walk's exponentials, the
  * re-walk; lazy sampling has 3: the level walk, residual masses, the draw with its re-draw;
  * typical acceptance and one-hot sampling have 2: the level walk, the draw with its

@@ -371,6 +371,18 @@ sv_status spec_verify_sample(const void *target_logits, int64_t t_batch_stride,
     float *csum = reinterpret_cast<float *>(at(workspace, L.csum));
 
     cudaError_t e = mark(0, s);
+    if (sv::single_sample_fits(B, gamma, ntile)) {  // one kernel; every later stage event after it
+        if (e == cudaSuccess)
+            e = sv::launch_single_sample(dt, vec, t, d, gamma, V, ntile, nrt, c, temperature, seed, offset, draft_tokens,
+                                         partial, rowstat, plan, csum, accepted_len, out_tokens,
+                                         reinterpret_cast<int *>(at(workspace, L.rctl)),
+                                         reinterpret_cast<int *>(at(workspace, L.rbar)),
+                                         reinterpret_cast<sv::RefineInfo *>(at(workspace, L.rlist)),
+                                         at(workspace, L.rsum), reinterpret_cast<int *>(at(workspace, L.ramb)),
+                                         at(workspace, L.rresc), s);
+        for (int st = 1; st <= 4 && e == cudaSuccess; ++st) e = mark(st, s);
+        return cuda_status(e);
+    }
     if (e == cudaSuccess)
         e = sv::launch_stats_tiles(dt, vec, t, gamma + 1, d, R, B, V, ntile, c, partial, s);
     if (e == cudaSuccess) e = mark(1, s);

@@ -84,6 +84,15 @@ cudaError_t launch_decide(int dtype, Logits t, Logits d, int B, int gamma, int V
 cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V,
                                   int nrt, float c, const void *rowstat, const void *plan, float *csum,
                                   cudaStream_t s);
+// One sequence whose 2 gamma + 1 rows hold at most kSingleTiles tiles: the whole sampling
+// call (the four kernels' stages and the re-draw) in one kernel of one CTA; same workspace.
+constexpr int kSingleTiles = 256;
+bool single_sample_fits(int B, int gamma, int ntile);
+cudaError_t launch_single_sample(int dtype, bool vec, Logits t, Logits d, int gamma, int V, int ntile, int nrt,
+                                 float c, float T, uint64_t seed, uint64_t offset, const int32_t *x, void *partial,
+                                 void *rowstat, void *plan, float *csum, int32_t *accepted_len, int32_t *out_tokens,
+                                 int *rctl, int *rbar, RefineInfo *rinfo, void *rsum, int *ramb, void *rresc,
+                                 cudaStream_t s);
 // Inverse-CDF draw of the final token on the stop row of every valid sequence, then the
 // extended-precision re-draw of every sequence it or decide marked (one cooperative grid;
 // rbar: its grid barrier's words; rsum, ramb, rresc: the re-draw's scratch, see above).

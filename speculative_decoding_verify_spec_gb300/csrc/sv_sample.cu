@@ -98,37 +98,21 @@ __global__ void __launch_bounds__(kThreads, 4)
 // Decide, one CTA per sequence: warp w merges the tile partials of rows w, w + kDecideWarps,
 // ... into (M, S); warp 0 then runs the accept scan.
 constexpr int kDecideWarps = 16;
-template <class D>
-__global__ void __launch_bounds__(kDecideWarps * 32)
-    decide_kernel(Logits t, Logits d, int B, int gamma, int V, int ntile, float c,
-                  const int32_t *__restrict__ x, uint64_t seed, uint64_t offset,
-                  const float2 *__restrict__ partial, float2 *__restrict__ rowstat,
-                  int2 *__restrict__ plan, int32_t *__restrict__ accepted_len,
-                  int32_t *__restrict__ out_tokens, int *__restrict__ rflag, int *__restrict__ rctl,
-                  int *__restrict__ rbar) {
-    extern __shared__ float2 s_stat[];  // [2 gamma + 1]
-    griddep_launch_next();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t seq = blockIdx.x;
-    const int R = 2 * gamma + 1;
 
-    // the accept test's operands for the first 32 drafts do not depend on the statistics
-    // (nor on an earlier kernel): their loads go out before the wait
-    int32_t x0 = 0;
-    float tx0 = 0.f, dx0 = 0.f;
-    if (warp == 0 && lane < gamma) {
-        x0 = x[seq * gamma + lane];
-        if (x0 >= 0 && x0 < V) {
-            tx0 = load_elem<D>(row_ptr(t, D::kBytes, seq, lane), x0);
-            dx0 = load_elem<D>(row_ptr(d, D::kBytes, seq, lane), x0);
-        }
-    }
-    griddep_wait();
-    if (blockIdx.x == 0 && threadIdx.x < kRefineCtlWords) {  // this call's re-draw lists and barrier
-        rctl[threadIdx.x] = 0;
-        rbar[threadIdx.x] = 0;
-    }
-    for (int r = warp; r < R; r += kDecideWarps) {
+// The decision of sequence seq by the NW warps of a CTA (after the previous kernel's data is
+// visible): warp w merges the tile partials of rows w, w + NW, ... into (M, S) (s_stat:
+// [2 gamma + 1]); warp 0 then runs the accept scan.  x0, tx0, dx0: lane i's (< gamma) draft
+// token and its two logits, loaded by the caller.
+template <class D, int NW>
+__device__ __forceinline__ void decide_sequence(Logits t, Logits d, int B, int gamma, int V, int ntile, float c,
+                                                const int32_t *__restrict__ x, uint64_t seed, uint64_t offset,
+                                                const float2 *__restrict__ partial, float2 *__restrict__ rowstat,
+                                                int2 *__restrict__ plan, int32_t *__restrict__ accepted_len,
+                                                int32_t *__restrict__ out_tokens, int *__restrict__ rflag,
+                                                int64_t seq, int32_t x0, float tx0, float dx0, float2 *s_stat) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int R = 2 * gamma + 1;
+    for (int r = warp; r < R; r += NW) {
         const bool in = SV_IN((seq * R + r + 1) * ntile - 1, int64_t(B) * R * ntile);
         const float2 st = in ? warp_merge_stats(partial + (seq * R + r) * ntile, ntile, c, lane) : make_float2(0.f, 1.f);
         if (lane == 0) {
@@ -199,6 +183,39 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
     }
 }
 
+template <class D>
+__global__ void __launch_bounds__(kDecideWarps * 32)
+    decide_kernel(Logits t, Logits d, int B, int gamma, int V, int ntile, float c,
+                  const int32_t *__restrict__ x, uint64_t seed, uint64_t offset,
+                  const float2 *__restrict__ partial, float2 *__restrict__ rowstat,
+                  int2 *__restrict__ plan, int32_t *__restrict__ accepted_len,
+                  int32_t *__restrict__ out_tokens, int *__restrict__ rflag, int *__restrict__ rctl,
+                  int *__restrict__ rbar) {
+    extern __shared__ float2 s_stat[];  // [2 gamma + 1]
+    griddep_launch_next();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t seq = blockIdx.x;
+
+    // the accept test's operands for the first 32 drafts do not depend on the statistics
+    // (nor on an earlier kernel): their loads go out before the wait
+    int32_t x0 = 0;
+    float tx0 = 0.f, dx0 = 0.f;
+    if (warp == 0 && lane < gamma) {
+        x0 = x[seq * gamma + lane];
+        if (x0 >= 0 && x0 < V) {
+            tx0 = load_elem<D>(row_ptr(t, D::kBytes, seq, lane), x0);
+            dx0 = load_elem<D>(row_ptr(d, D::kBytes, seq, lane), x0);
+        }
+    }
+    griddep_wait();
+    if (blockIdx.x == 0 && threadIdx.x < kRefineCtlWords) {  // this call's re-draw lists and barrier
+        rctl[threadIdx.x] = 0;
+        rbar[threadIdx.x] = 0;
+    }
+    decide_sequence<D, kDecideWarps>(t, d, B, gamma, V, ntile, c, x, seed, offset, partial, rowstat, plan,
+                                     accepted_len, out_tokens, rflag, seq, x0, tx0, dx0, s_stat);
+}
+
 // ------------------------------------------------------------------------------------
 // Residual masses: csum[seq * nrt + tile] = sum over the residual tile of (p - q)+ at the
 // stop row, for the sequences that rejected (plan mode 1); other entries are not written.
@@ -220,6 +237,33 @@ __device__ __forceinline__ void load_residual_tile(const char *tp, const char *d
         tv[u] = e0 < len ? load_vec<D, VEC>(tp, c0, e0, len) : neg_inf_vec<D>();
         dv[u] = e0 < len ? load_vec<D, VEC>(dp, c0, e0, len) : neg_inf_vec<D>();
     }
+}
+
+// The residual mass sum (p - q)+ of one loaded residual tile (every lane returns it): element
+// pairs in FP32x2, even and odd elements summed separately, then the warp.
+template <class D>
+__device__ __forceinline__ float residual_tile_mass(const uint4 (&tv)[kResVecs], const uint4 (&dv)[kResVecs], float c,
+                                                    float2 st, float inv_st, float2 sd, float inv_sd) {
+    float2 acc = make_float2(0.f, 0.f);
+    const float2 c2 = make_float2(c, c), nmt2 = make_float2(-st.x, -st.x), inv_st2 = make_float2(inv_st, inv_st),
+                 nmd2 = make_float2(-sd.x, -sd.x), inv_sd2 = make_float2(inv_sd, inv_sd);
+#pragma unroll
+    for (int u = 0; u < kResVecs; ++u) {
+        const uint32_t tw[4] = {tv[u].x, tv[u].y, tv[u].z, tv[u].w}, dw[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
+#pragma unroll
+        for (int q = 0; q < 4; q += (D::EPV == 8 ? 1 : 2)) {
+            float2 t2, d2;
+            if constexpr (D::EPV == 8) {
+                t2 = make_float2(bf16_lo(tw[q]), bf16_hi(tw[q]));
+                d2 = make_float2(bf16_lo(dw[q]), bf16_hi(dw[q]));
+            } else {
+                t2 = make_float2(__uint_as_float(tw[q]), __uint_as_float(tw[q + 1]));
+                d2 = make_float2(__uint_as_float(dw[q]), __uint_as_float(dw[q + 1]));
+            }
+            acc = __fadd2_rn(acc, residual_weight2(t2, d2, c2, nmt2, inv_st2, nmd2, inv_sd2));
+        }
+    }
+    return warp_reduce(acc.x + acc.y, [](float x, float y) { return x + y; });
 }
 
 template <class D, bool VEC>
@@ -253,27 +297,7 @@ __global__ void __launch_bounds__(kThreads, kResidualCtas)
                     const int64_t n0 = (it + 1 - seq * nrt) * RE;
                     load_residual_tile<D, VEC>(tp, dp, n0, unit_len(V, n0, RE), lane, ntv, ndv);
                 }
-                float2 acc = make_float2(0.f, 0.f);
-                const float2 c2 = make_float2(c, c), nmt2 = make_float2(-st.x, -st.x),
-                             inv_st2 = make_float2(inv_st, inv_st), nmd2 = make_float2(-sd.x, -sd.x),
-                             inv_sd2 = make_float2(inv_sd, inv_sd);
-#pragma unroll
-                for (int u = 0; u < kResVecs; ++u) {
-                    const uint32_t tw[4] = {tv[u].x, tv[u].y, tv[u].z, tv[u].w}, dw[4] = {dv[u].x, dv[u].y, dv[u].z, dv[u].w};
-#pragma unroll
-                    for (int q = 0; q < 4; q += (D::EPV == 8 ? 1 : 2)) {
-                        float2 t2, d2;
-                        if constexpr (D::EPV == 8) {
-                            t2 = make_float2(bf16_lo(tw[q]), bf16_hi(tw[q]));
-                            d2 = make_float2(bf16_lo(dw[q]), bf16_hi(dw[q]));
-                        } else {
-                            t2 = make_float2(__uint_as_float(tw[q]), __uint_as_float(tw[q + 1]));
-                            d2 = make_float2(__uint_as_float(dw[q]), __uint_as_float(dw[q + 1]));
-                        }
-                        acc = __fadd2_rn(acc, residual_weight2(t2, d2, c2, nmt2, inv_st2, nmd2, inv_sd2));
-                    }
-                }
-                const float mass = warp_reduce(acc.x + acc.y, [](float x, float y) { return x + y; });
+                const float mass = residual_tile_mass<D>(tv, dv, c, st, inv_st, sd, inv_sd);
                 if (lane == 0 && SV_IN(it, items)) csum[it] = mass;
                 if (it + 1 < run_end) {
                     if (kResidualPrefetch) {
@@ -581,6 +605,95 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ------------------------------------------------------------------------------------
+// One sequence whose rows hold few tiles (B = 1, at most kSingleTiles tiles): the whole
+// sampling call in ONE kernel of one CTA.  The stages are those of the four-kernel path --
+// the rows' tile partials, decide_sequence, the residual masses of the stop row, the draw
+// and the re-draw phases (a one-CTA grid meets at its grid barriers at once) -- each after
+// a CTA barrier, with the same per-tile, per-sequence and re-draw code, so the outputs are
+// the four-kernel path's bit for bit.  Such a call is bound by launch latency, not by its
+// arithmetic; one launch replaces four.
+template <class D, bool VEC>
+__global__ void __launch_bounds__(kThreads, 1)
+    single_sample_kernel(Logits t, Logits d, int gamma, int V, int ntile, int nrt, float c, float T, uint64_t seed,
+                         uint64_t offset, const int32_t *__restrict__ x, float2 *__restrict__ partial,
+                         float2 *__restrict__ rowstat, int2 *__restrict__ plan, float *__restrict__ csum,
+                         int32_t *__restrict__ accepted_len, int32_t *__restrict__ out_tokens, int *__restrict__ rctl,
+                         int *__restrict__ rbar, RefineInfo *__restrict__ rinfo, df *__restrict__ rsum,
+                         int *__restrict__ ramb, df *__restrict__ rresc) {
+    __shared__ RefineSmem sm;
+    __shared__ float2 s_stat[kSingleTiles];
+    griddep_launch_next();
+    griddep_wait();  // before any read: the caller's previous kernel may be writing the inputs
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int R = 2 * gamma + 1;
+    int *rflag = rctl + kRefineCtlWords;
+    if (threadIdx.x < kRefineCtlWords) {  // this call's re-draw lists and barrier
+        rctl[threadIdx.x] = 0;
+        rbar[threadIdx.x] = 0;
+    }
+    // the rows' tile partials, a warp per tile
+    const int items = R * ntile;
+    for (int it = warp; it < items; it += kWarps) {
+        const int local = it / ntile, tile = it - local * ntile;
+        const char *rp = local <= gamma ? row_ptr(t, D::kBytes, 0, local) : row_ptr(d, D::kBytes, 0, local - gamma - 1);
+        const int64_t c0 = int64_t(tile) * tile_elems<D>();
+        const int len = unit_len(V, c0, tile_elems<D>());
+        uint4 v[kTileVecs];
+#pragma unroll
+        for (int u = 0; u < kTileVecs; ++u) {
+            const int e0 = (lane + 32 * u) * D::EPV;
+            v[u] = e0 < len ? load_vec<D, VEC>(rp, c0, e0, len) : neg_inf_vec<D>();
+        }
+        const float M = warp_reduce(thread_max<D>(v), [](float a, float b) { return max_nan(a, b); });
+        float S = 0.f;
+        if (is_finite(M)) S = warp_reduce(thread_sumexp<D>(v, c, M), [](float a, float b) { return a + b; });
+        if (lane == 0 && SV_IN(it, items)) partial[it] = make_float2(M, S);
+    }
+    int32_t x0 = 0;
+    float tx0 = 0.f, dx0 = 0.f;
+    if (warp == 0 && lane < gamma) {
+        x0 = x[lane];
+        if (x0 >= 0 && x0 < V) {
+            tx0 = load_elem<D>(row_ptr(t, D::kBytes, 0, lane), x0);
+            dx0 = load_elem<D>(row_ptr(d, D::kBytes, 0, lane), x0);
+        }
+    }
+    __syncthreads();
+    decide_sequence<D, kWarps>(t, d, 1, gamma, V, ntile, c, x, seed, offset, partial, rowstat, plan, accepted_len,
+                               out_tokens, rflag, 0, x0, tx0, dx0, s_stat);
+    __syncthreads();
+    // the residual masses of the stop row, a warp per residual tile
+    int2 pl = plan[0];
+    if (pl.x < 0 || pl.x > gamma || pl.y < 0 || pl.y > 2 || (pl.y == 1 && pl.x == gamma)) pl = make_int2(-1, -1);
+    if (pl.y == 1) {
+        const int k = pl.x;
+        const float2 st = rowstat[k], sd = rowstat[gamma + 1 + k];
+        const float inv_st = 1.f / st.y, inv_sd = 1.f / sd.y;
+        const char *tp = row_ptr(t, D::kBytes, 0, k), *dp = row_ptr(d, D::kBytes, 0, k);
+        constexpr int RE = res_tile_elems<D>();
+        for (int it = warp; it < nrt; it += kWarps) {
+            uint4 tv[kResVecs], dv[kResVecs];
+            load_residual_tile<D, VEC>(tp, dp, int64_t(it) * RE, unit_len(V, int64_t(it) * RE, RE), lane, tv, dv);
+            const float mass = residual_tile_mass<D>(tv, dv, c, st, inv_st, sd, inv_sd);
+            if (lane == 0 && SV_IN(it, nrt)) csum[it] = mass;
+        }
+    }
+    __syncthreads();
+    // the draw (warp 0), then the re-draw phases over the whole (one-CTA) grid
+    if (warp == 0 && pl.y >= 0) {
+        const float2 st = rowstat[pl.x];
+        const float2 sdk = pl.y == 1 ? rowstat[gamma + 1 + pl.x] : make_float2(0.f, 1.f);
+        const float u1 = uniform01(seed, offset, 0u, uint32_t(pl.x), 1u);
+        draw_sequence<D, VEC>(t, d, 1, gamma, V, ntile, nrt, R, x, c, partial, csum, out_tokens, rflag, rctl, rinfo, 0,
+                              pl, st, sdk, rflag[0], u1, lane);
+    }
+    __syncthreads();
+    const RefineArgs ra{t, d, 1, gamma, V, kRuleSample, R, nullptr, T, seed, offset, x, rowstat, rctl, rbar, rinfo, rsum,
+                        ramb, rresc, accepted_len, out_tokens};
+    refine_phases<D>(ra, sm);
+}
+
+// ------------------------------------------------------------------------------------
 __global__ void rowstats_finalize_kernel(int rows, int ntile, float c, float inv_t,
                                          const float2 *__restrict__ partial, float *__restrict__ m_out,
                                          float *__restrict__ lse_out) {
@@ -655,6 +768,21 @@ cudaError_t launch_residual_tiles(int dtype, bool vec, Logits t, Logits d, int B
     const int64_t per = (items + nwarps - 1) / nwarps;
     return launch_after(k, grid, kThreads, 0, s, t, d, gamma, V, nrt, items, per, c,
                         static_cast<const float2 *>(rowstat), static_cast<const int2 *>(plan), csum);
+}
+
+bool single_sample_fits(int B, int gamma, int ntile) { return B == 1 && (2 * int64_t(gamma) + 1) * ntile <= kSingleTiles; }
+
+cudaError_t launch_single_sample(int dtype, bool vec, Logits t, Logits d, int gamma, int V, int ntile, int nrt,
+                                 float c, float T, uint64_t seed, uint64_t offset, const int32_t *x, void *partial,
+                                 void *rowstat, void *plan, float *csum, int32_t *accepted_len, int32_t *out_tokens,
+                                 int *rctl, int *rbar, RefineInfo *rinfo, void *rsum, int *ramb, void *rresc,
+                                 cudaStream_t s) {
+    auto k = pick(dtype, vec, single_sample_kernel<BF16, true>, single_sample_kernel<BF16, false>,
+                  single_sample_kernel<F32, true>, single_sample_kernel<F32, false>);
+    return launch_after(k, 1u, kThreads, 0, s, t, d, gamma, V, ntile, nrt, c, T, seed, offset, x,
+                        static_cast<float2 *>(partial), static_cast<float2 *>(rowstat), static_cast<int2 *>(plan), csum,
+                        accepted_len, out_tokens, rctl, rbar, rinfo, static_cast<df *>(rsum), ramb,
+                        static_cast<df *>(rresc));
 }
 
 cudaError_t launch_draw_refine(int dtype, bool vec, Logits t, Logits d, int B, int gamma, int V, int ntile, int nrt,

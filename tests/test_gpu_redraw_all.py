@@ -83,8 +83,8 @@ def tuned_accept_rows(V, u0, x, rng):
     return t, d
 
 
-def chain_batch(B, V, seed, offset, rng):
-    """gamma = 2, T = 1, fp32.  Sequence b of kind b % 3:
+def chain_batch(B, V, seed, offset, rng, kind_of=lambda b: b % 3):
+    """gamma = 2, T = 1, fp32.  Sequence b of kind kind_of(b) (b % 3 by default):
       0  accepted drafts (target = draft on rows 0, 1), the bonus draw on row 2 tuned;
       1  row 0 rejected for certain (q one-hot on x0, p(x0) ~ e^-40), the residual draw on
          row 0 tuned (the residual is p without x0);
@@ -94,7 +94,7 @@ def chain_batch(B, V, seed, offset, rng):
     d = t[:, :G].copy()
     x = rng.integers(0, V, (B, G)).astype(np.int32)
     for b in range(B):
-        kind = b % 3
+        kind = kind_of(b)
         if kind == 0:
             t[b, G], _ = tuned_draw_row(V, oracle.uniform(seed, offset, b, G, 1), rng)
         elif kind == 1:
@@ -211,3 +211,23 @@ def test_target_only_rules_redraw_every_marked_sequence():
     assert (acc.cpu().numpy() == s_acc).all()
     assert (out.cpu().numpy() == s_out).all()
     check_status(ws2, binding.MODE_SAMPLE_ONEHOT, 2, int(0.95 * B))
+
+
+def test_single_sequence_call_redoes_its_marked_sequence():
+    """B = 1 with few tiles runs as one kernel of one CTA (its stages and the re-draw in
+    one launch): each kind of near-boundary decision, planted for sequence 0, is marked,
+    redone and equals the oracle; the four-kernel path on a batch of two agrees on it."""
+    rng = np.random.default_rng(77)
+    for kind in (0, 1, 2):
+        for rep in range(3):
+            off = OFFSET + 100 * kind + rep
+            t, d, x = chain_batch(2, V, SEED, off, rng, kind_of=lambda b: kind)
+            o_acc, o_out, _ = oracle_sample(t[:1], d[:1], x[:1], 1.0, SEED, off)
+            ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_SAMPLE, 1, 2, V, binding.FP32),
+                             dtype=torch.uint8, device=DEV)
+            acc, out = sv.spec_verify_sample(cuda(t[:1]), cuda(d[:1]), cuda(x[:1]), 1.0, SEED, off, workspace=ws)
+            assert (acc.cpu().numpy() == o_acc).all() and (out.cpu().numpy() == o_out).all(), (kind, rep)
+            marked, redone, status, marks = binding.call_status(ws, binding.MODE_SAMPLE, 1, 2, V, binding.FP32)
+            assert status == 0 and marked == redone == 1 and marks[0] != 0, (kind, rep, marked, redone)
+            acc2, out2 = sv.spec_verify_sample(cuda(t), cuda(d), cuda(x), 1.0, SEED, off)
+            assert torch.equal(acc2[:1], acc) and torch.equal(out2[:1], out)

@@ -87,6 +87,23 @@ def test_small_cases(B, gamma, V, dtype, recipe, T):
     _run(s, f"small B={B} g={gamma} V={V} {dtype} {recipe} T={T}")
 
 
+@pytest.mark.parametrize("gamma,V,dtype,recipe,T", [(g, v, dt, r, t) for (_, g, v, dt, r, t) in SMALL]
+                         + [(4, 128256, "bf16", "peaked", 0.7), (7, 65536, "fp32", "normal", 1.0)])
+def test_single_sequence_matches_the_batch_path(gamma, V, dtype, recipe, T):
+    """A batch of one (run as a single kernel when its rows have few tiles) gives sequence 0
+    of a larger batch exactly: the uniforms are keyed by the sequence index, which is 0 in both."""
+    s = W.make_sample(6, gamma, V, dtype=dtype, recipe=recipe, temperature=T, seed=gamma * 13 + V,
+                      verify_seed=V + 3, device=DEV, target_std=3.0, noise_std=1.0,
+                      draft_scale=0.8 if recipe == "peaked" else 1.0)
+    for off in (0, 1, 2, 99991):
+        acc, out = sv.spec_verify_sample(s.target, s.draft, s.draft_tokens, T, s.seed, off)
+        t1, d1, x1 = s.target[:1], s.draft[:1], s.draft_tokens[:1]
+        acc1, out1 = sv.spec_verify_sample(t1, d1, x1, T, s.seed, off)
+        assert torch.equal(acc1, acc[:1]) and torch.equal(out1, out[:1]), off
+        o = oracle_sample(t1, d1, x1, T, s.seed, off, diagnostics=True)
+        compare_sample(acc1, out1, *o, label=f"single g={gamma} V={V} {dtype} off={off}", record=True)
+
+
 def test_offsets_change_the_draw():
     s = W.make_sample(64, 4, 3000, dtype="bf16", seed=5, verify_seed=9, device=DEV)
     _run(s, "offset 0", 0)
