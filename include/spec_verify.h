@@ -184,10 +184,12 @@ sv_status spec_verify_tree_greedy(const void *target_logits, int64_t t_batch_str
  * walk every marked one again in double-float arithmetic and rewrite its outputs, so the
  * result is the exact rule's except where a decision is closer than ~1e-12 to its boundary
  * (spec_verify_status_offset).  Workspace: spec_verify_workspace_size(SV_MODE_TREE_SAMPLE,
- * B, N, V, dtype) bytes, about 128 V min(N, 8) bytes: eight clusters re-walk the marked
- * sequences, the first eight with the double-float exponentials of up to 8 reached nodes
- * precomputed by the whole grid (115 MB at N = 64, V = 128256 with max_depth = 6 needing 7
- * of the 8 positions; the size assumes 8), later ones computing them in the cluster.
+ * B, N, V, dtype) bytes, about 128 V min(N, 8) bytes: the first eight marked sequences get
+ * the double-float exponentials of up to 8 reached nodes from the whole grid (115 MB at
+ * N = 64, V = 128256 with max_depth = 6 needing 7 of the 8 positions; the size assumes 8);
+ * those of them marked only at the final draw (the path certain) have the rejections at
+ * the reached node and the draw redone by the same grid, one grid-wide pass per rejection;
+ * eight clusters re-walk the others, later ones computing the exponentials in the cluster.
  */
 sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_stride,
                                   int64_t t_row_stride, const void *draft_logits,

@@ -90,7 +90,7 @@ Layout layout(sv_mode mode, int B, int rows, int V, sv_dtype dtype) {
         L.npos = off;
         off += up256(S * K * 4);
         L.um = off;
-        off += up256(S * nu * 8);
+        off += up256(2 * S * nu * 8);
         L.rsum = off;
         off += up256(S * 2 * C * 2 * 8);
         L.pmax = off;
@@ -509,7 +509,9 @@ sv_status spec_verify_tree_sample(const void *target_logits, int64_t t_batch_str
                                    reinterpret_cast<float2 *>(at(workspace, L.rowstat)), rw, K, accepted_len,
                                    out_tokens, out_path, s);
     if (e == cudaSuccess) e = mark(1, s);
-    if (e == cudaSuccess) e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, V, temperature, K, rw, accepted_len, s);
+    if (e == cudaSuccess)
+        e = sv::launch_tree_exp(dtype == SV_BF16, t, d, B, N, V, parent, node_tokens, max_depth, temperature, seed,
+                                offset, without_replacement, K, rw, accepted_len, out_tokens, out_path, s);
     if (e == cudaSuccess) e = mark(2, s);
     if (e == cudaSuccess)
         e = sv::launch_tree_rewalk(dtype == SV_BF16, t, d, B, N, V, parent, node_tokens, max_depth, temperature,

@@ -81,4 +81,19 @@ __device__ inline bool grid_barrier(int *ctl, int expected = -1, uint64_t limit_
     return ok_s != 0;
 }
 
+// Arrival at a grid_barrier without the wait, for a CTA that leaves the kernel after it:
+// the barrier's other CTAs still count it among the `expected` (the grid by default).
+__device__ inline void grid_arrive(int *ctl, int expected = -1) {
+    if (expected < 0) expected = int(gridDim.x);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(ctl + kBarCount, 1) == expected - 1) {
+            atomicExch(ctl + kBarCount, 0);
+            __threadfence();
+            atomicAdd(ctl + kBarGen, 1);
+        }
+    }
+}
+
 }  // namespace sv

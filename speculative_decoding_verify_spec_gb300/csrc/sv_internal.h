@@ -124,7 +124,8 @@ cudaError_t launch_draw_refine(int dtype, bool vec, Logits t, Logits d, int B, i
 constexpr int kTrMarkPath = 1, kTrMarkFinal = 2;
 constexpr int kTrMarked = 0;  // sequences the last call marked
 constexpr int kTrRedone = 4;  // sequences redone (every marked one)
-constexpr int kTrCtlWords = 8;
+constexpr int kTrFinalDone = 5;  // slots (bit j) whose final draw the exponentials kernel redid
+constexpr int kTrCtlWords = 8;  // (words 1, 2 and 3: that kernel's grid barrier; 3 is the status)
 constexpr int kMaxTreeRefine = 8;
 constexpr int kTreeRecNodes = 8;
 constexpr float kTreeAcceptWindow = 1e-6f;
@@ -137,7 +138,7 @@ struct df;
 // tree_refine_units(V):  ctl [kTrCtlWords]; mark, rlen [B]; rec [B][K] float4;
 // et [kMaxTreeRefine][K][2][V] and us [kMaxTreeRefine][K][2][nunit] double-float (the
 // exponentials of the recorded rows and their unit sums); npos [kMaxTreeRefine][K] int;
-// um [kMaxTreeRefine][nunit], part [kMaxTreeRefine][2][cluster][2] double-float; pmax
+// um [2][kMaxTreeRefine][nunit] (two buffers: passes in turn), part [kMaxTreeRefine][2][cluster][2] double-float; pmax
 // [kMaxTreeRefine][cluster][2] float; pcnt [kMaxTreeRefine][cluster] int.
 struct TreeRefineWs {
     int *ctl, *mark, *rlen;
@@ -155,11 +156,14 @@ __host__ __device__ inline int tree_refine_units(int V) {
 inline int tree_rec_nodes(int max_depth) { return max_depth + 1 < kTreeRecNodes ? max_depth + 1 : kTreeRecNodes; }
 inline size_t tree_refine_smem(int N, int max_depth) { return size_t(13 * N + max_depth + 1) * 4; }
 // The exponentials of the listed sequences' recorded rows (every resident CTA; for a
-// sequence marked only at its final draw, the reached node's rows alone), then the re-walk
-// (one cluster of 16 CTAs per listed sequence where the device holds one, else 8).
+// sequence marked only at its final draw, the reached node's rows alone) and the final
+// re-draw of those marked only there (the same grid), then the re-walk of the rest (one
+// cluster of 16 CTAs per listed sequence where the device holds one, else 8).
 // accepted_len: the walk's outputs (the depth it reached).
-cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws,
-                            const int32_t *accepted_len, cudaStream_t s);
+cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int N, int V, const int32_t *parent,
+                            const int32_t *node_tokens, int max_depth, float T, uint64_t seed, uint64_t offset,
+                            int without_replacement, int K, TreeRefineWs ws, int32_t *accepted_len,
+                            int32_t *out_tokens, int32_t *out_path, cudaStream_t s);
 cudaError_t launch_tree_rewalk(int dtype, Logits t, Logits d, int B, int N, int V, const int32_t *parent,
                                const int32_t *node_tokens, int max_depth, float T, uint64_t seed, uint64_t offset,
                                int without_replacement, int K, TreeRefineWs ws, int32_t *accepted_len,

@@ -10,10 +10,13 @@
 // (sv_df.cuh, ~48 bits; the arithmetic of the chain's re-draw), which settles every
 // comparison whose exact margin is above ~1e-12.
 //
-//   tree_exp_kernel     the whole grid: for every recorded node of the first eight marked
-//                       sequences, e_t(j) = exp((t_j - M_t) / T) and e_d(j) of its target
-//                       and draft rows, stored with their 256-logit unit sums and q's
-//                       support size;
+//   tree_exp_kernel     the whole grid (one cooperative launch): for every recorded node of
+//                       the first eight marked sequences, e_t(j) = exp((t_j - M_t) / T) and
+//                       e_d(j) of its target and draft rows, stored with their 256-logit unit
+//                       sums and q's support size; then, for those of them marked only at
+//                       their final draw (their path certain), the rejections at the reached
+//                       node and the final draw again, every residual pass spread over the
+//                       whole grid (slots in lock step, one grid barrier per pass);
 //   tree_rewalk_kernel  eight thread-block clusters, each taking every eighth marked
 //                       sequence in turn (the first one with those stored values, later ones
 //                       computing them in the cluster), its CTAs owning
@@ -26,6 +29,7 @@
 //                       CTA run, then the unit, then the logit holding u' x total, each by a
 //                       prefix in index order.  A node the walk did not record (the re-walk
 //                       took another child) gets its maxima and exponentials in the cluster.
+//                       A slot the exponentials kernel redid is skipped.
 // A token's q-mass is exactly zero when its exponential is (a -inf draft logit, or one more
 // than 87 T below the row maximum); q is out of mass once every token with mass has left.
 #include "spec_verify.h"
@@ -33,6 +37,7 @@
 #include "sv_device.cuh"
 #include "sv_df.cuh"
 #include "sv_dfwalk.cuh"
+#include "sv_grid.cuh"
 #include "sv_internal.h"
 
 namespace sv {
@@ -42,6 +47,18 @@ constexpr int kTrUnit = kTreeRefineUnit;  // logits per unit (one warp)
 constexpr int kTrLane = kTrUnit / 32;     // logits per lane in a unit (contiguous)
 constexpr int kRwThreads = 512;
 constexpr int kRwWarps = kRwThreads / 32;
+constexpr int kFinalChildren = 16;  // children of a reached node the grid-wide final re-draw replays
+static_assert(kWarps >= kMaxTreeRefine, "one warp of the exponentials kernel per slot");
+
+// The state of one slot's final re-draw at its reached node v, kept alike in every CTA:
+// the implicit (p, q) of the re-walk (A, Dt, s in S_t units) and the pass in flight.
+enum FinalState { kFinalNone = 0, kFinalAdvance = 1, kFinalPass = 2, kFinalDraw = 3 };
+struct FinalSlot {
+    df St, Sd, rho, A, Dt, s, erem;
+    df Anext, s_new, total;  // the pending pass's coefficient and q scale; the draw's mass
+    int seq, v, acc, nch, next, nrem, npos, npos_rem, state, ubuf;
+    bool has_q, rejected, ready, add, lastpass;
+};
 
 // The listed sequences: the first kMaxTreeRefine with mark[b] != 0, in index order, into
 // s_seq; returns how many are listed, *total = how many are marked.  Every CTA builds the
@@ -135,40 +152,105 @@ __device__ __forceinline__ bool final_only(int mark, int rlen, int acc, int K) {
     return mark == kTrMarkFinal && acc >= 0 && acc < K && rlen == acc + 1;
 }
 
+// The sums of the n stored values of a and of b (b may be null: 0) in warp_search's order --
+// lane l adds its run [l per, (l + 1) per) in index order, then an inclusive scan over the
+// lanes -- with each lane's loads of both lists in flight together.  Every lane returns
+// both sums.
+__device__ __forceinline__ void warp_totals2(const df *a, const df *b, int n, int lane, df *ta, df *tb) {
+    constexpr int kB = 16;
+    const int per = (n + 31) / 32;
+    df sa = df_zero(), sb = df_zero();
+    for (int q0 = 0; q0 < per; q0 += kB) {
+        df va[kB], vb[kB];
+#pragma unroll
+        for (int q = 0; q < kB; ++q) {
+            const int i = lane * per + q0 + q;
+            const bool in = q0 + q < per && i < n;
+            va[q] = in ? ldcg_df(a + i) : df_zero();
+            vb[q] = (in && b) ? ldcg_df(b + i) : df_zero();
+        }
+#pragma unroll
+        for (int q = 0; q < kB; ++q)
+            if (q0 + q < per && lane * per + q0 + q < n) {
+                sa = df_add(sa, va[q]);
+                sb = df_add(sb, vb[q]);
+            }
+    }
+    *ta = df_shfl(df_warp_scan(sa, lane), 31);
+    *tb = df_shfl(df_warp_scan(sb, lane), 31);
+}
+
 }  // namespace
 
 // The exponentials of the recorded nodes of the first kMaxTreeRefine marked sequences
-// (grid-stride over (slot, position, row, unit), one warp per unit).
+// (grid-stride over the (slot, position, row, unit) items that exist, one warp per unit,
+// from the grid's last warp down), then the final re-draw of those marked only at their
+// final draw by the first CTAs of the grid.
 template <class D>
 __global__ void __launch_bounds__(kThreads)
-    tree_exp_kernel(Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws,
-                    const int32_t *__restrict__ accepted_len) {
+    tree_exp_kernel(Logits t, Logits d, int B, int N, int V, const int32_t *__restrict__ parent,
+                    const int32_t *__restrict__ node_tokens, int max_depth, float T, uint64_t seed, uint64_t offset,
+                    int without_replacement, int K, TreeRefineWs ws, int32_t *__restrict__ accepted_len,
+                    int32_t *__restrict__ out_tokens, int32_t *__restrict__ out_path) {
     __shared__ int s_seq[kMaxTreeRefine];
     __shared__ unsigned s_bal[kWarps];
     __shared__ int s_cnt[2];
+    __shared__ FinalSlot s_fs[kMaxTreeRefine];
+    __shared__ int s_fcn[kMaxTreeRefine][kFinalChildren], s_fcx[kMaxTreeRefine][kFinalChildren];
+    __shared__ df s_fct[kMaxTreeRefine][kFinalChildren], s_fcd[kMaxTreeRefine][kFinalChildren];
+    __shared__ int s_frt[kMaxTreeRefine][kFinalChildren];  // removed tokens and their coefficients
+    __shared__ df s_frc[kMaxTreeRefine][kFinalChildren];
+    __shared__ int s_any;
     griddep_launch_next();
     griddep_wait();  // the walk's marks and records
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nunit = tree_refine_units(V);
     const df inv_t = df_div(df_from(1.f), df_from(T));
     const int64_t nw = int64_t(gridDim.x) * kWarps;
+    const int64_t gw = int64_t(blockIdx.x) * kWarps + warp;
     int total = 0;
     const int n = list_marked(ws.mark, B, s_seq, s_bal, s_cnt, &total);
     if (n == 0) return;
-    const int64_t items = int64_t(n) * K * 2 * nunit;
-    for (int64_t it = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); it < items; it += nw) {
-        const int u = int(it % nunit);
-        const int64_t rest = it / nunit;
-        const int r = int(rest % 2);
-        const int k = int((rest / 2) % K);
-        const int j = int(rest / (2 * int64_t(K)));
+    // the slots' records in shared memory (warp j, lane k): positions k0 .. k0 + nk - 1 have
+    // exponentials to compute (a slot marked only at its final draw: the reached node alone)
+    __shared__ float4 s_rec[kMaxTreeRefine][kTreeRecNodes];
+    __shared__ int s_k0[kMaxTreeRefine], s_nk[kMaxTreeRefine], s_fo[kMaxTreeRefine];
+    __shared__ int64_t s_ibase[kMaxTreeRefine + 1];
+    if (warp < n) {
+        const int64_t seq = s_seq[warp];
+        const bool ok = SV_IN(seq, B);
+        const int rlen = ok ? __ldcg(ws.rlen + seq) : 0;
+        const int acc = ok ? __ldcg(accepted_len + seq) : -1;
+        const bool fo = ok && final_only(__ldcg(ws.mark + seq), rlen, acc, K);
+        const int rl = min(max(rlen, 0), min(K, kTreeRecNodes));
+        if (lane < rl) s_rec[warp][lane] = __ldcg(ws.rec + seq * K + lane);
+        if (lane == 0) {
+            s_k0[warp] = fo ? acc : 0;
+            s_nk[warp] = fo ? 1 : rl;
+            s_fo[warp] = fo;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int64_t b = 0;
+        for (int jj = 0; jj < n; ++jj) {
+            s_ibase[jj] = b;
+            b += int64_t(s_nk[jj]) * 2 * nunit;
+        }
+        s_ibase[n] = b;
+    }
+    __syncthreads();
+    const int64_t items = s_ibase[n];
+    for (int64_t it = nw - 1 - gw; it < items; it += nw) {
+        int j = 0;
+        while (j + 1 < n && it >= s_ibase[j + 1]) ++j;
         const int64_t seq = s_seq[j];
-        if (!SV_IN(seq, B) || !SV_IN(j, kMaxTreeRefine)) continue;
-        const int rlen = __ldcg(ws.rlen + seq);
-        if (k >= rlen) continue;  // (uniform over the warp)
-        // marked only at the final draw: the reached node's rows alone
-        if (k != rlen - 1 && final_only(__ldcg(ws.mark + seq), rlen, __ldcg(accepted_len + seq), K)) continue;
-        const float4 rec = __ldcg(ws.rec + seq * K + k);
+        const int64_t loc = it - s_ibase[j];
+        const int u = int(loc % nunit);
+        const int r = int((loc / nunit) % 2);
+        const int k = s_k0[j] + int(loc / (2 * int64_t(nunit)));
+        if (!SV_IN(seq, B) || !SV_IN(k, kTreeRecNodes)) continue;
+        const float4 rec = s_rec[j][k];
         const int node = __float_as_int(rec.x);
         if (r == 1 && rec.w == 0.f) continue;  // a leaf: no draft row
         const char *row = row_ptr(r == 0 ? t : d, D::kBytes, seq, node);
@@ -179,6 +261,267 @@ __global__ void __launch_bounds__(kThreads)
             st_df(ws.us + ek * nunit + u, us);
             if (r == 1 && cnt) atomicAdd(ws.npos + int64_t(j) * K + k, cnt);
         }
+    }
+
+    // ---- The final re-draw of the slots marked only at their final draw.  Every decision
+    // on such a path was taken outside the fp32 error, so at the reached node v every child
+    // was rejected (or v is a leaf): the rejections are replayed in double-float (each
+    // child's test is taken again; one that now accepts leaves the slot to the re-walk),
+    // each residual pass spread over the warps of the first P CTAs (one unit each), and the
+    // final token drawn.  Those CTAs keep the same slot states: they change only through
+    // sums of the same stored values in the same order.  Warp j owns slot j.  The other
+    // CTAs only report their exponentials done at the first barrier.
+    const int64_t pw = (int64_t(n) * nunit + kWarps - 1) / kWarps;
+    const int P = pw < int64_t(gridDim.x) ? int(pw) : int(gridDim.x);
+    if (int(blockIdx.x) >= P) {
+        grid_arrive(ws.ctl);
+        return;
+    }
+    if (warp < n) {
+        FinalSlot &f = s_fs[warp];
+        const int64_t seq = s_seq[warp];
+        const bool fo = s_fo[warp];
+        const int acc = fo ? s_k0[warp] : -1;
+        const float4 rec = fo ? s_rec[warp][acc] : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int v = fo ? __float_as_int(rec.x) : -1;
+        int nch = 0;  // v's children in index order (the walk tested them in this order)
+        if (fo && v >= 0 && v < N)
+            for (int base = v + 1; base < N; base += 32) {
+                const int cn = base + lane;
+                const bool ch = cn < N && __ldg(parent + cn) == v;
+                const unsigned bal = __ballot_sync(0xFFFFFFFFu, ch);
+                const int idx = nch + __popc(bal & ((1u << lane) - 1u));
+                if (ch && idx < kFinalChildren) s_fcn[warp][idx] = cn;
+                nch += __popc(bal);
+            }
+        __syncwarp();
+        const bool take = fo && v >= 0 && v < N && nch <= kFinalChildren;
+        // the children's tokens and exponentials, as the exponentials above compute them
+        if (take && lane < nch) {
+            const int cn = s_fcn[warp][lane];
+            int x = __ldg(node_tokens + seq * N + cn);
+            if (!SV_IN(x, V)) x = 0;  // (the walk checked the tokens before marking)
+            s_fcx[warp][lane] = x;
+            s_fct[warp][lane] = weight1_df(load_elem<D>(row_ptr(t, D::kBytes, seq, v), x), rec.y, inv_t);
+            s_fcd[warp][lane] = weight1_df(load_elem<D>(row_ptr(d, D::kBytes, seq, v), x), rec.z, inv_t);
+        }
+        if (lane == 0) {
+            f.seq = int(seq);
+            f.v = v;
+            f.acc = acc;
+            f.nch = nch;
+            f.state = take ? kFinalAdvance : kFinalNone;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int a = 0;
+        for (int jj = 0; jj < n; ++jj) a |= s_fs[jj].state != kFinalNone;
+        s_any = a;
+    }
+    __syncthreads();
+    if (!s_any) return;  // (the same in every CTA of the P)
+    if (!grid_barrier(ws.ctl)) return;  // every slot's exponentials, unit sums and support counts
+
+    // The slot's stored rows at its reached node (position acc of the slot's records).
+    auto rows_of = [&](int jj, const df **Et, const df **Ed, const df **Ut, const df **Ud) {
+        const int64_t ek = (int64_t(jj) * K + s_fs[jj].acc) * 2;
+        *Et = ws.et + ek * V;
+        *Ed = *Et + V;
+        *Ut = ws.us + ek * nunit;
+        *Ud = *Ut + nunit;
+    };
+    if (warp < n && s_fs[warp].state == kFinalAdvance) {
+        FinalSlot &f = s_fs[warp];
+        const df *Et, *Ed, *Ut, *Ud;
+        rows_of(warp, &Et, &Ed, &Ut, &Ud);
+        const bool has_q = f.nch > 0;
+        const int np = lane == 0 ? __ldcg(ws.npos + int64_t(warp) * K + f.acc) : 0;  // (in flight with the sums)
+        df St, Sd;
+        warp_totals2(Ut, has_q ? Ud : nullptr, nunit, lane, &St, &Sd);
+        if (!has_q) Sd = df_from(1.f);
+        if (lane == 0) {
+            f.has_q = has_q;
+            f.St = St;
+            f.Sd = Sd;
+            f.rho = has_q ? df_div(St, Sd) : df_zero();
+            f.A = df_zero();
+            f.Dt = St;
+            f.s = df_from(1.f);
+            f.erem = df_zero();
+            f.npos = np;
+            f.npos_rem = 0;
+            f.nrem = 0;
+            f.next = 0;
+            f.rejected = false;
+            f.ready = false;
+        }
+    }
+    __syncthreads();
+
+    // Slot j's next step (one thread): the next child's test; a rejection sets up the pass
+    // under the new coefficient; after the last child the draw (a pass under the current
+    // coefficients first when the last residual had no mass).
+    auto advance = [&](int jj) {
+        FinalSlot &f = s_fs[jj];
+        if (f.next >= f.nch) {
+            if (f.rejected && !f.ready) {
+                f.Anext = f.A;
+                f.add = false;
+                f.lastpass = true;
+                f.state = kFinalPass;
+            } else {
+                f.total = f.rejected ? f.Dt : f.St;
+                f.state = kFinalDraw;
+            }
+            return;
+        }
+        const int c = f.next++;
+        const int x = s_fcx[jj][c];
+        const df ex_t = s_fct[jj][c], ex_d = s_fcd[jj][c];
+        df ax = f.A;
+        bool removed = false;
+        for (int r = 0; r < f.nrem; ++r)
+            if (s_frt[jj][r] == x) {
+                ax = s_frc[jj][r];
+                removed = true;
+            }
+        const df Wx = resid_w(ex_t, ex_d, df_mul(ax, f.rho));
+        const float uu = uniform01(seed, offset, uint32_t(f.seq), uint32_t(s_fcn[jj][c] - 1), 0u);
+        const df lhs = removed ? df_zero() : df_mul_f(df_mul(df_mul(f.s, ex_d), f.Dt), uu);
+        if (df_lt(lhs, df_mul(Wx, f.Sd))) {  // accepted after all: the re-walk takes the slot
+            f.state = kFinalNone;
+            return;
+        }
+        f.rejected = true;
+        const df Anew = df_add(f.A, df_mul(df_div(f.Dt, f.St), f.s));
+        df s_new = f.s;
+        const bool add = without_replacement && !removed;
+        if (add) {
+            if (SV_IN(f.nrem, kFinalChildren)) {
+                s_frt[jj][f.nrem] = x;
+                s_frc[jj][f.nrem] = Anew;
+            }
+            ++f.nrem;
+            f.erem = df_add(f.erem, ex_d);
+            if (df_pos(ex_d)) ++f.npos_rem;
+            const df rest = df_sub(f.Sd, f.erem);
+            s_new = (f.npos_rem >= f.npos || !df_pos(rest)) ? df_zero() : df_div(f.Sd, rest);
+        }
+        f.Anext = Anew;
+        f.s_new = s_new;
+        f.add = add;
+        f.lastpass = false;
+        f.state = kFinalPass;
+    };
+    // This lane's weights of unit u of slot jj under the coefficient a (removed tokens keep
+    // theirs); e_t alone at a leaf.  0 past the row's end.
+    auto unit_weights = [&](int jj, df a, const df *Et, const df *Ed, int u, df(&w)[kDfLane]) {
+        const FinalSlot &f = s_fs[jj];
+        const int64_t j0 = int64_t(u) * kTrUnit + lane * kTrLane;
+        df xt[kTrLane], xd[kTrLane];  // the loads first, all in flight together
+#pragma unroll
+        for (int e = 0; e < kTrLane; ++e) {
+            xt[e] = j0 + e < V ? ldcg_df(Et + j0 + e) : df_zero();
+            xd[e] = (f.rejected && j0 + e < V) ? ldcg_df(Ed + j0 + e) : df_zero();
+        }
+        const df ar = df_mul(a, f.rho);
+#pragma unroll
+        for (int e = 0; e < kTrLane; ++e) {
+            if (!f.rejected) {
+                w[e] = xt[e];
+                continue;
+            }
+            df arj = ar;
+            for (int r = 0; r < f.nrem && r < kFinalChildren; ++r)
+                if (s_frt[jj][r] == j0 + e) arj = df_mul(s_frc[jj][r], f.rho);
+            w[e] = j0 + e < V ? resid_w(xt[e], xd[e], arj) : df_zero();
+        }
+    };
+
+    for (int round = 0;; ++round) {
+        if (lane == 0 && warp < n && s_fs[warp].state == kFinalAdvance) advance(warp);
+        __syncthreads();
+        bool any = false;
+        for (int jj = 0; jj < n; ++jj) any |= s_fs[jj].state == kFinalPass;
+        if (!any) break;  // (the same in every CTA)
+        // the pass: (slot, unit) items over every warp of the grid, into buffer round & 1
+        // (its readers of two rounds ago are past the barrier of the last round)
+        df *umb = ws.um + int64_t(round & 1) * kMaxTreeRefine * nunit;
+        for (int64_t it = gw; it < int64_t(n) * nunit; it += int64_t(P) * kWarps) {
+            const int jj = int(it / nunit), u = int(it % nunit);
+            if (s_fs[jj].state != kFinalPass) continue;  // (uniform over the warp)
+            const df *Et, *Ed, *Ut, *Ud;
+            rows_of(jj, &Et, &Ed, &Ut, &Ud);
+            df w[kDfLane];
+            unit_weights(jj, s_fs[jj].Anext, Et, Ed, u, w);
+            const df us = unit_sum(w, lane);
+            if (lane == 0) st_df(umb + int64_t(jj) * nunit + u, us);
+        }
+        if (!grid_barrier(ws.ctl, P)) return;
+        if (warp < n && s_fs[warp].state == kFinalPass) {
+            FinalSlot &f = s_fs[warp];
+            df F, unused;
+            warp_totals2(umb + int64_t(warp) * nunit, nullptr, nunit, lane, &F, &unused);
+            if (lane == 0) {
+                if (f.lastpass) {
+                    f.total = F;
+                    f.ubuf = round & 1;
+                    f.state = kFinalDraw;
+                } else {
+                    if (df_pos(F)) {
+                        f.A = f.Anext;
+                        f.Dt = F;
+                        f.ready = true;
+                        f.ubuf = round & 1;
+                    } else {  // no residual mass: p stays (the removal from q still happens)
+                        f.ready = false;
+                        if (f.add && SV_IN(f.nrem - 1, kFinalChildren)) s_frc[warp][f.nrem - 1] = f.A;
+                    }
+                    f.s = f.s_new;
+                    f.state = kFinalAdvance;
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // The draws (CTA 0, warp j for slot j): the unit holding u' x total by a prefix over the
+    // unit masses in index order, then the logit inside it; the outputs rewritten.
+    if (blockIdx.x != 0 || warp >= n || s_fs[warp].state != kFinalDraw) return;
+    const FinalSlot &f = s_fs[warp];
+    const df *Et, *Ed, *Ut, *Ud;
+    rows_of(warp, &Et, &Ed, &Ut, &Ud);
+    const df *umv = f.rejected ? ws.um + int64_t(f.ubuf) * kMaxTreeRefine * nunit + int64_t(warp) * nunit : Ut;
+    const float u2 = uniform01(seed, offset, uint32_t(f.seq), uint32_t(f.v), 1u);
+    const df thr = df_mul_f(f.total, u2);
+    df run;
+    bool force;
+    int u = warp_search(umv, 1, nunit, df_zero(), thr, false, &run, &force, lane);
+    if (u < 0) u = 0;
+    if (u > nunit - 1) u = nunit - 1;
+    df w[kDfLane];
+    unit_weights(warp, f.A, Et, Ed, u, w);
+    const int tok = unit_pick(w, int64_t(u) * kTrUnit, int64_t(u) * kTrUnit + lane * kTrLane, V, run, thr, force, lane);
+    const int W = max_depth + 1;
+    const int64_t sq = f.seq;
+    int32_t *out = out_tokens + sq * W;
+    int32_t *opath = out_path ? out_path + sq * W : nullptr;
+    for (int i = lane; i < W; i += 32) {
+        int o = -1, pth = -1;
+        if (i <= f.acc && SV_IN(i, K)) pth = __float_as_int(__ldcg(ws.rec + sq * K + i).x);
+        if (i < f.acc && SV_IN(i + 1, K)) {
+            const int nx = __float_as_int(__ldcg(ws.rec + sq * K + i + 1).x);
+            o = SV_IN(nx, N) ? __ldg(node_tokens + sq * N + nx) : -1;
+        } else if (i == f.acc) {
+            o = tok;
+        }
+        out[i] = o;
+        if (opath) opath[i] = pth;
+    }
+    if (lane == 0) {
+        atomicOr(ws.ctl + kTrFinalDone, 1 << warp);
+        atomicAdd(ws.ctl + kTrRedone, 1);
     }
 }
 
@@ -616,18 +959,24 @@ __global__ void __launch_bounds__(kRwThreads, 1)
         const int64_t seq = nth_marked(ws.mark, B, j + iter * G, s_bal, s_cnt, &total_marked);
         if (iter == 0 && blockIdx.x == 0 && tid == 0) ws.ctl[kTrMarked] = total_marked;
         if (seq < 0 || !SV_IN(seq, B)) break;  // (the whole cluster)
+        // a slot the exponentials kernel re-drew (the same word in every CTA)
+        if (iter == 0 && ((__ldcg(ws.ctl + kTrFinalDone) >> j) & 1)) continue;
         walk_one(seq, iter == 0);
         csync<CS>();  // every CTA is done with the slot's scratch before the next sequence
         if (rank == 0 && tid == 0) atomicAdd(ws.ctl + kTrRedone, 1);
     }
 }
 
-cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int V, float T, int K, TreeRefineWs ws,
-                            const int32_t *accepted_len, cudaStream_t s) {
+cudaError_t launch_tree_exp(int dtype, Logits t, Logits d, int B, int N, int V, const int32_t *parent,
+                            const int32_t *node_tokens, int max_depth, float T, uint64_t seed, uint64_t offset,
+                            int without_replacement, int K, TreeRefineWs ws, int32_t *accepted_len,
+                            int32_t *out_tokens, int32_t *out_path, cudaStream_t s) {
     auto ke = dtype == 1 ? tree_exp_kernel<BF16> : tree_exp_kernel<F32>;
-    unsigned grid = 0;  // every resident CTA
+    unsigned grid = 0;  // every resident CTA (a cooperative launch: its passes meet at grid barriers)
     cudaError_t e = persistent_grid(ke, int64_t(1) << 40, &grid);
-    if (e == cudaSuccess) e = launch_after(ke, grid, kThreads, 0, s, t, d, B, V, T, K, ws, accepted_len);
+    if (e == cudaSuccess)
+        e = launch_after_ex(true, ke, grid, kThreads, 0, s, t, d, B, N, V, parent, node_tokens, max_depth, T, seed,
+                            offset, without_replacement, K, ws, accepted_len, out_tokens, out_path);
     return e;
 }
 
