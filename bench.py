@@ -44,10 +44,14 @@ DOMINANT_KERNEL = {"sample": "stats_tiles_kernel", "greedy": "max_tiles_kernel",
                    "sample_lazy": "level_kernel", "greedy_lazy": "greedy_walk_kernel",
                    "tree_lazy": "greedy_walk_kernel", "ngram": "ngram_draft_kernel",
                    "typical": "level_kernel", "onehot": "level_kernel"}
-# one sequence with few tiles runs as one kernel (single_sample_kernel): its stage events
-# 2..4 are recorded right after it
-DOMINANT_BY_WORKLOAD = {"sample_b1": "single_sample_kernel"}
-STAGES_BY_WORKLOAD = {"sample_b1": ["one_kernel", "none_1", "none_2", "none_3"]}
+# A sampling call with B = 1 whose 2 gamma + 1 rows have at most 256 tiles of 4 KB runs as
+# one kernel (single_sample_kernel); its stage events 2..4 are recorded right after it.
+SINGLE_STAGES = ["one_kernel", "none_1", "none_2", "none_3"]
+
+
+def single_kernel_call(mode: str, cfg: dict) -> bool:
+    tile = 1024 if cfg["dtype"] == "fp32" else 2048
+    return mode == "sample" and cfg["B"] == 1 and (2 * cfg["gamma"] + 1) * -(-cfg["V"] // tile) <= 256
 STAGE_STEPS = 200  # steps timed kernel by kernel (after the headline steps)
 ACCEPT_STEPS = 16  # untimed steps whose accepted lengths and re-draw counts are read back
 STAGES = {"sample": ["row_stats", "decide", "residual_mass", "draw_redraw"],
@@ -525,8 +529,9 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None, 
     kb = kernel_bytes(name, **ov)
     dom_ms = stage_ms[0]
     achieved = kb / (dom_ms / 1e3) / 1e9
-    kernel = DOMINANT_BY_WORKLOAD.get(name, DOMINANT_KERNEL[mode])
-    stage_names = STAGES_BY_WORKLOAD.get(name, STAGES[mode])
+    single = single_kernel_call(mode, cfg)
+    kernel = "single_sample_kernel" if single else DOMINANT_KERNEL[mode]
+    stage_names = SINGLE_STAGES if single else STAGES[mode]
     acc = outs[0].float()
     res = {
         "workload": W.DESCRIPTIONS[name], "value": value, "unit": UNIT, "ms_per_step": ms_step,
@@ -540,7 +545,7 @@ def measure(name, steps, warmup, rank, world, dev, peak, peak_kind, batch=None, 
                      "frac": achieved / peak,
                      "bytes_per_launch": kb,
                      "traffic": committed_traffic(kernel, name)},
-        "gpu_launches": steps * (nst if mode != "sample" or cfg["gamma"] > 0 else 4),
+        "gpu_launches": steps * (1 if single else nst if mode != "sample" or cfg["gamma"] > 0 else 4),
         **extra,
     }
     if mode == "tree_sample":

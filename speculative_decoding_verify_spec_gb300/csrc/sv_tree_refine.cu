@@ -180,6 +180,59 @@ __device__ __forceinline__ void warp_totals2(const df *a, const df *b, int n, in
     *tb = df_shfl(df_warp_scan(sb, lane), 31);
 }
 
+// warp_search(vals, 1, n, 0, thr, false, ...) for n <= 32 kSearchRegs values, each lane's
+// run loaded once (one round of loads; the crossing lane re-scans it from registers).
+constexpr int kSearchRegs = 16;
+__device__ __forceinline__ int search_regs(const df *vals, int n, df thr, df *run_out, bool *force_out, int lane) {
+    const int per = (n + 31) / 32;
+    df v[kSearchRegs];
+#pragma unroll
+    for (int q = 0; q < kSearchRegs; ++q) {
+        const int i = lane * per + q;
+        v[q] = (q < per && i < n) ? ldcg_df(vals + i) : df_zero();
+    }
+    df ls = df_zero();
+    int lastpos = -1;
+#pragma unroll
+    for (int q = 0; q < kSearchRegs; ++q) {
+        const int i = lane * per + q;
+        if (q < per && i < n) {
+            ls = df_add(ls, v[q]);
+            if (df_pos(v[q])) lastpos = i;
+        }
+    }
+    const df incl = df_warp_scan(ls, lane);
+    df excl = df_shfl_up(incl, 1);
+    if (lane == 0) excl = df_zero();
+    const unsigned bal = __ballot_sync(0xFFFFFFFFu, df_gt(df_add(df_zero(), incl), thr));
+    if (bal) {
+        const int l = __ffs(bal) - 1;
+        int found = -1;
+        df run = df_add(df_zero(), excl);
+        if (lane == l) {
+#pragma unroll
+            for (int q = 0; q < kSearchRegs; ++q) {
+                const int i = lane * per + q;
+                if (found < 0 && q < per && i < n) {
+                    const df nx = df_add(run, v[q]);
+                    if (df_gt(nx, thr)) found = i;
+                    else run = nx;
+                }
+            }
+        }
+        found = __shfl_sync(0xFFFFFFFFu, found, l);
+        run = df_shfl(run, l);
+        if (found >= 0) {
+            *run_out = run;
+            *force_out = false;
+            return found;
+        }
+    }
+    *run_out = df_zero();
+    *force_out = true;
+    return warp_reduce(lastpos, [](int a, int b) { return max(a, b); });
+}
+
 }  // namespace
 
 // The exponentials of the recorded nodes of the first kMaxTreeRefine marked sequences
@@ -200,6 +253,7 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ df s_fct[kMaxTreeRefine][kFinalChildren], s_fcd[kMaxTreeRefine][kFinalChildren];
     __shared__ int s_frt[kMaxTreeRefine][kFinalChildren];  // removed tokens and their coefficients
     __shared__ df s_frc[kMaxTreeRefine][kFinalChildren];
+    __shared__ int s_fpt[kMaxTreeRefine][kTreeRecNodes];  // the path's tokens (the outputs before the final one)
     __shared__ int s_any;
     griddep_launch_next();
     griddep_wait();  // the walk's marks and records
@@ -297,6 +351,10 @@ __global__ void __launch_bounds__(kThreads)
         __syncwarp();
         const bool take = fo && v >= 0 && v < N && nch <= kFinalChildren;
         // the children's tokens and exponentials, as the exponentials above compute them
+        if (take && lane < acc && SV_IN(lane + 1, kTreeRecNodes)) {  // the path below the root
+            const int nx = __float_as_int(s_rec[warp][lane + 1].x);
+            s_fpt[warp][lane] = SV_IN(nx, N) ? __ldg(node_tokens + seq * N + nx) : -1;
+        }
         if (take && lane < nch) {
             const int cn = s_fcn[warp][lane];
             int x = __ldg(node_tokens + seq * N + cn);
@@ -497,7 +555,8 @@ __global__ void __launch_bounds__(kThreads)
     const df thr = df_mul_f(f.total, u2);
     df run;
     bool force;
-    int u = warp_search(umv, 1, nunit, df_zero(), thr, false, &run, &force, lane);
+    int u = (nunit + 31) / 32 <= kSearchRegs ? search_regs(umv, nunit, thr, &run, &force, lane)
+                                              : warp_search(umv, 1, nunit, df_zero(), thr, false, &run, &force, lane);
     if (u < 0) u = 0;
     if (u > nunit - 1) u = nunit - 1;
     df w[kDfLane];
@@ -509,13 +568,9 @@ __global__ void __launch_bounds__(kThreads)
     int32_t *opath = out_path ? out_path + sq * W : nullptr;
     for (int i = lane; i < W; i += 32) {
         int o = -1, pth = -1;
-        if (i <= f.acc && SV_IN(i, K)) pth = __float_as_int(__ldcg(ws.rec + sq * K + i).x);
-        if (i < f.acc && SV_IN(i + 1, K)) {
-            const int nx = __float_as_int(__ldcg(ws.rec + sq * K + i + 1).x);
-            o = SV_IN(nx, N) ? __ldg(node_tokens + sq * N + nx) : -1;
-        } else if (i == f.acc) {
-            o = tok;
-        }
+        if (i <= f.acc && SV_IN(i, kTreeRecNodes)) pth = __float_as_int(s_rec[warp][i].x);
+        if (i < f.acc && SV_IN(i, kTreeRecNodes)) o = s_fpt[warp][i];
+        else if (i == f.acc) o = tok;
         out[i] = o;
         if (opath) opath[i] = pth;
     }
