@@ -160,3 +160,37 @@ def test_disagreements_are_below_one_in_ten_thousand():
     assert marked > 0  # the re-walk is exercised
     assert mism < 1e-4 * total, (mism, total)
 
+
+
+def test_wide_nodes_and_leaves_redo_every_final_draw():
+    """A root with 12 children, one of them with 18 children, the others leaves; the draft far
+    from the target, so most walks reject all 12 at the root.  A sequence marked only at its
+    final draw is redone by the exponentials kernel's grid-wide passes at the root (up to 12
+    rounds, several sequences in lock step), by the re-walk at the 18-child node (more
+    children than that re-draw replays), and at a leaf the draw is from p alone.  Over 60
+    rounds of 64 sequences every marked sequence is redone and equals the oracle, and each
+    of the three kinds of final-only mark occurs."""
+    parent = [-1] + [0] * 12 + [1] * 18
+    s = W.make_tree_sample(64, 128256, "bf16", seed=4242, verify_seed=99, device=DEV, temperature=1.0,
+                           without_replacement=True, parent=parent, draft_scale=0.3, noise_std=3.0)
+    B, N, V = s.target.shape
+    ws = torch.empty(sv.spec_verify_workspace_size(binding.MODE_TREE_SAMPLE, B, N, V, binding.BF16),
+                     dtype=torch.uint8, device=DEV)
+    t, d, x = host(s.target), host(s.draft), s.node_tokens.cpu().numpy()
+    kinds = {"root": 0, "wide": 0, "leaf": 0}
+    for off in range(60):
+        acc, out, path = sv.spec_verify_tree_sample(s.target, s.draft, s.parent, s.node_tokens, s.max_depth,
+                                                    s.temperature, s.seed, off,
+                                                    without_replacement=s.without_replacement, workspace=ws)
+        m, r, status, marks = binding.call_status(ws, binding.MODE_TREE_SAMPLE, B, N, V, binding.BF16)
+        assert status == 0 and r == m == int((marks != 0).sum()), (off, m, r, status)
+        o = oracle_tree_sample(t, d, s.parent, x, s.max_depth, s.temperature, s.seed, off, s.without_replacement)
+        compare_tree_sample(acc, out, path, *o, label=f"wide tree offset {off}", record=False)
+        a, op, pp = acc.cpu().numpy(), out.cpu().numpy(), path.cpu().numpy()
+        for b in np.nonzero(marks)[0]:
+            assert a[b] == o[0][b] and (op[b] == o[1][b]).all() and (pp[b] == o[2][b]).all(), (off, b)
+            if marks[b] == 2:  # marked only at the final draw
+                node = pp[b][a[b]]
+                kinds["root" if node == 0 else "wide" if node == 1 else "leaf"] += 1
+    print("final-only marks by the node they were drawn at:", kinds)
+    assert min(kinds.values()) >= 1, kinds
