@@ -189,13 +189,41 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_digest() -> str:
+# the translation unit that defines each dominant kernel
+KERNEL_SOURCE = {"stats_tiles_kernel": "sv_sample.cu", "single_sample_kernel": "sv_sample.cu",
+                 "max_tiles_kernel": "sv_greedy.cu", "level_kernel": "sv_level.cu",
+                 "greedy_walk_kernel": "sv_lazy.cu"}
+
+
+def kernel_sources(kernel: str) -> list:
+    """The files a kernel's code and launch come from: its translation unit, every header it
+    includes (transitively, from csrc/ and include/), and the host dispatch sv_api.cu with its
+    includes.  Every source file for a kernel not in KERNEL_SOURCE."""
     csrc = os.path.join(ROOT, "speculative_decoding_verify_spec_gb300", "csrc")
+    inc = os.path.join(ROOT, "include")
+    if kernel not in KERNEL_SOURCE:
+        return sorted(os.path.join(csrc, n) for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")))
+    seen, todo = set(), [os.path.join(csrc, KERNEL_SOURCE[kernel]), os.path.join(csrc, "sv_api.cu")]
+    while todo:
+        path = todo.pop()
+        if path in seen or not os.path.exists(path):
+            continue
+        seen.add(path)
+        for line in open(path, encoding="utf-8"):
+            line = line.strip()
+            if line.startswith("#include \""):
+                name = line.split('"')[1]
+                todo += [os.path.join(csrc, name), os.path.join(inc, name)]
+    return sorted(seen)
+
+
+def source_digest(kernel: str = "") -> str:
+    """A 16-hex-digit SHA-256 prefix over the kernel's sources (kernel_sources): a traffic
+    capture stays valid while they are unchanged."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for path in kernel_sources(kernel):
+        with open(path, "rb") as f:
+            h.update(os.path.basename(path).encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -205,7 +233,7 @@ def committed_traffic(kernel: str, workload: str):
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    digest = source_digest()
+    digest = source_digest(kernel)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and \

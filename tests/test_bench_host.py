@@ -74,3 +74,23 @@ def test_oracle_legs_run_every_workload():
         out = bench.oracle_acceptance(acc, flags)
         assert sum(out["accepted_len_hist"]) + out["invalid"] == 3, name
         assert ("oracle_flags" in out) == (mode != "greedy"), name
+
+
+def test_traffic_lines_are_keyed_to_their_kernels_sources():
+    """A traffic capture is keyed to the files its kernel is built from: its translation unit,
+    the headers it includes (transitively) and the host dispatch -- not the other kernels'
+    sources; the single-sequence kernel shares the sampling unit's key."""
+    names = lambda k: {os.path.basename(p) for p in bench.kernel_sources(k)}
+    s = names("stats_tiles_kernel")
+    assert {"sv_sample.cu", "sv_api.cu", "sv_refine.cuh", "sv_df.cuh", "sv_device.cuh", "spec_verify.h"} <= s
+    assert not s & {"sv_tree_refine.cu", "sv_dfwalk.cuh", "sv_greedy.cu", "sv_level.cu"}
+    assert names("max_tiles_kernel") >= {"sv_greedy.cu", "sv_api.cu"} and "sv_sample.cu" not in names("max_tiles_kernel")
+    assert bench.source_digest("single_sample_kernel") == bench.source_digest("stats_tiles_kernel")
+    assert bench.source_digest("level_kernel") != bench.source_digest("greedy_walk_kernel")
+    # an unknown kernel is keyed to every source file
+    assert "sv_tree_refine.cu" in names("tree_exp_kernel")
+    # every committed line names a dominant kernel and parses
+    for line in open(os.path.join(bench.ROOT, "profiles", "traffic.txt")):
+        if line.strip() and not line.startswith("#"):
+            k, w, dg, b = line.split()
+            assert k in bench.KERNEL_SOURCE and len(dg) == 16 and int(b) > 0, line
