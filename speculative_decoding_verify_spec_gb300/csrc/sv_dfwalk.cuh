@@ -45,9 +45,10 @@ __device__ __forceinline__ df unit_sum(const df (&w)[kDfLane], int lane) {
 // exponential and one of the single one, shared by every caller -- instead of being
 // inlined and unrolled at each call site.
 //
-// w[e] = exp((x[e] - M) / T) for kDfLane logits (independent chains, interleaved).
+// w[e] = exp((x[e] - M) / T) for kDfLane logits, two independent chains interleaved at a
+// time (a quarter of the code of all eight, which a cold instruction cache fetches faster).
 static __device__ __noinline__ void weights_df(const float *x, float M, df inv_t, df *w) {
-#pragma unroll
+#pragma unroll 2
     for (int e = 0; e < kDfLane; ++e) w[e] = weight_df(x[e], M, inv_t);
 }
 // exp((x - M) / T) for one logit.

@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t gw = int64_t(blockIdx.x) * kWarps + warp;
     int total = 0;
     const int n = list_marked(ws.mark, B, s_seq, s_bal, s_cnt, &total);
+    if (blockIdx.x == 0 && threadIdx.x == 0) ws.ctl[kTrMarked] = total;
     if (n == 0) return;
     // the slots' records in shared memory (warp j, lane k): positions k0 .. k0 + nk - 1 have
     // exponentials to compute (a slot marked only at its final draw: the reached node alone)
@@ -1006,13 +1007,15 @@ __global__ void __launch_bounds__(kRwThreads, 1)
     }
   };
 
+    // nothing left: every marked sequence was a slot the exponentials kernel re-drew (the
+    // same words in every CTA)
+    if (__ldcg(ws.ctl + kTrMarked) == __popc(__ldcg(ws.ctl + kTrFinalDone))) return;
     // cluster j takes the marked sequences of rank j, j + G, j + 2 G, ... (index order; G
     // clusters), the first of them with slot j's stored exponentials
     const int G = int(gridDim.x) / CS;
     for (int iter = 0;; ++iter) {
         int total_marked = 0;
         const int64_t seq = nth_marked(ws.mark, B, j + iter * G, s_bal, s_cnt, &total_marked);
-        if (iter == 0 && blockIdx.x == 0 && tid == 0) ws.ctl[kTrMarked] = total_marked;
         if (seq < 0 || !SV_IN(seq, B)) break;  // (the whole cluster)
         // a slot the exponentials kernel re-drew (the same word in every CTA)
         if (iter == 0 && ((__ldcg(ws.ctl + kTrFinalDone) >> j) & 1)) continue;
