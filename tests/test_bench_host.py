@@ -94,3 +94,21 @@ def test_traffic_lines_are_keyed_to_their_kernels_sources():
         if line.strip() and not line.startswith("#"):
             k, w, dg, b = line.split()
             assert k in bench.KERNEL_SOURCE and len(dg) == 16 and int(b) > 0, line
+
+
+def test_single_kernel_rule_matches_the_library_constants():
+    """bench.py's copy of the dispatch rule for the one-kernel sampling call (its stage names
+    and launch count) uses the library's tile sizes and tile limit: tiles of 32 lanes x 8
+    vectors of 16 bytes, and kSingleTiles."""
+    import re
+    src = open(os.path.join(bench.ROOT, "speculative_decoding_verify_spec_gb300", "csrc", "sv_internal.h")).read()
+    limit = int(re.search(r"constexpr int kSingleTiles = (\d+);", src).group(1))
+    assert "inline int tile_elems_of(sv_dtype d) { return 32 * 8 * (16 / elem_bytes(d)); }" in src
+    for dtype, tile in (("fp32", 1024), ("bf16", 2048)):
+        for gamma in (0, 1, 4, 40):
+            for V in (1, 1000, tile * 7 + 1, 128256):
+                ntile = -(-V // tile)
+                cfg = {"B": 1, "gamma": gamma, "V": V, "dtype": dtype}
+                assert bench.single_kernel_call("sample", cfg) == ((2 * gamma + 1) * ntile <= limit)
+                assert not bench.single_kernel_call("sample", dict(cfg, B=2))
+                assert not bench.single_kernel_call("sample_lazy", cfg)
