@@ -217,13 +217,38 @@ def kernel_sources(kernel: str) -> list:
     return sorted(seen)
 
 
+def strip_comments(text: str) -> str:
+    """C/C++ source without its comments and blank lines, each line stripped (string and
+    character literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # a literal, to its closing quote
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.strip() for line in "".join(out).splitlines() if line.strip())
+
+
 def source_digest(kernel: str = "") -> str:
-    """A 16-hex-digit SHA-256 prefix over the kernel's sources (kernel_sources): a traffic
-    capture stays valid while they are unchanged."""
+    """A 16-hex-digit SHA-256 prefix over the code of the kernel's sources (kernel_sources,
+    comments left out): a traffic capture stays valid while that code is unchanged."""
     h = hashlib.sha256()
     for path in kernel_sources(kernel):
-        with open(path, "rb") as f:
-            h.update(os.path.basename(path).encode() + b"\0" + f.read())
+        with open(path, encoding="utf-8") as f:
+            h.update(os.path.basename(path).encode() + b"\0" + strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

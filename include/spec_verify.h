@@ -403,8 +403,8 @@ sv_status spec_verify_exp_df(const float *y_hi, const float *y_lo, int n, float 
  * sequences (one cooperative grid); a sampling call with B = 1 and (2 gamma + 1) row tiles
  * of at most 256 runs all four stages in one kernel of one thread block, and records
  * events[2..4] right after it; greedy and tree have 2: tile maxima, finalize; the lazy
- * greedy walks have 1; tree sampling has 3: the walk, the re-walk's exponentials, the
- * re-walk; lazy sampling has 3: the level walk, residual masses, the draw with its re-draw;
+ * greedy walks have 1; tree sampling has 3: the walk, the re-walk's exponentials with
+ * the final re-draw of the sequences marked only at their final draw, the re-walk; lazy sampling has 3: the level walk, residual masses, the draw with its re-draw;
  * typical acceptance and one-hot sampling have 2: the level walk, the draw with its
  * re-draw).  The events are cudaEvent_t handles created and owned by the caller; recording
  * them adds no synchronisation.  Pass NULL (or 0) to turn it off.

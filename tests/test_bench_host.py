@@ -112,3 +112,12 @@ def test_single_kernel_rule_matches_the_library_constants():
                 assert bench.single_kernel_call("sample", cfg) == ((2 * gamma + 1) * ntile <= limit)
                 assert not bench.single_kernel_call("sample", dict(cfg, B=2))
                 assert not bench.single_kernel_call("sample_lazy", cfg)
+
+
+def test_source_digest_ignores_comments_and_blank_lines():
+    """A comment or a blank line leaves a kernel's key unchanged; code does not."""
+    a = "int f(int x) {  // twice\n    return 2 * x; /* doubled */\n}\n"
+    b = "/* f */\nint f(int x) {\n\n    return 2 * x;\n}  // end\n"
+    c = "int f(int x) {\n    return 3 * x;\n}\n"
+    assert bench.strip_comments(a) == bench.strip_comments(b) != bench.strip_comments(c)
+    assert bench.strip_comments('char *s = "a // b /* c */";') == 'char *s = "a // b /* c */";'
